@@ -1,0 +1,237 @@
+"""Float64 CPU oracle for the POET-X layer: packed skew generators, the
+Cayley-Neumann block build, y = R_b (W0 (P_b x)) and its backward.
+
+TEST INFRASTRUCTURE ONLY.  This module exists to check the CUDA library.
+Only the tests, the smoke check and the benchmark's CPU-baseline leg may
+import it; the library itself never calls it and has no CPU fallback.  It
+shares no code with the CUDA sources.
+
+Everything is plain numpy in float64; ``@`` (a library matmul) and
+``numpy.linalg.solve`` are the only library steps.  Nothing is blocked,
+fused or reordered beyond the formulas below.
+
+Sources (one web page each; the method's own paper is not available):
+  [abstract]  arXiv 2603.05500 abstract, "POET-X: Memory-efficient LLM
+              Training by Scaling Orthogonal Transformation": POET optimises
+              each weight by an orthogonal equivalence transformation that
+              preserves its spectrum.
+  [tech-1]    gist.science summary of the same paper, "Technische
+              Zusammenfassung", section 1 (Problemstellung, "Vorarbeit
+              (POET)"): W = R W0 P with trainable orthogonal R and P.
+  [tech-2-in] same page, section 2 (Methodik), bullet "Input-zentrische
+              Implementierung": apply the transforms to activations, never
+              form the merged weight.
+  [tech-2-bd] section 2, bullet "Batch-parallele Berechnung fuer
+              Block-diagonale Matrizen": R and P are block diagonal; the
+              blocks are independent matrices multiplied as a batch.
+  [tech-2-cnp] section 2, bullet "Effiziente Cayley-Neumann-
+              Parametrisierung (CNP)": the orthogonal blocks come from
+              skew-symmetric Q (Q = -Q^T) through the Cayley transform with
+              a Neumann-series inverse; only the upper triangle of Q is
+              stored; the powers Q^2, Q^3, Q^4 are the work of one fused
+              kernel.
+
+Readings taken where the pages are silent (each one is listed with its
+reason in the design notes):
+  * Cayley form C(Q) = (I+Q)(I-Q)^{-1}; the Neumann truncation after Q^k
+    replaces (I-Q)^{-1} by I+Q+...+Q^k, so a block is
+    R_k(Q) = (I+Q)(I+Q+...+Q^k) = I + 2Q + ... + 2Q^k + Q^{k+1}.
+    k = 3 gives the Q^2, Q^3, Q^4 of [tech-2-cnp].
+  * The packed vector holds the strict upper triangle row by row
+    (i < j; row i, then j ascending), Q[j][i] = -Q[i][j], zero diagonal.
+  * Activations are token-major [T][d]; W0 is [d_out][d_in]; per token
+    y_t = R (W0 (P x_t)).
+  * The gradient returned for the packed parameters is d loss / d theta:
+    dtheta[idx(i,j)] = G_Q[i][j] - G_Q[j][i].
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+
+# --------------------------------------------------------------------------
+# Packed upper triangle  [tech-2-cnp]
+# --------------------------------------------------------------------------
+
+def packed_size(b: int) -> int:
+    """Number of free parameters of a b x b skew-symmetric block."""
+    return b * (b - 1) // 2
+
+
+def packed_index(i, j, b: int):
+    """Position of Q[i][j] (0 <= i < j < b) in the row-by-row strict upper
+    triangle: rows 0..i-1 hold (b-1) + (b-2) + ... + (b-i) entries."""
+    i = np.asarray(i)
+    j = np.asarray(j)
+    return i * b - (i * (i + 1)) // 2 + (j - i - 1)
+
+
+def unpack(theta: np.ndarray, b: int) -> np.ndarray:
+    """theta [n][b(b-1)/2] -> skew-symmetric Q [n][b][b] (float64)."""
+    theta = np.asarray(theta, dtype=np.float64)
+    n = theta.shape[0]
+    assert theta.shape == (n, packed_size(b))
+    ii, jj = np.triu_indices(b, 1)
+    idx = packed_index(ii, jj, b)
+    Q = np.zeros((n, b, b), dtype=np.float64)
+    Q[:, ii, jj] = theta[:, idx]
+    Q[:, jj, ii] = -theta[:, idx]
+    return Q
+
+
+def pack_skew_grad(G_Q: np.ndarray) -> np.ndarray:
+    """Gradient of a loss with respect to the packed parameters, given its
+    gradient G_Q with respect to an unconstrained Q: theta feeds Q[i][j]
+    with +1 and Q[j][i] with -1."""
+    n, b, _ = G_Q.shape
+    ii, jj = np.triu_indices(b, 1)
+    out = np.zeros((n, packed_size(b)), dtype=np.float64)
+    out[:, packed_index(ii, jj, b)] = G_Q[:, ii, jj] - G_Q[:, jj, ii]
+    return out
+
+
+# --------------------------------------------------------------------------
+# Cayley-Neumann blocks  [tech-2-cnp]
+# --------------------------------------------------------------------------
+
+def neumann_coefficients(k: int) -> np.ndarray:
+    """c_i of R_k(Q) = sum_i c_i Q^i, i = 0..k+1:  (I+Q) * sum_{i<=k} Q^i."""
+    c = np.zeros(k + 2)
+    c[: k + 1] += 1.0      # I + Q + ... + Q^k
+    c[1: k + 2] += 1.0     # Q * (I + Q + ... + Q^k)
+    return c
+
+
+def matrix_powers(Q: np.ndarray, m: int) -> list:
+    """[Q^0, Q^1, ..., Q^m] for a stack of square matrices."""
+    n, b, _ = Q.shape
+    P = [np.broadcast_to(np.eye(b), (n, b, b)).copy()]
+    for _ in range(m):
+        P.append(P[-1] @ Q)
+    return P
+
+
+def cayley_neumann(Q: np.ndarray, k: int) -> np.ndarray:
+    """R_k = (I + Q)(I + Q + ... + Q^k), explicit powers."""
+    pw = matrix_powers(Q, k)
+    S = sum(pw)
+    return (pw[0] + Q) @ S
+
+
+def cayley_exact(Q: np.ndarray) -> np.ndarray:
+    """C = (I+Q)(I-Q)^{-1} = (I-Q)^{-1}(I+Q): solve (I-Q) C = I+Q."""
+    n, b, _ = Q.shape
+    eye = np.broadcast_to(np.eye(b), (n, b, b))
+    return np.linalg.solve(eye - Q, eye + Q)
+
+
+def build_blocks(theta: np.ndarray, b: int, k: int) -> np.ndarray:
+    """Packed parameters -> orthogonal (approximately) blocks [n][b][b]."""
+    return cayley_neumann(unpack(theta, b), k)
+
+
+# --------------------------------------------------------------------------
+# Block-diagonal application  [tech-2-bd], input-centric order [tech-2-in]
+# --------------------------------------------------------------------------
+
+def apply_blockdiag(X: np.ndarray, blocks: np.ndarray) -> np.ndarray:
+    """Row form of z_t = B x_t for block-diagonal B: token-major X [T][n*b],
+    output[:, g-block] = X[:, g-block] @ B_g^T."""
+    n, b, _ = blocks.shape
+    T = X.shape[0]
+    Xg = X.reshape(T, n, b)
+    out = np.einsum("tgj,gij->tgi", Xg, blocks)
+    return out.reshape(T, n * b)
+
+
+def apply_blockdiag_transposed(X: np.ndarray, blocks: np.ndarray) -> np.ndarray:
+    """Row form of z_t = B^T x_t: output[:, g-block] = X[:, g-block] @ B_g."""
+    n, b, _ = blocks.shape
+    T = X.shape[0]
+    Xg = X.reshape(T, n, b)
+    out = np.einsum("tgi,gij->tgj", Xg, blocks)
+    return out.reshape(T, n * b)
+
+
+def blockwise_outer(A: np.ndarray, B: np.ndarray, b: int) -> np.ndarray:
+    """Per block g: sum_t A[t, g-block]^T (outer) B[t, g-block] -> [n][b][b]."""
+    T, d = A.shape
+    n = d // b
+    return np.einsum("tgi,tgj->gij", A.reshape(T, n, b), B.reshape(T, n, b))
+
+
+def forward(x, W0, P_blocks, R_blocks):
+    """y_t = R_b (W0 (P_b x_t)) for every token.  Returns (y, u, v)."""
+    x = np.asarray(x, dtype=np.float64)
+    W0 = np.asarray(W0, dtype=np.float64)
+    u = apply_blockdiag(x, P_blocks)        # u_t = P x_t
+    v = u @ W0.T                            # v_t = W0 u_t
+    y = apply_blockdiag(v, R_blocks)        # y_t = R v_t
+    return y, u, v
+
+
+def backward(dy, x, W0, P_blocks, R_blocks, v):
+    """Gradients of L = sum_t <dy_t, y_t> with respect to x, P_b and R_b
+    (W0 is frozen and gets none).  Returns (dx, G_P, G_R) where G_* are the
+    gradients with respect to each full b x b block."""
+    dy = np.asarray(dy, dtype=np.float64)
+    x = np.asarray(x, dtype=np.float64)
+    W0 = np.asarray(W0, dtype=np.float64)
+    b = P_blocks.shape[1]
+    dv = apply_blockdiag_transposed(dy, R_blocks)   # dv_t = R^T dy_t
+    G_R = blockwise_outer(dy, v, b)                 # sum_t dy_t v_t^T
+    du = dv @ W0                                    # du_t = W0^T dv_t
+    G_P = blockwise_outer(du, x, b)                 # sum_t du_t x_t^T
+    dx = apply_blockdiag_transposed(du, P_blocks)   # dx_t = P^T du_t
+    return dx, G_P, G_R
+
+
+def cnp_adjoint(Q: np.ndarray, G: np.ndarray, k: int) -> np.ndarray:
+    """Gradient with respect to Q of <G, R_k(Q)>, R_k = sum_i c_i Q^i.
+    Written as the direct double sum of the derivative of each power:
+        G_Q = sum_i c_i sum_{j=0}^{i-1} (Q^T)^j G (Q^T)^{i-1-j}."""
+    c = neumann_coefficients(k)
+    QT = np.transpose(Q, (0, 2, 1))
+    pw = matrix_powers(QT, k)
+    G_Q = np.zeros_like(G, dtype=np.float64)
+    for i in range(1, k + 2):
+        for j in range(i):
+            G_Q += c[i] * (pw[j] @ G @ pw[i - 1 - j])
+    return G_Q
+
+
+def layer(theta_P, theta_R, W0, x, dy, b: int, k: int):
+    """Whole hot path: build both sides, forward, backward, packed grads.
+    Returns a dict of float64 arrays."""
+    Q_P = unpack(theta_P, b)
+    Q_R = unpack(theta_R, b)
+    P_blocks = cayley_neumann(Q_P, k)
+    R_blocks = cayley_neumann(Q_R, k)
+    y, u, v = forward(x, W0, P_blocks, R_blocks)
+    dx, G_P, G_R = backward(dy, x, W0, P_blocks, R_blocks, v)
+    dtheta_P = pack_skew_grad(cnp_adjoint(Q_P, G_P, k))
+    dtheta_R = pack_skew_grad(cnp_adjoint(Q_R, G_R, k))
+    return dict(P_blocks=P_blocks, R_blocks=R_blocks, u=u, v=v, y=y, dx=dx,
+                G_P=G_P, G_R=G_R, dtheta_P=dtheta_P, dtheta_R=dtheta_R)
+
+
+# --------------------------------------------------------------------------
+# Checks only: dense embedding and scalar loss for finite differences
+# --------------------------------------------------------------------------
+
+def dense_from_blocks(blocks: np.ndarray) -> np.ndarray:
+    """Explicit d x d block-diagonal matrix (d = n*b)."""
+    n, b, _ = blocks.shape
+    D = np.zeros((n * b, n * b))
+    for g in range(n):
+        D[g * b:(g + 1) * b, g * b:(g + 1) * b] = blocks[g]
+    return D
+
+
+def loss(theta_P, theta_R, W0, x, dy, b: int, k: int) -> float:
+    """L = sum_t <dy_t, y_t>, the scalar whose gradients backward() returns."""
+    P_blocks = build_blocks(theta_P, b, k)
+    R_blocks = build_blocks(theta_R, b, k)
+    y, _, _ = forward(x, W0, P_blocks, R_blocks)
+    return float(np.sum(np.asarray(dy, dtype=np.float64) * y))

@@ -1,0 +1,272 @@
+"""Pins for the float64 oracle: each test checks it against something other
+than itself (brute-force enumeration, closed forms, invariants of the
+mathematics, an independent dense construction, finite differences), so
+that a dropped term, a wrong sign or index or a transposed operand in the
+oracle fails at least one of them.  CPU only."""
+
+import json
+import os
+
+import numpy as np
+import pytest
+import scipy.linalg
+
+import oracle
+from orthogonal_reparameterized_packed_gb300.inputs import make_layer_inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rand_skew(rng, n, b, scale):
+    M = rng.standard_normal((n, b, b)) * scale
+    return M - np.transpose(M, (0, 2, 1))
+
+
+# ----------------------------------------------------------------- packing
+
+@pytest.mark.parametrize("b", [2, 3, 5, 8, 32, 64])
+def test_packed_index_matches_enumeration(b):
+    count = 0
+    for i in range(b):
+        for j in range(i + 1, b):
+            assert oracle.packed_index(i, j, b) == count
+            count += 1
+    assert count == oracle.packed_size(b)
+
+
+@pytest.mark.parametrize("b", [2, 4, 7, 32])
+def test_unpack_is_inverse_of_enumerated_pack(b):
+    rng = np.random.default_rng(1)
+    A = _rand_skew(rng, 3, b, 1.0)
+    theta = np.zeros((3, oracle.packed_size(b)))
+    for g in range(3):
+        c = 0
+        for i in range(b):
+            for j in range(i + 1, b):
+                theta[g, c] = A[g, i, j]
+                c += 1
+    Q = oracle.unpack(theta, b)
+    assert np.array_equal(Q, A)
+    assert np.array_equal(Q, -np.transpose(Q, (0, 2, 1)))
+    assert np.all(np.diagonal(Q, axis1=1, axis2=2) == 0)
+
+
+@pytest.mark.parametrize("b", [2, 5, 16])
+def test_pack_skew_grad_matches_enumeration(b):
+    rng = np.random.default_rng(2)
+    G = rng.standard_normal((2, b, b))
+    got = oracle.pack_skew_grad(G)
+    for g in range(2):
+        c = 0
+        for i in range(b):
+            for j in range(i + 1, b):
+                assert got[g, c] == G[g, i, j] - G[g, j, i]
+                c += 1
+
+
+def test_neumann_coefficients():
+    assert list(oracle.neumann_coefficients(0)) == [1, 1]
+    assert list(oracle.neumann_coefficients(3)) == [1, 2, 2, 2, 1]
+
+
+# ----------------------------------------------------- 2x2 closed forms
+
+def _two_by_two(a):
+    return oracle.unpack(np.array([[a]]), 2)
+
+
+def test_golden_2x2_rotation():
+    """Closed-form 2x2 values stored in tests/golden (see its header)."""
+    with open(os.path.join(GOLDEN, "cayley_2x2.json")) as f:
+        gold = json.load(f)
+    for case in gold["cases"]:
+        Q = _two_by_two(case["a"])
+        np.testing.assert_allclose(oracle.cayley_exact(Q)[0], case["cayley"],
+                                   rtol=0, atol=1e-15)
+        for k_str, R in case["neumann"].items():
+            np.testing.assert_allclose(oracle.cayley_neumann(Q, int(k_str))[0], R,
+                                       rtol=0, atol=1e-15)
+
+
+@pytest.mark.parametrize("a", [0.0, 0.1, -0.37, 0.9])
+@pytest.mark.parametrize("k", [0, 1, 2, 3, 4, 5])
+def test_2x2_neumann_closed_form(a, k):
+    # Q = [[0,a],[-a,0]] has Q^2 = -a^2 I, so sum_{i<=k} Q^i = alpha I + beta Q
+    alpha = sum((-a * a) ** m for m in range(k // 2 + 1))
+    beta = sum((-a * a) ** m for m in range((k - 1) // 2 + 1)) if k >= 1 else 0.0
+    diag = alpha - beta * a * a
+    off = alpha + beta
+    want = np.array([[diag, off * a], [-off * a, diag]])
+    got = oracle.cayley_neumann(_two_by_two(a), k)[0]
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-15)
+
+
+# ------------------------------------------------------- exact Cayley
+
+@pytest.mark.parametrize("b,scale", [(8, 0.3), (32, 0.1), (64, 0.05), (16, 2.0)])
+def test_exact_cayley_is_orthogonal(b, scale):
+    rng = np.random.default_rng(3)
+    Q = _rand_skew(rng, 4, b, scale)
+    C = oracle.cayley_exact(Q)
+    for g in range(4):
+        err = np.max(np.abs(C[g].T @ C[g] - np.eye(b)))
+        assert err <= 1e-12
+        assert abs(np.linalg.det(C[g]) - 1.0) < 1e-10
+
+
+@pytest.mark.parametrize("k", [0, 1, 2, 3, 5, 8])
+def test_neumann_truncation_error_closed_form(k):
+    # C - R_k = (I+Q) Q^{k+1} (I-Q)^{-1}; Q is normal with eigenvalues i*lam,
+    # |1+i lam| = |1-i lam|, so ||C - R_k||_2 = ||Q||_2^{k+1} exactly.
+    rng = np.random.default_rng(4)
+    b = 24
+    Q = _rand_skew(rng, 3, b, 0.08)
+    C = oracle.cayley_exact(Q)
+    R = oracle.cayley_neumann(Q, k)
+    I = np.eye(b)
+    for g in range(3):
+        rhs = (I + Q[g]) @ np.linalg.matrix_power(Q[g], k + 1) @ np.linalg.inv(I - Q[g])
+        np.testing.assert_allclose(C[g] - R[g], rhs, rtol=0, atol=1e-12)
+        rho = np.linalg.norm(Q[g], 2)
+        err = np.linalg.norm(C[g] - R[g], 2)
+        assert abs(err - rho ** (k + 1)) <= 1e-9 * max(1.0, rho ** (k + 1))
+
+
+def test_neumann_error_shrinks_with_k():
+    rng = np.random.default_rng(5)
+    Q = _rand_skew(rng, 2, 32, 0.05)
+    C = oracle.cayley_exact(Q)
+    errs = [np.linalg.norm(C - oracle.cayley_neumann(Q, k)) for k in range(7)]
+    rho = max(np.linalg.norm(Q[g], 2) for g in range(2))
+    assert rho < 1
+    for k in range(1, 7):
+        assert errs[k] < errs[k - 1]
+        assert errs[k] / errs[k - 1] <= rho * 1.0001
+
+
+# ---------------------------------------- forward: dense and spectrum
+
+def _dense_reference(theta_P, theta_R, W0, b, k):
+    """Independent dense construction with scipy's block_diag."""
+    P = scipy.linalg.block_diag(*oracle.build_blocks(theta_P, b, k))
+    R = scipy.linalg.block_diag(*oracle.build_blocks(theta_R, b, k))
+    return R @ np.asarray(W0, np.float64) @ P
+
+
+@pytest.mark.parametrize("d_in,d_out,b", [(16, 24, 4), (32, 32, 8), (12, 12, 12)])
+def test_blockdiag_path_equals_dense_product(d_in, d_out, b):
+    inp = make_layer_inputs(d_in, d_out, b, 3, 7, dtype="f32", sigma_theta=0.2, seed=6)
+    W = _dense_reference(inp.theta_P, inp.theta_R, inp.W0, b, 3)
+    P = oracle.build_blocks(inp.theta_P, b, 3)
+    R = oracle.build_blocks(inp.theta_R, b, 3)
+    y, _, _ = oracle.forward(inp.x, inp.W0, P, R)
+    want = np.asarray(inp.x, np.float64) @ W.T
+    np.testing.assert_allclose(y, want, rtol=0, atol=1e-13 * np.abs(want).max())
+
+
+def test_spectrum_preserved_with_exact_cayley():
+    rng = np.random.default_rng(7)
+    d_in, d_out, b = 32, 24, 8
+    W0 = rng.standard_normal((d_out, d_in))
+    CP = oracle.cayley_exact(_rand_skew(rng, d_in // b, b, 0.4))
+    CR = oracle.cayley_exact(_rand_skew(rng, d_out // b, b, 0.4))
+    # W from the input-centric forward: feeding x = I gives y = W^T
+    y, _, _ = oracle.forward(np.eye(d_in), W0, CP, CR)
+    W = y.T
+    s0 = np.linalg.svd(W0, compute_uv=False)
+    s = np.linalg.svd(W, compute_uv=False)
+    np.testing.assert_allclose(s, s0, rtol=1e-10, atol=0)
+    # the truncated series is not exactly orthogonal: its spectrum moves
+    PK = oracle.cayley_neumann(_rand_skew(np.random.default_rng(8), d_in // b, b, 0.4), 1)
+    yk, _, _ = oracle.forward(np.eye(d_in), W0, PK, CR)
+    sk = np.linalg.svd(yk.T, compute_uv=False)
+    assert np.max(np.abs(sk - s0) / s0) > 1e-4
+
+
+# ------------------------------------------------------ special cases
+
+def test_zero_theta_gives_identity_blocks_and_plain_linear():
+    inp = make_layer_inputs(16, 8, 4, 3, 5, dtype="f32", seed=9)
+    zP = np.zeros_like(inp.theta_P)
+    zR = np.zeros_like(inp.theta_R)
+    out = oracle.layer(zP, zR, inp.W0, inp.x, inp.dy, 4, 3)
+    assert np.array_equal(out["P_blocks"], np.broadcast_to(np.eye(4), (4, 4, 4)))
+    x = inp.x.astype(np.float64)
+    W0 = inp.W0.astype(np.float64)
+    dy = inp.dy.astype(np.float64)
+    np.testing.assert_allclose(out["y"], x @ W0.T, rtol=1e-14, atol=1e-14)
+    np.testing.assert_allclose(out["dx"], dy @ W0, rtol=1e-14, atol=1e-14)
+    # R_k'(0)[H] = 2H: dtheta_R = pack(2(G_R - G_R^T)) with G_R = sum_t dy_t v_t^T
+    v = x @ W0.T
+    G_R = np.einsum("tgi,tgj->gij", dy.reshape(5, 2, 4), v.reshape(5, 2, 4))
+    want = np.zeros_like(out["dtheta_R"])
+    c = 0
+    for i in range(4):
+        for j in range(i + 1, 4):
+            want[:, c] = 2 * (G_R[:, i, j] - G_R[:, j, i])
+            c += 1
+    np.testing.assert_allclose(out["dtheta_R"], want, rtol=1e-13, atol=1e-13)
+
+
+def test_k0_is_one_plus_q():
+    rng = np.random.default_rng(10)
+    Q = _rand_skew(rng, 3, 6, 0.3)
+    np.testing.assert_array_equal(oracle.cayley_neumann(Q, 0), np.eye(6) + Q)
+
+
+def test_single_block_b_equals_d():
+    inp = make_layer_inputs(8, 8, 8, 2, 3, dtype="f32", sigma_theta=0.3, seed=11)
+    P = oracle.build_blocks(inp.theta_P, 8, 2)[0]
+    R = oracle.build_blocks(inp.theta_R, 8, 2)[0]
+    y, _, _ = oracle.forward(inp.x, inp.W0, P[None], R[None])
+    want = inp.x.astype(np.float64) @ (R @ inp.W0.astype(np.float64) @ P).T
+    np.testing.assert_allclose(y, want, rtol=1e-13, atol=1e-13)
+
+
+# ------------------------------------------------- finite differences
+
+def _central_diff(f, x0, idx, h):
+    xp = x0.copy()
+    xm = x0.copy()
+    xp[idx] += h
+    xm[idx] -= h
+    return (f(xp) - f(xm)) / (2 * h)
+
+
+@pytest.mark.parametrize("k", [0, 1, 3])
+def test_gradients_match_central_differences(k):
+    inp = make_layer_inputs(8, 12, 4, k, 5, dtype="f32", sigma_theta=0.3, seed=12)
+    tP = inp.theta_P.astype(np.float64)
+    tR = inp.theta_R.astype(np.float64)
+    x = inp.x.astype(np.float64)
+    W0 = inp.W0.astype(np.float64)
+    dy = inp.dy.astype(np.float64)
+    out = oracle.layer(tP, tR, W0, x, dy, 4, k)
+    h = 1e-6
+
+    def rel(a, b):
+        return abs(a - b) / max(1e-8, abs(b))
+
+    for idx in np.ndindex(*tP.shape):
+        fd = _central_diff(lambda t: oracle.loss(t, tR, W0, x, dy, 4, k), tP, idx, h)
+        assert rel(out["dtheta_P"][idx], fd) <= 1e-6
+    for idx in np.ndindex(*tR.shape):
+        fd = _central_diff(lambda t: oracle.loss(tP, t, W0, x, dy, 4, k), tR, idx, h)
+        assert rel(out["dtheta_R"][idx], fd) <= 1e-6
+    for idx in [(0, 0), (2, 5), (4, 7), (1, 3)]:
+        fd = _central_diff(lambda xx: oracle.loss(tP, tR, W0, xx, dy, 4, k), x, idx, h)
+        assert rel(out["dx"][idx], fd) <= 1e-6
+
+
+def test_cnp_adjoint_matches_directional_derivative():
+    # unconstrained direction H (not skew) checks the full adjoint
+    rng = np.random.default_rng(13)
+    b, k = 6, 4
+    Q = _rand_skew(rng, 1, b, 0.3)
+    G = rng.standard_normal((1, b, b))
+    H = rng.standard_normal((1, b, b))
+    G_Q = oracle.cnp_adjoint(Q, G, k)
+    eps = 1e-6
+    f = lambda t: np.sum(G * oracle.cayley_neumann(Q + t * H, k))
+    fd = (f(eps) - f(-eps)) / (2 * eps)
+    assert abs(np.sum(G_Q * H) - fd) <= 1e-7 * max(1.0, abs(fd))
