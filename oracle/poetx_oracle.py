@@ -137,28 +137,34 @@ def build_blocks(theta: np.ndarray, b: int, k: int) -> np.ndarray:
 
 def apply_blockdiag(X: np.ndarray, blocks: np.ndarray) -> np.ndarray:
     """Row form of z_t = B x_t for block-diagonal B: token-major X [T][n*b],
-    output[:, g-block] = X[:, g-block] @ B_g^T."""
+    one independent product per block: out[:, g-block] = X[:, g-block] @ B_g^T."""
+    X = np.asarray(X, dtype=np.float64)
     n, b, _ = blocks.shape
-    T = X.shape[0]
-    Xg = X.reshape(T, n, b)
-    out = np.einsum("tgj,gij->tgi", Xg, blocks)
-    return out.reshape(T, n * b)
+    out = np.empty((X.shape[0], n * b))
+    for g in range(n):
+        out[:, g * b:(g + 1) * b] = X[:, g * b:(g + 1) * b] @ blocks[g].T
+    return out
 
 
 def apply_blockdiag_transposed(X: np.ndarray, blocks: np.ndarray) -> np.ndarray:
-    """Row form of z_t = B^T x_t: output[:, g-block] = X[:, g-block] @ B_g."""
+    """Row form of z_t = B^T x_t: out[:, g-block] = X[:, g-block] @ B_g."""
+    X = np.asarray(X, dtype=np.float64)
     n, b, _ = blocks.shape
-    T = X.shape[0]
-    Xg = X.reshape(T, n, b)
-    out = np.einsum("tgi,gij->tgj", Xg, blocks)
-    return out.reshape(T, n * b)
+    out = np.empty((X.shape[0], n * b))
+    for g in range(n):
+        out[:, g * b:(g + 1) * b] = X[:, g * b:(g + 1) * b] @ blocks[g]
+    return out
 
 
 def blockwise_outer(A: np.ndarray, B: np.ndarray, b: int) -> np.ndarray:
     """Per block g: sum_t A[t, g-block]^T (outer) B[t, g-block] -> [n][b][b]."""
-    T, d = A.shape
-    n = d // b
-    return np.einsum("tgi,tgj->gij", A.reshape(T, n, b), B.reshape(T, n, b))
+    A = np.asarray(A, dtype=np.float64)
+    B = np.asarray(B, dtype=np.float64)
+    n = A.shape[1] // b
+    G = np.empty((n, b, b))
+    for g in range(n):
+        G[g] = A[:, g * b:(g + 1) * b].T @ B[:, g * b:(g + 1) * b]
+    return G
 
 
 def forward(x, W0, P_blocks, R_blocks):
@@ -214,6 +220,18 @@ def layer(theta_P, theta_R, W0, x, dy, b: int, k: int):
     dtheta_R = pack_skew_grad(cnp_adjoint(Q_R, G_R, k))
     return dict(P_blocks=P_blocks, R_blocks=R_blocks, u=u, v=v, y=y, dx=dx,
                 G_P=G_P, G_R=G_R, dtheta_P=dtheta_P, dtheta_R=dtheta_R)
+
+
+def transform(theta, x, dout, b: int, k: int):
+    """The block-diagonal transform on its own, z_t = B x_t, and the
+    gradients of L = sum_t <dout_t, z_t> with respect to x and theta."""
+    Q = unpack(theta, b)
+    B = cayley_neumann(Q, k)
+    z = apply_blockdiag(x, B)
+    dx = apply_blockdiag_transposed(dout, B)
+    G = blockwise_outer(dout, x, b)
+    dtheta = pack_skew_grad(cnp_adjoint(Q, G, k))
+    return dict(blocks=B, z=z, dx=dx, G=G, dtheta=dtheta)
 
 
 # --------------------------------------------------------------------------

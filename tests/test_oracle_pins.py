@@ -270,3 +270,24 @@ def test_cnp_adjoint_matches_directional_derivative():
     f = lambda t: np.sum(G * oracle.cayley_neumann(Q + t * H, k))
     fd = (f(eps) - f(-eps)) / (2 * eps)
     assert abs(np.sum(G_Q * H) - fd) <= 1e-7 * max(1.0, abs(fd))
+
+
+def test_transform_gradients_match_central_differences():
+    inp = make_layer_inputs(12, 12, 4, 3, 6, dtype="f32", sigma_theta=0.3, seed=14)
+    th = inp.theta_P.astype(np.float64)
+    x = inp.x.astype(np.float64)
+    g = inp.dy.astype(np.float64)
+    out = oracle.transform(th, x, g, 4, 3)
+
+    def L(t, xx):
+        return float(np.sum(g * oracle.apply_blockdiag(xx, oracle.build_blocks(t, 4, 3))))
+
+    for idx in np.ndindex(*th.shape):
+        fd = _central_diff(lambda t: L(t, x), th, idx, 1e-6)
+        assert abs(out["dtheta"][idx] - fd) <= 1e-6 * max(1e-8, abs(fd))
+    for idx in [(0, 0), (3, 11), (5, 6)]:
+        fd = _central_diff(lambda xx: L(th, xx), x, idx, 1e-6)
+        assert abs(out["dx"][idx] - fd) <= 1e-6 * max(1e-8, abs(fd))
+    # block-diagonal application against scipy's dense block_diag
+    D = scipy.linalg.block_diag(*out["blocks"])
+    np.testing.assert_allclose(out["z"], x @ D.T, rtol=0, atol=1e-13)
