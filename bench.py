@@ -1,0 +1,374 @@
+"""POET-X layer forward+backward throughput on GB300.
+
+One step = the whole hot path for one projection: build the P and R blocks
+from their packed parameters, forward y = R (W0 (P x)), backward to dx and
+the packed dtheta_P, dtheta_R.  Default workload: the Llama-3-8B q/o
+projection, 4096 x 4096, b = 256, k = 3, 16384 tokens, bf16 with fp32
+accumulation.  Inputs are synthetic (seeded Gaussians of the documented
+shapes) and already resident in HBM; x, dy (128 MiB each) and the step's
+other tensors exceed the 129 MB L2, so no separate flush is needed.
+
+--gpus N under torchrun runs N independent replicas (the layer does not
+shard); value = tokens of all ranks / max time over ranks.
+--impl reference times the float64 CPU oracle on the host cores instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from orthogonal_reparameterized_packed_gb300.inputs import WORKLOADS, make_layer_inputs  # noqa
+
+METRIC = "POET-X layer fwd+bwd tokens/s (d=4096,b=256,bf16); % HBM / tensor-core roofline"
+UNIT = "tokens/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="poetx", choices=["poetx", "reference"])
+    ap.add_argument("--workload", default="llama3_8b_qo", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def workload_config(name):
+    w = dict(WORKLOADS[name])
+    return w
+
+
+def config_json(name, w, n):
+    return {"workload": name, "d_in": w["d_in"], "d_out": w["d_out"], "b": w["b"], "k": w["k"],
+            "tokens_per_gpu": w["tokens"], "dtype": w["dtype"], "parallelism": f"replicas{n}",
+            "l2": "inputs larger than L2 (x, dy 128 MiB each; ~1 GB touched per step)"}
+
+
+# ----------------------------------------------------------- CPU oracle
+
+def blas_threads():
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var):
+            try:
+                return int(os.environ[var])
+            except ValueError:
+                pass
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("num_threads")]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def oracle_sample(inp, sample_tokens):
+    """Time the oracle on a bounded sample: the token-independent part (block
+    build and CNP adjoint of both sides) once, and forward+backward on the
+    first `sample_tokens` tokens.  Returns (t_fixed_s, t_per_token_s)."""
+    import oracle
+    b, k = inp.b, inp.k
+    t0 = time.perf_counter()
+    QP = oracle.unpack(inp.theta_P, b)
+    QR = oracle.unpack(inp.theta_R, b)
+    P = oracle.cayley_neumann(QP, k)
+    R = oracle.cayley_neumann(QR, k)
+    t1 = time.perf_counter()
+    x = inp.x[:sample_tokens]
+    dy = inp.dy[:sample_tokens]
+    y, u, v = oracle.forward(x, inp.W0, P, R)
+    dx, G_P, G_R = oracle.backward(dy, x, inp.W0, P, R, v)
+    t2 = time.perf_counter()
+    oracle.pack_skew_grad(oracle.cnp_adjoint(QP, G_P, k))
+    oracle.pack_skew_grad(oracle.cnp_adjoint(QR, G_R, k))
+    t3 = time.perf_counter()
+    return (t1 - t0) + (t3 - t2), (t2 - t1) / sample_tokens
+
+
+def cpu_baseline(inp, sample_tokens):
+    t_fixed, t_tok = oracle_sample(inp, sample_tokens)
+    T = inp.tokens
+    value = T / (t_fixed + t_tok * T)
+    return {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "sample": (f"float64 numpy oracle: block build + CNP adjoint of both sides "
+                       f"({t_fixed:.2f} s) and forward+backward on {sample_tokens} of {T} "
+                       f"tokens ({t_tok * sample_tokens:.2f} s); tokens/s extrapolated "
+                       f"linearly in tokens to the full {T}")}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    name = args.workload
+    w = workload_config(name)
+    inp = make_layer_inputs(**w, seed=0)
+    sample = 256
+    for _ in range(args.warmup):
+        oracle_sample(inp, sample)
+    vals = []
+    t_all = 0.0
+    for _ in range(args.steps):
+        t_fixed, t_tok = oracle_sample(inp, sample)
+        step_s = t_fixed + t_tok * inp.tokens
+        t_all += step_s
+        vals.append(inp.tokens / step_s)
+    value = args.steps * inp.tokens / t_all
+    cores = blas_threads()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * t_all / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_json(name, w, args.gpus),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": (f"each step: block build + CNP adjoint of both sides "
+                                        f"and forward+backward on {sample} of {inp.tokens} "
+                                        f"tokens, extrapolated linearly in tokens")},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# -------------------------------------------------------------- GPU arm
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, \
+        "fallback"
+
+
+def algorithmic_work(tag, w):
+    """(amount, unit, bound) per launch for a kernel tag of one step."""
+    T, di, do, b = w["tokens"], w["d_in"], w["d_out"], w["b"]
+    if tag in ("gemm_w0", "gemm_w0_dgrad"):
+        return 2.0 * T * di * do / 1e12, "TFLOP", "tensor"
+    return None
+
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import orthogonal_reparameterized_packed_gb300 as poetx
+    from orthogonal_reparameterized_packed_gb300.layer import PoetxLayer, to_device
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    poetx.load_library()
+
+    name = args.workload
+    w = workload_config(name)
+    inp = make_layer_inputs(**w, seed=rank)
+    dev = to_device(inp)
+    layer = PoetxLayer(w["d_in"], w["d_out"], w["b"], w["k"], w["tokens"], dtype=w["dtype"])
+    stream = torch.cuda.current_stream()
+
+    def step():
+        layer.step(dev["theta_P"], dev["theta_R"], dev["W0"], dev["x"], dev["dy"])
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    if poetx.poetx_device_status() != 0:
+        raise RuntimeError("device status not OK after warm-up")
+
+    clocks = ClockSampler(local)
+    launches0 = poetx.poetx_launch_count()
+    poetx.poetx_profile_start(64 * args.steps)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)  # let the sampler take its first reading
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    poetx.poetx_profile_stop()
+    launches = poetx.poetx_launch_count() - launches0
+    ms = t0.elapsed_time(t1) / args.steps
+    ms_t = torch.tensor([ms], device="cuda")
+    if world > 1:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+    status = poetx.poetx_device_status()
+
+    # per-kernel times over the timed region
+    tags = ["build", "unpack", "identity_plus", "expand_superblocks", "transform",
+            "transform_t", "gemm_w0", "gemm_w0_dgrad", "outer", "reduce_extract", "cnp_bwd",
+            "pack_skew", "f32_to_bf16"]
+    kernels = {}
+    for t in tags:
+        n, tot = poetx.poetx_profile_query(t)
+        if n:
+            kernels[t] = {"launches": n, "total_ms": tot, "avg_us": 1e3 * tot / n}
+    peaks, peak_src = load_peaks()
+    dom = max((t for t in kernels if algorithmic_work(t, w)), key=lambda t: kernels[t]["total_ms"])
+    amount, unit, bound = algorithmic_work(dom, w)
+    avg_s = kernels[dom]["avg_us"] * 1e-6
+    long_region = ms * args.steps > 1000.0
+    peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
+    achieved = amount / avg_s
+    roofline = {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                "peak_source": f"{peak_src} ({'sustained' if long_region else 'burst'})",
+                "per_launch": f"2*T*d_in*d_out = {amount:.4f} TFLOP"}
+
+    # whole-step algorithmic tensor work for context
+    T, di, do, b = w["tokens"], w["d_in"], w["d_out"], w["b"]
+    step_flop = T * (4.0 * di * do + 6.0 * b * (di + do))
+
+    total_tokens = world * w["tokens"]
+    value = total_tokens / (ms_max * 1e-3)
+
+    # end to end through the C ABI from pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        hx = dev["x"].cpu().pin_memory()
+        hdy = dev["dy"].cpu().pin_memory()
+        hP = torch.empty(layer.dtheta_P.shape, dtype=torch.float32).pin_memory()
+        hR = torch.empty(layer.dtheta_R.shape, dtype=torch.float32).pin_memory()
+        dx_in = torch.empty_like(dev["x"])
+        dy_in = torch.empty_like(dev["dy"])
+
+        def e2e_step():
+            dx_in.copy_(hx, non_blocking=True)
+            dy_in.copy_(hdy, non_blocking=True)
+            layer.step(dev["theta_P"], dev["theta_R"], dev["W0"], dx_in, dy_in)
+            hP.copy_(layer.dtheta_P, non_blocking=True)
+            hR.copy_(layer.dtheta_R, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        ksteps = max(1, min(args.steps, 20))
+        for _ in range(ksteps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = e0.elapsed_time(e1) / ksteps
+        et = torch.tensor([ems], device="cuda")
+        if world > 1:
+            dist.all_reduce(et, op=dist.ReduceOp.MAX)
+        e2e = {"value": total_tokens / (float(et.item()) * 1e-3), "unit": UNIT,
+               "h2d_bytes_per_step": hx.numel() * hx.element_size() +
+               hdy.numel() * hdy.element_size(),
+               "d2h_bytes_per_step": (hP.numel() + hR.numel()) * 4,
+               "steps": ksteps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(inp, 512)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_max,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "bf16", "data": "synthetic", "config": config_json(name, w, world),
+                "gpu_launches": launches, "roofline": roofline,
+                "step_tflops": step_flop / (ms_max * 1e-3) / 1e12,
+                "kernels": kernels, "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
+                "device_status": status}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

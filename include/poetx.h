@@ -1,0 +1,174 @@
+/*
+ * poetx.h -- C ABI of the POET-X layer hot path on one NVIDIA GB300 (sm_103a).
+ *
+ * POET-X trains each weight as W = R * W0 * P with W0 frozen and R, P
+ * orthogonal, so the singular values of W0 are preserved (arXiv 2603.05500
+ * abstract, "POET-X: Memory-efficient LLM Training by Scaling Orthogonal
+ * Transformation"; gist.science technical summary of that paper, section 1,
+ * "Vorarbeit (POET)").  R and P are block diagonal with b x b blocks; each
+ * block is the Cayley transform of a skew-symmetric Q with the inverse
+ * replaced by a Neumann series cut after Q^k, and only the strict upper
+ * triangle of Q is stored (same summary, section 2, "Effiziente
+ * Cayley-Neumann-Parametrisierung (CNP)" and "Batch-parallele Berechnung
+ * fuer Block-diagonale Matrizen").  The transforms are applied to the
+ * activations, never to W0 (section 2, "Input-zentrische Implementierung"):
+ *
+ *     y_t = R (W0 (P x_t))          for every token t
+ *
+ * Conventions shared by every entry point
+ *   - Activations are token-major, row-major: x[t][i] at x + t*d_in + i.
+ *   - W0 is [d_out][d_in] row-major (v_t = W0 u_t).
+ *   - Packed parameters theta: [d/b][b(b-1)/2] float32; block g's entry
+ *     (i, j), i < j, sits at g*b(b-1)/2 + i*b - i(i+1)/2 + (j-i-1), and
+ *     Q[j][i] = -Q[i][j], Q[i][i] = 0.
+ *   - Blocks: [d/b][b][b] row-major in the working dtype; block g maps
+ *     features g*b .. g*b+b-1: z[g*b+i] = sum_j B_g[i][j] x[g*b+j].
+ *   - dtype POETX_BF16: activations, W0 and blocks are bfloat16, every
+ *     contraction accumulates in fp32 on the tensor cores (tcgen05).
+ *     POETX_F32: everything float32, fp32 FFMA on the CUDA cores.
+ *   - All pointers are device pointers, 16-byte aligned, owned by the
+ *     caller.  The library allocates no device memory and keeps no state
+ *     besides a per-device status word; scratch comes from the caller's
+ *     workspace, whose size the *_workspace_size functions return.
+ *   - Every call only enqueues work on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream) and returns; results are ready when the stream
+ *     is.  Calls on one stream may share one workspace; calls that may run
+ *     concurrently need separate workspaces.
+ *   - Supported shapes: b >= 2, b <= 512, d % b == 0 for F32.  BF16 also
+ *     needs b in {32, 64, 128, 256, 512} and every feature dimension a
+ *     multiple of max(b, 256) (POETX_ERR_UNSUPPORTED otherwise).  0 <= k
+ *     <= 16.  0 <= tokens <= 2^22; with tokens = 0 the activation pointers
+ *     may be NULL and outputs that are sums over tokens are set to zero.
+ *   - Errors: argument problems return POETX_ERR_INVALID_ARG /
+ *     UNSUPPORTED / WORKSPACE before anything is enqueued; a launch failure
+ *     returns POETX_ERR_CUDA.  A kernel that gives up on an internal wait
+ *     records POETX_ERR_TIMEOUT in the status word, read with
+ *     poetx_device_status().
+ */
+#ifndef POETX_H_
+#define POETX_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  POETX_OK = 0,
+  POETX_ERR_INVALID_ARG = 1,
+  POETX_ERR_UNSUPPORTED = 2,
+  POETX_ERR_WORKSPACE = 3,
+  POETX_ERR_CUDA = 4,
+  POETX_ERR_TIMEOUT = 5
+} poetx_status;
+
+typedef enum { POETX_F32 = 0, POETX_BF16 = 1 } poetx_dtype;
+
+typedef void* poetx_stream; /* cudaStream_t */
+
+/* Human-readable name of a status code (static storage). */
+const char* poetx_status_string(poetx_status s);
+
+/* Number of float32 parameters of one side: (d/b) * b(b-1)/2 ("only the
+ * upper triangle of the skew-symmetric Q is stored", technical summary,
+ * section 2, CNP bullet).  Returns 0 for invalid d, b. */
+size_t poetx_packed_size(int d, int b);
+
+/* ------------------------------------------------------------------------
+ * Block build: packed theta -> blocks R_k(Q_g) = (I + Q)(I + Q + ... + Q^k)
+ *   = I + 2Q + ... + 2Q^k + Q^{k+1}, the Neumann-truncated Cayley transform
+ * (technical summary, section 2, CNP bullet: the powers Q^2..Q^4 of k = 3
+ * are built in one fused step).  Arithmetic in fp32 (F32) or bf16 tensor
+ * cores with fp32 accumulation (BF16, b >= 128); rounded once at the store.
+ *   theta  [d/b][b(b-1)/2] float32 (read only)
+ *   blocks [d/b][b][b] dtype (written)
+ * ------------------------------------------------------------------------ */
+size_t poetx_build_workspace_size(int d, int b, int k, poetx_dtype dtype);
+poetx_status poetx_build_blocks(const float* theta, int d, int b, int k, poetx_dtype dtype,
+                                void* blocks, void* workspace, size_t workspace_bytes,
+                                poetx_stream stream);
+
+/* ------------------------------------------------------------------------
+ * Forward: y_t = R (W0 (P x_t)) (technical summary, section 2,
+ * "Input-zentrische Implementierung" and the block-diagonal bullet).
+ *   x       [tokens][d_in]   dtype (read)
+ *   W0      [d_out][d_in]    dtype (read; frozen)
+ *   P_blocks [d_in/b][b][b], R_blocks [d_out/b][b][b]  dtype (read)
+ *   y       [tokens][d_out]  dtype (written)
+ *   v_saved [tokens][d_out]  dtype, v_t = W0 P x_t, written if not NULL
+ *           (the backward pass needs it; pass NULL to have it recomputed)
+ * ------------------------------------------------------------------------ */
+size_t poetx_forward_workspace_size(int d_in, int d_out, int b, int64_t tokens,
+                                    poetx_dtype dtype);
+poetx_status poetx_forward(const void* x, const void* W0, const void* P_blocks,
+                           const void* R_blocks, void* y, void* v_saved, int d_in, int d_out,
+                           int b, int64_t tokens, poetx_dtype dtype, void* workspace,
+                           size_t workspace_bytes, poetx_stream stream);
+
+/* ------------------------------------------------------------------------
+ * Backward of L = sum_t <dy_t, y_t> with W0 frozen:
+ *   dx_t = P^T W0^T R^T dy_t,
+ *   dtheta_P, dtheta_R = d L / d theta for the packed parameters, i.e. the
+ *   adjoint of the Cayley-Neumann polynomial applied to the block gradient
+ *   G = sum_t (dout_t)(in_t)^T, then skew-projected and packed:
+ *   dtheta[idx(i,j)] = G_Q[i][j] - G_Q[j][i].
+ *   dy [tokens][d_out], x [tokens][d_in], W0, blocks: dtype (read)
+ *   theta_P, theta_R: packed float32 (read)
+ *   v_saved [tokens][d_out] from poetx_forward, or NULL: v is recomputed
+ *           from x (activation recompute, the POET-Xmem trade of memory for
+ *           time: technical summary, section 2, "Gradient Checkpointing")
+ *   dx [tokens][d_in] dtype, dtheta_P, dtheta_R float32: overwritten
+ * ------------------------------------------------------------------------ */
+size_t poetx_backward_workspace_size(int d_in, int d_out, int b, int k, int64_t tokens,
+                                     poetx_dtype dtype, int recompute_v);
+poetx_status poetx_backward(const void* dy, const void* x, const void* W0, const float* theta_P,
+                            const float* theta_R, const void* P_blocks, const void* R_blocks,
+                            const void* v_saved, void* dx, float* dtheta_P, float* dtheta_R,
+                            int d_in, int d_out, int b, int k, int64_t tokens, poetx_dtype dtype,
+                            void* workspace, size_t workspace_bytes, poetx_stream stream);
+
+/* ------------------------------------------------------------------------
+ * Isolated block-diagonal transform z_t = B x_t and its backward (the
+ * block-parallel product of the technical summary, section 2, on its own):
+ *   forward : out [tokens][d] = blockdiag(blocks) applied to x [tokens][d]
+ *   backward: dx_t = B^T dout_t and dtheta = packed d L / d theta for
+ *             L = sum_t <dout_t, z_t>
+ * ------------------------------------------------------------------------ */
+size_t poetx_transform_workspace_size(int d, int b, int k, int64_t tokens, poetx_dtype dtype);
+poetx_status poetx_transform_forward(const void* x, const void* blocks, void* out, int d, int b,
+                                     int64_t tokens, poetx_dtype dtype, void* workspace,
+                                     size_t workspace_bytes, poetx_stream stream);
+poetx_status poetx_transform_backward(const void* dout, const void* x, const float* theta,
+                                      const void* blocks, void* dx, float* dtheta, int d, int b,
+                                      int k, int64_t tokens, poetx_dtype dtype, void* workspace,
+                                      size_t workspace_bytes, poetx_stream stream);
+
+/* ------------------------------------------------------------------------
+ * Status and measurement
+ * ------------------------------------------------------------------------ */
+/* Synchronizes the current device, returns the status recorded by kernels
+ * since the last call (POETX_OK or POETX_ERR_TIMEOUT) and clears it;
+ * POETX_ERR_CUDA if the device reports an error. */
+poetx_status poetx_device_status(void);
+
+/* Total number of kernels this library has launched in this process. */
+long long poetx_launch_count(void);
+
+/* Launch timing: while on, every launch is bracketed by CUDA events on its
+ * own stream, grouped by kernel tag ("gemm_w0", "transform", ...).
+ * poetx_profile_start(capacity) clears earlier records and turns timing on
+ * for up to `capacity` launches; poetx_profile_stop() turns it off.
+ * poetx_profile_query(tag, &count, &total_ms) synchronizes the recorded
+ * events and sums the durations of launches with that tag (NULL = all).
+ * Returns 0, or -1 if no events could be created. */
+int poetx_profile_start(int capacity);
+void poetx_profile_stop(void);
+int poetx_profile_query(const char* tag, int* count, double* total_ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* POETX_H_ */

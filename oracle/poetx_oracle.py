@@ -193,6 +193,19 @@ def backward(dy, x, W0, P_blocks, R_blocks, v):
     return dx, G_P, G_R
 
 
+def forward_v_rows(x, W0, P_blocks, rows):
+    """v_t = W0 (P x_t) restricted to the output features `rows` (a slice):
+    the same products as forward(), for a subset of its outputs."""
+    u = apply_blockdiag(x, P_blocks)
+    return u @ np.asarray(W0, dtype=np.float64)[rows].T
+
+
+def backward_du_cols(dy, W0, R_blocks, cols):
+    """du_t = W0^T (R^T dy_t) restricted to the input features `cols`."""
+    dv = apply_blockdiag_transposed(dy, R_blocks)
+    return dv @ np.asarray(W0, dtype=np.float64)[:, cols]
+
+
 def cnp_adjoint(Q: np.ndarray, G: np.ndarray, k: int) -> np.ndarray:
     """Gradient with respect to Q of <G, R_k(Q)>, R_k = sum_i c_i Q^i.
     Written as the direct double sum of the derivative of each power:

@@ -1,0 +1,948 @@
+// C ABI of the POET-X layer (declared in include/poetx.h): argument checks,
+// workspace carving, and the order of kernels for the block build, the
+// forward and the backward pass.
+//
+// Dataflow (token-major rows; per token y_t = R (W0 (P x_t))):
+//   build   : theta -> Q (unpack) -> E_{k+1} = Q, E_i = 2Q + Q E_{i+1}
+//             -> block = I + E_1 = (I+Q)(I+Q+...+Q^k)
+//   forward : u = x P^T (block-diagonal), v = u W0^T, y = v R^T
+//   backward: dv = dy R, G_R = sum_t dy_t v_t^T, du = dv W0,
+//             dx = du P, G_P = sum_t du_t x_t^T, then for each side the
+//             reverse-mode sweep of the E recursion and the skew pack.
+// bf16 mode runs every contraction on the tcgen05 engine; narrow blocks
+// (b < 256) are placed on the diagonal of 256-wide zero-padded superblocks
+// so the token-wise contractions always see 256 x 256 operands.  fp32 mode
+// runs every contraction on the FFMA engine.
+#include <atomic>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "internal.h"
+#include "poetx.h"
+
+namespace poetx {
+
+// ------------------------------------------------------------ bookkeeping
+
+__device__ int g_status_word;
+
+int* device_status_ptr() {
+  static int* ptrs[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return nullptr;
+  if (ptrs[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) == cudaSuccess) ptrs[dev] = static_cast<int*>(p);
+  }
+  return ptrs[dev];
+}
+
+int read_and_clear_device_status() {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status_word, sizeof(int)) != cudaSuccess) return -1;
+  const int zero = 0;
+  cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int));
+  return v;
+}
+
+int sm_count() {
+  static int counts[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 1;
+  if (counts[dev] == 0) {
+    int c = 0;
+    cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev);
+    counts[dev] = c > 0 ? c : 1;
+  }
+  return counts[dev];
+}
+
+namespace {
+
+struct ProfRecord {
+  const char* tag;
+  cudaEvent_t start, stop;
+  bool closed;
+};
+
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<cudaEvent_t> g_prof_pool;
+std::vector<ProfRecord> g_prof_recs;
+size_t g_prof_used = 0;
+std::atomic<long long> g_launches{0};
+
+}  // namespace
+
+void prof_begin(const char* tag, cudaStream_t s) {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  if (!g_prof_on || g_prof_used + 2 > g_prof_pool.size()) return;
+  ProfRecord r{tag, g_prof_pool[g_prof_used], g_prof_pool[g_prof_used + 1], false};
+  g_prof_used += 2;
+  cudaEventRecord(r.start, s);
+  g_prof_recs.push_back(r);
+}
+
+void prof_end(const char* tag, cudaStream_t s) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  if (g_prof_recs.empty()) return;
+  ProfRecord& r = g_prof_recs.back();
+  if (r.closed || std::strcmp(r.tag, tag) != 0) return;
+  cudaEventRecord(r.stop, s);
+  r.closed = true;
+}
+
+namespace {
+
+using bf16 = __nv_bfloat16;
+
+// ---------------------------------------------------------------- helpers
+
+struct Carver {
+  char* base;
+  size_t off = 0;
+  explicit Carver(void* b) : base(static_cast<char*>(b)) {}
+  template <class T>
+  T* take(size_t count) {
+    off = (off + 255) & ~static_cast<size_t>(255);
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += count * sizeof(T);
+    return p;
+  }
+};
+
+#define CK(expr)                                    \
+  do {                                              \
+    cudaError_t e_ = (expr);                        \
+    if (e_ != cudaSuccess) return e_;               \
+  } while (0)
+
+constexpr long long kMaxTokens = 1ll << 22;
+constexpr int kTargetCtas = 152;  // split-K sizing; fixed so results do not depend on the device
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+poetx_status check_dims(int d, int b, bool is_bf16) {
+  if (b < 2 || b > 512 || d <= 0 || d % b != 0) return POETX_ERR_INVALID_ARG;
+  if (is_bf16) {
+    if (b != 32 && b != 64 && b != 128 && b != 256 && b != 512) return POETX_ERR_UNSUPPORTED;
+    const int S = b > 256 ? b : 256;
+    if (d % S != 0) return POETX_ERR_UNSUPPORTED;
+  }
+  return POETX_OK;
+}
+
+poetx_status check_common(int b, int k, long long tokens, poetx_dtype dtype) {
+  if (dtype != POETX_F32 && dtype != POETX_BF16) return POETX_ERR_INVALID_ARG;
+  if (k < 0 || k > 16) return POETX_ERR_INVALID_ARG;
+  if (tokens < 0 || tokens > kMaxTokens) return POETX_ERR_INVALID_ARG;
+  (void)b;
+  return POETX_OK;
+}
+
+poetx_status to_status(cudaError_t e) { return e == cudaSuccess ? POETX_OK : POETX_ERR_CUDA; }
+
+int superblock(int b) { return b > 256 ? b : 256; }
+bool tc_small(bool is_bf16, int b) { return is_bf16 && b >= 128; }
+
+TcOperand op(const void* ptr, long long rows, long long cols, long long pitch, bool mn_major,
+             int mn_per_g, int k_per_g) {
+  TcOperand o;
+  o.ptr = ptr;
+  o.rows = rows;
+  o.cols = cols;
+  o.pitch = pitch;
+  o.mn_major = mn_major;
+  o.mn_per_g = mn_per_g;
+  o.k_per_g = k_per_g;
+  return o;
+}
+
+int outer_splits(int d, int S, long long T) {
+  const int tiles = (d / S) * (S / 128) * (S / 256);
+  int splits = kTargetCtas / (tiles > 0 ? tiles : 1);
+  const long long ksteps = (T + 63) / 64;
+  long long cap = ksteps / 4;
+  if (cap < 1) cap = 1;
+  if (splits > cap) splits = static_cast<int>(cap);
+  if (splits < 1) splits = 1;
+  return tc_effective_splits(static_cast<int>(T), splits);
+}
+
+// ------------------------------------------------- token-wise contractions
+
+// out[:, sb g] = in[:, sb g] * SB_g^T (or * SB_g when transposed), bf16.
+cudaError_t tc_transform(const bf16* in, const bf16* sb, bf16* out, int d, int S, long long T,
+                         bool transposed, const char* tag, cudaStream_t s) {
+  TcGemm g;
+  g.M = static_cast<int>(T);
+  g.N = S;
+  g.K = S;
+  g.batches = d / S;
+  g.BN = 256;
+  g.A = op(in, T, d, d, false, 0, S);
+  g.B = transposed ? op(sb, d, S, S, true, 0, S) : op(sb, d, S, S, false, S, 0);
+  g.epi.out_bf16 = out;
+  g.epi.ld = d;
+  g.epi.g_off = S;
+  g.epi.row_limit = static_cast<int>(T);
+  g.tag = tag;
+  return tc_gemm_run(g, s);
+}
+
+// part[s][g][m][n] = sum over tokens of split s of A[t][g*S+m] * B[t][g*S+n].
+cudaError_t tc_outer(const bf16* A, const bf16* B, float* part, int d, int S, long long T,
+                     int splits, cudaStream_t s) {
+  TcGemm g;
+  g.M = S;
+  g.N = S;
+  g.K = static_cast<int>(T);
+  g.batches = d / S;
+  g.splits = splits;
+  g.BN = 256;
+  g.A = op(A, T, d, d, true, S, 0);
+  g.B = op(B, T, d, d, true, S, 0);
+  g.epi.out_f32 = part;
+  g.epi.ld = S;
+  g.epi.g_off = static_cast<long long>(S) * S;
+  g.epi.s_off = static_cast<long long>(d / S) * S * S;
+  g.tag = "outer";
+  return tc_gemm_run(g, s);
+}
+
+// v = u W0^T (fwd) or du = dv W0 (dgrad), bf16.
+cudaError_t tc_w0(const bf16* A, const bf16* W0, bf16* out, int d_in, int d_out, long long T,
+                  bool dgrad, cudaStream_t s) {
+  TcGemm g;
+  g.M = static_cast<int>(T);
+  g.BN = 256;
+  if (!dgrad) {
+    g.N = d_out;
+    g.K = d_in;
+    g.A = op(A, T, d_in, d_in, false, 0, 0);
+    g.B = op(W0, d_out, d_in, d_in, false, 0, 0);
+    g.epi.ld = d_out;
+    g.tag = "gemm_w0";
+  } else {
+    g.N = d_in;
+    g.K = d_out;
+    g.A = op(A, T, d_out, d_out, false, 0, 0);
+    g.B = op(W0, d_out, d_in, d_in, true, 0, 0);
+    g.epi.ld = d_in;
+    g.tag = "gemm_w0_dgrad";
+  }
+  g.epi.out_bf16 = out;
+  g.epi.row_limit = static_cast<int>(T);
+  return tc_gemm_run(g, s);
+}
+
+// fp32 block-diagonal transform: out[:, g] = in[:, g] B_g^T (or B_g).
+cudaError_t simt_transform(const float* in, const float* blocks, float* out, int d, int b,
+                           long long T, bool transposed, const char* tag, cudaStream_t s) {
+  SimtGemm g;
+  g.M = static_cast<int>(T);
+  g.N = b;
+  g.K = b;
+  g.batches = d / b;
+  g.A = in;
+  g.a_g = b;
+  g.a_m = d;
+  g.a_k = 1;
+  g.B = blocks;
+  g.b_g = static_cast<long long>(b) * b;
+  if (!transposed) {  // B(kk=j, n=i) = B_g[i][j]
+    g.b_k = 1;
+    g.b_n = b;
+  } else {  // B(kk=j, n=i) = B_g[j][i]
+    g.b_k = b;
+    g.b_n = 1;
+  }
+  g.epi.out_f32 = out;
+  g.epi.ld = d;
+  g.epi.g_off = b;
+  g.tag = tag;
+  return simt_gemm_run(g, s);
+}
+
+// fp32 G[g][i][j] = sum_t A[t][g*b+i] B[t][g*b+j].
+cudaError_t simt_outer(const float* A, const float* B, float* G, int d, int b, long long T,
+                       cudaStream_t s) {
+  SimtGemm g;
+  g.M = b;
+  g.N = b;
+  g.K = static_cast<int>(T);
+  g.batches = d / b;
+  g.A = A;
+  g.a_g = b;
+  g.a_m = 1;
+  g.a_k = d;
+  g.B = B;
+  g.b_g = b;
+  g.b_k = d;
+  g.b_n = 1;
+  g.epi.out_f32 = G;
+  g.epi.ld = b;
+  g.epi.g_off = static_cast<long long>(b) * b;
+  g.tag = "outer";
+  return simt_gemm_run(g, s);
+}
+
+cudaError_t simt_w0(const float* A, const float* W0, float* out, int d_in, int d_out,
+                    long long T, bool dgrad, cudaStream_t s) {
+  SimtGemm g;
+  g.M = static_cast<int>(T);
+  g.batches = 1;
+  g.A = A;
+  g.a_k = 1;
+  g.B = W0;
+  if (!dgrad) {  // v[t][o] = sum_i u[t][i] W0[o][i]
+    g.N = d_out;
+    g.K = d_in;
+    g.a_m = d_in;
+    g.b_k = 1;
+    g.b_n = d_in;
+    g.epi.ld = d_out;
+    g.tag = "gemm_w0";
+  } else {  // du[t][i] = sum_o dv[t][o] W0[o][i]
+    g.N = d_in;
+    g.K = d_out;
+    g.a_m = d_out;
+    g.b_k = d_in;
+    g.b_n = 1;
+    g.epi.ld = d_in;
+    g.tag = "gemm_w0_dgrad";
+  }
+  g.epi.out_f32 = out;
+  return simt_gemm_run(g, s);
+}
+
+// ------------------------------------------------------- b x b products
+
+// out = epi(L * Rm) over n blocks, where L = Q (or Q^T) and Rm = one of the
+// E / G matrices, chosen by `kind`:
+//   kind 0: Q * M          (builder recursion E_i = 2Q + Q E_{i+1})
+//   kind 1: M * N^T        (adjoint: G_i E_{i+1}^T)
+//   kind 2: Q^T * M        (adjoint: G_{i+1} = Q^T G_i)
+// tc: operands bf16 (q16 / m16 / n16); otherwise fp32 (q32 / m32 / n32).
+cudaError_t small_product(int kind, bool tc, int n, int b, const float* q32, const bf16* q16,
+                          const float* m32, const bf16* m16, const float* n32, const bf16* n16,
+                          const EpiArgs& epi, const char* tag, cudaStream_t s) {
+  const long long bb = static_cast<long long>(b) * b;
+  const long long rows = static_cast<long long>(n) * b;
+  if (tc) {
+    TcGemm g;
+    g.M = b;
+    g.N = b;
+    g.K = b;
+    g.batches = n;
+    g.BN = b < 256 ? b : 256;
+    if (kind == 0) {
+      g.A = op(q16, rows, b, b, false, b, 0);  // A[m][kk] = Q[m][kk]
+      g.B = op(m16, rows, b, b, true, 0, b);   // B[nn][kk] = M[kk][nn]
+    } else if (kind == 1) {
+      g.A = op(m16, rows, b, b, false, b, 0);  // A[m][kk] = M[m][kk]
+      g.B = op(n16, rows, b, b, false, b, 0);  // B[nn][kk] = N[nn][kk]
+    } else {
+      g.A = op(q16, rows, b, b, true, 0, b);   // A[m][kk] = Q[kk][m]
+      g.B = op(m16, rows, b, b, true, 0, b);   // B[nn][kk] = M[kk][nn]
+    }
+    g.epi = epi;
+    g.tag = tag;
+    return tc_gemm_run(g, s);
+  }
+  SimtGemm g;
+  g.M = b;
+  g.N = b;
+  g.K = b;
+  g.batches = n;
+  g.a_g = bb;
+  g.b_g = bb;
+  if (kind == 0) {
+    g.A = q32;
+    g.a_m = b;
+    g.a_k = 1;
+    g.B = m32;
+    g.b_k = b;
+    g.b_n = 1;
+  } else if (kind == 1) {
+    g.A = m32;
+    g.a_m = b;
+    g.a_k = 1;
+    g.B = n32;
+    g.b_k = 1;
+    g.b_n = b;
+  } else {
+    g.A = q32;
+    g.a_m = 1;
+    g.a_k = b;
+    g.B = m32;
+    g.b_k = b;
+    g.b_n = 1;
+  }
+  g.epi = epi;
+  g.tag = tag;
+  return simt_gemm_run(g, s);
+}
+
+EpiArgs block_epi(int b) {
+  EpiArgs e;
+  e.ld = b;
+  e.g_off = static_cast<long long>(b) * b;
+  return e;
+}
+
+// --------------------------------------------------------------- builder
+
+struct BuildBufs {
+  float* q32 = nullptr;
+  bf16* q16 = nullptr;
+  float* e32[2] = {nullptr, nullptr};
+  bf16* e16[2] = {nullptr, nullptr};
+};
+
+BuildBufs carve_build(Carver& c, int n, int b, bool tc) {
+  BuildBufs w;
+  const size_t nbb = static_cast<size_t>(n) * b * b;
+  w.q32 = c.take<float>(nbb);
+  if (tc) {
+    w.q16 = c.take<bf16>(nbb);
+    w.e16[0] = c.take<bf16>(nbb);
+    w.e16[1] = c.take<bf16>(nbb);
+  } else {
+    w.e32[0] = c.take<float>(nbb);
+    w.e32[1] = c.take<float>(nbb);
+  }
+  return w;
+}
+
+cudaError_t run_build(const float* theta, int n, int b, int k, bool is_bf16, void* blocks,
+                      const BuildBufs& w, cudaStream_t s) {
+  const bool tc = tc_small(is_bf16, b);
+  CK(launch_unpack(theta, n, b, w.q32, tc ? w.q16 : nullptr, s));
+  float* out32 = is_bf16 ? nullptr : static_cast<float*>(blocks);
+  bf16* out16 = is_bf16 ? static_cast<bf16*>(blocks) : nullptr;
+  if (k == 0) return launch_identity_plus(w.q32, n, b, out32, out16, s);
+  int cur = -1;  // -1: E_{k+1} = Q itself
+  for (int i = k; i >= 1; --i) {
+    const int nxt = cur == 0 ? 1 : 0;
+    EpiArgs e = block_epi(b);
+    e.X = w.q32;  // + 2 Q
+    e.beta = 2.f;
+    if (i == 1) {
+      e.delta = 1.f;  // + I
+      e.out_f32 = out32;
+      e.out_bf16 = out16;
+    } else if (tc) {
+      e.out_bf16 = w.e16[nxt];
+    } else {
+      e.out_f32 = w.e32[nxt];
+    }
+    const float* m32 = cur < 0 ? w.q32 : w.e32[cur];
+    const bf16* m16 = cur < 0 ? w.q16 : w.e16[cur];
+    CK(small_product(0, tc, n, b, w.q32, w.q16, m32, m16, nullptr, nullptr, e, "build", s));
+    cur = nxt;
+  }
+  return cudaSuccess;
+}
+
+// -------------------------------------------------- adjoint of the build
+
+struct CnpBufs {
+  float* q32 = nullptr;
+  bf16* q16 = nullptr;
+  float* e32[18] = {};
+  bf16* e16[18] = {};
+  float* g32[2] = {nullptr, nullptr};
+  bf16* g16[2] = {nullptr, nullptr};
+  float* dq = nullptr;
+};
+
+CnpBufs carve_cnp(Carver& c, int n, int b, int k, bool tc) {
+  CnpBufs w;
+  const size_t nbb = static_cast<size_t>(n) * b * b;
+  w.q32 = c.take<float>(nbb);
+  if (tc) w.q16 = c.take<bf16>(nbb);
+  for (int i = 2; i <= k; ++i) {
+    if (tc)
+      w.e16[i] = c.take<bf16>(nbb);
+    else
+      w.e32[i] = c.take<float>(nbb);
+  }
+  for (int j = 0; j < 2; ++j) {
+    w.g32[j] = c.take<float>(nbb);
+    if (tc) w.g16[j] = c.take<bf16>(nbb);
+  }
+  w.dq = c.take<float>(nbb);
+  return w;
+}
+
+// Input: the block gradient G in w.g32[0] (and w.g16[0] for tc).
+// Reverse sweep of E_{k+1} = Q, E_i = c_i Q + Q E_{i+1} (c_i = 2), R = I + E_1:
+//   Gbar_1 = G;  for i = 1..k:  dQ += 2 Gbar_i + Gbar_i E_{i+1}^T,
+//                               Gbar_{i+1} = Q^T Gbar_i;
+//   dQ += Gbar_{k+1};  dtheta = pack(dQ - dQ^T).
+cudaError_t run_cnp_backward(const float* theta, int n, int b, int k, bool is_bf16,
+                             const CnpBufs& w, float* dtheta, cudaStream_t s) {
+  const bool tc = tc_small(is_bf16, b);
+  if (k == 0) return launch_pack_skew(w.g32[0], nullptr, n, b, dtheta, s);
+  CK(launch_unpack(theta, n, b, w.q32, tc ? w.q16 : nullptr, s));
+  // E_i for i = k .. 2 (E_{k+1} = Q)
+  for (int i = k; i >= 2; --i) {
+    EpiArgs e = block_epi(b);
+    e.X = w.q32;
+    e.beta = 2.f;
+    if (tc)
+      e.out_bf16 = w.e16[i];
+    else
+      e.out_f32 = w.e32[i];
+    const float* m32 = (i + 1 == k + 1) ? w.q32 : w.e32[i + 1];
+    const bf16* m16 = (i + 1 == k + 1) ? w.q16 : w.e16[i + 1];
+    CK(small_product(0, tc, n, b, w.q32, w.q16, m32, m16, nullptr, nullptr, e, "cnp_bwd", s));
+  }
+  int cur = 0;
+  for (int i = 1; i <= k; ++i) {
+    const float* e32 = (i + 1 == k + 1) ? w.q32 : w.e32[i + 1];
+    const bf16* e16 = (i + 1 == k + 1) ? w.q16 : w.e16[i + 1];
+    EpiArgs e1 = block_epi(b);
+    if (i > 1) {
+      e1.X = w.dq;
+      e1.beta = 1.f;
+    }
+    e1.Y = w.g32[cur];
+    e1.gamma = 2.f;
+    e1.out_f32 = w.dq;
+    CK(small_product(1, tc, n, b, nullptr, nullptr, w.g32[cur], w.g16[cur], e32, e16, e1,
+                     "cnp_bwd", s));
+    EpiArgs e2 = block_epi(b);
+    e2.out_f32 = w.g32[1 - cur];
+    if (tc) e2.out_bf16 = w.g16[1 - cur];
+    CK(small_product(2, tc, n, b, w.q32, w.q16, w.g32[cur], w.g16[cur], nullptr, nullptr, e2,
+                     "cnp_bwd", s));
+    cur = 1 - cur;
+  }
+  return launch_pack_skew(w.dq, w.g32[cur], n, b, dtheta, s);
+}
+
+// -------------------------------------------------------- layer buffers
+
+struct SideBufs {  // token-wise scratch for one call
+  void* u = nullptr;
+  void* v = nullptr;
+  void* dv = nullptr;
+  void* du = nullptr;
+  bf16* psb = nullptr;
+  bf16* rsb = nullptr;
+  float* part = nullptr;
+};
+
+size_t elem_size(bool is_bf16) { return is_bf16 ? 2 : 4; }
+
+void* take_act(Carver& c, long long T, int d, bool is_bf16) {
+  return c.take<char>(static_cast<size_t>(T) * d * elem_size(is_bf16));
+}
+
+struct FwdPlan {
+  SideBufs sb;
+};
+
+FwdPlan carve_forward(Carver& c, int d_in, int d_out, int b, long long T, bool is_bf16,
+                      bool need_v) {
+  FwdPlan p;
+  p.sb.u = take_act(c, T, d_in, is_bf16);
+  if (need_v) p.sb.v = take_act(c, T, d_out, is_bf16);
+  if (is_bf16 && b < 256) {
+    p.sb.psb = c.take<bf16>(static_cast<size_t>(d_in) * 256);
+    p.sb.rsb = c.take<bf16>(static_cast<size_t>(d_out) * 256);
+  }
+  return p;
+}
+
+cudaError_t run_forward_uv(const void* x, const void* W0, const void* psb, void* u, void* v,
+                           int d_in, int d_out, int b, long long T, bool is_bf16,
+                           cudaStream_t s) {
+  if (is_bf16) {
+    const int S = superblock(b);
+    CK(tc_transform(static_cast<const bf16*>(x), static_cast<const bf16*>(psb),
+                    static_cast<bf16*>(u), d_in, S, T, false, "transform", s));
+    return tc_w0(static_cast<const bf16*>(u), static_cast<const bf16*>(W0), static_cast<bf16*>(v),
+                 d_in, d_out, T, false, s);
+  }
+  CK(simt_transform(static_cast<const float*>(x), static_cast<const float*>(psb),
+                    static_cast<float*>(u), d_in, b, T, false, "transform", s));
+  return simt_w0(static_cast<const float*>(u), static_cast<const float*>(W0),
+                 static_cast<float*>(v), d_in, d_out, T, false, s);
+}
+
+struct BwdPlan {
+  SideBufs sb;
+  CnpBufs cnp;
+  int splits_in = 1, splits_out = 1;
+};
+
+BwdPlan carve_backward(Carver& c, int d_in, int d_out, int b, int k, long long T, bool is_bf16,
+                       bool recompute_v) {
+  BwdPlan p;
+  if (recompute_v) {
+    p.sb.u = take_act(c, T, d_in, is_bf16);
+    p.sb.v = take_act(c, T, d_out, is_bf16);
+  }
+  p.sb.dv = take_act(c, T, d_out, is_bf16);
+  p.sb.du = take_act(c, T, d_in, is_bf16);
+  if (is_bf16) {
+    const int S = superblock(b);
+    if (b < 256) {
+      p.sb.psb = c.take<bf16>(static_cast<size_t>(d_in) * 256);
+      p.sb.rsb = c.take<bf16>(static_cast<size_t>(d_out) * 256);
+    }
+    p.splits_in = outer_splits(d_in, S, T);
+    p.splits_out = outer_splits(d_out, S, T);
+    const long long part_in = static_cast<long long>(p.splits_in) * d_in * S;
+    const long long part_out = static_cast<long long>(p.splits_out) * d_out * S;
+    p.sb.part = c.take<float>(static_cast<size_t>(part_in > part_out ? part_in : part_out));
+  }
+  const int n_max = (d_in > d_out ? d_in : d_out) / b;
+  p.cnp = carve_cnp(c, n_max, b, k, tc_small(is_bf16, b));
+  return p;
+}
+
+// Block gradient of one side into cnp.g32[0] (+ g16[0]), then its packed
+// adjoint into dtheta.
+cudaError_t side_gradient(const void* dout, const void* in, int d, int b, int k, long long T,
+                          bool is_bf16, const float* theta, float* part, int splits,
+                          const CnpBufs& cnp, float* dtheta, cudaStream_t s) {
+  const int n = d / b;
+  if (is_bf16) {
+    const int S = superblock(b);
+    CK(tc_outer(static_cast<const bf16*>(dout), static_cast<const bf16*>(in), part, d, S, T,
+                splits, s));
+    CK(launch_reduce_extract(part, splits, n, b, S, cnp.g32[0],
+                             tc_small(true, b) ? cnp.g16[0] : nullptr, s));
+  } else {
+    CK(simt_outer(static_cast<const float*>(dout), static_cast<const float*>(in), cnp.g32[0], d,
+                  b, T, s));
+  }
+  return run_cnp_backward(theta, n, b, k, is_bf16, cnp, dtheta, s);
+}
+
+const void* superblocks_or_blocks(const void* blocks, bf16* sb, int d, int b, bool is_bf16,
+                                  cudaStream_t s, cudaError_t* err) {
+  *err = cudaSuccess;
+  if (!is_bf16 || b >= 256) return blocks;
+  *err = launch_expand_superblocks(static_cast<const bf16*>(blocks), d / b, b, 256, sb, s);
+  return sb;
+}
+
+}  // namespace
+}  // namespace poetx
+
+using namespace poetx;
+
+// ====================================================================== ABI
+
+extern "C" {
+
+const char* poetx_status_string(poetx_status s) {
+  switch (s) {
+    case POETX_OK: return "POETX_OK";
+    case POETX_ERR_INVALID_ARG: return "POETX_ERR_INVALID_ARG: invalid argument";
+    case POETX_ERR_UNSUPPORTED: return "POETX_ERR_UNSUPPORTED: shape not supported";
+    case POETX_ERR_WORKSPACE: return "POETX_ERR_WORKSPACE: workspace too small";
+    case POETX_ERR_CUDA: return "POETX_ERR_CUDA: CUDA launch or device error";
+    case POETX_ERR_TIMEOUT: return "POETX_ERR_TIMEOUT: a kernel gave up on an internal wait";
+  }
+  return "unknown poetx_status";
+}
+
+size_t poetx_packed_size(int d, int b) {
+  if (b < 1 || d <= 0 || d % b != 0) return 0;
+  return static_cast<size_t>(d / b) * (static_cast<size_t>(b) * (b - 1) / 2);
+}
+
+size_t poetx_build_workspace_size(int d, int b, int k, poetx_dtype dtype) {
+  const bool is_bf16 = dtype == POETX_BF16;
+  if (check_dims(d, b, is_bf16) != POETX_OK || check_common(b, k, 0, dtype) != POETX_OK) return 0;
+  Carver c(nullptr);
+  carve_build(c, d / b, b, tc_small(is_bf16, b));
+  return c.off;
+}
+
+poetx_status poetx_build_blocks(const float* theta, int d, int b, int k, poetx_dtype dtype,
+                                void* blocks, void* workspace, size_t workspace_bytes,
+                                poetx_stream stream) {
+  const bool is_bf16 = dtype == POETX_BF16;
+  poetx_status st = check_common(b, k, 0, dtype);
+  if (st != POETX_OK) return st;
+  if ((st = check_dims(d, b, is_bf16)) != POETX_OK) return st;
+  if (theta == nullptr || blocks == nullptr || !aligned16(theta) || !aligned16(blocks))
+    return POETX_ERR_INVALID_ARG;
+  Carver c(workspace);
+  BuildBufs w = carve_build(c, d / b, b, tc_small(is_bf16, b));
+  if (workspace == nullptr || c.off > workspace_bytes || !aligned16(workspace))
+    return POETX_ERR_WORKSPACE;
+  return to_status(
+      run_build(theta, d / b, b, k, is_bf16, blocks, w, static_cast<cudaStream_t>(stream)));
+}
+
+size_t poetx_forward_workspace_size(int d_in, int d_out, int b, int64_t tokens,
+                                    poetx_dtype dtype) {
+  const bool is_bf16 = dtype == POETX_BF16;
+  if (check_dims(d_in, b, is_bf16) != POETX_OK || check_dims(d_out, b, is_bf16) != POETX_OK ||
+      check_common(b, 0, tokens, dtype) != POETX_OK)
+    return 0;
+  Carver c(nullptr);
+  carve_forward(c, d_in, d_out, b, tokens, is_bf16, true);
+  return c.off;
+}
+
+poetx_status poetx_forward(const void* x, const void* W0, const void* P_blocks,
+                           const void* R_blocks, void* y, void* v_saved, int d_in, int d_out,
+                           int b, int64_t tokens, poetx_dtype dtype, void* workspace,
+                           size_t workspace_bytes, poetx_stream stream) {
+  const bool is_bf16 = dtype == POETX_BF16;
+  poetx_status st = check_common(b, 0, tokens, dtype);
+  if (st != POETX_OK) return st;
+  if ((st = check_dims(d_in, b, is_bf16)) != POETX_OK) return st;
+  if ((st = check_dims(d_out, b, is_bf16)) != POETX_OK) return st;
+  if (tokens == 0) return POETX_OK;  // nothing to compute; pointers may be empty
+  if (x == nullptr || W0 == nullptr || P_blocks == nullptr || R_blocks == nullptr ||
+      y == nullptr)
+    return POETX_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(W0) || !aligned16(P_blocks) || !aligned16(R_blocks) ||
+      !aligned16(y) || !aligned16(v_saved))
+    return POETX_ERR_INVALID_ARG;
+  Carver c(workspace);
+  FwdPlan p = carve_forward(c, d_in, d_out, b, tokens, is_bf16, v_saved == nullptr);
+  if (workspace == nullptr || c.off > workspace_bytes || !aligned16(workspace))
+    return POETX_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  const void* psb = superblocks_or_blocks(P_blocks, p.sb.psb, d_in, b, is_bf16, s, &e);
+  if (e != cudaSuccess) return POETX_ERR_CUDA;
+  const void* rsb = superblocks_or_blocks(R_blocks, p.sb.rsb, d_out, b, is_bf16, s, &e);
+  if (e != cudaSuccess) return POETX_ERR_CUDA;
+  void* v = v_saved != nullptr ? v_saved : p.sb.v;
+  e = run_forward_uv(x, W0, psb, p.sb.u, v, d_in, d_out, b, tokens, is_bf16, s);
+  if (e != cudaSuccess) return POETX_ERR_CUDA;
+  if (is_bf16)
+    e = tc_transform(static_cast<const bf16*>(v), static_cast<const bf16*>(rsb),
+                     static_cast<bf16*>(y), d_out, superblock(b), tokens, false, "transform", s);
+  else
+    e = simt_transform(static_cast<const float*>(v), static_cast<const float*>(rsb),
+                       static_cast<float*>(y), d_out, b, tokens, false, "transform", s);
+  return to_status(e);
+}
+
+size_t poetx_backward_workspace_size(int d_in, int d_out, int b, int k, int64_t tokens,
+                                     poetx_dtype dtype, int recompute_v) {
+  const bool is_bf16 = dtype == POETX_BF16;
+  if (check_dims(d_in, b, is_bf16) != POETX_OK || check_dims(d_out, b, is_bf16) != POETX_OK ||
+      check_common(b, k, tokens, dtype) != POETX_OK)
+    return 0;
+  Carver c(nullptr);
+  carve_backward(c, d_in, d_out, b, k, tokens, is_bf16, recompute_v != 0);
+  return c.off;
+}
+
+poetx_status poetx_backward(const void* dy, const void* x, const void* W0, const float* theta_P,
+                            const float* theta_R, const void* P_blocks, const void* R_blocks,
+                            const void* v_saved, void* dx, float* dtheta_P, float* dtheta_R,
+                            int d_in, int d_out, int b, int k, int64_t tokens, poetx_dtype dtype,
+                            void* workspace, size_t workspace_bytes, poetx_stream stream) {
+  const bool is_bf16 = dtype == POETX_BF16;
+  poetx_status st = check_common(b, k, tokens, dtype);
+  if (st != POETX_OK) return st;
+  if ((st = check_dims(d_in, b, is_bf16)) != POETX_OK) return st;
+  if ((st = check_dims(d_out, b, is_bf16)) != POETX_OK) return st;
+  if (dtheta_P == nullptr || dtheta_R == nullptr || !aligned16(dtheta_P) || !aligned16(dtheta_R))
+    return POETX_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (tokens == 0) {  // empty sums: zero gradients; activation pointers may be empty
+    if (cudaMemsetAsync(dtheta_P, 0, poetx_packed_size(d_in, b) * sizeof(float), s) !=
+            cudaSuccess ||
+        cudaMemsetAsync(dtheta_R, 0, poetx_packed_size(d_out, b) * sizeof(float), s) !=
+            cudaSuccess)
+      return POETX_ERR_CUDA;
+    return POETX_OK;
+  }
+  const void* ptrs[] = {dy, x, W0, theta_P, theta_R, P_blocks, R_blocks, dx};
+  for (const void* q : ptrs)
+    if (q == nullptr || !aligned16(q)) return POETX_ERR_INVALID_ARG;
+  if (!aligned16(v_saved)) return POETX_ERR_INVALID_ARG;
+  const bool recompute = v_saved == nullptr;
+  Carver c(workspace);
+  BwdPlan p = carve_backward(c, d_in, d_out, b, k, tokens, is_bf16, recompute);
+  if (workspace == nullptr || c.off > workspace_bytes || !aligned16(workspace))
+    return POETX_ERR_WORKSPACE;
+  cudaError_t e;
+  const void* psb = superblocks_or_blocks(P_blocks, p.sb.psb, d_in, b, is_bf16, s, &e);
+  if (e != cudaSuccess) return POETX_ERR_CUDA;
+  const void* rsb = superblocks_or_blocks(R_blocks, p.sb.rsb, d_out, b, is_bf16, s, &e);
+  if (e != cudaSuccess) return POETX_ERR_CUDA;
+  const void* v = v_saved;
+  if (recompute) {
+    e = run_forward_uv(x, W0, psb, p.sb.u, p.sb.v, d_in, d_out, b, tokens, is_bf16, s);
+    if (e != cudaSuccess) return POETX_ERR_CUDA;
+    v = p.sb.v;
+  }
+  const int S = superblock(b);
+  // R side: dv = dy R, G_R = sum_t dy_t v_t^T
+  if (is_bf16)
+    e = tc_transform(static_cast<const bf16*>(dy), static_cast<const bf16*>(rsb),
+                     static_cast<bf16*>(p.sb.dv), d_out, S, tokens, true, "transform_t", s);
+  else
+    e = simt_transform(static_cast<const float*>(dy), static_cast<const float*>(rsb),
+                       static_cast<float*>(p.sb.dv), d_out, b, tokens, true, "transform_t", s);
+  if (e != cudaSuccess) return POETX_ERR_CUDA;
+  e = side_gradient(dy, v, d_out, b, k, tokens, is_bf16, theta_R, p.sb.part, p.splits_out,
+                    p.cnp, dtheta_R, s);
+  if (e != cudaSuccess) return POETX_ERR_CUDA;
+  // du = dv W0
+  if (is_bf16)
+    e = tc_w0(static_cast<const bf16*>(p.sb.dv), static_cast<const bf16*>(W0),
+              static_cast<bf16*>(p.sb.du), d_in, d_out, tokens, true, s);
+  else
+    e = simt_w0(static_cast<const float*>(p.sb.dv), static_cast<const float*>(W0),
+                static_cast<float*>(p.sb.du), d_in, d_out, tokens, true, s);
+  if (e != cudaSuccess) return POETX_ERR_CUDA;
+  // P side: dx = du P, G_P = sum_t du_t x_t^T
+  if (is_bf16)
+    e = tc_transform(static_cast<const bf16*>(p.sb.du), static_cast<const bf16*>(psb),
+                     static_cast<bf16*>(dx), d_in, S, tokens, true, "transform_t", s);
+  else
+    e = simt_transform(static_cast<const float*>(p.sb.du), static_cast<const float*>(psb),
+                       static_cast<float*>(dx), d_in, b, tokens, true, "transform_t", s);
+  if (e != cudaSuccess) return POETX_ERR_CUDA;
+  e = side_gradient(p.sb.du, x, d_in, b, k, tokens, is_bf16, theta_P, p.sb.part, p.splits_in,
+                    p.cnp, dtheta_P, s);
+  return to_status(e);
+}
+
+size_t poetx_transform_workspace_size(int d, int b, int k, int64_t tokens, poetx_dtype dtype) {
+  const bool is_bf16 = dtype == POETX_BF16;
+  if (check_dims(d, b, is_bf16) != POETX_OK || check_common(b, k, tokens, dtype) != POETX_OK)
+    return 0;
+  Carver c(nullptr);
+  if (is_bf16 && b < 256) c.take<bf16>(static_cast<size_t>(d) * 256);
+  if (is_bf16) {
+    const int S = superblock(b);
+    c.take<float>(static_cast<size_t>(outer_splits(d, S, tokens)) * d * S);
+  }
+  carve_cnp(c, d / b, b, k, tc_small(is_bf16, b));
+  return c.off;
+}
+
+poetx_status poetx_transform_forward(const void* x, const void* blocks, void* out, int d, int b,
+                                     int64_t tokens, poetx_dtype dtype, void* workspace,
+                                     size_t workspace_bytes, poetx_stream stream) {
+  const bool is_bf16 = dtype == POETX_BF16;
+  poetx_status st = check_common(b, 0, tokens, dtype);
+  if (st != POETX_OK) return st;
+  if ((st = check_dims(d, b, is_bf16)) != POETX_OK) return st;
+  if (tokens == 0) return POETX_OK;
+  if (x == nullptr || blocks == nullptr || out == nullptr || !aligned16(x) ||
+      !aligned16(blocks) || !aligned16(out))
+    return POETX_ERR_INVALID_ARG;
+  Carver c(workspace);
+  bf16* sbuf = (is_bf16 && b < 256) ? c.take<bf16>(static_cast<size_t>(d) * 256) : nullptr;
+  if (c.off > 0 && (workspace == nullptr || c.off > workspace_bytes || !aligned16(workspace)))
+    return POETX_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  const void* sb = superblocks_or_blocks(blocks, sbuf, d, b, is_bf16, s, &e);
+  if (e != cudaSuccess) return POETX_ERR_CUDA;
+  if (is_bf16)
+    e = tc_transform(static_cast<const bf16*>(x), static_cast<const bf16*>(sb),
+                     static_cast<bf16*>(out), d, superblock(b), tokens, false, "transform", s);
+  else
+    e = simt_transform(static_cast<const float*>(x), static_cast<const float*>(sb),
+                       static_cast<float*>(out), d, b, tokens, false, "transform", s);
+  return to_status(e);
+}
+
+poetx_status poetx_transform_backward(const void* dout, const void* x, const float* theta,
+                                      const void* blocks, void* dx, float* dtheta, int d, int b,
+                                      int k, int64_t tokens, poetx_dtype dtype, void* workspace,
+                                      size_t workspace_bytes, poetx_stream stream) {
+  const bool is_bf16 = dtype == POETX_BF16;
+  poetx_status st = check_common(b, k, tokens, dtype);
+  if (st != POETX_OK) return st;
+  if ((st = check_dims(d, b, is_bf16)) != POETX_OK) return st;
+  if (dtheta == nullptr || !aligned16(dtheta)) return POETX_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (tokens == 0)
+    return to_status(cudaMemsetAsync(dtheta, 0, poetx_packed_size(d, b) * sizeof(float), s));
+  const void* ptrs[] = {dout, x, theta, blocks, dx};
+  for (const void* q : ptrs)
+    if (q == nullptr || !aligned16(q)) return POETX_ERR_INVALID_ARG;
+  Carver c(workspace);
+  bf16* sbuf = (is_bf16 && b < 256) ? c.take<bf16>(static_cast<size_t>(d) * 256) : nullptr;
+  const int S = superblock(b);
+  const int splits = is_bf16 ? outer_splits(d, S, tokens) : 1;
+  float* part = is_bf16 ? c.take<float>(static_cast<size_t>(splits) * d * S) : nullptr;
+  CnpBufs cnp = carve_cnp(c, d / b, b, k, tc_small(is_bf16, b));
+  if (workspace == nullptr || c.off > workspace_bytes || !aligned16(workspace))
+    return POETX_ERR_WORKSPACE;
+  cudaError_t e;
+  const void* sb = superblocks_or_blocks(blocks, sbuf, d, b, is_bf16, s, &e);
+  if (e != cudaSuccess) return POETX_ERR_CUDA;
+  if (is_bf16)
+    e = tc_transform(static_cast<const bf16*>(dout), static_cast<const bf16*>(sb),
+                     static_cast<bf16*>(dx), d, S, tokens, true, "transform_t", s);
+  else
+    e = simt_transform(static_cast<const float*>(dout), static_cast<const float*>(sb),
+                       static_cast<float*>(dx), d, b, tokens, true, "transform_t", s);
+  if (e != cudaSuccess) return POETX_ERR_CUDA;
+  return to_status(
+      side_gradient(dout, x, d, b, k, tokens, is_bf16, theta, part, splits, cnp, dtheta, s));
+}
+
+poetx_status poetx_device_status(void) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return POETX_ERR_CUDA;
+  const int v = read_and_clear_device_status();
+  if (v < 0) return POETX_ERR_CUDA;
+  return v == 0 ? POETX_OK : static_cast<poetx_status>(v);
+}
+
+long long poetx_launch_count(void) { return g_launches.load(); }
+
+int poetx_profile_start(int capacity) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  g_prof_recs.clear();
+  g_prof_used = 0;
+  while (static_cast<int>(g_prof_pool.size()) < 2 * capacity) {
+    cudaEvent_t ev;
+    if (cudaEventCreate(&ev) != cudaSuccess) return -1;
+    g_prof_pool.push_back(ev);
+  }
+  g_prof_on = true;
+  return 0;
+}
+
+void poetx_profile_stop(void) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  g_prof_on = false;
+}
+
+int poetx_profile_query(const char* tag, int* count, double* total_ms) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  int n = 0;
+  double total = 0.0;
+  for (const ProfRecord& r : g_prof_recs) {
+    if (!r.closed) continue;
+    if (tag != nullptr && std::strcmp(tag, r.tag) != 0) continue;
+    if (cudaEventSynchronize(r.stop) != cudaSuccess) return -1;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess) return -1;
+    total += ms;
+    ++n;
+  }
+  if (count != nullptr) *count = n;
+  if (total_ms != nullptr) *total_ms = total;
+  return 0;
+}
+
+}  // extern "C"

@@ -1,0 +1,105 @@
+// Internal interfaces shared by the library's translation units.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+namespace poetx {
+
+// Where a contraction's result goes: for batch g, K-split s, row r and
+// column c of the (batch-local) result,
+//   v   = alpha * acc + beta * X[off] + gamma * Y[off] + delta * (r == c)
+//   off = g * g_off + s * s_off + r * ld + c
+// and v is stored to out_f32[off] and/or out_bf16[off].  Rows r >=
+// row_limit are skipped.  X, Y, out_f32, out_bf16 may each be null.
+struct EpiArgs {
+  float alpha = 1.f;
+  const float* X = nullptr;
+  float beta = 0.f;
+  const float* Y = nullptr;
+  float gamma = 0.f;
+  float delta = 0.f;
+  float* out_f32 = nullptr;
+  __nv_bfloat16* out_bf16 = nullptr;
+  long long ld = 0;
+  long long g_off = 0;
+  long long s_off = 0;
+  int row_limit = 0x7fffffff;
+};
+
+// ---------------------------------------------------------------- tcgen05
+// C = A * B^T per batch on the tensor cores (bf16 in, fp32 accumulate).
+// Each operand is a window of a 2-D row-major bf16 array:
+//   major K : array rows index M (or N), columns index K
+//   major MN: array rows index K, columns index M (or N)
+// For batch g the window starts at M/N coordinate g*mn_per_g and K
+// coordinate g*k_per_g.  Reads past the array's extent return zeros.
+struct TcOperand {
+  const void* ptr = nullptr;
+  long long rows = 0, cols = 0, pitch = 0;  // pitch in elements
+  bool mn_major = false;
+  int mn_per_g = 0, k_per_g = 0;
+};
+
+struct TcGemm {
+  int M = 0, N = 0, K = 0;  // per batch
+  int batches = 1;
+  int splits = 1;           // K is split; split s writes at s * epi.s_off
+  int BN = 256;             // 128 or 256
+  TcOperand A, B;
+  EpiArgs epi;
+  const char* tag = "tc_gemm";  // name under which launches are profiled
+};
+
+// Number of K splits the engine will actually use for `want` splits.
+int tc_effective_splits(int K, int want);
+cudaError_t tc_gemm_run(const TcGemm& g, cudaStream_t stream);
+
+// ------------------------------------------------------------------- SIMT
+// C = A * B per batch on the CUDA cores, fp32 accumulate, arbitrary strides:
+//   A(g, m, k) = A[g*a_g + m*a_m + k*a_k], B(g, k, n) = B[g*b_g + k*b_k + n*b_n]
+// Inputs are float or bf16 (both operands the same type).
+struct SimtGemm {
+  int M = 0, N = 0, K = 0, batches = 1;
+  bool bf16_inputs = false;
+  const void* A = nullptr;
+  long long a_g = 0, a_m = 0, a_k = 0;
+  const void* B = nullptr;
+  long long b_g = 0, b_k = 0, b_n = 0;
+  EpiArgs epi;
+  const char* tag = "simt_gemm";
+};
+cudaError_t simt_gemm_run(const SimtGemm& g, cudaStream_t stream);
+
+// ------------------------------------------------------------ elementwise
+// theta [n][b(b-1)/2] -> Q [n][b][b] (fp32 and/or bf16 copies).
+cudaError_t launch_unpack(const float* theta, int n, int b, float* q_f32, __nv_bfloat16* q_bf16,
+                          cudaStream_t s);
+// out = Q + I in the requested type (k = 0 blocks).
+cudaError_t launch_identity_plus(const float* q, int n, int b, float* out_f32,
+                                 __nv_bfloat16* out_bf16, cudaStream_t s);
+// blocks [n][b][b] bf16 -> superblocks [n*b/S][S][S] with the b-blocks on
+// the diagonal and zeros elsewhere.
+cudaError_t launch_expand_superblocks(const __nv_bfloat16* blocks, int n, int b, int S,
+                                      __nv_bfloat16* out, cudaStream_t s);
+// G[g] = sum_s part[s][sb][off..][off..] (diagonal b-block g of superblock
+// sb = g*b/S) -> fp32 and/or bf16 [n][b][b].
+cudaError_t launch_reduce_extract(const float* part, int splits, int n, int b, int S,
+                                  float* out_f32, __nv_bfloat16* out_bf16, cudaStream_t s);
+// dtheta[g][idx(i,j)] = M[g][i][j] - M[g][j][i] with M = A (+ B if B != null).
+cudaError_t launch_pack_skew(const float* A, const float* B, int n, int b, float* dtheta,
+                             cudaStream_t s);
+cudaError_t launch_f32_to_bf16(const float* in, long long count, __nv_bfloat16* out,
+                               cudaStream_t s);
+
+// ------------------------------------------------------------ bookkeeping
+int* device_status_ptr();            // per-device status word (device memory)
+int read_and_clear_device_status();  // synchronous
+int sm_count();
+// Every kernel launch is bracketed by these: they count launches and, while
+// profiling is on, record CUDA events on the launch stream under `tag`.
+void prof_begin(const char* tag, cudaStream_t s);
+void prof_end(const char* tag, cudaStream_t s);
+
+}  // namespace poetx

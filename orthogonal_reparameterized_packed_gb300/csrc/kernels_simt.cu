@@ -1,0 +1,254 @@
+// CUDA-core kernels: the fp32 contraction engine (FFMA; used for every
+// contraction in fp32 mode, where tensor-core tf32 would miss the fp32
+// tolerance, and for blocks narrower than one 128-wide MMA tile), plus the
+// small elementwise kernels of the path (unpack, superblock expansion,
+// split-K reduction, skew projection and pack).
+#include "internal.h"
+
+namespace poetx {
+
+namespace {
+
+constexpr int TM = 64, TN = 64, TK = 16, SIMT_THREADS = 256;
+
+template <typename T>
+__device__ __forceinline__ float load_f(const T* p, long long i);
+template <>
+__device__ __forceinline__ float load_f<float>(const float* p, long long i) {
+  return p[i];
+}
+template <>
+__device__ __forceinline__ float load_f<__nv_bfloat16>(const __nv_bfloat16* p, long long i) {
+  return __bfloat162float(p[i]);
+}
+
+// C(g) = A(g) * B(g), 64x64 output tile per CTA, 4x4 per thread.
+template <typename T>
+__global__ void __launch_bounds__(SIMT_THREADS) simt_gemm_kernel(const SimtGemm p) {
+  __shared__ float As[TK][TM + 4];
+  __shared__ float Bs[TK][TN + 4];
+  const int g = blockIdx.z;
+  const int m0 = blockIdx.y * TM;
+  const int n0 = blockIdx.x * TN;
+  const T* A = static_cast<const T*>(p.A) + static_cast<long long>(g) * p.a_g;
+  const T* B = static_cast<const T*>(p.B) + static_cast<long long>(g) * p.b_g;
+  const int tx = threadIdx.x % 16;  // n direction
+  const int ty = threadIdx.x / 16;  // m direction
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < p.K; k0 += TK) {
+    for (int e = threadIdx.x; e < TM * TK; e += SIMT_THREADS) {
+      const int mm = e / TK, kk = e % TK;
+      const int m = m0 + mm, k = k0 + kk;
+      As[kk][mm] = (m < p.M && k < p.K) ? load_f(A, m * p.a_m + k * p.a_k) : 0.f;
+    }
+    for (int e = threadIdx.x; e < TN * TK; e += SIMT_THREADS) {
+      const int nn = e % TN, kk = e / TN;
+      const int n = n0 + nn, k = k0 + kk;
+      Bs[kk][nn] = (n < p.N && k < p.K) ? load_f(B, k * p.b_k + n * p.b_n) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < TK; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+  const EpiArgs& e = p.epi;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int m = m0 + ty * 4 + i;
+    if (m >= p.M || m >= e.row_limit) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int n = n0 + tx * 4 + j;
+      if (n >= p.N) continue;
+      const long long off = static_cast<long long>(g) * e.g_off + static_cast<long long>(m) * e.ld + n;
+      float v = e.alpha * acc[i][j];
+      if (e.X != nullptr) v += e.beta * e.X[off];
+      if (e.Y != nullptr) v += e.gamma * e.Y[off];
+      if (m == n) v += e.delta;
+      if (e.out_f32 != nullptr) e.out_f32[off] = v;
+      if (e.out_bf16 != nullptr) e.out_bf16[off] = __float2bfloat16_rn(v);
+    }
+  }
+}
+
+// Position of Q[i][j] (i < j) in the row-by-row packed strict upper triangle.
+__device__ __forceinline__ long long packed_pos(int i, int j, int b) {
+  return static_cast<long long>(i) * b - static_cast<long long>(i) * (i + 1) / 2 + (j - i - 1);
+}
+
+__global__ void unpack_kernel(const float* __restrict__ theta, int n, int b,
+                              float* __restrict__ q32, __nv_bfloat16* __restrict__ q16) {
+  const long long total = static_cast<long long>(n) * b * b;
+  const long long m = static_cast<long long>(b) * (b - 1) / 2;
+  for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int j = static_cast<int>(idx % b);
+    const int i = static_cast<int>((idx / b) % b);
+    const long long g = idx / (static_cast<long long>(b) * b);
+    float v = 0.f;
+    if (i < j) v = theta[g * m + packed_pos(i, j, b)];
+    else if (i > j) v = -theta[g * m + packed_pos(j, i, b)];
+    if (q32 != nullptr) q32[idx] = v;
+    if (q16 != nullptr) q16[idx] = __float2bfloat16_rn(v);
+  }
+}
+
+__global__ void identity_plus_kernel(const float* __restrict__ q, int n, int b,
+                                     float* __restrict__ o32, __nv_bfloat16* __restrict__ o16) {
+  const long long total = static_cast<long long>(n) * b * b;
+  for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int j = static_cast<int>(idx % b);
+    const int i = static_cast<int>((idx / b) % b);
+    const float v = q[idx] + (i == j ? 1.f : 0.f);
+    if (o32 != nullptr) o32[idx] = v;
+    if (o16 != nullptr) o16[idx] = __float2bfloat16_rn(v);
+  }
+}
+
+__global__ void expand_superblocks_kernel(const __nv_bfloat16* __restrict__ blocks, int n, int b,
+                                          int S, __nv_bfloat16* __restrict__ out) {
+  const int per = S / b;
+  const int nsb = (n + per - 1) / per;
+  const long long total = static_cast<long long>(nsb) * S * S;
+  for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int c = static_cast<int>(idx % S);
+    const int r = static_cast<int>((idx / S) % S);
+    const long long sb = idx / (static_cast<long long>(S) * S);
+    __nv_bfloat16 v = __float2bfloat16_rn(0.f);
+    const long long gblk = sb * per + r / b;
+    if (r / b == c / b && gblk < n)
+      v = blocks[(gblk * b + (r % b)) * b + (c % b)];
+    out[idx] = v;
+  }
+}
+
+__global__ void reduce_extract_kernel(const float* __restrict__ part, int splits, int n, int b,
+                                      int S, float* __restrict__ o32,
+                                      __nv_bfloat16* __restrict__ o16) {
+  const int per = S / b;
+  const int nsb = (n + per - 1) / per;
+  const long long split_stride = static_cast<long long>(nsb) * S * S;
+  const long long total = static_cast<long long>(n) * b * b;
+  for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int j = static_cast<int>(idx % b);
+    const int i = static_cast<int>((idx / b) % b);
+    const long long g = idx / (static_cast<long long>(b) * b);
+    const long long sb = g / per;
+    const int off = static_cast<int>(g % per) * b;
+    const long long src = (sb * S + off + i) * S + off + j;
+    float v = 0.f;
+    for (int s = 0; s < splits; ++s) v += part[s * split_stride + src];
+    if (o32 != nullptr) o32[idx] = v;
+    if (o16 != nullptr) o16[idx] = __float2bfloat16_rn(v);
+  }
+}
+
+__global__ void pack_skew_kernel(const float* __restrict__ A, const float* __restrict__ B, int n,
+                                 int b, float* __restrict__ dtheta) {
+  const long long total = static_cast<long long>(n) * b * b;
+  const long long m = static_cast<long long>(b) * (b - 1) / 2;
+  for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int j = static_cast<int>(idx % b);
+    const int i = static_cast<int>((idx / b) % b);
+    if (i >= j) continue;
+    const long long g = idx / (static_cast<long long>(b) * b);
+    const long long ij = idx;
+    const long long ji = (g * b + j) * b + i;
+    float v = A[ij] - A[ji];
+    if (B != nullptr) v += B[ij] - B[ji];
+    dtheta[g * m + packed_pos(i, j, b)] = v;
+  }
+}
+
+__global__ void f32_to_bf16_kernel(const float* __restrict__ in, long long count,
+                                   __nv_bfloat16* __restrict__ out) {
+  for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < count;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x)
+    out[idx] = __float2bfloat16_rn(in[idx]);
+}
+
+int ew_grid(long long total) {
+  long long blocks = (total + 255) / 256;
+  const long long cap = static_cast<long long>(sm_count()) * 16;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return static_cast<int>(blocks);
+}
+
+}  // namespace
+
+cudaError_t simt_gemm_run(const SimtGemm& g, cudaStream_t stream) {
+  if (g.M <= 0 || g.N <= 0 || g.batches <= 0) return cudaSuccess;
+  if (g.batches > 65535) return cudaErrorInvalidValue;
+  dim3 grid((g.N + TN - 1) / TN, (g.M + TM - 1) / TM, g.batches);
+  if (grid.y > 65535) return cudaErrorInvalidValue;
+  prof_begin(g.tag, stream);
+  if (g.bf16_inputs)
+    simt_gemm_kernel<__nv_bfloat16><<<grid, SIMT_THREADS, 0, stream>>>(g);
+  else
+    simt_gemm_kernel<float><<<grid, SIMT_THREADS, 0, stream>>>(g);
+  prof_end(g.tag, stream);
+  return cudaGetLastError();
+}
+
+#define POETX_EW_LAUNCH(tag, total, kernel, ...)                         \
+  do {                                                                   \
+    if ((total) <= 0) return cudaSuccess;                                \
+    prof_begin(tag, s);                                                  \
+    kernel<<<ew_grid(total), 256, 0, s>>>(__VA_ARGS__);                  \
+    prof_end(tag, s);                                                    \
+    return cudaGetLastError();                                           \
+  } while (0)
+
+cudaError_t launch_unpack(const float* theta, int n, int b, float* q32, __nv_bfloat16* q16,
+                          cudaStream_t s) {
+  POETX_EW_LAUNCH("unpack", static_cast<long long>(n) * b * b, unpack_kernel, theta, n, b, q32,
+                  q16);
+}
+
+cudaError_t launch_identity_plus(const float* q, int n, int b, float* o32, __nv_bfloat16* o16,
+                                 cudaStream_t s) {
+  POETX_EW_LAUNCH("identity_plus", static_cast<long long>(n) * b * b, identity_plus_kernel, q, n,
+                  b, o32, o16);
+}
+
+cudaError_t launch_expand_superblocks(const __nv_bfloat16* blocks, int n, int b, int S,
+                                      __nv_bfloat16* out, cudaStream_t s) {
+  const int per = S / b;
+  const long long nsb = (n + per - 1) / per;
+  POETX_EW_LAUNCH("expand_superblocks", nsb * S * S, expand_superblocks_kernel, blocks, n, b, S,
+                  out);
+}
+
+cudaError_t launch_reduce_extract(const float* part, int splits, int n, int b, int S, float* o32,
+                                  __nv_bfloat16* o16, cudaStream_t s) {
+  POETX_EW_LAUNCH("reduce_extract", static_cast<long long>(n) * b * b, reduce_extract_kernel,
+                  part, splits, n, b, S, o32, o16);
+}
+
+cudaError_t launch_pack_skew(const float* A, const float* B, int n, int b, float* dtheta,
+                             cudaStream_t s) {
+  POETX_EW_LAUNCH("pack_skew", static_cast<long long>(n) * b * b, pack_skew_kernel, A, B, n, b,
+                  dtheta);
+}
+
+cudaError_t launch_f32_to_bf16(const float* in, long long count, __nv_bfloat16* out,
+                               cudaStream_t s) {
+  POETX_EW_LAUNCH("f32_to_bf16", count, f32_to_bf16_kernel, in, count, out);
+}
+
+}  // namespace poetx

@@ -1,0 +1,82 @@
+"""One POET-X layer step through the C ABI: device buffers held in torch
+tensors, one shared workspace, and the four calls of a training step
+(build P blocks, build R blocks, forward, backward) enqueued on one stream.
+"""
+
+from __future__ import annotations
+
+import torch
+
+from . import (BF16, F32, poetx_backward, poetx_backward_workspace_size, poetx_build_blocks,
+               poetx_build_workspace_size, poetx_forward, poetx_forward_workspace_size,
+               poetx_packed_size)
+
+_TORCH_DTYPE = {F32: torch.float32, BF16: torch.bfloat16}
+
+
+def dtype_code(name: str) -> int:
+    return {"f32": F32, "bf16": BF16}[name]
+
+
+class PoetxLayer:
+    """Buffers for one projection y = R (W0 (P x)) with `tokens` tokens."""
+
+    def __init__(self, d_in, d_out, b, k, tokens, dtype="bf16", device="cuda",
+                 recompute_v=False):
+        self.d_in, self.d_out, self.b, self.k, self.tokens = d_in, d_out, b, k, tokens
+        self.code = dtype_code(dtype)
+        self.recompute_v = recompute_v
+        tdt = _TORCH_DTYPE[self.code]
+        dev = torch.device(device)
+        nP, nR = d_in // b, d_out // b
+        self.P_blocks = torch.empty((nP, b, b), dtype=tdt, device=dev)
+        self.R_blocks = torch.empty((nR, b, b), dtype=tdt, device=dev)
+        self.y = torch.empty((tokens, d_out), dtype=tdt, device=dev)
+        self.v = None if recompute_v else torch.empty((tokens, d_out), dtype=tdt, device=dev)
+        self.dx = torch.empty((tokens, d_in), dtype=tdt, device=dev)
+        self.dtheta_P = torch.empty((poetx_packed_size(d_in, b),), dtype=torch.float32,
+                                    device=dev)
+        self.dtheta_R = torch.empty((poetx_packed_size(d_out, b),), dtype=torch.float32,
+                                    device=dev)
+        ws = max(poetx_build_workspace_size(d_in, b, k, self.code),
+                 poetx_build_workspace_size(d_out, b, k, self.code),
+                 poetx_forward_workspace_size(d_in, d_out, b, tokens, self.code),
+                 poetx_backward_workspace_size(d_in, d_out, b, k, tokens, self.code,
+                                               recompute_v))
+        self.workspace = torch.empty((max(ws, 16),), dtype=torch.uint8, device=dev)
+
+    def build(self, theta_P, theta_R, stream=None):
+        poetx_build_blocks(theta_P, self.d_in, self.b, self.k, self.code, self.P_blocks,
+                           self.workspace, stream)
+        poetx_build_blocks(theta_R, self.d_out, self.b, self.k, self.code, self.R_blocks,
+                           self.workspace, stream)
+
+    def forward(self, x, W0, stream=None):
+        poetx_forward(x, W0, self.P_blocks, self.R_blocks, self.y, self.v, self.d_in,
+                      self.d_out, self.b, self.tokens, self.code, self.workspace, stream)
+        return self.y
+
+    def backward(self, dy, x, W0, theta_P, theta_R, stream=None):
+        poetx_backward(dy, x, W0, theta_P, theta_R, self.P_blocks, self.R_blocks, self.v,
+                       self.dx, self.dtheta_P, self.dtheta_R, self.d_in, self.d_out, self.b,
+                       self.k, self.tokens, self.code, self.workspace, stream)
+        return self.dx, self.dtheta_P, self.dtheta_R
+
+    def step(self, theta_P, theta_R, W0, x, dy, stream=None):
+        """Build both sides, forward, backward (one training step's layer work)."""
+        self.build(theta_P, theta_R, stream)
+        self.forward(x, W0, stream)
+        self.backward(dy, x, W0, theta_P, theta_R, stream)
+        return self.y, self.dx, self.dtheta_P, self.dtheta_R
+
+
+def to_device(inp, device="cuda"):
+    """Upload a LayerInputs (numpy) to torch tensors in the working dtype."""
+    tdt = torch.bfloat16 if inp.dtype == "bf16" else torch.float32
+
+    def act(a):
+        return torch.from_numpy(a).to(device=device).to(tdt).contiguous()
+
+    return dict(theta_P=torch.from_numpy(inp.theta_P).to(device).contiguous(),
+                theta_R=torch.from_numpy(inp.theta_R).to(device).contiguous(),
+                W0=act(inp.W0), x=act(inp.x), dy=act(inp.dy))

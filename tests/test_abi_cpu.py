@@ -1,0 +1,127 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds and
+loads, it exports every function include/poetx.h declares, the workspace
+size queries agree with the documented buffer plan, and invalid arguments
+are rejected before anything is enqueued."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import orthogonal_reparameterized_packed_gb300 as poetx
+from orthogonal_reparameterized_packed_gb300.build import build_library
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "poetx.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_library()
+    return poetx.load_library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = set(re.findall(r"\b(poetx_[a-z0-9_]+)\s*\(", text))
+    return names
+
+
+def test_header_declares_the_three_core_calls():
+    names = _declared_functions()
+    for core in ("poetx_build_blocks", "poetx_forward", "poetx_backward"):
+        assert core in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert names == set(poetx.EXPORTED_SYMBOLS)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        s = poetx.poetx_status_string(code)
+        assert s.startswith("POETX_")
+    assert "unknown" in poetx.poetx_status_string(99)
+
+
+@pytest.mark.parametrize("d,b", [(256, 32), (4096, 256), (96, 3), (1024, 512)])
+def test_packed_size(lib, d, b):
+    assert poetx.poetx_packed_size(d, b) == (d // b) * b * (b - 1) // 2
+
+
+def test_packed_size_rejects_bad_dims(lib):
+    assert poetx.poetx_packed_size(100, 32) == 0
+    assert poetx.poetx_packed_size(0, 4) == 0
+
+
+def test_workspace_sizes_are_positive_and_monotone(lib):
+    F32, BF16 = poetx.F32, poetx.BF16
+    assert poetx.poetx_build_workspace_size(4096, 256, 3, BF16) > 0
+    assert poetx.poetx_build_workspace_size(256, 32, 3, F32) > 0
+    a = poetx.poetx_forward_workspace_size(4096, 4096, 256, 1024, BF16)
+    b = poetx.poetx_forward_workspace_size(4096, 4096, 256, 2048, BF16)
+    assert 0 < a < b
+    # the forward needs at least the intermediate u = P x
+    assert a >= 1024 * 4096 * 2
+    r0 = poetx.poetx_backward_workspace_size(4096, 4096, 256, 3, 1024, BF16, False)
+    r1 = poetx.poetx_backward_workspace_size(4096, 4096, 256, 3, 1024, BF16, True)
+    assert 0 < r0 < r1
+    assert poetx.poetx_transform_workspace_size(4096, 32, 5, 8192, BF16) > 0
+
+
+def test_unsupported_shapes_give_zero_workspace(lib):
+    BF16 = poetx.BF16
+    assert poetx.poetx_forward_workspace_size(4800, 4800, 48, 16, BF16) == 0  # b not a power of 2
+    assert poetx.poetx_forward_workspace_size(384, 384, 128, 16, BF16) == 0   # d % 256
+    assert poetx.poetx_build_workspace_size(100, 32, 3, poetx.F32) == 0       # d % b
+
+
+FAKE = 1 << 20  # an aligned non-null address; never dereferenced on these paths
+
+
+def _raw():
+    return poetx.load_library()
+
+
+def test_build_rejects_invalid_arguments(lib):
+    L = _raw()
+    ws = poetx.poetx_build_workspace_size(256, 32, 3, poetx.F32)
+    assert L.poetx_build_blocks(FAKE, 100, 32, 3, poetx.F32, FAKE, FAKE, ws, None) == 1
+    assert L.poetx_build_blocks(None, 256, 32, 3, poetx.F32, FAKE, FAKE, ws, None) == 1
+    assert L.poetx_build_blocks(FAKE + 4, 256, 32, 3, poetx.F32, FAKE, FAKE, ws, None) == 1
+    assert L.poetx_build_blocks(FAKE, 256, 32, -1, poetx.F32, FAKE, FAKE, ws, None) == 1
+    assert L.poetx_build_blocks(FAKE, 256, 32, 17, poetx.F32, FAKE, FAKE, ws, None) == 1
+    assert L.poetx_build_blocks(FAKE, 256, 32, 3, 7, FAKE, FAKE, ws, None) == 1
+    assert L.poetx_build_blocks(FAKE, 256, 32, 3, poetx.F32, FAKE, FAKE, ws - 1, None) == 3
+    assert L.poetx_build_blocks(FAKE, 256, 32, 3, poetx.F32, FAKE, None, ws, None) == 3
+    assert L.poetx_build_blocks(FAKE, 4800, 48, 3, poetx.BF16, FAKE, FAKE, ws, None) == 2
+
+
+def test_forward_and_backward_reject_invalid_arguments(lib):
+    L = _raw()
+    B = poetx.BF16
+    ws = poetx.poetx_forward_workspace_size(512, 512, 256, 64, B)
+    args = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE]
+    assert L.poetx_forward(*args, 512, 512, 256, -1, B, FAKE, ws, None) == 1
+    assert L.poetx_forward(*args, 512, 500, 256, 64, B, FAKE, ws, None) == 1
+    assert L.poetx_forward(*args, 512, 640, 128, 64, B, FAKE, ws, None) == 2
+    # v_saved = NULL: the workspace must also hold v
+    assert L.poetx_forward(FAKE, FAKE, FAKE, FAKE, FAKE, None, 512, 512, 256, 64, B, FAKE,
+                           ws - 256, None) == 3
+    assert L.poetx_forward(FAKE, FAKE, None, FAKE, FAKE, None, 512, 512, 256, 64, B, FAKE, ws,
+                           None) == 1
+    assert L.poetx_forward(FAKE, FAKE, FAKE, FAKE, FAKE + 8, None, 512, 512, 256, 64, B, FAKE,
+                           ws, None) == 1
+    wb = poetx.poetx_backward_workspace_size(512, 512, 256, 3, 64, B, 0)
+    bargs = [FAKE] * 7
+    assert L.poetx_backward(*bargs, FAKE, FAKE, FAKE, FAKE, 512, 512, 256, 3, 64, B, FAKE,
+                            wb - 1, None) == 3
+    assert L.poetx_backward(*bargs, FAKE, None, FAKE, FAKE, 512, 512, 256, 3, 64, B, FAKE,
+                            wb, None) == 1
+    assert L.poetx_backward(*bargs, FAKE, FAKE, FAKE, FAKE, 512, 512, 256, 20, 64, B, FAKE,
+                            wb, None) == 1
