@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--workload", default="llama3_8b_qo", choices=sorted(WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time eager launches instead of CUDA-graph replays")
     return ap.parse_args()
 
 
@@ -252,13 +254,12 @@ def run_gpu(args):
     if poetx.poetx_device_status() != 0:
         raise RuntimeError("device status not OK after warm-up")
 
-    clocks = ClockSampler(local)
+    # (1) eager pass: every launch bracketed by CUDA events on its stream,
+    #     giving the per-kernel durations the roofline uses
     launches0 = poetx.poetx_launch_count()
     poetx.poetx_profile_start(64 * args.steps)
     barrier()
     torch.cuda.synchronize()
-    clocks.start()
-    time.sleep(0.3)  # let the sampler take its first reading
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
@@ -267,9 +268,46 @@ def run_gpu(args):
     t1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    clk = clocks.stop()
     poetx.poetx_profile_stop()
-    launches = poetx.poetx_launch_count() - launches0
+    launches_per_step = (poetx.poetx_launch_count() - launches0) // args.steps
+    ms_eager = t0.elapsed_time(t1) / args.steps
+
+    # (2) the same step captured once in a CUDA graph and replayed: the timed
+    #     region of the headline number (no host launch overhead between kernels)
+    graph = None
+    if not args.no_graph:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+
+    def run_step():
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
+
+    clocks = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)  # let the sampler take its first reading
+    t0.record(stream)
+    for _ in range(args.steps):
+        run_step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clk = clocks.stop()
+    launches = launches_per_step * args.steps
     ms = t0.elapsed_time(t1) / args.steps
     ms_t = torch.tensor([ms], device="cuda")
     if world > 1:
@@ -290,13 +328,14 @@ def run_gpu(args):
     dom = max((t for t in kernels if algorithmic_work(t, w)), key=lambda t: kernels[t]["total_ms"])
     amount, unit, bound = algorithmic_work(dom, w)
     avg_s = kernels[dom]["avg_us"] * 1e-6
-    long_region = ms * args.steps > 1000.0
+    long_region = ms_eager * args.steps > 1000.0
     peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
     achieved = amount / avg_s
     roofline = {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
                 "peak_source": f"{peak_src} ({'sustained' if long_region else 'burst'})",
-                "per_launch": f"2*T*d_in*d_out = {amount:.4f} TFLOP"}
+                "per_launch": f"2*T*d_in*d_out = {amount:.4f} TFLOP",
+                "timing": "CUDA events around each launch, eager pass of the same K steps"}
 
     # whole-step algorithmic tensor work for context
     T, di, do, b = w["tokens"], w["d_in"], w["d_out"], w["b"]
@@ -312,13 +351,12 @@ def run_gpu(args):
         hdy = dev["dy"].cpu().pin_memory()
         hP = torch.empty(layer.dtheta_P.shape, dtype=torch.float32).pin_memory()
         hR = torch.empty(layer.dtheta_R.shape, dtype=torch.float32).pin_memory()
-        dx_in = torch.empty_like(dev["x"])
-        dy_in = torch.empty_like(dev["dy"])
 
         def e2e_step():
-            dx_in.copy_(hx, non_blocking=True)
-            dy_in.copy_(hdy, non_blocking=True)
-            layer.step(dev["theta_P"], dev["theta_R"], dev["W0"], dx_in, dy_in)
+            # inputs land in the buffers the step (or its graph) reads
+            dev["x"].copy_(hx, non_blocking=True)
+            dev["dy"].copy_(hdy, non_blocking=True)
+            run_step()
             hP.copy_(layer.dtheta_P, non_blocking=True)
             hR.copy_(layer.dtheta_R, non_blocking=True)
 
@@ -346,14 +384,15 @@ def run_gpu(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(inp, 512)
+        cpu = cpu_baseline(inp, 2048)
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
                 "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_max,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16", "data": "synthetic", "config": config_json(name, w, world),
-                "gpu_launches": launches, "roofline": roofline,
+                "gpu_launches": launches, "launch": "cuda_graph" if graph is not None else "eager",
+                "ms_per_step_eager": ms_eager, "roofline": roofline,
                 "step_tflops": step_flop / (ms_max * 1e-3) / 1e12,
                 "kernels": kernels, "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
                 "device_status": status}

@@ -128,6 +128,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 poetx_status check_dims(int d, int b, bool is_bf16) {
   if (b < 2 || b > 512 || d <= 0 || d % b != 0) return POETX_ERR_INVALID_ARG;
+  if (static_cast<long long>(d) * b > (1ll << 30)) return POETX_ERR_UNSUPPORTED;
   if (is_bf16) {
     if (b != 32 && b != 64 && b != 128 && b != 256 && b != 512) return POETX_ERR_UNSUPPORTED;
     const int S = b > 256 ? b : 256;
@@ -183,13 +184,15 @@ cudaError_t tc_transform(const bf16* in, const bf16* sb, bf16* out, int d, int S
   g.N = S;
   g.K = S;
   g.batches = d / S;
-  g.BN = 256;
+  g.BN = S == 256 ? 256 : 128;  // the resident B tile (BN x S bf16) must fit 128 KiB
+  g.b_resident = true;
   g.A = op(in, T, d, d, false, 0, S);
   g.B = transposed ? op(sb, d, S, S, true, 0, S) : op(sb, d, S, S, false, S, 0);
   g.epi.out_bf16 = out;
   g.epi.ld = d;
-  g.epi.g_off = S;
+  g.epi.col_g = S;
   g.epi.row_limit = static_cast<int>(T);
+  g.epi.out_rows = T;
   g.tag = tag;
   return tc_gemm_run(g, s);
 }
@@ -208,8 +211,9 @@ cudaError_t tc_outer(const bf16* A, const bf16* B, float* part, int d, int S, lo
   g.B = op(B, T, d, d, true, S, 0);
   g.epi.out_f32 = part;
   g.epi.ld = S;
-  g.epi.g_off = static_cast<long long>(S) * S;
-  g.epi.s_off = static_cast<long long>(d / S) * S * S;
+  g.epi.row_g = S;
+  g.epi.row_s = (d / S) * S;
+  g.epi.out_rows = static_cast<long long>(splits) * (d / S) * S;
   g.tag = "outer";
   return tc_gemm_run(g, s);
 }
@@ -237,6 +241,7 @@ cudaError_t tc_w0(const bf16* A, const bf16* W0, bf16* out, int d_in, int d_out,
   }
   g.epi.out_bf16 = out;
   g.epi.row_limit = static_cast<int>(T);
+  g.epi.out_rows = T;
   return tc_gemm_run(g, s);
 }
 
@@ -263,7 +268,7 @@ cudaError_t simt_transform(const float* in, const float* blocks, float* out, int
   }
   g.epi.out_f32 = out;
   g.epi.ld = d;
-  g.epi.g_off = b;
+  g.epi.col_g = b;
   g.tag = tag;
   return simt_gemm_run(g, s);
 }
@@ -286,7 +291,7 @@ cudaError_t simt_outer(const float* A, const float* B, float* G, int d, int b, l
   g.b_n = 1;
   g.epi.out_f32 = G;
   g.epi.ld = b;
-  g.epi.g_off = static_cast<long long>(b) * b;
+  g.epi.row_g = b;
   g.tag = "outer";
   return simt_gemm_run(g, s);
 }
@@ -339,7 +344,7 @@ cudaError_t small_product(int kind, bool tc, int n, int b, const float* q32, con
     g.N = b;
     g.K = b;
     g.batches = n;
-    g.BN = b < 256 ? b : 256;
+    g.BN = 128;  // b >= 128 here; 128-wide tiles give twice the CTAs of 256-wide ones
     if (kind == 0) {
       g.A = op(q16, rows, b, b, false, b, 0);  // A[m][kk] = Q[m][kk]
       g.B = op(m16, rows, b, b, true, 0, b);   // B[nn][kk] = M[kk][nn]
@@ -388,10 +393,10 @@ cudaError_t small_product(int kind, bool tc, int n, int b, const float* q32, con
   return simt_gemm_run(g, s);
 }
 
-EpiArgs block_epi(int b) {
+EpiArgs block_epi(int b) {  // [n][b][b] row-major outputs and addends
   EpiArgs e;
   e.ld = b;
-  e.g_off = static_cast<long long>(b) * b;
+  e.row_g = b;
   return e;
 }
 
@@ -422,7 +427,7 @@ BuildBufs carve_build(Carver& c, int n, int b, bool tc) {
 cudaError_t run_build(const float* theta, int n, int b, int k, bool is_bf16, void* blocks,
                       const BuildBufs& w, cudaStream_t s) {
   const bool tc = tc_small(is_bf16, b);
-  CK(launch_unpack(theta, n, b, w.q32, tc ? w.q16 : nullptr, s));
+  CK(launch_unpack(theta, n, nullptr, 0, b, w.q32, tc ? w.q16 : nullptr, s));
   float* out32 = is_bf16 ? nullptr : static_cast<float*>(blocks);
   bf16* out16 = is_bf16 ? static_cast<bf16*>(blocks) : nullptr;
   if (k == 0) return launch_identity_plus(w.q32, n, b, out32, out16, s);
@@ -480,16 +485,19 @@ CnpBufs carve_cnp(Carver& c, int n, int b, int k, bool tc) {
   return w;
 }
 
-// Input: the block gradient G in w.g32[0] (and w.g16[0] for tc).
+// Input: the block gradients G of n = n_a + n_b blocks in w.g32[0] (and
+// w.g16[0] for tc); blocks [0, n_a) belong to theta_a, the rest to theta_b.
 // Reverse sweep of E_{k+1} = Q, E_i = c_i Q + Q E_{i+1} (c_i = 2), R = I + E_1:
 //   Gbar_1 = G;  for i = 1..k:  dQ += 2 Gbar_i + Gbar_i E_{i+1}^T,
 //                               Gbar_{i+1} = Q^T Gbar_i;
 //   dQ += Gbar_{k+1};  dtheta = pack(dQ - dQ^T).
-cudaError_t run_cnp_backward(const float* theta, int n, int b, int k, bool is_bf16,
-                             const CnpBufs& w, float* dtheta, cudaStream_t s) {
+cudaError_t run_cnp_backward(const float* theta_a, int n_a, const float* theta_b, int n_b, int b,
+                             int k, bool is_bf16, const CnpBufs& w, float* dtheta_a,
+                             float* dtheta_b, cudaStream_t s) {
   const bool tc = tc_small(is_bf16, b);
-  if (k == 0) return launch_pack_skew(w.g32[0], nullptr, n, b, dtheta, s);
-  CK(launch_unpack(theta, n, b, w.q32, tc ? w.q16 : nullptr, s));
+  const int n = n_a + n_b;
+  if (k == 0) return launch_pack_skew(w.g32[0], nullptr, n_a, n_b, b, dtheta_a, dtheta_b, s);
+  CK(launch_unpack(theta_a, n_a, theta_b, n_b, b, w.q32, tc ? w.q16 : nullptr, s));
   // E_i for i = k .. 2 (E_{k+1} = Q)
   for (int i = k; i >= 2; --i) {
     EpiArgs e = block_epi(b);
@@ -524,7 +532,7 @@ cudaError_t run_cnp_backward(const float* theta, int n, int b, int k, bool is_bf
                      "cnp_bwd", s));
     cur = 1 - cur;
   }
-  return launch_pack_skew(w.dq, w.g32[cur], n, b, dtheta, s);
+  return launch_pack_skew(w.dq, w.g32[cur], n_a, n_b, b, dtheta_a, dtheta_b, s);
 }
 
 // -------------------------------------------------------- layer buffers
@@ -604,28 +612,25 @@ BwdPlan carve_backward(Carver& c, int d_in, int d_out, int b, int k, long long T
     const long long part_out = static_cast<long long>(p.splits_out) * d_out * S;
     p.sb.part = c.take<float>(static_cast<size_t>(part_in > part_out ? part_in : part_out));
   }
-  const int n_max = (d_in > d_out ? d_in : d_out) / b;
-  p.cnp = carve_cnp(c, n_max, b, k, tc_small(is_bf16, b));
+  p.cnp = carve_cnp(c, (d_in + d_out) / b, b, k, tc_small(is_bf16, b));
   return p;
 }
 
-// Block gradient of one side into cnp.g32[0] (+ g16[0]), then its packed
-// adjoint into dtheta.
-cudaError_t side_gradient(const void* dout, const void* in, int d, int b, int k, long long T,
-                          bool is_bf16, const float* theta, float* part, int splits,
-                          const CnpBufs& cnp, float* dtheta, cudaStream_t s) {
+// Block gradients G[g] = sum_t dout[t][g-block]^T in[t][g-block] of one side
+// into g32 (+ g16 for the bf16 adjoint), [d/b][b][b].
+cudaError_t block_gradient(const void* dout, const void* in, int d, int b, long long T,
+                           bool is_bf16, float* part, int splits, float* g32, bf16* g16,
+                           cudaStream_t s) {
   const int n = d / b;
   if (is_bf16) {
     const int S = superblock(b);
     CK(tc_outer(static_cast<const bf16*>(dout), static_cast<const bf16*>(in), part, d, S, T,
                 splits, s));
-    CK(launch_reduce_extract(part, splits, n, b, S, cnp.g32[0],
-                             tc_small(true, b) ? cnp.g16[0] : nullptr, s));
-  } else {
-    CK(simt_outer(static_cast<const float*>(dout), static_cast<const float*>(in), cnp.g32[0], d,
-                  b, T, s));
+    return launch_reduce_extract(part, splits, n, b, S, g32, tc_small(true, b) ? g16 : nullptr,
+                                 s);
   }
-  return run_cnp_backward(theta, n, b, k, is_bf16, cnp, dtheta, s);
+  return simt_outer(static_cast<const float*>(dout), static_cast<const float*>(in), g32, d, b, T,
+                    s);
 }
 
 const void* superblocks_or_blocks(const void* blocks, bf16* sb, int d, int b, bool is_bf16,
@@ -797,8 +802,9 @@ poetx_status poetx_backward(const void* dy, const void* x, const void* W0, const
     e = simt_transform(static_cast<const float*>(dy), static_cast<const float*>(rsb),
                        static_cast<float*>(p.sb.dv), d_out, b, tokens, true, "transform_t", s);
   if (e != cudaSuccess) return POETX_ERR_CUDA;
-  e = side_gradient(dy, v, d_out, b, k, tokens, is_bf16, theta_R, p.sb.part, p.splits_out,
-                    p.cnp, dtheta_R, s);
+  const long long off_R = static_cast<long long>(d_in) * b;  // R blocks follow the P blocks
+  e = block_gradient(dy, v, d_out, b, tokens, is_bf16, p.sb.part, p.splits_out,
+                     p.cnp.g32[0] + off_R, p.cnp.g16[0] ? p.cnp.g16[0] + off_R : nullptr, s);
   if (e != cudaSuccess) return POETX_ERR_CUDA;
   // du = dv W0
   if (is_bf16)
@@ -816,9 +822,12 @@ poetx_status poetx_backward(const void* dy, const void* x, const void* W0, const
     e = simt_transform(static_cast<const float*>(p.sb.du), static_cast<const float*>(psb),
                        static_cast<float*>(dx), d_in, b, tokens, true, "transform_t", s);
   if (e != cudaSuccess) return POETX_ERR_CUDA;
-  e = side_gradient(p.sb.du, x, d_in, b, k, tokens, is_bf16, theta_P, p.sb.part, p.splits_in,
-                    p.cnp, dtheta_P, s);
-  return to_status(e);
+  e = block_gradient(p.sb.du, x, d_in, b, tokens, is_bf16, p.sb.part, p.splits_in,
+                     p.cnp.g32[0], p.cnp.g16[0], s);
+  if (e != cudaSuccess) return POETX_ERR_CUDA;
+  // adjoint of the block build for both sides at once
+  return to_status(run_cnp_backward(theta_P, d_in / b, theta_R, d_out / b, b, k, is_bf16, p.cnp,
+                                    dtheta_P, dtheta_R, s));
 }
 
 size_t poetx_transform_workspace_size(int d, int b, int k, int64_t tokens, poetx_dtype dtype) {
@@ -896,8 +905,10 @@ poetx_status poetx_transform_backward(const void* dout, const void* x, const flo
     e = simt_transform(static_cast<const float*>(dout), static_cast<const float*>(sb),
                        static_cast<float*>(dx), d, b, tokens, true, "transform_t", s);
   if (e != cudaSuccess) return POETX_ERR_CUDA;
+  e = block_gradient(dout, x, d, b, tokens, is_bf16, part, splits, cnp.g32[0], cnp.g16[0], s);
+  if (e != cudaSuccess) return POETX_ERR_CUDA;
   return to_status(
-      side_gradient(dout, x, d, b, k, tokens, is_bf16, theta, part, splits, cnp, dtheta, s));
+      run_cnp_backward(theta, d / b, nullptr, 0, b, k, is_bf16, cnp, dtheta, nullptr, s));
 }
 
 poetx_status poetx_device_status(void) {

@@ -1,21 +1,27 @@
 // Tensor-core contraction engine for sm_103a: C = A * B^T per batch, bf16
 // operands staged by TMA into 128-byte-swizzled shared memory, tcgen05.mma
-// accumulating in TMEM, fp32 epilogue straight from TMEM.
+// accumulating in TMEM, epilogue straight from TMEM.
 //
 // One persistent CTA per SM, warp-specialised:
-//   warp 0      TMA producer (one elected lane), STAGES-deep smem ring
+//   warp 0      TMA producer (one elected lane)
 //   warp 1      TMEM allocator + MMA issuer (one elected lane)
-//   warps 2..5  epilogue: TMEM -> registers -> EpiArgs -> global
+//   warps 2..5  epilogue: TMEM -> registers -> global
 // Two TMEM accumulators (2 x BN fp32 columns) let the epilogue of tile i
-// overlap the main loop of tile i+1.  Every barrier wait is bounded: on
-// expiry the CTA records POETX_ERR_TIMEOUT, drains what it issued, frees
-// TMEM and returns.
+// overlap the main loop of tile i+1.
 //
-// Every contraction of the layer maps onto this engine: the W0 GEMM and its
-// transpose, the block-diagonal transforms (batch = diagonal block, K window
-// = that block's features), the per-block outer products summed over tokens
-// (split-K over tokens), and the b x b products of the block builder and its
-// adjoint.
+// Variants (template parameters):
+//   B_RES  the B operand of one (batch, N tile) stays resident in shared
+//          memory while the CTA walks a contiguous run of M tiles; only A
+//          streams through the ring.  Used by the block-diagonal transforms,
+//          whose B is one b x b block reused by every token tile.
+//   EPI    EPI_ROWS: each thread owns one accumulator row and applies the
+//          general EpiArgs (scale, fp32 addends, diagonal shift, fp32/bf16
+//          outputs) with 16-byte stores.  EPI_TMA_BF16 / EPI_TMA_F32: plain
+//          stores of one output; each warp writes its 32-row chunk into a
+//          128B-swizzled staging buffer and one lane issues a TMA tile store.
+//
+// Every barrier wait is bounded: on expiry the CTA records
+// POETX_ERR_TIMEOUT, drains what it issued, frees TMEM and returns.
 #include <algorithm>
 #include <cstdio>
 
@@ -31,12 +37,19 @@ constexpr int BK = 64;  // one 128-byte swizzle row of bf16
 constexpr int STAGES = 4;
 constexpr int NUM_THREADS = 192;
 constexpr int kStatusTimeout = 5;  // POETX_ERR_TIMEOUT
+constexpr int kResBytes = 128 * 1024;
 
-template <int BN>
+enum { EPI_ROWS = 0, EPI_TMA_BF16 = 1, EPI_TMA_F32 = 2 };
+
+template <int BN, bool B_RES, int EPI>
 struct TcShape {
   static constexpr int A_BYTES = BM * BK * 2;  // 16 KB
-  static constexpr int B_BYTES = BN * BK * 2;  // 16 or 32 KB
-  static constexpr int SMEM = 1024 + STAGES * (A_BYTES + B_BYTES) + 256;
+  static constexpr int B_BYTES = BN * BK * 2;  // one K step of B: 16 or 32 KB
+  static constexpr int RING = B_RES ? STAGES * A_BYTES : STAGES * (A_BYTES + B_BYTES);
+  static constexpr int RES = B_RES ? kResBytes : 0;
+  static constexpr int MAX_RES_KSTEPS = kResBytes / B_BYTES;
+  static constexpr int OUT_STAGE = EPI == EPI_ROWS ? 0 : 4 * 4096;  // per warp 32 rows x 128 B
+  static constexpr int SMEM = 1024 + RING + RES + OUT_STAGE + 256;
   static constexpr uint32_t TMEM_COLS = 2 * BN;
 };
 
@@ -53,12 +66,52 @@ __device__ __forceinline__ void record_timeout(int* status, volatile int* abort)
   *abort = 1;
 }
 
-// Apply the epilogue to 32 consecutive accumulator columns of one row.
+// Tile order: non-resident variants walk N fastest (consecutive tiles of a
+// CTA's wave share the A rows); resident-B variants walk M fastest so a CTA's
+// contiguous run of tiles keeps one B.
+template <bool B_RES>
+__device__ __forceinline__ void decode_tile(int t, const TcKernelArgs& p, int& g, int& sp, int& mt,
+                                            int& nt) {
+  if (B_RES) {
+    mt = t % p.m_tiles;
+    t /= p.m_tiles;
+    nt = t % p.n_tiles;
+    t /= p.n_tiles;
+  } else {
+    nt = t % p.n_tiles;
+    t /= p.n_tiles;
+    mt = t % p.m_tiles;
+    t /= p.m_tiles;
+  }
+  sp = t % p.splits;
+  g = t / p.splits;
+}
+
+// Tiles of this CTA: resident variants take a contiguous run, others stride.
+template <bool B_RES>
+struct TileRange {
+  int first, end, step;
+  __device__ explicit TileRange(int num_tiles) {
+    if (B_RES) {
+      const int per = (num_tiles + gridDim.x - 1) / gridDim.x;
+      first = blockIdx.x * per;
+      end = min(first + per, num_tiles);
+      step = 1;
+    } else {
+      first = blockIdx.x;
+      end = num_tiles;
+      step = gridDim.x;
+    }
+  }
+};
+
+// EPI_ROWS: one thread, one row, 32 consecutive columns.
 __device__ __forceinline__ void epilogue_row32(const EpiArgs& e, int g, int s, int row, int col0,
                                                const uint32_t (&r)[32]) {
   if (row >= e.row_limit) return;
-  const long long off = (long long)g * e.g_off + (long long)s * e.s_off +
-                        (long long)row * e.ld + col0;
+  const long long off =
+      (static_cast<long long>(g) * e.row_g + static_cast<long long>(s) * e.row_s + row) * e.ld +
+      static_cast<long long>(g) * e.col_g + col0;
   float v[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = e.alpha * __uint_as_float(r[j]);
@@ -111,27 +164,38 @@ __device__ __forceinline__ void epilogue_row32(const EpiArgs& e, int g, int s, i
   }
 }
 
-template <bool A_MN, bool B_MN, int BN>
+__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo, uint32_t hi) {
+  __nv_bfloat162 p2 = __floats2bfloat162_rn(__uint_as_float(lo), __uint_as_float(hi));
+  return *reinterpret_cast<uint32_t*>(&p2);
+}
+
+template <bool A_MN, bool B_MN, int BN, bool B_RES, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                   const __grid_constant__ CUtensorMap tmB, const TcKernelArgs p) {
-  using S = TcShape<BN>;
+                   const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const TcKernelArgs p) {
+  using S = TcShape<BN, B_RES, EPI>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sA = base;
-  uint8_t* sB = base + STAGES * S::A_BYTES;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(sB + STAGES * S::B_BYTES);
+  uint8_t* sA = base;                        // STAGES x A tile
+  uint8_t* sB = base + STAGES * S::A_BYTES;  // STAGES x B tile (streamed variants)
+  uint8_t* sRes = base + S::RING;            // resident B (B_RES)
+  uint8_t* sOut = base + S::RING + S::RES;   // TMA-store staging (EPI_TMA_*)
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(base + S::RING + S::RES + S::OUT_STAGE);
   uint64_t* empty_bar = full_bar + STAGES;
   uint64_t* tfull_bar = empty_bar + STAGES;  // [2]
   uint64_t* tempty_bar = tfull_bar + 2;      // [2]
   uint64_t* drain_bar = tempty_bar + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  uint64_t* bfull_bar = drain_bar + 1;
+  uint64_t* bempty_bar = bfull_bar + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bempty_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const int num_tiles = p.batches * p.splits * p.m_tiles * p.n_tiles;
+  const TileRange<B_RES> range(num_tiles);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -143,12 +207,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(&tempty_bar[a], 4);
     }
     mbar_init(drain_bar, 1);
+    mbar_init(bfull_bar, 1);
+    mbar_init(bempty_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (EPI != EPI_ROWS) tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, S::TMEM_COLS);
@@ -166,41 +233,64 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0;
       long long issued = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        int t = tile;
-        const int nt = t % p.n_tiles;
-        t /= p.n_tiles;
-        const int mt = t % p.m_tiles;
-        t /= p.m_tiles;
-        const int sp = t % p.splits;
-        const int g = t / p.splits;
+      int res_key = -1, res_loads = 0;
+      for (int tile = range.first; tile < range.end && ok; tile += range.step) {
+        int g, sp, mt, nt;
+        decode_tile<B_RES>(tile, p, g, sp, mt, nt);
         const int ks0 = sp * p.k_steps_per_split;
         const int ks1 = min(ks0 + p.k_steps_per_split, p.k_steps_total);
         const int a_mn = g * p.a_mn_per_g + mt * BM;
         const int b_mn = g * p.b_mn_per_g + nt * BN;
+        if (B_RES) {
+          const int key = g * p.n_tiles + nt;
+          if (key != res_key) {
+            // the previous resident B is free once the MMAs that read it are done
+            if (!mbar_wait(bempty_bar, (res_loads & 1) ^ 1, abort_flag)) {
+              record_timeout(p.status, abort_flag);
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bfull_bar, p.k_steps_total * S::B_BYTES);
+            for (int kc = 0; kc < p.k_steps_total; ++kc) {
+              const int b_k = g * p.b_k_per_g + kc * BK;
+              uint8_t* dst = sRes + kc * S::B_BYTES;
+              if (!B_MN) {
+                tma_load_2d(dst, &tmB, bfull_bar, b_k, b_mn);
+              } else {
+#pragma unroll
+                for (int c = 0; c < BN / 64; ++c)
+                  tma_load_2d(dst + c * 8192, &tmB, bfull_bar, b_mn + 64 * c, b_k);
+              }
+            }
+            res_key = key;
+            ++res_loads;
+          }
+        }
         for (int ks = ks0; ks < ks1; ++ks) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag)) {
             record_timeout(p.status, abort_flag);
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full_bar[stage], S::A_BYTES + S::B_BYTES);
+          mbar_arrive_expect_tx(&full_bar[stage], S::A_BYTES + (B_RES ? 0 : S::B_BYTES));
           const int a_k = g * p.a_k_per_g + ks * BK;
-          const int b_k = g * p.b_k_per_g + ks * BK;
           uint8_t* a_dst = sA + stage * S::A_BYTES;
-          uint8_t* b_dst = sB + stage * S::B_BYTES;
           if (!A_MN) {
             tma_load_2d(a_dst, &tmA, &full_bar[stage], a_k, a_mn);
           } else {
             tma_load_2d(a_dst, &tmA, &full_bar[stage], a_mn, a_k);
             tma_load_2d(a_dst + 8192, &tmA, &full_bar[stage], a_mn + 64, a_k);
           }
-          if (!B_MN) {
-            tma_load_2d(b_dst, &tmB, &full_bar[stage], b_k, b_mn);
-          } else {
+          if (!B_RES) {
+            const int b_k = g * p.b_k_per_g + ks * BK;
+            uint8_t* b_dst = sB + stage * S::B_BYTES;
+            if (!B_MN) {
+              tma_load_2d(b_dst, &tmB, &full_bar[stage], b_k, b_mn);
+            } else {
 #pragma unroll
-            for (int c = 0; c < BN / 64; ++c)
-              tma_load_2d(b_dst + c * 8192, &tmB, &full_bar[stage], b_mn + 64 * c, b_k);
+              for (int c = 0; c < BN / 64; ++c)
+                tma_load_2d(b_dst + c * 8192, &tmB, &full_bar[stage], b_mn + 64 * c, b_k);
+            }
           }
           ++issued;
           if (++stage == STAGES) {
@@ -223,6 +313,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           while (!mbar_try_wait(&full_bar[st], ph) && global_timer_ns() - t0 < 10000000ull) {
           }
         }
+        if (B_RES && res_loads > 0) {
+          const unsigned long long t0 = global_timer_ns();
+          while (!mbar_try_wait(bfull_bar, (res_loads - 1) & 1) &&
+                 global_timer_ns() - t0 < 10000000ull) {
+          }
+        }
       }
     }
   } else if (warp == 1) {
@@ -235,11 +331,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t acc_phase = 0;
       bool ok = true;
       bool any_mma = false;
-      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-        int t = tile / (p.n_tiles * p.m_tiles);
-        const int sp = t % p.splits;
+      int res_key = -1, res_loads = 0;
+      for (int tile = range.first; tile < range.end && ok; tile += range.step) {
+        int g, sp, mt, nt;
+        decode_tile<B_RES>(tile, p, g, sp, mt, nt);
         const int ks0 = sp * p.k_steps_per_split;
         const int ks1 = min(ks0 + p.k_steps_per_split, p.k_steps_total);
+        if (B_RES) {
+          const int key = g * p.n_tiles + nt;
+          if (key != res_key) {
+            if (res_loads > 0) umma_commit(bempty_bar);  // old B free after the MMAs so far
+            if (!mbar_wait(bfull_bar, res_loads & 1, abort_flag)) {
+              record_timeout(p.status, abort_flag);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            res_key = key;
+            ++res_loads;
+          }
+        }
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1, abort_flag)) {
           record_timeout(p.status, abort_flag);
           ok = false;
@@ -255,7 +366,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           tc_fence_after();
           const uint32_t a_base = smem_u32(sA + stage * S::A_BYTES);
-          const uint32_t b_base = smem_u32(sB + stage * S::B_BYTES);
+          const uint32_t b_base =
+              B_RES ? smem_u32(sRes + ks * S::B_BYTES) : smem_u32(sB + stage * S::B_BYTES);
 #pragma unroll
           for (int j = 0; j < BK / 16; ++j) {
             const uint64_t adesc = A_MN ? smem_desc_sw128(a_base + j * 2048, 8192, 1024)
@@ -287,31 +399,66 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else {
     // ----------------------------------------------------------- epilogue
     const int quarter = warp & 3;  // TMEM lanes this warp may read
-    const int row_in_tile = quarter * 32 + lane;
+    uint8_t* stg = sOut + quarter * 4096;
+    bool stores_pending = false;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-      int t = tile;
-      const int nt = t % p.n_tiles;
-      t /= p.n_tiles;
-      const int mt = t % p.m_tiles;
-      t /= p.m_tiles;
-      const int sp = t % p.splits;
-      const int g = t / p.splits;
+    for (int tile = range.first; tile < range.end; tile += range.step) {
+      int g, sp, mt, nt;
+      decode_tile<B_RES>(tile, p, g, sp, mt, nt);
       if (!mbar_wait(&tfull_bar[acc], acc_phase, abort_flag)) {
         record_timeout(p.status, abort_flag);
         break;
       }
       tc_fence_after();
-      const int row = mt * BM + row_in_tile;
-      const uint32_t t_base =
-          tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      const uint32_t t_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                              static_cast<uint32_t>(acc * BN);
+      if (EPI == EPI_ROWS) {
+        const int row = mt * BM + quarter * 32 + lane;
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
-        uint32_t r[32];
-        tmem_load_32cols(t_base + c0, r);
-        tmem_load_wait();
-        epilogue_row32(p.epi, g, sp, row, nt * BN + c0, r);
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t r[32];
+          tmem_load_32cols(t_base + c0, r);
+          tmem_load_wait();
+          epilogue_row32(p.epi, g, sp, row, nt * BN + c0, r);
+        }
+      } else {
+        // TMA tile stores: 128-byte rows of 64 bf16 or 32 fp32 per chunk
+        constexpr int CW = EPI == EPI_TMA_BF16 ? 64 : 32;
+        const int out_row = g * p.epi.row_g + sp * p.epi.row_s + mt * BM + quarter * 32;
+        const int out_col0 = g * p.epi.col_g + nt * BN;
+        uint8_t* my_row = stg + lane * 128;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += CW) {
+          uint32_t w[32];  // this lane's 128 bytes of the chunk
+          if (EPI == EPI_TMA_BF16) {
+            uint32_t r0[32], r1[32];
+            tmem_load_32cols(t_base + c0, r0);
+            tmem_load_32cols(t_base + c0 + 32, r1);
+            tmem_load_wait();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              w[j] = pack_bf16x2(r0[2 * j], r0[2 * j + 1]);
+              w[16 + j] = pack_bf16x2(r1[2 * j], r1[2 * j + 1]);
+            }
+          } else {
+            tmem_load_32cols(t_base + c0, w);
+            tmem_load_wait();
+          }
+          if (lane == 0 && stores_pending) bulk_wait_read_all();  // staging free again
+          __syncwarp();
+#pragma unroll
+          for (int q = 0; q < 8; ++q)  // 16-byte chunk q of the row, 128B-swizzled
+            st_shared_v4(my_row + ((q ^ (lane & 7)) << 4), w[4 * q], w[4 * q + 1], w[4 * q + 2],
+                         w[4 * q + 3]);
+          fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmC, stg, out_col0 + c0, out_row);
+            bulk_commit();
+            stores_pending = true;
+          }
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -319,6 +466,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
+    if (EPI != EPI_ROWS && lane == 0 && stores_pending) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -350,35 +498,49 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D bf16 map over a row-major array, box = box_cols x box_rows, 128B swizzle.
-bool make_map(CUtensorMap* map, const TcOperand& op, int box_cols, int box_rows) {
+// 2-D map over a row-major array, box = box_cols x box_rows, 128B swizzle.
+bool make_map(CUtensorMap* map, const void* ptr, long long rows, long long cols, long long pitch,
+              int elem_bytes, int box_cols, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(op.cols), static_cast<cuuint64_t>(op.rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(op.pitch) * 2};
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch) * elem_bytes};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(op.ptr), dims,
-                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  const CUtensorMapDataType dt =
+      elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  CUresult r = fn(map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-template <bool A_MN, bool B_MN, int BN>
+template <bool A_MN, bool B_MN, int BN, bool B_RES, int EPI>
 cudaError_t launch_tc(const TcGemm& g, cudaStream_t stream) {
-  using S = TcShape<BN>;
+  using S = TcShape<BN, B_RES, EPI>;
   static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<A_MN, B_MN, BN>,
+    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<A_MN, B_MN, BN, B_RES, EPI>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  CUtensorMap tmA, tmB;
-  if (!make_map(&tmA, g.A, 64, A_MN ? 64 : BM)) return cudaErrorInvalidValue;
-  if (!make_map(&tmB, g.B, 64, B_MN ? 64 : BN)) return cudaErrorInvalidValue;
+  CUtensorMap tmA, tmB, tmC;
+  if (!make_map(&tmA, g.A.ptr, g.A.rows, g.A.cols, g.A.pitch, 2, 64, A_MN ? 64 : BM))
+    return cudaErrorInvalidValue;
+  if (!make_map(&tmB, g.B.ptr, g.B.rows, g.B.cols, g.B.pitch, 2, 64, B_MN ? 64 : BN))
+    return cudaErrorInvalidValue;
+  if (EPI == EPI_TMA_BF16) {
+    if (!make_map(&tmC, g.epi.out_bf16, g.epi.out_rows, g.epi.ld, g.epi.ld, 2, 64, 32))
+      return cudaErrorInvalidValue;
+  } else if (EPI == EPI_TMA_F32) {
+    if (!make_map(&tmC, g.epi.out_f32, g.epi.out_rows, g.epi.ld, g.epi.ld, 4, 32, 32))
+      return cudaErrorInvalidValue;
+  } else {
+    tmC = tmA;  // unused
+  }
 
   TcKernelArgs p;
   p.m_tiles = (g.M + BM - 1) / BM;
@@ -394,13 +556,25 @@ cudaError_t launch_tc(const TcGemm& g, cudaStream_t stream) {
   p.b_k_per_g = g.B.k_per_g;
   p.epi = g.epi;
   p.status = device_status_ptr();
+  if (B_RES && (p.splits != 1 || p.k_steps_total > S::MAX_RES_KSTEPS))
+    return cudaErrorInvalidValue;
   const long long tiles = static_cast<long long>(p.batches) * p.splits * p.m_tiles * p.n_tiles;
   if (tiles <= 0) return cudaSuccess;
-  const int grid = static_cast<int>(std::min<long long>(tiles, sm_count()));
+  int grid = static_cast<int>(std::min<long long>(tiles, sm_count()));
+  if (B_RES) {  // contiguous runs: launch only the CTAs that get a run
+    const long long per = (tiles + grid - 1) / grid;
+    grid = static_cast<int>((tiles + per - 1) / per);
+  }
   prof_begin(g.tag, stream);
-  tc_gemm_kernel<A_MN, B_MN, BN><<<grid, NUM_THREADS, S::SMEM, stream>>>(tmA, tmB, p);
+  tc_gemm_kernel<A_MN, B_MN, BN, B_RES, EPI>
+      <<<grid, NUM_THREADS, S::SMEM, stream>>>(tmA, tmB, tmC, p);
   prof_end(g.tag, stream);
   return cudaGetLastError();
+}
+
+bool plain_output(const EpiArgs& e) {
+  return e.alpha == 1.f && e.X == nullptr && e.Y == nullptr && e.delta == 0.f &&
+         ((e.out_f32 == nullptr) != (e.out_bf16 == nullptr)) && e.out_rows > 0;
 }
 
 }  // namespace
@@ -416,16 +590,33 @@ cudaError_t tc_gemm_run(const TcGemm& g, cudaStream_t stream) {
   if (g.M <= 0 || g.N <= 0 || g.K <= 0 || g.batches <= 0) return cudaSuccess;
   if ((g.BN != 128 && g.BN != 256) || g.N % g.BN != 0) return cudaErrorInvalidValue;
   const bool a = g.A.mn_major, b = g.B.mn_major;
-  if (g.BN == 256) {
-    if (!a && !b) return launch_tc<false, false, 256>(g, stream);
-    if (!a && b) return launch_tc<false, true, 256>(g, stream);
-    if (a && b) return launch_tc<true, true, 256>(g, stream);
-  } else {
-    if (!a && !b) return launch_tc<false, false, 128>(g, stream);
-    if (!a && b) return launch_tc<false, true, 128>(g, stream);
-    if (a && b) return launch_tc<true, true, 128>(g, stream);
+  if (!plain_output(g.epi)) {
+    // general epilogue: the b x b products of the block build and its adjoint
+    if (g.BN != 128 || g.b_resident) return cudaErrorInvalidValue;
+    if (!a && !b) return launch_tc<false, false, 128, false, EPI_ROWS>(g, stream);
+    if (!a && b) return launch_tc<false, true, 128, false, EPI_ROWS>(g, stream);
+    if (a && b) return launch_tc<true, true, 128, false, EPI_ROWS>(g, stream);
+    return cudaErrorInvalidValue;
   }
-  return cudaErrorInvalidValue;  // (MN, K) is not used by the layer
+  const bool bf16_out = g.epi.out_bf16 != nullptr;
+  if (g.b_resident) {  // block-diagonal transforms (bf16 out)
+    if (a || !bf16_out) return cudaErrorInvalidValue;
+    if (g.BN == 256) {
+      if (!b) return launch_tc<false, false, 256, true, EPI_TMA_BF16>(g, stream);
+      return launch_tc<false, true, 256, true, EPI_TMA_BF16>(g, stream);
+    }
+    if (!b) return launch_tc<false, false, 128, true, EPI_TMA_BF16>(g, stream);
+    return launch_tc<false, true, 128, true, EPI_TMA_BF16>(g, stream);
+  }
+  if (g.BN != 256) return cudaErrorInvalidValue;
+  if (bf16_out) {  // the W0 GEMM and its transpose
+    if (!a && !b) return launch_tc<false, false, 256, false, EPI_TMA_BF16>(g, stream);
+    if (!a && b) return launch_tc<false, true, 256, false, EPI_TMA_BF16>(g, stream);
+    return cudaErrorInvalidValue;
+  }
+  // per-block sums over tokens (fp32 split-K partials)
+  if (a && b) return launch_tc<true, true, 256, false, EPI_TMA_F32>(g, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace poetx

@@ -10,9 +10,10 @@ namespace poetx {
 // Where a contraction's result goes: for batch g, K-split s, row r and
 // column c of the (batch-local) result,
 //   v   = alpha * acc + beta * X[off] + gamma * Y[off] + delta * (r == c)
-//   off = g * g_off + s * s_off + r * ld + c
+//   off = (g * row_g + s * row_s + r) * ld + g * col_g + c
 // and v is stored to out_f32[off] and/or out_bf16[off].  Rows r >=
 // row_limit are skipped.  X, Y, out_f32, out_bf16 may each be null.
+// out_rows x ld is the extent of the output array (used for TMA stores).
 struct EpiArgs {
   float alpha = 1.f;
   const float* X = nullptr;
@@ -23,9 +24,9 @@ struct EpiArgs {
   float* out_f32 = nullptr;
   __nv_bfloat16* out_bf16 = nullptr;
   long long ld = 0;
-  long long g_off = 0;
-  long long s_off = 0;
+  int row_g = 0, row_s = 0, col_g = 0;
   int row_limit = 0x7fffffff;
+  long long out_rows = 0;
 };
 
 // ---------------------------------------------------------------- tcgen05
@@ -45,8 +46,11 @@ struct TcOperand {
 struct TcGemm {
   int M = 0, N = 0, K = 0;  // per batch
   int batches = 1;
-  int splits = 1;           // K is split; split s writes at s * epi.s_off
+  int splits = 1;           // K is split; split s writes rows s * epi.row_s on
   int BN = 256;             // 128 or 256
+  // Keep the B operand of a (batch, N tile) resident in shared memory while
+  // the CTA walks consecutive M tiles (needs splits == 1 and BN*K*2 <= 128 KiB).
+  bool b_resident = false;
   TcOperand A, B;
   EpiArgs epi;
   const char* tag = "tc_gemm";  // name under which launches are profiled
@@ -73,9 +77,10 @@ struct SimtGemm {
 cudaError_t simt_gemm_run(const SimtGemm& g, cudaStream_t stream);
 
 // ------------------------------------------------------------ elementwise
-// theta [n][b(b-1)/2] -> Q [n][b][b] (fp32 and/or bf16 copies).
-cudaError_t launch_unpack(const float* theta, int n, int b, float* q_f32, __nv_bfloat16* q_bf16,
-                          cudaStream_t s);
+// Packed parameters of two sides (theta_a: n_a blocks, theta_b: n_b blocks;
+// theta_b may be null when n_b = 0) -> Q [n_a + n_b][b][b], fp32 and/or bf16.
+cudaError_t launch_unpack(const float* theta_a, int n_a, const float* theta_b, int n_b, int b,
+                          float* q_f32, __nv_bfloat16* q_bf16, cudaStream_t s);
 // out = Q + I in the requested type (k = 0 blocks).
 cudaError_t launch_identity_plus(const float* q, int n, int b, float* out_f32,
                                  __nv_bfloat16* out_bf16, cudaStream_t s);
@@ -87,9 +92,10 @@ cudaError_t launch_expand_superblocks(const __nv_bfloat16* blocks, int n, int b,
 // sb = g*b/S) -> fp32 and/or bf16 [n][b][b].
 cudaError_t launch_reduce_extract(const float* part, int splits, int n, int b, int S,
                                   float* out_f32, __nv_bfloat16* out_bf16, cudaStream_t s);
-// dtheta[g][idx(i,j)] = M[g][i][j] - M[g][j][i] with M = A (+ B if B != null).
-cudaError_t launch_pack_skew(const float* A, const float* B, int n, int b, float* dtheta,
-                             cudaStream_t s);
+// dtheta[g][idx(i,j)] = M[g][i][j] - M[g][j][i] with M = A (+ B if B != null),
+// for n_a + n_b blocks: the first n_a go to dtheta_a, the rest to dtheta_b.
+cudaError_t launch_pack_skew(const float* A, const float* B, int n_a, int n_b, int b,
+                             float* dtheta_a, float* dtheta_b, cudaStream_t s);
 cudaError_t launch_f32_to_bf16(const float* in, long long count, __nv_bfloat16* out,
                                cudaStream_t s);
 

@@ -70,7 +70,8 @@ __global__ void __launch_bounds__(SIMT_THREADS) simt_gemm_kernel(const SimtGemm 
     for (int j = 0; j < 4; ++j) {
       const int n = n0 + tx * 4 + j;
       if (n >= p.N) continue;
-      const long long off = static_cast<long long>(g) * e.g_off + static_cast<long long>(m) * e.ld + n;
+      const long long off =
+          (static_cast<long long>(g) * e.row_g + m) * e.ld + static_cast<long long>(g) * e.col_g + n;
       float v = e.alpha * acc[i][j];
       if (e.X != nullptr) v += e.beta * e.X[off];
       if (e.Y != nullptr) v += e.gamma * e.Y[off];
@@ -82,34 +83,40 @@ __global__ void __launch_bounds__(SIMT_THREADS) simt_gemm_kernel(const SimtGemm 
 }
 
 // Position of Q[i][j] (i < j) in the row-by-row packed strict upper triangle.
-__device__ __forceinline__ long long packed_pos(int i, int j, int b) {
-  return static_cast<long long>(i) * b - static_cast<long long>(i) * (i + 1) / 2 + (j - i - 1);
+__device__ __forceinline__ int packed_pos(int i, int j, int b) {
+  return i * b - (i * (i + 1)) / 2 + (j - i - 1);
 }
 
-__global__ void unpack_kernel(const float* __restrict__ theta, int n, int b,
+// Index arithmetic below is 32-bit: the host guarantees n * b * b < 2^31.
+// Blocks [0, n_a) come from theta_a, blocks [n_a, n_a + n_b) from theta_b.
+__global__ void unpack_kernel(const float* __restrict__ theta_a, int n_a,
+                              const float* __restrict__ theta_b, int b, int total,
                               float* __restrict__ q32, __nv_bfloat16* __restrict__ q16) {
-  const long long total = static_cast<long long>(n) * b * b;
-  const long long m = static_cast<long long>(b) * (b - 1) / 2;
-  for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
-       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int j = static_cast<int>(idx % b);
-    const int i = static_cast<int>((idx / b) % b);
-    const long long g = idx / (static_cast<long long>(b) * b);
+  const int bb = b * b;
+  const int m = b * (b - 1) / 2;
+  for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += gridDim.x * blockDim.x) {
+    const int g = idx / bb;
+    const int rem = idx - g * bb;
+    const int i = rem / b;
+    const int j = rem - i * b;
+    const float* th = g < n_a ? theta_a + g * m : theta_b + (g - n_a) * m;
     float v = 0.f;
-    if (i < j) v = theta[g * m + packed_pos(i, j, b)];
-    else if (i > j) v = -theta[g * m + packed_pos(j, i, b)];
+    if (i < j) v = th[packed_pos(i, j, b)];
+    else if (i > j) v = -th[packed_pos(j, i, b)];
     if (q32 != nullptr) q32[idx] = v;
     if (q16 != nullptr) q16[idx] = __float2bfloat16_rn(v);
   }
 }
 
-__global__ void identity_plus_kernel(const float* __restrict__ q, int n, int b,
+__global__ void identity_plus_kernel(const float* __restrict__ q, int b, int total,
                                      float* __restrict__ o32, __nv_bfloat16* __restrict__ o16) {
-  const long long total = static_cast<long long>(n) * b * b;
-  for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
-       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int j = static_cast<int>(idx % b);
-    const int i = static_cast<int>((idx / b) % b);
+  const int bb = b * b;
+  for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += gridDim.x * blockDim.x) {
+    const int rem = idx % bb;
+    const int i = rem / b;
+    const int j = rem - i * b;
     const float v = q[idx] + (i == j ? 1.f : 0.f);
     if (o32 != nullptr) o32[idx] = v;
     if (o16 != nullptr) o16[idx] = __float2bfloat16_rn(v);
@@ -117,38 +124,38 @@ __global__ void identity_plus_kernel(const float* __restrict__ q, int n, int b,
 }
 
 __global__ void expand_superblocks_kernel(const __nv_bfloat16* __restrict__ blocks, int n, int b,
-                                          int S, __nv_bfloat16* __restrict__ out) {
+                                          int S, int total, __nv_bfloat16* __restrict__ out) {
   const int per = S / b;
-  const int nsb = (n + per - 1) / per;
-  const long long total = static_cast<long long>(nsb) * S * S;
-  for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
-       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int c = static_cast<int>(idx % S);
-    const int r = static_cast<int>((idx / S) % S);
-    const long long sb = idx / (static_cast<long long>(S) * S);
+  for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += gridDim.x * blockDim.x) {
+    const int c = idx % S;
+    const int r = (idx / S) % S;
+    const int sb = idx / (S * S);
     __nv_bfloat16 v = __float2bfloat16_rn(0.f);
-    const long long gblk = sb * per + r / b;
-    if (r / b == c / b && gblk < n)
-      v = blocks[(gblk * b + (r % b)) * b + (c % b)];
+    const int gblk = sb * per + r / b;
+    if (r / b == c / b && gblk < n) v = blocks[(gblk * b + (r % b)) * b + (c % b)];
     out[idx] = v;
   }
 }
 
+// out[g] (g < n) = sum over splits of the diagonal b-block of superblock
+// g / (S/b) in part [splits][nsb][S][S].
 __global__ void reduce_extract_kernel(const float* __restrict__ part, int splits, int n, int b,
-                                      int S, float* __restrict__ o32,
+                                      int S, int total, float* __restrict__ o32,
                                       __nv_bfloat16* __restrict__ o16) {
   const int per = S / b;
   const int nsb = (n + per - 1) / per;
   const long long split_stride = static_cast<long long>(nsb) * S * S;
-  const long long total = static_cast<long long>(n) * b * b;
-  for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
-       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int j = static_cast<int>(idx % b);
-    const int i = static_cast<int>((idx / b) % b);
-    const long long g = idx / (static_cast<long long>(b) * b);
-    const long long sb = g / per;
-    const int off = static_cast<int>(g % per) * b;
-    const long long src = (sb * S + off + i) * S + off + j;
+  const int bb = b * b;
+  for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += gridDim.x * blockDim.x) {
+    const int g = idx / bb;
+    const int rem = idx - g * bb;
+    const int i = rem / b;
+    const int j = rem - i * b;
+    const int sb = g / per;
+    const int off = (g - sb * per) * b;
+    const long long src = (static_cast<long long>(sb) * S + off + i) * S + off + j;
     float v = 0.f;
     for (int s = 0; s < splits; ++s) v += part[s * split_stride + src];
     if (o32 != nullptr) o32[idx] = v;
@@ -156,21 +163,25 @@ __global__ void reduce_extract_kernel(const float* __restrict__ part, int splits
   }
 }
 
-__global__ void pack_skew_kernel(const float* __restrict__ A, const float* __restrict__ B, int n,
-                                 int b, float* __restrict__ dtheta) {
-  const long long total = static_cast<long long>(n) * b * b;
-  const long long m = static_cast<long long>(b) * (b - 1) / 2;
-  for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
-       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int j = static_cast<int>(idx % b);
-    const int i = static_cast<int>((idx / b) % b);
+// dtheta[g][idx(i,j)] = M[g][i][j] - M[g][j][i], M = A (+ B): one thread per
+// (g, i, j) with i < j; blocks [0, n_a) go to dtheta_a, the rest to dtheta_b.
+__global__ void pack_skew_kernel(const float* __restrict__ A, const float* __restrict__ B, int n_a,
+                                 int b, int total, float* __restrict__ dtheta_a,
+                                 float* __restrict__ dtheta_b) {
+  const int m = b * (b - 1) / 2;
+  const int bb = b * b;
+  for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += gridDim.x * blockDim.x) {
+    const int g = idx / bb;
+    const int rem = idx - g * bb;
+    const int i = rem / b;
+    const int j = rem - i * b;
     if (i >= j) continue;
-    const long long g = idx / (static_cast<long long>(b) * b);
-    const long long ij = idx;
-    const long long ji = (g * b + j) * b + i;
-    float v = A[ij] - A[ji];
-    if (B != nullptr) v += B[ij] - B[ji];
-    dtheta[g * m + packed_pos(i, j, b)] = v;
+    const int ji = g * bb + j * b + i;
+    float v = A[idx] - A[ji];
+    if (B != nullptr) v += B[idx] - B[ji];
+    if (g < n_a) dtheta_a[g * m + packed_pos(i, j, b)] = v;
+    else dtheta_b[(g - n_a) * m + packed_pos(i, j, b)] = v;
   }
 }
 
@@ -214,36 +225,38 @@ cudaError_t simt_gemm_run(const SimtGemm& g, cudaStream_t stream) {
     return cudaGetLastError();                                           \
   } while (0)
 
-cudaError_t launch_unpack(const float* theta, int n, int b, float* q32, __nv_bfloat16* q16,
-                          cudaStream_t s) {
-  POETX_EW_LAUNCH("unpack", static_cast<long long>(n) * b * b, unpack_kernel, theta, n, b, q32,
-                  q16);
+cudaError_t launch_unpack(const float* theta_a, int n_a, const float* theta_b, int n_b, int b,
+                          float* q32, __nv_bfloat16* q16, cudaStream_t s) {
+  const int total = (n_a + n_b) * b * b;
+  POETX_EW_LAUNCH("unpack", total, unpack_kernel, theta_a, n_a, theta_b, b, total, q32, q16);
 }
 
 cudaError_t launch_identity_plus(const float* q, int n, int b, float* o32, __nv_bfloat16* o16,
                                  cudaStream_t s) {
-  POETX_EW_LAUNCH("identity_plus", static_cast<long long>(n) * b * b, identity_plus_kernel, q, n,
-                  b, o32, o16);
+  const int total = n * b * b;
+  POETX_EW_LAUNCH("identity_plus", total, identity_plus_kernel, q, b, total, o32, o16);
 }
 
 cudaError_t launch_expand_superblocks(const __nv_bfloat16* blocks, int n, int b, int S,
                                       __nv_bfloat16* out, cudaStream_t s) {
   const int per = S / b;
-  const long long nsb = (n + per - 1) / per;
-  POETX_EW_LAUNCH("expand_superblocks", nsb * S * S, expand_superblocks_kernel, blocks, n, b, S,
+  const int nsb = (n + per - 1) / per;
+  const int total = nsb * S * S;
+  POETX_EW_LAUNCH("expand_superblocks", total, expand_superblocks_kernel, blocks, n, b, S, total,
                   out);
 }
 
 cudaError_t launch_reduce_extract(const float* part, int splits, int n, int b, int S, float* o32,
                                   __nv_bfloat16* o16, cudaStream_t s) {
-  POETX_EW_LAUNCH("reduce_extract", static_cast<long long>(n) * b * b, reduce_extract_kernel,
-                  part, splits, n, b, S, o32, o16);
+  const int total = n * b * b;
+  POETX_EW_LAUNCH("reduce_extract", total, reduce_extract_kernel, part, splits, n, b, S, total,
+                  o32, o16);
 }
 
-cudaError_t launch_pack_skew(const float* A, const float* B, int n, int b, float* dtheta,
-                             cudaStream_t s) {
-  POETX_EW_LAUNCH("pack_skew", static_cast<long long>(n) * b * b, pack_skew_kernel, A, B, n, b,
-                  dtheta);
+cudaError_t launch_pack_skew(const float* A, const float* B, int n_a, int n_b, int b,
+                             float* dtheta_a, float* dtheta_b, cudaStream_t s) {
+  const int total = (n_a + n_b) * b * b;
+  POETX_EW_LAUNCH("pack_skew", total, pack_skew_kernel, A, B, n_a, b, total, dtheta_a, dtheta_b);
 }
 
 cudaError_t launch_f32_to_bf16(const float* in, long long count, __nv_bfloat16* out,
