@@ -146,6 +146,24 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------ ranks
+
+def max_over_ranks(x, device="cpu"):
+    """Largest value of x over all ranks (x itself without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank, world, ms_max):
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return tokens_per_rank * world / (ms_max * 1e-3)
+
+
 # -------------------------------------------------------------- GPU arm
 
 class ClockSampler:
@@ -209,6 +227,31 @@ def load_peaks():
         return d, "measured"
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, \
         "fallback"
+
+
+def source_hash():
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "orthogonal_reparameterized_packed_gb300",
+                                           "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def captured_traffic(workload, tag):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    summary is for other sources or another workload."""
+    p = os.path.join(ROOT, "profiles", f"traffic_{workload}.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    k = d.get("kernels", {}).get(tag)
+    if k is None or d.get("source_hash") != source_hash():
+        return None
+    return k["dram_read"] + k["dram_write"]
 
 
 def algorithmic_work(tag, w):
@@ -309,10 +352,7 @@ def run_gpu(args):
     clk = clocks.stop()
     launches = launches_per_step * args.steps
     ms = t0.elapsed_time(t1) / args.steps
-    ms_t = torch.tensor([ms], device="cuda")
-    if world > 1:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
+    ms_max = max_over_ranks(ms, "cuda")
     status = poetx.poetx_device_status()
 
     # per-kernel times over the timed region
@@ -332,7 +372,8 @@ def run_gpu(args):
     peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
     achieved = amount / avg_s
     roofline = {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": captured_traffic(name, dom),
                 "peak_source": f"{peak_src} ({'sustained' if long_region else 'burst'})",
                 "per_launch": f"2*T*d_in*d_out = {amount:.4f} TFLOP",
                 "timing": "CUDA events around each launch, eager pass of the same K steps"}
@@ -342,7 +383,7 @@ def run_gpu(args):
     step_flop = T * (4.0 * di * do + 6.0 * b * (di + do))
 
     total_tokens = world * w["tokens"]
-    value = total_tokens / (ms_max * 1e-3)
+    value = job_throughput(w["tokens"], world, ms_max)
 
     # end to end through the C ABI from pinned host buffers
     e2e = None
@@ -372,11 +413,8 @@ def run_gpu(args):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        ems = e0.elapsed_time(e1) / ksteps
-        et = torch.tensor([ems], device="cuda")
-        if world > 1:
-            dist.all_reduce(et, op=dist.ReduceOp.MAX)
-        e2e = {"value": total_tokens / (float(et.item()) * 1e-3), "unit": UNIT,
+        ems = max_over_ranks(e0.elapsed_time(e1) / ksteps, "cuda")
+        e2e = {"value": job_throughput(w["tokens"], world, ems), "unit": UNIT,
                "h2d_bytes_per_step": hx.numel() * hx.element_size() +
                hdy.numel() * hdy.element_size(),
                "d2h_bytes_per_step": (hP.numel() + hR.numel()) * 4,
