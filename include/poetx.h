@@ -90,6 +90,26 @@ poetx_status poetx_build_blocks(const float* theta, int d, int b, int k, poetx_d
                                 void* blocks, void* workspace, size_t workspace_bytes,
                                 poetx_stream stream);
 
+/* Block build for callers that cannot allocate device memory.  The paper has
+ * no counterpart: this is a convenience of this library.  Callers running
+ * under a memory plan that forbids new allocations, or that own every
+ * device buffer and have no workspace to offer, can build blocks here
+ * without passing a workspace.  Same arithmetic and kernels as
+ * poetx_build_blocks; the scratch is one fixed device array of the library
+ * (12 MiB + 1 KiB, held on every GPU that loads the library until the
+ * process exits), so:
+ *   - (d/b) * b * b = d * b must be <= 2^20 (e.g. d = 4096 with b = 256);
+ *     larger builds return POETX_ERR_WORKSPACE before anything is enqueued;
+ *   - the first call on each device looks up that array's device address
+ *     (cudaGetSymbolAddress) with the device current; make that first call
+ *     before any stream capture;
+ *   - calls share the array: calls that overlap on the GPU (other streams
+ *     or host threads on the same device) race and must be serialised;
+ *     nothing needs to be zeroed between calls.
+ * Allocates no device memory. */
+poetx_status poetx_build_blocks_noalloc(const float* theta, int d, int b, int k, poetx_dtype dtype,
+                                        void* blocks, poetx_stream stream);
+
 /* ------------------------------------------------------------------------
  * Forward: y_t = R (W0 (P x_t)) (technical summary, section 2,
  * "Input-zentrische Implementierung" and the block-diagonal bullet).

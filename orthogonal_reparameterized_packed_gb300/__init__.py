@@ -15,6 +15,7 @@ import os
 __all__ = [
     "PoetxError", "load_library", "F32", "BF16",
     "poetx_packed_size", "poetx_build_workspace_size", "poetx_build_blocks",
+    "poetx_build_blocks_noalloc",
     "poetx_forward_workspace_size", "poetx_forward",
     "poetx_backward_workspace_size", "poetx_backward",
     "poetx_transform_workspace_size", "poetx_transform_forward", "poetx_transform_backward",
@@ -39,6 +40,8 @@ _SIGNATURES = {
     "poetx_build_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
     "poetx_build_blocks": (_c_int, [_c_ptr, _c_int, _c_int, _c_int, _c_int, _c_ptr, _c_ptr,
                                     _c_size, _c_ptr]),
+    "poetx_build_blocks_noalloc": (_c_int, [_c_ptr, _c_int, _c_int, _c_int, _c_int, _c_ptr,
+                                            _c_ptr]),
     "poetx_forward_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_i64, _c_int]),
     "poetx_forward": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_int,
                                _c_int, _c_i64, _c_int, _c_ptr, _c_size, _c_ptr]),
@@ -130,6 +133,14 @@ def poetx_build_blocks(theta, d, b, k, dtype, blocks, workspace, stream=None):
     _check("poetx_build_blocks", load_library().poetx_build_blocks(
         _ptr(theta), d, b, k, dtype, _ptr(blocks), _ptr(workspace), _nbytes(workspace),
         _stream(stream)))
+
+
+def poetx_build_blocks_noalloc(theta, d, b, k, dtype, blocks, stream=None):
+    """Block build without a workspace, for callers that cannot allocate
+    device memory (scratch is the library's fixed device array; d * b must be
+    at most 2^20; calls that overlap on the GPU race on that array)."""
+    _check("poetx_build_blocks_noalloc", load_library().poetx_build_blocks_noalloc(
+        _ptr(theta), d, b, k, dtype, _ptr(blocks), _stream(stream)))
 
 
 def poetx_forward_workspace_size(d_in, d_out, b, tokens, dtype) -> int:

@@ -644,6 +644,62 @@ const void* superblocks_or_blocks(const void* blocks, bf16* sb, int d, int b, bo
 }  // namespace
 }  // namespace poetx
 
+
+// ===================================================== block build, no alloc
+//
+// Some callers cannot allocate device memory at the point where they need
+// the block build: code running under an allocator that forbids new
+// allocations (a static memory plan, a real-time loop, or an embedding
+// framework that owns every device buffer and hands out only the tensors
+// it planned), or a caller that simply has no workspace to offer.  For them
+// poetx_build_blocks_noalloc runs the same kernels as poetx_build_blocks
+// but takes its scratch from one file-scope device array of fixed size,
+// created when the library's module is loaded on a GPU and held by every
+// GPU that loads the library until the process exits.
+//
+// Host code may not use that array's name as a device address (in host
+// code it names a host-side stand-in), so the device address is looked up
+// with cudaGetSymbolAddress once per device, with that device current, on
+// the first call made on it, and handed to the kernels.
+//
+// Every call shares the one array and the array keeps whatever the last call
+// left in it.  The build needs no part of it to start at zero: every word a
+// call reads was written earlier in the same call.  Calls that overlap on
+// the GPU (different streams, or different host threads, on one device)
+// race on the array and must be serialised by the caller.
+
+namespace poetx {
+namespace {
+
+// Largest build served: (d/b) * b * b = d * b <= 2^20 elements, e.g. d = 4096
+// with b = 256, d = 2048 with b = 512 or d = 8192 with b = 128.  At that size
+// the fp32 path needs three fp32 b x b stacks (12 MiB) and the bf16
+// tensor-core path one fp32 and three bf16 stacks (10 MiB).
+constexpr long long kNoAllocMaxElems = 1ll << 20;
+constexpr size_t kNoAllocScratchBytes = (12u << 20) + 1024;
+
+static __device__ __align__(256) unsigned char g_build_scratch[kNoAllocScratchBytes];
+
+std::mutex g_scratch_mu;
+
+// Device address of g_build_scratch on the current device (nullptr on
+// failure); looked up once per device.
+void* build_scratch_address() {
+  static void* addr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_build_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+}  // namespace
+}  // namespace poetx
+
 using namespace poetx;
 
 // ====================================================================== ABI
@@ -956,4 +1012,25 @@ int poetx_profile_query(const char* tag, int* count, double* total_ms) {
   return 0;
 }
 
+poetx_status poetx_build_blocks_noalloc(const float* theta, int d, int b, int k, poetx_dtype dtype,
+                                        void* blocks, poetx_stream stream) {
+  const bool is_bf16 = dtype == POETX_BF16;
+  poetx_status st = check_common(b, k, 0, dtype);
+  if (st != POETX_OK) return st;
+  if ((st = check_dims(d, b, is_bf16)) != POETX_OK) return st;
+  if (theta == nullptr || blocks == nullptr || !aligned16(theta) || !aligned16(blocks))
+    return POETX_ERR_INVALID_ARG;
+  if (static_cast<long long>(d) * b > kNoAllocMaxElems) return POETX_ERR_WORKSPACE;
+  Carver dry(nullptr);
+  carve_build(dry, d / b, b, tc_small(is_bf16, b));
+  if (dry.off > kNoAllocScratchBytes) return POETX_ERR_WORKSPACE;
+  void* scratch = build_scratch_address();
+  if (scratch == nullptr) return POETX_ERR_CUDA;
+  Carver c(scratch);
+  BuildBufs w = carve_build(c, d / b, b, tc_small(is_bf16, b));
+  return to_status(
+      run_build(theta, d / b, b, k, is_bf16, blocks, w, static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"
+
