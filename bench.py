@@ -318,19 +318,25 @@ def run_gpu(args):
     # (2) the same step captured once in a CUDA graph and replayed: the timed
     #     region of the headline number (no host launch overhead between kernels)
     graph = None
+    graph_error = None
     if not args.no_graph:
-        side = torch.cuda.Stream()
-        side.wait_stream(stream)
-        with torch.cuda.stream(side):
-            step()
-        stream.wait_stream(side)
-        torch.cuda.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            step()
-        for _ in range(3):
-            graph.replay()
-        torch.cuda.synchronize()
+        try:
+            side = torch.cuda.Stream()
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                step()
+            stream.wait_stream(side)
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                step()
+            for _ in range(3):
+                graph.replay()
+            torch.cuda.synchronize()
+        except Exception as exc:  # capture refused: time eager launches instead
+            graph = None
+            graph_error = repr(exc)[:200]
+            torch.cuda.synchronize()
 
     def run_step():
         if graph is not None:
@@ -358,7 +364,7 @@ def run_gpu(args):
     # per-kernel times over the timed region
     tags = ["build", "unpack", "identity_plus", "expand_superblocks", "transform",
             "transform_t", "gemm_w0", "gemm_w0_dgrad", "outer", "reduce_extract", "cnp_bwd",
-            "pack_skew", "f32_to_bf16"]
+            "pack_skew", "f32_to_bf16", "chain"]
     kernels = {}
     for t in tags:
         n, tot = poetx.poetx_profile_query(t)
@@ -430,6 +436,7 @@ def run_gpu(args):
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "bf16", "data": "synthetic", "config": config_json(name, w, world),
                 "gpu_launches": launches, "launch": "cuda_graph" if graph is not None else "eager",
+                "graph_error": graph_error,
                 "ms_per_step_eager": ms_eager, "roofline": roofline,
                 "step_tflops": step_flop / (ms_max * 1e-3) / 1e12,
                 "kernels": kernels, "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,

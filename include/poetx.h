@@ -173,6 +173,13 @@ poetx_status poetx_transform_backward(const void* dout, const void* x, const flo
  * POETX_ERR_CUDA if the device reports an error. */
 poetx_status poetx_device_status(void);
 
+/* Self-check of the timeout path: enqueues one kernel whose barrier wait is
+ * never satisfied; after limit_us microseconds (1..10^6) the wait gives up,
+ * records POETX_ERR_TIMEOUT in the status word and the kernel returns.  A
+ * following poetx_device_status() reports POETX_ERR_TIMEOUT once and the
+ * context stays usable.  (No counterpart on the pages: library plumbing.) */
+poetx_status poetx_selftest_wait_timeout(unsigned int limit_us, poetx_stream stream);
+
 /* Total number of kernels this library has launched in this process. */
 long long poetx_launch_count(void);
 

@@ -19,7 +19,7 @@ __all__ = [
     "poetx_forward_workspace_size", "poetx_forward",
     "poetx_backward_workspace_size", "poetx_backward",
     "poetx_transform_workspace_size", "poetx_transform_forward", "poetx_transform_backward",
-    "poetx_device_status", "poetx_launch_count", "poetx_profile_start", "poetx_profile_stop",
+    "poetx_device_status", "poetx_selftest_wait_timeout", "poetx_launch_count", "poetx_profile_start", "poetx_profile_stop",
     "poetx_profile_query", "poetx_status_string", "EXPORTED_SYMBOLS",
 ]
 
@@ -57,6 +57,7 @@ _SIGNATURES = {
                                           _c_int, _c_int, _c_i64, _c_int, _c_ptr, _c_size,
                                           _c_ptr]),
     "poetx_device_status": (_c_int, []),
+    "poetx_selftest_wait_timeout": (_c_int, [ctypes.c_uint, _c_ptr]),
     "poetx_launch_count": (ctypes.c_longlong, []),
     "poetx_profile_start": (_c_int, [_c_int]),
     "poetx_profile_stop": (None, []),
@@ -186,6 +187,12 @@ def poetx_transform_backward(dout, x, theta, blocks, dx, dtheta, d, b, k, tokens
 
 def poetx_device_status() -> int:
     return load_library().poetx_device_status()
+
+
+def poetx_selftest_wait_timeout(limit_us: int, stream=None) -> None:
+    """Enqueue the self-check kernel whose barrier wait must time out."""
+    _check("poetx_selftest_wait_timeout",
+           load_library().poetx_selftest_wait_timeout(limit_us, _stream(stream)))
 
 
 def poetx_launch_count() -> int:

@@ -407,6 +407,7 @@ struct BuildBufs {
   bf16* q16 = nullptr;
   float* e32[2] = {nullptr, nullptr};
   bf16* e16[2] = {nullptr, nullptr};
+  unsigned int* counter = nullptr;  // grid barrier of the chain launch
 };
 
 BuildBufs carve_build(Carver& c, int n, int b, bool tc) {
@@ -417,6 +418,7 @@ BuildBufs carve_build(Carver& c, int n, int b, bool tc) {
     w.q16 = c.take<bf16>(nbb);
     w.e16[0] = c.take<bf16>(nbb);
     w.e16[1] = c.take<bf16>(nbb);
+    w.counter = c.take<unsigned int>(1);
   } else {
     w.e32[0] = c.take<float>(nbb);
     w.e32[1] = c.take<float>(nbb);
@@ -427,6 +429,9 @@ BuildBufs carve_build(Carver& c, int n, int b, bool tc) {
 cudaError_t run_build(const float* theta, int n, int b, int k, bool is_bf16, void* blocks,
                       const BuildBufs& w, cudaStream_t s) {
   const bool tc = tc_small(is_bf16, b);
+  if (tc && k <= kChainMaxK)  // the whole recursion in one cooperative launch
+    return chain_build(theta, n, b, k, w.q32, w.q16, w.e16[0], w.e16[1], w.counter,
+                       static_cast<bf16*>(blocks), s);
   CK(launch_unpack(theta, n, nullptr, 0, b, w.q32, tc ? w.q16 : nullptr, s));
   float* out32 = is_bf16 ? nullptr : static_cast<float*>(blocks);
   bf16* out16 = is_bf16 ? static_cast<bf16*>(blocks) : nullptr;
@@ -464,6 +469,7 @@ struct CnpBufs {
   float* g32[2] = {nullptr, nullptr};
   bf16* g16[2] = {nullptr, nullptr};
   float* dq = nullptr;
+  unsigned int* counter = nullptr;
 };
 
 CnpBufs carve_cnp(Carver& c, int n, int b, int k, bool tc) {
@@ -482,7 +488,45 @@ CnpBufs carve_cnp(Carver& c, int n, int b, int k, bool tc) {
     if (tc) w.g16[j] = c.take<bf16>(nbb);
   }
   w.dq = c.take<float>(nbb);
+  if (tc) w.counter = c.take<unsigned int>(1);
   return w;
+}
+
+bool use_chain(bool is_bf16, int b, int k) { return tc_small(is_bf16, b) && k <= kChainMaxK; }
+
+// The adjoint chain for blocks [0, n_a) (side a) and [n_a, n_a + n_b) (side b)
+// from the split-K partials of the transposed block gradients.
+cudaError_t chain_adjoint_from_parts(const float* theta_a, int n_a, const float* part_a,
+                                     int splits_a, const float* theta_b, int n_b,
+                                     const float* part_b, int splits_b, int b, int k,
+                                     const CnpBufs& w, float* dtheta_a, float* dtheta_b,
+                                     cudaStream_t s) {
+  ChainAdjointArgs a;
+  a.n_a = n_a;
+  a.n_b = n_b;
+  a.b = b;
+  a.k = k;
+  a.theta_a = theta_a;
+  a.theta_b = theta_b;
+  a.q32 = w.q32;
+  a.q16 = w.q16;
+  for (int i = 2; i <= k; ++i) a.e16[i] = w.e16[i];
+  a.f32[0] = w.g32[0];
+  a.f32[1] = w.g32[1];
+  a.f16[0] = w.g16[0];
+  a.f16[1] = w.g16[1];
+  a.d32 = w.dq;
+  a.S = superblock(b);
+  a.part_a = part_a;
+  a.splits_a = splits_a;
+  a.nsb_a = n_a * b / a.S;
+  a.part_b = part_b;
+  a.splits_b = splits_b;
+  a.nsb_b = n_b * b / a.S;
+  a.dtheta_a = dtheta_a;
+  a.dtheta_b = dtheta_b;
+  a.counter = w.counter;
+  return chain_adjoint(a, s);
 }
 
 // Input: the block gradients G of n = n_a + n_b blocks in w.g32[0] (and
@@ -588,6 +632,7 @@ cudaError_t run_forward_uv(const void* x, const void* W0, const void* psb, void*
 struct BwdPlan {
   SideBufs sb;
   CnpBufs cnp;
+  float* part_out = nullptr;  // chain mode: the R side's partials live until the chain
   int splits_in = 1, splits_out = 1;
 };
 
@@ -610,7 +655,12 @@ BwdPlan carve_backward(Carver& c, int d_in, int d_out, int b, int k, long long T
     p.splits_out = outer_splits(d_out, S, T);
     const long long part_in = static_cast<long long>(p.splits_in) * d_in * S;
     const long long part_out = static_cast<long long>(p.splits_out) * d_out * S;
-    p.sb.part = c.take<float>(static_cast<size_t>(part_in > part_out ? part_in : part_out));
+    if (use_chain(is_bf16, b, k)) {
+      p.sb.part = c.take<float>(static_cast<size_t>(part_in));
+      p.part_out = c.take<float>(static_cast<size_t>(part_out));
+    } else {
+      p.sb.part = c.take<float>(static_cast<size_t>(part_in > part_out ? part_in : part_out));
+    }
   }
   p.cnp = carve_cnp(c, (d_in + d_out) / b, b, k, tc_small(is_bf16, b));
   return p;
@@ -858,9 +908,14 @@ poetx_status poetx_backward(const void* dy, const void* x, const void* W0, const
     e = simt_transform(static_cast<const float*>(dy), static_cast<const float*>(rsb),
                        static_cast<float*>(p.sb.dv), d_out, b, tokens, true, "transform_t", s);
   if (e != cudaSuccess) return POETX_ERR_CUDA;
+  const bool chain = use_chain(is_bf16, b, k);
   const long long off_R = static_cast<long long>(d_in) * b;  // R blocks follow the P blocks
-  e = block_gradient(dy, v, d_out, b, tokens, is_bf16, p.sb.part, p.splits_out,
-                     p.cnp.g32[0] + off_R, p.cnp.g16[0] ? p.cnp.g16[0] + off_R : nullptr, s);
+  if (chain)  // G_R^T partials: sum_t v_t dy_t^T per block
+    e = tc_outer(static_cast<const bf16*>(v), static_cast<const bf16*>(dy), p.part_out, d_out,
+                 S, tokens, p.splits_out, s);
+  else
+    e = block_gradient(dy, v, d_out, b, tokens, is_bf16, p.sb.part, p.splits_out,
+                       p.cnp.g32[0] + off_R, p.cnp.g16[0] ? p.cnp.g16[0] + off_R : nullptr, s);
   if (e != cudaSuccess) return POETX_ERR_CUDA;
   // du = dv W0
   if (is_bf16)
@@ -878,6 +933,14 @@ poetx_status poetx_backward(const void* dy, const void* x, const void* W0, const
     e = simt_transform(static_cast<const float*>(p.sb.du), static_cast<const float*>(psb),
                        static_cast<float*>(dx), d_in, b, tokens, true, "transform_t", s);
   if (e != cudaSuccess) return POETX_ERR_CUDA;
+  if (chain) {  // G_P^T partials, then the whole adjoint of both sides in one launch
+    e = tc_outer(static_cast<const bf16*>(x), static_cast<const bf16*>(p.sb.du), p.sb.part, d_in,
+                 S, tokens, p.splits_in, s);
+    if (e != cudaSuccess) return POETX_ERR_CUDA;
+    return to_status(chain_adjoint_from_parts(theta_P, d_in / b, p.sb.part, p.splits_in,
+                                              theta_R, d_out / b, p.part_out, p.splits_out, b, k,
+                                              p.cnp, dtheta_P, dtheta_R, s));
+  }
   e = block_gradient(p.sb.du, x, d_in, b, tokens, is_bf16, p.sb.part, p.splits_in,
                      p.cnp.g32[0], p.cnp.g16[0], s);
   if (e != cudaSuccess) return POETX_ERR_CUDA;
@@ -961,6 +1024,13 @@ poetx_status poetx_transform_backward(const void* dout, const void* x, const flo
     e = simt_transform(static_cast<const float*>(dout), static_cast<const float*>(sb),
                        static_cast<float*>(dx), d, b, tokens, true, "transform_t", s);
   if (e != cudaSuccess) return POETX_ERR_CUDA;
+  if (use_chain(is_bf16, b, k)) {  // G^T partials, then the adjoint in one launch
+    e = tc_outer(static_cast<const bf16*>(x), static_cast<const bf16*>(dout), part, d, S, tokens,
+                 splits, s);
+    if (e != cudaSuccess) return POETX_ERR_CUDA;
+    return to_status(chain_adjoint_from_parts(theta, d / b, part, splits, nullptr, 0, nullptr, 1,
+                                              b, k, cnp, dtheta, nullptr, s));
+  }
   e = block_gradient(dout, x, d, b, tokens, is_bf16, part, splits, cnp.g32[0], cnp.g16[0], s);
   if (e != cudaSuccess) return POETX_ERR_CUDA;
   return to_status(

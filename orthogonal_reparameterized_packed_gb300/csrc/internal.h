@@ -76,6 +76,39 @@ struct SimtGemm {
 };
 cudaError_t simt_gemm_run(const SimtGemm& g, cudaStream_t stream);
 
+// ------------------------------------------------------------ b x b chains
+// One cooperative launch per chain of b x b products (tensor cores, b a
+// multiple of 128, k <= kChainMaxK); see chain_tc.cu.
+constexpr int kChainMaxK = 8;
+
+// blocks = (I + Q)(I + Q + ... + Q^k) for the n blocks of one side, bf16 out.
+// Scratch: q32 [n][b][b] fp32, q16 and e16a/e16b bf16, one counter word.
+cudaError_t chain_build(const float* theta, int n, int b, int k, float* q32, __nv_bfloat16* q16,
+                        __nv_bfloat16* e16a, __nv_bfloat16* e16b, unsigned int* counter,
+                        __nv_bfloat16* blocks, cudaStream_t stream);
+
+// Packed gradients of both sides from the split-K partials of the TRANSPOSED
+// block gradients G^T (blocks [0, n_a) from part_a / theta_a, the rest from
+// part_b / theta_b).  Scratch buffers are [n_a + n_b][b][b].
+struct ChainAdjointArgs {
+  int n_a = 0, n_b = 0, b = 0, k = 0;
+  const float* theta_a = nullptr;
+  const float* theta_b = nullptr;
+  float* q32 = nullptr;
+  __nv_bfloat16* q16 = nullptr;
+  __nv_bfloat16* e16[kChainMaxK + 2] = {};
+  float* f32[2] = {nullptr, nullptr};
+  __nv_bfloat16* f16[2] = {nullptr, nullptr};
+  float* d32 = nullptr;
+  const float* part_a = nullptr;
+  const float* part_b = nullptr;
+  int splits_a = 1, splits_b = 1, nsb_a = 0, nsb_b = 0, S = 0;
+  float* dtheta_a = nullptr;
+  float* dtheta_b = nullptr;
+  unsigned int* counter = nullptr;
+};
+cudaError_t chain_adjoint(const ChainAdjointArgs& a, cudaStream_t stream);
+
 // ------------------------------------------------------------ elementwise
 // Packed parameters of two sides (theta_a: n_a blocks, theta_b: n_b blocks;
 // theta_b may be null when n_b = 0) -> Q [n_a + n_b][b][b], fp32 and/or bf16.
