@@ -150,13 +150,12 @@ poetx_status to_status(cudaError_t e) { return e == cudaSuccess ? POETX_OK : POE
 int superblock(int b) { return b > 256 ? b : 256; }
 bool tc_small(bool is_bf16, int b) { return is_bf16 && b >= 128; }
 
-// The one-launch chains are switched off until their phases beat separate
-// launches (measured: 104 / 333 us per build / adjoint chain against about
-// 40 / 180 us as separate launches on the q/o projection).
-constexpr bool kChainEnabled = false;
+// The b x b chains run as one cooperative launch each where they fit
+// (chain_tc.cu); otherwise as one launch per product.
+constexpr bool kChainEnabled = true;
 
-bool use_chain(bool is_bf16, int b, int k) {
-  return kChainEnabled && tc_small(is_bf16, b) && k <= kChainMaxK;
+bool use_chain(bool is_bf16, int n, int b, int k) {
+  return kChainEnabled && tc_small(is_bf16, b) && chain_fits(n, b, k);
 }
 
 TcOperand op(const void* ptr, long long rows, long long cols, long long pitch, bool mn_major,
@@ -417,17 +416,30 @@ struct BuildBufs {
   float* e32[2] = {nullptr, nullptr};
   bf16* e16[2] = {nullptr, nullptr};
   unsigned int* counter = nullptr;  // grid barrier of the chain launch
+  bf16* q_lo = nullptr;             // chain: bf16 remainder Q - bf16(Q)
+  bf16* two_i = nullptr;            // chain: constant 2I
 };
 
-BuildBufs carve_build(Carver& c, int n, int b, bool tc) {
+// Buffers of one block build: the one-launch chain needs bf16 Q (hi and lo
+// parts), 2I and two bf16 E stacks; the per-product path fp32 Q plus bf16 (tensor
+// cores) or fp32 (FFMA) E stacks.
+BuildBufs carve_build(Carver& c, int n, int b, int k, bool is_bf16) {
   BuildBufs w;
   const size_t nbb = static_cast<size_t>(n) * b * b;
+  if (use_chain(is_bf16, n, b, k)) {
+    w.q16 = c.take<bf16>(nbb);
+    w.q_lo = c.take<bf16>(nbb);
+    w.e16[0] = c.take<bf16>(nbb);
+    w.e16[1] = c.take<bf16>(nbb);
+    w.two_i = c.take<bf16>(static_cast<size_t>(b) * b);
+    w.counter = c.take<unsigned int>(1);
+    return w;
+  }
   w.q32 = c.take<float>(nbb);
-  if (tc) {
+  if (tc_small(is_bf16, b)) {
     w.q16 = c.take<bf16>(nbb);
     w.e16[0] = c.take<bf16>(nbb);
     w.e16[1] = c.take<bf16>(nbb);
-    w.counter = c.take<unsigned int>(1);
   } else {
     w.e32[0] = c.take<float>(nbb);
     w.e32[1] = c.take<float>(nbb);
@@ -438,9 +450,21 @@ BuildBufs carve_build(Carver& c, int n, int b, bool tc) {
 cudaError_t run_build(const float* theta, int n, int b, int k, bool is_bf16, void* blocks,
                       const BuildBufs& w, cudaStream_t s) {
   const bool tc = tc_small(is_bf16, b);
-  if (use_chain(is_bf16, b, k))  // the whole recursion in one cooperative launch
-    return chain_build(theta, n, b, k, w.q32, w.q16, w.e16[0], w.e16[1], w.counter,
-                       static_cast<bf16*>(blocks), s);
+  if (use_chain(is_bf16, n, b, k)) {  // the whole recursion in one cooperative launch
+    ChainBuildArgs a;
+    a.n = n;
+    a.b = b;
+    a.k = k;
+    a.theta = theta;
+    a.q_hi = w.q16;
+    a.q_lo = w.q_lo;
+    a.two_i = w.two_i;
+    a.e16[0] = w.e16[0];
+    a.e16[1] = w.e16[1];
+    a.counter = w.counter;
+    a.blocks = static_cast<bf16*>(blocks);
+    return chain_build(a, s);
+  }
   CK(launch_unpack(theta, n, nullptr, 0, b, w.q32, tc ? w.q16 : nullptr, s));
   float* out32 = is_bf16 ? nullptr : static_cast<float*>(blocks);
   bf16* out16 = is_bf16 ? static_cast<bf16*>(blocks) : nullptr;
@@ -479,6 +503,7 @@ struct CnpBufs {
   bf16* g16[2] = {nullptr, nullptr};
   float* dq = nullptr;
   unsigned int* counter = nullptr;
+  bf16* two_i = nullptr;  // chain: constant 2I
 };
 
 CnpBufs carve_cnp(Carver& c, int n, int b, int k, bool tc) {
@@ -497,7 +522,10 @@ CnpBufs carve_cnp(Carver& c, int n, int b, int k, bool tc) {
     if (tc) w.g16[j] = c.take<bf16>(nbb);
   }
   w.dq = c.take<float>(nbb);
-  if (tc) w.counter = c.take<unsigned int>(1);
+  if (tc) {
+    w.counter = c.take<unsigned int>(1);
+    w.two_i = c.take<bf16>(static_cast<size_t>(b) * b);
+  }
   return w;
 }
 
@@ -517,11 +545,9 @@ cudaError_t chain_adjoint_from_parts(const float* theta_a, int n_a, const float*
   a.k = k;
   a.theta_a = theta_a;
   a.theta_b = theta_b;
-  a.q32 = w.q32;
   a.q16 = w.q16;
+  a.two_i = w.two_i;
   for (int i = 2; i <= k; ++i) a.e16[i] = w.e16[i];
-  a.f32[0] = w.g32[0];
-  a.f32[1] = w.g32[1];
   a.f16[0] = w.g16[0];
   a.f16[1] = w.g16[1];
   a.d32 = w.dq;
@@ -664,7 +690,7 @@ BwdPlan carve_backward(Carver& c, int d_in, int d_out, int b, int k, long long T
     p.splits_out = outer_splits(d_out, S, T);
     const long long part_in = static_cast<long long>(p.splits_in) * d_in * S;
     const long long part_out = static_cast<long long>(p.splits_out) * d_out * S;
-    if (use_chain(is_bf16, b, k)) {
+    if (use_chain(is_bf16, (d_in + d_out) / b, b, k)) {
       p.sb.part = c.take<float>(static_cast<size_t>(part_in));
       p.part_out = c.take<float>(static_cast<size_t>(part_out));
     } else {
@@ -786,7 +812,7 @@ size_t poetx_build_workspace_size(int d, int b, int k, poetx_dtype dtype) {
   const bool is_bf16 = dtype == POETX_BF16;
   if (check_dims(d, b, is_bf16) != POETX_OK || check_common(b, k, 0, dtype) != POETX_OK) return 0;
   Carver c(nullptr);
-  carve_build(c, d / b, b, tc_small(is_bf16, b));
+  carve_build(c, d / b, b, k, is_bf16);
   return c.off;
 }
 
@@ -800,7 +826,7 @@ poetx_status poetx_build_blocks(const float* theta, int d, int b, int k, poetx_d
   if (theta == nullptr || blocks == nullptr || !aligned16(theta) || !aligned16(blocks))
     return POETX_ERR_INVALID_ARG;
   Carver c(workspace);
-  BuildBufs w = carve_build(c, d / b, b, tc_small(is_bf16, b));
+  BuildBufs w = carve_build(c, d / b, b, k, is_bf16);
   if (workspace == nullptr || c.off > workspace_bytes || !aligned16(workspace))
     return POETX_ERR_WORKSPACE;
   return to_status(
@@ -917,7 +943,7 @@ poetx_status poetx_backward(const void* dy, const void* x, const void* W0, const
     e = simt_transform(static_cast<const float*>(dy), static_cast<const float*>(rsb),
                        static_cast<float*>(p.sb.dv), d_out, b, tokens, true, "transform_t", s);
   if (e != cudaSuccess) return POETX_ERR_CUDA;
-  const bool chain = use_chain(is_bf16, b, k);
+  const bool chain = use_chain(is_bf16, (d_in + d_out) / b, b, k);
   const long long off_R = static_cast<long long>(d_in) * b;  // R blocks follow the P blocks
   if (chain)  // G_R^T partials: sum_t v_t dy_t^T per block
     e = tc_outer(static_cast<const bf16*>(v), static_cast<const bf16*>(dy), p.part_out, d_out,
@@ -1033,7 +1059,7 @@ poetx_status poetx_transform_backward(const void* dout, const void* x, const flo
     e = simt_transform(static_cast<const float*>(dout), static_cast<const float*>(sb),
                        static_cast<float*>(dx), d, b, tokens, true, "transform_t", s);
   if (e != cudaSuccess) return POETX_ERR_CUDA;
-  if (use_chain(is_bf16, b, k)) {  // G^T partials, then the adjoint in one launch
+  if (use_chain(is_bf16, d / b, b, k)) {  // G^T partials, then the adjoint in one launch
     e = tc_outer(static_cast<const bf16*>(x), static_cast<const bf16*>(dout), part, d, S, tokens,
                  splits, s);
     if (e != cudaSuccess) return POETX_ERR_CUDA;
@@ -1101,12 +1127,12 @@ poetx_status poetx_build_blocks_noalloc(const float* theta, int d, int b, int k,
     return POETX_ERR_INVALID_ARG;
   if (static_cast<long long>(d) * b > kNoAllocMaxElems) return POETX_ERR_WORKSPACE;
   Carver dry(nullptr);
-  carve_build(dry, d / b, b, tc_small(is_bf16, b));
+  carve_build(dry, d / b, b, k, is_bf16);
   if (dry.off > kNoAllocScratchBytes) return POETX_ERR_WORKSPACE;
   void* scratch = build_scratch_address();
   if (scratch == nullptr) return POETX_ERR_CUDA;
   Carver c(scratch);
-  BuildBufs w = carve_build(c, d / b, b, tc_small(is_bf16, b));
+  BuildBufs w = carve_build(c, d / b, b, k, is_bf16);
   return to_status(
       run_build(theta, d / b, b, k, is_bf16, blocks, w, static_cast<cudaStream_t>(stream)));
 }

@@ -2,22 +2,28 @@
 // as ONE cooperative persistent launch.
 //
 // A chain is a short program of phases executed by every CTA in order:
-//   elementwise phases  (unpack theta -> Q; split-K sums of the token-wise
-//                        block gradients; I + Q; skew pack)  run by the four
-//                        epilogue warps of every CTA, grid-stride;
-//   product phases      1 or 2 problems  out = epi(A_g * B_g^T)  over all
-//                        b x b blocks g, as 128 x 128 tcgen05 tiles
-//                        (A K-major, B MN-major; both read by TMA from the
-//                        row-major [n][b][b] stacks).
+//   elementwise phases  unpack theta -> Q (bf16 hi / lo parts), the split-K
+//                       sums of the token-wise block gradients, the constant
+//                       2I, the skew pack; run by the epilogue warps of every
+//                       CTA, grid-stride, four independent elements per step;
+//   product phases      1 or 2 products over all b x b blocks g, each a sum
+//                       of up to three MMA terms  sum_t A_t(g) * B_t(g)^T
+//                       (A K-major, B MN-major, read by TMA from the
+//                       row-major [n][b][b] stacks or from a constant b x b
+//                       matrix), as 128 x 128 tcgen05 tiles.
+// Addends are MMA terms too (2Q = Q_hi * 2I + Q_lo * 2I, 2F = F * 2I), so
+// epilogues only store.  The adjoint's running sum D stays in TMEM across
+// its phases: each CTA owns the same D tiles in every phase.
+//
 // Phase p+1 may read anything phase p wrote, so phases are separated by a
 // grid barrier: every CTA bumps a global counter when its epilogue warps are
-// done with phase p, and producers / epilogues of phase p+1 wait until the
-// counter reaches (p+1) * gridDim.x.  The launch is cooperative, so all CTAs
-// are resident; every wait is bounded (2 s) and records POETX_ERR_TIMEOUT.
+// done with phase p; producers and epilogues of phase p+1 wait until the
+// counter reaches (p+1) * gridDim.x.  The launch is cooperative (all CTAs
+// resident); every wait is bounded (2 s) and records POETX_ERR_TIMEOUT.
 //
-// This is the "one fused kernel for Q^2, Q^3, Q^4" of the pages' CNP step,
-// extended to the adjoint: a 256 x 256 bf16 operand pair does not fit one
-// SM, so the chain runs on all SMs and synchronises between powers.
+// This is the "Q^2, Q^3, Q^4 in one fused kernel" of the pages' CNP step,
+// extended to the adjoint; a 256 x 256 bf16 operand pair does not fit one
+// SM, so the chain spans all SMs and synchronises between powers.
 #include <algorithm>
 #include <mutex>
 
@@ -35,16 +41,32 @@ constexpr int CH_BN = 128;
 constexpr int CH_A_BYTES = BM * BK * 2;     // 16 KB
 constexpr int CH_B_BYTES = CH_BN * BK * 2;  // 16 KB
 constexpr int CH_SMEM = 1024 + CH_STAGES * (CH_A_BYTES + CH_B_BYTES) + 256;
-constexpr uint32_t CH_TMEM_COLS = 2 * CH_BN;
+constexpr uint32_t CH_TMEM_COLS = 512;  // 2 rotating accumulators + 2 persistent D slots
+constexpr int kMaxDSlots = 2;
 
-enum { OP_GEMM = 0, OP_UNPACK = 1, OP_PREP_BWD = 2, OP_IDENTITY = 3, OP_PACK = 4 };
+enum {
+  OP_GEMM = 0,
+  OP_UNPACK_SPLIT = 1,   // Q -> q_hi, q_lo (bf16); 2I
+  OP_IDENTITY = 2,       // blocks = I + Q straight from theta (k = 0)
+  OP_PREP_BWD = 3,       // Q -> q_hi; F_1 = sum of partials; 2I
+  OP_PACK = 4            // dtheta = sign * (D - D^T) packed
+};
+enum { PROD_STORE = 0, PROD_ACC = 1, PROD_ACC_STORE = 2 };
 
-constexpr int kChainMaxMaps = 40;
-constexpr int kChainMaxPhases = 24;
+constexpr int kChainMaxMaps = 48;
+constexpr int kChainMaxPhases = 20;
+
+struct ChainTerm {
+  int a_map, b_map;  // A: K-major box map, B: MN-major box map
+  int b_batched;     // B rows offset by g * b (0: one constant b x b matrix)
+};
 
 struct ChainProd {
-  int a_map, b_map;  // A: K-major box map, B: MN-major box map
-  EpiArgs epi;
+  int nterms;
+  ChainTerm term[3];
+  int mode;       // PROD_STORE / PROD_ACC / PROD_ACC_STORE
+  int first_acc;  // ACC modes: this phase initialises the persistent slot
+  EpiArgs epi;    // stores only: alpha, delta, out_f32 / out_bf16
 };
 
 struct ChainPhase {
@@ -58,23 +80,21 @@ struct ChainParams {
   ChainPhase phases[kChainMaxPhases];
   int nphases;
   int n, b, n_a;  // blocks, block size, blocks of the first side
-  // elementwise operands
   const float* theta_a;
   const float* theta_b;
-  float* q32;
-  __nv_bfloat16* q16;
-  const float* part_a;  // split-K partials [splits][nsb][S][S] of each side
+  __nv_bfloat16* q_hi;
+  __nv_bfloat16* q_lo;  // builder only
+  __nv_bfloat16* two_i;  // constant 2I, b x b
+  const float* part_a;   // split-K partials [splits][nsb][S][S] of each side
   const float* part_b;
   int splits_a, splits_b, nsb_a, nsb_b, S;
-  float* g32;  // reduced block gradients (fp32 + bf16)
-  __nv_bfloat16* g16;
-  const float* pack_A;
-  const float* pack_B;
+  __nv_bfloat16* f16;  // F_1 (bf16)
+  float* f32;          // F_1 (fp32, k = 0 only)
+  const float* pack_src;
   float pack_sign;
   float* dtheta_a;
   float* dtheta_b;
-  float* id32;
-  __nv_bfloat16* id16;
+  __nv_bfloat16* blocks;  // identity phase output
   unsigned int* counter;
   int* status;
 };
@@ -97,7 +117,7 @@ __device__ bool grid_wait(const ChainParams& P, int phase, volatile int* abort) 
   if (ld_acquire_u32(P.counter) >= target) return true;
   const unsigned long long t0 = global_timer_ns();
   while (true) {
-    __nanosleep(64);
+    __nanosleep(100);
     if (ld_acquire_u32(P.counter) >= target) return true;
     if (*abort) return false;
     if (global_timer_ns() - t0 > kWaitLimitNs) {
@@ -111,51 +131,64 @@ __device__ __forceinline__ int packed_index(int i, int j, int b) {
   return i * b - (i * (i + 1)) / 2 + (j - i - 1);
 }
 
-// Elementwise phases, grid-stride over the n * b * b block entries.
-__device__ void elementwise_phase(const ChainParams& P, int op, int tid, int nthreads) {
-  const int b = P.b, bb = b * b, m = b * (b - 1) / 2;
-  const int total = P.n * bb;
-  for (int idx = tid; idx < total; idx += nthreads) {
-    const int g = idx / bb;
-    const int rem = idx - g * bb;
-    const int i = rem / b;
-    const int j = rem - i * b;
-    const bool side_a = g < P.n_a;
-    if (op == OP_UNPACK || op == OP_PREP_BWD) {
-      const float* th = side_a ? P.theta_a + g * m : P.theta_b + (g - P.n_a) * m;
-      float q = 0.f;
-      if (i < j) q = th[packed_index(i, j, b)];
-      else if (i > j) q = -th[packed_index(j, i, b)];
-      P.q32[idx] = q;
-      P.q16[idx] = __float2bfloat16_rn(q);
-    }
-    if (op == OP_PREP_BWD) {
-      // diagonal b-block of superblock g / (S/b), summed over the K splits
-      const int per = P.S / b;
-      const int gl = side_a ? g : g - P.n_a;
-      const int sb = gl / per;
-      const int off = (gl - sb * per) * b;
-      const float* part = side_a ? P.part_a : P.part_b;
-      const int splits = side_a ? P.splits_a : P.splits_b;
-      const long long stride = static_cast<long long>(side_a ? P.nsb_a : P.nsb_b) * P.S * P.S;
-      const long long src = (static_cast<long long>(sb) * P.S + off + i) * P.S + off + j;
-      float v = 0.f;
-      for (int s = 0; s < splits; ++s) v += part[s * stride + src];
-      P.g32[idx] = v;
-      P.g16[idx] = __float2bfloat16_rn(v);
-    }
+__device__ __forceinline__ float theta_at(const ChainParams& P, int g, int i, int j) {
+  const int b = P.b, m = b * (b - 1) / 2;
+  const float* th = g < P.n_a ? P.theta_a + g * m : P.theta_b + (g - P.n_a) * m;
+  if (i < j) return th[packed_index(i, j, b)];
+  if (i > j) return -th[packed_index(j, i, b)];
+  return 0.f;
+}
+
+// One element of an elementwise phase; all its loads are issued before its
+// stores so four unrolled elements keep four loads in flight.
+__device__ __forceinline__ void elementwise_one(const ChainParams& P, int op, int idx) {
+  const int b = P.b, bb = b * b;
+  const int g = idx / bb;
+  const int rem = idx - g * bb;
+  const int i = rem / b;
+  const int j = rem - i * b;
+  if (op == OP_UNPACK_SPLIT || op == OP_PREP_BWD || op == OP_IDENTITY) {
+    const float q = theta_at(P, g, i, j);
     if (op == OP_IDENTITY) {
-      const float v = P.q32[idx] + (i == j ? 1.f : 0.f);
-      if (P.id32 != nullptr) P.id32[idx] = v;
-      if (P.id16 != nullptr) P.id16[idx] = __float2bfloat16_rn(v);
+      P.blocks[idx] = __float2bfloat16_rn(q + (i == j ? 1.f : 0.f));
+    } else {
+      const __nv_bfloat16 hi = __float2bfloat16_rn(q);
+      P.q_hi[idx] = hi;
+      if (op == OP_UNPACK_SPLIT) P.q_lo[idx] = __float2bfloat16_rn(q - __bfloat162float(hi));
+      if (g == 0) P.two_i[rem] = __float2bfloat16_rn(i == j ? 2.f : 0.f);
     }
-    if (op == OP_PACK && i < j) {
-      const int ji = g * bb + j * b + i;
-      float v = P.pack_A[idx] - P.pack_A[ji];
-      if (P.pack_B != nullptr) v += P.pack_B[idx] - P.pack_B[ji];
-      v *= P.pack_sign;
-      if (side_a) P.dtheta_a[g * m + packed_index(i, j, b)] = v;
-      else P.dtheta_b[(g - P.n_a) * m + packed_index(i, j, b)] = v;
+  }
+  if (op == OP_PREP_BWD) {
+    // diagonal b-block of superblock g / (S/b), summed over the K splits
+    const bool side_a = g < P.n_a;
+    const int per = P.S / b;
+    const int gl = side_a ? g : g - P.n_a;
+    const int sb = gl / per;
+    const int off = (gl - sb * per) * b;
+    const float* part = side_a ? P.part_a : P.part_b;
+    const int splits = side_a ? P.splits_a : P.splits_b;
+    const long long stride = static_cast<long long>(side_a ? P.nsb_a : P.nsb_b) * P.S * P.S;
+    const long long src = (static_cast<long long>(sb) * P.S + off + i) * P.S + off + j;
+    float v = 0.f;
+    for (int s = 0; s < splits; ++s) v += part[s * stride + src];
+    P.f16[idx] = __float2bfloat16_rn(v);
+    if (P.f32 != nullptr) P.f32[idx] = v;
+  }
+  if (op == OP_PACK && i < j) {
+    const float v = P.pack_sign * (P.pack_src[idx] - P.pack_src[g * bb + j * b + i]);
+    const int m = b * (b - 1) / 2;
+    if (g < P.n_a) P.dtheta_a[g * m + packed_index(i, j, b)] = v;
+    else P.dtheta_b[(g - P.n_a) * m + packed_index(i, j, b)] = v;
+  }
+}
+
+__device__ void elementwise_phase(const ChainParams& P, int op, int tid, int nthreads) {
+  const int total = P.n * P.b * P.b;
+  for (int base = tid; base < total; base += 4 * nthreads) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int idx = base + u * nthreads;
+      if (idx < total) elementwise_one(P, op, idx);
     }
   }
 }
@@ -181,9 +214,11 @@ __global__ void __launch_bounds__(CH_THREADS, 1) chain_kernel(const __grid_const
   uint64_t* empty_bar = full_bar + CH_STAGES;
   uint64_t* tfull_bar = empty_bar + CH_STAGES;  // [2]
   uint64_t* tempty_bar = tfull_bar + 2;         // [2]
-  uint64_t* drain_bar = tempty_bar + 2;
+  uint64_t* dfull_bar = tempty_bar + 2;         // [kMaxDSlots]
+  uint64_t* drain_bar = dfull_bar + kMaxDSlots;
   uint64_t* epi_done_bar = drain_bar + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epi_done_bar + 1);
+  uint64_t* go_bar = epi_done_bar + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(go_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32;
@@ -200,8 +235,10 @@ __global__ void __launch_bounds__(CH_THREADS, 1) chain_kernel(const __grid_const
       mbar_init(&tfull_bar[a], 1);
       mbar_init(&tempty_bar[a], 4);
     }
+    for (int d = 0; d < kMaxDSlots; ++d) mbar_init(&dfull_bar[d], 1);
     mbar_init(drain_bar, 1);
     mbar_init(epi_done_bar, 4);
+    mbar_init(go_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -233,24 +270,28 @@ __global__ void __launch_bounds__(CH_THREADS, 1) chain_kernel(const __grid_const
         for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
           int prod, g, mt, nt;
           decode_chain_tile(t, P.n, mtl, ntl, prod, g, mt, nt);
-          const CUtensorMap* ma = &P.maps[PH.prod[prod].a_map];
-          const CUtensorMap* mb = &P.maps[PH.prod[prod].b_map];
-          for (int ks = 0; ks < ksteps; ++ks) {
-            if (!mbar_wait(&empty_bar[stage], phase_bit ^ 1, abort_flag)) {
-              record_timeout(P.status, abort_flag);
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(&full_bar[stage], CH_A_BYTES + CH_B_BYTES);
-            uint8_t* a_dst = sA + stage * CH_A_BYTES;
-            uint8_t* b_dst = sB + stage * CH_B_BYTES;
-            tma_load_2d(a_dst, ma, &full_bar[stage], ks * BK, g * b + mt * BM);
-            tma_load_2d(b_dst, mb, &full_bar[stage], nt * CH_BN, g * b + ks * BK);
-            tma_load_2d(b_dst + 8192, mb, &full_bar[stage], nt * CH_BN + 64, g * b + ks * BK);
-            ++issued;
-            if (++stage == CH_STAGES) {
-              stage = 0;
-              phase_bit ^= 1;
+          const ChainProd& PR = PH.prod[prod];
+          for (int term = 0; term < PR.nterms && ok; ++term) {
+            const CUtensorMap* ma = &P.maps[PR.term[term].a_map];
+            const CUtensorMap* mb = &P.maps[PR.term[term].b_map];
+            const int b_row0 = PR.term[term].b_batched ? g * b : 0;
+            for (int ks = 0; ks < ksteps; ++ks) {
+              if (!mbar_wait(&empty_bar[stage], phase_bit ^ 1, abort_flag)) {
+                record_timeout(P.status, abort_flag);
+                ok = false;
+                break;
+              }
+              mbar_arrive_expect_tx(&full_bar[stage], CH_A_BYTES + CH_B_BYTES);
+              uint8_t* a_dst = sA + stage * CH_A_BYTES;
+              uint8_t* b_dst = sB + stage * CH_B_BYTES;
+              tma_load_2d(a_dst, ma, &full_bar[stage], ks * BK, g * b + mt * BM);
+              tma_load_2d(b_dst, mb, &full_bar[stage], nt * CH_BN, b_row0 + ks * BK);
+              tma_load_2d(b_dst + 8192, mb, &full_bar[stage], nt * CH_BN + 64, b_row0 + ks * BK);
+              ++issued;
+              if (++stage == CH_STAGES) {
+                stage = 0;
+                phase_bit ^= 1;
+              }
             }
           }
         }
@@ -284,39 +325,57 @@ __global__ void __launch_bounds__(CH_THREADS, 1) chain_kernel(const __grid_const
         if (PH.op != OP_GEMM) continue;
         const int tiles = PH.nprod * P.n * mtl * ntl;
         for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-          if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1, abort_flag)) {
-            record_timeout(P.status, abort_flag);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * CH_BN);
-          for (int ks = 0; ks < ksteps; ++ks) {
-            if (!mbar_wait(&full_bar[stage], phase_bit, abort_flag)) {
+          int prod, g, mt, nt;
+          decode_chain_tile(t, P.n, mtl, ntl, prod, g, mt, nt);
+          const ChainProd& PR = PH.prod[prod];
+          const bool persistent = PR.mode != PROD_STORE;
+          const int dslot = t / gridDim.x;  // same tile -> same CTA and slot in every phase
+          uint32_t d_tmem;
+          if (persistent) {
+            d_tmem = tmem_base + 256u + static_cast<uint32_t>(dslot * CH_BN);
+          } else {
+            if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1, abort_flag)) {
               record_timeout(P.status, abort_flag);
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint32_t a_base = smem_u32(sA + stage * CH_A_BYTES);
-            const uint32_t b_base = smem_u32(sB + stage * CH_B_BYTES);
+            d_tmem = tmem_base + static_cast<uint32_t>(acc * CH_BN);
+          }
+          bool fresh = !persistent || PR.first_acc;
+          for (int term = 0; term < PR.nterms && ok; ++term) {
+            for (int ks = 0; ks < ksteps; ++ks) {
+              if (!mbar_wait(&full_bar[stage], phase_bit, abort_flag)) {
+                record_timeout(P.status, abort_flag);
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t a_base = smem_u32(sA + stage * CH_A_BYTES);
+              const uint32_t b_base = smem_u32(sB + stage * CH_B_BYTES);
 #pragma unroll
-            for (int j = 0; j < BK / 16; ++j) {
-              const uint64_t adesc = smem_desc_sw128(a_base + j * 32, 16, 1024);
-              const uint64_t bdesc = smem_desc_sw128(b_base + j * 2048, 8192, 1024);
-              umma_bf16(d_tmem, adesc, bdesc, IDESC, (ks > 0 || j > 0) ? 1u : 0u);
-            }
-            any_mma = true;
-            umma_commit(&empty_bar[stage]);
-            if (++stage == CH_STAGES) {
-              stage = 0;
-              phase_bit ^= 1;
+              for (int j = 0; j < BK / 16; ++j) {
+                const uint64_t adesc = smem_desc_sw128(a_base + j * 32, 16, 1024);
+                const uint64_t bdesc = smem_desc_sw128(b_base + j * 2048, 8192, 1024);
+                umma_bf16(d_tmem, adesc, bdesc, IDESC, fresh ? 0u : 1u);
+                fresh = false;
+              }
+              any_mma = true;
+              umma_commit(&empty_bar[stage]);
+              if (++stage == CH_STAGES) {
+                stage = 0;
+                phase_bit ^= 1;
+              }
             }
           }
           if (!ok) break;
-          umma_commit(&tfull_bar[acc]);
-          acc ^= 1;
-          if (acc == 0) acc_phase ^= 1;
+          if (!persistent) {
+            umma_commit(&tfull_bar[acc]);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1;
+          } else if (PR.mode == PROD_ACC_STORE) {
+            umma_commit(&dfull_bar[dslot]);  // the running sum is final
+          }
         }
       }
       if (!ok && any_mma) {
@@ -335,57 +394,76 @@ __global__ void __launch_bounds__(CH_THREADS, 1) chain_kernel(const __grid_const
     uint32_t acc_phase = 0;
     for (int ph = 0; ph < P.nphases; ++ph) {
       const ChainPhase& PH = P.phases[ph];
-      int ok = 1;
-      if (ph > 0 && lane == 0) ok = grid_wait(P, ph, abort_flag) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
+      // one poller per CTA; the other epilogue warps learn through go_bar
+      bool ok = true;
+      if (ph > 0) {
+        if (warp == 2 && lane == 0) {
+          ok = grid_wait(P, ph, abort_flag);
+          if (ok) mbar_arrive(go_bar);
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (ok && warp != 2) ok = mbar_wait(go_bar, (ph - 1) & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) break;
+      }
       if (PH.op == OP_GEMM) {
         const int tiles = PH.nprod * P.n * mtl * ntl;
         for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
           int prod, g, mt, nt;
           decode_chain_tile(t, P.n, mtl, ntl, prod, g, mt, nt);
-          const bool got = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag);
-          if (!__all_sync(0xffffffffu, got)) {  // the whole warp unwinds together
+          const ChainProd& PR = PH.prod[prod];
+          if (PR.mode == PROD_ACC) continue;  // the running sum stays in TMEM
+          const int dslot = t / gridDim.x;
+          const bool got = PR.mode == PROD_STORE
+                               ? mbar_wait(&tfull_bar[acc], acc_phase, abort_flag)
+                               : mbar_wait(&dfull_bar[dslot], 0, abort_flag);
+          if (!__all_sync(0xffffffffu, got)) {
             record_timeout(P.status, abort_flag);
-            ok = 0;
+            ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t t_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                  static_cast<uint32_t>(acc * CH_BN);
+          const uint32_t col = PR.mode == PROD_STORE
+                                   ? static_cast<uint32_t>(acc * CH_BN)
+                                   : 256u + static_cast<uint32_t>(dslot * CH_BN);
+          const uint32_t t_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + col;
           const int row = mt * BM + quarter * 32 + lane;
 #pragma unroll 1
           for (int c0 = 0; c0 < CH_BN; c0 += 32) {
             uint32_t r[32];
             tmem_load_32cols(t_base + c0, r);
             tmem_load_wait();
-            epilogue_row32(PH.prod[prod].epi, g, 0, row, nt * CH_BN + c0, r);
+            epilogue_row32(PR.epi, g, 0, row, nt * CH_BN + c0, r);
           }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&tempty_bar[acc]);
-          acc ^= 1;
-          if (acc == 0) acc_phase ^= 1;
+          if (PR.mode == PROD_STORE) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty_bar[acc]);
+            acc ^= 1;
+            if (acc == 0) acc_phase ^= 1;
+          }
         }
         if (!ok) break;
       } else {
         elementwise_phase(P, PH.op, etid, ethreads);
       }
-      // this warp is done with the phase; the first epilogue warp publishes
-      // the CTA's completion once all four are
+      // this warp is done with the phase; warp 2 publishes the CTA's
+      // completion once all four epilogue warps are
       __syncwarp();
       if (lane == 0) mbar_arrive(epi_done_bar);
-      if (warp == 2 && lane == 0) {
-        if (!mbar_wait(epi_done_bar, ph & 1, abort_flag)) {
-          record_timeout(P.status, abort_flag);
-          ok = 0;
-        } else {
-          __threadfence();
-          atomicAdd(P.counter, 1u);
+      if (warp == 2) {
+        bool done = true;
+        if (lane == 0) {
+          done = mbar_wait(epi_done_bar, ph & 1, abort_flag);
+          if (done) {
+            __threadfence();
+            atomicAdd(P.counter, 1u);
+          } else {
+            record_timeout(P.status, abort_flag);
+          }
         }
+        done = __shfl_sync(0xffffffffu, done ? 1 : 0, 0) != 0;
+        if (!done) break;
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
     }
   }
 
@@ -400,21 +478,20 @@ __global__ void __launch_bounds__(CH_THREADS, 1) chain_kernel(const __grid_const
 
 // ------------------------------------------------------------- host side
 
-// Map index of buffer `buf` used as a K-major A operand (box 64 x 128) or an
-// MN-major B operand (box 64 x 64).
+// Two maps per buffer: K-major box (64 x 128) for A, MN-major box (64 x 64)
+// for B; `rows` rows of b columns.
 struct MapTable {
   ChainParams* P;
   int count = 0;
   bool ok = true;
-  const void* ptrs[kChainMaxMaps / 2];
-  int add(const void* buf, int n, int b) {  // returns the K-box index; MN-box = +1
+  const void* ptrs[kChainMaxMaps / 2] = {};
+  int add(const void* buf, long long rows, int b) {  // returns the K-box index; MN-box = +1
     for (int i = 0; i < count; i += 2)
       if (ptrs[i / 2] == buf) return i;
     if (count + 2 > kChainMaxMaps) {
       ok = false;
       return 0;
     }
-    const long long rows = static_cast<long long>(n) * b;
     ok = ok && make_map(&P->maps[count], buf, rows, b, b, 2, BK, BM);
     ok = ok && make_map(&P->maps[count + 1], buf, rows, b, b, 2, BK, 64);
     ptrs[count / 2] = buf;
@@ -422,6 +499,14 @@ struct MapTable {
     return count - 2;
   }
 };
+
+ChainTerm term(int a_map, int b_map, bool b_batched) {
+  ChainTerm t;
+  t.a_map = a_map;
+  t.b_map = b_map + 1;  // MN-major box
+  t.b_batched = b_batched ? 1 : 0;
+  return t;
+}
 
 EpiArgs chain_epi(int b) {
   EpiArgs e;
@@ -451,12 +536,16 @@ cudaError_t launch_chain(ChainParams& P, cudaStream_t stream) {
       attr_set[dev] = true;
     }
   }
-  int most_tiles = 1;
+  const int grid = std::min(max_ctas[dev], sm_count());
+  if (grid < 1) return cudaErrorLaunchOutOfResources;
+  // every persistent D tile needs a slot in its CTA
   for (int ph = 0; ph < P.nphases; ++ph)
     if (P.phases[ph].op == OP_GEMM)
-      most_tiles = std::max(most_tiles, P.phases[ph].nprod * P.n * (P.b / BM) * (P.b / CH_BN));
-  const int grid = std::min(most_tiles, std::min(max_ctas[dev], sm_count()));
-  if (grid < 1) return cudaErrorLaunchOutOfResources;
+      for (int q = 0; q < P.phases[ph].nprod; ++q)
+        if (P.phases[ph].prod[q].mode != PROD_STORE) {
+          const int tiles = P.n * (P.b / BM) * (P.b / CH_BN);
+          if (q != 0 || (tiles + grid - 1) / grid > kMaxDSlots) return cudaErrorInvalidValue;
+        }
   P.status = device_status_ptr();
   cudaError_t e = cudaMemsetAsync(P.counter, 0, sizeof(unsigned int), stream);
   if (e != cudaSuccess) return e;
@@ -478,52 +567,66 @@ cudaError_t launch_chain(ChainParams& P, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+std::mutex g_chain_mu;
+ChainParams g_chain_params;  // large: kept off the stack; launches are host-serialised
+
 }  // namespace
 
-cudaError_t chain_build(const float* theta, int n, int b, int k, float* q32, __nv_bfloat16* q16,
-                        __nv_bfloat16* e16a, __nv_bfloat16* e16b, unsigned int* counter,
-                        __nv_bfloat16* blocks, cudaStream_t stream) {
-  if (k > kChainMaxK || b % CH_BN != 0) return cudaErrorInvalidValue;
-  static ChainParams P;  // large: kept off the stack; calls are host-serialised below
-  static std::mutex mu;
-  std::lock_guard<std::mutex> lock(mu);
+bool chain_fits(int n, int b, int k) {
+  if (k < 0 || k > kChainMaxK || b % CH_BN != 0) return false;
+  const int tiles = n * (b / BM) * (b / CH_BN);
+  return (tiles + sm_count() - 1) / sm_count() <= kMaxDSlots;
+}
+
+cudaError_t chain_build(const ChainBuildArgs& a, cudaStream_t stream) {
+  const int n = a.n, b = a.b, k = a.k;
+  if (!chain_fits(n, b, k)) return cudaErrorInvalidValue;
+  std::lock_guard<std::mutex> lock(g_chain_mu);
+  ChainParams& P = g_chain_params;
   P = ChainParams();
   P.n = n;
   P.b = b;
   P.n_a = n;
-  P.theta_a = theta;
-  P.q32 = q32;
-  P.q16 = q16;
-  P.id16 = blocks;
-  P.counter = counter;
+  P.theta_a = a.theta;
+  P.q_hi = a.q_hi;
+  P.q_lo = a.q_lo;
+  P.two_i = a.two_i;
+  P.blocks = a.blocks;
+  P.counter = a.counter;
   MapTable maps{&P};
   int ph = 0;
-  P.phases[ph++].op = OP_UNPACK;
   if (k == 0) {
-    P.phases[ph++].op = OP_IDENTITY;
+    P.phases[ph++].op = OP_IDENTITY;  // blocks = I + Q, rounded once
   } else {
-    const int q_map = maps.add(q16, n, b);
-    int cur_map = q_map;  // E_{k+1} = Q
-    __nv_bfloat16* ebuf[2] = {e16a, e16b};
+    P.phases[ph++].op = OP_UNPACK_SPLIT;
+    const long long rows = static_cast<long long>(n) * b;
+    const int hi = maps.add(a.q_hi, rows, b);
+    const int lo = maps.add(a.q_lo, rows, b);
+    const int two = maps.add(a.two_i, b, b);
+    int cur = hi;  // E_{k+1} = Q
+    __nv_bfloat16* ebuf[2] = {a.e16[0], a.e16[1]};
     int nxt = 0;
     for (int i = k; i >= 1; --i) {
+      // E_i = Q E_{i+1} + 2Q,  2Q = Q_hi 2I + Q_lo 2I;  R = I + E_1
       ChainPhase& PH = P.phases[ph++];
       PH.op = OP_GEMM;
       PH.nprod = 1;
-      PH.prod[0].a_map = q_map;        // Q, K-major
-      PH.prod[0].b_map = cur_map + 1;  // E_{i+1}, MN-major: B[n][kk] = E[kk][n]
+      ChainProd& PR = PH.prod[0];
+      PR.nterms = 3;
+      PR.term[0] = term(hi, cur, true);
+      PR.term[1] = term(hi, two, false);
+      PR.term[2] = term(lo, two, false);
+      PR.mode = PROD_STORE;
       EpiArgs e = chain_epi(b);
-      e.X = q32;  // + 2 Q
-      e.beta = 2.f;
       if (i == 1) {
-        e.delta = 1.f;  // + I
-        e.out_bf16 = blocks;
+        e.delta = 1.f;
+        e.out_bf16 = a.blocks;
       } else {
         e.out_bf16 = ebuf[nxt];
-        cur_map = maps.add(ebuf[nxt], n, b);
+        cur = maps.add(ebuf[nxt], rows, b);
         nxt ^= 1;
       }
-      PH.prod[0].epi = e;
+      PR.epi = e;
     }
   }
   P.nphases = ph;
@@ -533,18 +636,17 @@ cudaError_t chain_build(const float* theta, int n, int b, int k, float* q32, __n
 
 cudaError_t chain_adjoint(const ChainAdjointArgs& a, cudaStream_t stream) {
   const int k = a.k, b = a.b, n = a.n_a + a.n_b;
-  if (k > kChainMaxK || b % CH_BN != 0) return cudaErrorInvalidValue;
-  static ChainParams P;
-  static std::mutex mu;
-  std::lock_guard<std::mutex> lock(mu);
+  if (!chain_fits(n, b, k)) return cudaErrorInvalidValue;
+  std::lock_guard<std::mutex> lock(g_chain_mu);
+  ChainParams& P = g_chain_params;
   P = ChainParams();
   P.n = n;
   P.b = b;
   P.n_a = a.n_a;
   P.theta_a = a.theta_a;
   P.theta_b = a.theta_b;
-  P.q32 = a.q32;
-  P.q16 = a.q16;
+  P.q_hi = a.q16;
+  P.two_i = a.two_i;
   P.part_a = a.part_a;
   P.part_b = a.part_b;
   P.splits_a = a.splits_a;
@@ -552,67 +654,73 @@ cudaError_t chain_adjoint(const ChainAdjointArgs& a, cudaStream_t stream) {
   P.nsb_a = a.nsb_a;
   P.nsb_b = a.nsb_b;
   P.S = a.S;
-  P.g32 = a.f32[0];
-  P.g16 = a.f16[0];
+  P.f16 = a.f16[0];
+  P.f32 = k == 0 ? a.d32 : nullptr;
   P.dtheta_a = a.dtheta_a;
   P.dtheta_b = a.dtheta_b;
+  P.pack_src = a.d32;
   P.pack_sign = -1.f;  // D = dQ^T: pack(dQ - dQ^T) = -pack(D - D^T)
   P.counter = a.counter;
   MapTable maps{&P};
+  const long long rows = static_cast<long long>(n) * b;
   int ph = 0;
-  P.phases[ph++].op = OP_PREP_BWD;  // Q, and F_1 = G^T from the split-K partials
-  const int q_map = maps.add(a.q16, n, b);
-  int e_map[kChainMaxK + 2];
-  e_map[k + 1] = q_map;
-  // E_i = 2Q + Q E_{i+1}, i = k .. 2
-  for (int i = k; i >= 2; --i) {
-    ChainPhase& PH = P.phases[ph++];
-    PH.op = OP_GEMM;
-    PH.nprod = 1;
-    PH.prod[0].a_map = q_map;
-    PH.prod[0].b_map = e_map[i + 1] + 1;
-    EpiArgs e = chain_epi(b);
-    e.X = a.q32;
-    e.beta = 2.f;
-    e.out_bf16 = a.e16[i];
-    PH.prod[0].epi = e;
-    e_map[i] = maps.add(a.e16[i], n, b);
-  }
-  // transposed reverse sweep: D += 2 F_i + E_{i+1} F_i,  F_{i+1} = F_i Q
-  int cur = 0;
-  for (int i = 1; i <= k; ++i) {
-    ChainPhase& PH = P.phases[ph++];
-    PH.op = OP_GEMM;
-    PH.nprod = 2;
-    const int f_map = maps.add(a.f16[cur], n, b);
-    PH.prod[0].a_map = e_map[i + 1];  // E_{i+1}, K-major
-    PH.prod[0].b_map = f_map + 1;     // B[n][kk] = F_i[kk][n]
-    EpiArgs e0 = chain_epi(b);
-    if (i > 1) {
-      e0.X = a.d32;
-      e0.beta = 1.f;
+  P.phases[ph++].op = OP_PREP_BWD;  // Q, F_1 = G^T from the split-K partials, 2I
+  if (k > 0) {
+    const int q = maps.add(a.q16, rows, b);
+    const int two = maps.add(a.two_i, b, b);
+    int e_map[kChainMaxK + 2];
+    e_map[k + 1] = q;
+    // E_i = Q E_{i+1} + Q 2I, i = k .. 2
+    for (int i = k; i >= 2; --i) {
+      ChainPhase& PH = P.phases[ph++];
+      PH.op = OP_GEMM;
+      PH.nprod = 1;
+      ChainProd& PR = PH.prod[0];
+      PR.nterms = 2;
+      PR.term[0] = term(q, e_map[i + 1], true);
+      PR.term[1] = term(q, two, false);
+      PR.mode = PROD_STORE;
+      EpiArgs e = chain_epi(b);
+      e.out_bf16 = a.e16[i];
+      PR.epi = e;
+      e_map[i] = maps.add(a.e16[i], rows, b);
     }
-    e0.Y = a.f32[cur];
-    e0.gamma = 2.f;
-    e0.out_f32 = a.d32;
-    PH.prod[0].epi = e0;
-    PH.prod[1].a_map = f_map;      // F_i, K-major
-    PH.prod[1].b_map = q_map + 1;  // B[n][kk] = Q[kk][n]
-    EpiArgs e1 = chain_epi(b);
-    e1.out_f32 = a.f32[1 - cur];
-    e1.out_bf16 = a.f16[1 - cur];
-    PH.prod[1].epi = e1;
-    cur = 1 - cur;
+    // transposed reverse sweep with D = dQ^T in TMEM:
+    //   i < k:  D += E_{i+1} F_i + F_i 2I,   F_{i+1} = F_i Q
+    //   i = k:  D += Q F_k + F_k 2I + F_k Q   (the last term is F_{k+1})
+    int cur = 0;
+    for (int i = 1; i <= k; ++i) {
+      ChainPhase& PH = P.phases[ph++];
+      PH.op = OP_GEMM;
+      const int f = maps.add(a.f16[cur], rows, b);
+      ChainProd& D = PH.prod[0];
+      D.term[0] = term(e_map[i + 1], f, true);
+      D.term[1] = term(f, two, false);
+      D.nterms = 2;
+      D.first_acc = i == 1 ? 1 : 0;
+      if (i < k) {
+        D.mode = PROD_ACC;
+        PH.nprod = 2;
+        ChainProd& F = PH.prod[1];
+        F.nterms = 1;
+        F.term[0] = term(f, q, true);
+        F.mode = PROD_STORE;
+        EpiArgs e = chain_epi(b);
+        e.out_bf16 = a.f16[1 - cur];
+        F.epi = e;
+        cur = 1 - cur;
+      } else {
+        D.term[2] = term(f, q, true);
+        D.nterms = 3;
+        D.mode = PROD_ACC_STORE;
+        EpiArgs e = chain_epi(b);
+        e.out_f32 = a.d32;
+        D.epi = e;
+        PH.nprod = 1;
+      }
+    }
   }
-  ChainPhase& PK = P.phases[ph++];
-  PK.op = OP_PACK;
-  if (k == 0) {
-    P.pack_A = a.f32[0];
-    P.pack_B = nullptr;
-  } else {
-    P.pack_A = a.d32;
-    P.pack_B = a.f32[cur];  // F_{k+1}
-  }
+  P.phases[ph++].op = OP_PACK;
   P.nphases = ph;
   if (!maps.ok) return cudaErrorInvalidValue;
   return launch_chain(P, stream);

@@ -81,23 +81,36 @@ cudaError_t simt_gemm_run(const SimtGemm& g, cudaStream_t stream);
 // multiple of 128, k <= kChainMaxK); see chain_tc.cu.
 constexpr int kChainMaxK = 8;
 
+// True when the chain of n blocks of size b and order k runs as one launch
+// (b a multiple of 128, k <= kChainMaxK, at most two persistent D tiles per CTA).
+bool chain_fits(int n, int b, int k);
+
 // blocks = (I + Q)(I + Q + ... + Q^k) for the n blocks of one side, bf16 out.
-// Scratch: q32 [n][b][b] fp32, q16 and e16a/e16b bf16, one counter word.
-cudaError_t chain_build(const float* theta, int n, int b, int k, float* q32, __nv_bfloat16* q16,
-                        __nv_bfloat16* e16a, __nv_bfloat16* e16b, unsigned int* counter,
-                        __nv_bfloat16* blocks, cudaStream_t stream);
+// Scratch [n][b][b] bf16: q_hi, q_lo, e16[0], e16[1]; two_i [b][b] bf16; one
+// counter word.
+struct ChainBuildArgs {
+  int n = 0, b = 0, k = 0;
+  const float* theta = nullptr;
+  __nv_bfloat16* q_hi = nullptr;
+  __nv_bfloat16* q_lo = nullptr;
+  __nv_bfloat16* two_i = nullptr;
+  __nv_bfloat16* e16[2] = {nullptr, nullptr};
+  unsigned int* counter = nullptr;
+  __nv_bfloat16* blocks = nullptr;
+};
+cudaError_t chain_build(const ChainBuildArgs& a, cudaStream_t stream);
 
 // Packed gradients of both sides from the split-K partials of the TRANSPOSED
 // block gradients G^T (blocks [0, n_a) from part_a / theta_a, the rest from
-// part_b / theta_b).  Scratch buffers are [n_a + n_b][b][b].
+// part_b / theta_b).  Scratch [n_a + n_b][b][b]: q16, e16[2..k], f16[0..1]
+// (bf16) and d32 (fp32); two_i [b][b] bf16; one counter word.
 struct ChainAdjointArgs {
   int n_a = 0, n_b = 0, b = 0, k = 0;
   const float* theta_a = nullptr;
   const float* theta_b = nullptr;
-  float* q32 = nullptr;
   __nv_bfloat16* q16 = nullptr;
+  __nv_bfloat16* two_i = nullptr;
   __nv_bfloat16* e16[kChainMaxK + 2] = {};
-  float* f32[2] = {nullptr, nullptr};
   __nv_bfloat16* f16[2] = {nullptr, nullptr};
   float* d32 = nullptr;
   const float* part_a = nullptr;
