@@ -432,7 +432,7 @@ BuildBufs carve_build(Carver& c, int n, int b, int k, bool is_bf16) {
     w.e16[0] = c.take<bf16>(nbb);
     w.e16[1] = c.take<bf16>(nbb);
     w.two_i = c.take<bf16>(static_cast<size_t>(b) * b);
-    w.counter = c.take<unsigned int>(1);
+    w.counter = c.take<unsigned int>(kChainMaxPhases);
     return w;
   }
   w.q32 = c.take<float>(nbb);
@@ -523,7 +523,7 @@ CnpBufs carve_cnp(Carver& c, int n, int b, int k, bool tc) {
   }
   w.dq = c.take<float>(nbb);
   if (tc) {
-    w.counter = c.take<unsigned int>(1);
+    w.counter = c.take<unsigned int>(kChainMaxPhases);
     w.two_i = c.take<bf16>(static_cast<size_t>(b) * b);
   }
   return w;

@@ -1,27 +1,25 @@
 // The b x b product chains of the block build and of its adjoint, each run
-// as ONE cooperative persistent launch.
+// as ONE cooperative persistent launch of product phases.
 //
-// A chain is a short program of phases executed by every CTA in order:
-//   elementwise phases  unpack theta -> Q (bf16 hi / lo parts), the split-K
-//                       sums of the token-wise block gradients, the constant
-//                       2I, the skew pack; run by the epilogue warps of every
-//                       CTA, grid-stride, four independent elements per step;
-//   product phases      1 or 2 products over all b x b blocks g, each a sum
-//                       of up to three MMA terms  sum_t A_t(g) * B_t(g)^T
-//                       (A K-major, B MN-major, read by TMA from the
-//                       row-major [n][b][b] stacks or from a constant b x b
-//                       matrix), as 128 x 128 tcgen05 tiles.
-// Addends are MMA terms too (2Q = Q_hi * 2I + Q_lo * 2I, 2F = F * 2I), so
-// epilogues only store.  The adjoint's running sum D stays in TMEM across
-// its phases: each CTA owns the same D tiles in every phase.
+// Phase p computes 1 or 2 products over all b x b blocks g, each a sum of up
+// to three MMA terms  sum_t A_t(g) * B_t(g)^T  (A K-major, B MN-major, read
+// by TMA from the row-major [n][b][b] stacks or from a constant b x b
+// matrix), as 128 x 128 tcgen05 tiles.  Addends are MMA terms too
+// (2Q = Q_hi * 2I + Q_lo * 2I, 2F = F * 2I), so epilogues only store.  The
+// adjoint's running sum D stays in TMEM across its phases: each CTA owns the
+// same D tiles in every phase.  The elementwise steps around a chain (theta
+// -> Q, split-K sums, skew pack) are separate, massively parallel tiled
+// kernels (kernels_simt.cu).
 //
-// Phase p+1 may read anything phase p wrote, so phases are separated by a
-// grid barrier: every CTA bumps a global counter when its epilogue warps are
-// done with phase p; producers and epilogues of phase p+1 wait until the
-// counter reaches (p+1) * gridDim.x.  The launch is cooperative (all CTAs
-// resident); every wait is bounded (2 s) and records POETX_ERR_TIMEOUT.
+// Phase p+1 reads what phase p wrote, so a grid barrier separates phases:
+// each CTA bumps counter[p] when its epilogue warps have stored phase p, and
+// producers of phase p+1 wait until counter[p] == gridDim.x.  One counter per
+// phase: a CTA without tiles finishes later phases at once, and its early
+// arrivals must not count towards an earlier phase.
+// The launch is cooperative (all CTAs resident); every wait is bounded (2 s)
+// and records POETX_ERR_TIMEOUT.
 //
-// This is the "Q^2, Q^3, Q^4 in one fused kernel" of the pages' CNP step,
+// This is the pages' "Q^2, Q^3, Q^4 in one fused kernel" of the CNP step,
 // extended to the adjoint; a 256 x 256 bf16 operand pair does not fit one
 // SM, so the chain spans all SMs and synchronises between powers.
 #include <algorithm>
@@ -40,21 +38,14 @@ constexpr int CH_THREADS = 192;
 constexpr int CH_BN = 128;
 constexpr int CH_A_BYTES = BM * BK * 2;     // 16 KB
 constexpr int CH_B_BYTES = CH_BN * BK * 2;  // 16 KB
-constexpr int CH_SMEM = 1024 + CH_STAGES * (CH_A_BYTES + CH_B_BYTES) + 256;
+constexpr int CH_BARRIER_BYTES = 512;
+constexpr int CH_SMEM = 1024 + CH_STAGES * (CH_A_BYTES + CH_B_BYTES) + CH_BARRIER_BYTES;
 constexpr uint32_t CH_TMEM_COLS = 512;  // 2 rotating accumulators + 2 persistent D slots
 constexpr int kMaxDSlots = 2;
 
-enum {
-  OP_GEMM = 0,
-  OP_UNPACK_SPLIT = 1,   // Q -> q_hi, q_lo (bf16); 2I
-  OP_IDENTITY = 2,       // blocks = I + Q straight from theta (k = 0)
-  OP_PREP_BWD = 3,       // Q -> q_hi; F_1 = sum of partials; 2I
-  OP_PACK = 4            // dtheta = sign * (D - D^T) packed
-};
 enum { PROD_STORE = 0, PROD_ACC = 1, PROD_ACC_STORE = 2 };
 
 constexpr int kChainMaxMaps = 48;
-constexpr int kChainMaxPhases = 20;
 
 struct ChainTerm {
   int a_map, b_map;  // A: K-major box map, B: MN-major box map
@@ -70,7 +61,6 @@ struct ChainProd {
 };
 
 struct ChainPhase {
-  int op;
   int nprod;
   ChainProd prod[2];
 };
@@ -79,27 +69,14 @@ struct ChainParams {
   CUtensorMap maps[kChainMaxMaps];  // first member: keeps the maps 64-byte aligned
   ChainPhase phases[kChainMaxPhases];
   int nphases;
-  int n, b, n_a;  // blocks, block size, blocks of the first side
-  const float* theta_a;
-  const float* theta_b;
-  __nv_bfloat16* q_hi;
-  __nv_bfloat16* q_lo;  // builder only
-  __nv_bfloat16* two_i;  // constant 2I, b x b
-  const float* part_a;   // split-K partials [splits][nsb][S][S] of each side
-  const float* part_b;
-  int splits_a, splits_b, nsb_a, nsb_b, S;
-  __nv_bfloat16* f16;  // F_1 (bf16)
-  float* f32;          // F_1 (fp32, k = 0 only)
-  const float* pack_src;
-  float pack_sign;
-  float* dtheta_a;
-  float* dtheta_b;
-  __nv_bfloat16* blocks;  // identity phase output
-  unsigned int* counter;
+  int n, b;  // blocks, block size
+  unsigned int* counter;  // [kChainMaxPhases] per-phase arrival counts
   int* status;
 };
 
 static_assert(sizeof(ChainParams) <= 32000, "chain parameters exceed the kernel parameter space");
+static_assert((2 * CH_STAGES + 4 + kMaxDSlots + 1 + kChainMaxPhases) * 8 + 8 <= CH_BARRIER_BYTES,
+              "chain barriers exceed their shared-memory area");
 
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
   unsigned v;
@@ -111,84 +88,20 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-// Wait until every CTA has finished the phases before `phase`.
+// Wait until every CTA has finished phase `phase - 1`.
 __device__ bool grid_wait(const ChainParams& P, int phase, volatile int* abort) {
-  const unsigned target = static_cast<unsigned>(phase) * gridDim.x;
-  if (ld_acquire_u32(P.counter) >= target) return true;
+  if (phase == 0) return true;
+  const unsigned* c = P.counter + (phase - 1);
+  const unsigned target = gridDim.x;
+  if (ld_acquire_u32(c) >= target) return true;
   const unsigned long long t0 = global_timer_ns();
   while (true) {
     __nanosleep(100);
-    if (ld_acquire_u32(P.counter) >= target) return true;
+    if (ld_acquire_u32(c) >= target) return true;
     if (*abort) return false;
     if (global_timer_ns() - t0 > kWaitLimitNs) {
       record_timeout(P.status, abort);
       return false;
-    }
-  }
-}
-
-__device__ __forceinline__ int packed_index(int i, int j, int b) {
-  return i * b - (i * (i + 1)) / 2 + (j - i - 1);
-}
-
-__device__ __forceinline__ float theta_at(const ChainParams& P, int g, int i, int j) {
-  const int b = P.b, m = b * (b - 1) / 2;
-  const float* th = g < P.n_a ? P.theta_a + g * m : P.theta_b + (g - P.n_a) * m;
-  if (i < j) return th[packed_index(i, j, b)];
-  if (i > j) return -th[packed_index(j, i, b)];
-  return 0.f;
-}
-
-// One element of an elementwise phase; all its loads are issued before its
-// stores so four unrolled elements keep four loads in flight.
-__device__ __forceinline__ void elementwise_one(const ChainParams& P, int op, int idx) {
-  const int b = P.b, bb = b * b;
-  const int g = idx / bb;
-  const int rem = idx - g * bb;
-  const int i = rem / b;
-  const int j = rem - i * b;
-  if (op == OP_UNPACK_SPLIT || op == OP_PREP_BWD || op == OP_IDENTITY) {
-    const float q = theta_at(P, g, i, j);
-    if (op == OP_IDENTITY) {
-      P.blocks[idx] = __float2bfloat16_rn(q + (i == j ? 1.f : 0.f));
-    } else {
-      const __nv_bfloat16 hi = __float2bfloat16_rn(q);
-      P.q_hi[idx] = hi;
-      if (op == OP_UNPACK_SPLIT) P.q_lo[idx] = __float2bfloat16_rn(q - __bfloat162float(hi));
-      if (g == 0) P.two_i[rem] = __float2bfloat16_rn(i == j ? 2.f : 0.f);
-    }
-  }
-  if (op == OP_PREP_BWD) {
-    // diagonal b-block of superblock g / (S/b), summed over the K splits
-    const bool side_a = g < P.n_a;
-    const int per = P.S / b;
-    const int gl = side_a ? g : g - P.n_a;
-    const int sb = gl / per;
-    const int off = (gl - sb * per) * b;
-    const float* part = side_a ? P.part_a : P.part_b;
-    const int splits = side_a ? P.splits_a : P.splits_b;
-    const long long stride = static_cast<long long>(side_a ? P.nsb_a : P.nsb_b) * P.S * P.S;
-    const long long src = (static_cast<long long>(sb) * P.S + off + i) * P.S + off + j;
-    float v = 0.f;
-    for (int s = 0; s < splits; ++s) v += part[s * stride + src];
-    P.f16[idx] = __float2bfloat16_rn(v);
-    if (P.f32 != nullptr) P.f32[idx] = v;
-  }
-  if (op == OP_PACK && i < j) {
-    const float v = P.pack_sign * (P.pack_src[idx] - P.pack_src[g * bb + j * b + i]);
-    const int m = b * (b - 1) / 2;
-    if (g < P.n_a) P.dtheta_a[g * m + packed_index(i, j, b)] = v;
-    else P.dtheta_b[(g - P.n_a) * m + packed_index(i, j, b)] = v;
-  }
-}
-
-__device__ void elementwise_phase(const ChainParams& P, int op, int tid, int nthreads) {
-  const int total = P.n * P.b * P.b;
-  for (int base = tid; base < total; base += 4 * nthreads) {
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int idx = base + u * nthreads;
-      if (idx < total) elementwise_one(P, op, idx);
     }
   }
 }
@@ -216,9 +129,10 @@ __global__ void __launch_bounds__(CH_THREADS, 1) chain_kernel(const __grid_const
   uint64_t* tempty_bar = tfull_bar + 2;         // [2]
   uint64_t* dfull_bar = tempty_bar + 2;         // [kMaxDSlots]
   uint64_t* drain_bar = dfull_bar + kMaxDSlots;
-  uint64_t* epi_done_bar = drain_bar + 1;
-  uint64_t* go_bar = epi_done_bar + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(go_bar + 1);
+  // one per phase, each completed once: epilogue warps of an idle CTA run
+  // ahead through the phases, so a reused barrier would mix their arrivals
+  uint64_t* epi_done_bar = drain_bar + 1;  // [kChainMaxPhases]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epi_done_bar + kChainMaxPhases);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32;
@@ -237,8 +151,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1) chain_kernel(const __grid_const
     }
     for (int d = 0; d < kMaxDSlots; ++d) mbar_init(&dfull_bar[d], 1);
     mbar_init(drain_bar, 1);
-    mbar_init(epi_done_bar, 4);
-    mbar_init(go_bar, 1);
+    for (int q = 0; q < kChainMaxPhases; ++q) mbar_init(&epi_done_bar[q], 4);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -260,7 +173,6 @@ __global__ void __launch_bounds__(CH_THREADS, 1) chain_kernel(const __grid_const
       bool ok = true;
       for (int ph = 0; ph < P.nphases && ok; ++ph) {
         const ChainPhase& PH = P.phases[ph];
-        if (PH.op != OP_GEMM) continue;
         if (!grid_wait(P, ph, abort_flag)) {
           ok = false;
           break;
@@ -322,7 +234,6 @@ __global__ void __launch_bounds__(CH_THREADS, 1) chain_kernel(const __grid_const
       bool ok = true, any_mma = false;
       for (int ph = 0; ph < P.nphases && ok; ++ph) {
         const ChainPhase& PH = P.phases[ph];
-        if (PH.op != OP_GEMM) continue;
         const int tiles = PH.nprod * P.n * mtl * ntl;
         for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
           int prod, g, mt, nt;
@@ -386,83 +297,68 @@ __global__ void __launch_bounds__(CH_THREADS, 1) chain_kernel(const __grid_const
       }
     }
   } else {
-    // ---------------------------------------------- epilogue / elementwise
+    // ----------------------------------------------------------- epilogue
     const int quarter = warp & 3;
-    const int etid = blockIdx.x * 128 + (threadIdx.x - 64);
-    const int ethreads = gridDim.x * 128;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int ph = 0; ph < P.nphases; ++ph) {
       const ChainPhase& PH = P.phases[ph];
-      // one poller per CTA; the other epilogue warps learn through go_bar
       bool ok = true;
-      if (ph > 0) {
-        if (warp == 2 && lane == 0) {
-          ok = grid_wait(P, ph, abort_flag);
-          if (ok) mbar_arrive(go_bar);
+      const int tiles = PH.nprod * P.n * mtl * ntl;
+      for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
+        int prod, g, mt, nt;
+        decode_chain_tile(t, P.n, mtl, ntl, prod, g, mt, nt);
+        const ChainProd& PR = PH.prod[prod];
+        if (PR.mode == PROD_ACC) continue;  // the running sum stays in TMEM
+        const int dslot = t / gridDim.x;
+        const bool got = PR.mode == PROD_STORE ? mbar_wait(&tfull_bar[acc], acc_phase, abort_flag)
+                                               : mbar_wait(&dfull_bar[dslot], 0, abort_flag);
+        if (!__all_sync(0xffffffffu, got)) {
+          record_timeout(P.status, abort_flag);
+          ok = false;
+          break;
         }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (ok && warp != 2) ok = mbar_wait(go_bar, (ph - 1) & 1, abort_flag);
-        if (!__all_sync(0xffffffffu, ok)) break;
-      }
-      if (PH.op == OP_GEMM) {
-        const int tiles = PH.nprod * P.n * mtl * ntl;
-        for (int t = blockIdx.x; t < tiles; t += gridDim.x) {
-          int prod, g, mt, nt;
-          decode_chain_tile(t, P.n, mtl, ntl, prod, g, mt, nt);
-          const ChainProd& PR = PH.prod[prod];
-          if (PR.mode == PROD_ACC) continue;  // the running sum stays in TMEM
-          const int dslot = t / gridDim.x;
-          const bool got = PR.mode == PROD_STORE
-                               ? mbar_wait(&tfull_bar[acc], acc_phase, abort_flag)
-                               : mbar_wait(&dfull_bar[dslot], 0, abort_flag);
-          if (!__all_sync(0xffffffffu, got)) {
-            record_timeout(P.status, abort_flag);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t col = PR.mode == PROD_STORE
-                                   ? static_cast<uint32_t>(acc * CH_BN)
-                                   : 256u + static_cast<uint32_t>(dslot * CH_BN);
-          const uint32_t t_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + col;
-          const int row = mt * BM + quarter * 32 + lane;
+        tc_fence_after();
+        const uint32_t col = PR.mode == PROD_STORE ? static_cast<uint32_t>(acc * CH_BN)
+                                                   : 256u + static_cast<uint32_t>(dslot * CH_BN);
+        const uint32_t t_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + col;
+        const int row = mt * BM + quarter * 32 + lane;
 #pragma unroll 1
-          for (int c0 = 0; c0 < CH_BN; c0 += 32) {
-            uint32_t r[32];
-            tmem_load_32cols(t_base + c0, r);
-            tmem_load_wait();
-            epilogue_row32(PR.epi, g, 0, row, nt * CH_BN + c0, r);
-          }
-          if (PR.mode == PROD_STORE) {
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tempty_bar[acc]);
-            acc ^= 1;
-            if (acc == 0) acc_phase ^= 1;
-          }
+        for (int c0 = 0; c0 < CH_BN; c0 += 32) {
+          uint32_t r[32];
+          tmem_load_32cols(t_base + c0, r);
+          tmem_load_wait();
+          epilogue_row32(PR.epi, g, 0, row, nt * CH_BN + c0, r);
         }
-        if (!ok) break;
-      } else {
-        elementwise_phase(P, PH.op, etid, ethreads);
+        if (PR.mode == PROD_STORE) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&tempty_bar[acc]);
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1;
+        }
       }
-      // this warp is done with the phase; warp 2 publishes the CTA's
-      // completion once all four epilogue warps are
+      if (!ok) break;
+      if (ph + 1 == P.nphases) break;  // nobody waits on the last phase
+      // this warp has stored the phase; warp 2 publishes the CTA's completion
+      // once all four epilogue warps have.  The next phase reads these
+      // stores through TMA (the async proxy): each writing thread orders its
+      // generic-proxy stores before that with a proxy fence.
+      fence_proxy_async_global();
       __syncwarp();
-      if (lane == 0) mbar_arrive(epi_done_bar);
+      if (lane == 0) mbar_arrive(&epi_done_bar[ph]);
       if (warp == 2) {
         bool done = true;
         if (lane == 0) {
-          done = mbar_wait(epi_done_bar, ph & 1, abort_flag);
+          done = mbar_wait(&epi_done_bar[ph], 0, abort_flag);
           if (done) {
             __threadfence();
-            atomicAdd(P.counter, 1u);
+            atomicAdd(P.counter + ph, 1u);
           } else {
             record_timeout(P.status, abort_flag);
           }
         }
-        done = __shfl_sync(0xffffffffu, done ? 1 : 0, 0) != 0;
-        if (!done) break;
+        if (__shfl_sync(0xffffffffu, done ? 1 : 0, 0) == 0) break;
       }
     }
   }
@@ -540,14 +436,13 @@ cudaError_t launch_chain(ChainParams& P, cudaStream_t stream) {
   if (grid < 1) return cudaErrorLaunchOutOfResources;
   // every persistent D tile needs a slot in its CTA
   for (int ph = 0; ph < P.nphases; ++ph)
-    if (P.phases[ph].op == OP_GEMM)
-      for (int q = 0; q < P.phases[ph].nprod; ++q)
-        if (P.phases[ph].prod[q].mode != PROD_STORE) {
-          const int tiles = P.n * (P.b / BM) * (P.b / CH_BN);
-          if (q != 0 || (tiles + grid - 1) / grid > kMaxDSlots) return cudaErrorInvalidValue;
-        }
+    for (int q = 0; q < P.phases[ph].nprod; ++q)
+      if (P.phases[ph].prod[q].mode != PROD_STORE) {
+        const int tiles = P.n * (P.b / BM) * (P.b / CH_BN);
+        if (q != 0 || (tiles + grid - 1) / grid > kMaxDSlots) return cudaErrorInvalidValue;
+      }
   P.status = device_status_ptr();
-  cudaError_t e = cudaMemsetAsync(P.counter, 0, sizeof(unsigned int), stream);
+  cudaError_t e = cudaMemsetAsync(P.counter, 0, sizeof(unsigned int) * kChainMaxPhases, stream);
   if (e != cudaSuccess) return e;
 
   cudaLaunchConfig_t cfg = {};
@@ -573,7 +468,7 @@ ChainParams g_chain_params;  // large: kept off the stack; launches are host-ser
 }  // namespace
 
 bool chain_fits(int n, int b, int k) {
-  if (k < 0 || k > kChainMaxK || b % CH_BN != 0) return false;
+  if (k < 1 || k > kChainMaxK || b % CH_BN != 0) return false;
   const int tiles = n * (b / BM) * (b / CH_BN);
   return (tiles + sm_count() - 1) / sm_count() <= kMaxDSlots;
 }
@@ -581,53 +476,49 @@ bool chain_fits(int n, int b, int k) {
 cudaError_t chain_build(const ChainBuildArgs& a, cudaStream_t stream) {
   const int n = a.n, b = a.b, k = a.k;
   if (!chain_fits(n, b, k)) return cudaErrorInvalidValue;
+  PrepTilesArgs pa;  // Q as bf16 hi + lo parts, and 2I
+  pa.n_a = n;
+  pa.b = b;
+  pa.theta_a = a.theta;
+  pa.q_hi = a.q_hi;
+  pa.q_lo = a.q_lo;
+  pa.two_i = a.two_i;
+  cudaError_t e = launch_prep_tiles(pa, stream);
+  if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(g_chain_mu);
   ChainParams& P = g_chain_params;
   P = ChainParams();
   P.n = n;
   P.b = b;
-  P.n_a = n;
-  P.theta_a = a.theta;
-  P.q_hi = a.q_hi;
-  P.q_lo = a.q_lo;
-  P.two_i = a.two_i;
-  P.blocks = a.blocks;
   P.counter = a.counter;
   MapTable maps{&P};
-  int ph = 0;
-  if (k == 0) {
-    P.phases[ph++].op = OP_IDENTITY;  // blocks = I + Q, rounded once
-  } else {
-    P.phases[ph++].op = OP_UNPACK_SPLIT;
-    const long long rows = static_cast<long long>(n) * b;
-    const int hi = maps.add(a.q_hi, rows, b);
-    const int lo = maps.add(a.q_lo, rows, b);
-    const int two = maps.add(a.two_i, b, b);
-    int cur = hi;  // E_{k+1} = Q
-    __nv_bfloat16* ebuf[2] = {a.e16[0], a.e16[1]};
-    int nxt = 0;
-    for (int i = k; i >= 1; --i) {
-      // E_i = Q E_{i+1} + 2Q,  2Q = Q_hi 2I + Q_lo 2I;  R = I + E_1
-      ChainPhase& PH = P.phases[ph++];
-      PH.op = OP_GEMM;
-      PH.nprod = 1;
-      ChainProd& PR = PH.prod[0];
-      PR.nterms = 3;
-      PR.term[0] = term(hi, cur, true);
-      PR.term[1] = term(hi, two, false);
-      PR.term[2] = term(lo, two, false);
-      PR.mode = PROD_STORE;
-      EpiArgs e = chain_epi(b);
-      if (i == 1) {
-        e.delta = 1.f;
-        e.out_bf16 = a.blocks;
-      } else {
-        e.out_bf16 = ebuf[nxt];
-        cur = maps.add(ebuf[nxt], rows, b);
-        nxt ^= 1;
-      }
-      PR.epi = e;
+  const long long rows = static_cast<long long>(n) * b;
+  const int hi = maps.add(a.q_hi, rows, b);
+  const int lo = maps.add(a.q_lo, rows, b);
+  const int two = maps.add(a.two_i, b, b);
+  int cur = hi;  // E_{k+1} = Q
+  __nv_bfloat16* ebuf[2] = {a.e16[0], a.e16[1]};
+  int nxt = 0, ph = 0;
+  for (int i = k; i >= 1; --i) {
+    // E_i = Q E_{i+1} + 2Q,  2Q = Q_hi 2I + Q_lo 2I;  block = I + E_1
+    ChainPhase& PH = P.phases[ph++];
+    PH.nprod = 1;
+    ChainProd& PR = PH.prod[0];
+    PR.nterms = 3;
+    PR.term[0] = term(hi, cur, true);
+    PR.term[1] = term(hi, two, false);
+    PR.term[2] = term(lo, two, false);
+    PR.mode = PROD_STORE;
+    EpiArgs ep = chain_epi(b);
+    if (i == 1) {
+      ep.delta = 1.f;
+      ep.out_bf16 = a.blocks;
+    } else {
+      ep.out_bf16 = ebuf[nxt];
+      cur = maps.add(ebuf[nxt], rows, b);
+      nxt ^= 1;
     }
+    PR.epi = ep;
   }
   P.nphases = ph;
   if (!maps.ok) return cudaErrorInvalidValue;
@@ -637,52 +528,50 @@ cudaError_t chain_build(const ChainBuildArgs& a, cudaStream_t stream) {
 cudaError_t chain_adjoint(const ChainAdjointArgs& a, cudaStream_t stream) {
   const int k = a.k, b = a.b, n = a.n_a + a.n_b;
   if (!chain_fits(n, b, k)) return cudaErrorInvalidValue;
-  std::lock_guard<std::mutex> lock(g_chain_mu);
-  ChainParams& P = g_chain_params;
-  P = ChainParams();
-  P.n = n;
-  P.b = b;
-  P.n_a = a.n_a;
-  P.theta_a = a.theta_a;
-  P.theta_b = a.theta_b;
-  P.q_hi = a.q16;
-  P.two_i = a.two_i;
-  P.part_a = a.part_a;
-  P.part_b = a.part_b;
-  P.splits_a = a.splits_a;
-  P.splits_b = a.splits_b;
-  P.nsb_a = a.nsb_a;
-  P.nsb_b = a.nsb_b;
-  P.S = a.S;
-  P.f16 = a.f16[0];
-  P.f32 = k == 0 ? a.d32 : nullptr;
-  P.dtheta_a = a.dtheta_a;
-  P.dtheta_b = a.dtheta_b;
-  P.pack_src = a.d32;
-  P.pack_sign = -1.f;  // D = dQ^T: pack(dQ - dQ^T) = -pack(D - D^T)
-  P.counter = a.counter;
-  MapTable maps{&P};
-  const long long rows = static_cast<long long>(n) * b;
-  int ph = 0;
-  P.phases[ph++].op = OP_PREP_BWD;  // Q, F_1 = G^T from the split-K partials, 2I
-  if (k > 0) {
+  PrepTilesArgs pa;  // Q (bf16), 2I, F_1 = G^T summed over the K splits
+  pa.n_a = a.n_a;
+  pa.n_b = a.n_b;
+  pa.b = b;
+  pa.theta_a = a.theta_a;
+  pa.theta_b = a.theta_b;
+  pa.q_hi = a.q16;
+  pa.two_i = a.two_i;
+  pa.part_a = a.part_a;
+  pa.part_b = a.part_b;
+  pa.splits_a = a.splits_a;
+  pa.splits_b = a.splits_b;
+  pa.nsb_a = a.nsb_a;
+  pa.nsb_b = a.nsb_b;
+  pa.S = a.S;
+  pa.f16 = a.f16[0];
+  cudaError_t e = launch_prep_tiles(pa, stream);
+  if (e != cudaSuccess) return e;
+  {
+    std::lock_guard<std::mutex> lock(g_chain_mu);
+    ChainParams& P = g_chain_params;
+    P = ChainParams();
+    P.n = n;
+    P.b = b;
+    P.counter = a.counter;
+    MapTable maps{&P};
+    const long long rows = static_cast<long long>(n) * b;
     const int q = maps.add(a.q16, rows, b);
     const int two = maps.add(a.two_i, b, b);
     int e_map[kChainMaxK + 2];
     e_map[k + 1] = q;
+    int ph = 0;
     // E_i = Q E_{i+1} + Q 2I, i = k .. 2
     for (int i = k; i >= 2; --i) {
       ChainPhase& PH = P.phases[ph++];
-      PH.op = OP_GEMM;
       PH.nprod = 1;
       ChainProd& PR = PH.prod[0];
       PR.nterms = 2;
       PR.term[0] = term(q, e_map[i + 1], true);
       PR.term[1] = term(q, two, false);
       PR.mode = PROD_STORE;
-      EpiArgs e = chain_epi(b);
-      e.out_bf16 = a.e16[i];
-      PR.epi = e;
+      EpiArgs ep = chain_epi(b);
+      ep.out_bf16 = a.e16[i];
+      PR.epi = ep;
       e_map[i] = maps.add(a.e16[i], rows, b);
     }
     // transposed reverse sweep with D = dQ^T in TMEM:
@@ -691,7 +580,6 @@ cudaError_t chain_adjoint(const ChainAdjointArgs& a, cudaStream_t stream) {
     int cur = 0;
     for (int i = 1; i <= k; ++i) {
       ChainPhase& PH = P.phases[ph++];
-      PH.op = OP_GEMM;
       const int f = maps.add(a.f16[cur], rows, b);
       ChainProd& D = PH.prod[0];
       D.term[0] = term(e_map[i + 1], f, true);
@@ -705,25 +593,27 @@ cudaError_t chain_adjoint(const ChainAdjointArgs& a, cudaStream_t stream) {
         F.nterms = 1;
         F.term[0] = term(f, q, true);
         F.mode = PROD_STORE;
-        EpiArgs e = chain_epi(b);
-        e.out_bf16 = a.f16[1 - cur];
-        F.epi = e;
+        EpiArgs ep = chain_epi(b);
+        ep.out_bf16 = a.f16[1 - cur];
+        F.epi = ep;
         cur = 1 - cur;
       } else {
         D.term[2] = term(f, q, true);
         D.nterms = 3;
         D.mode = PROD_ACC_STORE;
-        EpiArgs e = chain_epi(b);
-        e.out_f32 = a.d32;
-        D.epi = e;
+        EpiArgs ep = chain_epi(b);
+        ep.out_f32 = a.d32;
+        D.epi = ep;
         PH.nprod = 1;
       }
     }
+    P.nphases = ph;
+    if (!maps.ok) return cudaErrorInvalidValue;
+    e = launch_chain(P, stream);
+    if (e != cudaSuccess) return e;
   }
-  P.phases[ph++].op = OP_PACK;
-  P.nphases = ph;
-  if (!maps.ok) return cudaErrorInvalidValue;
-  return launch_chain(P, stream);
+  // D = dQ^T: pack(dQ - dQ^T) = -pack(D - D^T)
+  return launch_pack_tiles(a.d32, -1.f, a.n_a, a.n_b, b, a.dtheta_a, a.dtheta_b, stream);
 }
 
 }  // namespace poetx

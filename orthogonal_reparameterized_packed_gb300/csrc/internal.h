@@ -80,14 +80,15 @@ cudaError_t simt_gemm_run(const SimtGemm& g, cudaStream_t stream);
 // One cooperative launch per chain of b x b products (tensor cores, b a
 // multiple of 128, k <= kChainMaxK); see chain_tc.cu.
 constexpr int kChainMaxK = 8;
+constexpr int kChainMaxPhases = 20;  // >= 2 * kChainMaxK - 1 product phases
 
 // True when the chain of n blocks of size b and order k runs as one launch
 // (b a multiple of 128, k <= kChainMaxK, at most two persistent D tiles per CTA).
 bool chain_fits(int n, int b, int k);
 
 // blocks = (I + Q)(I + Q + ... + Q^k) for the n blocks of one side, bf16 out.
-// Scratch [n][b][b] bf16: q_hi, q_lo, e16[0], e16[1]; two_i [b][b] bf16; one
-// counter word.
+// Scratch [n][b][b] bf16: q_hi, q_lo, e16[0], e16[1]; two_i [b][b] bf16;
+// counter [kChainMaxPhases] words.
 struct ChainBuildArgs {
   int n = 0, b = 0, k = 0;
   const float* theta = nullptr;
@@ -103,7 +104,7 @@ cudaError_t chain_build(const ChainBuildArgs& a, cudaStream_t stream);
 // Packed gradients of both sides from the split-K partials of the TRANSPOSED
 // block gradients G^T (blocks [0, n_a) from part_a / theta_a, the rest from
 // part_b / theta_b).  Scratch [n_a + n_b][b][b]: q16, e16[2..k], f16[0..1]
-// (bf16) and d32 (fp32); two_i [b][b] bf16; one counter word.
+// (bf16) and d32 (fp32); two_i [b][b] bf16; counter [kChainMaxPhases] words.
 struct ChainAdjointArgs {
   int n_a = 0, n_b = 0, b = 0, k = 0;
   const float* theta_a = nullptr;
@@ -142,6 +143,27 @@ cudaError_t launch_reduce_extract(const float* part, int splits, int n, int b, i
 // for n_a + n_b blocks: the first n_a go to dtheta_a, the rest to dtheta_b.
 cudaError_t launch_pack_skew(const float* A, const float* B, int n_a, int n_b, int b,
                              float* dtheta_a, float* dtheta_b, cudaStream_t s);
+// Tiled elementwise steps of the b x b chains (b a multiple of 32), blocks
+// [0, n_a) of side a and [n_a, n_a + n_b) of side b; null outputs are skipped:
+//   q_hi (+ q_lo) = bf16 Q (+ bf16 remainder) from theta;  two_i = 2I;
+//   f16 (+ f32) = sum over splits of the diagonal b-blocks of the partials.
+struct PrepTilesArgs {
+  int n_a = 0, n_b = 0, b = 0;
+  const float* theta_a = nullptr;
+  const float* theta_b = nullptr;
+  __nv_bfloat16* q_hi = nullptr;
+  __nv_bfloat16* q_lo = nullptr;
+  __nv_bfloat16* two_i = nullptr;
+  const float* part_a = nullptr;
+  const float* part_b = nullptr;
+  int splits_a = 1, splits_b = 1, nsb_a = 0, nsb_b = 0, S = 0;
+  __nv_bfloat16* f16 = nullptr;
+  float* f32 = nullptr;
+};
+cudaError_t launch_prep_tiles(const PrepTilesArgs& a, cudaStream_t s);
+// dtheta = sign * pack(D - D^T) per block.
+cudaError_t launch_pack_tiles(const float* D, float sign, int n_a, int n_b, int b,
+                              float* dtheta_a, float* dtheta_b, cudaStream_t s);
 cudaError_t launch_f32_to_bf16(const float* in, long long count, __nv_bfloat16* out,
                                cudaStream_t s);
 

@@ -192,6 +192,117 @@ __global__ void f32_to_bf16_kernel(const float* __restrict__ in, long long count
     out[idx] = __float2bfloat16_rn(in[idx]);
 }
 
+// --------------------------------------------------- 32 x 32 tile kernels
+// One CTA (32 x 8 threads) per 32 x 32 tile (ti, tj) of one b x b block, so
+// the transposed half of a skew matrix is read and written as coalesced
+// 32-element row segments through a shared-memory tile.
+
+constexpr int TT = 32;
+
+// Q from theta for the tile pair (ti, tj), (tj, ti) with ti <= tj; writes
+// the bf16 value (hi) and optionally the bf16 remainder (lo) of each entry.
+__device__ __forceinline__ void unpack_tile_pair(const float* __restrict__ th, int b, int ti,
+                                                 int tj, __nv_bfloat16* __restrict__ hi,
+                                                 __nv_bfloat16* __restrict__ lo,
+                                                 float (*tile)[TT + 1]) {
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  for (int r = ty; r < TT; r += 8) {  // entries (i, j) of tile (ti, tj), upper part only
+    const int i = ti * TT + r, j = tj * TT + tx;
+    tile[r][tx] = i < j ? th[packed_pos(i, j, b)] : 0.f;
+  }
+  __syncthreads();
+  for (int r = ty; r < TT; r += 8) {
+    // tile (ti, tj): Q[i][j] = theta (i < j), -theta[j][i] (i > j, diagonal tile), 0
+    const int i = ti * TT + r, j = tj * TT + tx;
+    float q = tile[r][tx];
+    if (ti == tj && r > tx) q = -tile[tx][r];
+    const int o = i * b + j;
+    const __nv_bfloat16 h = __float2bfloat16_rn(q);
+    hi[o] = h;
+    if (lo != nullptr) lo[o] = __float2bfloat16_rn(q - __bfloat162float(h));
+    if (ti != tj) {  // mirrored tile (tj, ti): Q[j'][i'] = -theta[i'][j']
+      const int i2 = tj * TT + r, j2 = ti * TT + tx;
+      const float q2 = -tile[tx][r];
+      const int o2 = i2 * b + j2;
+      const __nv_bfloat16 h2 = __float2bfloat16_rn(q2);
+      hi[o2] = h2;
+      if (lo != nullptr) lo[o2] = __float2bfloat16_rn(q2 - __bfloat162float(h2));
+    }
+  }
+}
+
+// grid (tiles_per_block^2, n_a + n_b):
+//   Q (bf16, plus lo if q_lo) from theta for tiles with ti <= tj,
+//   2I into two_i for block 0,
+//   F = sum over splits of the diagonal b-block of the partials (if f16).
+__global__ void __launch_bounds__(256) prep_tiles_kernel(PrepTilesArgs a) {
+  __shared__ float tile[TT][TT + 1];
+  const int t = a.b / TT;
+  const int ti = blockIdx.x / t, tj = blockIdx.x % t;
+  const int g = blockIdx.y;
+  const int bb = a.b * a.b;
+  const int m = a.b * (a.b - 1) / 2;
+  const bool side_a = g < a.n_a;
+  const int gl = side_a ? g : g - a.n_a;
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  if (a.f16 != nullptr) {
+    const int per = a.S / a.b;
+    const int sb = gl / per;
+    const int off = (gl - sb * per) * a.b;
+    const float* part = side_a ? a.part_a : a.part_b;
+    const int splits = side_a ? a.splits_a : a.splits_b;
+    const long long stride = static_cast<long long>(side_a ? a.nsb_a : a.nsb_b) * a.S * a.S;
+    for (int r = ty; r < TT; r += 8) {
+      const int i = ti * TT + r, j = tj * TT + tx;
+      const long long src = (static_cast<long long>(sb) * a.S + off + i) * a.S + off + j;
+      float v = 0.f;
+      for (int s = 0; s < splits; ++s) v += part[s * stride + src];
+      const long long o = static_cast<long long>(g) * bb + i * a.b + j;
+      a.f16[o] = __float2bfloat16_rn(v);
+      if (a.f32 != nullptr) a.f32[o] = v;
+    }
+  }
+  if (g == 0 && a.two_i != nullptr) {
+    for (int r = ty; r < TT; r += 8) {
+      const int i = ti * TT + r, j = tj * TT + tx;
+      a.two_i[i * a.b + j] = __float2bfloat16_rn(i == j ? 2.f : 0.f);
+    }
+  }
+  if (ti <= tj && a.q_hi != nullptr) {
+    const float* th = side_a ? a.theta_a + static_cast<long long>(gl) * m
+                             : a.theta_b + static_cast<long long>(gl) * m;
+    unpack_tile_pair(th, a.b, ti, tj, a.q_hi + static_cast<long long>(g) * bb,
+                     a.q_lo != nullptr ? a.q_lo + static_cast<long long>(g) * bb : nullptr, tile);
+  }
+}
+
+// dtheta[g][idx(i,j)] = sign * (D[g][i][j] - D[g][j][i]) for the i < j entries of
+// tile (ti, tj), ti <= tj; grid (tiles_per_block^2, n_a + n_b).
+__global__ void __launch_bounds__(256) pack_tiles_kernel(const float* __restrict__ D, float sign,
+                                                         int n_a, int b,
+                                                         float* __restrict__ dtheta_a,
+                                                         float* __restrict__ dtheta_b) {
+  __shared__ float tile[TT][TT + 1];
+  const int t = b / TT;
+  const int ti = blockIdx.x / t, tj = blockIdx.x % t;
+  if (ti > tj) return;
+  const int g = blockIdx.y;
+  const long long base = static_cast<long long>(g) * b * b;
+  const int m = b * (b - 1) / 2;
+  const int tx = threadIdx.x, ty = threadIdx.y;
+  for (int r = ty; r < TT; r += 8)  // D[j][i] for the tile: rows of tile (tj, ti)
+    tile[r][tx] = D[base + static_cast<long long>(tj * TT + r) * b + ti * TT + tx];
+  __syncthreads();
+  float* out = g < n_a ? dtheta_a + static_cast<long long>(g) * m
+                       : dtheta_b + static_cast<long long>(g - n_a) * m;
+  for (int r = ty; r < TT; r += 8) {
+    const int i = ti * TT + r, j = tj * TT + tx;
+    if (i >= j) continue;
+    const float v = D[base + static_cast<long long>(i) * b + j] - tile[tx][r];
+    out[packed_pos(i, j, b)] = sign * v;
+  }
+}
+
 int ew_grid(long long total) {
   long long blocks = (total + 255) / 256;
   const long long cap = static_cast<long long>(sm_count()) * 16;
@@ -257,6 +368,27 @@ cudaError_t launch_pack_skew(const float* A, const float* B, int n_a, int n_b, i
                              float* dtheta_a, float* dtheta_b, cudaStream_t s) {
   const int total = (n_a + n_b) * b * b;
   POETX_EW_LAUNCH("pack_skew", total, pack_skew_kernel, A, B, n_a, b, total, dtheta_a, dtheta_b);
+}
+
+cudaError_t launch_prep_tiles(const PrepTilesArgs& a, cudaStream_t s) {
+  if (a.b % TT != 0 || a.n_a + a.n_b <= 0) return cudaErrorInvalidValue;
+  const int t = a.b / TT;
+  dim3 grid(t * t, a.n_a + a.n_b);
+  prof_begin("prep_tiles", s);
+  prep_tiles_kernel<<<grid, dim3(TT, 8), 0, s>>>(a);
+  prof_end("prep_tiles", s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_tiles(const float* D, float sign, int n_a, int n_b, int b,
+                              float* dtheta_a, float* dtheta_b, cudaStream_t s) {
+  if (b % TT != 0 || n_a + n_b <= 0) return cudaErrorInvalidValue;
+  const int t = b / TT;
+  dim3 grid(t * t, n_a + n_b);
+  prof_begin("pack_tiles", s);
+  pack_tiles_kernel<<<grid, dim3(TT, 8), 0, s>>>(D, sign, n_a, b, dtheta_a, dtheta_b);
+  prof_end("pack_tiles", s);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_f32_to_bf16(const float* in, long long count, __nv_bfloat16* out,
