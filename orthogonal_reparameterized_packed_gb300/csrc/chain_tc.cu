@@ -17,7 +17,8 @@
 // phase: a CTA without tiles finishes later phases at once, and its early
 // arrivals must not count towards an earlier phase.
 // The launch is cooperative (all CTAs resident); every wait is bounded (2 s)
-// and records POETX_ERR_TIMEOUT.
+// and records POETX_ERR_TIMEOUT.  The counters are zeroed by the tiled prep
+// kernel that always runs right before a chain.
 //
 // This is the pages' "Q^2, Q^3, Q^4 in one fused kernel" of the CNP step,
 // extended to the adjoint; a 256 x 256 bf16 operand pair does not fit one
@@ -163,6 +164,8 @@ __global__ void __launch_bounds__(CH_THREADS, 1) chain_kernel(const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();
+  pdl_trigger();  // the kernel after the chain may start its prologue
 
   if (warp == 0) {
     if (lane == 0) {
@@ -442,8 +445,7 @@ cudaError_t launch_chain(ChainParams& P, cudaStream_t stream) {
         if (q != 0 || (tiles + grid - 1) / grid > kMaxDSlots) return cudaErrorInvalidValue;
       }
   P.status = device_status_ptr();
-  cudaError_t e = cudaMemsetAsync(P.counter, 0, sizeof(unsigned int) * kChainMaxPhases, stream);
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -483,6 +485,8 @@ cudaError_t chain_build(const ChainBuildArgs& a, cudaStream_t stream) {
   pa.q_hi = a.q_hi;
   pa.q_lo = a.q_lo;
   pa.two_i = a.two_i;
+  pa.zero_words = a.counter;
+  pa.n_zero_words = kChainMaxPhases;
   cudaError_t e = launch_prep_tiles(pa, stream);
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(g_chain_mu);
@@ -544,6 +548,8 @@ cudaError_t chain_adjoint(const ChainAdjointArgs& a, cudaStream_t stream) {
   pa.nsb_b = a.nsb_b;
   pa.S = a.S;
   pa.f16 = a.f16[0];
+  pa.zero_words = a.counter;
+  pa.n_zero_words = kChainMaxPhases;
   cudaError_t e = launch_prep_tiles(pa, stream);
   if (e != cudaSuccess) return e;
   {

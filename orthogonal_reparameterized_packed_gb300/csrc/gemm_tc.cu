@@ -154,6 +154,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // the predecessor's outputs are complete from here on
+  pdl_trigger();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -461,10 +463,10 @@ cudaError_t launch_tc(const TcGemm& g, cudaStream_t stream) {
     grid = static_cast<int>((tiles + per - 1) / per);
   }
   prof_begin(g.tag, stream);
-  tc_gemm_kernel<A_MN, B_MN, BN, B_RES, EPI>
-      <<<grid, NUM_THREADS, S::SMEM, stream>>>(tmA, tmB, tmC, p);
+  cudaError_t e = launch_pdl(tc_gemm_kernel<A_MN, B_MN, BN, B_RES, EPI>, dim3(grid),
+                             dim3(NUM_THREADS), S::SMEM, stream, tmA, tmB, tmC, p);
   prof_end(g.tag, stream);
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 bool plain_output(const EpiArgs& e) {

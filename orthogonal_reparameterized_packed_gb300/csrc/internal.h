@@ -2,10 +2,30 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
 namespace poetx {
+
+// Launch with programmatic stream serialization: the kernel may start
+// before its predecessor on `s` has finished; every kernel of the library
+// calls pdl_wait() before it touches global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Where a contraction's result goes: for batch g, K-split s, row r and
 // column c of the (batch-local) result,
@@ -159,6 +179,8 @@ struct PrepTilesArgs {
   int splits_a = 1, splits_b = 1, nsb_a = 0, nsb_b = 0, S = 0;
   __nv_bfloat16* f16 = nullptr;
   float* f32 = nullptr;
+  unsigned int* zero_words = nullptr;  // if set: zeroed (the next chain's barrier counters)
+  int n_zero_words = 0;
 };
 cudaError_t launch_prep_tiles(const PrepTilesArgs& a, cudaStream_t s);
 // dtheta = sign * pack(D - D^T) per block.

@@ -4,6 +4,7 @@
 // small elementwise kernels of the path (unpack, superblock expansion,
 // split-K reduction, skew projection and pack).
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace poetx {
 
@@ -25,6 +26,8 @@ __device__ __forceinline__ float load_f<__nv_bfloat16>(const __nv_bfloat16* p, l
 // C(g) = A(g) * B(g), 64x64 output tile per CTA, 4x4 per thread.
 template <typename T>
 __global__ void __launch_bounds__(SIMT_THREADS) simt_gemm_kernel(const SimtGemm p) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float As[TK][TM + 4];
   __shared__ float Bs[TK][TN + 4];
   const int g = blockIdx.z;
@@ -92,6 +95,8 @@ __device__ __forceinline__ int packed_pos(int i, int j, int b) {
 __global__ void unpack_kernel(const float* __restrict__ theta_a, int n_a,
                               const float* __restrict__ theta_b, int b, int total,
                               float* __restrict__ q32, __nv_bfloat16* __restrict__ q16) {
+  pdl_wait();
+  pdl_trigger();
   const int bb = b * b;
   const int m = b * (b - 1) / 2;
   for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < total;
@@ -111,6 +116,8 @@ __global__ void unpack_kernel(const float* __restrict__ theta_a, int n_a,
 
 __global__ void identity_plus_kernel(const float* __restrict__ q, int b, int total,
                                      float* __restrict__ o32, __nv_bfloat16* __restrict__ o16) {
+  pdl_wait();
+  pdl_trigger();
   const int bb = b * b;
   for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += gridDim.x * blockDim.x) {
@@ -125,6 +132,8 @@ __global__ void identity_plus_kernel(const float* __restrict__ q, int b, int tot
 
 __global__ void expand_superblocks_kernel(const __nv_bfloat16* __restrict__ blocks, int n, int b,
                                           int S, int total, __nv_bfloat16* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   const int per = S / b;
   for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += gridDim.x * blockDim.x) {
@@ -143,6 +152,8 @@ __global__ void expand_superblocks_kernel(const __nv_bfloat16* __restrict__ bloc
 __global__ void reduce_extract_kernel(const float* __restrict__ part, int splits, int n, int b,
                                       int S, int total, float* __restrict__ o32,
                                       __nv_bfloat16* __restrict__ o16) {
+  pdl_wait();
+  pdl_trigger();
   const int per = S / b;
   const int nsb = (n + per - 1) / per;
   const long long split_stride = static_cast<long long>(nsb) * S * S;
@@ -168,6 +179,8 @@ __global__ void reduce_extract_kernel(const float* __restrict__ part, int splits
 __global__ void pack_skew_kernel(const float* __restrict__ A, const float* __restrict__ B, int n_a,
                                  int b, int total, float* __restrict__ dtheta_a,
                                  float* __restrict__ dtheta_b) {
+  pdl_wait();
+  pdl_trigger();
   const int m = b * (b - 1) / 2;
   const int bb = b * b;
   for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < total;
@@ -187,6 +200,8 @@ __global__ void pack_skew_kernel(const float* __restrict__ A, const float* __res
 
 __global__ void f32_to_bf16_kernel(const float* __restrict__ in, long long count,
                                    __nv_bfloat16* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < count;
        idx += static_cast<long long>(gridDim.x) * blockDim.x)
     out[idx] = __float2bfloat16_rn(in[idx]);
@@ -236,6 +251,8 @@ __device__ __forceinline__ void unpack_tile_pair(const float* __restrict__ th, i
 //   2I into two_i for block 0,
 //   F = sum over splits of the diagonal b-block of the partials (if f16).
 __global__ void __launch_bounds__(256) prep_tiles_kernel(PrepTilesArgs a) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float tile[TT][TT + 1];
   const int t = a.b / TT;
   const int ti = blockIdx.x / t, tj = blockIdx.x % t;
@@ -245,6 +262,9 @@ __global__ void __launch_bounds__(256) prep_tiles_kernel(PrepTilesArgs a) {
   const bool side_a = g < a.n_a;
   const int gl = side_a ? g : g - a.n_a;
   const int tx = threadIdx.x, ty = threadIdx.y;
+  if (a.zero_words != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && ty == 0 &&
+      tx < a.n_zero_words)
+    a.zero_words[tx] = 0u;
   if (a.f16 != nullptr) {
     const int per = a.S / a.b;
     const int sb = gl / per;
@@ -282,6 +302,8 @@ __global__ void __launch_bounds__(256) pack_tiles_kernel(const float* __restrict
                                                          int n_a, int b,
                                                          float* __restrict__ dtheta_a,
                                                          float* __restrict__ dtheta_b) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float tile[TT][TT + 1];
   const int t = b / TT;
   const int ti = blockIdx.x / t, tj = blockIdx.x % t;
@@ -319,21 +341,21 @@ cudaError_t simt_gemm_run(const SimtGemm& g, cudaStream_t stream) {
   dim3 grid((g.N + TN - 1) / TN, (g.M + TM - 1) / TM, g.batches);
   if (grid.y > 65535) return cudaErrorInvalidValue;
   prof_begin(g.tag, stream);
-  if (g.bf16_inputs)
-    simt_gemm_kernel<__nv_bfloat16><<<grid, SIMT_THREADS, 0, stream>>>(g);
-  else
-    simt_gemm_kernel<float><<<grid, SIMT_THREADS, 0, stream>>>(g);
+  cudaError_t e =
+      g.bf16_inputs
+          ? launch_pdl(simt_gemm_kernel<__nv_bfloat16>, grid, dim3(SIMT_THREADS), 0, stream, g)
+          : launch_pdl(simt_gemm_kernel<float>, grid, dim3(SIMT_THREADS), 0, stream, g);
   prof_end(g.tag, stream);
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 #define POETX_EW_LAUNCH(tag, total, kernel, ...)                         \
   do {                                                                   \
     if ((total) <= 0) return cudaSuccess;                                \
     prof_begin(tag, s);                                                  \
-    kernel<<<ew_grid(total), 256, 0, s>>>(__VA_ARGS__);                  \
+    cudaError_t e_ = launch_pdl(kernel, dim3(ew_grid(total)), dim3(256), 0, s, __VA_ARGS__); \
     prof_end(tag, s);                                                    \
-    return cudaGetLastError();                                           \
+    return e_ != cudaSuccess ? e_ : cudaGetLastError();                  \
   } while (0)
 
 cudaError_t launch_unpack(const float* theta_a, int n_a, const float* theta_b, int n_b, int b,
@@ -375,9 +397,9 @@ cudaError_t launch_prep_tiles(const PrepTilesArgs& a, cudaStream_t s) {
   const int t = a.b / TT;
   dim3 grid(t * t, a.n_a + a.n_b);
   prof_begin("prep_tiles", s);
-  prep_tiles_kernel<<<grid, dim3(TT, 8), 0, s>>>(a);
+  cudaError_t e = launch_pdl(prep_tiles_kernel, grid, dim3(TT, 8), 0, s, a);
   prof_end("prep_tiles", s);
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_pack_tiles(const float* D, float sign, int n_a, int n_b, int b,
@@ -386,9 +408,10 @@ cudaError_t launch_pack_tiles(const float* D, float sign, int n_a, int n_b, int 
   const int t = b / TT;
   dim3 grid(t * t, n_a + n_b);
   prof_begin("pack_tiles", s);
-  pack_tiles_kernel<<<grid, dim3(TT, 8), 0, s>>>(D, sign, n_a, b, dtheta_a, dtheta_b);
+  cudaError_t e = launch_pdl(pack_tiles_kernel, grid, dim3(TT, 8), 0, s, D, sign, n_a, b,
+                             dtheta_a, dtheta_b);
   prof_end("pack_tiles", s);
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_f32_to_bf16(const float* in, long long count, __nv_bfloat16* out,

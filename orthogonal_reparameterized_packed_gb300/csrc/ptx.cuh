@@ -72,6 +72,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// ------------------------------------------- programmatic dependent launch
+// Kernels are launched so that they may start while their predecessor on the
+// stream is still finishing: pdl_wait() blocks until the predecessor grid has
+// completed and its writes are visible (no-op when launched normally), and
+// pdl_trigger() lets the next kernel start its own prologue early.
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* tm) {
