@@ -24,6 +24,10 @@ Sources (one web page each; the method's own paper is not available):
   [tech-2-bd] section 2, bullet "Batch-parallele Berechnung fuer
               Block-diagonale Matrizen": R and P are block diagonal; the
               blocks are independent matrices multiplied as a batch.
+  [tech-2-perm] section 2, bullet "Permutations-Beschleunigung und
+              -Reduktion": POET mixes the blocks with permutation matrices;
+              POET-X applies the permutations as index maps on the data and
+              folds two of the four forward permutations into W once.
   [tech-2-cnp] section 2, bullet "Effiziente Cayley-Neumann-
               Parametrisierung (CNP)": the orthogonal blocks come from
               skew-symmetric Q (Q = -Q^T) through the Cayley transform with
@@ -245,6 +249,60 @@ def transform(theta, x, dout, b: int, k: int):
     G = blockwise_outer(dout, x, b)
     dtheta = pack_skew_grad(cnp_adjoint(Q, G, k))
     return dict(blocks=B, z=z, dx=dx, G=G, dtheta=dtheta)
+
+
+# --------------------------------------------------------------------------
+# Permuted blocks  [tech-2-perm], with explicit permutation matrices
+# --------------------------------------------------------------------------
+
+def permutation_matrix(perm) -> np.ndarray:
+    """Pi with (Pi x)[i] = x[perm[i]]."""
+    perm = np.asarray(perm)
+    return np.eye(len(perm))[perm]
+
+
+def layer_permuted(theta_P, theta_R, W0, x, dy, b: int, k: int, perm_P, perm_R):
+    """The layer with permuted block-diagonal factors, written with dense
+    matrices: R = Pi_R^T B_R Pi_R, P = Pi_P^T B_P Pi_P, y_t = R W0 P x_t.
+    Gradients of L = sum_t <dy_t, y_t> by the chain rule through the dense
+    matrices; the block gradients are the diagonal blocks of the dense
+    gradients taken in the permuted basis."""
+    x = np.asarray(x, dtype=np.float64)
+    dy = np.asarray(dy, dtype=np.float64)
+    W0 = np.asarray(W0, dtype=np.float64)
+    Q_P = unpack(theta_P, b)
+    Q_R = unpack(theta_R, b)
+    BP = dense_from_blocks(cayley_neumann(Q_P, k))
+    BR = dense_from_blocks(cayley_neumann(Q_R, k))
+    PiP = permutation_matrix(perm_P)
+    PiR = permutation_matrix(perm_R)
+    P = PiP.T @ BP @ PiP
+    R = PiR.T @ BR @ PiR
+    y = x @ (R @ W0 @ P).T
+    dx = dy @ (R @ W0 @ P)
+    # dL/dBR = sum_t (Pi_R dy_t)(Pi_R W0 P x_t)^T ; dL/dBP = sum_t (Pi_P P^T... )
+    a_R = dy @ PiR.T                      # rows: Pi_R dy_t
+    c_R = x @ (PiR @ W0 @ P).T            # rows: Pi_R W0 P x_t
+    dBR = a_R.T @ c_R
+    a_P = dy @ (R @ W0 @ PiP.T)           # rows: Pi_P W0^T R^T dy_t
+    c_P = x @ PiP.T                       # rows: Pi_P x_t
+    dBP = a_P.T @ c_P
+    nP, nR = BP.shape[0] // b, BR.shape[0] // b
+    G_P = np.stack([dBP[g * b:(g + 1) * b, g * b:(g + 1) * b] for g in range(nP)])
+    G_R = np.stack([dBR[g * b:(g + 1) * b, g * b:(g + 1) * b] for g in range(nR)])
+    return dict(y=y, dx=dx,
+                dtheta_P=pack_skew_grad(cnp_adjoint(Q_P, G_P, k)),
+                dtheta_R=pack_skew_grad(cnp_adjoint(Q_R, G_R, k)))
+
+
+def loss_permuted(theta_P, theta_R, W0, x, dy, b, k, perm_P, perm_R) -> float:
+    BP = dense_from_blocks(build_blocks(theta_P, b, k))
+    BR = dense_from_blocks(build_blocks(theta_R, b, k))
+    PiP = permutation_matrix(perm_P)
+    PiR = permutation_matrix(perm_R)
+    W = PiR.T @ BR @ PiR @ np.asarray(W0, np.float64) @ PiP.T @ BP @ PiP
+    y = np.asarray(x, np.float64) @ W.T
+    return float(np.sum(np.asarray(dy, np.float64) * y))
 
 
 # --------------------------------------------------------------------------

@@ -291,3 +291,52 @@ def test_transform_gradients_match_central_differences():
     # block-diagonal application against scipy's dense block_diag
     D = scipy.linalg.block_diag(*out["blocks"])
     np.testing.assert_allclose(out["z"], x @ D.T, rtol=0, atol=1e-13)
+
+
+# ------------------------------------------------- permuted blocks
+
+def test_permuted_layer_with_identity_permutations_is_the_plain_layer():
+    inp = make_layer_inputs(12, 8, 4, 3, 5, dtype="f32", sigma_theta=0.3, seed=15)
+    a = oracle.layer(inp.theta_P, inp.theta_R, inp.W0, inp.x, inp.dy, 4, 3)
+    p = oracle.layer_permuted(inp.theta_P, inp.theta_R, inp.W0, inp.x, inp.dy, 4, 3,
+                              np.arange(12), np.arange(8))
+    for name in ("y", "dx", "dtheta_P", "dtheta_R"):
+        np.testing.assert_allclose(p[name], a[name], rtol=1e-12, atol=1e-12)
+
+
+def test_permutation_matrix_gathers():
+    perm = np.array([2, 0, 3, 1])
+    x = np.array([10.0, 11.0, 12.0, 13.0])
+    assert list(oracle.permutation_matrix(perm) @ x) == [12.0, 10.0, 13.0, 11.0]
+
+
+def test_permuted_layer_gradients_match_central_differences():
+    rng = np.random.default_rng(16)
+    inp = make_layer_inputs(8, 12, 4, 2, 4, dtype="f32", sigma_theta=0.3, seed=17)
+    pP, pR = rng.permutation(8), rng.permutation(12)
+    tP = inp.theta_P.astype(np.float64)
+    tR = inp.theta_R.astype(np.float64)
+    x = inp.x.astype(np.float64)
+    W0 = inp.W0.astype(np.float64)
+    dy = inp.dy.astype(np.float64)
+    out = oracle.layer_permuted(tP, tR, W0, x, dy, 4, 2, pP, pR)
+
+    def L(a, c, xx):
+        return oracle.loss_permuted(a, c, W0, xx, dy, 4, 2, pP, pR)
+
+    for idx in np.ndindex(*tP.shape):
+        fd = _central_diff(lambda t: L(t, tR, x), tP, idx, 1e-6)
+        assert abs(out["dtheta_P"][idx] - fd) <= 1e-6 * max(1e-8, abs(fd))
+    for idx in np.ndindex(*tR.shape):
+        fd = _central_diff(lambda t: L(tP, t, x), tR, idx, 1e-6)
+        assert abs(out["dtheta_R"][idx] - fd) <= 1e-6 * max(1e-8, abs(fd))
+    for idx in [(0, 1), (3, 7)]:
+        fd = _central_diff(lambda xx: L(tP, tR, xx), x, idx, 1e-6)
+        assert abs(out["dx"][idx] - fd) <= 1e-6 * max(1e-8, abs(fd))
+    # y from the dense product
+    assert np.allclose(out["y"], x @ (oracle.permutation_matrix(pR).T
+                                      @ oracle.dense_from_blocks(oracle.build_blocks(tR, 4, 2))
+                                      @ oracle.permutation_matrix(pR) @ W0
+                                      @ oracle.permutation_matrix(pP).T
+                                      @ oracle.dense_from_blocks(oracle.build_blocks(tP, 4, 2))
+                                      @ oracle.permutation_matrix(pP)).T)
