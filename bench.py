@@ -46,6 +46,11 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true",
                     help="time eager launches instead of CUDA-graph replays")
+    ap.add_argument("--permute", action="store_true",
+                    help="permuted block-diagonal factors (index maps around the plain step; "
+                         "the two inner permutations folded into W0 once, before timing)")
+    ap.add_argument("--recompute-v", action="store_true",
+                    help="backward recomputes v = W0 P x instead of reading it (saves T x d_out)")
     return ap.parse_args()
 
 
@@ -54,10 +59,15 @@ def workload_config(name):
     return w
 
 
-def config_json(name, w, n):
-    return {"workload": name, "d_in": w["d_in"], "d_out": w["d_out"], "b": w["b"], "k": w["k"],
-            "tokens_per_gpu": w["tokens"], "dtype": w["dtype"], "parallelism": f"replicas{n}",
-            "l2": "inputs larger than L2 (x, dy 128 MiB each; ~1 GB touched per step)"}
+def config_json(name, w, n, args=None):
+    c = {"workload": name, "d_in": w["d_in"], "d_out": w["d_out"], "b": w["b"], "k": w["k"],
+         "tokens_per_gpu": w["tokens"], "dtype": w["dtype"], "parallelism": f"replicas{n}",
+         "l2": "inputs larger than L2 (x, dy 128 MiB each; ~1 GB touched per step)"}
+    if args is not None and getattr(args, "permute", False):
+        c["permuted_blocks"] = True
+    if args is not None and getattr(args, "recompute_v", False):
+        c["recompute_v"] = True
+    return c
 
 
 # ----------------------------------------------------------- CPU oracle
@@ -281,11 +291,23 @@ def run_gpu(args):
     w = workload_config(name)
     inp = make_layer_inputs(**w, seed=rank)
     dev = to_device(inp)
-    layer = PoetxLayer(w["d_in"], w["d_out"], w["b"], w["k"], w["tokens"], dtype=w["dtype"])
     stream = torch.cuda.current_stream()
+    if args.permute:
+        from orthogonal_reparameterized_packed_gb300.layer import PoetxPermutedLayer
+        prng = np.random.default_rng(1000 + rank)
+        layer = PoetxPermutedLayer(w["d_in"], w["d_out"], w["b"], w["k"], w["tokens"],
+                                   prng.permutation(w["d_in"]), prng.permutation(w["d_out"]),
+                                   dtype=w["dtype"])
+        layer.fold(dev["W0"])  # once per weight, outside the timed steps
 
-    def step():
-        layer.step(dev["theta_P"], dev["theta_R"], dev["W0"], dev["x"], dev["dy"])
+        def step():
+            layer.step(dev["theta_P"], dev["theta_R"], dev["x"], dev["dy"])
+    else:
+        layer = PoetxLayer(w["d_in"], w["d_out"], w["b"], w["k"], w["tokens"], dtype=w["dtype"],
+                           recompute_v=args.recompute_v)
+
+        def step():
+            layer.step(dev["theta_P"], dev["theta_R"], dev["W0"], dev["x"], dev["dy"])
 
     def barrier():
         if world > 1:
@@ -364,7 +386,7 @@ def run_gpu(args):
     # per-kernel times over the timed region
     tags = ["build", "unpack", "identity_plus", "expand_superblocks", "transform",
             "transform_t", "gemm_w0", "gemm_w0_dgrad", "outer", "reduce_extract", "cnp_bwd",
-            "pack_skew", "f32_to_bf16", "chain"]
+            "pack_skew", "f32_to_bf16", "chain", "prep_tiles", "pack_tiles", "permute"]
     kernels = {}
     for t in tags:
         n, tot = poetx.poetx_profile_query(t)
@@ -383,6 +405,15 @@ def run_gpu(args):
                 "peak_source": f"{peak_src} ({'sustained' if long_region else 'burst'})",
                 "per_launch": f"2*T*d_in*d_out = {amount:.4f} TFLOP",
                 "timing": "CUDA events around each launch, eager pass of the same K steps"}
+
+    if "permute" in kernels:  # index-map kernel: HBM-bound, reads and writes T x d
+        pk = kernels["permute"]
+        dsum = w["d_in"] + w["d_out"]  # per step: 2 maps over d_in, 2 over d_out
+        moved = 2.0 * w["tokens"] * dsum * 2 * 2  # read + write, bf16, 4 launches
+        gbs = moved / (pk["total_ms"] / args.steps * 1e-3) / 1e9
+        roofline["secondary"] = {"kernel": "permute", "bound": "hbm", "achieved": gbs,
+                                 "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                 "frac": gbs / peaks["hbm_gbs"]}
 
     # whole-step algorithmic tensor work for context
     T, di, do, b = w["tokens"], w["d_in"], w["d_out"], w["b"]
@@ -434,7 +465,7 @@ def run_gpu(args):
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
                 "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_max,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": "bf16", "data": "synthetic", "config": config_json(name, w, world),
+                "dtype": "bf16", "data": "synthetic", "config": config_json(name, w, world, args),
                 "gpu_launches": launches, "launch": "cuda_graph" if graph is not None else "eager",
                 "graph_error": graph_error,
                 "ms_per_step_eager": ms_eager, "roofline": roofline,

@@ -166,6 +166,30 @@ poetx_status poetx_transform_backward(const void* dout, const void* x, const flo
                                       size_t workspace_bytes, poetx_stream stream);
 
 /* ------------------------------------------------------------------------
+ * Permuted blocks (technical summary, section 2, "Permutations-Beschleunigung
+ * und -Reduktion"): POET mixes the blocks as R = Pi_R^T B_R Pi_R and
+ * P = Pi_P^T B_P Pi_P; POET-X applies the permutations to the data as index
+ * maps and folds the two inner ones into the weight once, so that
+ *     y = Pi_R^T B_R W0' B_P Pi_P x,   W0' = Pi_R W0 Pi_P^T.
+ * A permuted step is: x' = Pi_P x, the plain forward/backward on
+ * (x', W0', blocks), y = Pi_R^T y', dy' = Pi_R dy, dx = Pi_P^T dx'; the
+ * packed gradients come out of the plain backward unchanged.
+ *   perm arrays: int32 device arrays holding a permutation of 0..d-1;
+ *   (Pi x)[i] = x[perm[i]], so Pi^T is applied with the inverse permutation.
+ *   Entries outside 0..d-1 are not followed: the output gets 0 and
+ *   POETX_ERR_INVALID_ARG is recorded in the status word.  Rows must be a
+ *   multiple of 16 bytes and at most 100 KiB (d <= 51200 bf16, 25600 fp32).
+ * ------------------------------------------------------------------------ */
+/* out[r][i] = in[r][perm[i]] for rows x d activations (in != out). */
+poetx_status poetx_permute_features(const void* in, const int32_t* perm, void* out, int64_t rows,
+                                    int d, poetx_dtype dtype, poetx_stream stream);
+/* W0_folded[i][j] = W0[perm_out[i]][perm_in[j]], i.e. Pi_R W0 Pi_P^T with
+ * perm_out = the permutation of R and perm_in = the permutation of P. */
+poetx_status poetx_fold_permutations(const void* W0, const int32_t* perm_out,
+                                     const int32_t* perm_in, void* W0_folded, int d_in,
+                                     int d_out, poetx_dtype dtype, poetx_stream stream);
+
+/* ------------------------------------------------------------------------
  * Status and measurement
  * ------------------------------------------------------------------------ */
 /* Synchronizes the current device, returns the status recorded by kernels

@@ -19,6 +19,7 @@ __all__ = [
     "poetx_forward_workspace_size", "poetx_forward",
     "poetx_backward_workspace_size", "poetx_backward",
     "poetx_transform_workspace_size", "poetx_transform_forward", "poetx_transform_backward",
+    "poetx_permute_features", "poetx_fold_permutations",
     "poetx_device_status", "poetx_selftest_wait_timeout", "poetx_launch_count", "poetx_profile_start", "poetx_profile_stop",
     "poetx_profile_query", "poetx_status_string", "EXPORTED_SYMBOLS",
 ]
@@ -56,6 +57,9 @@ _SIGNATURES = {
     "poetx_transform_backward": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int,
                                           _c_int, _c_int, _c_i64, _c_int, _c_ptr, _c_size,
                                           _c_ptr]),
+    "poetx_permute_features": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_i64, _c_int, _c_int, _c_ptr]),
+    "poetx_fold_permutations": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_int, _c_int,
+                                         _c_ptr]),
     "poetx_device_status": (_c_int, []),
     "poetx_selftest_wait_timeout": (_c_int, [ctypes.c_uint, _c_ptr]),
     "poetx_launch_count": (ctypes.c_longlong, []),
@@ -183,6 +187,17 @@ def poetx_transform_backward(dout, x, theta, blocks, dx, dtheta, d, b, k, tokens
     _check("poetx_transform_backward", load_library().poetx_transform_backward(
         _ptr(dout), _ptr(x), _ptr(theta), _ptr(blocks), _ptr(dx), _ptr(dtheta), d, b, k, tokens,
         dtype, _ptr(workspace), _nbytes(workspace), _stream(stream)))
+
+
+def poetx_permute_features(inp, perm, out, rows, d, dtype, stream=None):
+    _check("poetx_permute_features", load_library().poetx_permute_features(
+        _ptr(inp), _ptr(perm), _ptr(out), rows, d, dtype, _stream(stream)))
+
+
+def poetx_fold_permutations(W0, perm_out, perm_in, W0_folded, d_in, d_out, dtype, stream=None):
+    _check("poetx_fold_permutations", load_library().poetx_fold_permutations(
+        _ptr(W0), _ptr(perm_out), _ptr(perm_in), _ptr(W0_folded), d_in, d_out, dtype,
+        _stream(stream)))
 
 
 def poetx_device_status() -> int:

@@ -325,6 +325,71 @@ __global__ void __launch_bounds__(256) pack_tiles_kernel(const float* __restrict
   }
 }
 
+// out[r][i] = in[row_map ? row_map[r] : r][col_map[i]] for r < rows, i < d.
+// One warp per row: the warp reads its source row with 16-byte coalesced
+// loads into its own slice of shared memory, then each lane gathers 16 bytes
+// of consecutive outputs (column map read as 16-byte vectors) and writes them
+// with one 16-byte store.  Only __syncwarp separates the two halves, so the
+// eight warps of a CTA stream rows independently.  Map entries outside
+// [0, d) (or [0, in_rows)) are not followed: the output gets 0 and the
+// status word POETX_ERR_INVALID_ARG.
+constexpr int kPermWarps = 8;
+
+template <typename T>
+__global__ void __launch_bounds__(kPermWarps * 32)
+    permute_rows_kernel(const T* __restrict__ in, long long in_rows,
+                        const int* __restrict__ row_map, const int* __restrict__ col_map,
+                        T* __restrict__ out, long long rows, int d, int* status) {
+  pdl_wait();
+  pdl_trigger();
+  extern __shared__ __align__(16) unsigned char row_smem[];
+  constexpr int V = 16 / sizeof(T);  // elements per 16-byte vector
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  T* rb = reinterpret_cast<T*>(row_smem) + static_cast<long long>(warp) * d;
+  const int nv = d / V;
+  const int nwarps = blockDim.x / 32;
+  const long long wstride = static_cast<long long>(gridDim.x) * nwarps;
+  for (long long r = static_cast<long long>(blockIdx.x) * nwarps + warp; r < rows;
+       r += wstride) {
+    long long src = r;
+    if (row_map != nullptr) {
+      const int m = row_map[r];
+      src = (m >= 0 && m < in_rows) ? m : -1;
+      if (src < 0 && lane == 0) atomicCAS(status, 0, 1);
+    }
+    if (src >= 0) {
+      const uint4* s4 = reinterpret_cast<const uint4*>(in + src * d);
+      uint4* b4 = reinterpret_cast<uint4*>(rb);
+      for (int v = lane; v < nv; v += 32) b4[v] = s4[v];
+    }
+    __syncwarp();
+    uint4* o4 = reinterpret_cast<uint4*>(out + r * d);
+    const int4* c4 = reinterpret_cast<const int4*>(col_map);
+    for (int v = lane; v < nv; v += 32) {
+      int cols[V];
+#pragma unroll
+      for (int q = 0; q < V / 4; ++q) {
+        const int4 c = c4[v * (V / 4) + q];
+        cols[4 * q + 0] = c.x;
+        cols[4 * q + 1] = c.y;
+        cols[4 * q + 2] = c.z;
+        cols[4 * q + 3] = c.w;
+      }
+      alignas(16) T vals[V];
+      bool bad = false;
+#pragma unroll
+      for (int e = 0; e < V; ++e) {
+        const bool in_range = src >= 0 && cols[e] >= 0 && cols[e] < d;
+        bad |= src >= 0 && !in_range;
+        vals[e] = in_range ? rb[cols[e]] : T(0.f);
+      }
+      if (bad) atomicCAS(status, 0, 1);
+      o4[v] = *reinterpret_cast<const uint4*>(vals);
+    }
+    __syncwarp();  // the row buffer is free for the next row
+  }
+}
+
 int ew_grid(long long total) {
   long long blocks = (total + 255) / 256;
   const long long cap = static_cast<long long>(sm_count()) * 16;
@@ -411,6 +476,39 @@ cudaError_t launch_pack_tiles(const float* D, float sign, int n_a, int n_b, int 
   cudaError_t e = launch_pdl(pack_tiles_kernel, grid, dim3(TT, 8), 0, s, D, sign, n_a, b,
                              dtheta_a, dtheta_b);
   prof_end("pack_tiles", s);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_permute_rows(const void* in, long long in_rows, const int* row_map,
+                                const int* col_map, void* out, long long rows, int d,
+                                bool is_bf16, cudaStream_t s) {
+  if (rows <= 0 || d <= 0) return cudaSuccess;
+  const size_t row_bytes = static_cast<size_t>(d) * (is_bf16 ? 2 : 4);
+  if (row_bytes > 100 * 1024) return cudaErrorInvalidValue;
+  int warps = static_cast<int>((200 * 1024) / row_bytes);  // one row buffer per warp
+  if (warps > kPermWarps) warps = kPermWarps;
+  const size_t smem = row_bytes * warps;
+  const long long groups = (rows + warps - 1) / warps;
+  const long long cap = static_cast<long long>(sm_count()) * 8;
+  const dim3 grid(static_cast<unsigned>(groups < cap ? groups : cap));
+  cudaError_t e;
+  prof_begin("permute", s);
+  if (is_bf16) {
+    if (smem > 48 * 1024)
+      cudaFuncSetAttribute(permute_rows_kernel<__nv_bfloat16>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    e = launch_pdl(permute_rows_kernel<__nv_bfloat16>, grid, dim3(warps * 32), smem, s,
+                   static_cast<const __nv_bfloat16*>(in), in_rows, row_map, col_map,
+                   static_cast<__nv_bfloat16*>(out), rows, d, device_status_ptr());
+  } else {
+    if (smem > 48 * 1024)
+      cudaFuncSetAttribute(permute_rows_kernel<float>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    e = launch_pdl(permute_rows_kernel<float>, grid, dim3(warps * 32), smem, s,
+                   static_cast<const float*>(in), in_rows, row_map, col_map,
+                   static_cast<float*>(out), rows, d, device_status_ptr());
+  }
+  prof_end("permute", s);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

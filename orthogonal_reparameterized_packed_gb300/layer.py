@@ -8,8 +8,8 @@ from __future__ import annotations
 import torch
 
 from . import (BF16, F32, poetx_backward, poetx_backward_workspace_size, poetx_build_blocks,
-               poetx_build_workspace_size, poetx_forward, poetx_forward_workspace_size,
-               poetx_packed_size)
+               poetx_build_workspace_size, poetx_fold_permutations, poetx_forward,
+               poetx_forward_workspace_size, poetx_packed_size, poetx_permute_features)
 
 _TORCH_DTYPE = {F32: torch.float32, BF16: torch.bfloat16}
 
@@ -80,3 +80,55 @@ def to_device(inp, device="cuda"):
     return dict(theta_P=torch.from_numpy(inp.theta_P).to(device).contiguous(),
                 theta_R=torch.from_numpy(inp.theta_R).to(device).contiguous(),
                 W0=act(inp.W0), x=act(inp.x), dy=act(inp.dy))
+
+
+class PoetxPermutedLayer:
+    """One projection with permuted block-diagonal factors,
+    R = Pi_R^T B_R Pi_R and P = Pi_P^T B_P Pi_P.  The two inner permutations
+    are folded into the weight once (fold()); each step applies the outer two
+    to the activations as index maps around a plain PoetxLayer step."""
+
+    def __init__(self, d_in, d_out, b, k, tokens, perm_P, perm_R, dtype="bf16", device="cuda"):
+        import numpy as np
+        self.inner = PoetxLayer(d_in, d_out, b, k, tokens, dtype=dtype, device=device)
+        self.code = self.inner.code
+        dev = torch.device(device)
+
+        def as_dev(p):
+            return torch.from_numpy(np.ascontiguousarray(p, dtype=np.int32)).to(dev)
+
+        perm_P = np.asarray(perm_P)
+        perm_R = np.asarray(perm_R)
+        self.perm_P, self.perm_R = as_dev(perm_P), as_dev(perm_R)
+        self.inv_P, self.inv_R = as_dev(np.argsort(perm_P)), as_dev(np.argsort(perm_R))
+        tdt = _TORCH_DTYPE[self.code]
+        self.W0_folded = torch.empty((d_out, d_in), dtype=tdt, device=dev)
+        self.xp = torch.empty((tokens, d_in), dtype=tdt, device=dev)
+        self.dyp = torch.empty((tokens, d_out), dtype=tdt, device=dev)
+        self.y = torch.empty((tokens, d_out), dtype=tdt, device=dev)
+        self.dx = torch.empty((tokens, d_in), dtype=tdt, device=dev)
+
+    @property
+    def dtheta_P(self):
+        return self.inner.dtheta_P
+
+    @property
+    def dtheta_R(self):
+        return self.inner.dtheta_R
+
+    def fold(self, W0, stream=None):
+        """W0' = Pi_R W0 Pi_P^T, once per weight."""
+        poetx_fold_permutations(W0, self.perm_R, self.perm_P, self.W0_folded, self.inner.d_in,
+                                self.inner.d_out, self.code, stream)
+
+    def step(self, theta_P, theta_R, x, dy, stream=None):
+        L = self.inner
+        T = L.tokens
+        poetx_permute_features(x, self.perm_P, self.xp, T, L.d_in, self.code, stream)
+        L.build(theta_P, theta_R, stream)
+        L.forward(self.xp, self.W0_folded, stream)
+        poetx_permute_features(L.y, self.inv_R, self.y, T, L.d_out, self.code, stream)
+        poetx_permute_features(dy, self.perm_R, self.dyp, T, L.d_out, self.code, stream)
+        L.backward(self.dyp, self.xp, self.W0_folded, theta_P, theta_R, stream)
+        poetx_permute_features(L.dx, self.inv_P, self.dx, T, L.d_in, self.code, stream)
+        return self.y, self.dx, L.dtheta_P, L.dtheta_R

@@ -1,0 +1,92 @@
+"""Permuted block-diagonal factors (R = Pi_R^T B_R Pi_R, P = Pi_P^T B_P Pi_P)
+through the C ABI: the weight fold, the activation index maps and a whole
+permuted step against the dense-permutation-matrix oracle.  Index maps are
+bit-exact; the step uses the layer tolerances (1e-4 fp32, 2e-2 bf16)."""
+
+import numpy as np
+import pytest
+
+import oracle
+from orthogonal_reparameterized_packed_gb300.inputs import make_layer_inputs
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-4, "bf16": 2e-2}
+
+
+@pytest.fixture(scope="module")
+def px():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    import orthogonal_reparameterized_packed_gb300 as poetx
+    poetx.load_library()
+    return poetx
+
+
+def rel_fro(got, want):
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    return float(np.linalg.norm(got - want) / max(np.linalg.norm(want), 1e-300))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_index_maps_are_exact(px, dtype):
+    rng = np.random.default_rng(40)
+    T, d = 37, 1024
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    code = px.BF16 if dtype == "bf16" else px.F32
+    x = torch.randn((T, d), device="cuda").to(tdt)
+    perm = rng.permutation(d).astype(np.int32)
+    out = torch.empty_like(x)
+    px.poetx_permute_features(x, torch.from_numpy(perm).cuda(), out, T, d, code)
+    torch.cuda.synchronize()
+    assert px.poetx_device_status() == 0
+    assert torch.equal(out, x[:, torch.from_numpy(perm).long().cuda()])
+    # fold: W'[i][j] = W[perm_out[i]][perm_in[j]]
+    W = torch.randn((512, d), device="cuda").to(tdt)
+    po = rng.permutation(512).astype(np.int32)
+    Wf = torch.empty_like(W)
+    px.poetx_fold_permutations(W, torch.from_numpy(po).cuda(), torch.from_numpy(perm).cuda(), Wf,
+                               d, 512, code)
+    torch.cuda.synchronize()
+    want = W[torch.from_numpy(po).long().cuda()][:, torch.from_numpy(perm).long().cuda()]
+    assert torch.equal(Wf, want)
+
+
+def test_out_of_range_map_entries_are_not_followed(px):
+    x = torch.randn((4, 256), device="cuda").to(torch.bfloat16)
+    perm = np.arange(256, dtype=np.int32)
+    perm[5] = 999  # out of range
+    out = torch.full_like(x, 7.0)
+    px.poetx_permute_features(x, torch.from_numpy(perm).cuda(), out, 4, 256, px.BF16)
+    torch.cuda.synchronize()
+    assert px.poetx_device_status() == 1  # POETX_ERR_INVALID_ARG recorded
+    assert torch.all(out[:, 5] == 0)
+    assert torch.equal(out[:, :5], x[:, :5])
+
+
+@pytest.mark.parametrize("d_in,d_out,b,k,T,dtype", [
+    (512, 768, 256, 3, 200, "bf16"),
+    (256, 512, 128, 2, 130, "bf16"),
+    (256, 256, 32, 3, 96, "f32"),
+])
+def test_permuted_step_matches_oracle(px, d_in, d_out, b, k, T, dtype):
+    from orthogonal_reparameterized_packed_gb300.layer import PoetxPermutedLayer, to_device
+    rng = np.random.default_rng(41)
+    perm_P, perm_R = rng.permutation(d_in), rng.permutation(d_out)
+    inp = make_layer_inputs(d_in, d_out, b, k, T, dtype=dtype, seed=42)
+    dev = to_device(inp)
+    layer = PoetxPermutedLayer(d_in, d_out, b, k, T, perm_P, perm_R, dtype=dtype)
+    layer.fold(dev["W0"])
+    layer.step(dev["theta_P"], dev["theta_R"], dev["x"], dev["dy"])
+    torch.cuda.synchronize()
+    assert px.poetx_device_status() == 0
+    ref = oracle.layer_permuted(inp.theta_P, inp.theta_R, inp.W0, inp.x, inp.dy, b, k,
+                                perm_P, perm_R)
+    got = dict(y=layer.y, dx=layer.dx,
+               dtheta_P=layer.dtheta_P.view(d_in // b, -1),
+               dtheta_R=layer.dtheta_R.view(d_out // b, -1))
+    errs = {n: rel_fro(t.float().cpu().numpy(), ref[n]) for n, t in got.items()}
+    assert all(e <= TOL[dtype] for e in errs.values()), errs
