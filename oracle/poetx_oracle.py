@@ -24,6 +24,10 @@ Sources (one web page each; the method's own paper is not available):
   [tech-2-bd] section 2, bullet "Batch-parallele Berechnung fuer
               Block-diagonale Matrizen": R and P are block diagonal; the
               blocks are independent matrices multiplied as a batch.
+  [tech-2-merge] section 2, bullet "Input-zentrische Implementierung": the
+              original POET updates the weight itself, W <- R W P; here the
+              same merge folds the trained factors into W0 (and the factors
+              restart from the identity, theta = 0).
   [tech-2-perm] section 2, bullet "Permutations-Beschleunigung und
               -Reduktion": POET mixes the blocks with permutation matrices;
               POET-X applies the permutations as index maps on the data and
@@ -303,6 +307,32 @@ def loss_permuted(theta_P, theta_R, W0, x, dy, b, k, perm_P, perm_R) -> float:
     W = PiR.T @ BR @ PiR @ np.asarray(W0, np.float64) @ PiP.T @ BP @ PiP
     y = np.asarray(x, np.float64) @ W.T
     return float(np.sum(np.asarray(dy, np.float64) * y))
+
+
+# --------------------------------------------------------------------------
+# Around the layer: merge and parameter update  [tech-2-merge]
+# --------------------------------------------------------------------------
+
+def merge(theta_P, theta_R, W0, b: int, k: int) -> np.ndarray:
+    """W0 <- R W0 P with the current blocks, as dense matrices."""
+    P = dense_from_blocks(build_blocks(theta_P, b, k))
+    R = dense_from_blocks(build_blocks(theta_R, b, k))
+    return R @ np.asarray(W0, dtype=np.float64) @ P
+
+
+def adam_update(theta, grad, m, v, step: int, lr: float, beta1: float = 0.9,
+                beta2: float = 0.999, eps: float = 1e-8, weight_decay: float = 0.0):
+    """One Adam step on the packed parameters (Kingma and Ba, with bias
+    correction; optional decoupled weight decay).  The pages do not name the
+    optimizer of theta; this is the plain reading.  Returns (theta, m, v)."""
+    theta = np.asarray(theta, dtype=np.float64)
+    grad = np.asarray(grad, dtype=np.float64)
+    m = beta1 * np.asarray(m, dtype=np.float64) + (1 - beta1) * grad
+    v = beta2 * np.asarray(v, dtype=np.float64) + (1 - beta2) * grad * grad
+    m_hat = m / (1 - beta1 ** step)
+    v_hat = v / (1 - beta2 ** step)
+    theta = theta - lr * (m_hat / (np.sqrt(v_hat) + eps) + weight_decay * theta)
+    return theta, m, v
 
 
 # --------------------------------------------------------------------------

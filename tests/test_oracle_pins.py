@@ -340,3 +340,44 @@ def test_permuted_layer_gradients_match_central_differences():
                                       @ oracle.permutation_matrix(pP).T
                                       @ oracle.dense_from_blocks(oracle.build_blocks(tP, 4, 2))
                                       @ oracle.permutation_matrix(pP)).T)
+
+
+# ------------------------------------------------- merge and update
+
+def test_merge_equals_the_layer_with_zero_theta():
+    # after W0' = R W0 P, the layer with theta = 0 (identity blocks) gives the
+    # same y as the layer with theta on the old W0
+    inp = make_layer_inputs(16, 12, 4, 3, 6, dtype="f32", sigma_theta=0.3, seed=18)
+    W1 = oracle.merge(inp.theta_P, inp.theta_R, inp.W0, 4, 3)
+    a = oracle.layer(inp.theta_P, inp.theta_R, inp.W0, inp.x, inp.dy, 4, 3)
+    z = oracle.layer(np.zeros_like(inp.theta_P), np.zeros_like(inp.theta_R), W1, inp.x, inp.dy,
+                     4, 3)
+    np.testing.assert_allclose(z["y"], a["y"], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(z["dx"], a["dx"], rtol=1e-12, atol=1e-12)
+    # zero parameters leave W0 unchanged
+    W2 = oracle.merge(np.zeros_like(inp.theta_P), np.zeros_like(inp.theta_R), inp.W0, 4, 3)
+    assert np.array_equal(W2, inp.W0.astype(np.float64))
+
+
+def test_adam_first_step_closed_form():
+    # m = v = 0 at step 1: m_hat = g, v_hat = g^2, update = lr g / (|g| + eps)
+    g = np.array([0.5, -2.0, 1e-3, 0.0])
+    th, m, v = oracle.adam_update(np.zeros(4), g, np.zeros(4), np.zeros(4), 1, lr=0.1, eps=1e-8)
+    np.testing.assert_allclose(th, -0.1 * g / (np.abs(g) + 1e-8), rtol=1e-12, atol=0)
+    np.testing.assert_allclose(m, 0.1 * g)
+    np.testing.assert_allclose(v, 0.001 * g * g)
+
+
+def test_adam_second_step_by_hand():
+    g1, g2 = 0.3, -0.7
+    th, m, v = oracle.adam_update(np.array([1.0]), np.array([g1]), np.zeros(1), np.zeros(1), 1,
+                                  lr=0.01, weight_decay=0.1)
+    th, m, v = oracle.adam_update(th, np.array([g2]), m, v, 2, lr=0.01, weight_decay=0.1)
+    m_want = 0.9 * 0.1 * g1 + 0.1 * g2
+    v_want = 0.999 * 0.001 * g1 * g1 + 0.001 * g2 * g2
+    th1 = 1.0 - 0.01 * (g1 / (abs(g1) + 1e-8) + 0.1 * 1.0)
+    th2 = th1 - 0.01 * ((m_want / (1 - 0.81)) / (np.sqrt(v_want / (1 - 0.999 ** 2)) + 1e-8)
+                        + 0.1 * th1)
+    np.testing.assert_allclose(th, [th2], rtol=1e-12)
+    np.testing.assert_allclose(m, [m_want], rtol=1e-12)
+    np.testing.assert_allclose(v, [v_want], rtol=1e-12)
