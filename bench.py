@@ -49,6 +49,9 @@ def parse():
     ap.add_argument("--permute", action="store_true",
                     help="permuted block-diagonal factors (index maps around the plain step; "
                          "the two inner permutations folded into W0 once, before timing)")
+    ap.add_argument("--train-step", action="store_true",
+                    help="each step also applies Adam to theta_P and theta_R; the merge "
+                         "W0 <- R W0 P is timed separately after the timed region")
     ap.add_argument("--recompute-v", action="store_true",
                     help="backward recomputes v = W0 P x instead of reading it (saves T x d_out)")
     return ap.parse_args()
@@ -67,6 +70,8 @@ def config_json(name, w, n, args=None):
         c["permuted_blocks"] = True
     if args is not None and getattr(args, "recompute_v", False):
         c["recompute_v"] = True
+    if args is not None and getattr(args, "train_step", False):
+        c["optimizer"] = "adam (fused, in the step)"
     return c
 
 
@@ -272,12 +277,38 @@ def algorithmic_work(tag, w):
     return None
 
 
+def time_merge(poetx, layer, dev, w, stream, peaks, reps=20):
+    """Time the merge W0 <- R W0 P (into a copy of W0, factors kept) with CUDA
+    events after the timed region: it runs once per merge period, not per step."""
+    import torch
+    W = dev["W0"].clone()
+    for _ in range(3):
+        poetx.poetx_merge(dev["W0"], layer.P_blocks, layer.R_blocks, W, None, None, w["d_in"],
+                          w["d_out"], w["b"], layer.code, layer.workspace, stream)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        poetx.poetx_merge(dev["W0"], layer.P_blocks, layer.R_blocks, W, None, None, w["d_in"],
+                          w["d_out"], w["b"], layer.code, layer.workspace, stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) / reps * 1e3
+    S = max(w["b"], 256)
+    flop = 4.0 * w["d_in"] * w["d_out"] * S  # W0 P and R (W0 P), superblock width S
+    moved = 2.0 * 2 * w["d_in"] * w["d_out"]  # read W0, write W0_out (bf16)
+    return {"us": us, "tflops": flop / (us * 1e-6) / 1e12,
+            "hbm_gbs_min_bytes": moved / (us * 1e-6) / 1e9, "hbm_peak_gbs": peaks["hbm_gbs"],
+            "note": "two launches (W0 P, then R M); once per merge period, not per step"}
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
 
     import orthogonal_reparameterized_packed_gb300 as poetx
-    from orthogonal_reparameterized_packed_gb300.layer import PoetxLayer, to_device
+    from orthogonal_reparameterized_packed_gb300.layer import PoetxAdam, PoetxLayer, to_device
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -306,8 +337,16 @@ def run_gpu(args):
         layer = PoetxLayer(w["d_in"], w["d_out"], w["b"], w["k"], w["tokens"], dtype=w["dtype"],
                            recompute_v=args.recompute_v)
 
-        def step():
-            layer.step(dev["theta_P"], dev["theta_R"], dev["W0"], dev["x"], dev["dy"])
+        if args.train_step:
+            # the graph replays the captured launch's bias correction
+            opt = PoetxAdam([dev["theta_P"], dev["theta_R"]], lr=1e-4)
+
+            def step():
+                layer.step(dev["theta_P"], dev["theta_R"], dev["W0"], dev["x"], dev["dy"])
+                opt.step([layer.dtheta_P, layer.dtheta_R])
+        else:
+            def step():
+                layer.step(dev["theta_P"], dev["theta_R"], dev["W0"], dev["x"], dev["dy"])
 
     def barrier():
         if world > 1:
@@ -386,7 +425,7 @@ def run_gpu(args):
     # per-kernel times over the timed region
     tags = ["build", "unpack", "identity_plus", "expand_superblocks", "transform",
             "transform_t", "gemm_w0", "gemm_w0_dgrad", "outer", "reduce_extract", "cnp_bwd",
-            "pack_skew", "f32_to_bf16", "chain", "prep_tiles", "pack_tiles", "permute"]
+            "pack_skew", "f32_to_bf16", "chain", "prep_tiles", "pack_tiles", "permute", "adam"]
     kernels = {}
     for t in tags:
         n, tot = poetx.poetx_profile_query(t)
@@ -414,6 +453,10 @@ def run_gpu(args):
         roofline["secondary"] = {"kernel": "permute", "bound": "hbm", "achieved": gbs,
                                  "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                  "frac": gbs / peaks["hbm_gbs"]}
+
+    merge = None
+    if args.train_step and not args.permute:
+        merge = time_merge(poetx, layer, dev, w, stream, peaks)
 
     # whole-step algorithmic tensor work for context
     T, di, do, b = w["tokens"], w["d_in"], w["d_out"], w["b"]
@@ -470,7 +513,7 @@ def run_gpu(args):
                 "graph_error": graph_error,
                 "ms_per_step_eager": ms_eager, "roofline": roofline,
                 "step_tflops": step_flop / (ms_max * 1e-3) / 1e12,
-                "kernels": kernels, "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
+                "kernels": kernels, "merge": merge, "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
                 "device_status": status}
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -190,6 +190,29 @@ poetx_status poetx_fold_permutations(const void* W0, const int32_t* perm_out,
                                      int d_out, poetx_dtype dtype, poetx_stream stream);
 
 /* ------------------------------------------------------------------------
+ * Around the layer step.
+ * Merge (technical summary, section 2, "Input-zentrische Implementierung":
+ * the original POET updates the weight itself, W <- R W P): folds the
+ * current blocks into the frozen weight, W0_out = R W0 P, and restarts the
+ * factors from the identity by zeroing theta_P / theta_R when they are not
+ * NULL (rebuild the blocks afterwards).  W0_out may be W0.
+ *   W0, W0_out [d_out][d_in] dtype; blocks as for poetx_forward.
+ * ------------------------------------------------------------------------ */
+size_t poetx_merge_workspace_size(int d_in, int d_out, int b, poetx_dtype dtype);
+poetx_status poetx_merge(const void* W0, const void* P_blocks, const void* R_blocks, void* W0_out,
+                         float* theta_P, float* theta_R, int d_in, int d_out, int b,
+                         poetx_dtype dtype, void* workspace, size_t workspace_bytes,
+                         poetx_stream stream);
+/* One Adam step (bias-corrected, decoupled weight decay) on n packed
+ * parameters, in place: m <- b1 m + (1-b1) g; v <- b2 v + (1-b2) g^2;
+ * theta <- theta - lr (m/(1-b1^step) / (sqrt(v/(1-b2^step)) + eps) + wd theta).
+ * The pages name no optimizer for theta; this is the plain choice.  All
+ * arrays float32 device memory; step >= 1. */
+poetx_status poetx_adam_update(float* theta, const float* grad, float* m, float* v, int64_t n,
+                               int step, float lr, float beta1, float beta2, float eps,
+                               float weight_decay, poetx_stream stream);
+
+/* ------------------------------------------------------------------------
  * Status and measurement
  * ------------------------------------------------------------------------ */
 /* Synchronizes the current device, returns the status recorded by kernels

@@ -19,7 +19,8 @@ __all__ = [
     "poetx_forward_workspace_size", "poetx_forward",
     "poetx_backward_workspace_size", "poetx_backward",
     "poetx_transform_workspace_size", "poetx_transform_forward", "poetx_transform_backward",
-    "poetx_permute_features", "poetx_fold_permutations",
+    "poetx_permute_features", "poetx_fold_permutations", "poetx_merge_workspace_size",
+    "poetx_merge", "poetx_adam_update",
     "poetx_device_status", "poetx_selftest_wait_timeout", "poetx_launch_count", "poetx_profile_start", "poetx_profile_stop",
     "poetx_profile_query", "poetx_status_string", "EXPORTED_SYMBOLS",
 ]
@@ -60,6 +61,12 @@ _SIGNATURES = {
     "poetx_permute_features": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_i64, _c_int, _c_int, _c_ptr]),
     "poetx_fold_permutations": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_int, _c_int,
                                          _c_ptr]),
+    "poetx_merge_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
+    "poetx_merge": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_int, _c_int,
+                             _c_int, _c_ptr, _c_size, _c_ptr]),
+    "poetx_adam_update": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_i64, _c_int,
+                                   ctypes.c_float, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                   ctypes.c_float, _c_ptr]),
     "poetx_device_status": (_c_int, []),
     "poetx_selftest_wait_timeout": (_c_int, [ctypes.c_uint, _c_ptr]),
     "poetx_launch_count": (ctypes.c_longlong, []),
@@ -197,6 +204,24 @@ def poetx_permute_features(inp, perm, out, rows, d, dtype, stream=None):
 def poetx_fold_permutations(W0, perm_out, perm_in, W0_folded, d_in, d_out, dtype, stream=None):
     _check("poetx_fold_permutations", load_library().poetx_fold_permutations(
         _ptr(W0), _ptr(perm_out), _ptr(perm_in), _ptr(W0_folded), d_in, d_out, dtype,
+        _stream(stream)))
+
+
+def poetx_merge_workspace_size(d_in, d_out, b, dtype) -> int:
+    return load_library().poetx_merge_workspace_size(d_in, d_out, b, dtype)
+
+
+def poetx_merge(W0, P_blocks, R_blocks, W0_out, theta_P, theta_R, d_in, d_out, b, dtype,
+                workspace, stream=None):
+    _check("poetx_merge", load_library().poetx_merge(
+        _ptr(W0), _ptr(P_blocks), _ptr(R_blocks), _ptr(W0_out), _ptr(theta_P), _ptr(theta_R),
+        d_in, d_out, b, dtype, _ptr(workspace), _nbytes(workspace), _stream(stream)))
+
+
+def poetx_adam_update(theta, grad, m, v, n, step, lr, beta1=0.9, beta2=0.999, eps=1e-8,
+                      weight_decay=0.0, stream=None):
+    _check("poetx_adam_update", load_library().poetx_adam_update(
+        _ptr(theta), _ptr(grad), _ptr(m), _ptr(v), n, step, lr, beta1, beta2, eps, weight_decay,
         _stream(stream)))
 
 

@@ -14,6 +14,7 @@
 // so the token-wise contractions always see 256 x 256 operands.  fp32 mode
 // runs every contraction on the FFMA engine.
 #include <atomic>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -1168,6 +1169,120 @@ poetx_status poetx_fold_permutations(const void* W0, const int32_t* perm_out,
                                        is_bf16, static_cast<cudaStream_t>(stream)));
 }
 
+size_t poetx_merge_workspace_size(int d_in, int d_out, int b, poetx_dtype dtype) {
+  const bool is_bf16 = dtype == POETX_BF16;
+  if (check_dims(d_in, b, is_bf16) != POETX_OK || check_dims(d_out, b, is_bf16) != POETX_OK ||
+      check_common(b, 0, 0, dtype) != POETX_OK)
+    return 0;
+  Carver c(nullptr);
+  c.take<char>(static_cast<size_t>(d_out) * d_in * elem_size(is_bf16));
+  if (is_bf16 && b < 256) {
+    c.take<bf16>(static_cast<size_t>(d_in) * 256);
+    c.take<bf16>(static_cast<size_t>(d_out) * 256);
+  }
+  return c.off;
+}
+
+poetx_status poetx_merge(const void* W0, const void* P_blocks, const void* R_blocks, void* W0_out,
+                         float* theta_P, float* theta_R, int d_in, int d_out, int b,
+                         poetx_dtype dtype, void* workspace, size_t workspace_bytes,
+                         poetx_stream stream) {
+  const bool is_bf16 = dtype == POETX_BF16;
+  poetx_status st = check_common(b, 0, 0, dtype);
+  if (st != POETX_OK) return st;
+  if ((st = check_dims(d_in, b, is_bf16)) != POETX_OK) return st;
+  if ((st = check_dims(d_out, b, is_bf16)) != POETX_OK) return st;
+  const void* ptrs[] = {W0, P_blocks, R_blocks, W0_out};
+  for (const void* q : ptrs)
+    if (q == nullptr || !aligned16(q)) return POETX_ERR_INVALID_ARG;
+  if (!aligned16(theta_P) || !aligned16(theta_R)) return POETX_ERR_INVALID_ARG;
+  Carver c(workspace);
+  void* M = c.take<char>(static_cast<size_t>(d_out) * d_in * elem_size(is_bf16));
+  bf16* psb = nullptr;
+  bf16* rsb = nullptr;
+  if (is_bf16 && b < 256) {
+    psb = c.take<bf16>(static_cast<size_t>(d_in) * 256);
+    rsb = c.take<bf16>(static_cast<size_t>(d_out) * 256);
+  }
+  if (workspace == nullptr || c.off > workspace_bytes || !aligned16(workspace))
+    return POETX_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  const void* P = superblocks_or_blocks(P_blocks, psb, d_in, b, is_bf16, s, &e);
+  if (e != cudaSuccess) return POETX_ERR_CUDA;
+  const void* R = superblocks_or_blocks(R_blocks, rsb, d_out, b, is_bf16, s, &e);
+  if (e != cudaSuccess) return POETX_ERR_CUDA;
+  if (is_bf16) {
+    const int S = superblock(b);
+    // M = W0 P: W0's rows through the transposed block transform
+    e = tc_transform(static_cast<const bf16*>(W0), static_cast<const bf16*>(P),
+                     static_cast<bf16*>(M), d_in, S, d_out, true, "merge", s);
+    if (e != cudaSuccess) return POETX_ERR_CUDA;
+    // W0_out = R M: one S x S block of R times S rows of M per batch
+    TcGemm g;
+    g.M = S;
+    g.N = d_in;
+    g.K = S;
+    g.batches = d_out / S;
+    g.BN = 256;
+    g.A = op(R, d_out, S, S, false, S, 0);     // A[m][kk] = R_g[m][kk]
+    g.B = op(M, d_out, d_in, d_in, true, 0, S);  // B[n][kk] = M[g*S + kk][n]
+    g.epi.out_bf16 = static_cast<bf16*>(W0_out);
+    g.epi.ld = d_in;
+    g.epi.row_g = S;
+    g.epi.out_rows = d_out;
+    g.tag = "merge";
+    e = tc_gemm_run(g, s);
+  } else {
+    e = simt_transform(static_cast<const float*>(W0), static_cast<const float*>(P),
+                       static_cast<float*>(M), d_in, b, d_out, true, "merge", s);
+    if (e != cudaSuccess) return POETX_ERR_CUDA;
+    SimtGemm g;
+    g.M = b;
+    g.N = d_in;
+    g.K = b;
+    g.batches = d_out / b;
+    g.A = R;
+    g.a_g = static_cast<long long>(b) * b;
+    g.a_m = b;
+    g.a_k = 1;
+    g.B = M;
+    g.b_g = static_cast<long long>(b) * d_in;
+    g.b_k = d_in;
+    g.b_n = 1;
+    g.epi.out_f32 = static_cast<float*>(W0_out);
+    g.epi.ld = d_in;
+    g.epi.row_g = b;
+    g.tag = "merge";
+    e = simt_gemm_run(g, s);
+  }
+  if (e != cudaSuccess) return POETX_ERR_CUDA;
+  if (theta_P != nullptr &&
+      cudaMemsetAsync(theta_P, 0, poetx_packed_size(d_in, b) * sizeof(float), s) != cudaSuccess)
+    return POETX_ERR_CUDA;
+  if (theta_R != nullptr &&
+      cudaMemsetAsync(theta_R, 0, poetx_packed_size(d_out, b) * sizeof(float), s) != cudaSuccess)
+    return POETX_ERR_CUDA;
+  return POETX_OK;
+}
+
+poetx_status poetx_adam_update(float* theta, const float* grad, float* m, float* v, int64_t n,
+                               int step, float lr, float beta1, float beta2, float eps,
+                               float weight_decay, poetx_stream stream) {
+  if (n < 0 || step < 1 || !(beta1 >= 0.f && beta1 < 1.f) || !(beta2 >= 0.f && beta2 < 1.f) ||
+      !(eps > 0.f))
+    return POETX_ERR_INVALID_ARG;
+  if (n == 0) return POETX_OK;
+  if (theta == nullptr || grad == nullptr || m == nullptr || v == nullptr)
+    return POETX_ERR_INVALID_ARG;
+  const double bc1 = 1.0 - std::pow(static_cast<double>(beta1), step);
+  const double bc2 = 1.0 - std::pow(static_cast<double>(beta2), step);
+  return to_status(launch_adam(theta, grad, m, v, n, lr, beta1, beta2, eps, weight_decay,
+                               static_cast<float>(bc1), static_cast<float>(bc2),
+                               static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"
+
 
 

@@ -193,6 +193,10 @@ cudaError_t launch_pack_tiles(const float* D, float sign, int n_a, int n_b, int 
 cudaError_t launch_permute_rows(const void* in, long long in_rows, const int* row_map,
                                 const int* col_map, void* out, long long rows, int d,
                                 bool is_bf16, cudaStream_t s);
+// theta -= lr * (m_hat / (sqrt(v_hat) + eps) + wd * theta) with updated moments.
+cudaError_t launch_adam(float* theta, const float* grad, float* m, float* v, long long n,
+                        float lr, float beta1, float beta2, float eps, float wd, float bc1,
+                        float bc2, cudaStream_t s);
 cudaError_t launch_f32_to_bf16(const float* in, long long count, __nv_bfloat16* out,
                                cudaStream_t s);
 

@@ -390,6 +390,25 @@ __global__ void __launch_bounds__(kPermWarps * 32)
   }
 }
 
+// One Adam step on packed parameters: m, v moments, bias corrections bc1 =
+// 1 - beta1^step and bc2 = 1 - beta2^step, decoupled weight decay wd.
+__global__ void adam_kernel(float* __restrict__ theta, const float* __restrict__ grad,
+                            float* __restrict__ m, float* __restrict__ v, long long n, float lr,
+                            float beta1, float beta2, float eps, float wd, float bc1, float bc2) {
+  pdl_wait();
+  pdl_trigger();
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const float g = grad[i];
+    const float mi = beta1 * m[i] + (1.f - beta1) * g;
+    const float vi = beta2 * v[i] + (1.f - beta2) * g * g;
+    m[i] = mi;
+    v[i] = vi;
+    const float th = theta[i];
+    theta[i] = th - lr * ((mi / bc1) / (sqrtf(vi / bc2) + eps) + wd * th);
+  }
+}
+
 int ew_grid(long long total) {
   long long blocks = (total + 255) / 256;
   const long long cap = static_cast<long long>(sm_count()) * 16;
@@ -510,6 +529,13 @@ cudaError_t launch_permute_rows(const void* in, long long in_rows, const int* ro
   }
   prof_end("permute", s);
   return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_adam(float* theta, const float* grad, float* m, float* v, long long n,
+                        float lr, float beta1, float beta2, float eps, float wd, float bc1,
+                        float bc2, cudaStream_t s) {
+  POETX_EW_LAUNCH("adam", n, adam_kernel, theta, grad, m, v, n, lr, beta1, beta2, eps, wd, bc1,
+                  bc2);
 }
 
 cudaError_t launch_f32_to_bf16(const float* in, long long count, __nv_bfloat16* out,

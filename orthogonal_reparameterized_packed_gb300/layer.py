@@ -7,9 +7,10 @@ from __future__ import annotations
 
 import torch
 
-from . import (BF16, F32, poetx_backward, poetx_backward_workspace_size, poetx_build_blocks,
-               poetx_build_workspace_size, poetx_fold_permutations, poetx_forward,
-               poetx_forward_workspace_size, poetx_packed_size, poetx_permute_features)
+from . import (BF16, F32, poetx_adam_update, poetx_backward, poetx_backward_workspace_size,
+               poetx_build_blocks, poetx_build_workspace_size, poetx_fold_permutations,
+               poetx_forward, poetx_forward_workspace_size, poetx_merge,
+               poetx_merge_workspace_size, poetx_packed_size, poetx_permute_features)
 
 _TORCH_DTYPE = {F32: torch.float32, BF16: torch.bfloat16}
 
@@ -42,7 +43,8 @@ class PoetxLayer:
                  poetx_build_workspace_size(d_out, b, k, self.code),
                  poetx_forward_workspace_size(d_in, d_out, b, tokens, self.code),
                  poetx_backward_workspace_size(d_in, d_out, b, k, tokens, self.code,
-                                               recompute_v))
+                                               recompute_v),
+                 poetx_merge_workspace_size(d_in, d_out, b, self.code))
         self.workspace = torch.empty((max(ws, 16),), dtype=torch.uint8, device=dev)
 
     def build(self, theta_P, theta_R, stream=None):
@@ -68,6 +70,39 @@ class PoetxLayer:
         self.forward(x, W0, stream)
         self.backward(dy, x, W0, theta_P, theta_R, stream)
         return self.y, self.dx, self.dtheta_P, self.dtheta_R
+
+
+    def merge(self, W0, theta_P, theta_R, stream=None):
+        """Fold the current blocks into the weight, W0 <- R W0 P (in place),
+        and restart both factors at the identity (theta_P = theta_R = 0).
+        Uses the blocks of the last build()."""
+        poetx_merge(W0, self.P_blocks, self.R_blocks, W0, theta_P, theta_R, self.d_in,
+                    self.d_out, self.b, self.code, self.workspace, stream)
+
+
+class PoetxAdam:
+    """Adam on packed parameter vectors (float32 device tensors), one fused
+    launch per vector per step."""
+
+    def __init__(self, params, lr, betas=(0.9, 0.999), eps=1e-8, weight_decay=0.0):
+        self.params = list(params)
+        self.lr, self.betas, self.eps, self.weight_decay = lr, betas, eps, weight_decay
+        self.m = [torch.zeros_like(p) for p in self.params]
+        self.v = [torch.zeros_like(p) for p in self.params]
+        self.t = 0
+
+    def reset(self):
+        """Zero the moments (after a merge restarts the factors)."""
+        for m, v in zip(self.m, self.v):
+            m.zero_()
+            v.zero_()
+        self.t = 0
+
+    def step(self, grads, stream=None):
+        self.t += 1
+        for p, g, m, v in zip(self.params, grads, self.m, self.v):
+            poetx_adam_update(p, g, m, v, p.numel(), self.t, self.lr, self.betas[0],
+                              self.betas[1], self.eps, self.weight_decay, stream)
 
 
 def to_device(inp, device="cuda"):

@@ -125,3 +125,34 @@ def test_forward_and_backward_reject_invalid_arguments(lib):
                             wb, None) == 1
     assert L.poetx_backward(*bargs, FAKE, FAKE, FAKE, FAKE, 512, 512, 256, 20, 64, B, FAKE,
                             wb, None) == 1
+
+
+def test_merge_and_adam_reject_invalid_arguments(lib):
+    L = _raw()
+    B, F = poetx.BF16, poetx.F32
+    ws = poetx.poetx_merge_workspace_size(512, 768, 256, B)
+    # the merge needs W0 P (bf16) in the workspace
+    assert ws >= 768 * 512 * 2
+    assert poetx.poetx_merge_workspace_size(512, 768, 48, B) == 0
+    assert poetx.poetx_merge_workspace_size(100, 64, 32, F) == 0
+    p4 = [FAKE] * 4
+    assert L.poetx_merge(*p4, None, None, 512, 700, 256, B, FAKE, ws, None) == 1
+    assert L.poetx_merge(FAKE, None, FAKE, FAKE, None, None, 512, 768, 256, B, FAKE, ws,
+                         None) == 1
+    assert L.poetx_merge(*p4, FAKE + 4, None, 512, 768, 256, B, FAKE, ws, None) == 1
+    assert L.poetx_merge(*p4, None, None, 512, 768, 256, B, FAKE, ws - 1, None) == 3
+    assert L.poetx_merge(*p4, None, None, 512, 768, 256, B, None, ws, None) == 3
+    assert L.poetx_merge(*p4, None, None, 512, 640, 128, B, FAKE, ws, None) == 2
+    f = ctypes.c_float
+    assert L.poetx_adam_update(FAKE, FAKE, FAKE, FAKE, 4, 0, f(1e-3), f(0.9), f(0.999), f(1e-8),
+                               f(0.0), None) == 1
+    assert L.poetx_adam_update(FAKE, FAKE, FAKE, FAKE, -1, 1, f(1e-3), f(0.9), f(0.999),
+                               f(1e-8), f(0.0), None) == 1
+    assert L.poetx_adam_update(FAKE, FAKE, FAKE, FAKE, 4, 1, f(1e-3), f(1.0), f(0.999), f(1e-8),
+                               f(0.0), None) == 1
+    assert L.poetx_adam_update(FAKE, FAKE, FAKE, FAKE, 4, 1, f(1e-3), f(0.9), f(0.999), f(0.0),
+                               f(0.0), None) == 1
+    assert L.poetx_adam_update(None, FAKE, FAKE, FAKE, 4, 1, f(1e-3), f(0.9), f(0.999), f(1e-8),
+                               f(0.0), None) == 1
+    assert L.poetx_adam_update(None, None, None, None, 0, 1, f(1e-3), f(0.9), f(0.999), f(1e-8),
+                               f(0.0), None) == 0
