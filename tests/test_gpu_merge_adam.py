@@ -4,7 +4,9 @@ parameters, against the float64 oracle.
 
 Tolerances: merge 1e-4 relative Frobenius in fp32; in bf16 the blocks, the
 intermediate W0 P and the result are each rounded to bf16 once, so 1e-2.
-Adam: fp32 arithmetic on O(1) quantities, 1e-5 relative per element.
+Adam: fp32 arithmetic, 1e-5 relative per element plus 2e-7 of the array's
+largest magnitude (the moment updates cancel, so their rounding error scales
+with the terms rather than with the result).
 """
 
 import numpy as np
@@ -100,7 +102,7 @@ def test_step_after_merge_matches_the_unmerged_layer(px):
     assert rel_fro(y_after.cpu().numpy(), y_before.cpu().numpy()) <= 1e-5
 
 
-@pytest.mark.parametrize("n,wd", [(1, 0.0), (1000, 0.0), (123457, 0.01)])
+@pytest.mark.parametrize("n,wd", [(1, 0.0), (1000, 0.0), (123457, 0.1)])
 def test_adam_two_steps_match_oracle(px, n, wd):
     rng = np.random.default_rng(34)
     theta = rng.standard_normal(n) * 0.1
@@ -109,16 +111,22 @@ def test_adam_two_steps_match_oracle(px, n, wd):
     t = torch.from_numpy(theta.astype(np.float32)).cuda()
     m = torch.zeros_like(t)
     v = torch.zeros_like(t)
-    want_t, want_m, want_v = theta, np.zeros(n), np.zeros(n)
+    want_t, want_m, want_v = theta.astype(np.float32), np.zeros(n), np.zeros(n)
+    # the hyperparameters cross the C ABI as float32: give the oracle the same values
+    f32 = lambda a: float(np.float32(a))  # noqa: E731
+    lr, b1, b2, eps, wd32 = f32(1e-3), f32(0.9), f32(0.999), f32(1e-8), f32(wd)
     for step, g in ((1, g1), (2, g2)):
         gd = torch.from_numpy(g.astype(np.float32)).cuda()
-        px.poetx_adam_update(t, gd, m, v, n, step, 1e-3, 0.9, 0.999, 1e-8, wd)
+        px.poetx_adam_update(t, gd, m, v, n, step, lr, b1, b2, eps, wd32)
         want_t, want_m, want_v = oracle.adam_update(want_t, g.astype(np.float32), want_m,
-                                                    want_v, step, 1e-3, weight_decay=wd)
+                                                    want_v, step, lr, beta1=b1, beta2=b2,
+                                                    eps=eps, weight_decay=wd32)
     check_status(px)
     for got, want in ((t, want_t), (m, want_m), (v, want_v)):
         got = got.cpu().numpy().astype(np.float64)
-        assert np.max(np.abs(got - want) / np.maximum(np.abs(want), 1e-3)) <= 1e-5
+        # m = b1 m + (1-b1) g cancels: its fp32 error scales with the terms, not the sum
+        scale = np.max(np.abs(want))
+        assert np.all(np.abs(got - want) <= 1e-5 * np.abs(want) + 2e-7 * scale)
 
 
 def test_adam_rejects_bad_arguments(px):
