@@ -339,11 +339,12 @@ def run_gpu(args):
 
         if args.train_step:
             # the graph replays the captured launch's bias correction
-            opt = PoetxAdam([dev["theta_P"], dev["theta_R"]], lr=1e-4)
+            # theta_P, theta_R (and dtheta_P, dtheta_R) are one buffer: one launch
+            opt = PoetxAdam([dev["theta"]], lr=1e-4)
 
             def step():
                 layer.step(dev["theta_P"], dev["theta_R"], dev["W0"], dev["x"], dev["dy"])
-                opt.step([layer.dtheta_P, layer.dtheta_R])
+                opt.step([layer.dtheta])
         else:
             def step():
                 layer.step(dev["theta_P"], dev["theta_R"], dev["W0"], dev["x"], dev["dy"])

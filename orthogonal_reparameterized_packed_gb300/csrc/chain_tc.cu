@@ -51,7 +51,15 @@ constexpr int kChainMaxMaps = 48;
 struct ChainTerm {
   int a_map, b_map;  // A: K-major box map, B: MN-major box map
   int b_batched;     // B rows offset by g * b (0: one constant b x b matrix)
+  int diag;          // B is diagonal (2I): only the K steps of the tile's own columns count
 };
+
+// K steps [k0, k1) of a term for output column tile nt
+__device__ __forceinline__ void term_ksteps(const ChainTerm& T, int nt, int ksteps, int& k0,
+                                            int& k1) {
+  k0 = T.diag ? nt * (CH_BN / BK) : 0;
+  k1 = T.diag ? k0 + CH_BN / BK : ksteps;
+}
 
 struct ChainProd {
   int nterms;
@@ -190,7 +198,9 @@ __global__ void __launch_bounds__(CH_THREADS, 1) chain_kernel(const __grid_const
             const CUtensorMap* ma = &P.maps[PR.term[term].a_map];
             const CUtensorMap* mb = &P.maps[PR.term[term].b_map];
             const int b_row0 = PR.term[term].b_batched ? g * b : 0;
-            for (int ks = 0; ks < ksteps; ++ks) {
+            int k0, k1;
+            term_ksteps(PR.term[term], nt, ksteps, k0, k1);
+            for (int ks = k0; ks < k1; ++ks) {
               if (!mbar_wait(&empty_bar[stage], phase_bit ^ 1, abort_flag)) {
                 record_timeout(P.status, abort_flag);
                 ok = false;
@@ -258,7 +268,9 @@ __global__ void __launch_bounds__(CH_THREADS, 1) chain_kernel(const __grid_const
           }
           bool fresh = !persistent || PR.first_acc;
           for (int term = 0; term < PR.nterms && ok; ++term) {
-            for (int ks = 0; ks < ksteps; ++ks) {
+            int k0, k1;
+            term_ksteps(PR.term[term], nt, ksteps, k0, k1);
+            for (int ks = k0; ks < k1; ++ks) {
               if (!mbar_wait(&full_bar[stage], phase_bit, abort_flag)) {
                 record_timeout(P.status, abort_flag);
                 ok = false;
@@ -404,6 +416,14 @@ ChainTerm term(int a_map, int b_map, bool b_batched) {
   t.a_map = a_map;
   t.b_map = b_map + 1;  // MN-major box
   t.b_batched = b_batched ? 1 : 0;
+  t.diag = 0;
+  return t;
+}
+
+// A times the constant 2I: of the K sum only the tile's own column range is non-zero
+ChainTerm term_2i(int a_map, int two_map) {
+  ChainTerm t = term(a_map, two_map, false);
+  t.diag = 1;
   return t;
 }
 
@@ -510,8 +530,8 @@ cudaError_t chain_build(const ChainBuildArgs& a, cudaStream_t stream) {
     ChainProd& PR = PH.prod[0];
     PR.nterms = 3;
     PR.term[0] = term(hi, cur, true);
-    PR.term[1] = term(hi, two, false);
-    PR.term[2] = term(lo, two, false);
+    PR.term[1] = term_2i(hi, two);
+    PR.term[2] = term_2i(lo, two);
     PR.mode = PROD_STORE;
     EpiArgs ep = chain_epi(b);
     if (i == 1) {
@@ -573,7 +593,7 @@ cudaError_t chain_adjoint(const ChainAdjointArgs& a, cudaStream_t stream) {
       ChainProd& PR = PH.prod[0];
       PR.nterms = 2;
       PR.term[0] = term(q, e_map[i + 1], true);
-      PR.term[1] = term(q, two, false);
+      PR.term[1] = term_2i(q, two);
       PR.mode = PROD_STORE;
       EpiArgs ep = chain_epi(b);
       ep.out_bf16 = a.e16[i];
@@ -589,7 +609,7 @@ cudaError_t chain_adjoint(const ChainAdjointArgs& a, cudaStream_t stream) {
       const int f = maps.add(a.f16[cur], rows, b);
       ChainProd& D = PH.prod[0];
       D.term[0] = term(e_map[i + 1], f, true);
-      D.term[1] = term(f, two, false);
+      D.term[1] = term_2i(f, two);
       D.nterms = 2;
       D.first_acc = i == 1 ? 1 : 0;
       if (i < k) {

@@ -5,6 +5,7 @@ tensors, one shared workspace, and the four calls of a training step
 
 from __future__ import annotations
 
+import numpy as np
 import torch
 
 from . import (BF16, F32, poetx_adam_update, poetx_backward, poetx_backward_workspace_size,
@@ -19,8 +20,28 @@ def dtype_code(name: str) -> int:
     return {"f32": F32, "bf16": BF16}[name]
 
 
+def adjacent(a, b):
+    """The combined tensor if float32 tensors a and b lie back to back in one
+    allocation (a first), else None."""
+    if not (a.is_contiguous() and b.is_contiguous() and a.dtype == b.dtype == torch.float32):
+        return None
+    if a.data_ptr() + a.numel() * 4 != b.data_ptr():
+        return None
+    if a.untyped_storage().data_ptr() != b.untyped_storage().data_ptr():
+        return None
+    base = a.untyped_storage()
+    off = (a.data_ptr() - base.data_ptr()) // 4
+    return torch.empty(0, dtype=torch.float32, device=a.device).set_(
+        base, off, (a.numel() + b.numel(),), (1,))
+
+
 class PoetxLayer:
-    """Buffers for one projection y = R (W0 (P x)) with `tokens` tokens."""
+    """Buffers for one projection y = R (W0 (P x)) with `tokens` tokens.
+
+    The P and R blocks (and dtheta_P, dtheta_R) are views of one allocation,
+    P first: blocks are independent, so when theta_P and theta_R also lie
+    back to back the two factors are built by a single call over
+    d_in + d_out features."""
 
     def __init__(self, d_in, d_out, b, k, tokens, dtype="bf16", device="cuda",
                  recompute_v=False):
@@ -30,17 +51,19 @@ class PoetxLayer:
         tdt = _TORCH_DTYPE[self.code]
         dev = torch.device(device)
         nP, nR = d_in // b, d_out // b
-        self.P_blocks = torch.empty((nP, b, b), dtype=tdt, device=dev)
-        self.R_blocks = torch.empty((nR, b, b), dtype=tdt, device=dev)
+        self.blocks = torch.empty((nP + nR, b, b), dtype=tdt, device=dev)
+        self.P_blocks = self.blocks[:nP]
+        self.R_blocks = self.blocks[nP:]
         self.y = torch.empty((tokens, d_out), dtype=tdt, device=dev)
         self.v = None if recompute_v else torch.empty((tokens, d_out), dtype=tdt, device=dev)
         self.dx = torch.empty((tokens, d_in), dtype=tdt, device=dev)
-        self.dtheta_P = torch.empty((poetx_packed_size(d_in, b),), dtype=torch.float32,
-                                    device=dev)
-        self.dtheta_R = torch.empty((poetx_packed_size(d_out, b),), dtype=torch.float32,
-                                    device=dev)
+        mP, mR = poetx_packed_size(d_in, b), poetx_packed_size(d_out, b)
+        self.dtheta = torch.empty((mP + mR,), dtype=torch.float32, device=dev)
+        self.dtheta_P = self.dtheta[:mP]
+        self.dtheta_R = self.dtheta[mP:]
         ws = max(poetx_build_workspace_size(d_in, b, k, self.code),
                  poetx_build_workspace_size(d_out, b, k, self.code),
+                 poetx_build_workspace_size(d_in + d_out, b, k, self.code),
                  poetx_forward_workspace_size(d_in, d_out, b, tokens, self.code),
                  poetx_backward_workspace_size(d_in, d_out, b, k, tokens, self.code,
                                                recompute_v),
@@ -48,6 +71,11 @@ class PoetxLayer:
         self.workspace = torch.empty((max(ws, 16),), dtype=torch.uint8, device=dev)
 
     def build(self, theta_P, theta_R, stream=None):
+        theta = adjacent(theta_P, theta_R)
+        if theta is not None:  # both factors in one call
+            poetx_build_blocks(theta, self.d_in + self.d_out, self.b, self.k, self.code,
+                               self.blocks, self.workspace, stream)
+            return
         poetx_build_blocks(theta_P, self.d_in, self.b, self.k, self.code, self.P_blocks,
                            self.workspace, stream)
         poetx_build_blocks(theta_R, self.d_out, self.b, self.k, self.code, self.R_blocks,
@@ -106,14 +134,18 @@ class PoetxAdam:
 
 
 def to_device(inp, device="cuda"):
-    """Upload a LayerInputs (numpy) to torch tensors in the working dtype."""
+    """Upload a LayerInputs (numpy) to torch tensors in the working dtype.
+    theta_P and theta_R are views of one buffer `theta` (P first)."""
     tdt = torch.bfloat16 if inp.dtype == "bf16" else torch.float32
 
     def act(a):
         return torch.from_numpy(a).to(device=device).to(tdt).contiguous()
 
-    return dict(theta_P=torch.from_numpy(inp.theta_P).to(device).contiguous(),
-                theta_R=torch.from_numpy(inp.theta_R).to(device).contiguous(),
+    nP = inp.theta_P.size
+    theta = torch.from_numpy(np.concatenate([inp.theta_P.ravel(), inp.theta_R.ravel()])).to(
+        device)
+    return dict(theta=theta, theta_P=theta[:nP].view(inp.theta_P.shape),
+                theta_R=theta[nP:].view(inp.theta_R.shape),
                 W0=act(inp.W0), x=act(inp.x), dy=act(inp.dy))
 
 
@@ -124,7 +156,6 @@ class PoetxPermutedLayer:
     to the activations as index maps around a plain PoetxLayer step."""
 
     def __init__(self, d_in, d_out, b, k, tokens, perm_P, perm_R, dtype="bf16", device="cuda"):
-        import numpy as np
         self.inner = PoetxLayer(d_in, d_out, b, k, tokens, dtype=dtype, device=device)
         self.code = self.inner.code
         dev = torch.device(device)

@@ -244,3 +244,21 @@ def test_deterministic(px):
     b = run_layer(px, inp)
     for name in ("y", "dx", "dtheta_P", "dtheta_R"):
         assert torch.equal(getattr(a, name), getattr(b, name)), name
+
+
+@pytest.mark.parametrize("dtype,b", [("bf16", 256), ("bf16", 64), ("f32", 32)])
+def test_one_call_build_equals_two_calls(px, dtype, b):
+    # theta_P and theta_R back to back are built by one call over d_in + d_out
+    # features; the blocks must be bitwise those of two separate calls.
+    from orthogonal_reparameterized_packed_gb300.layer import PoetxLayer, adjacent, to_device
+    inp = make_layer_inputs(512, 768, b, 3, 8, dtype=dtype, seed=7)
+    dev = to_device(inp)
+    assert adjacent(dev["theta_P"], dev["theta_R"]) is not None
+    one = PoetxLayer(512, 768, b, 3, 8, dtype=dtype)
+    one.build(dev["theta_P"], dev["theta_R"])
+    two = PoetxLayer(512, 768, b, 3, 8, dtype=dtype)
+    tP, tR = dev["theta_P"].clone(), dev["theta_R"].clone()
+    assert adjacent(tP, tR) is None
+    two.build(tP, tR)
+    check_status(px)
+    assert torch.equal(one.blocks, two.blocks)
