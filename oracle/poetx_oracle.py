@@ -32,6 +32,9 @@ Sources (one web page each; the method's own paper is not available):
               -Reduktion": POET mixes the blocks with permutation matrices;
               POET-X applies the permutations as index maps on the data and
               folds two of the four forward permutations into W once.
+  [tech-2-xq] section 2, bullet "Quantisierte Unterstuetzung (POET-XQ)":
+              the frozen W0 is needed only as the operand of one matmul, so
+              it can be held quantised (INT8) without more activation memory.
   [tech-2-cnp] section 2, bullet "Effiziente Cayley-Neumann-
               Parametrisierung (CNP)": the orthogonal blocks come from
               skew-symmetric Q (Q = -Q^T) through the Cayley transform with
@@ -51,6 +54,11 @@ reason in the design notes):
     y_t = R (W0 (P x_t)).
   * The gradient returned for the packed parameters is d loss / d theta:
     dtheta[idx(i,j)] = G_Q[i][j] - G_Q[j][i].
+  * INT8 W0 [tech-2-xq]: symmetric, one scale per output row,
+    scale = max|W0[o,:]| / 127, code = round-half-even(W0 / scale) clamped
+    to [-127, 127]; a zero row has scale 0 and codes 0.  The quotient that
+    decides each code, and the dequantised value code * scale, are taken in
+    float32 (the precision of the kernels), so codes are exact to compare.
 """
 
 from __future__ import annotations
@@ -333,6 +341,35 @@ def adam_update(theta, grad, m, v, step: int, lr: float, beta1: float = 0.9,
     v_hat = v / (1 - beta2 ** step)
     theta = theta - lr * (m_hat / (np.sqrt(v_hat) + eps) + weight_decay * theta)
     return theta, m, v
+
+
+# --------------------------------------------------------------------------
+# INT8 frozen weight  [tech-2-xq]
+# --------------------------------------------------------------------------
+
+def quantize_w0(W0):
+    """Per-output-row symmetric INT8 codes and float32 scales of W0
+    (float32 arithmetic: the division decides the integer code)."""
+    W = np.asarray(W0, dtype=np.float32)
+    d_out, d_in = W.shape
+    codes = np.zeros((d_out, d_in), dtype=np.int8)
+    scales = np.zeros(d_out, dtype=np.float32)
+    for o in range(d_out):
+        amax = np.float32(np.max(np.abs(W[o]))) if d_in else np.float32(0)
+        if amax == 0:
+            continue
+        s = np.float32(amax / np.float32(127))
+        scales[o] = s
+        q = np.rint(W[o] / s)  # float32 quotient, ties to even
+        codes[o] = np.clip(q, -127, 127).astype(np.int8)
+    return codes, scales
+
+
+def dequantize_w0(codes, scales):
+    """W0[o][i] = code[o][i] * scale[o], one float32 product per entry."""
+    q = np.asarray(codes, dtype=np.int8).astype(np.float32)
+    s = np.asarray(scales, dtype=np.float32)
+    return q * s[:, None]
 
 
 # --------------------------------------------------------------------------

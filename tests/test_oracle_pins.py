@@ -381,3 +381,52 @@ def test_adam_second_step_by_hand():
     np.testing.assert_allclose(th, [th2], rtol=1e-12)
     np.testing.assert_allclose(m, [m_want], rtol=1e-12)
     np.testing.assert_allclose(v, [v_want], rtol=1e-12)
+
+
+# ------------------------------------------------------- INT8 frozen weight
+
+def test_quantize_rows_with_exact_scales():
+    # amax 127 gives scale 1 and amax 63.5 gives scale 0.5 exactly, so the
+    # codes are the round-half-even of the entries (or of twice them).
+    W = np.array([[127.0, 3.25, -64.5, 2.5, 0.0],
+                  [63.5, 1.25, -0.75, 0.5, -63.5]], dtype=np.float32)
+    q, s = oracle.quantize_w0(W)
+    assert s.dtype == np.float32 and q.dtype == np.int8
+    assert s.tolist() == [1.0, 0.5]
+    assert q.tolist() == [[127, 3, -64, 2, 0], [127, 2, -2, 1, -127]]
+    assert np.array_equal(oracle.dequantize_w0(q, s),
+                          np.array([[127, 3, -64, 2, 0], [63.5, 1, -1, 0.5, -63.5]],
+                                   dtype=np.float32))
+
+
+def test_quantize_zero_row_and_nearest_code():
+    rng = np.random.default_rng(50)
+    W = (rng.standard_normal((6, 200)) / np.sqrt(200)).astype(np.float32)
+    W[3] = 0
+    q, s = oracle.quantize_w0(W)
+    assert s[3] == 0 and not q[3].any()
+    assert np.all(oracle.dequantize_w0(q, s)[3] == 0)
+    for o in (0, 1, 2, 4, 5):
+        # the row's largest entry takes the largest code; every code is the
+        # nearest integer to W / scale (checked against the neighbours)
+        assert np.max(np.abs(q[o].astype(int))) == 127
+        assert int(q[o][np.argmax(np.abs(W[o]))]) == int(np.sign(W[o][np.argmax(np.abs(W[o]))])) * 127
+        ratio = W[o].astype(np.float64) / np.float64(s[o])
+        err = np.abs(ratio - q[o])
+        assert np.all(err <= 0.5 + 1e-5)
+        assert np.all(err <= np.abs(ratio - (q[o] + 1)) + 1e-9)
+        assert np.all(err <= np.abs(ratio - (q[o] - 1)) + 1e-9)
+        # the round trip is within half a step
+        deq = oracle.dequantize_w0(q[o:o + 1], s[o:o + 1])[0].astype(np.float64)
+        assert np.all(np.abs(deq - W[o]) <= 0.5 * s[o] * (1 + 1e-5))
+
+
+def test_quantize_scale_and_sign_symmetry():
+    rng = np.random.default_rng(51)
+    W = rng.standard_normal((4, 64)).astype(np.float32)
+    q, s = oracle.quantize_w0(W)
+    qn, sn = oracle.quantize_w0(-W)
+    assert np.array_equal(sn, s) and np.array_equal(qn, -q)
+    # a power-of-two scaling of a row scales its scale and keeps its codes
+    q2, s2 = oracle.quantize_w0(W * np.float32(4))
+    assert np.array_equal(q2, q) and np.array_equal(s2, s * 4)
