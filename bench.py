@@ -52,6 +52,9 @@ def parse():
     ap.add_argument("--train-step", action="store_true",
                     help="each step also applies Adam to theta_P and theta_R; the merge "
                          "W0 <- R W0 P is timed separately after the timed region")
+    ap.add_argument("--w0-int8", action="store_true",
+                    help="frozen weight held as INT8 codes with per-row scales, dequantised "
+                         "into a bf16 buffer inside every step")
     ap.add_argument("--recompute-v", action="store_true",
                     help="backward recomputes v = W0 P x instead of reading it (saves T x d_out)")
     return ap.parse_args()
@@ -70,6 +73,8 @@ def config_json(name, w, n, args=None):
         c["permuted_blocks"] = True
     if args is not None and getattr(args, "recompute_v", False):
         c["recompute_v"] = True
+    if args is not None and getattr(args, "w0_int8", False):
+        c["w0"] = "int8, per-row scales, dequantised each step"
     if args is not None and getattr(args, "train_step", False):
         c["optimizer"] = "adam (fused, in the step)"
     return c
@@ -333,6 +338,15 @@ def run_gpu(args):
 
         def step():
             layer.step(dev["theta_P"], dev["theta_R"], dev["x"], dev["dy"])
+    elif args.w0_int8:
+        from orthogonal_reparameterized_packed_gb300.layer import PoetxQLayer, quantize
+        layer = PoetxQLayer(w["d_in"], w["d_out"], w["b"], w["k"], w["tokens"], dtype=w["dtype"],
+                            recompute_v=args.recompute_v)
+        W0_q, scales = quantize(dev["W0"], layer.code)  # once per weight
+        del dev["W0"]
+
+        def step():
+            layer.step(dev["theta_P"], dev["theta_R"], W0_q, scales, dev["x"], dev["dy"])
     else:
         layer = PoetxLayer(w["d_in"], w["d_out"], w["b"], w["k"], w["tokens"], dtype=w["dtype"],
                            recompute_v=args.recompute_v)
@@ -426,7 +440,8 @@ def run_gpu(args):
     # per-kernel times over the timed region
     tags = ["build", "unpack", "identity_plus", "expand_superblocks", "transform",
             "transform_t", "gemm_w0", "gemm_w0_dgrad", "outer", "reduce_extract", "cnp_bwd",
-            "pack_skew", "f32_to_bf16", "chain", "prep_tiles", "pack_tiles", "permute", "adam"]
+            "pack_skew", "f32_to_bf16", "chain", "prep_tiles", "pack_tiles", "permute", "adam",
+            "dequantize", "quantize"]
     kernels = {}
     for t in tags:
         n, tot = poetx.poetx_profile_query(t)
@@ -455,8 +470,15 @@ def run_gpu(args):
                                  "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                  "frac": gbs / peaks["hbm_gbs"]}
 
+    if "dequantize" in kernels:  # INT8 -> bf16 weight, HBM-bound: 1 + 2 bytes per entry
+        dk = kernels["dequantize"]
+        gbs = 3.0 * w["d_in"] * w["d_out"] / (dk["avg_us"] * 1e-6) / 1e9
+        roofline["secondary"] = {"kernel": "dequantize", "bound": "hbm", "achieved": gbs,
+                                 "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                 "frac": gbs / peaks["hbm_gbs"]}
+
     merge = None
-    if args.train_step and not args.permute:
+    if args.train_step and not args.permute and not args.w0_int8:
         merge = time_merge(poetx, layer, dev, w, stream, peaks)
 
     # whole-step algorithmic tensor work for context

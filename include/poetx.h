@@ -213,6 +213,23 @@ poetx_status poetx_adam_update(float* theta, const float* grad, float* m, float*
                                float weight_decay, poetx_stream stream);
 
 /* ------------------------------------------------------------------------
+ * INT8 frozen weight (POET-XQ; technical summary, section 2, "Quantisierte
+ * Unterstuetzung (POET-XQ)": W0 is only the operand of one matmul, so it can
+ * be held quantised).  Symmetric, one scale per output row:
+ *   scale[o] = max_i |W0[o][i]| / 127   (float32; 0 for a zero row)
+ *   W0_q[o][i] = rint(W0[o][i] / scale[o]) clamped to [-127, 127]
+ *   (float32 IEEE division, ties to even).
+ * Dequantisation writes W0[o][i] = W0_q[o][i] * scale[o] (one float32
+ * product, rounded to dtype), the operand the forward and backward take.
+ *   W0, W0_q [d_out][d_in] row-major; scales [d_out] float32.
+ * d_in == 0 or d_out == 0 is a no-op; NULL pointers are INVALID_ARG.
+ * ------------------------------------------------------------------------ */
+poetx_status poetx_quantize_w0(const void* W0, int8_t* W0_q, float* scales, int d_in, int d_out,
+                               poetx_dtype dtype, poetx_stream stream);
+poetx_status poetx_dequantize_w0(const int8_t* W0_q, const float* scales, void* W0, int d_in,
+                                 int d_out, poetx_dtype dtype, poetx_stream stream);
+
+/* ------------------------------------------------------------------------
  * Status and measurement
  * ------------------------------------------------------------------------ */
 /* Synchronizes the current device, returns the status recorded by kernels

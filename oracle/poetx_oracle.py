@@ -56,7 +56,7 @@ reason in the design notes):
     dtheta[idx(i,j)] = G_Q[i][j] - G_Q[j][i].
   * INT8 W0 [tech-2-xq]: symmetric, one scale per output row,
     scale = max|W0[o,:]| / 127, code = round-half-even(W0 / scale) clamped
-    to [-127, 127]; a zero row has scale 0 and codes 0.  The quotient that
+    to [-127, 127]; a row whose scale is 0 has codes 0.  The quotient that
     decides each code, and the dequantised value code * scale, are taken in
     float32 (the precision of the kernels), so codes are exact to compare.
 """
@@ -356,9 +356,9 @@ def quantize_w0(W0):
     scales = np.zeros(d_out, dtype=np.float32)
     for o in range(d_out):
         amax = np.float32(np.max(np.abs(W[o]))) if d_in else np.float32(0)
-        if amax == 0:
-            continue
         s = np.float32(amax / np.float32(127))
+        if s == 0:  # a zero row (or one whose scale underflows): codes 0
+            continue
         scales[o] = s
         q = np.rint(W[o] / s)  # float32 quotient, ties to even
         codes[o] = np.clip(q, -127, 127).astype(np.int8)

@@ -20,7 +20,7 @@ __all__ = [
     "poetx_backward_workspace_size", "poetx_backward",
     "poetx_transform_workspace_size", "poetx_transform_forward", "poetx_transform_backward",
     "poetx_permute_features", "poetx_fold_permutations", "poetx_merge_workspace_size",
-    "poetx_merge", "poetx_adam_update",
+    "poetx_merge", "poetx_adam_update", "poetx_quantize_w0", "poetx_dequantize_w0",
     "poetx_device_status", "poetx_selftest_wait_timeout", "poetx_launch_count", "poetx_profile_start", "poetx_profile_stop",
     "poetx_profile_query", "poetx_status_string", "EXPORTED_SYMBOLS",
 ]
@@ -67,6 +67,8 @@ _SIGNATURES = {
     "poetx_adam_update": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_i64, _c_int,
                                    ctypes.c_float, ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                    ctypes.c_float, _c_ptr]),
+    "poetx_quantize_w0": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_ptr]),
+    "poetx_dequantize_w0": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_ptr]),
     "poetx_device_status": (_c_int, []),
     "poetx_selftest_wait_timeout": (_c_int, [ctypes.c_uint, _c_ptr]),
     "poetx_launch_count": (ctypes.c_longlong, []),
@@ -223,6 +225,16 @@ def poetx_adam_update(theta, grad, m, v, n, step, lr, beta1=0.9, beta2=0.999, ep
     _check("poetx_adam_update", load_library().poetx_adam_update(
         _ptr(theta), _ptr(grad), _ptr(m), _ptr(v), n, step, lr, beta1, beta2, eps, weight_decay,
         _stream(stream)))
+
+
+def poetx_quantize_w0(W0, W0_q, scales, d_in, d_out, dtype, stream=None):
+    _check("poetx_quantize_w0", load_library().poetx_quantize_w0(
+        _ptr(W0), _ptr(W0_q), _ptr(scales), d_in, d_out, dtype, _stream(stream)))
+
+
+def poetx_dequantize_w0(W0_q, scales, W0, d_in, d_out, dtype, stream=None):
+    _check("poetx_dequantize_w0", load_library().poetx_dequantize_w0(
+        _ptr(W0_q), _ptr(scales), _ptr(W0), d_in, d_out, dtype, _stream(stream)))
 
 
 def poetx_device_status() -> int:

@@ -1282,7 +1282,28 @@ poetx_status poetx_adam_update(float* theta, const float* grad, float* m, float*
                                static_cast<cudaStream_t>(stream)));
 }
 
+poetx_status poetx_quantize_w0(const void* W0, int8_t* W0_q, float* scales, int d_in, int d_out,
+                               poetx_dtype dtype, poetx_stream stream) {
+  if (dtype != POETX_F32 && dtype != POETX_BF16) return POETX_ERR_INVALID_ARG;
+  if (d_in < 0 || d_out < 0) return POETX_ERR_INVALID_ARG;
+  if (d_in == 0 || d_out == 0) return POETX_OK;
+  if (W0 == nullptr || W0_q == nullptr || scales == nullptr) return POETX_ERR_INVALID_ARG;
+  return to_status(launch_quantize_rows(W0, dtype == POETX_BF16, W0_q, scales, d_in, d_out,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+poetx_status poetx_dequantize_w0(const int8_t* W0_q, const float* scales, void* W0, int d_in,
+                                 int d_out, poetx_dtype dtype, poetx_stream stream) {
+  if (dtype != POETX_F32 && dtype != POETX_BF16) return POETX_ERR_INVALID_ARG;
+  if (d_in < 0 || d_out < 0) return POETX_ERR_INVALID_ARG;
+  if (d_in == 0 || d_out == 0) return POETX_OK;
+  if (W0 == nullptr || W0_q == nullptr || scales == nullptr) return POETX_ERR_INVALID_ARG;
+  return to_status(launch_dequantize(W0_q, scales, W0, dtype == POETX_BF16, d_in, d_out,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"
+
 
 
 

@@ -193,6 +193,11 @@ cudaError_t launch_pack_tiles(const float* D, float sign, int n_a, int n_b, int 
 cudaError_t launch_permute_rows(const void* in, long long in_rows, const int* row_map,
                                 const int* col_map, void* out, long long rows, int d,
                                 bool is_bf16, cudaStream_t s);
+// INT8 frozen weight: per-row codes and scales from W (bf16 or fp32), and back.
+cudaError_t launch_quantize_rows(const void* W, bool is_bf16, int8_t* q, float* scales, int d_in,
+                                 int d_out, cudaStream_t s);
+cudaError_t launch_dequantize(const int8_t* q, const float* scales, void* W, bool is_bf16,
+                              int d_in, int d_out, cudaStream_t s);
 // theta -= lr * (m_hat / (sqrt(v_hat) + eps) + wd * theta) with updated moments.
 cudaError_t launch_adam(float* theta, const float* grad, float* m, float* v, long long n,
                         float lr, float beta1, float beta2, float eps, float wd, float bc1,

@@ -409,6 +409,110 @@ __global__ void adam_kernel(float* __restrict__ theta, const float* __restrict__
   }
 }
 
+// ----------------------------------------------------- INT8 frozen weight
+// One CTA of 256 threads per output row: absmax, scale = absmax / 127, then
+// code = rint(w / scale) clamped to +-127 (float32 IEEE division; a zero row
+// gets scale 0 and codes 0).
+template <typename T>
+__device__ __forceinline__ float load_f32(const T* p, long long i);
+template <>
+__device__ __forceinline__ float load_f32<float>(const float* p, long long i) {
+  return p[i];
+}
+template <>
+__device__ __forceinline__ float load_f32<__nv_bfloat16>(const __nv_bfloat16* p, long long i) {
+  return __bfloat162float(p[i]);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) quantize_rows_kernel(const T* __restrict__ W,
+                                                            int8_t* __restrict__ q,
+                                                            float* __restrict__ scales, int d_in) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ float red[8];
+  const long long row0 = static_cast<long long>(blockIdx.x) * d_in;
+  float amax = 0.f;
+  for (int i = threadIdx.x; i < d_in; i += 256) amax = fmaxf(amax, fabsf(load_f32(W, row0 + i)));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  amax = red[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) amax = fmaxf(amax, red[w]);
+  const float scale = amax > 0.f ? amax / 127.f : 0.f;
+  if (threadIdx.x == 0) scales[blockIdx.x] = scale;
+  for (int i = threadIdx.x; i < d_in; i += 256) {
+    float c = scale > 0.f ? rintf(load_f32(W, row0 + i) / scale) : 0.f;
+    c = fminf(fmaxf(c, -127.f), 127.f);
+    q[row0 + i] = static_cast<int8_t>(static_cast<int>(c));
+  }
+}
+
+// W[o][i] = code * scale[o] (one float32 product, rounded to T); sixteen
+// codes per thread and 16-byte accesses when d_in % 16 == 0.
+template <typename T>
+__device__ __forceinline__ void store_16(T* dst, const float* v);
+template <>
+__device__ __forceinline__ void store_16<float>(float* dst, const float* v) {
+  float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) d[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+}
+template <>
+__device__ __forceinline__ void store_16<__nv_bfloat16>(__nv_bfloat16* dst, const float* v) {
+  uint32_t w[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+    w[j] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  uint4* d = reinterpret_cast<uint4*>(dst);
+  d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float v);
+template <>
+__device__ __forceinline__ float from_f32<float>(float v) {
+  return v;
+}
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+template <typename T>
+__global__ void dequantize_kernel(const int8_t* __restrict__ q, const float* __restrict__ scales,
+                                  T* __restrict__ W, int d_in, long long total, int vec) {
+  pdl_wait();
+  pdl_trigger();
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  if (vec) {
+    const long long chunks = total / 16;
+    for (long long c = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; c < chunks;
+         c += stride) {
+      const long long e0 = c * 16;
+      const float s = scales[e0 / d_in];  // d_in % 16 == 0: one row per chunk
+      const int4 raw = reinterpret_cast<const int4*>(q)[c];
+      const int words[4] = {raw.x, raw.y, raw.z, raw.w};
+      float v[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int byte = (words[j >> 2] >> (8 * (j & 3))) & 0xff;
+        v[j] = static_cast<float>(static_cast<int8_t>(byte)) * s;
+      }
+      store_16(W + e0, v);
+    }
+  } else {
+    for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < total;
+         e += stride)
+      W[e] = from_f32<T>(static_cast<float>(q[e]) * scales[e / d_in]);
+  }
+}
+
 int ew_grid(long long total) {
   long long blocks = (total + 255) / 256;
   const long long cap = static_cast<long long>(sm_count()) * 16;
@@ -536,6 +640,42 @@ cudaError_t launch_adam(float* theta, const float* grad, float* m, float* v, lon
                         float bc2, cudaStream_t s) {
   POETX_EW_LAUNCH("adam", n, adam_kernel, theta, grad, m, v, n, lr, beta1, beta2, eps, wd, bc1,
                   bc2);
+}
+
+cudaError_t launch_quantize_rows(const void* W, bool is_bf16, int8_t* q, float* scales, int d_in,
+                                 int d_out, cudaStream_t s) {
+  if (d_in <= 0 || d_out <= 0) return cudaSuccess;
+  prof_begin("quantize", s);
+  cudaError_t e =
+      is_bf16 ? launch_pdl(quantize_rows_kernel<__nv_bfloat16>, dim3(d_out), dim3(256), 0, s,
+                           static_cast<const __nv_bfloat16*>(W), q, scales, d_in)
+              : launch_pdl(quantize_rows_kernel<float>, dim3(d_out), dim3(256), 0, s,
+                           static_cast<const float*>(W), q, scales, d_in);
+  prof_end("quantize", s);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_dequantize(const int8_t* q, const float* scales, void* W, bool is_bf16,
+                              int d_in, int d_out, cudaStream_t s) {
+  const long long total = static_cast<long long>(d_in) * d_out;
+  if (total <= 0) return cudaSuccess;
+  const int vec = (d_in % 16 == 0 && reinterpret_cast<uintptr_t>(q) % 16 == 0 &&
+                   reinterpret_cast<uintptr_t>(W) % 16 == 0)
+                      ? 1
+                      : 0;
+  const long long items = vec ? total / 16 : total;
+  long long blocks = (items + 255) / 256;
+  const long long cap = static_cast<long long>(sm_count()) * 8;
+  if (blocks > cap) blocks = cap;
+  prof_begin("dequantize", s);
+  cudaError_t e =
+      is_bf16 ? launch_pdl(dequantize_kernel<__nv_bfloat16>, dim3(static_cast<unsigned>(blocks)),
+                           dim3(256), 0, s, q, scales, static_cast<__nv_bfloat16*>(W), d_in,
+                           total, vec)
+              : launch_pdl(dequantize_kernel<float>, dim3(static_cast<unsigned>(blocks)),
+                           dim3(256), 0, s, q, scales, static_cast<float*>(W), d_in, total, vec);
+  prof_end("dequantize", s);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_f32_to_bf16(const float* in, long long count, __nv_bfloat16* out,

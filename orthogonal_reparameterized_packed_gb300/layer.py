@@ -9,9 +9,10 @@ import numpy as np
 import torch
 
 from . import (BF16, F32, poetx_adam_update, poetx_backward, poetx_backward_workspace_size,
-               poetx_build_blocks, poetx_build_workspace_size, poetx_fold_permutations,
-               poetx_forward, poetx_forward_workspace_size, poetx_merge,
-               poetx_merge_workspace_size, poetx_packed_size, poetx_permute_features)
+               poetx_build_blocks, poetx_build_workspace_size, poetx_dequantize_w0,
+               poetx_fold_permutations, poetx_forward, poetx_forward_workspace_size,
+               poetx_merge, poetx_merge_workspace_size, poetx_packed_size,
+               poetx_permute_features, poetx_quantize_w0)
 
 _TORCH_DTYPE = {F32: torch.float32, BF16: torch.bfloat16}
 
@@ -106,6 +107,48 @@ class PoetxLayer:
         Uses the blocks of the last build()."""
         poetx_merge(W0, self.P_blocks, self.R_blocks, W0, theta_P, theta_R, self.d_in,
                     self.d_out, self.b, self.code, self.workspace, stream)
+
+
+class PoetxQLayer(PoetxLayer):
+    """The layer with its frozen weight held as INT8 codes and per-row
+    scales.  Each step dequantises W0 into a bf16 (or fp32) buffer that the
+    forward and backward read; the buffer is scratch shared by nothing
+    else, so a model can reuse one for all its layers."""
+
+    def __init__(self, d_in, d_out, b, k, tokens, dtype="bf16", device="cuda",
+                 recompute_v=False):
+        super().__init__(d_in, d_out, b, k, tokens, dtype=dtype, device=device,
+                         recompute_v=recompute_v)
+        self.W0 = torch.empty((d_out, d_in), dtype=_TORCH_DTYPE[self.code],
+                              device=torch.device(device))
+
+    def dequantize(self, W0_q, scales, stream=None):
+        poetx_dequantize_w0(W0_q, scales, self.W0, self.d_in, self.d_out, self.code, stream)
+        return self.W0
+
+    def step(self, theta_P, theta_R, W0_q, scales, x, dy, stream=None):
+        self.build(theta_P, theta_R, stream)
+        self.dequantize(W0_q, scales, stream)
+        self.forward(x, self.W0, stream)
+        self.backward(dy, x, self.W0, theta_P, theta_R, stream)
+        return self.y, self.dx, self.dtheta_P, self.dtheta_R
+
+    def merge_quantized(self, W0_q, scales, theta_P, theta_R, stream=None):
+        """W0 <- R W0 P on the dequantised weight, then re-quantised in place;
+        the factors restart at the identity.  Uses the blocks of the last
+        build()."""
+        self.dequantize(W0_q, scales, stream)
+        self.merge(self.W0, theta_P, theta_R, stream)
+        poetx_quantize_w0(self.W0, W0_q, scales, self.d_in, self.d_out, self.code, stream)
+
+
+def quantize(W0, code, stream=None):
+    """INT8 codes and float32 scales of a [d_out][d_in] weight tensor."""
+    d_out, d_in = W0.shape
+    q = torch.empty((d_out, d_in), dtype=torch.int8, device=W0.device)
+    s = torch.empty((d_out,), dtype=torch.float32, device=W0.device)
+    poetx_quantize_w0(W0, q, s, d_in, d_out, code, stream)
+    return q, s
 
 
 class PoetxAdam:

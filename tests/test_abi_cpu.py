@@ -156,3 +156,14 @@ def test_merge_and_adam_reject_invalid_arguments(lib):
                                f(0.0), None) == 1
     assert L.poetx_adam_update(None, None, None, None, 0, 1, f(1e-3), f(0.9), f(0.999), f(1e-8),
                                f(0.0), None) == 0
+
+
+def test_int8_weight_calls_reject_invalid_arguments(lib):
+    L = _raw()
+    for fn in (L.poetx_quantize_w0, L.poetx_dequantize_w0):
+        assert fn(FAKE, FAKE, FAKE, 64, 64, 7, None) == 1
+        assert fn(FAKE, FAKE, FAKE, -1, 64, poetx.BF16, None) == 1
+        assert fn(None, FAKE, FAKE, 64, 64, poetx.BF16, None) == 1
+        assert fn(FAKE, None, FAKE, 64, 64, poetx.F32, None) == 1
+        assert fn(FAKE, FAKE, None, 64, 64, poetx.F32, None) == 1
+        assert fn(None, None, None, 0, 64, poetx.BF16, None) == 0  # empty: nothing to do
