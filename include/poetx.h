@@ -84,6 +84,9 @@ size_t poetx_packed_size(int d, int b);
  * cores with fp32 accumulation (BF16, b >= 128); rounded once at the store.
  *   theta  [d/b][b(b-1)/2] float32 (read only)
  *   blocks [d/b][b][b] dtype (written)
+ * Blocks are independent, so both factors of a layer are one call when
+ * theta_P and theta_R lie back to back (and the blocks likewise):
+ * d = d_in + d_out builds P's blocks then R's, bitwise as two calls would.
  * ------------------------------------------------------------------------ */
 size_t poetx_build_workspace_size(int d, int b, int k, poetx_dtype dtype);
 poetx_status poetx_build_blocks(const float* theta, int d, int b, int k, poetx_dtype dtype,
