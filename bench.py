@@ -282,7 +282,11 @@ def algorithmic_work(tag, w):
     """(amount, unit, bound) per launch for a kernel tag of one step."""
     T, di, do, b = w["tokens"], w["d_in"], w["d_out"], w["b"]
     if tag in ("gemm_w0", "gemm_w0_dgrad"):
-        return 2.0 * T * di * do / 1e12, "TFLOP", "tensor"
+        return 2.0 * T * di * do / 1e12, "TFLOP", "tensor", "2*T*d_in*d_out"
+    if tag == "gemm_w0_r":  # v = u W0^T with y = v R^T in the epilogue
+        return 2.0 * T * do * (di + b) / 1e12, "TFLOP", "tensor", "2*T*d_out*(d_in+b)"
+    if tag == "gemm_w0_dgrad_p":  # du = dv W0 with dx = du P in the epilogue
+        return 2.0 * T * di * (do + b) / 1e12, "TFLOP", "tensor", "2*T*d_in*(d_out+b)"
     return None
 
 
@@ -443,7 +447,7 @@ def run_gpu(args):
 
     # per-kernel times over the timed region
     tags = ["build", "unpack", "identity_plus", "expand_superblocks", "transform",
-            "transform_t", "gemm_w0", "gemm_w0_dgrad", "outer", "reduce_extract", "cnp_bwd",
+            "transform_t", "gemm_w0", "gemm_w0_dgrad", "gemm_w0_r", "gemm_w0_dgrad_p", "outer", "reduce_extract", "cnp_bwd",
             "pack_skew", "f32_to_bf16", "chain", "prep_tiles", "pack_tiles", "permute", "adam",
             "dequantize", "quantize"]
     kernels = {}
@@ -453,7 +457,7 @@ def run_gpu(args):
             kernels[t] = {"launches": n, "total_ms": tot, "avg_us": 1e3 * tot / n}
     peaks, peak_src = load_peaks()
     dom = max((t for t in kernels if algorithmic_work(t, w)), key=lambda t: kernels[t]["total_ms"])
-    amount, unit, bound = algorithmic_work(dom, w)
+    amount, unit, bound, formula = algorithmic_work(dom, w)
     avg_s = kernels[dom]["avg_us"] * 1e-6
     long_region = ms_eager * args.steps > 1000.0
     peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
@@ -462,7 +466,7 @@ def run_gpu(args):
                 "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": captured_traffic(name, dom),
                 "peak_source": f"{peak_src} ({'sustained' if long_region else 'burst'})",
-                "per_launch": f"2*T*d_in*d_out = {amount:.4f} TFLOP",
+                "per_launch": f"{formula} = {amount:.4f} TFLOP",
                 "timing": "CUDA events around each launch, eager pass of the same K steps"}
 
     if "permute" in kernels:  # index-map kernel: HBM-bound, reads and writes T x d

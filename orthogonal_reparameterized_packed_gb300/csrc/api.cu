@@ -254,6 +254,43 @@ cudaError_t tc_w0(const bf16* A, const bf16* W0, bf16* out, int d_in, int d_out,
   return tc_gemm_run(g, s);
 }
 
+// The W0 GEMMs with the block-diagonal factor applied in the epilogue (256 x
+// 256 superblocks): fwd v = u W0^T and y = v R^T per block; dgrad du = dv W0
+// and dx = du P per block.  `out` (v or du) may be null: then only the
+// block output is written.
+constexpr bool kFuseBlockEpilogue = true;
+
+bool fuse_block_epilogue(bool is_bf16, int b) { return kFuseBlockEpilogue && is_bf16 && b <= 256; }
+
+cudaError_t tc_w0_block(const bf16* A, const bf16* W0, const bf16* sb, bf16* out, bf16* out_blk,
+                        int d_in, int d_out, long long T, bool dgrad, cudaStream_t s) {
+  TcGemm g;
+  g.M = static_cast<int>(T);
+  g.BN = 256;
+  if (!dgrad) {
+    g.N = d_out;
+    g.K = d_in;
+    g.A = op(A, T, d_in, d_in, false, 0, 0);
+    g.B = op(W0, d_out, d_in, d_in, false, 0, 0);
+    g.blk = op(sb, d_out, 256, 256, false, 0, 0);  // blk_j[n][kk] = R_j[n][kk]
+    g.epi.ld = d_out;
+    g.tag = "gemm_w0_r";
+  } else {
+    g.N = d_in;
+    g.K = d_out;
+    g.A = op(A, T, d_out, d_out, false, 0, 0);
+    g.B = op(W0, d_out, d_in, d_in, true, 0, 0);
+    g.blk = op(sb, d_in, 256, 256, true, 0, 0);  // rows kk, columns n of P_j
+    g.epi.ld = d_in;
+    g.tag = "gemm_w0_dgrad_p";
+  }
+  g.epi.out_bf16 = out;
+  g.out_blk = out_blk;
+  g.epi.row_limit = static_cast<int>(T);
+  g.epi.out_rows = T;
+  return tc_gemm_run(g, s);
+}
+
 // fp32 block-diagonal transform: out[:, g] = in[:, g] B_g^T (or B_g).
 cudaError_t simt_transform(const float* in, const float* blocks, float* out, int d, int b,
                            long long T, bool transposed, const char* tag, cudaStream_t s) {
@@ -641,7 +678,7 @@ FwdPlan carve_forward(Carver& c, int d_in, int d_out, int b, long long T, bool i
                       bool need_v) {
   FwdPlan p;
   p.sb.u = take_act(c, T, d_in, is_bf16);
-  if (need_v) p.sb.v = take_act(c, T, d_out, is_bf16);
+  if (need_v && !fuse_block_epilogue(is_bf16, b)) p.sb.v = take_act(c, T, d_out, is_bf16);
   if (is_bf16 && b < 256) {
     p.sb.psb = c.take<bf16>(static_cast<size_t>(d_in) * 256);
     p.sb.rsb = c.take<bf16>(static_cast<size_t>(d_out) * 256);
@@ -871,6 +908,14 @@ poetx_status poetx_forward(const void* x, const void* W0, const void* P_blocks,
   if (e != cudaSuccess) return POETX_ERR_CUDA;
   const void* rsb = superblocks_or_blocks(R_blocks, p.sb.rsb, d_out, b, is_bf16, s, &e);
   if (e != cudaSuccess) return POETX_ERR_CUDA;
+  if (fuse_block_epilogue(is_bf16, b)) {  // u = P x; v = W0 u and y = R v in one GEMM
+    e = tc_transform(static_cast<const bf16*>(x), static_cast<const bf16*>(psb),
+                     static_cast<bf16*>(p.sb.u), d_in, 256, tokens, false, "transform", s);
+    if (e != cudaSuccess) return POETX_ERR_CUDA;
+    return to_status(tc_w0_block(static_cast<const bf16*>(p.sb.u), static_cast<const bf16*>(W0),
+                                 static_cast<const bf16*>(rsb), static_cast<bf16*>(v_saved),
+                                 static_cast<bf16*>(y), d_in, d_out, tokens, false, s));
+  }
   void* v = v_saved != nullptr ? v_saved : p.sb.v;
   e = run_forward_uv(x, W0, psb, p.sb.u, v, d_in, d_out, b, tokens, is_bf16, s);
   if (e != cudaSuccess) return POETX_ERR_CUDA;
@@ -953,8 +998,13 @@ poetx_status poetx_backward(const void* dy, const void* x, const void* W0, const
     e = block_gradient(dy, v, d_out, b, tokens, is_bf16, p.sb.part, p.splits_out,
                        p.cnp.g32[0] + off_R, p.cnp.g16[0] ? p.cnp.g16[0] + off_R : nullptr, s);
   if (e != cudaSuccess) return POETX_ERR_CUDA;
-  // du = dv W0
-  if (is_bf16)
+  // du = dv W0, and dx = du P (in the same GEMM's epilogue when it fuses)
+  const bool fused = fuse_block_epilogue(is_bf16, b);
+  if (fused)
+    e = tc_w0_block(static_cast<const bf16*>(p.sb.dv), static_cast<const bf16*>(W0),
+                    static_cast<const bf16*>(psb), static_cast<bf16*>(p.sb.du),
+                    static_cast<bf16*>(dx), d_in, d_out, tokens, true, s);
+  else if (is_bf16)
     e = tc_w0(static_cast<const bf16*>(p.sb.dv), static_cast<const bf16*>(W0),
               static_cast<bf16*>(p.sb.du), d_in, d_out, tokens, true, s);
   else
@@ -962,7 +1012,9 @@ poetx_status poetx_backward(const void* dy, const void* x, const void* W0, const
                 static_cast<float*>(p.sb.du), d_in, d_out, tokens, true, s);
   if (e != cudaSuccess) return POETX_ERR_CUDA;
   // P side: dx = du P, G_P = sum_t du_t x_t^T
-  if (is_bf16)
+  if (fused)
+    e = cudaSuccess;
+  else if (is_bf16)
     e = tc_transform(static_cast<const bf16*>(p.sb.du), static_cast<const bf16*>(psb),
                      static_cast<bf16*>(dx), d_in, S, tokens, true, "transform_t", s);
   else

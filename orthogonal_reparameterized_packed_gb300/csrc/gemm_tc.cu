@@ -19,6 +19,13 @@
 //          outputs) with 16-byte stores.  EPI_TMA_BF16 / EPI_TMA_F32: plain
 //          stores of one output; each warp writes its 32-row chunk into a
 //          128B-swizzled staging buffer and one lane issues a TMA tile store.
+//          EPI_BLOCK: the block-diagonal factor applied in the epilogue.  The
+//          output tile (128 rows x 256 = one 256 x 256 block's columns) is
+//          rounded to bf16 into a 64 KiB staging tile (stored as the main
+//          output when one is given), which then is the A operand of a second
+//          MMA with that block (streamed through the ring) into the same
+//          accumulator; the result is the block output.  Three ring stages
+//          leave room for the staging tile.
 //
 // Every barrier wait is bounded: on expiry the CTA records
 // POETX_ERR_TIMEOUT, drains what it issued, frees TMEM and returns.
@@ -33,29 +40,35 @@ namespace poetx {
 
 namespace {
 
-constexpr int STAGES = 4;
 constexpr int NUM_THREADS = 192;
 constexpr int kResBytes = 128 * 1024;
 
-enum { EPI_ROWS = 0, EPI_TMA_BF16 = 1, EPI_TMA_F32 = 2 };
+enum { EPI_ROWS = 0, EPI_TMA_BF16 = 1, EPI_TMA_F32 = 2, EPI_BLOCK = 3 };
 
 template <int BN, bool B_RES, int EPI>
 struct TcShape {
+  static constexpr int STAGES = EPI == EPI_BLOCK ? 3 : 4;
   static constexpr int A_BYTES = BM * BK * 2;  // 16 KB
   static constexpr int B_BYTES = BN * BK * 2;  // one K step of B: 16 or 32 KB
   static constexpr int RING = B_RES ? STAGES * A_BYTES : STAGES * (A_BYTES + B_BYTES);
   static constexpr int RES = B_RES ? kResBytes : 0;
   static constexpr int MAX_RES_KSTEPS = kResBytes / B_BYTES;
-  static constexpr int OUT_STAGE = EPI == EPI_ROWS ? 0 : 4 * 4096;  // per warp 32 rows x 128 B
+  // TMA-store staging: per warp 32 rows x 128 B; EPI_BLOCK: the 128 x 256 bf16 tile
+  static constexpr int OUT_STAGE = EPI == EPI_ROWS ? 0 : (EPI == EPI_BLOCK ? BM * BN * 2 : 4 * 4096);
   static constexpr int SMEM = 1024 + RING + RES + OUT_STAGE + 256;
   static constexpr uint32_t TMEM_COLS = 2 * BN;
+  static_assert(EPI != EPI_BLOCK || (BN == 256 && !B_RES), "block epilogue: 256-wide tiles");
+  static_assert(SMEM <= 227 * 1024, "shared memory per CTA");
 };
+
+constexpr int kBlockKSteps = 256 / BK;  // K steps of the epilogue's 256 x 256 block
 
 struct TcKernelArgs {
   int m_tiles, n_tiles, splits, batches;
   int k_steps_total, k_steps_per_split;
   int a_mn_per_g, a_k_per_g, b_mn_per_g, b_k_per_g;
   EpiArgs epi;
+  int store_main;  // EPI_BLOCK: also store the tile before the block (tmC)
   int* status;
 };
 
@@ -98,15 +111,50 @@ struct TileRange {
   }
 };
 
+// EPI_BLOCK: this warp's 32 accumulator rows (256 fp32 columns) -> bf16 rows
+// of the 128 x 256 staging tile, laid out as four 128B-swizzled K-major
+// 128 x 64 chunks (the form TMA stores from and the MMA reads A from).
+__device__ __forceinline__ void stage_rows_bf16(uint32_t t_base, uint8_t* stage, int row) {
+#pragma unroll 1
+  for (int cc = 0; cc < 4; ++cc) {
+    uint32_t r0[32], r1[32];
+    tmem_load_32cols(t_base + cc * 64, r0);
+    tmem_load_32cols(t_base + cc * 64 + 32, r1);
+    tmem_load_wait();
+    uint32_t w[32];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      w[j] = pack_bf16x2(r0[2 * j], r0[2 * j + 1]);
+      w[16 + j] = pack_bf16x2(r1[2 * j], r1[2 * j + 1]);
+    }
+    uint8_t* dst = stage + cc * (BM * 128) + row * 128;
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      st_shared_v4(dst + ((q ^ (row & 7)) << 4), w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+  }
+}
+
+// One lane stores this warp's 32 staged rows (four 64-column boxes).
+__device__ __forceinline__ void store_staged_rows(const CUtensorMap* map, uint8_t* stage,
+                                                  int quarter, int col0, int row0) {
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc)
+    tma_store_2d(map, stage + cc * (BM * 128) + quarter * 4096, col0 + cc * 64, row0);
+  bulk_commit();
+}
+
 template <bool A_MN, bool B_MN, int BN, bool B_RES, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, const TcKernelArgs p) {
+                   const __grid_constant__ CUtensorMap tmC,
+                   const __grid_constant__ CUtensorMap tmR,
+                   const __grid_constant__ CUtensorMap tmY, const TcKernelArgs p) {
   using S = TcShape<BN, B_RES, EPI>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  constexpr int STAGES = S::STAGES;
   uint8_t* sA = base;                        // STAGES x A tile
   uint8_t* sB = base + STAGES * S::A_BYTES;  // STAGES x B tile (streamed variants)
   uint8_t* sRes = base + S::RING;            // resident B (B_RES)
@@ -118,7 +166,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* drain_bar = tempty_bar + 2;
   uint64_t* bfull_bar = drain_bar + 1;
   uint64_t* bempty_bar = bfull_bar + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bempty_bar + 1);
+  uint64_t* vstaged_bar = bempty_bar + 1;  // EPI_BLOCK: staging tile written (4 warps)
+  uint64_t* yfull_bar = vstaged_bar + 1;   // EPI_BLOCK: block MMA done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(yfull_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32;
@@ -138,6 +188,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(drain_bar, 1);
     mbar_init(bfull_bar, 1);
     mbar_init(bempty_bar, 1);
+    mbar_init(vstaged_bar, 4);
+    mbar_init(yfull_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -145,6 +197,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     if (EPI != EPI_ROWS) tma_prefetch_desc(&tmC);
+    if (EPI == EPI_BLOCK) {
+      tma_prefetch_desc(&tmR);
+      tma_prefetch_desc(&tmY);
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, S::TMEM_COLS);
@@ -229,6 +285,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             phase ^= 1;
           }
         }
+        if (EPI == EPI_BLOCK) {
+          // the 256 x 256 block of this N tile, one K step per ring stage (B slot)
+          for (int kc = 0; kc < kBlockKSteps && ok; ++kc) {
+            if (!mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag)) {
+              record_timeout(p.status, abort_flag);
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full_bar[stage], S::B_BYTES);
+            uint8_t* b_dst = sB + stage * S::B_BYTES;
+            const int blk_row = nt * BN;  // block nt covers output columns nt*256 ..
+            if (!B_MN) {
+              tma_load_2d(b_dst, &tmR, &full_bar[stage], kc * BK, blk_row);
+            } else {
+#pragma unroll
+              for (int c = 0; c < BN / 64; ++c)
+                tma_load_2d(b_dst + c * 8192, &tmR, &full_bar[stage], 64 * c, blk_row + kc * BK);
+            }
+            ++issued;
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+        }
       }
       if (!ok) {
         // Let the copies already issued land before the CTA exits.
@@ -263,6 +344,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool ok = true;
       bool any_mma = false;
       int res_key = -1, res_loads = 0;
+      uint32_t vphase = 0;
       for (int tile = range.first; tile < range.end && ok; tile += range.step) {
         int g, sp, mt, nt;
         decode_tile<B_RES>(tile, p, g, sp, mt, nt);
@@ -316,6 +398,41 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (!ok) break;
         umma_commit(&tfull_bar[acc]);  // accumulator ready for the epilogue
+        if (EPI == EPI_BLOCK) {
+          // the epilogue has read the tile and staged it in bf16: the block
+          // product overwrites the same accumulator
+          if (!mbar_wait(vstaged_bar, vphase, abort_flag)) {
+            record_timeout(p.status, abort_flag);
+            ok = false;
+            break;
+          }
+          vphase ^= 1;
+          tc_fence_after();
+          const uint32_t v_base = smem_u32(sOut);
+          for (int kc = 0; kc < kBlockKSteps; ++kc) {
+            if (!mbar_wait(&full_bar[stage], phase, abort_flag)) {
+              record_timeout(p.status, abort_flag);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t b_base = smem_u32(sB + stage * S::B_BYTES);
+#pragma unroll
+            for (int j = 0; j < BK / 16; ++j) {
+              const uint64_t adesc = smem_desc_sw128(v_base + kc * (BM * 128) + j * 32, 16, 1024);
+              const uint64_t bdesc = B_MN ? smem_desc_sw128(b_base + j * 2048, 8192, 1024)
+                                          : smem_desc_sw128(b_base + j * 32, 16, 1024);
+              umma_bf16(d_tmem, adesc, bdesc, IDESC, (kc > 0 || j > 0) ? 1u : 0u);
+            }
+            umma_commit(&empty_bar[stage]);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1;
+            }
+          }
+          if (!ok) break;
+          umma_commit(yfull_bar);
+        }
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
       }
@@ -334,6 +451,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     bool stores_pending = false;
     int acc = 0;
     uint32_t acc_phase = 0;
+    uint32_t yphase = 0;
     for (int tile = range.first; tile < range.end; tile += range.step) {
       int g, sp, mt, nt;
       decode_tile<B_RES>(tile, p, g, sp, mt, nt);
@@ -345,7 +463,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_after();
       const uint32_t t_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                               static_cast<uint32_t>(acc * BN);
-      if (EPI == EPI_ROWS) {
+      if (EPI == EPI_BLOCK) {
+        const int out_row = g * p.epi.row_g + sp * p.epi.row_s + mt * BM + quarter * 32;
+        const int out_col0 = g * p.epi.col_g + nt * BN;
+        const int row = quarter * 32 + lane;
+        // the staging rows are free once this warp's last stores have read them
+        if (lane == 0 && stores_pending) bulk_wait_read_all();
+        __syncwarp();
+        stage_rows_bf16(t_base, sOut, row);
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0 && p.store_main) {
+          store_staged_rows(&tmC, sOut, quarter, out_col0, out_row);
+          stores_pending = true;
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(vstaged_bar);
+        const bool ygot = mbar_wait(yfull_bar, yphase, abort_flag);
+        yphase ^= 1;
+        if (!__all_sync(0xffffffffu, ygot)) {
+          record_timeout(p.status, abort_flag);
+          break;
+        }
+        tc_fence_after();
+        if (lane == 0 && stores_pending) bulk_wait_read_all();
+        __syncwarp();
+        stage_rows_bf16(t_base, sOut, row);
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+          store_staged_rows(&tmY, sOut, quarter, out_col0, out_row);
+          stores_pending = true;
+        }
+      } else if (EPI == EPI_ROWS) {
         const int row = mt * BM + quarter * 32 + lane;
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
@@ -424,12 +575,12 @@ cudaError_t launch_tc(const TcGemm& g, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  CUtensorMap tmA, tmB, tmC;
+  CUtensorMap tmA, tmB, tmC, tmR, tmY;
   if (!make_map(&tmA, g.A.ptr, g.A.rows, g.A.cols, g.A.pitch, 2, 64, A_MN ? 64 : BM))
     return cudaErrorInvalidValue;
   if (!make_map(&tmB, g.B.ptr, g.B.rows, g.B.cols, g.B.pitch, 2, 64, B_MN ? 64 : BN))
     return cudaErrorInvalidValue;
-  if (EPI == EPI_TMA_BF16) {
+  if (EPI == EPI_TMA_BF16 || (EPI == EPI_BLOCK && g.epi.out_bf16 != nullptr)) {
     if (!make_map(&tmC, g.epi.out_bf16, g.epi.out_rows, g.epi.ld, g.epi.ld, 2, 64, 32))
       return cudaErrorInvalidValue;
   } else if (EPI == EPI_TMA_F32) {
@@ -437,6 +588,16 @@ cudaError_t launch_tc(const TcGemm& g, cudaStream_t stream) {
       return cudaErrorInvalidValue;
   } else {
     tmC = tmA;  // unused
+  }
+  if (EPI == EPI_BLOCK) {
+    if (g.epi.out_bf16 == nullptr) tmC = tmA;  // no main output: never stored
+    if (!make_map(&tmR, g.blk.ptr, g.blk.rows, g.blk.cols, g.blk.pitch, 2, 64, B_MN ? 64 : BN))
+      return cudaErrorInvalidValue;
+    if (!make_map(&tmY, g.out_blk, g.epi.out_rows, g.epi.ld, g.epi.ld, 2, 64, 32))
+      return cudaErrorInvalidValue;
+  } else {
+    tmR = tmA;  // unused
+    tmY = tmA;
   }
 
   TcKernelArgs p;
@@ -452,6 +613,7 @@ cudaError_t launch_tc(const TcGemm& g, cudaStream_t stream) {
   p.b_mn_per_g = g.B.mn_per_g;
   p.b_k_per_g = g.B.k_per_g;
   p.epi = g.epi;
+  p.store_main = g.epi.out_bf16 != nullptr ? 1 : 0;
   p.status = device_status_ptr();
   if (B_RES && (p.splits != 1 || p.k_steps_total > S::MAX_RES_KSTEPS))
     return cudaErrorInvalidValue;
@@ -464,7 +626,7 @@ cudaError_t launch_tc(const TcGemm& g, cudaStream_t stream) {
   }
   prof_begin(g.tag, stream);
   cudaError_t e = launch_pdl(tc_gemm_kernel<A_MN, B_MN, BN, B_RES, EPI>, dim3(grid),
-                             dim3(NUM_THREADS), S::SMEM, stream, tmA, tmB, tmC, p);
+                             dim3(NUM_THREADS), S::SMEM, stream, tmA, tmB, tmC, tmR, tmY, p);
   prof_end(g.tag, stream);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -487,6 +649,16 @@ cudaError_t tc_gemm_run(const TcGemm& g, cudaStream_t stream) {
   if (g.M <= 0 || g.N <= 0 || g.K <= 0 || g.batches <= 0) return cudaSuccess;
   if ((g.BN != 128 && g.BN != 256) || g.N % g.BN != 0) return cudaErrorInvalidValue;
   const bool a = g.A.mn_major, b = g.B.mn_major;
+  if (g.out_blk != nullptr) {
+    // W0 GEMM with the block-diagonal factor applied in its epilogue; the
+    // block operand has the same major-ness as B
+    if (g.BN != 256 || g.b_resident || a || g.batches != 1 || g.splits != 1 ||
+        g.blk.mn_major != b || g.epi.out_f32 != nullptr || g.epi.alpha != 1.f ||
+        g.epi.X != nullptr || g.epi.Y != nullptr || g.epi.delta != 0.f || g.epi.out_rows <= 0)
+      return cudaErrorInvalidValue;
+    if (!b) return launch_tc<false, false, 256, false, EPI_BLOCK>(g, stream);
+    return launch_tc<false, true, 256, false, EPI_BLOCK>(g, stream);
+  }
   if (!plain_output(g.epi)) {
     // general epilogue: the b x b products of the block build and its adjoint
     if (g.BN != 128 || g.b_resident) return cudaErrorInvalidValue;

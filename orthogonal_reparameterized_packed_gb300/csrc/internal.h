@@ -73,6 +73,13 @@ struct TcGemm {
   bool b_resident = false;
   TcOperand A, B;
   EpiArgs epi;
+  // Block-diagonal factor in the epilogue (W0 GEMMs, BN = 256): N tile j of
+  // the product (written to epi.out_bf16 when that is set) is multiplied by
+  // the 256 x 256 block j of `blk` (rows j*256.., same major-ness as B:
+  // out_blk[:, j] = C[:, j] * blk_j^T for K-major, C[:, j] * blk_j for
+  // MN-major) and written to out_blk with the layout of epi.
+  TcOperand blk;
+  __nv_bfloat16* out_blk = nullptr;
   const char* tag = "tc_gemm";  // name under which launches are profiled
 };
 
