@@ -221,6 +221,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       long long issued = 0;
       bool ok = true;
       int res_key = -1, res_loads = 0;
+      int prev_nt = -1;
+      // EPI_BLOCK: the 256 x 256 block of N tile j, one K step per ring stage (B slot)
+      auto load_block = [&](int j) -> bool {
+        for (int kc = 0; kc < kBlockKSteps; ++kc) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag)) {
+            record_timeout(p.status, abort_flag);
+            return false;
+          }
+          mbar_arrive_expect_tx(&full_bar[stage], S::B_BYTES);
+          uint8_t* b_dst = sB + stage * S::B_BYTES;
+          const int blk_row = j * BN;  // block j covers output columns j*256 ..
+          if (!B_MN) {
+            tma_load_2d(b_dst, &tmR, &full_bar[stage], kc * BK, blk_row);
+          } else {
+#pragma unroll
+            for (int c = 0; c < BN / 64; ++c)
+              tma_load_2d(b_dst + c * 8192, &tmR, &full_bar[stage], 64 * c, blk_row + kc * BK);
+          }
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        return true;
+      };
       for (int tile = range.first; tile < range.end && ok; tile += range.step) {
         int g, sp, mt, nt;
         decode_tile<B_RES>(tile, p, g, sp, mt, nt);
@@ -285,32 +311,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             phase ^= 1;
           }
         }
-        if (EPI == EPI_BLOCK) {
-          // the 256 x 256 block of this N tile, one K step per ring stage (B slot)
-          for (int kc = 0; kc < kBlockKSteps && ok; ++kc) {
-            if (!mbar_wait(&empty_bar[stage], phase ^ 1, abort_flag)) {
-              record_timeout(p.status, abort_flag);
-              ok = false;
-              break;
-            }
-            mbar_arrive_expect_tx(&full_bar[stage], S::B_BYTES);
-            uint8_t* b_dst = sB + stage * S::B_BYTES;
-            const int blk_row = nt * BN;  // block nt covers output columns nt*256 ..
-            if (!B_MN) {
-              tma_load_2d(b_dst, &tmR, &full_bar[stage], kc * BK, blk_row);
-            } else {
-#pragma unroll
-              for (int c = 0; c < BN / 64; ++c)
-                tma_load_2d(b_dst + c * 8192, &tmR, &full_bar[stage], 64 * c, blk_row + kc * BK);
-            }
-            ++issued;
-            if (++stage == STAGES) {
-              stage = 0;
-              phase ^= 1;
-            }
+        if (EPI == EPI_BLOCK && ok) {
+          // the previous tile's block goes after this tile's main loop: its
+          // MMA then waits for nothing the epilogue is still doing
+          if (prev_nt >= 0 && !load_block(prev_nt)) {
+            ok = false;
+            break;
           }
+          prev_nt = nt;
         }
       }
+      if (EPI == EPI_BLOCK && ok && prev_nt >= 0 && !load_block(prev_nt)) ok = false;
       if (!ok) {
         // Let the copies already issued land before the CTA exits.
         const int outstanding = issued < STAGES ? static_cast<int>(issued) : STAGES;
@@ -345,6 +356,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       bool any_mma = false;
       int res_key = -1, res_loads = 0;
       uint32_t vphase = 0;
+      bool have_prev = false;
+      // EPI_BLOCK: once the epilogue has staged a tile in bf16, multiply it by
+      // its block (from the ring) into accumulator d, then signal yfull
+      auto block_mma = [&](uint32_t d) -> bool {
+        if (!mbar_wait(vstaged_bar, vphase, abort_flag)) {
+          record_timeout(p.status, abort_flag);
+          return false;
+        }
+        vphase ^= 1;
+        tc_fence_after();
+        const uint32_t v_base = smem_u32(sOut);
+        for (int kc = 0; kc < kBlockKSteps; ++kc) {
+          if (!mbar_wait(&full_bar[stage], phase, abort_flag)) {
+            record_timeout(p.status, abort_flag);
+            return false;
+          }
+          tc_fence_after();
+          const uint32_t b_base = smem_u32(sB + stage * S::B_BYTES);
+#pragma unroll
+          for (int j = 0; j < BK / 16; ++j) {
+            const uint64_t adesc = smem_desc_sw128(v_base + kc * (BM * 128) + j * 32, 16, 1024);
+            const uint64_t bdesc = B_MN ? smem_desc_sw128(b_base + j * 2048, 8192, 1024)
+                                        : smem_desc_sw128(b_base + j * 32, 16, 1024);
+            umma_bf16(d, adesc, bdesc, IDESC, (kc > 0 || j > 0) ? 1u : 0u);
+          }
+          umma_commit(&empty_bar[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        umma_commit(yfull_bar);
+        return true;
+      };
       for (int tile = range.first; tile < range.end && ok; tile += range.step) {
         int g, sp, mt, nt;
         decode_tile<B_RES>(tile, p, g, sp, mt, nt);
@@ -399,43 +444,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!ok) break;
         umma_commit(&tfull_bar[acc]);  // accumulator ready for the epilogue
         if (EPI == EPI_BLOCK) {
-          // the epilogue has read the tile and staged it in bf16: the block
-          // product overwrites the same accumulator
-          if (!mbar_wait(vstaged_bar, vphase, abort_flag)) {
-            record_timeout(p.status, abort_flag);
+          // block product of the previous tile, into that tile's accumulator
+          if (have_prev && !block_mma(tmem_base + static_cast<uint32_t>((acc ^ 1) * BN))) {
             ok = false;
             break;
           }
-          vphase ^= 1;
-          tc_fence_after();
-          const uint32_t v_base = smem_u32(sOut);
-          for (int kc = 0; kc < kBlockKSteps; ++kc) {
-            if (!mbar_wait(&full_bar[stage], phase, abort_flag)) {
-              record_timeout(p.status, abort_flag);
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t b_base = smem_u32(sB + stage * S::B_BYTES);
-#pragma unroll
-            for (int j = 0; j < BK / 16; ++j) {
-              const uint64_t adesc = smem_desc_sw128(v_base + kc * (BM * 128) + j * 32, 16, 1024);
-              const uint64_t bdesc = B_MN ? smem_desc_sw128(b_base + j * 2048, 8192, 1024)
-                                          : smem_desc_sw128(b_base + j * 32, 16, 1024);
-              umma_bf16(d_tmem, adesc, bdesc, IDESC, (kc > 0 || j > 0) ? 1u : 0u);
-            }
-            umma_commit(&empty_bar[stage]);
-            if (++stage == STAGES) {
-              stage = 0;
-              phase ^= 1;
-            }
-          }
-          if (!ok) break;
-          umma_commit(yfull_bar);
+          have_prev = true;
         }
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1;
       }
+      if (EPI == EPI_BLOCK && ok && have_prev &&
+          !block_mma(tmem_base + static_cast<uint32_t>((acc ^ 1) * BN)))
+        ok = false;
       if (!ok && any_mma) {
         // Wait for the MMAs in flight before TMEM is released.
         umma_commit(drain_bar);
@@ -452,6 +473,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     uint32_t yphase = 0;
+    bool have_prev = false;  // EPI_BLOCK: a staged tile whose block product is pending
+    uint32_t t_prev = 0;
+    int prev_row = 0, prev_col0 = 0, prev_acc = 0;
+    // EPI_BLOCK: wait for the pending block product, stage it in bf16, free
+    // its accumulator and store it as the block output
+    auto drain_prev = [&](uint32_t t_src) -> bool {
+      const bool ygot = mbar_wait(yfull_bar, yphase, abort_flag);
+      yphase ^= 1;
+      if (!__all_sync(0xffffffffu, ygot)) {
+        record_timeout(p.status, abort_flag);
+        return false;
+      }
+      tc_fence_after();
+      if (lane == 0 && stores_pending) bulk_wait_read_all();
+      __syncwarp();
+      stage_rows_bf16(t_src, sOut, quarter * 32 + lane);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty_bar[prev_acc]);
+      fence_proxy_async_shared();
+      __syncwarp();
+      if (lane == 0) {
+        store_staged_rows(&tmY, sOut, quarter, prev_col0, prev_row);
+        stores_pending = true;
+      }
+      return true;
+    };
     for (int tile = range.first; tile < range.end; tile += range.step) {
       int g, sp, mt, nt;
       decode_tile<B_RES>(tile, p, g, sp, mt, nt);
@@ -466,11 +514,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (EPI == EPI_BLOCK) {
         const int out_row = g * p.epi.row_g + sp * p.epi.row_s + mt * BM + quarter * 32;
         const int out_col0 = g * p.epi.col_g + nt * BN;
-        const int row = quarter * 32 + lane;
-        // the staging rows are free once this warp's last stores have read them
+        // (1) the previous tile's block product: to bf16, free its accumulator, store
+        if (have_prev && !drain_prev(t_prev)) break;
+        // (2) this tile to bf16 in the staging tile, the A operand of its block
+        //     product (issued after the next tile's main loop)
         if (lane == 0 && stores_pending) bulk_wait_read_all();
         __syncwarp();
-        stage_rows_bf16(t_base, sOut, row);
+        stage_rows_bf16(t_base, sOut, quarter * 32 + lane);
         fence_proxy_async_shared();
         __syncwarp();
         if (lane == 0 && p.store_main) {
@@ -480,22 +530,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(vstaged_bar);
-        const bool ygot = mbar_wait(yfull_bar, yphase, abort_flag);
-        yphase ^= 1;
-        if (!__all_sync(0xffffffffu, ygot)) {
-          record_timeout(p.status, abort_flag);
-          break;
-        }
-        tc_fence_after();
-        if (lane == 0 && stores_pending) bulk_wait_read_all();
-        __syncwarp();
-        stage_rows_bf16(t_base, sOut, row);
-        fence_proxy_async_shared();
-        __syncwarp();
-        if (lane == 0) {
-          store_staged_rows(&tmY, sOut, quarter, out_col0, out_row);
-          stores_pending = true;
-        }
+        have_prev = true;
+        t_prev = t_base;
+        prev_row = out_row;
+        prev_col0 = out_col0;
+        prev_acc = acc;
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+        continue;  // this accumulator is freed by (1) of the next tile
       } else if (EPI == EPI_ROWS) {
         const int row = mt * BM + quarter * 32 + lane;
 #pragma unroll 1
@@ -549,6 +591,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
+    if (EPI == EPI_BLOCK && have_prev && !*abort_flag) drain_prev(t_prev);
     if (EPI != EPI_ROWS && lane == 0 && stores_pending) bulk_wait_all();
   }
 
