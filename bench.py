@@ -55,6 +55,9 @@ def parse():
     ap.add_argument("--w0-int8", action="store_true",
                     help="frozen weight held as INT8 codes with per-row scales, dequantised "
                          "into a bf16 buffer inside every step")
+    ap.add_argument("--fuse-epilogue", action="store_true",
+                    help="apply the block-diagonal factors in the W0 GEMMs' epilogues "
+                         "(y = R v, dx = du P) instead of separate block transforms")
     ap.add_argument("--recompute-v", action="store_true",
                     help="backward recomputes v = W0 P x instead of reading it (saves T x d_out)")
     return ap.parse_args()
@@ -73,6 +76,8 @@ def config_json(name, w, n, args=None):
         c["permuted_blocks"] = True
     if args is not None and getattr(args, "recompute_v", False):
         c["recompute_v"] = True
+    if args is not None and getattr(args, "fuse_epilogue", False):
+        c["block_epilogue"] = "fused into the W0 GEMMs"
     if args is not None and getattr(args, "w0_int8", False):
         c["w0"] = "int8, per-row scales, dequantised each step"
     if args is not None and getattr(args, "train_step", False):
@@ -330,6 +335,7 @@ def run_gpu(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     poetx.load_library()
+    poetx.poetx_set_block_epilogue_fusion(args.fuse_epilogue)
 
     name = args.workload
     w = workload_config(name)

@@ -232,6 +232,18 @@ poetx_status poetx_quantize_w0(const void* W0, int8_t* W0_q, float* scales, int 
 poetx_status poetx_dequantize_w0(const int8_t* W0_q, const float* scales, void* W0, int d_in,
                                  int d_out, poetx_dtype dtype, poetx_stream stream);
 
+/* The W0 GEMM fused with the block-diagonal factors (technical summary,
+ * section 2, input-centric bullet; the fusion itself is this library's):
+ * with fusion on, poetx_forward computes y = R v in the epilogue of the
+ * GEMM that produces v (v is stored only into a non-NULL v_saved), and
+ * poetx_backward computes dx = du P in the epilogue of the GEMM that
+ * produces du, for BF16 with b <= 256.  Results agree with the unfused path
+ * to bf16 rounding.  Off by default: on GB300 the fused GEMM's 64 KiB
+ * staging tile leaves room for a 3-stage operand ring only, and it runs
+ * slower than the plain GEMM plus the separate block transform.  Process-
+ * wide; returns the previous setting. */
+int poetx_set_block_epilogue_fusion(int enable);
+
 /* ------------------------------------------------------------------------
  * Status and measurement
  * ------------------------------------------------------------------------ */

@@ -21,6 +21,7 @@ __all__ = [
     "poetx_transform_workspace_size", "poetx_transform_forward", "poetx_transform_backward",
     "poetx_permute_features", "poetx_fold_permutations", "poetx_merge_workspace_size",
     "poetx_merge", "poetx_adam_update", "poetx_quantize_w0", "poetx_dequantize_w0",
+    "poetx_set_block_epilogue_fusion",
     "poetx_device_status", "poetx_selftest_wait_timeout", "poetx_launch_count", "poetx_profile_start", "poetx_profile_stop",
     "poetx_profile_query", "poetx_status_string", "EXPORTED_SYMBOLS",
 ]
@@ -69,6 +70,7 @@ _SIGNATURES = {
                                    ctypes.c_float, _c_ptr]),
     "poetx_quantize_w0": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_ptr]),
     "poetx_dequantize_w0": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_ptr]),
+    "poetx_set_block_epilogue_fusion": (_c_int, [_c_int]),
     "poetx_device_status": (_c_int, []),
     "poetx_selftest_wait_timeout": (_c_int, [ctypes.c_uint, _c_ptr]),
     "poetx_launch_count": (ctypes.c_longlong, []),
@@ -235,6 +237,12 @@ def poetx_quantize_w0(W0, W0_q, scales, d_in, d_out, dtype, stream=None):
 def poetx_dequantize_w0(W0_q, scales, W0, d_in, d_out, dtype, stream=None):
     _check("poetx_dequantize_w0", load_library().poetx_dequantize_w0(
         _ptr(W0_q), _ptr(scales), _ptr(W0), d_in, d_out, dtype, _stream(stream)))
+
+
+def poetx_set_block_epilogue_fusion(enable: bool) -> bool:
+    """Turn the W0 GEMM's block-diagonal epilogue on or off (process-wide);
+    returns the previous setting."""
+    return bool(load_library().poetx_set_block_epilogue_fusion(1 if enable else 0))
 
 
 def poetx_device_status() -> int:

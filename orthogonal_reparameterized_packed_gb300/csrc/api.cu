@@ -257,10 +257,14 @@ cudaError_t tc_w0(const bf16* A, const bf16* W0, bf16* out, int d_in, int d_out,
 // The W0 GEMMs with the block-diagonal factor applied in the epilogue (256 x
 // 256 superblocks): fwd v = u W0^T and y = v R^T per block; dgrad du = dv W0
 // and dx = du P per block.  `out` (v or du) may be null: then only the
-// block output is written.
-constexpr bool kFuseBlockEpilogue = true;
+// block output is written.  Off unless poetx_set_block_epilogue_fusion(1):
+// its 64 KiB staging tile leaves a 3-stage operand ring, and the GEMM then
+// loses more than the separate block transform costs.
+std::atomic<int> g_fuse_block_epilogue{0};
 
-bool fuse_block_epilogue(bool is_bf16, int b) { return kFuseBlockEpilogue && is_bf16 && b <= 256; }
+bool fuse_block_epilogue(bool is_bf16, int b) {
+  return g_fuse_block_epilogue.load(std::memory_order_relaxed) != 0 && is_bf16 && b <= 256;
+}
 
 cudaError_t tc_w0_block(const bf16* A, const bf16* W0, const bf16* sb, bf16* out, bf16* out_blk,
                         int d_in, int d_out, long long T, bool dgrad, cudaStream_t s) {
@@ -678,7 +682,7 @@ FwdPlan carve_forward(Carver& c, int d_in, int d_out, int b, long long T, bool i
                       bool need_v) {
   FwdPlan p;
   p.sb.u = take_act(c, T, d_in, is_bf16);
-  if (need_v && !fuse_block_epilogue(is_bf16, b)) p.sb.v = take_act(c, T, d_out, is_bf16);
+  if (need_v) p.sb.v = take_act(c, T, d_out, is_bf16);  // (unused by the fused forward)
   if (is_bf16 && b < 256) {
     p.sb.psb = c.take<bf16>(static_cast<size_t>(d_in) * 256);
     p.sb.rsb = c.take<bf16>(static_cast<size_t>(d_out) * 256);
@@ -1354,7 +1358,12 @@ poetx_status poetx_dequantize_w0(const int8_t* W0_q, const float* scales, void* 
                                      static_cast<cudaStream_t>(stream)));
 }
 
+int poetx_set_block_epilogue_fusion(int enable) {
+  return g_fuse_block_epilogue.exchange(enable != 0 ? 1 : 0);
+}
+
 }  // extern "C"
+
 
 
 
