@@ -713,6 +713,12 @@ struct BwdPlan {
   int splits_in = 1, splits_out = 1;
 };
 
+// The backward's transposed transforms and token sums run fused (one pass over
+// dy and one over du) on the chain path with 256 x 256 superblocks.
+bool use_transform_sum(bool is_bf16, int n, int b, int k) {
+  return use_chain(is_bf16, n, b, k) && b <= 256;
+}
+
 BwdPlan carve_backward(Carver& c, int d_in, int d_out, int b, int k, long long T, bool is_bf16,
                        bool recompute_v) {
   BwdPlan p;
@@ -728,8 +734,9 @@ BwdPlan carve_backward(Carver& c, int d_in, int d_out, int b, int k, long long T
       p.sb.psb = c.take<bf16>(static_cast<size_t>(d_in) * 256);
       p.sb.rsb = c.take<bf16>(static_cast<size_t>(d_out) * 256);
     }
-    p.splits_in = outer_splits(d_in, S, T);
-    p.splits_out = outer_splits(d_out, S, T);
+    const bool ts = use_transform_sum(is_bf16, (d_in + d_out) / b, b, k);
+    p.splits_in = ts ? transform_sum_splits(d_in, T) : outer_splits(d_in, S, T);
+    p.splits_out = ts ? transform_sum_splits(d_out, T) : outer_splits(d_out, S, T);
     const long long part_in = static_cast<long long>(p.splits_in) * d_in * S;
     const long long part_out = static_cast<long long>(p.splits_out) * d_out * S;
     if (use_chain(is_bf16, (d_in + d_out) / b, b, k)) {
@@ -985,6 +992,26 @@ poetx_status poetx_backward(const void* dy, const void* x, const void* W0, const
     v = p.sb.v;
   }
   const int S = superblock(b);
+  const bool chain = use_chain(is_bf16, (d_in + d_out) / b, b, k);
+  const long long off_R = static_cast<long long>(d_in) * b;  // R blocks follow the P blocks
+  if (use_transform_sum(is_bf16, (d_in + d_out) / b, b, k)) {
+    // dv = dy R with the G_R^T partials (sum_t v_t dy_t^T) in one pass over dy
+    e = tc_transform_sum(static_cast<const bf16*>(dy), static_cast<const bf16*>(v),
+                         static_cast<const bf16*>(rsb), static_cast<bf16*>(p.sb.dv), p.part_out,
+                         d_out, tokens, p.splits_out, s);
+    if (e != cudaSuccess) return POETX_ERR_CUDA;
+    e = tc_w0(static_cast<const bf16*>(p.sb.dv), static_cast<const bf16*>(W0),
+              static_cast<bf16*>(p.sb.du), d_in, d_out, tokens, true, s);
+    if (e != cudaSuccess) return POETX_ERR_CUDA;
+    // dx = du P with the G_P^T partials (sum_t x_t du_t^T) in one pass over du
+    e = tc_transform_sum(static_cast<const bf16*>(p.sb.du), static_cast<const bf16*>(x),
+                         static_cast<const bf16*>(psb), static_cast<bf16*>(dx), p.sb.part, d_in,
+                         tokens, p.splits_in, s);
+    if (e != cudaSuccess) return POETX_ERR_CUDA;
+    return to_status(chain_adjoint_from_parts(theta_P, d_in / b, p.sb.part, p.splits_in,
+                                              theta_R, d_out / b, p.part_out, p.splits_out, b, k,
+                                              p.cnp, dtheta_P, dtheta_R, s));
+  }
   // R side: dv = dy R, G_R = sum_t dy_t v_t^T
   if (is_bf16)
     e = tc_transform(static_cast<const bf16*>(dy), static_cast<const bf16*>(rsb),
@@ -993,8 +1020,6 @@ poetx_status poetx_backward(const void* dy, const void* x, const void* W0, const
     e = simt_transform(static_cast<const float*>(dy), static_cast<const float*>(rsb),
                        static_cast<float*>(p.sb.dv), d_out, b, tokens, true, "transform_t", s);
   if (e != cudaSuccess) return POETX_ERR_CUDA;
-  const bool chain = use_chain(is_bf16, (d_in + d_out) / b, b, k);
-  const long long off_R = static_cast<long long>(d_in) * b;  // R blocks follow the P blocks
   if (chain)  // G_R^T partials: sum_t v_t dy_t^T per block
     e = tc_outer(static_cast<const bf16*>(v), static_cast<const bf16*>(dy), p.part_out, d_out,
                  S, tokens, p.splits_out, s);

@@ -1,0 +1,399 @@
+// The backward's two passes over one activation gradient fused into one
+// kernel (sm_103a, tcgen05 + TMA): for a gradient X [T][d], another
+// activation Z [T][d] and the 256 x 256 superblocks SB of one side,
+//
+//   out[t][g*256 + n]  = sum_kk X[t][g*256 + kk] SB[g*256 + kk][n]     (bf16)
+//   part[s][g][m][n]   = sum_{t in split s} Z[t][g*256 + m] X[t][g*256 + n]  (fp32)
+//
+// i.e. the transposed block transform (dv = dy R, dx = du P) and the
+// split-K token sums G^T of the block gradients (sum_t v_t dy_t^T,
+// sum_t x_t du_t^T).  Separately they read X twice from HBM; here every X
+// tile that lands in shared memory feeds both products.
+//
+// One CTA per (block g, half h, token split s):
+//   transform half: out columns g*256 + h*128 .. +127, all 256 K features;
+//                   SB's 256 x 128 half stays resident in shared memory
+//   sum half:       rows m = h*128 .. +127 of part[s][g], all 256 columns
+// Both halves of a block read the same X tiles at about the same time, so
+// the second read is served by L2.  TMEM: two 128-column accumulators for
+// the transform tiles (the epilogue of one overlaps the next) and one
+// 256-column accumulator for the sum, 512 columns in all.
+//
+// Warp roles: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 2-5
+// epilogue.  Every wait is bounded; on expiry the CTA records
+// POETX_ERR_TIMEOUT, lets its copies and MMAs in flight land and returns.
+#include <algorithm>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "tc_common.cuh"
+
+namespace poetx {
+
+namespace {
+
+constexpr int TS_THREADS = 192;
+constexpr int TS_XSTAGES = 4;                  // X ring: one 128 x 64 chunk per stage
+constexpr int TS_ZSTAGES = 2;                  // Z ring: one 128 x 128 half tile per stage
+constexpr int TS_RES_BYTES = 256 * 128 * 2;    // SB half, 64 KiB
+constexpr int TS_X_BYTES = BM * 64 * 2;        // 16 KiB
+constexpr int TS_Z_BYTES = BM * 128 * 2;       // 32 KiB
+constexpr int TS_OUT_BYTES = 4 * 4096;         // per epilogue warp 32 rows x 128 B
+constexpr int TS_BAR_BYTES = 256;
+constexpr int TS_SMEM = 1024 + TS_RES_BYTES + TS_XSTAGES * TS_X_BYTES + TS_ZSTAGES * TS_Z_BYTES +
+                        TS_OUT_BYTES + TS_BAR_BYTES;
+constexpr uint32_t TS_TMEM_COLS = 512;
+static_assert(TS_SMEM <= 227 * 1024, "shared memory per CTA");
+
+struct TsArgs {
+  int d;            // features (multiple of 256)
+  int m_tiles;      // token tiles of 128
+  int splits;       // token splits
+  int per;          // token tiles per split
+  int* status;
+};
+
+__global__ void __launch_bounds__(TS_THREADS, 1)
+    transform_sum_kernel(const __grid_constant__ CUtensorMap tmX,   // X [T][d], box 64 x 128
+                         const __grid_constant__ CUtensorMap tmZ,   // Z [T][d], box 64 x 128
+                         const __grid_constant__ CUtensorMap tmB,   // SB [d][256], box 64 x 64
+                         const __grid_constant__ CUtensorMap tmO,   // out [T][d] bf16, box 64 x 32
+                         const __grid_constant__ CUtensorMap tmP,   // part [splits*d][256] f32, box 32 x 32
+                         const TsArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sRes = base;
+  uint8_t* sX = sRes + TS_RES_BYTES;
+  uint8_t* sZ = sX + TS_XSTAGES * TS_X_BYTES;
+  uint8_t* sOut = sZ + TS_ZSTAGES * TS_Z_BYTES;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(sOut + TS_OUT_BYTES);
+  uint64_t* empty_bar = full_bar + TS_XSTAGES;
+  uint64_t* zfull_bar = empty_bar + TS_XSTAGES;
+  uint64_t* zempty_bar = zfull_bar + TS_ZSTAGES;
+  uint64_t* tfull_bar = zempty_bar + TS_ZSTAGES;  // [2]
+  uint64_t* tempty_bar = tfull_bar + 2;           // [2]
+  uint64_t* bfull_bar = tempty_bar + 2;
+  uint64_t* gfull_bar = bfull_bar + 1;
+  uint64_t* drain_bar = gfull_bar + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  // work unit: token split fastest, then the half, then the block
+  const int s = blockIdx.x % p.splits;
+  const int h = (blockIdx.x / p.splits) & 1;
+  const int g = blockIdx.x / (2 * p.splits);
+  const int t_first = s * p.per;
+  const int t_end = min(t_first + p.per, p.m_tiles);
+  const int col_blk = g * 256;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < TS_XSTAGES; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], 1);
+    }
+    for (int i = 0; i < TS_ZSTAGES; ++i) {
+      mbar_init(&zfull_bar[i], 1);
+      mbar_init(&zempty_bar[i], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull_bar[a], 1);
+      mbar_init(&tempty_bar[a], 4);
+    }
+    mbar_init(bfull_bar, 1);
+    mbar_init(gfull_bar, 1);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(&tmZ);
+    tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmO);
+    tma_prefetch_desc(&tmP);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TS_TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();
+  pdl_trigger();
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------ TMA producer
+      bool ok = true;
+      int xs = 0, zs = 0;
+      uint32_t xphase = 0, zphase = 0;
+      long long x_issued = 0, z_issued = 0;
+      // SB's half: K rows g*256 .. +255, columns h*128 .. +127 (MN-major B)
+      mbar_arrive_expect_tx(bfull_bar, TS_RES_BYTES);
+      for (int kc = 0; kc < 4; ++kc)
+        for (int c2 = 0; c2 < 2; ++c2)
+          tma_load_2d(sRes + kc * 16384 + c2 * 8192, &tmB, bfull_bar, h * 128 + 64 * c2,
+                      col_blk + kc * 64);
+      for (int t = t_first; t < t_end && ok; ++t) {
+        if (!mbar_wait(&zempty_bar[zs], zphase ^ 1, abort_flag)) {
+          record_timeout(p.status, abort_flag);
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&zfull_bar[zs], TS_Z_BYTES);
+        uint8_t* z_dst = sZ + zs * TS_Z_BYTES;
+        tma_load_2d(z_dst, &tmZ, &zfull_bar[zs], col_blk + h * 128, t * BM);
+        tma_load_2d(z_dst + 16384, &tmZ, &zfull_bar[zs], col_blk + h * 128 + 64, t * BM);
+        ++z_issued;
+        if (++zs == TS_ZSTAGES) {
+          zs = 0;
+          zphase ^= 1;
+        }
+        for (int c = 0; c < 4; ++c) {
+          if (!mbar_wait(&empty_bar[xs], xphase ^ 1, abort_flag)) {
+            record_timeout(p.status, abort_flag);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full_bar[xs], TS_X_BYTES);
+          tma_load_2d(sX + xs * TS_X_BYTES, &tmX, &full_bar[xs], col_blk + 64 * c, t * BM);
+          ++x_issued;
+          if (++xs == TS_XSTAGES) {
+            xs = 0;
+            xphase ^= 1;
+          }
+        }
+      }
+      if (!ok) {  // let the copies in flight land before the CTA exits
+        auto settle = [](uint64_t* bars, int nst, int st, uint32_t ph, long long issued) {
+          const int outstanding = issued < nst ? static_cast<int>(issued) : nst;
+          for (int i = 0; i < outstanding; ++i) {
+            if (--st < 0) {
+              st = nst - 1;
+              ph ^= 1;
+            }
+            const unsigned long long t0 = global_timer_ns();
+            while (!mbar_try_wait(&bars[st], ph) && global_timer_ns() - t0 < 10000000ull) {
+            }
+          }
+        };
+        settle(full_bar, TS_XSTAGES, xs, xphase, x_issued);
+        settle(zfull_bar, TS_ZSTAGES, zs, zphase, z_issued);
+        const unsigned long long t0 = global_timer_ns();
+        while (!mbar_try_wait(bfull_bar, 0) && global_timer_ns() - t0 < 10000000ull) {
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------- MMA issuer
+      constexpr uint32_t IDESC_T = instr_desc_bf16(BM, 128, false, true);  // X K-major, SB MN-major
+      constexpr uint32_t IDESC_S = instr_desc_bf16(BM, 64, true, true);    // Z, X both MN-major
+      const uint32_t g_tmem = tmem_base + 256u;
+      bool ok = mbar_wait(bfull_bar, 0, abort_flag);
+      if (!ok) record_timeout(p.status, abort_flag);
+      tc_fence_after();
+      bool any_mma = false;
+      int xs = 0, zs = 0, acc = 0;
+      uint32_t xphase = 0, zphase = 0, acc_phase = 0;
+      const uint32_t res_base = smem_u32(sRes);
+      for (int t = t_first; t < t_end && ok; ++t) {
+        if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1, abort_flag) ||
+            !mbar_wait(&zfull_bar[zs], zphase, abort_flag)) {
+          record_timeout(p.status, abort_flag);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t t_tmem = tmem_base + static_cast<uint32_t>(acc * 128);
+        const uint32_t z_base = smem_u32(sZ + zs * TS_Z_BYTES);
+        for (int c = 0; c < 4; ++c) {
+          if (!mbar_wait(&full_bar[xs], xphase, abort_flag)) {
+            record_timeout(p.status, abort_flag);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t x_base = smem_u32(sX + xs * TS_X_BYTES);
+          // transform: out tile += X chunk c (K = features 64c ..) x SB rows 64c ..
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            umma_bf16(t_tmem, smem_desc_sw128(x_base + j * 32, 16, 1024),
+                      smem_desc_sw128(res_base + c * 16384 + j * 2048, 8192, 1024), IDESC_T,
+                      (c > 0 || j > 0) ? 1u : 0u);
+          // token sum: G[m][64c ..] += sum over the tile's tokens of Z[t][m] X[t][64c ..]
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            umma_bf16(g_tmem + static_cast<uint32_t>(64 * c),
+                      smem_desc_sw128(z_base + j * 2048, 16384, 1024),
+                      smem_desc_sw128(x_base + j * 2048, 16384, 1024), IDESC_S,
+                      (t > t_first || j > 0) ? 1u : 0u);
+          any_mma = true;
+          umma_commit(&empty_bar[xs]);
+          if (++xs == TS_XSTAGES) {
+            xs = 0;
+            xphase ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull_bar[acc]);
+        umma_commit(&zempty_bar[zs]);
+        if (++zs == TS_ZSTAGES) {
+          zs = 0;
+          zphase ^= 1;
+        }
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      if (ok) {
+        umma_commit(gfull_bar);  // the split's sum is complete
+      } else if (any_mma) {
+        umma_commit(drain_bar);
+        const unsigned long long t0 = global_timer_ns();
+        while (!mbar_try_wait(drain_bar, 0) && global_timer_ns() - t0 < 10000000ull) {
+        }
+      }
+    }
+  } else {
+    // ----------------------------------------------------------- epilogue
+    const int quarter = warp & 3;
+    uint8_t* stg = sOut + quarter * 4096;
+    uint8_t* my_row = stg + lane * 128;
+    bool stores_pending = false, ok = true;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = t_first; t < t_end; ++t) {
+      const bool got = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag);
+      if (!__all_sync(0xffffffffu, got)) {
+        record_timeout(p.status, abort_flag);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t t_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                              static_cast<uint32_t>(acc * 128);
+#pragma unroll 1
+      for (int c0 = 0; c0 < 128; c0 += 64) {
+        uint32_t r0[32], r1[32], w[32];
+        tmem_load_32cols(t_base + c0, r0);
+        tmem_load_32cols(t_base + c0 + 32, r1);
+        tmem_load_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          w[j] = pack_bf16x2(r0[2 * j], r0[2 * j + 1]);
+          w[16 + j] = pack_bf16x2(r1[2 * j], r1[2 * j + 1]);
+        }
+        if (lane == 0 && stores_pending) bulk_wait_read_all();
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          st_shared_v4(my_row + ((q ^ (lane & 7)) << 4), w[4 * q], w[4 * q + 1], w[4 * q + 2],
+                       w[4 * q + 3]);
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmO, stg, col_blk + h * 128 + c0, t * BM + quarter * 32);
+          bulk_commit();
+          stores_pending = true;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty_bar[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+    if (ok && t_end > t_first) {
+      // the split's partial sum: rows h*128 + quarter*32 .. of part[s][g], fp32
+      const bool got = mbar_wait(gfull_bar, 0, abort_flag);
+      if (!__all_sync(0xffffffffu, got)) {
+        record_timeout(p.status, abort_flag);
+      } else {
+        tc_fence_after();
+        const uint32_t g_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + 256u;
+        const int prow = s * p.d + col_blk + h * 128 + quarter * 32;
+#pragma unroll 1
+        for (int c0 = 0; c0 < 256; c0 += 32) {
+          uint32_t w[32];
+          tmem_load_32cols(g_base + c0, w);
+          tmem_load_wait();
+          if (lane == 0 && stores_pending) bulk_wait_read_all();
+          __syncwarp();
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            st_shared_v4(my_row + ((q ^ (lane & 7)) << 4), w[4 * q], w[4 * q + 1], w[4 * q + 2],
+                         w[4 * q + 3]);
+          fence_proxy_async_shared();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&tmP, stg, c0, prow);
+            bulk_commit();
+            stores_pending = true;
+          }
+        }
+      }
+    }
+    if (lane == 0 && stores_pending) bulk_wait_all();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TS_TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+int transform_sum_splits(int d, long long T) {
+  const int m_tiles = static_cast<int>((T + BM - 1) / BM);
+  const int units = 2 * (d / 256);
+  int splits = sm_count() / (units > 0 ? units : 1);
+  if (splits < 1) splits = 1;
+  if (splits > m_tiles) splits = m_tiles;
+  if (splits < 1) splits = 1;
+  const int per = (m_tiles + splits - 1) / splits;
+  return (m_tiles + per - 1) / per;  // no empty split
+}
+
+cudaError_t tc_transform_sum(const __nv_bfloat16* X, const __nv_bfloat16* Z,
+                             const __nv_bfloat16* sb, __nv_bfloat16* out, float* part, int d,
+                             long long T, int splits, cudaStream_t stream) {
+  if (T <= 0) return cudaSuccess;
+  if (d <= 0 || d % 256 != 0 || splits != transform_sum_splits(d, T)) return cudaErrorInvalidValue;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(transform_sum_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, TS_SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  CUtensorMap tmX, tmZ, tmB, tmO, tmP;
+  if (!make_map(&tmX, X, T, d, d, 2, 64, BM) || !make_map(&tmZ, Z, T, d, d, 2, 64, BM) ||
+      !make_map(&tmB, sb, d, 256, 256, 2, 64, 64) || !make_map(&tmO, out, T, d, d, 2, 64, 32) ||
+      !make_map(&tmP, part, static_cast<long long>(splits) * d, 256, 256, 4, 32, 32))
+    return cudaErrorInvalidValue;
+  TsArgs a;
+  a.d = d;
+  a.m_tiles = static_cast<int>((T + BM - 1) / BM);
+  a.splits = splits;
+  a.per = (a.m_tiles + splits - 1) / splits;
+  a.status = device_status_ptr();
+  const int grid = 2 * (d / 256) * splits;
+  prof_begin("transform_sum", stream);
+  cudaError_t e = launch_pdl(transform_sum_kernel, dim3(grid), dim3(TS_THREADS), TS_SMEM, stream,
+                             tmX, tmZ, tmB, tmO, tmP, a);
+  prof_end("transform_sum", stream);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+}  // namespace poetx
