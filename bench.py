@@ -254,9 +254,14 @@ def load_peaks():
         "fallback"
 
 
-# the files the tcgen05 GEMM kernels are compiled from: their DRAM counters
-# stay valid while these are unchanged
+# the files each kernel is compiled from: its DRAM counters stay valid while
+# these are unchanged
 GEMM_SOURCES = ("gemm_tc.cu", "tc_common.cuh", "ptx.cuh", "internal.h")
+KERNEL_SOURCES = {
+    "gemm_w0": GEMM_SOURCES, "gemm_w0_dgrad": GEMM_SOURCES, "transform": GEMM_SOURCES,
+    "transform_t": GEMM_SOURCES, "outer": GEMM_SOURCES,
+    "transform_sum": ("transform_sum_tc.cu", "tc_common.cuh", "ptx.cuh", "internal.h"),
+}
 
 
 def source_hash(files=GEMM_SOURCES):
@@ -271,14 +276,14 @@ def source_hash(files=GEMM_SOURCES):
 
 def captured_traffic(workload, tag):
     """DRAM bytes per launch from the committed ncu summary, or None when the
-    summary is for other sources or another workload."""
+    summary is for other sources (of that kernel) or another workload."""
     p = os.path.join(ROOT, "profiles", f"traffic_{workload}.json")
-    if not os.path.exists(p):
+    if not os.path.exists(p) or tag not in KERNEL_SOURCES:
         return None
     with open(p) as f:
         d = json.load(f)
     k = d.get("kernels", {}).get(tag)
-    if k is None or d.get("source_hash") != source_hash():
+    if k is None or k.get("source_hash") != source_hash(KERNEL_SOURCES[tag]):
         return None
     return k["dram_read"] + k["dram_write"]
 
@@ -455,6 +460,7 @@ def run_gpu(args):
     tags = ["build", "unpack", "identity_plus", "expand_superblocks", "transform",
             "transform_t", "gemm_w0", "gemm_w0_dgrad", "gemm_w0_r", "gemm_w0_dgrad_p", "outer", "reduce_extract", "cnp_bwd",
             "pack_skew", "f32_to_bf16", "chain", "prep_tiles", "pack_tiles", "permute", "adam",
+            "transform_sum",
             "dequantize", "quantize"]
     kernels = {}
     for t in tags:
@@ -475,21 +481,31 @@ def run_gpu(args):
                 "per_launch": f"{formula} = {amount:.4f} TFLOP",
                 "timing": "CUDA events around each launch, eager pass of the same K steps"}
 
-    if "permute" in kernels:  # index-map kernel: HBM-bound, reads and writes T x d
-        pk = kernels["permute"]
-        dsum = w["d_in"] + w["d_out"]  # per step: 2 maps over d_in, 2 over d_out
-        moved = 2.0 * w["tokens"] * dsum * 2 * 2  # read + write, bf16, 4 launches
-        gbs = moved / (pk["total_ms"] / args.steps * 1e-3) / 1e9
-        roofline["secondary"] = {"kernel": "permute", "bound": "hbm", "achieved": gbs,
-                                 "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                 "frac": gbs / peaks["hbm_gbs"]}
-
-    if "dequantize" in kernels:  # INT8 -> bf16 weight, HBM-bound: 1 + 2 bytes per entry
-        dk = kernels["dequantize"]
-        gbs = 3.0 * w["d_in"] * w["d_out"] / (dk["avg_us"] * 1e-6) / 1e9
-        roofline["secondary"] = {"kernel": "dequantize", "bound": "hbm", "achieved": gbs,
-                                 "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                 "frac": gbs / peaks["hbm_gbs"]}
+    # the HBM-bound kernels: algorithmic bytes of all their launches in the
+    # timed steps / their summed event time
+    T, di, do = w["tokens"], w["d_in"], w["d_out"]
+    S = max(w["b"], 256)
+    hbm_bytes = {
+        # u = P x and y = R v: read + write bf16 activations, the superblocks
+        "transform": 4.0 * T * (di + do) + 2.0 * S * (di + do),
+        "transform_t": 4.0 * T * (di + do) + 2.0 * S * (di + do),
+        # dv = dy R with sum_t v dy^T, dx = du P with sum_t x du^T: two reads, one write
+        "transform_sum": 6.0 * T * (di + do) + 2.0 * S * (di + do),
+        "outer": 4.0 * T * (di + do),
+        # index maps: 2 over d_in, 2 over d_out, each reads and writes T x d bf16
+        "permute": 8.0 * T * (di + do),
+        # INT8 -> bf16 weight: 1 + 2 bytes per entry
+        "dequantize": 3.0 * di * do,
+    }
+    hbm = []
+    for tag, per_step in hbm_bytes.items():
+        if tag in kernels:
+            kt = kernels[tag]
+            gbs = per_step * args.steps / (kt["total_ms"] * 1e-3) / 1e9
+            hbm.append({"kernel": tag, "bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                        "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                        "bytes_per_step": per_step, "traffic": captured_traffic(name, tag)})
+    roofline["hbm_kernels"] = hbm
 
     merge = None
     if args.train_step and not args.permute and not args.w0_int8:

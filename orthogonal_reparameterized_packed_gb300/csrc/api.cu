@@ -1074,7 +1074,9 @@ size_t poetx_transform_workspace_size(int d, int b, int k, int64_t tokens, poetx
   if (is_bf16 && b < 256) c.take<bf16>(static_cast<size_t>(d) * 256);
   if (is_bf16) {
     const int S = superblock(b);
-    c.take<float>(static_cast<size_t>(outer_splits(d, S, tokens)) * d * S);
+    const int splits = use_transform_sum(is_bf16, d / b, b, k) ? transform_sum_splits(d, tokens)
+                                                               : outer_splits(d, S, tokens);
+    c.take<float>(static_cast<size_t>(splits) * d * S);
   }
   carve_cnp(c, d / b, b, k, tc_small(is_bf16, b));
   return c.off;
@@ -1126,7 +1128,9 @@ poetx_status poetx_transform_backward(const void* dout, const void* x, const flo
   Carver c(workspace);
   bf16* sbuf = (is_bf16 && b < 256) ? c.take<bf16>(static_cast<size_t>(d) * 256) : nullptr;
   const int S = superblock(b);
-  const int splits = is_bf16 ? outer_splits(d, S, tokens) : 1;
+  const bool ts = use_transform_sum(is_bf16, d / b, b, k);
+  const int splits =
+      !is_bf16 ? 1 : (ts ? transform_sum_splits(d, tokens) : outer_splits(d, S, tokens));
   float* part = is_bf16 ? c.take<float>(static_cast<size_t>(splits) * d * S) : nullptr;
   CnpBufs cnp = carve_cnp(c, d / b, b, k, tc_small(is_bf16, b));
   if (workspace == nullptr || c.off > workspace_bytes || !aligned16(workspace))
@@ -1134,6 +1138,14 @@ poetx_status poetx_transform_backward(const void* dout, const void* x, const flo
   cudaError_t e;
   const void* sb = superblocks_or_blocks(blocks, sbuf, d, b, is_bf16, s, &e);
   if (e != cudaSuccess) return POETX_ERR_CUDA;
+  if (ts) {  // dx = dout B with the G^T partials (sum_t x_t dout_t^T) in one pass
+    e = tc_transform_sum(static_cast<const bf16*>(dout), static_cast<const bf16*>(x),
+                         static_cast<const bf16*>(sb), static_cast<bf16*>(dx), part, d, tokens,
+                         splits, s);
+    if (e != cudaSuccess) return POETX_ERR_CUDA;
+    return to_status(chain_adjoint_from_parts(theta, d / b, part, splits, nullptr, 0, nullptr, 1,
+                                              b, k, cnp, dtheta, nullptr, s));
+  }
   if (is_bf16)
     e = tc_transform(static_cast<const bf16*>(dout), static_cast<const bf16*>(sb),
                      static_cast<bf16*>(dx), d, S, tokens, true, "transform_t", s);
