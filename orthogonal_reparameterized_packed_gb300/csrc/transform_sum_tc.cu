@@ -34,6 +34,7 @@ namespace {
 
 constexpr int TS_THREADS = 192;
 constexpr int TS_XSTAGES = 4;                  // X ring: one 128 x 64 chunk per stage
+static_assert(TS_XSTAGES == 4, "a tile's four chunks must sit in slots 0..3");
 constexpr int TS_ZSTAGES = 2;                  // Z ring: one 128 x 128 half tile per stage
 constexpr int TS_RES_BYTES = 256 * 128 * 2;    // SB half, 64 KiB
 constexpr int TS_X_BYTES = BM * 64 * 2;        // 16 KiB
@@ -193,7 +194,7 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
     if (lane == 0) {
       // ------------------------------------------------------- MMA issuer
       constexpr uint32_t IDESC_T = instr_desc_bf16(BM, 128, false, true);  // X K-major, SB MN-major
-      constexpr uint32_t IDESC_S = instr_desc_bf16(BM, 64, true, true);    // Z, X both MN-major
+      constexpr uint32_t IDESC_S = instr_desc_bf16(BM, 128, true, true);   // Z, X both MN-major
       const uint32_t g_tmem = tmem_base + 256u;
       bool ok = mbar_wait(bfull_bar, 0, abort_flag);
       if (!ok) record_timeout(p.status, abort_flag);
@@ -226,15 +227,20 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
             umma_bf16(t_tmem, smem_desc_sw128(x_base + j * 32, 16, 1024),
                       smem_desc_sw128(res_base + c * 16384 + j * 2048, 8192, 1024), IDESC_T,
                       (c > 0 || j > 0) ? 1u : 0u);
-          // token sum: G[m][64c ..] += sum over the tile's tokens of Z[t][m] X[t][64c ..]
+          if (c & 1) {
+            // token sum over chunks c-1, c (adjacent ring slots: a tile's chunk
+            // i always sits in slot i): G[m][64(c-1) ..] += sum_t Z[t][m] X[t][..]
+            const uint32_t x_pair = x_base - TS_X_BYTES;
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            umma_bf16(g_tmem + static_cast<uint32_t>(64 * c),
-                      smem_desc_sw128(z_base + j * 2048, 16384, 1024),
-                      smem_desc_sw128(x_base + j * 2048, 16384, 1024), IDESC_S,
-                      (t > t_first || j > 0) ? 1u : 0u);
+            for (int j = 0; j < 8; ++j)
+              umma_bf16(g_tmem + static_cast<uint32_t>(64 * (c - 1)),
+                        smem_desc_sw128(z_base + j * 2048, 16384, 1024),
+                        smem_desc_sw128(x_pair + j * 2048, TS_X_BYTES, 1024), IDESC_S,
+                        (t > t_first || j > 0) ? 1u : 0u);
+            umma_commit(&empty_bar[xs - 1]);
+            umma_commit(&empty_bar[xs]);
+          }
           any_mma = true;
-          umma_commit(&empty_bar[xs]);
           if (++xs == TS_XSTAGES) {
             xs = 0;
             xphase ^= 1;
