@@ -20,7 +20,8 @@
 // 256-column accumulator for the sum, 512 columns in all.
 //
 // Warp roles: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 2-5
-// epilogue.  Every wait is bounded; on expiry the CTA records
+// epilogue (row-per-thread 16-byte stores: the shared memory a TMA-store
+// staging tile would take holds two more gradient chunks in flight).  Every wait is bounded; on expiry the CTA records
 // POETX_ERR_TIMEOUT, lets its copies and MMAs in flight land and returns.
 #include <algorithm>
 
@@ -33,16 +34,17 @@ namespace poetx {
 namespace {
 
 constexpr int TS_THREADS = 192;
-constexpr int TS_XSTAGES = 4;                  // X ring: one 128 x 64 chunk per stage
-static_assert(TS_XSTAGES == 4, "a tile's four chunks must sit in slots 0..3");
+constexpr int TS_XSTAGES = 6;                  // X ring: one 128 x 64 chunk per stage
+// a tile's chunk pairs (0,1), (2,3) sit in adjacent slots (2i, 2i+1): tiles
+// start on even slots when the ring length is even
+static_assert(TS_XSTAGES % 2 == 0, "even ring length");
 constexpr int TS_ZSTAGES = 2;                  // Z ring: one 128 x 128 half tile per stage
 constexpr int TS_RES_BYTES = 256 * 128 * 2;    // SB half, 64 KiB
 constexpr int TS_X_BYTES = BM * 64 * 2;        // 16 KiB
 constexpr int TS_Z_BYTES = BM * 128 * 2;       // 32 KiB
-constexpr int TS_OUT_BYTES = 4 * 4096;         // per epilogue warp 32 rows x 128 B
 constexpr int TS_BAR_BYTES = 256;
-constexpr int TS_SMEM = 1024 + TS_RES_BYTES + TS_XSTAGES * TS_X_BYTES + TS_ZSTAGES * TS_Z_BYTES +
-                        TS_OUT_BYTES + TS_BAR_BYTES;
+constexpr int TS_SMEM =
+    1024 + TS_RES_BYTES + TS_XSTAGES * TS_X_BYTES + TS_ZSTAGES * TS_Z_BYTES + TS_BAR_BYTES;
 constexpr uint32_t TS_TMEM_COLS = 512;
 static_assert(TS_SMEM <= 227 * 1024, "shared memory per CTA");
 
@@ -51,6 +53,9 @@ struct TsArgs {
   int m_tiles;      // token tiles of 128
   int splits;       // token splits
   int per;          // token tiles per split
+  long long T;      // tokens
+  __nv_bfloat16* out;  // [T][d]
+  float* part;         // [splits][d][256]
   int* status;
 };
 
@@ -58,8 +63,6 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
     transform_sum_kernel(const __grid_constant__ CUtensorMap tmX,   // X [T][d], box 64 x 128
                          const __grid_constant__ CUtensorMap tmZ,   // Z [T][d], box 64 x 128
                          const __grid_constant__ CUtensorMap tmB,   // SB [d][256], box 64 x 64
-                         const __grid_constant__ CUtensorMap tmO,   // out [T][d] bf16, box 64 x 32
-                         const __grid_constant__ CUtensorMap tmP,   // part [splits*d][256] f32, box 32 x 32
                          const TsArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
@@ -67,8 +70,7 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
   uint8_t* sRes = base;
   uint8_t* sX = sRes + TS_RES_BYTES;
   uint8_t* sZ = sX + TS_XSTAGES * TS_X_BYTES;
-  uint8_t* sOut = sZ + TS_ZSTAGES * TS_Z_BYTES;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(sOut + TS_OUT_BYTES);
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(sZ + TS_ZSTAGES * TS_Z_BYTES);
   uint64_t* empty_bar = full_bar + TS_XSTAGES;
   uint64_t* zfull_bar = empty_bar + TS_XSTAGES;
   uint64_t* zempty_bar = zfull_bar + TS_ZSTAGES;
@@ -113,8 +115,6 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
     tma_prefetch_desc(&tmX);
     tma_prefetch_desc(&tmZ);
     tma_prefetch_desc(&tmB);
-    tma_prefetch_desc(&tmO);
-    tma_prefetch_desc(&tmP);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, TS_TMEM_COLS);
@@ -267,10 +267,11 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
     }
   } else {
     // ----------------------------------------------------------- epilogue
+    // Each thread owns one accumulator row and stores it with 16-byte stores
+    // (the transform tile's 128 bf16 columns, then the sum's 256 fp32).
     const int quarter = warp & 3;
-    uint8_t* stg = sOut + quarter * 4096;
-    uint8_t* my_row = stg + lane * 128;
-    bool stores_pending = false, ok = true;
+    const int row_in_tile = quarter * 32 + lane;
+    bool ok = true;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = t_first; t < t_end; ++t) {
@@ -283,29 +284,20 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
       tc_fence_after();
       const uint32_t t_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                               static_cast<uint32_t>(acc * 128);
+      const long long row = static_cast<long long>(t) * BM + row_in_tile;
+      uint4* dst = reinterpret_cast<uint4*>(p.out + row * p.d + col_blk + h * 128);
 #pragma unroll 1
-      for (int c0 = 0; c0 < 128; c0 += 64) {
-        uint32_t r0[32], r1[32], w[32];
-        tmem_load_32cols(t_base + c0, r0);
-        tmem_load_32cols(t_base + c0 + 32, r1);
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        uint32_t r[32];
+        tmem_load_32cols(t_base + c0, r);
         tmem_load_wait();
+        if (row < p.T) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          w[j] = pack_bf16x2(r0[2 * j], r0[2 * j + 1]);
-          w[16 + j] = pack_bf16x2(r1[2 * j], r1[2 * j + 1]);
-        }
-        if (lane == 0 && stores_pending) bulk_wait_read_all();
-        __syncwarp();
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          st_shared_v4(my_row + ((q ^ (lane & 7)) << 4), w[4 * q], w[4 * q + 1], w[4 * q + 2],
-                       w[4 * q + 3]);
-        fence_proxy_async_shared();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_2d(&tmO, stg, col_blk + h * 128 + c0, t * BM + quarter * 32);
-          bulk_commit();
-          stores_pending = true;
+          for (int q = 0; q < 4; ++q)
+            dst[c0 / 8 + q] = make_uint4(pack_bf16x2(r[8 * q], r[8 * q + 1]),
+                                         pack_bf16x2(r[8 * q + 2], r[8 * q + 3]),
+                                         pack_bf16x2(r[8 * q + 4], r[8 * q + 5]),
+                                         pack_bf16x2(r[8 * q + 6], r[8 * q + 7]));
         }
       }
       tc_fence_before();
@@ -315,36 +307,26 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
       if (acc == 0) acc_phase ^= 1;
     }
     if (ok && t_end > t_first) {
-      // the split's partial sum: rows h*128 + quarter*32 .. of part[s][g], fp32
+      // the split's partial sum: row h*128 + row_in_tile of part[s][g], fp32
       const bool got = mbar_wait(gfull_bar, 0, abort_flag);
       if (!__all_sync(0xffffffffu, got)) {
         record_timeout(p.status, abort_flag);
       } else {
         tc_fence_after();
         const uint32_t g_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + 256u;
-        const int prow = s * p.d + col_blk + h * 128 + quarter * 32;
+        const long long prow = static_cast<long long>(s) * p.d + col_blk + h * 128 + row_in_tile;
+        uint4* dst = reinterpret_cast<uint4*>(p.part + prow * 256);
 #pragma unroll 1
         for (int c0 = 0; c0 < 256; c0 += 32) {
-          uint32_t w[32];
-          tmem_load_32cols(g_base + c0, w);
+          uint32_t r[32];
+          tmem_load_32cols(g_base + c0, r);
           tmem_load_wait();
-          if (lane == 0 && stores_pending) bulk_wait_read_all();
-          __syncwarp();
 #pragma unroll
           for (int q = 0; q < 8; ++q)
-            st_shared_v4(my_row + ((q ^ (lane & 7)) << 4), w[4 * q], w[4 * q + 1], w[4 * q + 2],
-                         w[4 * q + 3]);
-          fence_proxy_async_shared();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tmP, stg, c0, prow);
-            bulk_commit();
-            stores_pending = true;
-          }
+            dst[c0 / 4 + q] = make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
         }
       }
     }
-    if (lane == 0 && stores_pending) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -383,21 +365,25 @@ cudaError_t tc_transform_sum(const __nv_bfloat16* X, const __nv_bfloat16* Z,
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  CUtensorMap tmX, tmZ, tmB, tmO, tmP;
+  CUtensorMap tmX, tmZ, tmB;
   if (!make_map(&tmX, X, T, d, d, 2, 64, BM) || !make_map(&tmZ, Z, T, d, d, 2, 64, BM) ||
-      !make_map(&tmB, sb, d, 256, 256, 2, 64, 64) || !make_map(&tmO, out, T, d, d, 2, 64, 32) ||
-      !make_map(&tmP, part, static_cast<long long>(splits) * d, 256, 256, 4, 32, 32))
+      !make_map(&tmB, sb, d, 256, 256, 2, 64, 64))
+    return cudaErrorInvalidValue;
+  if (reinterpret_cast<uintptr_t>(out) % 16 != 0 || reinterpret_cast<uintptr_t>(part) % 16 != 0)
     return cudaErrorInvalidValue;
   TsArgs a;
   a.d = d;
   a.m_tiles = static_cast<int>((T + BM - 1) / BM);
   a.splits = splits;
   a.per = (a.m_tiles + splits - 1) / splits;
+  a.T = T;
+  a.out = out;
+  a.part = part;
   a.status = device_status_ptr();
   const int grid = 2 * (d / 256) * splits;
   prof_begin("transform_sum", stream);
   cudaError_t e = launch_pdl(transform_sum_kernel, dim3(grid), dim3(TS_THREADS), TS_SMEM, stream,
-                             tmX, tmZ, tmB, tmO, tmP, a);
+                             tmX, tmZ, tmB, a);
   prof_end("transform_sum", stream);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
