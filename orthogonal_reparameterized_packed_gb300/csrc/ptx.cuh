@@ -101,15 +101,6 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* t
       : "memory");
 }
 
-// Prefetch one box of a 2-D tensor into L2 (no shared memory, no completion
-// signal): raises the number of DRAM requests in flight beyond what the
-// shared-memory ring holds.
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* tm, int c0, int c1) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(tm),
-               "r"(c0), "r"(c1)
-               : "memory");
-}
-
 // 2-D tiled store of one box from shared memory (bulk-group completion).
 // Parts of the box outside the tensor are not written.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, const void* smem_src, int c0,

@@ -39,7 +39,6 @@ constexpr int TS_XSTAGES = 6;                  // X ring: one 128 x 64 chunk per
 // start on even slots when the ring length is even
 static_assert(TS_XSTAGES % 2 == 0, "even ring length");
 constexpr int TS_ZSTAGES = 2;                  // Z ring: one 128 x 128 half tile per stage
-constexpr int TS_PREFETCH = 2;                 // tiles prefetched into L2 beyond the next one
 constexpr int TS_RES_BYTES = 256 * 128 * 2;    // SB half, 64 KiB
 constexpr int TS_X_BYTES = BM * 64 * 2;        // 16 KiB
 constexpr int TS_Z_BYTES = BM * 128 * 2;       // 32 KiB
@@ -141,17 +140,7 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
         for (int c2 = 0; c2 < 2; ++c2)
           tma_load_2d(sRes + kc * 16384 + c2 * 8192, &tmB, bfull_bar, h * 128 + 64 * c2,
                       col_blk + kc * 64);
-      // L2 prefetch TS_PREFETCH tiles ahead of the ring: the gradient tile by
-      // the h = 0 CTA of the pair, each CTA its own half of Z
-      auto prefetch_tile = [&](int t) {
-        if (h == 0)
-          for (int c = 0; c < 4; ++c) tma_prefetch_l2_2d(&tmX, col_blk + 64 * c, t * BM);
-        tma_prefetch_l2_2d(&tmZ, col_blk + h * 128, t * BM);
-        tma_prefetch_l2_2d(&tmZ, col_blk + h * 128 + 64, t * BM);
-      };
-      for (int t = t_first + 1; t < t_first + 1 + TS_PREFETCH && t < t_end; ++t) prefetch_tile(t);
       for (int t = t_first; t < t_end && ok; ++t) {
-        if (t + 1 + TS_PREFETCH < t_end) prefetch_tile(t + 1 + TS_PREFETCH);
         if (!mbar_wait(&zempty_bar[zs], zphase ^ 1, abort_flag)) {
           record_timeout(p.status, abort_flag);
           ok = false;
