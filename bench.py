@@ -511,6 +511,11 @@ def run_gpu(args):
     if args.train_step and not args.permute and not args.w0_int8:
         merge = time_merge(poetx, layer, dev, w, stream, peaks)
 
+    # whole step against the HBM floor of a fully fused layer: x, y, v in the
+    # forward, dy, v, x in and dx out in the backward (bf16), W0 read twice
+    min_step_bytes = (T * ((2 * di + 4 * do) + (4 * di + 4 * do)) + 2 * 2.0 * di * do
+                      if w["dtype"] == "bf16" else None)
+
     # whole-step algorithmic tensor work for context
     T, di, do, b = w["tokens"], w["d_in"], w["d_out"], w["b"]
     step_flop = T * (4.0 * di * do + 6.0 * b * (di + do))
@@ -566,6 +571,11 @@ def run_gpu(args):
                 "graph_error": graph_error,
                 "ms_per_step_eager": ms_eager, "roofline": roofline,
                 "step_tflops": step_flop / (ms_max * 1e-3) / 1e12,
+                "step_hbm": None if min_step_bytes is None else {
+                    "min_bytes": min_step_bytes,
+                    "achieved_gbs": min_step_bytes / (ms_max * 1e-3) / 1e9,
+                    "frac": min_step_bytes / (ms_max * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                    "note": "algorithmic floor of a fully fused layer step / step time"},
                 "kernels": kernels, "merge": merge, "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
                 "device_status": status}
         print(json.dumps(line), flush=True)

@@ -208,11 +208,31 @@ __global__ void f32_to_bf16_kernel(const float* __restrict__ in, long long count
 }
 
 // --------------------------------------------------- 32 x 32 tile kernels
-// One CTA (32 x 8 threads) per 32 x 32 tile (ti, tj) of one b x b block, so
-// the transposed half of a skew matrix is read and written as coalesced
-// 32-element row segments through a shared-memory tile.
+// One CTA of 256 threads per 32 x 32 tile (ti, tj) of one b x b block; thread
+// (r, c4) owns row r, columns c4 .. c4+3 of the tile (16-byte fp32 / 8-byte
+// bf16 accesses).  The transposed half of a skew matrix goes through a
+// shared-memory tile, so it is read and written row-wise as well.
 
 constexpr int TT = 32;
+
+__device__ __forceinline__ void store_bf16x4(__nv_bfloat16* dst, float a, float b, float c,
+                                             float d) {
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(a, b);
+  const __nv_bfloat162 hi = __floats2bfloat162_rn(c, d);
+  uint2 w;
+  w.x = *reinterpret_cast<const uint32_t*>(&lo);
+  w.y = *reinterpret_cast<const uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(dst) = w;
+}
+
+// bf16 value and bf16 remainder of four entries
+__device__ __forceinline__ void store_hi_lo(__nv_bfloat16* hi, __nv_bfloat16* lo, const float* q) {
+  float h[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) h[e] = __bfloat162float(__float2bfloat16_rn(q[e]));
+  store_bf16x4(hi, h[0], h[1], h[2], h[3]);
+  if (lo != nullptr) store_bf16x4(lo, q[0] - h[0], q[1] - h[1], q[2] - h[2], q[3] - h[3]);
+}
 
 // Q from theta for the tile pair (ti, tj), (tj, ti) with ti <= tj; writes
 // the bf16 value (hi) and optionally the bf16 remainder (lo) of each entry.
@@ -220,33 +240,32 @@ __device__ __forceinline__ void unpack_tile_pair(const float* __restrict__ th, i
                                                  int tj, __nv_bfloat16* __restrict__ hi,
                                                  __nv_bfloat16* __restrict__ lo,
                                                  float (*tile)[TT + 1]) {
-  const int tx = threadIdx.x, ty = threadIdx.y;
-  for (int r = ty; r < TT; r += 8) {  // entries (i, j) of tile (ti, tj), upper part only
-    const int i = ti * TT + r, j = tj * TT + tx;
-    tile[r][tx] = i < j ? th[packed_pos(i, j, b)] : 0.f;
+  const int tid = threadIdx.x;
+  for (int e = tid; e < TT * TT; e += 256) {  // upper entries (i < j) of tile (ti, tj)
+    const int rr = e / TT, cc = e % TT;
+    const int i = ti * TT + rr, j = tj * TT + cc;
+    tile[rr][cc] = i < j ? th[packed_pos(i, j, b)] : 0.f;
   }
   __syncthreads();
-  for (int r = ty; r < TT; r += 8) {
-    // tile (ti, tj): Q[i][j] = theta (i < j), -theta[j][i] (i > j, diagonal tile), 0
-    const int i = ti * TT + r, j = tj * TT + tx;
-    float q = tile[r][tx];
-    if (ti == tj && r > tx) q = -tile[tx][r];
-    const int o = i * b + j;
-    const __nv_bfloat16 h = __float2bfloat16_rn(q);
-    hi[o] = h;
-    if (lo != nullptr) lo[o] = __float2bfloat16_rn(q - __bfloat162float(h));
-    if (ti != tj) {  // mirrored tile (tj, ti): Q[j'][i'] = -theta[i'][j']
-      const int i2 = tj * TT + r, j2 = ti * TT + tx;
-      const float q2 = -tile[tx][r];
-      const int o2 = i2 * b + j2;
-      const __nv_bfloat16 h2 = __float2bfloat16_rn(q2);
-      hi[o2] = h2;
-      if (lo != nullptr) lo[o2] = __float2bfloat16_rn(q2 - __bfloat162float(h2));
-    }
+  const int r = tid >> 3, c4 = (tid & 7) * 4;
+  // tile (ti, tj): Q[i][j] = theta (i < j), -theta[j][i] (below the diagonal), 0
+  float q[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int c = c4 + e;
+    q[e] = (ti == tj && r > c) ? -tile[c][r] : tile[r][c];
+  }
+  const long long o = static_cast<long long>(ti * TT + r) * b + tj * TT + c4;
+  store_hi_lo(hi + o, lo != nullptr ? lo + o : nullptr, q);
+  if (ti != tj) {  // mirrored tile (tj, ti): Q[j'][i'] = -theta[i'][j']
+#pragma unroll
+    for (int e = 0; e < 4; ++e) q[e] = -tile[c4 + e][r];
+    const long long o2 = static_cast<long long>(tj * TT + r) * b + ti * TT + c4;
+    store_hi_lo(hi + o2, lo != nullptr ? lo + o2 : nullptr, q);
   }
 }
 
-// grid (tiles_per_block^2, n_a + n_b):
+// grid (tiles_per_block^2, n_a + n_b), 256 threads:
 //   Q (bf16, plus lo if q_lo) from theta for tiles with ti <= tj,
 //   2I into two_i for block 0,
 //   F = sum over splits of the diagonal b-block of the partials (if f16).
@@ -257,14 +276,15 @@ __global__ void __launch_bounds__(256) prep_tiles_kernel(PrepTilesArgs a) {
   const int t = a.b / TT;
   const int ti = blockIdx.x / t, tj = blockIdx.x % t;
   const int g = blockIdx.y;
-  const int bb = a.b * a.b;
+  const long long bb = static_cast<long long>(a.b) * a.b;
   const int m = a.b * (a.b - 1) / 2;
   const bool side_a = g < a.n_a;
   const int gl = side_a ? g : g - a.n_a;
-  const int tx = threadIdx.x, ty = threadIdx.y;
-  if (a.zero_words != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && ty == 0 &&
-      tx < a.n_zero_words)
-    a.zero_words[tx] = 0u;
+  const int tid = threadIdx.x;
+  const int r = tid >> 3, c4 = (tid & 7) * 4;
+  const int i = ti * TT + r, j0 = tj * TT + c4;
+  if (a.zero_words != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && tid < a.n_zero_words)
+    a.zero_words[tid] = 0u;
   if (a.f16 != nullptr) {
     const int per = a.S / a.b;
     const int sb = gl / per;
@@ -272,32 +292,32 @@ __global__ void __launch_bounds__(256) prep_tiles_kernel(PrepTilesArgs a) {
     const float* part = side_a ? a.part_a : a.part_b;
     const int splits = side_a ? a.splits_a : a.splits_b;
     const long long stride = static_cast<long long>(side_a ? a.nsb_a : a.nsb_b) * a.S * a.S;
-    for (int r = ty; r < TT; r += 8) {
-      const int i = ti * TT + r, j = tj * TT + tx;
-      const long long src = (static_cast<long long>(sb) * a.S + off + i) * a.S + off + j;
-      float v = 0.f;
-      for (int s = 0; s < splits; ++s) v += part[s * stride + src];
-      const long long o = static_cast<long long>(g) * bb + i * a.b + j;
-      a.f16[o] = __float2bfloat16_rn(v);
-      if (a.f32 != nullptr) a.f32[o] = v;
+    const long long src = (static_cast<long long>(sb) * a.S + off + i) * a.S + off + j0;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < splits; ++s) {
+      const float4 w = *reinterpret_cast<const float4*>(part + s * stride + src);
+      v.x += w.x;
+      v.y += w.y;
+      v.z += w.z;
+      v.w += w.w;
     }
+    const long long o = g * bb + static_cast<long long>(i) * a.b + j0;
+    store_bf16x4(a.f16 + o, v.x, v.y, v.z, v.w);
+    if (a.f32 != nullptr) *reinterpret_cast<float4*>(a.f32 + o) = v;
   }
-  if (g == 0 && a.two_i != nullptr) {
-    for (int r = ty; r < TT; r += 8) {
-      const int i = ti * TT + r, j = tj * TT + tx;
-      a.two_i[i * a.b + j] = __float2bfloat16_rn(i == j ? 2.f : 0.f);
-    }
-  }
+  if (g == 0 && a.two_i != nullptr)
+    store_bf16x4(a.two_i + static_cast<long long>(i) * a.b + j0, i == j0 ? 2.f : 0.f,
+                 i == j0 + 1 ? 2.f : 0.f, i == j0 + 2 ? 2.f : 0.f, i == j0 + 3 ? 2.f : 0.f);
   if (ti <= tj && a.q_hi != nullptr) {
     const float* th = side_a ? a.theta_a + static_cast<long long>(gl) * m
                              : a.theta_b + static_cast<long long>(gl) * m;
-    unpack_tile_pair(th, a.b, ti, tj, a.q_hi + static_cast<long long>(g) * bb,
-                     a.q_lo != nullptr ? a.q_lo + static_cast<long long>(g) * bb : nullptr, tile);
+    unpack_tile_pair(th, a.b, ti, tj, a.q_hi + g * bb,
+                     a.q_lo != nullptr ? a.q_lo + g * bb : nullptr, tile);
   }
 }
 
 // dtheta[g][idx(i,j)] = sign * (D[g][i][j] - D[g][j][i]) for the i < j entries of
-// tile (ti, tj), ti <= tj; grid (tiles_per_block^2, n_a + n_b).
+// tile (ti, tj), ti <= tj; grid (tiles_per_block^2, n_a + n_b), 256 threads.
 __global__ void __launch_bounds__(256) pack_tiles_kernel(const float* __restrict__ D, float sign,
                                                          int n_a, int b,
                                                          float* __restrict__ dtheta_a,
@@ -311,17 +331,28 @@ __global__ void __launch_bounds__(256) pack_tiles_kernel(const float* __restrict
   const int g = blockIdx.y;
   const long long base = static_cast<long long>(g) * b * b;
   const int m = b * (b - 1) / 2;
-  const int tx = threadIdx.x, ty = threadIdx.y;
-  for (int r = ty; r < TT; r += 8)  // D[j][i] for the tile: rows of tile (tj, ti)
-    tile[r][tx] = D[base + static_cast<long long>(tj * TT + r) * b + ti * TT + tx];
+  const int tid = threadIdx.x;
+  const int r = tid >> 3, c4 = (tid & 7) * 4;
+  {  // D[j][i] for the tile: rows of tile (tj, ti)
+    const float4 w =
+        *reinterpret_cast<const float4*>(D + base + static_cast<long long>(tj * TT + r) * b +
+                                         ti * TT + c4);
+    tile[r][c4] = w.x;
+    tile[r][c4 + 1] = w.y;
+    tile[r][c4 + 2] = w.z;
+    tile[r][c4 + 3] = w.w;
+  }
   __syncthreads();
   float* out = g < n_a ? dtheta_a + static_cast<long long>(g) * m
                        : dtheta_b + static_cast<long long>(g - n_a) * m;
-  for (int r = ty; r < TT; r += 8) {
-    const int i = ti * TT + r, j = tj * TT + tx;
-    if (i >= j) continue;
-    const float v = D[base + static_cast<long long>(i) * b + j] - tile[tx][r];
-    out[packed_pos(i, j, b)] = sign * v;
+  const int i = ti * TT + r, j0 = tj * TT + c4;
+  const float4 dij =
+      *reinterpret_cast<const float4*>(D + base + static_cast<long long>(i) * b + j0);
+  const float d4[4] = {dij.x, dij.y, dij.z, dij.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int j = j0 + e;
+    if (i < j) out[packed_pos(i, j, b)] = sign * (d4[e] - tile[c4 + e][r]);
   }
 }
 
@@ -585,7 +616,7 @@ cudaError_t launch_prep_tiles(const PrepTilesArgs& a, cudaStream_t s) {
   const int t = a.b / TT;
   dim3 grid(t * t, a.n_a + a.n_b);
   prof_begin("prep_tiles", s);
-  cudaError_t e = launch_pdl(prep_tiles_kernel, grid, dim3(TT, 8), 0, s, a);
+  cudaError_t e = launch_pdl(prep_tiles_kernel, grid, dim3(256), 0, s, a);
   prof_end("prep_tiles", s);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -596,7 +627,7 @@ cudaError_t launch_pack_tiles(const float* D, float sign, int n_a, int n_b, int 
   const int t = b / TT;
   dim3 grid(t * t, n_a + n_b);
   prof_begin("pack_tiles", s);
-  cudaError_t e = launch_pdl(pack_tiles_kernel, grid, dim3(TT, 8), 0, s, D, sign, n_a, b,
+  cudaError_t e = launch_pdl(pack_tiles_kernel, grid, dim3(256), 0, s, D, sign, n_a, b,
                              dtheta_a, dtheta_b);
   prof_end("pack_tiles", s);
   return e != cudaSuccess ? e : cudaGetLastError();
