@@ -546,6 +546,7 @@ struct CnpBufs {
   float* dq = nullptr;
   unsigned int* counter = nullptr;
   bf16* two_i = nullptr;  // chain: constant 2I
+  bf16* x16 = nullptr;    // chain, k = 3: 2Q
 };
 
 CnpBufs carve_cnp(Carver& c, int n, int b, int k, bool tc) {
@@ -567,6 +568,7 @@ CnpBufs carve_cnp(Carver& c, int n, int b, int k, bool tc) {
   if (tc) {
     w.counter = c.take<unsigned int>(kChainMaxPhases);
     w.two_i = c.take<bf16>(static_cast<size_t>(b) * b);
+    if (k == 3) w.x16 = c.take<bf16>(nbb);
   }
   return w;
 }
@@ -592,6 +594,7 @@ cudaError_t chain_adjoint_from_parts(const float* theta_a, int n_a, const float*
   for (int i = 2; i <= k; ++i) a.e16[i] = w.e16[i];
   a.f16[0] = w.g16[0];
   a.f16[1] = w.g16[1];
+  a.x16 = w.x16;
   a.d32 = w.dq;
   a.S = superblock(b);
   a.part_a = part_a;

@@ -47,6 +47,7 @@ constexpr int kMaxDSlots = 2;
 enum { PROD_STORE = 0, PROD_ACC = 1, PROD_ACC_STORE = 2 };
 
 constexpr int kChainMaxMaps = 48;
+constexpr int kChainMaxTerms = 5;
 
 struct ChainTerm {
   int a_map, b_map;  // A: K-major box map, B: MN-major box map
@@ -63,7 +64,7 @@ __device__ __forceinline__ void term_ksteps(const ChainTerm& T, int nt, int kste
 
 struct ChainProd {
   int nterms;
-  ChainTerm term[3];
+  ChainTerm term[kChainMaxTerms];
   int mode;       // PROD_STORE / PROD_ACC / PROD_ACC_STORE
   int first_acc;  // ACC modes: this phase initialises the persistent slot
   EpiArgs epi;    // stores only: alpha, delta, out_f32 / out_bf16
@@ -504,6 +505,7 @@ cudaError_t chain_build(const ChainBuildArgs& a, cudaStream_t stream) {
   pa.theta_a = a.theta;
   pa.q_hi = a.q_hi;
   pa.q_lo = a.q_lo;
+  pa.q_x2 = k == 3 ? a.e16[1] : nullptr;  // 2 Q_hi for the two-phase k = 3 build
   pa.two_i = a.two_i;
   pa.zero_words = a.counter;
   pa.n_zero_words = kChainMaxPhases;
@@ -520,9 +522,40 @@ cudaError_t chain_build(const ChainBuildArgs& a, cudaStream_t stream) {
   const int hi = maps.add(a.q_hi, rows, b);
   const int lo = maps.add(a.q_lo, rows, b);
   const int two = maps.add(a.two_i, b, b);
+  int ph = 0;
+  if (k == 3) {
+    // R_3 = I + 2Q + Q^2 (2I + 2Q + Q^2): two dependent products instead of
+    // three (the even/odd split of the Neumann polynomial in Q^2).
+    //   phase 1: Q2 = Q_hi Q_hi
+    //   phase 2: block = I + Q_hi 2I + Q_lo 2I + Q2 2I + (2 Q_hi) Q2 + Q2 Q2
+    const int q2 = maps.add(a.e16[0], rows, b);
+    const int hi2 = maps.add(a.e16[1], rows, b);  // 2 Q_hi from the prep launch
+    ChainProd& P1 = P.phases[ph].prod[0];
+    P.phases[ph++].nprod = 1;
+    P1.nterms = 1;
+    P1.term[0] = term(hi, hi, true);
+    P1.mode = PROD_STORE;
+    P1.epi = chain_epi(b);
+    P1.epi.out_bf16 = a.e16[0];
+    ChainProd& P2 = P.phases[ph].prod[0];
+    P.phases[ph++].nprod = 1;
+    P2.nterms = 5;
+    P2.term[0] = term_2i(hi, two);
+    P2.term[1] = term_2i(lo, two);
+    P2.term[2] = term_2i(q2, two);
+    P2.term[3] = term(hi2, q2, true);
+    P2.term[4] = term(q2, q2, true);
+    P2.mode = PROD_STORE;
+    P2.epi = chain_epi(b);
+    P2.epi.delta = 1.f;
+    P2.epi.out_bf16 = a.blocks;
+    P.nphases = ph;
+    if (!maps.ok) return cudaErrorInvalidValue;
+    return launch_chain(P, stream);
+  }
   int cur = hi;  // E_{k+1} = Q
   __nv_bfloat16* ebuf[2] = {a.e16[0], a.e16[1]};
-  int nxt = 0, ph = 0;
+  int nxt = 0;
   for (int i = k; i >= 1; --i) {
     // E_i = Q E_{i+1} + 2Q,  2Q = Q_hi 2I + Q_lo 2I;  block = I + E_1
     ChainPhase& PH = P.phases[ph++];
@@ -568,11 +601,71 @@ cudaError_t chain_adjoint(const ChainAdjointArgs& a, cudaStream_t stream) {
   pa.nsb_b = a.nsb_b;
   pa.S = a.S;
   pa.f16 = a.f16[0];
+  pa.q_x2 = k == 3 ? a.x16 : nullptr;
   pa.zero_words = a.counter;
   pa.n_zero_words = kChainMaxPhases;
+  if (k == 3 && a.x16 == nullptr) return cudaErrorInvalidValue;
   cudaError_t e = launch_prep_tiles(pa, stream);
   if (e != cudaSuccess) return e;
-  {
+  if (k == 3) {
+    // Adjoint of R = I + 2Q + Q2 M, M = 2I + 2Q + Q2, Q2 = Q Q, on transposes
+    // (H = G^T, D = dQ^T), with Q^T = -Q and Q2^T = Q2:
+    //   phase 1: Q2 = Q Q,  Q2d = (2Q) Q
+    //   phase 2: D2 = dQ2^T = H 2I + (2Q) H + Q2 H + H Q2
+    //   phase 3: D = H 2I + H Q2d + Q D2 + D2 Q
+    // three dependent products instead of 2k - 1 = 5.
+    std::lock_guard<std::mutex> lock(g_chain_mu);
+    ChainParams& P = g_chain_params;
+    P = ChainParams();
+    P.n = n;
+    P.b = b;
+    P.counter = a.counter;
+    MapTable maps{&P};
+    const long long rows = static_cast<long long>(n) * b;
+    const int q = maps.add(a.q16, rows, b);
+    const int x = maps.add(a.x16, rows, b);
+    const int two = maps.add(a.two_i, b, b);
+    const int h = maps.add(a.f16[0], rows, b);
+    const int q2 = maps.add(a.e16[2], rows, b);
+    const int q2d = maps.add(a.e16[3], rows, b);
+    const int d2 = maps.add(a.f16[1], rows, b);
+    ChainPhase& P1 = P.phases[0];
+    P1.nprod = 2;
+    P1.prod[0].nterms = 1;
+    P1.prod[0].term[0] = term(q, q, true);
+    P1.prod[0].mode = PROD_STORE;
+    P1.prod[0].epi = chain_epi(b);
+    P1.prod[0].epi.out_bf16 = a.e16[2];
+    P1.prod[1].nterms = 1;
+    P1.prod[1].term[0] = term(x, q, true);
+    P1.prod[1].mode = PROD_STORE;
+    P1.prod[1].epi = chain_epi(b);
+    P1.prod[1].epi.out_bf16 = a.e16[3];
+    ChainProd& P2 = P.phases[1].prod[0];
+    P.phases[1].nprod = 1;
+    P2.nterms = 4;
+    P2.term[0] = term_2i(h, two);
+    P2.term[1] = term(x, h, true);
+    P2.term[2] = term(q2, h, true);
+    P2.term[3] = term(h, q2, true);
+    P2.mode = PROD_STORE;
+    P2.epi = chain_epi(b);
+    P2.epi.out_bf16 = a.f16[1];
+    ChainProd& P3 = P.phases[2].prod[0];
+    P.phases[2].nprod = 1;
+    P3.nterms = 4;
+    P3.term[0] = term_2i(h, two);
+    P3.term[1] = term(h, q2d, true);
+    P3.term[2] = term(q, d2, true);
+    P3.term[3] = term(d2, q, true);
+    P3.mode = PROD_STORE;
+    P3.epi = chain_epi(b);
+    P3.epi.out_f32 = a.d32;
+    P.nphases = 3;
+    if (!maps.ok) return cudaErrorInvalidValue;
+    e = launch_chain(P, stream);
+    if (e != cudaSuccess) return e;
+  } else {
     std::lock_guard<std::mutex> lock(g_chain_mu);
     ChainParams& P = g_chain_params;
     P = ChainParams();

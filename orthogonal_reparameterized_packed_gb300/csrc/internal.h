@@ -140,8 +140,8 @@ cudaError_t chain_build(const ChainBuildArgs& a, cudaStream_t stream);
 
 // Packed gradients of both sides from the split-K partials of the TRANSPOSED
 // block gradients G^T (blocks [0, n_a) from part_a / theta_a, the rest from
-// part_b / theta_b).  Scratch [n_a + n_b][b][b]: q16, e16[2..k], f16[0..1]
-// (bf16) and d32 (fp32); two_i [b][b] bf16; counter [kChainMaxPhases] words.
+// part_b / theta_b).  Scratch [n_a + n_b][b][b]: q16, e16[2..k], f16[0..1],
+// x16 (bf16) and d32 (fp32); two_i [b][b] bf16; counter [kChainMaxPhases] words.
 struct ChainAdjointArgs {
   int n_a = 0, n_b = 0, b = 0, k = 0;
   const float* theta_a = nullptr;
@@ -150,6 +150,7 @@ struct ChainAdjointArgs {
   __nv_bfloat16* two_i = nullptr;
   __nv_bfloat16* e16[kChainMaxK + 2] = {};
   __nv_bfloat16* f16[2] = {nullptr, nullptr};
+  __nv_bfloat16* x16 = nullptr;  // k = 3: 2Q
   float* d32 = nullptr;
   const float* part_a = nullptr;
   const float* part_b = nullptr;
@@ -190,6 +191,7 @@ struct PrepTilesArgs {
   const float* theta_b = nullptr;
   __nv_bfloat16* q_hi = nullptr;
   __nv_bfloat16* q_lo = nullptr;
+  __nv_bfloat16* q_x2 = nullptr;  // if set: 2 * q_hi (exact in bf16)
   __nv_bfloat16* two_i = nullptr;
   const float* part_a = nullptr;
   const float* part_b = nullptr;

@@ -225,13 +225,15 @@ __device__ __forceinline__ void store_bf16x4(__nv_bfloat16* dst, float a, float 
   *reinterpret_cast<uint2*>(dst) = w;
 }
 
-// bf16 value and bf16 remainder of four entries
-__device__ __forceinline__ void store_hi_lo(__nv_bfloat16* hi, __nv_bfloat16* lo, const float* q) {
+// bf16 value, bf16 remainder and twice the bf16 value of four entries
+__device__ __forceinline__ void store_hi_lo(__nv_bfloat16* hi, __nv_bfloat16* lo,
+                                            __nv_bfloat16* x2, const float* q) {
   float h[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) h[e] = __bfloat162float(__float2bfloat16_rn(q[e]));
   store_bf16x4(hi, h[0], h[1], h[2], h[3]);
   if (lo != nullptr) store_bf16x4(lo, q[0] - h[0], q[1] - h[1], q[2] - h[2], q[3] - h[3]);
+  if (x2 != nullptr) store_bf16x4(x2, 2.f * h[0], 2.f * h[1], 2.f * h[2], 2.f * h[3]);
 }
 
 // Q from theta for the tile pair (ti, tj), (tj, ti) with ti <= tj; writes
@@ -239,6 +241,7 @@ __device__ __forceinline__ void store_hi_lo(__nv_bfloat16* hi, __nv_bfloat16* lo
 __device__ __forceinline__ void unpack_tile_pair(const float* __restrict__ th, int b, int ti,
                                                  int tj, __nv_bfloat16* __restrict__ hi,
                                                  __nv_bfloat16* __restrict__ lo,
+                                                 __nv_bfloat16* __restrict__ x2,
                                                  float (*tile)[TT + 1]) {
   const int tid = threadIdx.x;
   for (int e = tid; e < TT * TT; e += 256) {  // upper entries (i < j) of tile (ti, tj)
@@ -256,17 +259,18 @@ __device__ __forceinline__ void unpack_tile_pair(const float* __restrict__ th, i
     q[e] = (ti == tj && r > c) ? -tile[c][r] : tile[r][c];
   }
   const long long o = static_cast<long long>(ti * TT + r) * b + tj * TT + c4;
-  store_hi_lo(hi + o, lo != nullptr ? lo + o : nullptr, q);
+  store_hi_lo(hi + o, lo != nullptr ? lo + o : nullptr, x2 != nullptr ? x2 + o : nullptr, q);
   if (ti != tj) {  // mirrored tile (tj, ti): Q[j'][i'] = -theta[i'][j']
 #pragma unroll
     for (int e = 0; e < 4; ++e) q[e] = -tile[c4 + e][r];
     const long long o2 = static_cast<long long>(tj * TT + r) * b + ti * TT + c4;
-    store_hi_lo(hi + o2, lo != nullptr ? lo + o2 : nullptr, q);
+    store_hi_lo(hi + o2, lo != nullptr ? lo + o2 : nullptr, x2 != nullptr ? x2 + o2 : nullptr,
+                q);
   }
 }
 
 // grid (tiles_per_block^2, n_a + n_b), 256 threads:
-//   Q (bf16, plus lo if q_lo) from theta for tiles with ti <= tj,
+//   Q (bf16, plus lo if q_lo, plus 2Q if q_x2) from theta for tiles with ti <= tj,
 //   2I into two_i for block 0,
 //   F = sum over splits of the diagonal b-block of the partials (if f16).
 __global__ void __launch_bounds__(256) prep_tiles_kernel(PrepTilesArgs a) {
@@ -312,7 +316,8 @@ __global__ void __launch_bounds__(256) prep_tiles_kernel(PrepTilesArgs a) {
     const float* th = side_a ? a.theta_a + static_cast<long long>(gl) * m
                              : a.theta_b + static_cast<long long>(gl) * m;
     unpack_tile_pair(th, a.b, ti, tj, a.q_hi + g * bb,
-                     a.q_lo != nullptr ? a.q_lo + g * bb : nullptr, tile);
+                     a.q_lo != nullptr ? a.q_lo + g * bb : nullptr,
+                     a.q_x2 != nullptr ? a.q_x2 + g * bb : nullptr, tile);
   }
 }
 
