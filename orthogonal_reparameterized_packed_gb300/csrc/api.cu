@@ -227,6 +227,9 @@ cudaError_t tc_outer(const bf16* A, const bf16* B, float* part, int d, int S, lo
   return tc_gemm_run(g, s);
 }
 
+// The W0 GEMMs run as clusters of two CTAs that share each B (W0) tile.
+constexpr bool kW0Clusters = true;
+
 // v = u W0^T (fwd) or du = dv W0 (dgrad), bf16.
 cudaError_t tc_w0(const bf16* A, const bf16* W0, bf16* out, int d_in, int d_out, long long T,
                   bool dgrad, cudaStream_t s) {
@@ -251,6 +254,7 @@ cudaError_t tc_w0(const bf16* A, const bf16* W0, bf16* out, int d_in, int d_out,
   g.epi.out_bf16 = out;
   g.epi.row_limit = static_cast<int>(T);
   g.epi.out_rows = T;
+  g.cluster2 = kW0Clusters;
   return tc_gemm_run(g, s);
 }
 

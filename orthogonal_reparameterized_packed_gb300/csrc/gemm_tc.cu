@@ -65,6 +65,7 @@ constexpr int kBlockKSteps = 256 / BK;  // K steps of the epilogue's 256 x 256 b
 
 struct TcKernelArgs {
   int m_tiles, n_tiles, splits, batches;
+  int m_pairs;  // CL2: pairs of M tiles, one per cluster of two CTAs
   int k_steps_total, k_steps_per_split;
   int a_mn_per_g, a_k_per_g, b_mn_per_g, b_k_per_g;
   EpiArgs epi;
@@ -93,12 +94,34 @@ __device__ __forceinline__ void decode_tile(int t, const TcKernelArgs& p, int& g
   g = t / p.splits;
 }
 
-// Tiles of this CTA: resident variants take a contiguous run, others stride.
-template <bool B_RES>
+// CL2: a cluster of two CTAs takes work units (g, split, M pair, N tile); CTA
+// rank r of the cluster computes M tile 2 * pair + r, so the two share B.
+template <bool B_RES, bool CL2>
+__device__ __forceinline__ void decode_unit(int t, const TcKernelArgs& p, uint32_t crank, int& g,
+                                            int& sp, int& mt, int& nt) {
+  if (CL2) {
+    nt = t % p.n_tiles;
+    t /= p.n_tiles;
+    mt = 2 * (t % p.m_pairs) + static_cast<int>(crank);
+    t /= p.m_pairs;
+    sp = t % p.splits;
+    g = t / p.splits;
+  } else {
+    decode_tile<B_RES>(t, p, g, sp, mt, nt);
+  }
+}
+
+// Tiles of this CTA: resident variants take a contiguous run, others stride
+// (CL2: over clusters).
+template <bool B_RES, bool CL2>
 struct TileRange {
   int first, end, step;
   __device__ explicit TileRange(int num_tiles) {
-    if (B_RES) {
+    if (CL2) {
+      first = static_cast<int>(cluster_id_x());
+      end = num_tiles;
+      step = static_cast<int>(cluster_count_x());
+    } else if (B_RES) {
       const int per = (num_tiles + gridDim.x - 1) / gridDim.x;
       first = blockIdx.x * per;
       end = min(first + per, num_tiles);
@@ -143,7 +166,7 @@ __device__ __forceinline__ void store_staged_rows(const CUtensorMap* map, uint8_
   bulk_commit();
 }
 
-template <bool A_MN, bool B_MN, int BN, bool B_RES, int EPI>
+template <bool A_MN, bool B_MN, int BN, bool B_RES, int EPI, bool CL2>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB,
@@ -151,6 +174,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                    const __grid_constant__ CUtensorMap tmR,
                    const __grid_constant__ CUtensorMap tmY, const TcKernelArgs p) {
   using S = TcShape<BN, B_RES, EPI>;
+  static_assert(!CL2 || (EPI == EPI_TMA_BF16 && !B_RES && BN == 256), "clusters: W0 GEMMs");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -173,13 +197,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const int num_tiles = p.batches * p.splits * p.m_tiles * p.n_tiles;
-  const TileRange<B_RES> range(num_tiles);
+  const uint32_t crank = CL2 ? cluster_ctarank() : 0u;
+  const int num_tiles = p.batches * p.splits * (CL2 ? p.m_pairs : p.m_tiles) * p.n_tiles;
+  const TileRange<B_RES, CL2> range(num_tiles);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], 1);
+      mbar_init(&empty_bar[s], CL2 ? 2 : 1);  // CL2: both CTAs' MMAs free a stage
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull_bar[a], 1);
@@ -208,6 +233,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (CL2) cluster_sync();  // the peer's barriers exist before any multicast reaches them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   pdl_wait();  // the predecessor's outputs are complete from here on
@@ -249,7 +275,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       };
       for (int tile = range.first; tile < range.end && ok; tile += range.step) {
         int g, sp, mt, nt;
-        decode_tile<B_RES>(tile, p, g, sp, mt, nt);
+        decode_unit<B_RES, CL2>(tile, p, crank, g, sp, mt, nt);
         const int ks0 = sp * p.k_steps_per_split;
         const int ks1 = min(ks0 + p.k_steps_per_split, p.k_steps_total);
         const int a_mn = g * p.a_mn_per_g + mt * BM;
@@ -294,7 +320,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tma_load_2d(a_dst, &tmA, &full_bar[stage], a_mn, a_k);
             tma_load_2d(a_dst + 8192, &tmA, &full_bar[stage], a_mn + 64, a_k);
           }
-          if (!B_RES) {
+          if (!B_RES && CL2) {
+            // this CTA's half of the shared B tile, delivered to both CTAs
+            const int b_k = g * p.b_k_per_g + ks * BK;
+            uint8_t* b_dst = sB + stage * S::B_BYTES;
+            if (!B_MN) {
+              tma_load_2d_mc(b_dst + crank * (BN / 2) * 128, &tmB, &full_bar[stage], b_k,
+                             b_mn + static_cast<int>(crank) * (BN / 2), 0x3);
+            } else {
+#pragma unroll
+              for (int c = 0; c < BN / 128; ++c) {
+                const int cc = static_cast<int>(crank) * (BN / 128) + c;
+                tma_load_2d_mc(b_dst + cc * 8192, &tmB, &full_bar[stage], b_mn + 64 * cc, b_k,
+                               0x3);
+              }
+            }
+          } else if (!B_RES) {
             const int b_k = g * p.b_k_per_g + ks * BK;
             uint8_t* b_dst = sB + stage * S::B_BYTES;
             if (!B_MN) {
@@ -392,7 +433,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       };
       for (int tile = range.first; tile < range.end && ok; tile += range.step) {
         int g, sp, mt, nt;
-        decode_tile<B_RES>(tile, p, g, sp, mt, nt);
+        decode_unit<B_RES, CL2>(tile, p, crank, g, sp, mt, nt);
         const int ks0 = sp * p.k_steps_per_split;
         const int ks1 = min(ks0 + p.k_steps_per_split, p.k_steps_total);
         if (B_RES) {
@@ -435,7 +476,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             umma_bf16(d_tmem, adesc, bdesc, IDESC, (ks > ks0 || j > 0) ? 1u : 0u);
           }
           any_mma = true;
-          umma_commit(&empty_bar[stage]);  // frees this smem stage when done
+          if (CL2)  // the stage is free once both CTAs' MMAs have read it
+            umma_commit_mc(&empty_bar[stage], 0x3);
+          else
+            umma_commit(&empty_bar[stage]);  // frees this smem stage when done
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -502,7 +546,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     };
     for (int tile = range.first; tile < range.end; tile += range.step) {
       int g, sp, mt, nt;
-      decode_tile<B_RES>(tile, p, g, sp, mt, nt);
+      decode_unit<B_RES, CL2>(tile, p, crank, g, sp, mt, nt);
       const bool got = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag);
       if (!__all_sync(0xffffffffu, got)) {  // the whole warp unwinds together
         record_timeout(p.status, abort_flag);
@@ -597,6 +641,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (CL2) cluster_sync();  // no CTA leaves while its peer may still write to it
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -606,22 +651,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 // ------------------------------------------------------------- host side
 
-template <bool A_MN, bool B_MN, int BN, bool B_RES, int EPI>
+template <bool A_MN, bool B_MN, int BN, bool B_RES, int EPI, bool CL2 = false>
 cudaError_t launch_tc(const TcGemm& g, cudaStream_t stream) {
   using S = TcShape<BN, B_RES, EPI>;
+  auto* kernel = tc_gemm_kernel<A_MN, B_MN, BN, B_RES, EPI, CL2>;
   static bool attr_set[64] = {false};
+  static int max_clusters[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<A_MN, B_MN, BN, B_RES, EPI>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
     if (e != cudaSuccess) return e;
+    if (CL2) {  // clusters of two that fit at once (SMs pair up within a GPC)
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2 * sm_count());
+      cfg.blockDim = dim3(NUM_THREADS);
+      cfg.dynamicSmemBytes = S::SMEM;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+      if (e != cudaSuccess) return e;
+      if (n < 1) return cudaErrorLaunchOutOfResources;
+      max_clusters[dev] = n;
+    }
     attr_set[dev] = true;
   }
   CUtensorMap tmA, tmB, tmC, tmR, tmY;
   if (!make_map(&tmA, g.A.ptr, g.A.rows, g.A.cols, g.A.pitch, 2, 64, A_MN ? 64 : BM))
     return cudaErrorInvalidValue;
-  if (!make_map(&tmB, g.B.ptr, g.B.rows, g.B.cols, g.B.pitch, 2, 64, B_MN ? 64 : BN))
+  // CL2: each CTA of a cluster loads half of a K-major B tile
+  if (!make_map(&tmB, g.B.ptr, g.B.rows, g.B.cols, g.B.pitch, 2, 64,
+                B_MN ? 64 : (CL2 ? BN / 2 : BN)))
     return cudaErrorInvalidValue;
   if (EPI == EPI_TMA_BF16 || (EPI == EPI_BLOCK && g.epi.out_bf16 != nullptr)) {
     if (!make_map(&tmC, g.epi.out_bf16, g.epi.out_rows, g.epi.ld, g.epi.ld, 2, 64, 32))
@@ -645,6 +713,7 @@ cudaError_t launch_tc(const TcGemm& g, cudaStream_t stream) {
 
   TcKernelArgs p;
   p.m_tiles = (g.M + BM - 1) / BM;
+  p.m_pairs = (p.m_tiles + 1) / 2;
   p.n_tiles = g.N / BN;
   p.k_steps_total = (g.K + BK - 1) / BK;
   const int splits = tc_effective_splits(g.K, g.splits);
@@ -660,6 +729,30 @@ cudaError_t launch_tc(const TcGemm& g, cudaStream_t stream) {
   p.status = device_status_ptr();
   if (B_RES && (p.splits != 1 || p.k_steps_total > S::MAX_RES_KSTEPS))
     return cudaErrorInvalidValue;
+  if (CL2) {
+    const long long units =
+        static_cast<long long>(p.batches) * p.splits * p.m_pairs * p.n_tiles;
+    if (units <= 0) return cudaSuccess;
+    const int clusters = static_cast<int>(std::min<long long>(units, max_clusters[dev]));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = S::SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    prof_begin(g.tag, stream);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmC, tmR, tmY, p);
+    prof_end(g.tag, stream);
+    return e != cudaSuccess ? e : cudaGetLastError();
+  }
   const long long tiles = static_cast<long long>(p.batches) * p.splits * p.m_tiles * p.n_tiles;
   if (tiles <= 0) return cudaSuccess;
   int grid = static_cast<int>(std::min<long long>(tiles, sm_count()));
@@ -668,8 +761,8 @@ cudaError_t launch_tc(const TcGemm& g, cudaStream_t stream) {
     grid = static_cast<int>((tiles + per - 1) / per);
   }
   prof_begin(g.tag, stream);
-  cudaError_t e = launch_pdl(tc_gemm_kernel<A_MN, B_MN, BN, B_RES, EPI>, dim3(grid),
-                             dim3(NUM_THREADS), S::SMEM, stream, tmA, tmB, tmC, tmR, tmY, p);
+  cudaError_t e = launch_pdl(kernel, dim3(grid), dim3(NUM_THREADS), S::SMEM, stream, tmA, tmB,
+                             tmC, tmR, tmY, p);
   prof_end(g.tag, stream);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -722,6 +815,10 @@ cudaError_t tc_gemm_run(const TcGemm& g, cudaStream_t stream) {
   }
   if (g.BN != 256) return cudaErrorInvalidValue;
   if (bf16_out) {  // the W0 GEMM and its transpose
+    if (g.cluster2 && g.batches == 1 && g.splits == 1 && g.M > BM) {  // B shared by two CTAs
+      if (!a && !b) return launch_tc<false, false, 256, false, EPI_TMA_BF16, true>(g, stream);
+      if (!a && b) return launch_tc<false, true, 256, false, EPI_TMA_BF16, true>(g, stream);
+    }
     if (!a && !b) return launch_tc<false, false, 256, false, EPI_TMA_BF16>(g, stream);
     if (!a && b) return launch_tc<false, true, 256, false, EPI_TMA_BF16>(g, stream);
     return cudaErrorInvalidValue;

@@ -71,6 +71,9 @@ struct TcGemm {
   // Keep the B operand of a (batch, N tile) resident in shared memory while
   // the CTA walks consecutive M tiles (needs splits == 1 and BN*K*2 <= 128 KiB).
   bool b_resident = false;
+  // W0 GEMMs: run as clusters of two CTAs on adjacent M tiles that load one
+  // half of each shared B tile each (TMA multicast)
+  bool cluster2 = false;
   TcOperand A, B;
   EpiArgs epi;
   // Block-diagonal factor in the epilogue (W0 GEMMs, BN = 256): N tile j of
