@@ -552,29 +552,26 @@ def run_gpu(args):
               for _ in range(2)]
         hR = [torch.empty(layer.dtheta_R.shape, dtype=torch.float32).pin_memory()
               for _ in range(2)]
-        # x and dy upload on two streams (two copy engines)
-        h2d = [torch.cuda.Stream(), torch.cuda.Stream()]
-        d2h = torch.cuda.Stream()
-        up = [[torch.cuda.Event() for _ in range(2)] for _ in range(2)]
+        h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+        up = [torch.cuda.Event() for _ in range(2)]
         done = [torch.cuda.Event() for _ in range(2)]
         down = [torch.cuda.Event() for _ in range(2)]
 
         def upload(j, after=None):
-            for c, (key, host) in enumerate((("x", hx), ("dy", hdy))):
-                with torch.cuda.stream(h2d[c]):
-                    if after is not None:
-                        h2d[c].wait_event(after)  # the set's previous step has read it
-                    sets[j][0][key].copy_(host, non_blocking=True)
-                    up[j][c].record(h2d[c])
+            with torch.cuda.stream(h2d):
+                if after is not None:
+                    h2d.wait_event(after)  # the set's previous step has read its inputs
+                sets[j][0]["x"].copy_(hx, non_blocking=True)
+                sets[j][0]["dy"].copy_(hdy, non_blocking=True)
+                up[j].record(h2d)
 
         def pipeline(k, start):
-            for st in (*h2d, d2h):
-                st.wait_event(start)
+            h2d.wait_event(start)
+            d2h.wait_event(start)
             upload(0)
             for i in range(k):
                 j = i % 2
-                stream.wait_event(up[j][0])
-                stream.wait_event(up[j][1])
+                stream.wait_event(up[j])
                 if i >= 2:
                     stream.wait_event(down[j])  # the set's dtheta has been read back
                 sets[j][2]()
@@ -587,8 +584,7 @@ def run_gpu(args):
                     hR[j].copy_(sets[j][1].dtheta_R, non_blocking=True)
                     down[j].record(d2h)
             stream.wait_stream(d2h)
-            for st in h2d:
-                stream.wait_stream(st)
+            stream.wait_stream(h2d)
 
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
