@@ -29,7 +29,8 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from orthogonal_reparameterized_packed_gb300.inputs import WORKLOADS, make_layer_inputs  # noqa
+from orthogonal_reparameterized_packed_gb300.inputs import (COMPOSITES, WORKLOADS,  # noqa
+                                                            make_layer_inputs)
 
 METRIC = "POET-X layer fwd+bwd tokens/s (d=4096,b=256,bf16); % HBM / tensor-core roofline"
 UNIT = "tokens/s"
@@ -41,7 +42,11 @@ def parse():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="poetx", choices=["poetx", "reference"])
-    ap.add_argument("--workload", default="llama3_8b_qo", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="llama3_8b_qo",
+                    choices=sorted(WORKLOADS) + sorted(COMPOSITES),
+                    help="one projection, or a composite run as its projections in sequence "
+                         "(llama3_8b_block: the 7 of a Llama-3-8B decoder block; "
+                         "llama_1p3b_model: all 168 of the 1.3B-shaped model)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true",
@@ -68,10 +73,32 @@ def workload_config(name):
     return w
 
 
-def config_json(name, w, n, args=None):
-    c = {"workload": name, "d_in": w["d_in"], "d_out": w["d_out"], "b": w["b"], "k": w["k"],
-         "tokens_per_gpu": w["tokens"], "dtype": w["dtype"], "parallelism": f"replicas{n}",
+def projections(name):
+    """The (projection, workload key) pairs one step runs, in order."""
+    return COMPOSITES[name] if name in COMPOSITES else [(name, name)]
+
+
+def step_shapes(name):
+    """Distinct workload keys of a step and how often each runs."""
+    counts = {}
+    for _, key in projections(name):
+        counts[key] = counts.get(key, 0) + 1
+    return counts
+
+
+def config_json(name, n, args=None):
+    counts = step_shapes(name)
+    w = WORKLOADS[next(iter(counts))]
+    c = {"workload": name, "b": w["b"], "k": w["k"], "tokens_per_gpu": w["tokens"],
+         "dtype": w["dtype"], "parallelism": f"replicas{n}",
          "l2": "inputs larger than L2 (x, dy 128 MiB each; ~1 GB touched per step)"}
+    if name in WORKLOADS:
+        c["d_in"], c["d_out"] = w["d_in"], w["d_out"]
+    else:
+        c["projections"] = len(projections(name))
+        c["shapes"] = {key: {"d_in": WORKLOADS[key]["d_in"], "d_out": WORKLOADS[key]["d_out"],
+                             "count": cnt} for key, cnt in counts.items()}
+        c["l2"] = "every projection's activations exceed L2 or are evicted by the next ones"
     if args is not None and getattr(args, "permute", False):
         c["permuted_blocks"] = True
     if args is not None and getattr(args, "recompute_v", False):
@@ -127,15 +154,26 @@ def oracle_sample(inp, sample_tokens):
     return (t1 - t0) + (t3 - t2), (t2 - t1) / sample_tokens
 
 
-def cpu_baseline(inp, sample_tokens):
-    t_fixed, t_tok = oracle_sample(inp, sample_tokens)
-    T = inp.tokens
+def cpu_baseline(name, sample_tokens, seed=0):
+    """The oracle on a bounded sample: each distinct projection shape of the
+    step once, scaled by how often the step runs it."""
+    t_fixed = t_tok = 0.0
+    T = None
+    for key, cnt in step_shapes(name).items():
+        inp = make_layer_inputs(**WORKLOADS[key], seed=seed)
+        f, tt = oracle_sample(inp, sample_tokens)
+        t_fixed += cnt * f
+        t_tok += cnt * tt
+        T = inp.tokens
     value = T / (t_fixed + t_tok * T)
     return {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
             "sample": (f"float64 numpy oracle: block build + CNP adjoint of both sides "
                        f"({t_fixed:.2f} s) and forward+backward on {sample_tokens} of {T} "
-                       f"tokens ({t_tok * sample_tokens:.2f} s); tokens/s extrapolated "
-                       f"linearly in tokens to the full {T}")}
+                       f"tokens ({t_tok * sample_tokens:.2f} s) per step"
+                       + ("" if name in WORKLOADS else
+                          f" (each of the {len(step_shapes(name))} distinct shapes timed once, "
+                          f"weighted by its count in the {len(projections(name))} projections)")
+                       + f"; tokens/s extrapolated linearly in tokens to the full {T}")}
 
 
 def run_reference(args):
@@ -143,29 +181,30 @@ def run_reference(args):
     if rank != 0:
         return
     name = args.workload
-    w = workload_config(name)
-    inp = make_layer_inputs(**w, seed=0)
+    counts = step_shapes(name)
+    inps = {key: make_layer_inputs(**WORKLOADS[key], seed=0) for key in counts}
+    T = next(iter(inps.values())).tokens
     sample = 256
     for _ in range(args.warmup):
-        oracle_sample(inp, sample)
-    vals = []
+        for inp in inps.values():
+            oracle_sample(inp, sample)
     t_all = 0.0
     for _ in range(args.steps):
-        t_fixed, t_tok = oracle_sample(inp, sample)
-        step_s = t_fixed + t_tok * inp.tokens
-        t_all += step_s
-        vals.append(inp.tokens / step_s)
-    value = args.steps * inp.tokens / t_all
+        for key, inp in inps.items():
+            t_fixed, t_tok = oracle_sample(inp, sample)
+            t_all += counts[key] * (t_fixed + t_tok * T)
+    value = args.steps * T / t_all
     cores = blas_threads()
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * t_all / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": config_json(name, w, args.gpus),
+            "config": config_json(name, args.gpus),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": (f"each step: block build + CNP adjoint of both sides "
-                                        f"and forward+backward on {sample} of {inp.tokens} "
-                                        f"tokens, extrapolated linearly in tokens")},
+                                        f"and forward+backward on {sample} of {T} tokens per "
+                                        f"distinct projection shape, extrapolated linearly in "
+                                        f"tokens and weighted by the shape's count")},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -343,15 +382,18 @@ def run_gpu(args):
     poetx.poetx_set_block_epilogue_fusion(args.fuse_epilogue)
 
     name = args.workload
-    w = workload_config(name)
-    inp = make_layer_inputs(**w, seed=rank)
-    dev = to_device(inp)
+    projs = projections(name)
+    counts = step_shapes(name)
+    single = name in WORKLOADS
+    keys = list(counts)
+    w = workload_config(keys[0])  # the (first) projection shape
     stream = torch.cuda.current_stream()
     shared = {}  # per-weight preparation shared by every layer instance
 
-    def make_step(acts):
-        """A layer instance and its step over the activation buffers `acts`
-        (x, dy); every instance has its own outputs and workspace."""
+    def make_step(w, dev, acts):
+        """A layer instance of shape w and its step over the weights and
+        parameters in dev and the activation buffers `acts` (x, dy); every
+        instance has its own outputs and workspace."""
         if args.permute:
             from orthogonal_reparameterized_packed_gb300.layer import PoetxPermutedLayer
             prng = np.random.default_rng(1000 + rank)
@@ -366,12 +408,13 @@ def run_gpu(args):
             from orthogonal_reparameterized_packed_gb300.layer import PoetxQLayer, quantize
             lay = PoetxQLayer(w["d_in"], w["d_out"], w["b"], w["k"], w["tokens"],
                               dtype=w["dtype"], recompute_v=args.recompute_v)
-            if "W0_q" not in shared:  # once per weight
-                shared["W0_q"], shared["scales"] = quantize(dev["W0"], lay.code)
+            wkey = id(dev["W0"])
+            if wkey not in shared:  # once per weight
+                shared[wkey] = quantize(dev["W0"], lay.code)
+            W0_q, scales = shared[wkey]
 
             def fn():
-                lay.step(dev["theta_P"], dev["theta_R"], shared["W0_q"], shared["scales"],
-                         acts["x"], acts["dy"])
+                lay.step(dev["theta_P"], dev["theta_R"], W0_q, scales, acts["x"], acts["dy"])
         else:
             lay = PoetxLayer(w["d_in"], w["d_out"], w["b"], w["k"], w["tokens"],
                              dtype=w["dtype"], recompute_v=args.recompute_v)
@@ -388,7 +431,19 @@ def run_gpu(args):
                     lay.step(dev["theta_P"], dev["theta_R"], dev["W0"], acts["x"], acts["dy"])
         return lay, fn
 
-    layer, step = make_step(dev)
+    insts = {}  # per distinct projection shape: inputs on the device, layer, step
+    for i, key in enumerate(keys):
+        wk = workload_config(key)
+        inp_k = make_layer_inputs(**wk, seed=rank if single else 1000 * rank + i)
+        dev_k = to_device(inp_k)
+        lay_k, fn_k = make_step(wk, dev_k, dev_k)
+        insts[key] = {"w": wk, "dev": dev_k, "layer": lay_k, "step": fn_k}
+    dev, layer = insts[keys[0]]["dev"], insts[keys[0]]["layer"]
+    order = [insts[key]["step"] for _, key in projs]
+
+    def step():
+        for fn in order:
+            fn()
 
     def barrier():
         if world > 1:
@@ -402,21 +457,23 @@ def run_gpu(args):
 
     # (1) eager pass: every launch bracketed by CUDA events on its stream,
     #     giving the per-kernel durations the roofline uses
+    # (a composite step profiles a few steps: its launch count is large)
+    prof_steps = args.steps if single else min(args.steps, 3)
     launches0 = poetx.poetx_launch_count()
-    poetx.poetx_profile_start(64 * args.steps)
+    poetx.poetx_profile_start(16 * len(projs) * prof_steps)
     barrier()
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(prof_steps):
         step()
     t1.record(stream)
     torch.cuda.synchronize()
     barrier()
     poetx.poetx_profile_stop()
-    launches_per_step = (poetx.poetx_launch_count() - launches0) // args.steps
-    ms_eager = t0.elapsed_time(t1) / args.steps
+    launches_per_step = (poetx.poetx_launch_count() - launches0) // prof_steps
+    ms_eager = t0.elapsed_time(t1) / prof_steps
 
     # (2) the same step captured once in a CUDA graph and replayed: the timed
     #     region of the headline number (no host launch overhead between kernels)
@@ -477,59 +534,79 @@ def run_gpu(args):
         if n:
             kernels[t] = {"launches": n, "total_ms": tot, "avg_us": 1e3 * tot / n}
     peaks, peak_src = load_peaks()
+    shapes = [insts[key]["w"] for _, key in projs]  # one entry per projection of the step
+
+    def per_step(fn):
+        return sum(fn(wp) for wp in shapes)
+
+    # the dominant kernel: algorithmic work of all its launches / their summed time
     dom = max((t for t in kernels if algorithmic_work(t, w)), key=lambda t: kernels[t]["total_ms"])
-    amount, unit, bound, formula = algorithmic_work(dom, w)
-    avg_s = kernels[dom]["avg_us"] * 1e-6
-    long_region = ms_eager * args.steps > 1000.0
-    peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
-    achieved = amount / avg_s
+    _, unit, bound, formula = algorithmic_work(dom, w)
+    work = per_step(lambda wp: algorithmic_work(dom, wp)[0])
+    achieved = work * prof_steps / (kernels[dom]["total_ms"] * 1e-3)
+    long_region = ms_eager * prof_steps > 1000.0
+    if w["dtype"] == "bf16":
+        peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
+        peak_note = f"{peak_src} bf16 ({'sustained' if long_region else 'burst'})"
+    else:  # fp32 FFMA on the CUDA cores: 128 lanes x 2 flop per SM per clock
+        bound = "alu"
+        sm_mhz = (clk or {}).get("sm_max_mhz") or 2070.0
+        peak = torch.cuda.get_device_properties(local).multi_processor_count * 128 * 2 * \
+            sm_mhz * 1e6 / 1e12
+        peak_note = f"fp32 FFMA: SMs x 128 lanes x 2 flop x {sm_mhz:.0f} MHz"
     roofline = {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak,
                 "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": captured_traffic(name, dom),
-                "peak_source": f"{peak_src} ({'sustained' if long_region else 'burst'})",
-                "per_launch": f"{formula} = {amount:.4f} TFLOP",
+                "traffic": captured_traffic(name, dom) if single else None,
+                "peak_source": peak_note,
+                "per_launch": (f"{formula} = {work:.4f} TFLOP" if single else
+                               f"{formula} summed over the {len(projs)} projections: "
+                               f"{work:.4f} TFLOP per step"),
                 "timing": "CUDA events around each launch, eager pass of the same K steps"}
 
     # the HBM-bound kernels: algorithmic bytes of all their launches in the
     # timed steps / their summed event time
-    T, di, do = w["tokens"], w["d_in"], w["d_out"]
-    S = max(w["b"], 256)
-    hbm_bytes = {
-        # u = P x and y = R v: read + write bf16 activations, the superblocks
-        "transform": 4.0 * T * (di + do) + 2.0 * S * (di + do),
-        "transform_t": 4.0 * T * (di + do) + 2.0 * S * (di + do),
-        # dv = dy R with sum_t v dy^T, dx = du P with sum_t x du^T: two reads, one write
-        "transform_sum": 6.0 * T * (di + do) + 2.0 * S * (di + do),
-        "outer": 4.0 * T * (di + do),
-        # index maps: 2 over d_in, 2 over d_out, each reads and writes T x d bf16
-        "permute": 8.0 * T * (di + do),
-        # INT8 -> bf16 weight: 1 + 2 bytes per entry
-        "dequantize": 3.0 * di * do,
-    }
+    def hbm_bytes(tag, wp):
+        T, di, do = wp["tokens"], wp["d_in"], wp["d_out"]
+        S = max(wp["b"], 256)
+        return {
+            # u = P x and y = R v: read + write bf16 activations, the superblocks
+            "transform": 4.0 * T * (di + do) + 2.0 * S * (di + do),
+            "transform_t": 4.0 * T * (di + do) + 2.0 * S * (di + do),
+            # dv = dy R with sum_t v dy^T, dx = du P with sum_t x du^T: two reads, one write
+            "transform_sum": 6.0 * T * (di + do) + 2.0 * S * (di + do),
+            "outer": 4.0 * T * (di + do),
+            # index maps: 2 over d_in, 2 over d_out, each reads and writes T x d bf16
+            "permute": 8.0 * T * (di + do),
+            # INT8 -> bf16 weight: 1 + 2 bytes per entry
+            "dequantize": 3.0 * di * do,
+        }[tag]
+
     hbm = []
-    for tag, per_step in hbm_bytes.items():
-        if tag in kernels:
+    for tag in ("transform", "transform_t", "transform_sum", "outer", "permute", "dequantize"):
+        if tag in kernels and w["dtype"] == "bf16":
             kt = kernels[tag]
-            gbs = per_step * args.steps / (kt["total_ms"] * 1e-3) / 1e9
+            bytes_step = per_step(lambda wp: hbm_bytes(tag, wp))
+            gbs = bytes_step * prof_steps / (kt["total_ms"] * 1e-3) / 1e9
             hbm.append({"kernel": tag, "bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
                         "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
-                        "bytes_per_step": per_step, "traffic": captured_traffic(name, tag)})
+                        "bytes_per_step": bytes_step,
+                        "traffic": captured_traffic(name, tag) if single else None})
     roofline["hbm_kernels"] = hbm
 
     merge = None
-    if args.train_step and not args.permute and not args.w0_int8:
+    if single and args.train_step and not args.permute and not args.w0_int8:
         merge = time_merge(poetx, layer, dev, w, stream, peaks)
 
     # whole step against the HBM floor of a fully fused layer: x, y, v in the
     # forward, dy, v, x in and dx out in the backward (bf16), W0 read twice
-    min_step_bytes = (T * ((2 * di + 4 * do) + (4 * di + 4 * do)) + 2 * 2.0 * di * do
+    min_step_bytes = (per_step(lambda wp: wp["tokens"] * ((2 * wp["d_in"] + 4 * wp["d_out"]) +
+                                                          (4 * wp["d_in"] + 4 * wp["d_out"])) +
+                               4.0 * wp["d_in"] * wp["d_out"])
                       if w["dtype"] == "bf16" else None)
 
     # whole-step algorithmic tensor work for context
-    T, di, do, b = w["tokens"], w["d_in"], w["d_out"], w["b"]
-    step_flop = T * (4.0 * di * do + 6.0 * b * (di + do))
-
-    total_tokens = world * w["tokens"]
+    step_flop = per_step(lambda wp: wp["tokens"] * (4.0 * wp["d_in"] * wp["d_out"] +
+                                                    6.0 * wp["b"] * (wp["d_in"] + wp["d_out"])))
     value = job_throughput(w["tokens"], world, ms_max)
 
     # end to end through the C ABI from pinned host buffers: every step's x and
@@ -537,13 +614,13 @@ def run_gpu(args):
     # region.  Two buffer sets: step i+1's inputs upload (copy stream) while
     # step i computes, and step i's dtheta reads back during step i+1.
     e2e = None
-    if not args.no_e2e:
+    if single and not args.no_e2e:
         hx = dev["x"].cpu().pin_memory()
         hdy = dev["dy"].cpu().pin_memory()
         acts2 = {"x": torch.empty_like(dev["x"]), "dy": torch.empty_like(dev["dy"])}
         acts2["x"].copy_(dev["x"])
         acts2["dy"].copy_(dev["dy"])
-        layer2, step2 = make_step(acts2)
+        layer2, step2 = make_step(w, dev, acts2)
         step2()
         torch.cuda.synchronize()
         run_step2, _ = capture(step2)
@@ -608,13 +685,14 @@ def run_gpu(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(inp, 2048)
+        cpu = cpu_baseline(name, 2048 if single else 512, seed=rank)
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
                 "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": ms_max,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": "bf16", "data": "synthetic", "config": config_json(name, w, world, args),
+                "dtype": w["dtype"].replace("f32", "fp32"), "data": "synthetic",
+                "config": config_json(name, world, args),
                 "gpu_launches": launches, "launch": "cuda_graph" if graph is not None else "eager",
                 "graph_error": graph_error,
                 "ms_per_step_eager": ms_eager, "roofline": roofline,

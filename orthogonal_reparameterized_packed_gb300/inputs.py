@@ -99,7 +99,26 @@ WORKLOADS = {
     "llama3_8b_down": dict(d_in=14336, d_out=4096, b=256, k=3, tokens=16384, dtype="bf16"),
 }
 
+# 1.3B-shaped Llama-style model (d_model 2048, ffn 5632), 16384 tokens (batch 8 x seq 2048)
+WORKLOADS.update({
+    "llama_1p3b_attn": dict(d_in=2048, d_out=2048, b=256, k=3, tokens=16384, dtype="bf16"),
+    "llama_1p3b_up": dict(d_in=2048, d_out=5632, b=256, k=3, tokens=16384, dtype="bf16"),
+    "llama_1p3b_down": dict(d_in=5632, d_out=2048, b=256, k=3, tokens=16384, dtype="bf16"),
+})
+
 # Llama-3-8B decoder block: the seven projections (name, workload key)
 LLAMA3_8B_BLOCK = [("q", "llama3_8b_qo"), ("k", "llama3_8b_kv"), ("v", "llama3_8b_kv"),
                    ("o", "llama3_8b_qo"), ("gate", "llama3_8b_gate_up"),
                    ("up", "llama3_8b_gate_up"), ("down", "llama3_8b_down")]
+
+# one layer of the 1.3B-shaped model; the model has 24 of them (168 projections)
+LLAMA_1P3B_LAYER = [("q", "llama_1p3b_attn"), ("k", "llama_1p3b_attn"), ("v", "llama_1p3b_attn"),
+                    ("o", "llama_1p3b_attn"), ("gate", "llama_1p3b_up"), ("up", "llama_1p3b_up"),
+                    ("down", "llama_1p3b_down")]
+
+# workloads made of several projections run one after another in a step
+# (all with the same token count): (projection name, workload key) lists
+COMPOSITES = {
+    "llama3_8b_block": LLAMA3_8B_BLOCK,
+    "llama_1p3b_model": [(f"L{i}.{n}", key) for i in range(24) for n, key in LLAMA_1P3B_LAYER],
+}
