@@ -53,6 +53,7 @@ struct ChainTerm {
   int a_map, b_map;  // A: K-major box map, B: MN-major box map
   int b_batched;     // B rows offset by g * b (0: one constant b x b matrix)
   int diag;          // B is diagonal (2I): only the K steps of the tile's own columns count
+  int dep;           // lazy phases: the phase whose outputs this term reads (-1: none)
 };
 
 // K steps [k0, k1) of a term for output column tile nt
@@ -72,6 +73,11 @@ struct ChainProd {
 
 struct ChainPhase {
   int nprod;
+  // lazy: the producer waits for each term's own dependency instead of for
+  // the previous phase, so terms that read only the inputs (listed first)
+  // load and multiply while the grid barrier is still open.  Only for phases
+  // that overwrite nothing a running phase still reads.
+  int lazy;
   ChainProd prod[2];
 };
 
@@ -183,19 +189,31 @@ __global__ void __launch_bounds__(CH_THREADS, 1) chain_kernel(const __grid_const
       uint32_t phase_bit = 0;
       long long issued = 0;
       bool ok = true;
+      int waited = 0;  // phases known complete on the whole grid
       for (int ph = 0; ph < P.nphases && ok; ++ph) {
         const ChainPhase& PH = P.phases[ph];
-        if (!grid_wait(P, ph, abort_flag)) {
-          ok = false;
-          break;
+        if (!PH.lazy && ph > waited) {
+          if (!grid_wait(P, ph, abort_flag)) {
+            ok = false;
+            break;
+          }
+          waited = ph;
+          fence_proxy_async_global();  // generic writes of earlier phases -> TMA reads
         }
-        fence_proxy_async_global();  // generic writes of earlier phases -> TMA reads
         const int tiles = PH.nprod * P.n * mtl * ntl;
         for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
           int prod, g, mt, nt;
           decode_chain_tile(t, P.n, mtl, ntl, prod, g, mt, nt);
           const ChainProd& PR = PH.prod[prod];
           for (int term = 0; term < PR.nterms && ok; ++term) {
+            if (PH.lazy && PR.term[term].dep + 1 > waited) {
+              if (!grid_wait(P, PR.term[term].dep + 1, abort_flag)) {
+                ok = false;
+                break;
+              }
+              waited = PR.term[term].dep + 1;
+              fence_proxy_async_global();
+            }
             const CUtensorMap* ma = &P.maps[PR.term[term].a_map];
             const CUtensorMap* mb = &P.maps[PR.term[term].b_map];
             const int b_row0 = PR.term[term].b_batched ? g * b : 0;
@@ -418,6 +436,12 @@ ChainTerm term(int a_map, int b_map, bool b_batched) {
   t.b_map = b_map + 1;  // MN-major box
   t.b_batched = b_batched ? 1 : 0;
   t.diag = 0;
+  t.dep = -1;
+  return t;
+}
+
+ChainTerm dep_on(ChainTerm t, int phase) {
+  t.dep = phase;
   return t;
 }
 
@@ -538,13 +562,14 @@ cudaError_t chain_build(const ChainBuildArgs& a, cudaStream_t stream) {
     P1.epi = chain_epi(b);
     P1.epi.out_bf16 = a.e16[0];
     ChainProd& P2 = P.phases[ph].prod[0];
+    P.phases[ph].lazy = 1;  // Q_hi 2I, Q_lo 2I need no phase-1 output
     P.phases[ph++].nprod = 1;
     P2.nterms = 5;
     P2.term[0] = term_2i(hi, two);
     P2.term[1] = term_2i(lo, two);
-    P2.term[2] = term_2i(q2, two);
-    P2.term[3] = term(hi2, q2, true);
-    P2.term[4] = term(q2, q2, true);
+    P2.term[2] = dep_on(term_2i(q2, two), 0);
+    P2.term[3] = dep_on(term(hi2, q2, true), 0);
+    P2.term[4] = dep_on(term(q2, q2, true), 0);
     P2.mode = PROD_STORE;
     P2.epi = chain_epi(b);
     P2.epi.delta = 1.f;
@@ -643,21 +668,23 @@ cudaError_t chain_adjoint(const ChainAdjointArgs& a, cudaStream_t stream) {
     P1.prod[1].epi.out_bf16 = a.e16[3];
     ChainProd& P2 = P.phases[1].prod[0];
     P.phases[1].nprod = 1;
+    P.phases[1].lazy = 1;  // H 2I and (2Q) H need no phase-1 output
     P2.nterms = 4;
     P2.term[0] = term_2i(h, two);
     P2.term[1] = term(x, h, true);
-    P2.term[2] = term(q2, h, true);
-    P2.term[3] = term(h, q2, true);
+    P2.term[2] = dep_on(term(q2, h, true), 0);
+    P2.term[3] = dep_on(term(h, q2, true), 0);
     P2.mode = PROD_STORE;
     P2.epi = chain_epi(b);
     P2.epi.out_bf16 = a.f16[1];
     ChainProd& P3 = P.phases[2].prod[0];
     P.phases[2].nprod = 1;
+    P.phases[2].lazy = 1;
     P3.nterms = 4;
     P3.term[0] = term_2i(h, two);
-    P3.term[1] = term(h, q2d, true);
-    P3.term[2] = term(q, d2, true);
-    P3.term[3] = term(d2, q, true);
+    P3.term[1] = dep_on(term(h, q2d, true), 0);
+    P3.term[2] = dep_on(term(q, d2, true), 1);
+    P3.term[3] = dep_on(term(d2, q, true), 1);
     P3.mode = PROD_STORE;
     P3.epi = chain_epi(b);
     P3.epi.out_f32 = a.d32;
