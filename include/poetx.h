@@ -177,11 +177,13 @@ poetx_status poetx_transform_backward(const void* dout, const void* x, const flo
  * A permuted step is: x' = Pi_P x, the plain forward/backward on
  * (x', W0', blocks), y = Pi_R^T y', dy' = Pi_R dy, dx = Pi_P^T dx'; the
  * packed gradients come out of the plain backward unchanged.
- *   perm arrays: int32 device arrays holding a permutation of 0..d-1;
- *   (Pi x)[i] = x[perm[i]], so Pi^T is applied with the inverse permutation.
+ *   perm arrays: int32 device arrays holding a permutation of 0..d-1
+ *   (16-byte aligned like every other pointer; perm_out of the fold needs
+ *   only 4); (Pi x)[i] = x[perm[i]], so Pi^T is applied with the inverse
+ *   permutation.
  *   Entries outside 0..d-1 are not followed: the output gets 0 and
  *   POETX_ERR_INVALID_ARG is recorded in the status word.  Rows must be a
- *   multiple of 16 bytes and at most 100 KiB (d <= 51200 bf16, 25600 fp32).
+ *   multiple of 16 bytes and d <= 25600 (INVALID_ARG otherwise).
  * ------------------------------------------------------------------------ */
 /* out[r][i] = in[r][perm[i]] for rows x d activations (in != out). */
 poetx_status poetx_permute_features(const void* in, const int32_t* perm, void* out, int64_t rows,

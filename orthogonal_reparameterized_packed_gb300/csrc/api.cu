@@ -1238,15 +1238,19 @@ poetx_status poetx_build_blocks_noalloc(const float* theta, int d, int b, int k,
       run_build(theta, d / b, b, k, is_bf16, blocks, w, static_cast<cudaStream_t>(stream)));
 }
 
+// The index-map kernel keeps one 8-byte entry per feature (4 bf16 or 2 fp32
+// rows interleaved) in 200 KiB of shared memory.
+constexpr int kMaxPermuteFeatures = 25600;
+
 poetx_status poetx_permute_features(const void* in, const int32_t* perm, void* out, int64_t rows,
                                     int d, poetx_dtype dtype, poetx_stream stream) {
   const bool is_bf16 = dtype == POETX_BF16;
   if (dtype != POETX_F32 && dtype != POETX_BF16) return POETX_ERR_INVALID_ARG;
-  if (rows < 0 || d <= 0 || (d * (is_bf16 ? 2 : 4)) % 16 != 0 || d * (is_bf16 ? 2 : 4) > 100 * 1024)
+  if (rows < 0 || d <= 0 || (d * (is_bf16 ? 2 : 4)) % 16 != 0 || d > kMaxPermuteFeatures)
     return POETX_ERR_INVALID_ARG;
   if (rows == 0) return POETX_OK;
   if (in == nullptr || perm == nullptr || out == nullptr || in == out || !aligned16(in) ||
-      !aligned16(out) || (reinterpret_cast<uintptr_t>(perm) & 3u) != 0)
+      !aligned16(out) || !aligned16(perm))  // the column map is read as 16-byte vectors
     return POETX_ERR_INVALID_ARG;
   return to_status(launch_permute_rows(in, rows, nullptr, perm, out, rows, d, is_bf16,
                                        static_cast<cudaStream_t>(stream)));
@@ -1258,12 +1262,11 @@ poetx_status poetx_fold_permutations(const void* W0, const int32_t* perm_out,
   const bool is_bf16 = dtype == POETX_BF16;
   if (dtype != POETX_F32 && dtype != POETX_BF16) return POETX_ERR_INVALID_ARG;
   if (d_in <= 0 || d_out <= 0 || (d_in * (is_bf16 ? 2 : 4)) % 16 != 0 ||
-      d_in * (is_bf16 ? 2 : 4) > 100 * 1024)
+      d_in > kMaxPermuteFeatures)
     return POETX_ERR_INVALID_ARG;
   if (W0 == nullptr || perm_out == nullptr || perm_in == nullptr || W0_folded == nullptr ||
       W0 == W0_folded || !aligned16(W0) || !aligned16(W0_folded) ||
-      (reinterpret_cast<uintptr_t>(perm_out) & 3u) != 0 ||
-      (reinterpret_cast<uintptr_t>(perm_in) & 3u) != 0)
+      (reinterpret_cast<uintptr_t>(perm_out) & 3u) != 0 || !aligned16(perm_in))
     return POETX_ERR_INVALID_ARG;
   return to_status(launch_permute_rows(W0, d_out, perm_out, perm_in, W0_folded, d_out, d_in,
                                        is_bf16, static_cast<cudaStream_t>(stream)));

@@ -3,6 +3,8 @@
 // tolerance, and for blocks narrower than one 128-wide MMA tile), plus the
 // small elementwise kernels of the path (unpack, superblock expansion,
 // split-K reduction, skew projection and pack).
+#include <type_traits>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -362,13 +364,16 @@ __global__ void __launch_bounds__(256) pack_tiles_kernel(const float* __restrict
 }
 
 // out[r][i] = in[row_map ? row_map[r] : r][col_map[i]] for r < rows, i < d.
-// One warp per row: the warp reads its source row with 16-byte coalesced
-// loads into its own slice of shared memory, then each lane gathers 16 bytes
-// of consecutive outputs (column map read as 16-byte vectors) and writes them
-// with one 16-byte store.  Only __syncwarp separates the two halves, so the
-// eight warps of a CTA stream rows independently.  Map entries outside
-// [0, d) (or [0, in_rows)) are not followed: the output gets 0 and the
-// status word POETX_ERR_INVALID_ARG.
+// One warp per group of R rows (R = 8 bytes / element: 4 bf16 or 2 fp32
+// rows): the warp reads its R source rows with 16-byte coalesced loads and
+// writes them into shared memory interleaved, one 8-byte entry per column
+// holding that column of all R rows; each lane then gathers 8-byte entries
+// at the mapped columns (column map read as 16-byte vectors), so one random
+// shared-memory read serves R outputs, and writes each row's 16 bytes of
+// consecutive outputs with one 16-byte store.  Only __syncwarp separates the
+// two halves, so the warps of a CTA stream rows independently.  Map entries
+// outside [0, d) (or [0, in_rows)) are not followed: the output gets 0 and
+// the status word POETX_ERR_INVALID_ARG.
 constexpr int kPermWarps = 8;
 
 template <typename T>
@@ -380,26 +385,69 @@ __global__ void __launch_bounds__(kPermWarps * 32)
   pdl_trigger();
   extern __shared__ __align__(16) unsigned char row_smem[];
   constexpr int V = 16 / sizeof(T);  // elements per 16-byte vector
+  constexpr int R = 8 / sizeof(T);   // rows per warp group: one 8-byte entry per column
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  T* rb = reinterpret_cast<T*>(row_smem) + static_cast<long long>(warp) * d;
+  uint2* ent = reinterpret_cast<uint2*>(row_smem) + static_cast<long long>(warp) * d;
   const int nv = d / V;
   const int nwarps = blockDim.x / 32;
+  const long long groups = (rows + R - 1) / R;
   const long long wstride = static_cast<long long>(gridDim.x) * nwarps;
-  for (long long r = static_cast<long long>(blockIdx.x) * nwarps + warp; r < rows;
-       r += wstride) {
-    long long src = r;
-    if (row_map != nullptr) {
-      const int m = row_map[r];
-      src = (m >= 0 && m < in_rows) ? m : -1;
-      if (src < 0 && lane == 0) atomicCAS(status, 0, 1);
+  for (long long grp = static_cast<long long>(blockIdx.x) * nwarps + warp; grp < groups;
+       grp += wstride) {
+    const long long r0 = grp * R;
+    long long src[R];
+    bool any_bad_row = false;
+#pragma unroll
+    for (int q = 0; q < R; ++q) {
+      const long long r = r0 + q;
+      src[q] = -1;
+      if (r < rows) {
+        src[q] = r;
+        if (row_map != nullptr) {
+          const int m = row_map[r];
+          src[q] = (m >= 0 && m < in_rows) ? m : -1;
+          any_bad_row |= src[q] < 0;
+        }
+      }
     }
-    if (src >= 0) {
-      const uint4* s4 = reinterpret_cast<const uint4*>(in + src * d);
-      uint4* b4 = reinterpret_cast<uint4*>(rb);
-      for (int v = lane; v < nv; v += 32) b4[v] = s4[v];
+    if (any_bad_row && lane == 0) atomicCAS(status, 0, 1);
+    // interleave: entry j holds column j of the R rows (missing rows: 0);
+    // bf16: (r0 | r1 << 16, r2 | r3 << 16), fp32: (r0, r1)
+    for (int v = lane; v < nv; v += 32) {
+      uint32_t w[R][4];
+#pragma unroll
+      for (int q = 0; q < R; ++q) {
+        uint4 u = make_uint4(0u, 0u, 0u, 0u);
+        if (src[q] >= 0) u = reinterpret_cast<const uint4*>(in + src[q] * d)[v];
+        w[q][0] = u.x;
+        w[q][1] = u.y;
+        w[q][2] = u.z;
+        w[q][3] = u.w;
+      }
+      // word i of row q, i chosen at run time, by selects (no local memory)
+      auto pick = [&](int q, int i) {
+        uint32_t r = w[q][0];
+        r = i == 1 ? w[q][1] : r;
+        r = i == 2 ? w[q][2] : r;
+        r = i == 3 ? w[q][3] : r;
+        return r;
+      };
+#pragma unroll
+      for (int k = 0; k < V; ++k) {
+        const int e = (k + lane) & (V - 1);  // rotated order spreads the banks
+        uint2 entry;
+        if constexpr (sizeof(T) == 2) {
+          const int sh = 16 * (e & 1);
+          entry.x = ((pick(0, e >> 1) >> sh) & 0xffffu) | (((pick(1, e >> 1) >> sh) & 0xffffu) << 16);
+          entry.y = ((pick(2, e >> 1) >> sh) & 0xffffu) | (((pick(3, e >> 1) >> sh) & 0xffffu) << 16);
+        } else {
+          entry.x = pick(0, e);
+          entry.y = pick(1, e);
+        }
+        ent[v * V + e] = entry;
+      }
     }
     __syncwarp();
-    uint4* o4 = reinterpret_cast<uint4*>(out + r * d);
     const int4* c4 = reinterpret_cast<const int4*>(col_map);
     for (int v = lane; v < nv; v += 32) {
       int cols[V];
@@ -411,18 +459,40 @@ __global__ void __launch_bounds__(kPermWarps * 32)
         cols[4 * q + 2] = c.z;
         cols[4 * q + 3] = c.w;
       }
-      alignas(16) T vals[V];
+      uint32_t o[R][4];
+#pragma unroll
+      for (int q = 0; q < R; ++q)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[q][i] = 0u;
       bool bad = false;
 #pragma unroll
       for (int e = 0; e < V; ++e) {
-        const bool in_range = src >= 0 && cols[e] >= 0 && cols[e] < d;
-        bad |= src >= 0 && !in_range;
-        vals[e] = in_range ? rb[cols[e]] : T(0.f);
+        const bool in_range = cols[e] >= 0 && cols[e] < d;
+        bad |= !in_range;
+        uint2 u = make_uint2(0u, 0u);
+        if (in_range) u = ent[cols[e]];
+        if constexpr (sizeof(T) == 2) {
+          const int sh = 16 * (e & 1);
+          o[0][e >> 1] |= (u.x & 0xffffu) << sh;
+          o[1][e >> 1] |= (u.x >> 16) << sh;
+          o[2][e >> 1] |= (u.y & 0xffffu) << sh;
+          o[3][e >> 1] |= (u.y >> 16) << sh;
+        } else {
+          o[0][e] = u.x;
+          o[1][e] = u.y;
+        }
       }
       if (bad) atomicCAS(status, 0, 1);
-      o4[v] = *reinterpret_cast<const uint4*>(vals);
+#pragma unroll
+      for (int q = 0; q < R; ++q) {
+        if (r0 + q < rows) {
+          uint4 val = make_uint4(o[q][0], o[q][1], o[q][2], o[q][3]);
+          if (src[q] < 0) val = make_uint4(0u, 0u, 0u, 0u);
+          reinterpret_cast<uint4*>(out + (r0 + q) * d)[v] = val;
+        }
+      }
     }
-    __syncwarp();  // the row buffer is free for the next row
+    __syncwarp();  // the entries are free for the next group
   }
 }
 
@@ -642,14 +712,16 @@ cudaError_t launch_permute_rows(const void* in, long long in_rows, const int* ro
                                 const int* col_map, void* out, long long rows, int d,
                                 bool is_bf16, cudaStream_t s) {
   if (rows <= 0 || d <= 0) return cudaSuccess;
-  const size_t row_bytes = static_cast<size_t>(d) * (is_bf16 ? 2 : 4);
-  if (row_bytes > 100 * 1024) return cudaErrorInvalidValue;
-  int warps = static_cast<int>((200 * 1024) / row_bytes);  // one row buffer per warp
+  const size_t group_bytes = static_cast<size_t>(d) * 8;  // one 8-byte entry per column
+  if (group_bytes > 200 * 1024) return cudaErrorInvalidValue;
+  int warps = static_cast<int>((200 * 1024) / group_bytes);  // one group buffer per warp
   if (warps > kPermWarps) warps = kPermWarps;
-  const size_t smem = row_bytes * warps;
-  const long long groups = (rows + warps - 1) / warps;
+  const size_t smem = group_bytes * warps;
+  const int R = is_bf16 ? 4 : 2;
+  const long long groups = (rows + R - 1) / R;
+  const long long ctas = (groups + warps - 1) / warps;
   const long long cap = static_cast<long long>(sm_count()) * 8;
-  const dim3 grid(static_cast<unsigned>(groups < cap ? groups : cap));
+  const dim3 grid(static_cast<unsigned>(ctas < cap ? ctas : cap));
   cudaError_t e;
   prof_begin("permute", s);
   if (is_bf16) {

@@ -167,3 +167,17 @@ def test_int8_weight_calls_reject_invalid_arguments(lib):
         assert fn(FAKE, None, FAKE, 64, 64, poetx.F32, None) == 1
         assert fn(FAKE, FAKE, None, 64, 64, poetx.F32, None) == 1
         assert fn(None, None, None, 0, 64, poetx.BF16, None) == 0  # empty: nothing to do
+
+
+def test_index_map_calls_reject_invalid_arguments(lib):
+    L = _raw()
+    B, F = poetx.BF16, poetx.F32
+    # d beyond the shared-memory entry table, d * element size not a multiple of 16
+    assert L.poetx_permute_features(FAKE, FAKE, FAKE + 4096, 8, 25600 + 8, B, None) == 1
+    assert L.poetx_permute_features(FAKE, FAKE, FAKE + 4096, 8, 12, B, None) == 1
+    # the column map is read as 16-byte vectors
+    assert L.poetx_permute_features(FAKE, FAKE + 4, FAKE + 4096, 8, 64, B, None) == 1
+    assert L.poetx_permute_features(FAKE, FAKE, FAKE, 8, 64, B, None) == 1  # in == out
+    assert L.poetx_permute_features(None, None, None, 0, 64, F, None) == 0  # no rows
+    assert L.poetx_fold_permutations(FAKE, FAKE, FAKE + 4, FAKE + 4096, 64, 64, B, None) == 1
+    assert L.poetx_fold_permutations(FAKE, FAKE, FAKE, FAKE + 4096, 25608, 64, B, None) == 1
