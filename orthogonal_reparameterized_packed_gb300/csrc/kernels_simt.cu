@@ -364,20 +364,20 @@ __global__ void __launch_bounds__(256) pack_tiles_kernel(const float* __restrict
 }
 
 // out[r][i] = in[row_map ? row_map[r] : r][col_map[i]] for r < rows, i < d.
-// One warp per group of R rows (R = 8 bytes / element: 4 bf16 or 2 fp32
-// rows): the warp reads its R source rows with 16-byte coalesced loads and
-// writes them into shared memory interleaved, one 8-byte entry per column
-// holding that column of all R rows; each lane then gathers 8-byte entries
+// One CTA per group of R rows at a time (R = 8 bytes / element: 4 bf16 or 2
+// fp32 rows): the CTA reads its R source rows with 16-byte coalesced loads
+// and writes them into shared memory interleaved, one 8-byte entry per column
+// holding that column of all R rows; each thread then gathers 8-byte entries
 // at the mapped columns (column map read as 16-byte vectors), so one random
 // shared-memory read serves R outputs, and writes each row's 16 bytes of
-// consecutive outputs with one 16-byte store.  Only __syncwarp separates the
-// two halves, so the warps of a CTA stream rows independently.  Map entries
-// outside [0, d) (or [0, in_rows)) are not followed: the output gets 0 and
-// the status word POETX_ERR_INVALID_ARG.
-constexpr int kPermWarps = 8;
+// consecutive outputs with one 16-byte store.  The d x 8-byte table is small
+// enough for several CTAs per SM, whose groups overlap one another's loads.
+// Map entries outside [0, d) (or [0, in_rows)) are not followed: the output
+// gets 0 and the status word POETX_ERR_INVALID_ARG.
+constexpr int kPermThreads = 256;
 
 template <typename T>
-__global__ void __launch_bounds__(kPermWarps * 32)
+__global__ void __launch_bounds__(kPermThreads)
     permute_rows_kernel(const T* __restrict__ in, long long in_rows,
                         const int* __restrict__ row_map, const int* __restrict__ col_map,
                         T* __restrict__ out, long long rows, int d, int* status) {
@@ -385,15 +385,12 @@ __global__ void __launch_bounds__(kPermWarps * 32)
   pdl_trigger();
   extern __shared__ __align__(16) unsigned char row_smem[];
   constexpr int V = 16 / sizeof(T);  // elements per 16-byte vector
-  constexpr int R = 8 / sizeof(T);   // rows per warp group: one 8-byte entry per column
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  uint2* ent = reinterpret_cast<uint2*>(row_smem) + static_cast<long long>(warp) * d;
+  constexpr int R = 8 / sizeof(T);   // rows per group: one 8-byte entry per column
+  const int lane = threadIdx.x % 32;
+  uint2* ent = reinterpret_cast<uint2*>(row_smem);
   const int nv = d / V;
-  const int nwarps = blockDim.x / 32;
   const long long groups = (rows + R - 1) / R;
-  const long long wstride = static_cast<long long>(gridDim.x) * nwarps;
-  for (long long grp = static_cast<long long>(blockIdx.x) * nwarps + warp; grp < groups;
-       grp += wstride) {
+  for (long long grp = blockIdx.x; grp < groups; grp += gridDim.x) {
     const long long r0 = grp * R;
     long long src[R];
     bool any_bad_row = false;
@@ -410,10 +407,10 @@ __global__ void __launch_bounds__(kPermWarps * 32)
         }
       }
     }
-    if (any_bad_row && lane == 0) atomicCAS(status, 0, 1);
+    if (any_bad_row && threadIdx.x == 0) atomicCAS(status, 0, 1);
     // interleave: entry j holds column j of the R rows (missing rows: 0);
     // bf16: (r0 | r1 << 16, r2 | r3 << 16), fp32: (r0, r1)
-    for (int v = lane; v < nv; v += 32) {
+    for (int v = threadIdx.x; v < nv; v += kPermThreads) {
       uint32_t w[R][4];
 #pragma unroll
       for (int q = 0; q < R; ++q) {
@@ -447,9 +444,9 @@ __global__ void __launch_bounds__(kPermWarps * 32)
         ent[v * V + e] = entry;
       }
     }
-    __syncwarp();
+    __syncthreads();
     const int4* c4 = reinterpret_cast<const int4*>(col_map);
-    for (int v = lane; v < nv; v += 32) {
+    for (int v = threadIdx.x; v < nv; v += kPermThreads) {
       int cols[V];
 #pragma unroll
       for (int q = 0; q < V / 4; ++q) {
@@ -492,7 +489,7 @@ __global__ void __launch_bounds__(kPermWarps * 32)
         }
       }
     }
-    __syncwarp();  // the entries are free for the next group
+    __syncthreads();  // the entries are free for the next group
   }
 }
 
@@ -712,16 +709,16 @@ cudaError_t launch_permute_rows(const void* in, long long in_rows, const int* ro
                                 const int* col_map, void* out, long long rows, int d,
                                 bool is_bf16, cudaStream_t s) {
   if (rows <= 0 || d <= 0) return cudaSuccess;
-  const size_t group_bytes = static_cast<size_t>(d) * 8;  // one 8-byte entry per column
-  if (group_bytes > 200 * 1024) return cudaErrorInvalidValue;
-  int warps = static_cast<int>((200 * 1024) / group_bytes);  // one group buffer per warp
-  if (warps > kPermWarps) warps = kPermWarps;
-  const size_t smem = group_bytes * warps;
+  const size_t smem = static_cast<size_t>(d) * 8;  // one 8-byte entry per column
+  if (smem > 200 * 1024) return cudaErrorInvalidValue;
   const int R = is_bf16 ? 4 : 2;
   const long long groups = (rows + R - 1) / R;
-  const long long ctas = (groups + warps - 1) / warps;
-  const long long cap = static_cast<long long>(sm_count()) * 8;
-  const dim3 grid(static_cast<unsigned>(ctas < cap ? ctas : cap));
+  long long per_sm = (228 * 1024) / static_cast<long long>(smem + 1024);
+  if (per_sm > 2048 / kPermThreads) per_sm = 2048 / kPermThreads;
+  if (per_sm < 1) per_sm = 1;
+  const long long cap = static_cast<long long>(sm_count()) * per_sm;
+  const dim3 grid(static_cast<unsigned>(groups < cap ? groups : cap));
+  const int warps = kPermThreads / 32;
   cudaError_t e;
   prof_begin("permute", s);
   if (is_bf16) {
