@@ -66,10 +66,6 @@ constexpr int kBlockKSteps = 256 / BK;  // K steps of the epilogue's 256 x 256 b
 struct TcKernelArgs {
   int m_tiles, n_tiles, splits, batches;
   int m_pairs;  // CL2: pairs of M tiles, one per cluster of two CTAs
-  // Work units [0, full_units) are whole tiles; each later unit is done as two
-  // half-width (N = BN / 2) items, so a last partial wave of whole tiles
-  // becomes a full wave of halves.
-  int full_units;
   int k_steps_total, k_steps_per_split;
   int a_mn_per_g, a_k_per_g, b_mn_per_g, b_k_per_g;
   EpiArgs epi;
@@ -176,9 +172,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                    const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC,
                    const __grid_constant__ CUtensorMap tmR,
-                   const __grid_constant__ CUtensorMap tmY,
-                   const __grid_constant__ CUtensorMap tmBh,  // half-width items' B (K-major)
-                   const TcKernelArgs p) {
+                   const __grid_constant__ CUtensorMap tmY, const TcKernelArgs p) {
   using S = TcShape<BN, B_RES, EPI>;
   static_assert(!CL2 || (EPI == EPI_TMA_BF16 && !B_RES && BN == 256), "clusters: W0 GEMMs");
   extern __shared__ uint8_t smem_raw[];
@@ -204,19 +198,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const uint32_t crank = CL2 ? cluster_ctarank() : 0u;
-  constexpr bool HALVES = EPI == EPI_TMA_BF16 && !B_RES && BN == 256;
-  const int num_units = p.batches * p.splits * (CL2 ? p.m_pairs : p.m_tiles) * p.n_tiles;
-  const int num_tiles = HALVES ? p.full_units + 2 * (num_units - p.full_units) : num_units;
+  const int num_tiles = p.batches * p.splits * (CL2 ? p.m_pairs : p.m_tiles) * p.n_tiles;
   const TileRange<B_RES, CL2> range(num_tiles);
-  // work item -> unit and half (-1: the whole N tile, 0/1: that half of it)
-  auto item_unit = [&](int item, int& half) {
-    if (!HALVES || item < p.full_units) {
-      half = -1;
-      return item;
-    }
-    half = (item - p.full_units) & 1;
-    return p.full_units + ((item - p.full_units) >> 1);
-  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -243,7 +226,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tma_prefetch_desc(&tmR);
       tma_prefetch_desc(&tmY);
     }
-    if (HALVES && !B_MN) tma_prefetch_desc(&tmBh);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, S::TMEM_COLS);
@@ -292,12 +274,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         return true;
       };
       for (int tile = range.first; tile < range.end && ok; tile += range.step) {
-        int g, sp, mt, nt, half;
-        decode_unit<B_RES, CL2>(item_unit(tile, half), p, crank, g, sp, mt, nt);
+        int g, sp, mt, nt;
+        decode_unit<B_RES, CL2>(tile, p, crank, g, sp, mt, nt);
         const int ks0 = sp * p.k_steps_per_split;
         const int ks1 = min(ks0 + p.k_steps_per_split, p.k_steps_total);
         const int a_mn = g * p.a_mn_per_g + mt * BM;
-        const int b_mn = g * p.b_mn_per_g + nt * BN + (half > 0 ? BN / 2 : 0);
+        const int b_mn = g * p.b_mn_per_g + nt * BN;
         if (B_RES) {
           const int key = g * p.n_tiles + nt;
           if (key != res_key) {
@@ -329,8 +311,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full_bar[stage],
-                                S::A_BYTES + (B_RES ? 0 : (half >= 0 ? S::B_BYTES / 2 : S::B_BYTES)));
+          mbar_arrive_expect_tx(&full_bar[stage], S::A_BYTES + (B_RES ? 0 : S::B_BYTES));
           const int a_k = g * p.a_k_per_g + ks * BK;
           uint8_t* a_dst = sA + stage * S::A_BYTES;
           if (!A_MN) {
@@ -339,25 +320,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tma_load_2d(a_dst, &tmA, &full_bar[stage], a_mn, a_k);
             tma_load_2d(a_dst + 8192, &tmA, &full_bar[stage], a_mn + 64, a_k);
           }
-          if (HALVES && half >= 0) {
-            // half-width item: B rows (K-major) or columns (MN-major) of one half
-            const int b_k = g * p.b_k_per_g + ks * BK;
-            uint8_t* b_dst = sB + stage * S::B_BYTES;
-            if (CL2) {  // each CTA loads half of the half, delivered to both
-              if (!B_MN)
-                tma_load_2d_mc(b_dst + crank * (BN / 4) * 128, &tmBh, &full_bar[stage], b_k,
-                               b_mn + static_cast<int>(crank) * (BN / 4), 0x3);
-              else
-                tma_load_2d_mc(b_dst + crank * 8192, &tmB, &full_bar[stage],
-                               b_mn + 64 * static_cast<int>(crank), b_k, 0x3);
-            } else if (!B_MN) {
-              tma_load_2d(b_dst, &tmBh, &full_bar[stage], b_k, b_mn);
-            } else {
-#pragma unroll
-              for (int c = 0; c < BN / 128; ++c)
-                tma_load_2d(b_dst + c * 8192, &tmB, &full_bar[stage], b_mn + 64 * c, b_k);
-            }
-          } else if (!B_RES && CL2) {
+          if (!B_RES && CL2) {
             // this CTA's half of the shared B tile, delivered to both CTAs
             const int b_k = g * p.b_k_per_g + ks * BK;
             uint8_t* b_dst = sB + stage * S::B_BYTES;
@@ -468,11 +431,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         umma_commit(yfull_bar);
         return true;
       };
-      constexpr uint32_t IDESC_HALF = instr_desc_bf16(BM, BN / 2, A_MN, B_MN);
       for (int tile = range.first; tile < range.end && ok; tile += range.step) {
-        int g, sp, mt, nt, half;
-        decode_unit<B_RES, CL2>(item_unit(tile, half), p, crank, g, sp, mt, nt);
-        const uint32_t idesc = half >= 0 ? IDESC_HALF : IDESC;
+        int g, sp, mt, nt;
+        decode_unit<B_RES, CL2>(tile, p, crank, g, sp, mt, nt);
         const int ks0 = sp * p.k_steps_per_split;
         const int ks1 = min(ks0 + p.k_steps_per_split, p.k_steps_total);
         if (B_RES) {
@@ -512,7 +473,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                         : smem_desc_sw128(a_base + j * 32, 16, 1024);
             const uint64_t bdesc = B_MN ? smem_desc_sw128(b_base + j * 2048, 8192, 1024)
                                         : smem_desc_sw128(b_base + j * 32, 16, 1024);
-            umma_bf16(d_tmem, adesc, bdesc, idesc, (ks > ks0 || j > 0) ? 1u : 0u);
+            umma_bf16(d_tmem, adesc, bdesc, IDESC, (ks > ks0 || j > 0) ? 1u : 0u);
           }
           any_mma = true;
           if (CL2)  // the stage is free once both CTAs' MMAs have read it
@@ -584,8 +545,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       return true;
     };
     for (int tile = range.first; tile < range.end; tile += range.step) {
-      int g, sp, mt, nt, half;
-      decode_unit<B_RES, CL2>(item_unit(tile, half), p, crank, g, sp, mt, nt);
+      int g, sp, mt, nt;
+      decode_unit<B_RES, CL2>(tile, p, crank, g, sp, mt, nt);
       const bool got = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag);
       if (!__all_sync(0xffffffffu, got)) {  // the whole warp unwinds together
         record_timeout(p.status, abort_flag);
@@ -634,11 +595,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // TMA tile stores: 128-byte rows of 64 bf16 or 32 fp32 per chunk
         constexpr int CW = EPI == EPI_TMA_BF16 ? 64 : 32;
         const int out_row = g * p.epi.row_g + sp * p.epi.row_s + mt * BM + quarter * 32;
-        const int out_col0 = g * p.epi.col_g + nt * BN + (half > 0 ? BN / 2 : 0);
-        const int cols = half >= 0 ? BN / 2 : BN;
+        const int out_col0 = g * p.epi.col_g + nt * BN;
         uint8_t* my_row = stg + lane * 128;
 #pragma unroll 1
-        for (int c0 = 0; c0 < cols; c0 += CW) {
+        for (int c0 = 0; c0 < BN; c0 += CW) {
           uint32_t w[32];  // this lane's 128 bytes of the chunk
           if (EPI == EPI_TMA_BF16) {
             uint32_t r0[32], r1[32];
@@ -731,12 +691,6 @@ cudaError_t launch_tc(const TcGemm& g, cudaStream_t stream) {
   if (!make_map(&tmB, g.B.ptr, g.B.rows, g.B.cols, g.B.pitch, 2, 64,
                 B_MN ? 64 : (CL2 ? BN / 2 : BN)))
     return cudaErrorInvalidValue;
-  // half-width items of the last wave: a K-major B box of BN / 2 rows (CL2: BN / 4 per CTA)
-  constexpr bool HALVES = EPI == EPI_TMA_BF16 && !B_RES && BN == 256;
-  CUtensorMap tmBh = tmA;  // unused otherwise
-  if (HALVES && !B_MN &&
-      !make_map(&tmBh, g.B.ptr, g.B.rows, g.B.cols, g.B.pitch, 2, 64, CL2 ? BN / 4 : BN / 2))
-    return cudaErrorInvalidValue;
   if (EPI == EPI_TMA_BF16 || (EPI == EPI_BLOCK && g.epi.out_bf16 != nullptr)) {
     if (!make_map(&tmC, g.epi.out_bf16, g.epi.out_rows, g.epi.ld, g.epi.ld, 2, 64, 32))
       return cudaErrorInvalidValue;
@@ -775,21 +729,11 @@ cudaError_t launch_tc(const TcGemm& g, cudaStream_t stream) {
   p.status = device_status_ptr();
   if (B_RES && (p.splits != 1 || p.k_steps_total > S::MAX_RES_KSTEPS))
     return cudaErrorInvalidValue;
-  // whole units, and the last partial wave as half-width items when its
-  // halves fit in one wave
-  const long long units = static_cast<long long>(p.batches) * p.splits *
-                          (CL2 ? p.m_pairs : p.m_tiles) * p.n_tiles;
-  const long long gmax = CL2 ? max_clusters[dev] : sm_count();
-  long long full_units = units;
-  if (HALVES && gmax > 0) {
-    const long long rem = units % gmax;
-    if (rem > 0 && 2 * rem <= gmax) full_units = units - rem;
-  }
-  p.full_units = static_cast<int>(full_units);
-  const long long items = full_units + 2 * (units - full_units);
   if (CL2) {
-    if (items <= 0) return cudaSuccess;
-    const int clusters = static_cast<int>(std::min<long long>(items, max_clusters[dev]));
+    const long long units =
+        static_cast<long long>(p.batches) * p.splits * p.m_pairs * p.n_tiles;
+    if (units <= 0) return cudaSuccess;
+    const int clusters = static_cast<int>(std::min<long long>(units, max_clusters[dev]));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters);
     cfg.blockDim = dim3(NUM_THREADS);
@@ -805,11 +749,11 @@ cudaError_t launch_tc(const TcGemm& g, cudaStream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     prof_begin(g.tag, stream);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmC, tmR, tmY, tmBh, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, tmA, tmB, tmC, tmR, tmY, p);
     prof_end(g.tag, stream);
     return e != cudaSuccess ? e : cudaGetLastError();
   }
-  const long long tiles = items;
+  const long long tiles = static_cast<long long>(p.batches) * p.splits * p.m_tiles * p.n_tiles;
   if (tiles <= 0) return cudaSuccess;
   int grid = static_cast<int>(std::min<long long>(tiles, sm_count()));
   if (B_RES) {  // contiguous runs: launch only the CTAs that get a run
@@ -818,7 +762,7 @@ cudaError_t launch_tc(const TcGemm& g, cudaStream_t stream) {
   }
   prof_begin(g.tag, stream);
   cudaError_t e = launch_pdl(kernel, dim3(grid), dim3(NUM_THREADS), S::SMEM, stream, tmA, tmB,
-                             tmC, tmR, tmY, tmBh, p);
+                             tmC, tmR, tmY, p);
   prof_end(g.tag, stream);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
