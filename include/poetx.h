@@ -249,11 +249,9 @@ int poetx_set_block_epilogue_fusion(int enable);
 /* Host -> device copy of `bytes` from page-locked (pinned) host memory,
  * pulled by the SMs over the host link instead of a copy engine; used to
  * feed a step's activations while the previous step computes.  bytes a
- * multiple of 16, both pointers 16-byte aligned; host_src must be memory
- * the device can address: page-locked memory, or any host memory where the
- * GPU reads pageable memory (INVALID_ARG otherwise, nothing enqueued).
- * Enqueued on `stream` like every call.  Not part of the method: a
- * data-loading helper. */
+ * multiple of 16, both pointers 16-byte aligned; host_src must be pinned
+ * and mapped (INVALID_ARG otherwise, nothing enqueued).  Enqueued on
+ * `stream` like every call.  Not part of the method: a data-loading helper. */
 poetx_status poetx_copy_from_host(const void* host_src, void* dev_dst, size_t bytes,
                                   poetx_stream stream);
 
