@@ -48,8 +48,6 @@ def parse():
                          "(llama3_8b_block: the 7 of a Llama-3-8B decoder block; "
                          "llama_1p3b_model: all 168 of the 1.3B-shaped model)")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--e2e-copy", default="pull", choices=["pull", "engine"],
-                    help="end-to-end uploads: SMs pulling pinned host memory, or copy engines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true",
                     help="time eager launches instead of CUDA-graph replays")
@@ -529,7 +527,7 @@ def run_gpu(args):
             "transform_t", "gemm_w0", "gemm_w0_dgrad", "gemm_w0_r", "gemm_w0_dgrad_p", "outer", "reduce_extract", "cnp_bwd",
             "pack_skew", "f32_to_bf16", "chain", "prep_tiles", "pack_tiles", "permute", "adam",
             "transform_sum",
-            "dequantize", "quantize", "host_pull"]
+            "dequantize", "quantize"]
     kernels = {}
     for t in tags:
         n, tot = poetx.poetx_profile_query(t)
@@ -643,12 +641,8 @@ def run_gpu(args):
             with torch.cuda.stream(h2d):
                 if after is not None:
                     h2d.wait_event(after)  # the set's previous step has read its inputs
-                if args.e2e_copy == "pull":  # the SMs pull from pinned host memory
-                    poetx.poetx_copy_from_host(hx, sets[j][0]["x"], stream=h2d)
-                    poetx.poetx_copy_from_host(hdy, sets[j][0]["dy"], stream=h2d)
-                else:  # the copy engines
-                    sets[j][0]["x"].copy_(hx, non_blocking=True)
-                    sets[j][0]["dy"].copy_(hdy, non_blocking=True)
+                sets[j][0]["x"].copy_(hx, non_blocking=True)
+                sets[j][0]["dy"].copy_(hdy, non_blocking=True)
                 up[j].record(h2d)
 
         def pipeline(k, start):
@@ -690,9 +684,7 @@ def run_gpu(args):
                "d2h_bytes_per_step": (hP[0].numel() + hR[0].numel()) * 4,
                "steps": ksteps, "ms_per_step": ems,
                "overlap": "double-buffered: uploads of step i+1 and read-back of step i-1 "
-                          "run on copy streams during step i",
-               "upload": ("SMs pull pinned host memory (poetx_copy_from_host)"
-                          if args.e2e_copy == "pull" else "copy engines (cudaMemcpyAsync)")}
+                          "run on copy streams during step i"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

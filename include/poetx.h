@@ -246,15 +246,6 @@ poetx_status poetx_dequantize_w0(const int8_t* W0_q, const float* scales, void* 
  * wide; returns the previous setting. */
 int poetx_set_block_epilogue_fusion(int enable);
 
-/* Host -> device copy of `bytes` from page-locked (pinned) host memory,
- * pulled by the SMs over the host link instead of a copy engine; used to
- * feed a step's activations while the previous step computes.  bytes a
- * multiple of 16, both pointers 16-byte aligned; host_src must be pinned
- * and mapped (INVALID_ARG otherwise, nothing enqueued).  Enqueued on
- * `stream` like every call.  Not part of the method: a data-loading helper. */
-poetx_status poetx_copy_from_host(const void* host_src, void* dev_dst, size_t bytes,
-                                  poetx_stream stream);
-
 /* ------------------------------------------------------------------------
  * Status and measurement
  * ------------------------------------------------------------------------ */

@@ -21,7 +21,7 @@ __all__ = [
     "poetx_transform_workspace_size", "poetx_transform_forward", "poetx_transform_backward",
     "poetx_permute_features", "poetx_fold_permutations", "poetx_merge_workspace_size",
     "poetx_merge", "poetx_adam_update", "poetx_quantize_w0", "poetx_dequantize_w0",
-    "poetx_set_block_epilogue_fusion", "poetx_copy_from_host",
+    "poetx_set_block_epilogue_fusion",
     "poetx_device_status", "poetx_selftest_wait_timeout", "poetx_launch_count", "poetx_profile_start", "poetx_profile_stop",
     "poetx_profile_query", "poetx_status_string", "EXPORTED_SYMBOLS",
 ]
@@ -71,7 +71,6 @@ _SIGNATURES = {
     "poetx_quantize_w0": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_ptr]),
     "poetx_dequantize_w0": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_ptr]),
     "poetx_set_block_epilogue_fusion": (_c_int, [_c_int]),
-    "poetx_copy_from_host": (_c_int, [_c_ptr, _c_ptr, _c_size, _c_ptr]),
     "poetx_device_status": (_c_int, []),
     "poetx_selftest_wait_timeout": (_c_int, [ctypes.c_uint, _c_ptr]),
     "poetx_launch_count": (ctypes.c_longlong, []),
@@ -244,13 +243,6 @@ def poetx_set_block_epilogue_fusion(enable: bool) -> bool:
     """Turn the W0 GEMM's block-diagonal epilogue on or off (process-wide);
     returns the previous setting."""
     return bool(load_library().poetx_set_block_epilogue_fusion(1 if enable else 0))
-
-
-def poetx_copy_from_host(host_src, dev_dst, nbytes=None, stream=None):
-    """dev_dst <- host_src (a pinned CPU tensor), pulled by the SMs."""
-    n = _nbytes(host_src) if nbytes is None else nbytes
-    _check("poetx_copy_from_host", load_library().poetx_copy_from_host(
-        _ptr(host_src), _ptr(dev_dst), n, _stream(stream)))
 
 
 def poetx_device_status() -> int:

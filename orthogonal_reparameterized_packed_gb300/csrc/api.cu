@@ -1409,25 +1409,7 @@ int poetx_set_block_epilogue_fusion(int enable) {
   return g_fuse_block_epilogue.exchange(enable != 0 ? 1 : 0);
 }
 
-poetx_status poetx_copy_from_host(const void* host_src, void* dev_dst, size_t bytes,
-                                  poetx_stream stream) {
-  if (bytes == 0) return POETX_OK;
-  if (host_src == nullptr || dev_dst == nullptr || bytes % 16 != 0 ||
-      (reinterpret_cast<uintptr_t>(host_src) & 15u) != 0 || !aligned16(dev_dst))
-    return POETX_ERR_INVALID_ARG;
-  // the device-side address of the page-locked host buffer
-  void* mapped = nullptr;
-  if (cudaHostGetDevicePointer(&mapped, const_cast<void*>(host_src), 0) != cudaSuccess ||
-      mapped == nullptr) {
-    cudaGetLastError();  // not page-locked and mapped: nothing enqueued
-    return POETX_ERR_INVALID_ARG;
-  }
-  return to_status(launch_host_pull(mapped, dev_dst, static_cast<long long>(bytes / 16),
-                                    static_cast<cudaStream_t>(stream)));
-}
-
 }  // extern "C"
-
 
 
 

@@ -220,8 +220,6 @@ cudaError_t launch_quantize_rows(const void* W, bool is_bf16, int8_t* q, float* 
                                  int d_out, cudaStream_t s);
 cudaError_t launch_dequantize(const int8_t* q, const float* scales, void* W, bool is_bf16,
                               int d_in, int d_out, cudaStream_t s);
-// dst = src (n16 16-byte words) pulled by the SMs from mapped host memory.
-cudaError_t launch_host_pull(const void* src, void* dst, long long n16, cudaStream_t s);
 // theta -= lr * (m_hat / (sqrt(v_hat) + eps) + wd * theta) with updated moments.
 cudaError_t launch_adam(float* theta, const float* grad, float* m, float* v, long long n,
                         float lr, float beta1, float beta2, float eps, float wd, float bc1,

@@ -493,23 +493,6 @@ __global__ void __launch_bounds__(kPermThreads)
   }
 }
 
-// dst = src for n16 16-byte words, src in page-locked host memory mapped
-// into the device's address space: the SMs pull over the host link, each
-// thread keeping four 16-byte loads in flight.
-__global__ void __launch_bounds__(256) host_pull_kernel(const uint4* __restrict__ src,
-                                                        uint4* __restrict__ dst, long long n16) {
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
-  for (; i + 3 * stride < n16; i += 4 * stride) {
-    const uint4 a = src[i], b = src[i + stride], c = src[i + 2 * stride], d = src[i + 3 * stride];
-    dst[i] = a;
-    dst[i + stride] = b;
-    dst[i + 2 * stride] = c;
-    dst[i + 3 * stride] = d;
-  }
-  for (; i < n16; i += stride) dst[i] = src[i];
-}
-
 // One Adam step on packed parameters: m, v moments, bias corrections bc1 =
 // 1 - beta1^step and bc2 = 1 - beta2^step, decoupled weight decay wd.
 __global__ void adam_kernel(float* __restrict__ theta, const float* __restrict__ grad,
@@ -755,18 +738,6 @@ cudaError_t launch_permute_rows(const void* in, long long in_rows, const int* ro
   }
   prof_end("permute", s);
   return e != cudaSuccess ? e : cudaGetLastError();
-}
-
-cudaError_t launch_host_pull(const void* src, void* dst, long long n16, cudaStream_t s) {
-  if (n16 <= 0) return cudaSuccess;
-  long long blocks = (n16 + 255) / 256;
-  const long long cap = static_cast<long long>(sm_count()) * 4;
-  if (blocks > cap) blocks = cap;
-  prof_begin("host_pull", s);
-  host_pull_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-      static_cast<const uint4*>(src), static_cast<uint4*>(dst), n16);
-  prof_end("host_pull", s);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_adam(float* theta, const float* grad, float* m, float* v, long long n,

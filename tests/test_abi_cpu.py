@@ -181,12 +181,3 @@ def test_index_map_calls_reject_invalid_arguments(lib):
     assert L.poetx_permute_features(None, None, None, 0, 64, F, None) == 0  # no rows
     assert L.poetx_fold_permutations(FAKE, FAKE, FAKE + 4, FAKE + 4096, 64, 64, B, None) == 1
     assert L.poetx_fold_permutations(FAKE, FAKE, FAKE, FAKE + 4096, 25608, 64, B, None) == 1
-
-
-def test_copy_from_host_rejects_invalid_arguments(lib):
-    L = _raw()
-    assert L.poetx_copy_from_host(FAKE, FAKE, 0, None) == 0       # nothing to copy
-    assert L.poetx_copy_from_host(None, FAKE, 64, None) == 1
-    assert L.poetx_copy_from_host(FAKE, None, 64, None) == 1
-    assert L.poetx_copy_from_host(FAKE, FAKE, 24, None) == 1      # not a multiple of 16
-    assert L.poetx_copy_from_host(FAKE + 8, FAKE, 64, None) == 1  # misaligned source
