@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(256) pack_tiles_kernel(const float* __restrict
 // enough for several CTAs per SM, whose groups overlap one another's loads.
 // Map entries outside [0, d) (or [0, in_rows)) are not followed: the output
 // gets 0 and the status word POETX_ERR_INVALID_ARG.
-constexpr int kPermThreads = 256;
+constexpr int kPermThreads = 128;  // small CTAs: six fit an SM by registers and shared memory
 
 template <typename T>
 __global__ void __launch_bounds__(kPermThreads)
@@ -713,25 +713,33 @@ cudaError_t launch_permute_rows(const void* in, long long in_rows, const int* ro
   if (smem > 200 * 1024) return cudaErrorInvalidValue;
   const int R = is_bf16 ? 4 : 2;
   const long long groups = (rows + R - 1) / R;
-  long long per_sm = (228 * 1024) / static_cast<long long>(smem + 1024);
-  if (per_sm > 2048 / kPermThreads) per_sm = 2048 / kPermThreads;
-  if (per_sm < 1) per_sm = 1;
+  // as many CTAs as fit at once (each holds R rows in flight)
+  const void* fn = is_bf16 ? reinterpret_cast<const void*>(permute_rows_kernel<__nv_bfloat16>)
+                           : reinterpret_cast<const void*>(permute_rows_kernel<float>);
+  static bool attr_set[2][64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[is_bf16][dev]) {
+    cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                         cudaSharedmemCarveoutMaxShared);
+    cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    attr_set[is_bf16][dev] = true;
+  }
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kPermThreads, smem) !=
+          cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
   const long long cap = static_cast<long long>(sm_count()) * per_sm;
   const dim3 grid(static_cast<unsigned>(groups < cap ? groups : cap));
   const int warps = kPermThreads / 32;
   cudaError_t e;
   prof_begin("permute", s);
   if (is_bf16) {
-    if (smem > 48 * 1024)
-      cudaFuncSetAttribute(permute_rows_kernel<__nv_bfloat16>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     e = launch_pdl(permute_rows_kernel<__nv_bfloat16>, grid, dim3(warps * 32), smem, s,
                    static_cast<const __nv_bfloat16*>(in), in_rows, row_map, col_map,
                    static_cast<__nv_bfloat16*>(out), rows, d, device_status_ptr());
   } else {
-    if (smem > 48 * 1024)
-      cudaFuncSetAttribute(permute_rows_kernel<float>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     e = launch_pdl(permute_rows_kernel<float>, grid, dim3(warps * 32), smem, s,
                    static_cast<const float*>(in), in_rows, row_map, col_map,
                    static_cast<float*>(out), rows, d, device_status_ptr());
