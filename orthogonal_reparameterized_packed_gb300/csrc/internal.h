@@ -89,8 +89,8 @@ struct TcGemm {
 // The transposed block transform and the token sums of the block gradient in
 // one pass over X (transform_sum_tc.cu), 256 x 256 superblocks:
 //   out[t][g*256+n] = sum_kk X[t][g*256+kk] sb[g*256+kk][n]              (bf16)
-//   part[s][g][m][n]: slabs whose sum over s is sum_t Z[t][g*256+m] X[t][g*256+n]
-// `splits` (the slab count) must be transform_sum_splits(d, T).
+//   part[s][g][m][n] = sum_{t in split s} Z[t][g*256+m] X[t][g*256+n]     (fp32)
+// `splits` must be transform_sum_splits(d, T).
 int transform_sum_splits(int d, long long T);
 cudaError_t tc_transform_sum(const __nv_bfloat16* X, const __nv_bfloat16* Z,
                              const __nv_bfloat16* sb, __nv_bfloat16* out, float* part, int d,

@@ -3,32 +3,26 @@
 // activation Z [T][d] and the 256 x 256 superblocks SB of one side,
 //
 //   out[t][g*256 + n]  = sum_kk X[t][g*256 + kk] SB[g*256 + kk][n]     (bf16)
-//   part[s][g][m][n]   = sum over the token tiles of slab s of block g of
-//                        Z[t][g*256 + m] X[t][g*256 + n]                  (fp32)
+//   part[s][g][m][n]   = sum_{t in split s} Z[t][g*256 + m] X[t][g*256 + n]  (fp32)
 //
 // i.e. the transposed block transform (dv = dy R, dx = du P) and the
 // split-K token sums G^T of the block gradients (sum_t v_t dy_t^T,
 // sum_t x_t du_t^T).  Separately they read X twice from HBM; here every X
 // tile that lands in shared memory feeds both products.
 //
-// Work: the (block, token tile) positions, block-major, are cut into equal
-// runs, one per pair of CTAs (as many pairs as half the SMs).  CTA h of a
-// pair computes, for every position of its run,
-//   transform half: out columns g*256 + h*128 .. +127, all 256 K features,
-//                   with SB's 256 x 128 half resident in shared memory
-//   sum half:       rows m = h*128 .. +127 of G^T, all 256 columns
-// and stores the sum of each block its run touches (a segment) as one slab;
-// a block's slabs are numbered by the pairs that cover it, and the pair that
-// covers it last zeroes its unused slabs.  Both CTAs of a pair read the same
-// X tiles at about the same time, so the second read is served by L2.  TMEM:
-// two 128-column accumulators for the transform tiles (the epilogue of one
-// overlaps the next) and one 256-column accumulator for the sum.
+// One CTA per (block g, half h, token split s):
+//   transform half: out columns g*256 + h*128 .. +127, all 256 K features;
+//                   SB's 256 x 128 half stays resident in shared memory
+//   sum half:       rows m = h*128 .. +127 of part[s][g], all 256 columns
+// Both halves of a block read the same X tiles at about the same time, so
+// the second read is served by L2.  TMEM: two 128-column accumulators for
+// the transform tiles (the epilogue of one overlaps the next) and one
+// 256-column accumulator for the sum, 512 columns in all.
 //
 // Warp roles: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 2-5
 // epilogue (row-per-thread 16-byte stores: the shared memory a TMA-store
-// staging tile would take holds two more gradient chunks in flight).  Every
-// wait is bounded; on expiry the CTA records POETX_ERR_TIMEOUT, lets its
-// copies and MMAs in flight land and returns.
+// staging tile would take holds two more gradient chunks in flight).  Every wait is bounded; on expiry the CTA records
+// POETX_ERR_TIMEOUT, lets its copies and MMAs in flight land and returns.
 #include <algorithm>
 
 #include "internal.h"
@@ -55,25 +49,15 @@ constexpr uint32_t TS_TMEM_COLS = 512;
 static_assert(TS_SMEM <= 227 * 1024, "shared memory per CTA");
 
 struct TsArgs {
-  int d;               // features (multiple of 256)
-  int m_tiles;         // token tiles of 128
-  int per;             // (block, token tile) positions per pair of CTAs
-  int total;           // (d / 256) * m_tiles positions
-  int slabs;           // partial-sum slabs per block (the most pairs covering one block)
-  long long T;         // tokens
+  int d;            // features (multiple of 256)
+  int m_tiles;      // token tiles of 128
+  int splits;       // token splits
+  int per;          // token tiles per split
+  long long T;      // tokens
   __nv_bfloat16* out;  // [T][d]
-  float* part;         // [slabs][d][256]
+  float* part;         // [splits][d][256]
   int* status;
 };
-
-// Pair p covers positions [p * per, (p + 1) * per) of the (block, token tile)
-// sequence, block-major; its segment on block g is slab p - first_pair(g).
-__host__ __device__ __forceinline__ int ts_first_pair(int g, int m_tiles, int per) {
-  return (g * m_tiles) / per;
-}
-__host__ __device__ __forceinline__ int ts_last_pair(int g, int m_tiles, int per) {
-  return (g * m_tiles + m_tiles - 1) / per;
-}
 
 __global__ void __launch_bounds__(TS_THREADS, 1)
     transform_sum_kernel(const __grid_constant__ CUtensorMap tmX,   // X [T][d], box 64 x 128
@@ -92,21 +76,21 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
   uint64_t* zempty_bar = zfull_bar + TS_ZSTAGES;
   uint64_t* tfull_bar = zempty_bar + TS_ZSTAGES;  // [2]
   uint64_t* tempty_bar = tfull_bar + 2;           // [2]
-  uint64_t* bfull_bar = tempty_bar + 2;           // the block's SB half landed
-  uint64_t* bempty_bar = bfull_bar + 1;           // the MMAs reading it are done
-  uint64_t* gfull_bar = bempty_bar + 1;           // a segment's sum is complete
-  uint64_t* gempty_bar = gfull_bar + 1;           // the epilogue has read it (4 warps)
-  uint64_t* drain_bar = gempty_bar + 1;
+  uint64_t* bfull_bar = tempty_bar + 2;
+  uint64_t* gfull_bar = bfull_bar + 1;
+  uint64_t* drain_bar = gfull_bar + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  // the two CTAs of a pair (adjacent, so they run together) share positions
-  const int pair = blockIdx.x >> 1;
-  const int h = blockIdx.x & 1;
-  const int pos0 = pair * p.per;
-  const int pos1 = min(pos0 + p.per, p.total);
+  // work unit: token split fastest, then the half, then the block
+  const int s = blockIdx.x % p.splits;
+  const int h = (blockIdx.x / p.splits) & 1;
+  const int g = blockIdx.x / (2 * p.splits);
+  const int t_first = s * p.per;
+  const int t_end = min(t_first + p.per, p.m_tiles);
+  const int col_blk = g * 256;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < TS_XSTAGES; ++i) {
@@ -122,9 +106,7 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
       mbar_init(&tempty_bar[a], 4);
     }
     mbar_init(bfull_bar, 1);
-    mbar_init(bempty_bar, 1);
     mbar_init(gfull_bar, 1);
-    mbar_init(gempty_bar, 4);
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -149,28 +131,16 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
     if (lane == 0) {
       // ------------------------------------------------------ TMA producer
       bool ok = true;
-      int xs = 0, zs = 0, cur_g = -1, res_loads = 0;
+      int xs = 0, zs = 0;
       uint32_t xphase = 0, zphase = 0;
       long long x_issued = 0, z_issued = 0;
-      for (int pos = pos0; pos < pos1 && ok; ++pos) {
-        const int g = pos / p.m_tiles;
-        const int t = pos - g * p.m_tiles;
-        const int col_blk = g * 256;
-        if (g != cur_g) {
-          // SB's half for block g: K rows g*256 .. +255, columns h*128 .. +127
-          if (res_loads > 0 && !mbar_wait(bempty_bar, (res_loads - 1) & 1, abort_flag)) {
-            record_timeout(p.status, abort_flag);
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(bfull_bar, TS_RES_BYTES);
-          for (int kc = 0; kc < 4; ++kc)
-            for (int c2 = 0; c2 < 2; ++c2)
-              tma_load_2d(sRes + kc * 16384 + c2 * 8192, &tmB, bfull_bar, h * 128 + 64 * c2,
-                          col_blk + kc * 64);
-          cur_g = g;
-          ++res_loads;
-        }
+      // SB's half: K rows g*256 .. +255, columns h*128 .. +127 (MN-major B)
+      mbar_arrive_expect_tx(bfull_bar, TS_RES_BYTES);
+      for (int kc = 0; kc < 4; ++kc)
+        for (int c2 = 0; c2 < 2; ++c2)
+          tma_load_2d(sRes + kc * 16384 + c2 * 8192, &tmB, bfull_bar, h * 128 + 64 * c2,
+                      col_blk + kc * 64);
+      for (int t = t_first; t < t_end && ok; ++t) {
         if (!mbar_wait(&zempty_bar[zs], zphase ^ 1, abort_flag)) {
           record_timeout(p.status, abort_flag);
           ok = false;
@@ -215,11 +185,8 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
         };
         settle(full_bar, TS_XSTAGES, xs, xphase, x_issued);
         settle(zfull_bar, TS_ZSTAGES, zs, zphase, z_issued);
-        if (res_loads > 0) {
-          const unsigned long long t0 = global_timer_ns();
-          while (!mbar_try_wait(bfull_bar, (res_loads - 1) & 1) &&
-                 global_timer_ns() - t0 < 10000000ull) {
-          }
+        const unsigned long long t0 = global_timer_ns();
+        while (!mbar_try_wait(bfull_bar, 0) && global_timer_ns() - t0 < 10000000ull) {
         }
       }
     }
@@ -229,28 +196,14 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
       constexpr uint32_t IDESC_T = instr_desc_bf16(BM, 128, false, true);  // X K-major, SB MN-major
       constexpr uint32_t IDESC_S = instr_desc_bf16(BM, 128, true, true);   // Z, X both MN-major
       const uint32_t g_tmem = tmem_base + 256u;
-      bool ok = true, any_mma = false, seg_start = false;
-      int xs = 0, zs = 0, acc = 0, cur_g = -1, segs = 0;
+      bool ok = mbar_wait(bfull_bar, 0, abort_flag);
+      if (!ok) record_timeout(p.status, abort_flag);
+      tc_fence_after();
+      bool any_mma = false;
+      int xs = 0, zs = 0, acc = 0;
       uint32_t xphase = 0, zphase = 0, acc_phase = 0;
       const uint32_t res_base = smem_u32(sRes);
-      for (int pos = pos0; pos < pos1 && ok; ++pos) {
-        const int g = pos / p.m_tiles;
-        if (g != cur_g) {  // a new segment: its block's SB, and an empty sum
-          if (segs > 0) {
-            umma_commit(gfull_bar);   // the previous segment's sum is complete
-            umma_commit(bempty_bar);  // and its SB half free once those MMAs are done
-          }
-          if (!mbar_wait(bfull_bar, segs & 1, abort_flag) ||
-              (segs > 0 && !mbar_wait(gempty_bar, (segs - 1) & 1, abort_flag))) {
-            record_timeout(p.status, abort_flag);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          cur_g = g;
-          ++segs;
-          seg_start = true;
-        }
+      for (int t = t_first; t < t_end && ok; ++t) {
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1, abort_flag) ||
             !mbar_wait(&zfull_bar[zs], zphase, abort_flag)) {
           record_timeout(p.status, abort_flag);
@@ -276,14 +229,14 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
                       (c > 0 || j > 0) ? 1u : 0u);
           if (c & 1) {
             // token sum over chunks c-1, c (adjacent ring slots: a tile's chunk
-            // pairs start on even slots): G[m][64(c-1) ..] += sum_t Z[t][m] X[t][..]
+            // i always sits in slot i): G[m][64(c-1) ..] += sum_t Z[t][m] X[t][..]
             const uint32_t x_pair = x_base - TS_X_BYTES;
 #pragma unroll
             for (int j = 0; j < 8; ++j)
               umma_bf16(g_tmem + static_cast<uint32_t>(64 * (c - 1)),
                         smem_desc_sw128(z_base + j * 2048, 16384, 1024),
                         smem_desc_sw128(x_pair + j * 2048, TS_X_BYTES, 1024), IDESC_S,
-                        (!seg_start || j > 0) ? 1u : 0u);
+                        (t > t_first || j > 0) ? 1u : 0u);
             umma_commit(&empty_bar[xs - 1]);
             umma_commit(&empty_bar[xs]);
           }
@@ -294,7 +247,6 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
           }
         }
         if (!ok) break;
-        seg_start = false;
         umma_commit(&tfull_bar[acc]);
         umma_commit(&zempty_bar[zs]);
         if (++zs == TS_ZSTAGES) {
@@ -305,7 +257,7 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
         if (acc == 0) acc_phase ^= 1;
       }
       if (ok) {
-        if (segs > 0) umma_commit(gfull_bar);  // the last segment's sum is complete
+        umma_commit(gfull_bar);  // the split's sum is complete
       } else if (any_mma) {
         umma_commit(drain_bar);
         const unsigned long long t0 = global_timer_ns();
@@ -316,57 +268,13 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
   } else {
     // ----------------------------------------------------------- epilogue
     // Each thread owns one accumulator row and stores it with 16-byte stores
-    // (the transform tile's 128 bf16 columns; a segment's 256 fp32 sums).
+    // (the transform tile's 128 bf16 columns, then the sum's 256 fp32).
     const int quarter = warp & 3;
     const int row_in_tile = quarter * 32 + lane;
     bool ok = true;
-    int acc = 0, cur_g = -1, segs = 0;
+    int acc = 0;
     uint32_t acc_phase = 0;
-    // the sum of segment `seg` (block g) -> its slab; the pair that covers the
-    // block last also zeroes the block's unused slabs
-    auto store_sum = [&](int g, int seg) -> bool {
-      const bool got = mbar_wait(gfull_bar, seg & 1, abort_flag);
-      if (!__all_sync(0xffffffffu, got)) {
-        record_timeout(p.status, abort_flag);
-        return false;
-      }
-      tc_fence_after();
-      const uint32_t g_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + 256u;
-      const int first = ts_first_pair(g, p.m_tiles, p.per);
-      const long long row = static_cast<long long>(g) * 256 + h * 128 + row_in_tile;
-      uint4* dst = reinterpret_cast<uint4*>(
-          p.part + (static_cast<long long>(pair - first) * p.d + row) * 256);
-#pragma unroll 1
-      for (int c0 = 0; c0 < 256; c0 += 32) {
-        uint32_t r[32];
-        tmem_load_32cols(g_base + c0, r);
-        tmem_load_wait();
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          dst[c0 / 4 + q] = make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(gempty_bar);
-      if (pair == ts_last_pair(g, p.m_tiles, p.per)) {
-        for (int sl = pair - first + 1; sl < p.slabs; ++sl) {
-          uint4* z = reinterpret_cast<uint4*>(p.part + (static_cast<long long>(sl) * p.d + row) * 256);
-          for (int q = 0; q < 64; ++q) z[q] = make_uint4(0u, 0u, 0u, 0u);
-        }
-      }
-      return true;
-    };
-    for (int pos = pos0; pos < pos1; ++pos) {
-      const int g = pos / p.m_tiles;
-      const int t = pos - g * p.m_tiles;
-      if (g != cur_g) {
-        if (segs > 0 && !store_sum(cur_g, segs - 1)) {
-          ok = false;
-          break;
-        }
-        cur_g = g;
-        ++segs;
-      }
+    for (int t = t_first; t < t_end; ++t) {
       const bool got = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag);
       if (!__all_sync(0xffffffffu, got)) {
         record_timeout(p.status, abort_flag);
@@ -377,7 +285,7 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
       const uint32_t t_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                               static_cast<uint32_t>(acc * 128);
       const long long row = static_cast<long long>(t) * BM + row_in_tile;
-      uint4* dst = reinterpret_cast<uint4*>(p.out + row * p.d + g * 256 + h * 128);
+      uint4* dst = reinterpret_cast<uint4*>(p.out + row * p.d + col_blk + h * 128);
 #pragma unroll 1
       for (int c0 = 0; c0 < 128; c0 += 32) {
         uint32_t r[32];
@@ -398,7 +306,27 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
-    if (ok && segs > 0) store_sum(cur_g, segs - 1);
+    if (ok && t_end > t_first) {
+      // the split's partial sum: row h*128 + row_in_tile of part[s][g], fp32
+      const bool got = mbar_wait(gfull_bar, 0, abort_flag);
+      if (!__all_sync(0xffffffffu, got)) {
+        record_timeout(p.status, abort_flag);
+      } else {
+        tc_fence_after();
+        const uint32_t g_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + 256u;
+        const long long prow = static_cast<long long>(s) * p.d + col_blk + h * 128 + row_in_tile;
+        uint4* dst = reinterpret_cast<uint4*>(p.part + prow * 256);
+#pragma unroll 1
+        for (int c0 = 0; c0 < 256; c0 += 32) {
+          uint32_t r[32];
+          tmem_load_32cols(g_base + c0, r);
+          tmem_load_wait();
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dst[c0 / 4 + q] = make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+        }
+      }
+    }
   }
 
   tc_fence_before();
@@ -410,34 +338,17 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
   }
 }
 
-// The split of the positions into pairs of CTAs, and the slabs per block.
-struct TsPlan {
-  int m_tiles = 0, per = 1, pairs = 0, slabs = 1, total = 0;
-};
-
-TsPlan ts_plan(int d, long long T) {
-  TsPlan q;
-  q.m_tiles = static_cast<int>((T + BM - 1) / BM);
-  const int nb = d / 256;
-  q.total = nb * q.m_tiles;
-  int pairs_max = sm_count() / 2;
-  if (pairs_max < 1) pairs_max = 1;
-  q.per = (q.total + pairs_max - 1) / pairs_max;
-  if (q.per < 1) q.per = 1;
-  q.pairs = (q.total + q.per - 1) / q.per;
-  q.slabs = 1;
-  for (int g = 0; g < nb; ++g) {
-    const int cnt = ts_last_pair(g, q.m_tiles, q.per) - ts_first_pair(g, q.m_tiles, q.per) + 1;
-    if (cnt > q.slabs) q.slabs = cnt;
-  }
-  return q;
-}
-
 }  // namespace
 
 int transform_sum_splits(int d, long long T) {
-  if (T <= 0 || d <= 0 || d % 256 != 0) return 1;
-  return ts_plan(d, T).slabs;
+  const int m_tiles = static_cast<int>((T + BM - 1) / BM);
+  const int units = 2 * (d / 256);
+  int splits = sm_count() / (units > 0 ? units : 1);
+  if (splits < 1) splits = 1;
+  if (splits > m_tiles) splits = m_tiles;
+  if (splits < 1) splits = 1;
+  const int per = (m_tiles + splits - 1) / splits;
+  return (m_tiles + per - 1) / per;  // no empty split
 }
 
 cudaError_t tc_transform_sum(const __nv_bfloat16* X, const __nv_bfloat16* Z,
@@ -460,18 +371,16 @@ cudaError_t tc_transform_sum(const __nv_bfloat16* X, const __nv_bfloat16* Z,
     return cudaErrorInvalidValue;
   if (reinterpret_cast<uintptr_t>(out) % 16 != 0 || reinterpret_cast<uintptr_t>(part) % 16 != 0)
     return cudaErrorInvalidValue;
-  const TsPlan q = ts_plan(d, T);
   TsArgs a;
   a.d = d;
-  a.m_tiles = q.m_tiles;
-  a.per = q.per;
-  a.total = q.total;
-  a.slabs = q.slabs;
+  a.m_tiles = static_cast<int>((T + BM - 1) / BM);
+  a.splits = splits;
+  a.per = (a.m_tiles + splits - 1) / splits;
   a.T = T;
   a.out = out;
   a.part = part;
   a.status = device_status_ptr();
-  const int grid = 2 * q.pairs;
+  const int grid = 2 * (d / 256) * splits;
   prof_begin("transform_sum", stream);
   cudaError_t e = launch_pdl(transform_sum_kernel, dim3(grid), dim3(TS_THREADS), TS_SMEM, stream,
                              tmX, tmZ, tmB, a);
