@@ -116,11 +116,6 @@ __device__ __forceinline__ void decode_unit(int t, const TcKernelArgs& p, uint32
 template <bool B_RES, bool CL2>
 struct TileRange {
   int first, end, step;
-  // resident variants walk their run from its end: the last rows a previous
-  // kernel wrote are the likeliest still in L2
-  __device__ __forceinline__ int order(int tile) const {
-    return B_RES && !CL2 ? first + end - 1 - tile : tile;
-  }
   __device__ explicit TileRange(int num_tiles) {
     if (CL2) {
       first = static_cast<int>(cluster_id_x());
@@ -280,7 +275,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       };
       for (int tile = range.first; tile < range.end && ok; tile += range.step) {
         int g, sp, mt, nt;
-        decode_unit<B_RES, CL2>(range.order(tile), p, crank, g, sp, mt, nt);
+        decode_unit<B_RES, CL2>(tile, p, crank, g, sp, mt, nt);
         const int ks0 = sp * p.k_steps_per_split;
         const int ks1 = min(ks0 + p.k_steps_per_split, p.k_steps_total);
         const int a_mn = g * p.a_mn_per_g + mt * BM;
@@ -438,7 +433,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       };
       for (int tile = range.first; tile < range.end && ok; tile += range.step) {
         int g, sp, mt, nt;
-        decode_unit<B_RES, CL2>(range.order(tile), p, crank, g, sp, mt, nt);
+        decode_unit<B_RES, CL2>(tile, p, crank, g, sp, mt, nt);
         const int ks0 = sp * p.k_steps_per_split;
         const int ks1 = min(ks0 + p.k_steps_per_split, p.k_steps_total);
         if (B_RES) {
@@ -551,7 +546,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     };
     for (int tile = range.first; tile < range.end; tile += range.step) {
       int g, sp, mt, nt;
-      decode_unit<B_RES, CL2>(range.order(tile), p, crank, g, sp, mt, nt);
+      decode_unit<B_RES, CL2>(tile, p, crank, g, sp, mt, nt);
       const bool got = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag);
       if (!__all_sync(0xffffffffu, got)) {  // the whole warp unwinds together
         record_timeout(p.status, abort_flag);

@@ -88,13 +88,8 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
   const int s = blockIdx.x % p.splits;
   const int h = (blockIdx.x / p.splits) & 1;
   const int g = blockIdx.x / (2 * p.splits);
-  // split s takes token tiles s, s + splits, ... from the highest down: the
-  // last rows the previous kernel wrote are the likeliest still in L2
-  const int n_mine = p.m_tiles > s ? (p.m_tiles - 1 - s) / p.splits + 1 : 0;
-  auto tile_of = [&](int i) {
-    const int last = s + (n_mine - 1) * p.splits;
-    return last - i * p.splits;
-  };
+  const int t_first = s * p.per;
+  const int t_end = min(t_first + p.per, p.m_tiles);
   const int col_blk = g * 256;
 
   if (threadIdx.x == 0) {
@@ -145,8 +140,7 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
         for (int c2 = 0; c2 < 2; ++c2)
           tma_load_2d(sRes + kc * 16384 + c2 * 8192, &tmB, bfull_bar, h * 128 + 64 * c2,
                       col_blk + kc * 64);
-      for (int i = 0; i < n_mine && ok; ++i) {
-        const int t = tile_of(i);
+      for (int t = t_first; t < t_end && ok; ++t) {
         if (!mbar_wait(&zempty_bar[zs], zphase ^ 1, abort_flag)) {
           record_timeout(p.status, abort_flag);
           ok = false;
@@ -209,7 +203,7 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
       int xs = 0, zs = 0, acc = 0;
       uint32_t xphase = 0, zphase = 0, acc_phase = 0;
       const uint32_t res_base = smem_u32(sRes);
-      for (int i = 0; i < n_mine && ok; ++i) {
+      for (int t = t_first; t < t_end && ok; ++t) {
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1, abort_flag) ||
             !mbar_wait(&zfull_bar[zs], zphase, abort_flag)) {
           record_timeout(p.status, abort_flag);
@@ -242,7 +236,7 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
               umma_bf16(g_tmem + static_cast<uint32_t>(64 * (c - 1)),
                         smem_desc_sw128(z_base + j * 2048, 16384, 1024),
                         smem_desc_sw128(x_pair + j * 2048, TS_X_BYTES, 1024), IDESC_S,
-                        (i > 0 || j > 0) ? 1u : 0u);
+                        (t > t_first || j > 0) ? 1u : 0u);
             umma_commit(&empty_bar[xs - 1]);
             umma_commit(&empty_bar[xs]);
           }
@@ -280,8 +274,7 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
     bool ok = true;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int i = 0; i < n_mine; ++i) {
-      const int t = tile_of(i);
+    for (int t = t_first; t < t_end; ++t) {
       const bool got = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag);
       if (!__all_sync(0xffffffffu, got)) {
         record_timeout(p.status, abort_flag);
@@ -313,7 +306,7 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
-    if (ok && n_mine > 0) {
+    if (ok && t_end > t_first) {
       // the split's partial sum: row h*128 + row_in_tile of part[s][g], fp32
       const bool got = mbar_wait(gfull_bar, 0, abort_flag);
       if (!__all_sync(0xffffffffu, got)) {
