@@ -117,7 +117,8 @@ def test_unpack_is_bit_exact(px, dtype, d, b):
     ("f32", 256, 32, 3), ("f32", 512, 256, 3), ("f32", 64, 8, 5), ("f32", 96, 3, 1),
     ("bf16", 512, 32, 5), ("bf16", 512, 64, 3), ("bf16", 512, 128, 1), ("bf16", 512, 128, 3),
     ("bf16", 1024, 256, 3), ("bf16", 1024, 256, 5), ("bf16", 1024, 512, 3),
-    ("bf16", 1024, 512, 1), ("bf16", 512, 256, 10), ("bf16", 512, 128, 0)])
+    ("bf16", 1024, 512, 1), ("bf16", 512, 256, 10), ("bf16", 512, 128, 0),
+    ("bf16", 512, 256, 16), ("f32", 64, 8, 16), ("bf16", 768, 256, 8)])  # k = 16: the maximum
 def test_build_blocks_matches_oracle(px, dtype, d, b, k):
     rng = np.random.default_rng(21)
     theta = (rng.standard_normal((d // b, b * (b - 1) // 2)) * 0.02).astype(np.float32)
@@ -194,6 +195,8 @@ LAYER_CASES = [
     (256, 256, 256, 5, 1, "bf16"),
     (256, 256, 256, 3, 127, "bf16"),
     (256, 512, 128, 9, 64, "bf16"),      # k above the one-launch chain limit
+    (512, 256, 256, 16, 40, "bf16"),     # the largest k
+    (64, 32, 8, 16, 20, "f32"),
     (512, 256, 256, 0, 70, "bf16"),
 ]
 
