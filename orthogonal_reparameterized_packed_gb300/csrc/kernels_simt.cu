@@ -271,8 +271,19 @@ __device__ __forceinline__ void unpack_tile_pair(const float* __restrict__ th, i
   }
 }
 
-// grid (tiles_per_block^2, n_a + n_b), 256 threads:
-//   Q (bf16, plus lo if q_lo, plus 2Q if q_x2) from theta for tiles with ti <= tj,
+// Tile pair k (k < t(t+1)/2) of a t x t tiling: tiles (ti, tj) and (tj, ti), ti <= tj.
+__device__ __forceinline__ void tile_pair(int k, int t, int& ti, int& tj) {
+  ti = 0;
+  while (k >= t - ti) {
+    k -= t - ti;
+    ++ti;
+  }
+  tj = ti + k;
+}
+
+// grid (tile pairs per block, n_a + n_b), 256 threads; for tiles (ti, tj) and
+// (tj, ti) of block g:
+//   Q (bf16, plus lo if q_lo, plus 2Q if q_x2) from theta,
 //   2I into two_i for block 0,
 //   F = sum over splits of the diagonal b-block of the partials (if f16).
 __global__ void __launch_bounds__(256) prep_tiles_kernel(PrepTilesArgs a) {
@@ -280,7 +291,8 @@ __global__ void __launch_bounds__(256) prep_tiles_kernel(PrepTilesArgs a) {
   pdl_trigger();
   __shared__ float tile[TT][TT + 1];
   const int t = a.b / TT;
-  const int ti = blockIdx.x / t, tj = blockIdx.x % t;
+  int ti, tj;
+  tile_pair(blockIdx.x, t, ti, tj);
   const int g = blockIdx.y;
   const long long bb = static_cast<long long>(a.b) * a.b;
   const int m = a.b * (a.b - 1) / 2;
@@ -288,9 +300,9 @@ __global__ void __launch_bounds__(256) prep_tiles_kernel(PrepTilesArgs a) {
   const int gl = side_a ? g : g - a.n_a;
   const int tid = threadIdx.x;
   const int r = tid >> 3, c4 = (tid & 7) * 4;
-  const int i = ti * TT + r, j0 = tj * TT + c4;
   if (a.zero_words != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && tid < a.n_zero_words)
     a.zero_words[tid] = 0u;
+  const int ntiles = ti == tj ? 1 : 2;
   if (a.f16 != nullptr) {
     const int per = a.S / a.b;
     const int sb = gl / per;
@@ -298,23 +310,30 @@ __global__ void __launch_bounds__(256) prep_tiles_kernel(PrepTilesArgs a) {
     const float* part = side_a ? a.part_a : a.part_b;
     const int splits = side_a ? a.splits_a : a.splits_b;
     const long long stride = static_cast<long long>(side_a ? a.nsb_a : a.nsb_b) * a.S * a.S;
-    const long long src = (static_cast<long long>(sb) * a.S + off + i) * a.S + off + j0;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < splits; ++s) {
-      const float4 w = *reinterpret_cast<const float4*>(part + s * stride + src);
-      v.x += w.x;
-      v.y += w.y;
-      v.z += w.z;
-      v.w += w.w;
+    for (int q = 0; q < ntiles; ++q) {
+      const int i = (q == 0 ? ti : tj) * TT + r, j0 = (q == 0 ? tj : ti) * TT + c4;
+      const long long src = (static_cast<long long>(sb) * a.S + off + i) * a.S + off + j0;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s = 0; s < splits; ++s) {
+        const float4 w = *reinterpret_cast<const float4*>(part + s * stride + src);
+        v.x += w.x;
+        v.y += w.y;
+        v.z += w.z;
+        v.w += w.w;
+      }
+      const long long o = g * bb + static_cast<long long>(i) * a.b + j0;
+      store_bf16x4(a.f16 + o, v.x, v.y, v.z, v.w);
+      if (a.f32 != nullptr) *reinterpret_cast<float4*>(a.f32 + o) = v;
     }
-    const long long o = g * bb + static_cast<long long>(i) * a.b + j0;
-    store_bf16x4(a.f16 + o, v.x, v.y, v.z, v.w);
-    if (a.f32 != nullptr) *reinterpret_cast<float4*>(a.f32 + o) = v;
   }
-  if (g == 0 && a.two_i != nullptr)
-    store_bf16x4(a.two_i + static_cast<long long>(i) * a.b + j0, i == j0 ? 2.f : 0.f,
-                 i == j0 + 1 ? 2.f : 0.f, i == j0 + 2 ? 2.f : 0.f, i == j0 + 3 ? 2.f : 0.f);
-  if (ti <= tj && a.q_hi != nullptr) {
+  if (g == 0 && a.two_i != nullptr) {
+    for (int q = 0; q < ntiles; ++q) {
+      const int i = (q == 0 ? ti : tj) * TT + r, j0 = (q == 0 ? tj : ti) * TT + c4;
+      store_bf16x4(a.two_i + static_cast<long long>(i) * a.b + j0, i == j0 ? 2.f : 0.f,
+                   i == j0 + 1 ? 2.f : 0.f, i == j0 + 2 ? 2.f : 0.f, i == j0 + 3 ? 2.f : 0.f);
+    }
+  }
+  if (a.q_hi != nullptr) {
     const float* th = side_a ? a.theta_a + static_cast<long long>(gl) * m
                              : a.theta_b + static_cast<long long>(gl) * m;
     unpack_tile_pair(th, a.b, ti, tj, a.q_hi + g * bb,
@@ -324,7 +343,7 @@ __global__ void __launch_bounds__(256) prep_tiles_kernel(PrepTilesArgs a) {
 }
 
 // dtheta[g][idx(i,j)] = sign * (D[g][i][j] - D[g][j][i]) for the i < j entries of
-// tile (ti, tj), ti <= tj; grid (tiles_per_block^2, n_a + n_b), 256 threads.
+// tile (ti, tj), ti <= tj; grid (tile pairs per block, n_a + n_b), 256 threads.
 __global__ void __launch_bounds__(256) pack_tiles_kernel(const float* __restrict__ D, float sign,
                                                          int n_a, int b,
                                                          float* __restrict__ dtheta_a,
@@ -333,8 +352,8 @@ __global__ void __launch_bounds__(256) pack_tiles_kernel(const float* __restrict
   pdl_trigger();
   __shared__ float tile[TT][TT + 1];
   const int t = b / TT;
-  const int ti = blockIdx.x / t, tj = blockIdx.x % t;
-  if (ti > tj) return;
+  int ti, tj;
+  tile_pair(blockIdx.x, t, ti, tj);
   const int g = blockIdx.y;
   const long long base = static_cast<long long>(g) * b * b;
   const int m = b * (b - 1) / 2;
@@ -686,7 +705,7 @@ cudaError_t launch_pack_skew(const float* A, const float* B, int n_a, int n_b, i
 cudaError_t launch_prep_tiles(const PrepTilesArgs& a, cudaStream_t s) {
   if (a.b % TT != 0 || a.n_a + a.n_b <= 0) return cudaErrorInvalidValue;
   const int t = a.b / TT;
-  dim3 grid(t * t, a.n_a + a.n_b);
+  dim3 grid(t * (t + 1) / 2, a.n_a + a.n_b);
   prof_begin("prep_tiles", s);
   cudaError_t e = launch_pdl(prep_tiles_kernel, grid, dim3(256), 0, s, a);
   prof_end("prep_tiles", s);
@@ -697,7 +716,7 @@ cudaError_t launch_pack_tiles(const float* D, float sign, int n_a, int n_b, int 
                               float* dtheta_a, float* dtheta_b, cudaStream_t s) {
   if (b % TT != 0 || n_a + n_b <= 0) return cudaErrorInvalidValue;
   const int t = b / TT;
-  dim3 grid(t * t, n_a + n_b);
+  dim3 grid(t * (t + 1) / 2, n_a + n_b);
   prof_begin("pack_tiles", s);
   cudaError_t e = launch_pdl(pack_tiles_kernel, grid, dim3(256), 0, s, D, sign, n_a, b,
                              dtheta_a, dtheta_b);
