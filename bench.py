@@ -63,6 +63,9 @@ def parse():
     ap.add_argument("--fuse-epilogue", action="store_true",
                     help="apply the block-diagonal factors in the W0 GEMMs' epilogues "
                          "(y = R v, dx = du P) instead of separate block transforms")
+    ap.add_argument("--no-split-tail", action="store_true",
+                    help="W0 GEMMs: every tile sums K in one CTA (no K split of the last "
+                         "partial round of tiles across a cluster's two CTAs)")
     ap.add_argument("--recompute-v", action="store_true",
                     help="backward recomputes v = W0 P x instead of reading it (saves T x d_out)")
     return ap.parse_args()
@@ -105,6 +108,8 @@ def config_json(name, n, args=None):
         c["recompute_v"] = True
     if args is not None and getattr(args, "fuse_epilogue", False):
         c["block_epilogue"] = "fused into the W0 GEMMs"
+    if args is not None and getattr(args, "no_split_tail", False):
+        c["w0_split_tail"] = False
     if args is not None and getattr(args, "w0_int8", False):
         c["w0"] = "int8, per-row scales, dequantised each step"
     if args is not None and getattr(args, "train_step", False):
@@ -380,6 +385,7 @@ def run_gpu(args):
     torch.cuda.set_device(local)
     poetx.load_library()
     poetx.poetx_set_block_epilogue_fusion(args.fuse_epilogue)
+    poetx.poetx_set_w0_split_tail(not args.no_split_tail)
 
     name = args.workload
     projs = projections(name)

@@ -246,6 +246,19 @@ poetx_status poetx_dequantize_w0(const int8_t* W0_q, const float* scales, void* 
  * wide; returns the previous setting. */
 int poetx_set_block_epilogue_fusion(int enable);
 
+/* Scheduling of the W0 GEMMs (technical summary, section 2: the frozen-
+ * weight product; the schedule is this library's).  The GEMMs run as
+ * clusters of two CTAs on 128 x 256 output tiles.  When the tiles do not
+ * fill the last round of clusters and at most half of the clusters would be
+ * busy in it, its tiles are spread one per cluster and each cluster's two
+ * CTAs sum the two halves of K, which the epilogue adds: the round takes
+ * half as long.  That changes the fp32 summation order of those tiles only,
+ * so v and du agree with the unsplit schedule to rounding; with the split
+ * off every tile sums K in order in one CTA and the results do not depend
+ * on the GPU's SM count.  On by default.  Process-wide; returns the
+ * previous setting. */
+int poetx_set_w0_split_tail(int enable);
+
 /* ------------------------------------------------------------------------
  * Status and measurement
  * ------------------------------------------------------------------------ */

@@ -22,6 +22,7 @@ __all__ = [
     "poetx_permute_features", "poetx_fold_permutations", "poetx_merge_workspace_size",
     "poetx_merge", "poetx_adam_update", "poetx_quantize_w0", "poetx_dequantize_w0",
     "poetx_set_block_epilogue_fusion",
+    "poetx_set_w0_split_tail",
     "poetx_device_status", "poetx_selftest_wait_timeout", "poetx_launch_count", "poetx_profile_start", "poetx_profile_stop",
     "poetx_profile_query", "poetx_status_string", "EXPORTED_SYMBOLS",
 ]
@@ -71,6 +72,7 @@ _SIGNATURES = {
     "poetx_quantize_w0": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_ptr]),
     "poetx_dequantize_w0": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_ptr]),
     "poetx_set_block_epilogue_fusion": (_c_int, [_c_int]),
+    "poetx_set_w0_split_tail": (_c_int, [_c_int]),
     "poetx_device_status": (_c_int, []),
     "poetx_selftest_wait_timeout": (_c_int, [ctypes.c_uint, _c_ptr]),
     "poetx_launch_count": (ctypes.c_longlong, []),
@@ -243,6 +245,12 @@ def poetx_set_block_epilogue_fusion(enable: bool) -> bool:
     """Turn the W0 GEMM's block-diagonal epilogue on or off (process-wide);
     returns the previous setting."""
     return bool(load_library().poetx_set_block_epilogue_fusion(1 if enable else 0))
+
+
+def poetx_set_w0_split_tail(enable: bool) -> bool:
+    """Turn the K split of the W0 GEMMs' last partial round of tiles on or
+    off (process-wide); returns the previous setting."""
+    return bool(load_library().poetx_set_w0_split_tail(1 if enable else 0))
 
 
 def poetx_device_status() -> int:

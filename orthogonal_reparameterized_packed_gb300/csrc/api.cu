@@ -230,6 +230,10 @@ cudaError_t tc_outer(const bf16* A, const bf16* B, float* part, int d, int S, lo
 // The W0 GEMMs run as clusters of two CTAs that share each B (W0) tile.
 constexpr bool kW0Clusters = true;
 
+// The last, partial round of W0 GEMM tiles is spread one tile per cluster
+// with its K steps split between the two CTAs (poetx_set_w0_split_tail).
+std::atomic<int> g_w0_split_tail{1};
+
 // v = u W0^T (fwd) or du = dv W0 (dgrad), bf16.
 cudaError_t tc_w0(const bf16* A, const bf16* W0, bf16* out, int d_in, int d_out, long long T,
                   bool dgrad, cudaStream_t s) {
@@ -255,6 +259,7 @@ cudaError_t tc_w0(const bf16* A, const bf16* W0, bf16* out, int d_in, int d_out,
   g.epi.row_limit = static_cast<int>(T);
   g.epi.out_rows = T;
   g.cluster2 = kW0Clusters;
+  g.split_tail = g_w0_split_tail.load(std::memory_order_relaxed) != 0;
   return tc_gemm_run(g, s);
 }
 
@@ -1407,6 +1412,10 @@ poetx_status poetx_dequantize_w0(const int8_t* W0_q, const float* scales, void* 
 
 int poetx_set_block_epilogue_fusion(int enable) {
   return g_fuse_block_epilogue.exchange(enable != 0 ? 1 : 0);
+}
+
+int poetx_set_w0_split_tail(int enable) {
+  return g_w0_split_tail.exchange(enable != 0 ? 1 : 0);
 }
 
 }  // extern "C"

@@ -26,6 +26,13 @@
 //          MMA with that block (streamed through the ring) into the same
 //          accumulator; the result is the block output.  Three ring stages
 //          leave room for the staging tile.
+//   CL2    clusters of two CTAs computing adjacent M tiles of one N tile;
+//          each loads half of the shared B tile and multicasts it to both.
+//          When the last round of tiles would leave clusters idle, its tiles
+//          are spread one per cluster instead, the two CTAs taking the two
+//          halves of the K steps; each CTA sends the partial sums of the
+//          rows its peer finishes into the peer's (then idle) ring through
+//          distributed shared memory and adds the peer's for its own rows.
 //
 // Every barrier wait is bounded: on expiry the CTA records
 // POETX_ERR_TIMEOUT, drains what it issued, frees TMEM and returns.
@@ -66,6 +73,10 @@ constexpr int kBlockKSteps = 256 / BK;  // K steps of the epilogue's 256 x 256 b
 struct TcKernelArgs {
   int m_tiles, n_tiles, splits, batches;
   int m_pairs;  // CL2: pairs of M tiles, one per cluster of two CTAs
+  // CL2 work items: units [0, tail_first) whole; each later unit becomes two
+  // items (its two M tiles), each taken by one cluster whose CTAs split its
+  // K steps in halves of k_half; items = tail_first + 2 * (units - tail_first)
+  int tail_first, items, k_half;
   int k_steps_total, k_steps_per_split;
   int a_mn_per_g, a_k_per_g, b_mn_per_g, b_k_per_g;
   EpiArgs epi;
@@ -111,6 +122,33 @@ __device__ __forceinline__ void decode_unit(int t, const TcKernelArgs& p, uint32
   }
 }
 
+// One CTA's share of a work item: tile (g, sp, mt, nt) over K steps
+// [ks0, ks1).  split: a CL2 tail item, whose two CTAs accumulate the two K
+// halves of the same tile and combine them in the epilogue.
+struct WorkItem {
+  int g, sp, mt, nt, ks0, ks1;
+  bool split;
+};
+
+template <bool B_RES, bool CL2>
+__device__ __forceinline__ WorkItem decode_item(int t, const TcKernelArgs& p, uint32_t crank) {
+  WorkItem w;
+  w.split = CL2 && t >= p.tail_first;
+  if (w.split) {
+    // item i of the tail: M tile (i & 1) of unit tail_first + i / 2
+    const int i = t - p.tail_first;
+    decode_unit<B_RES, CL2>(p.tail_first + i / 2, p, static_cast<uint32_t>(i & 1), w.g, w.sp,
+                            w.mt, w.nt);
+    w.ks0 = w.sp * p.k_steps_per_split + static_cast<int>(crank) * p.k_half;
+    w.ks1 = min(w.ks0 + p.k_half, p.k_steps_total);
+  } else {
+    decode_unit<B_RES, CL2>(t, p, crank, w.g, w.sp, w.mt, w.nt);
+    w.ks0 = w.sp * p.k_steps_per_split;
+    w.ks1 = min(w.ks0 + p.k_steps_per_split, p.k_steps_total);
+  }
+  return w;
+}
+
 // Tiles of this CTA: resident variants take a contiguous run, others stride
 // (CL2: over clusters).
 template <bool B_RES, bool CL2>
@@ -133,6 +171,20 @@ struct TileRange {
     }
   }
 };
+
+// Split items: a 64-row half tile of fp32 partial sums in the peer's ring,
+// 1 KiB per row (lr); the 16-byte chunk q of a row sits at chunk q ^ (lr & 7)
+// of its 128-byte group, so eight consecutive rows hit distinct banks.
+__device__ __forceinline__ uint32_t xchg_offset(int q, int lr) {
+  return static_cast<uint32_t>(lr * 1024 + (((q & ~7) | ((q ^ lr) & 7)) << 4));
+}
+
+__device__ __forceinline__ void add_f4(uint32_t* r, const float4 v) {
+  r[0] = __float_as_uint(__uint_as_float(r[0]) + v.x);
+  r[1] = __float_as_uint(__uint_as_float(r[1]) + v.y);
+  r[2] = __float_as_uint(__uint_as_float(r[2]) + v.z);
+  r[3] = __float_as_uint(__uint_as_float(r[3]) + v.w);
+}
 
 // EPI_BLOCK: this warp's 32 accumulator rows (256 fp32 columns) -> bf16 rows
 // of the 128 x 256 staging tile, laid out as four 128B-swizzled K-major
@@ -175,6 +227,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                    const __grid_constant__ CUtensorMap tmY, const TcKernelArgs p) {
   using S = TcShape<BN, B_RES, EPI>;
   static_assert(!CL2 || (EPI == EPI_TMA_BF16 && !B_RES && BN == 256), "clusters: W0 GEMMs");
+  static_assert(!CL2 || S::STAGES * S::A_BYTES >= 64 * BN * 4, "split items: 64 fp32 rows in sA");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -192,13 +245,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* bempty_bar = bfull_bar + 1;
   uint64_t* vstaged_bar = bempty_bar + 1;  // EPI_BLOCK: staging tile written (4 warps)
   uint64_t* yfull_bar = vstaged_bar + 1;   // EPI_BLOCK: block MMA done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(yfull_bar + 1);
+  uint64_t* xready_bar = yfull_bar + 1;    // CL2 split item: the peer's ring is free
+  uint64_t* xfull_bar = xready_bar + 1;    // CL2 split item: the peer's partial rows are here
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xfull_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
   const uint32_t crank = CL2 ? cluster_ctarank() : 0u;
-  const int num_tiles = p.batches * p.splits * (CL2 ? p.m_pairs : p.m_tiles) * p.n_tiles;
+  const int num_tiles = CL2 ? p.items : p.batches * p.splits * p.m_tiles * p.n_tiles;
   const TileRange<B_RES, CL2> range(num_tiles);
 
   if (threadIdx.x == 0) {
@@ -215,6 +270,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(bempty_bar, 1);
     mbar_init(vstaged_bar, 4);
     mbar_init(yfull_bar, 1);
+    mbar_init(xready_bar, 1);
+    mbar_init(xfull_bar, 64);  // the peer's two sending warps, every lane
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -274,10 +331,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         return true;
       };
       for (int tile = range.first; tile < range.end && ok; tile += range.step) {
-        int g, sp, mt, nt;
-        decode_unit<B_RES, CL2>(tile, p, crank, g, sp, mt, nt);
-        const int ks0 = sp * p.k_steps_per_split;
-        const int ks1 = min(ks0 + p.k_steps_per_split, p.k_steps_total);
+        const WorkItem item = decode_item<B_RES, CL2>(tile, p, crank);
+        const int g = item.g, mt = item.mt, nt = item.nt, ks0 = item.ks0, ks1 = item.ks1;
         const int a_mn = g * p.a_mn_per_g + mt * BM;
         const int b_mn = g * p.b_mn_per_g + nt * BN;
         if (B_RES) {
@@ -320,7 +375,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tma_load_2d(a_dst, &tmA, &full_bar[stage], a_mn, a_k);
             tma_load_2d(a_dst + 8192, &tmA, &full_bar[stage], a_mn + 64, a_k);
           }
-          if (!B_RES && CL2) {
+          if (!B_RES && CL2 && item.split) {
+            // split item: the CTAs read different K steps, each its whole B tile
+            const int b_k = g * p.b_k_per_g + ks * BK;
+            uint8_t* b_dst = sB + stage * S::B_BYTES;
+            if (!B_MN) {
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh)
+                tma_load_2d(b_dst + hh * (BN / 2) * 128, &tmB, &full_bar[stage], b_k,
+                            b_mn + hh * (BN / 2));
+            } else {
+#pragma unroll
+              for (int c = 0; c < BN / 64; ++c)
+                tma_load_2d(b_dst + c * 8192, &tmB, &full_bar[stage], b_mn + 64 * c, b_k);
+            }
+          } else if (!B_RES && CL2) {
             // this CTA's half of the shared B tile, delivered to both CTAs
             const int b_k = g * p.b_k_per_g + ks * BK;
             uint8_t* b_dst = sB + stage * S::B_BYTES;
@@ -432,10 +501,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         return true;
       };
       for (int tile = range.first; tile < range.end && ok; tile += range.step) {
-        int g, sp, mt, nt;
-        decode_unit<B_RES, CL2>(tile, p, crank, g, sp, mt, nt);
-        const int ks0 = sp * p.k_steps_per_split;
-        const int ks1 = min(ks0 + p.k_steps_per_split, p.k_steps_total);
+        const WorkItem item = decode_item<B_RES, CL2>(tile, p, crank);
+        const int g = item.g, nt = item.nt, ks0 = item.ks0, ks1 = item.ks1;
         if (B_RES) {
           const int key = g * p.n_tiles + nt;
           if (key != res_key) {
@@ -545,8 +612,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       return true;
     };
     for (int tile = range.first; tile < range.end; tile += range.step) {
-      int g, sp, mt, nt;
-      decode_unit<B_RES, CL2>(tile, p, crank, g, sp, mt, nt);
+      const WorkItem item = decode_item<B_RES, CL2>(tile, p, crank);
+      const int g = item.g, sp = item.sp, mt = item.mt, nt = item.nt;
       const bool got = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag);
       if (!__all_sync(0xffffffffu, got)) {  // the whole warp unwinds together
         record_timeout(p.status, abort_flag);
@@ -592,19 +659,68 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           epilogue_row32(p.epi, g, sp, row, nt * BN + c0, r);
         }
       } else {
+        // split item (the last of this CTA): the two CTAs hold the two K halves
+        // of one tile; rank r finishes rows 64r .. 64r+63, and the warps with
+        // the other half's rows send their partial sums into the peer's ring
+        bool send_only = false;
+        const uint8_t* recv = nullptr;  // the peer's partial sums (finishing warps)
+        const int lr = (quarter & 1) * 32 + lane;  // row within the half
+        if (CL2 && item.split) {
+          const uint32_t peer = crank ^ 1u;
+          // this CTA's MMAs are done and no load follows: its ring is free
+          if (quarter == 0 && lane == 0) mbar_arrive_remote(map_peer(smem_u32(xready_bar), peer));
+          if ((quarter >> 1) != static_cast<int>(crank)) {
+            send_only = true;
+            const bool ready = mbar_wait_cluster(xready_bar, 0, abort_flag);
+            if (!__all_sync(0xffffffffu, ready)) {
+              record_timeout(p.status, abort_flag);
+              break;
+            }
+            const uint32_t dst = map_peer(smem_u32(sA), peer);
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+              uint32_t r[32];
+              tmem_load_32cols(t_base + c0, r);
+              tmem_load_wait();
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                st_cluster_v4(dst + xchg_offset(c0 / 4 + i, lr), r[4 * i], r[4 * i + 1],
+                              r[4 * i + 2], r[4 * i + 3]);
+            }
+            mbar_arrive_remote(map_peer(smem_u32(xfull_bar), peer));
+          } else {
+            const bool full = mbar_wait_cluster(xfull_bar, 0, abort_flag);
+            if (!__all_sync(0xffffffffu, full)) {
+              record_timeout(p.status, abort_flag);
+              break;
+            }
+            recv = sA;
+          }
+        }
         // TMA tile stores: 128-byte rows of 64 bf16 or 32 fp32 per chunk
         constexpr int CW = EPI == EPI_TMA_BF16 ? 64 : 32;
         const int out_row = g * p.epi.row_g + sp * p.epi.row_s + mt * BM + quarter * 32;
         const int out_col0 = g * p.epi.col_g + nt * BN;
         uint8_t* my_row = stg + lane * 128;
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += CW) {
+        for (int c0 = 0; c0 < BN && !send_only; c0 += CW) {
           uint32_t w[32];  // this lane's 128 bytes of the chunk
           if (EPI == EPI_TMA_BF16) {
             uint32_t r0[32], r1[32];
             tmem_load_32cols(t_base + c0, r0);
             tmem_load_32cols(t_base + c0 + 32, r1);
             tmem_load_wait();
+            if (CL2 && recv != nullptr) {  // + the peer's K half
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float4 a =
+                    *reinterpret_cast<const float4*>(recv + xchg_offset(c0 / 4 + i, lr));
+                const float4 b =
+                    *reinterpret_cast<const float4*>(recv + xchg_offset(c0 / 4 + 8 + i, lr));
+                add_f4(r0 + 4 * i, a);
+                add_f4(r1 + 4 * i, b);
+              }
+            }
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
               w[j] = pack_bf16x2(r0[2 * j], r0[2 * j + 1]);
@@ -714,6 +830,7 @@ cudaError_t launch_tc(const TcGemm& g, cudaStream_t stream) {
   TcKernelArgs p;
   p.m_tiles = (g.M + BM - 1) / BM;
   p.m_pairs = (p.m_tiles + 1) / 2;
+  p.tail_first = p.items = p.k_half = 0;  // set for CL2 below
   p.n_tiles = g.N / BN;
   p.k_steps_total = (g.K + BK - 1) / BK;
   const int splits = tc_effective_splits(g.K, g.splits);
@@ -733,7 +850,25 @@ cudaError_t launch_tc(const TcGemm& g, cudaStream_t stream) {
     const long long units =
         static_cast<long long>(p.batches) * p.splits * p.m_pairs * p.n_tiles;
     if (units <= 0) return cudaSuccess;
-    const int clusters = static_cast<int>(std::min<long long>(units, max_clusters[dev]));
+    const long long cmax = max_clusters[dev];
+    int clusters = static_cast<int>(std::min<long long>(units, cmax));
+    // A last round of r < cmax units leaves clusters idle; when 2r fit in one
+    // round, its 2r tiles go to 2r clusters instead, each tile's K steps
+    // split between the cluster's two CTAs (half the round's time).
+    p.tail_first = static_cast<int>(units);
+    p.items = static_cast<int>(units);
+    p.k_half = p.k_steps_total / 2;
+    if (g.split_tail && p.batches == 1 && p.splits == 1 && p.k_steps_total % 2 == 0) {
+      const long long r = units % cmax;
+      if (units >= cmax && r > 0 && 2 * r <= cmax) {
+        p.tail_first = static_cast<int>(units - r);
+        p.items = static_cast<int>(units + r);
+      } else if (units < cmax && 2 * units <= cmax) {
+        p.tail_first = 0;
+        p.items = static_cast<int>(2 * units);
+        clusters = static_cast<int>(2 * units);
+      }
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters);
     cfg.blockDim = dim3(NUM_THREADS);

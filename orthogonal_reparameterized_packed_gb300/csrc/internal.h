@@ -74,6 +74,9 @@ struct TcGemm {
   // W0 GEMMs: run as clusters of two CTAs on adjacent M tiles that load one
   // half of each shared B tile each (TMA multicast)
   bool cluster2 = false;
+  // cluster2: when the last round of tiles would leave clusters idle, spread
+  // its tiles one per cluster, the two CTAs summing halves of K
+  bool split_tail = false;
   TcOperand A, B;
   EpiArgs epi;
   // Block-diagonal factor in the epilogue (W0 GEMMs, BN = 256): N tile j of

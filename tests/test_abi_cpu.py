@@ -181,3 +181,11 @@ def test_index_map_calls_reject_invalid_arguments(lib):
     assert L.poetx_permute_features(None, None, None, 0, 64, F, None) == 0  # no rows
     assert L.poetx_fold_permutations(FAKE, FAKE, FAKE + 4, FAKE + 4096, 64, 64, B, None) == 1
     assert L.poetx_fold_permutations(FAKE, FAKE, FAKE, FAKE + 4096, 25608, 64, B, None) == 1
+
+
+def test_process_wide_switches_return_the_previous_setting(lib):
+    # host-only state: block-epilogue fusion off and the W0 tail split on by default
+    assert poetx.poetx_set_block_epilogue_fusion(False) is False
+    assert poetx.poetx_set_w0_split_tail(False) is True
+    assert poetx.poetx_set_w0_split_tail(True) is False
+    assert poetx.poetx_set_w0_split_tail(True) is True

@@ -1,7 +1,9 @@
 """The W0 GEMM with the block-diagonal factor in its epilogue (opt-in):
 parity with the oracle at the layer tolerances, and the same bits as the
 unfused path (the block product runs the same MMA sequence on the same
-bf16-rounded tile, whether it comes from HBM or from the staging tile)."""
+bf16-rounded tile, whether it comes from HBM or from the staging tile).
+The bit comparison runs with the unfused GEMM's K split of its last round
+off, so that both sum every tile's K steps in the same order."""
 
 import numpy as np
 import pytest
@@ -35,11 +37,13 @@ def run(px, inp, fused, recompute_v=False):
     layer = PoetxLayer(inp.d_in, inp.d_out, inp.b, inp.k, inp.tokens, dtype=inp.dtype,
                        recompute_v=recompute_v)
     prev = px.poetx_set_block_epilogue_fusion(fused)
+    prev_split = px.poetx_set_w0_split_tail(False)
     try:
         layer.step(dev["theta_P"], dev["theta_R"], dev["W0"], dev["x"], dev["dy"])
         torch.cuda.synchronize()
     finally:
         px.poetx_set_block_epilogue_fusion(prev)
+        px.poetx_set_w0_split_tail(prev_split)
     st = px.poetx_device_status()
     assert st == 0, px.poetx_status_string(st)
     return layer
