@@ -54,7 +54,8 @@ enum { EPI_ROWS = 0, EPI_TMA_BF16 = 1, EPI_TMA_F32 = 2, EPI_BLOCK = 3 };
 
 template <int BN, bool B_RES, int EPI>
 struct TcShape {
-  static constexpr int STAGES = EPI == EPI_BLOCK ? 3 : 4;
+  // resident B: only A streams, and a fifth 16 KiB stage still fits
+  static constexpr int STAGES = EPI == EPI_BLOCK ? 3 : (B_RES ? 5 : 4);
   static constexpr int A_BYTES = BM * BK * 2;  // 16 KB
   static constexpr int B_BYTES = BN * BK * 2;  // one K step of B: 16 or 32 KB
   static constexpr int RING = B_RES ? STAGES * A_BYTES : STAGES * (A_BYTES + B_BYTES);

@@ -20,9 +20,12 @@
 // 256-column accumulator for the sum, 512 columns in all.
 //
 // Warp roles: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 2-5
-// epilogue (row-per-thread 16-byte stores: the shared memory a TMA-store
-// staging tile would take holds two more gradient chunks in flight).  Every wait is bounded; on expiry the CTA records
-// POETX_ERR_TIMEOUT, lets its copies and MMAs in flight land and returns.
+// epilogue (transform tiles: row-per-thread 16-byte stores, as the shared
+// memory a TMA-store staging tile would take holds two more gradient chunks
+// in flight; the split's partial sum at the end: staged in the then idle
+// operand rings and stored by TMA).  Every wait is bounded; on expiry the CTA
+// records POETX_ERR_TIMEOUT, lets its copies and MMAs in flight land and
+// returns.
 #include <algorithm>
 
 #include "internal.h"
@@ -47,6 +50,8 @@ constexpr int TS_SMEM =
     1024 + TS_RES_BYTES + TS_XSTAGES * TS_X_BYTES + TS_ZSTAGES * TS_Z_BYTES + TS_BAR_BYTES;
 constexpr uint32_t TS_TMEM_COLS = 512;
 static_assert(TS_SMEM <= 227 * 1024, "shared memory per CTA");
+// the final partial sum is staged in the idle X and Z rings: 4 warps x 32 KiB
+static_assert(TS_XSTAGES * TS_X_BYTES + TS_ZSTAGES * TS_Z_BYTES >= 4 * 32768, "staging room");
 
 struct TsArgs {
   int d;            // features (multiple of 256)
@@ -63,6 +68,7 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
     transform_sum_kernel(const __grid_constant__ CUtensorMap tmX,   // X [T][d], box 64 x 128
                          const __grid_constant__ CUtensorMap tmZ,   // Z [T][d], box 64 x 128
                          const __grid_constant__ CUtensorMap tmB,   // SB [d][256], box 64 x 64
+                         const __grid_constant__ CUtensorMap tmP,   // part [splits*d][256] fp32, box 32 x 32
                          const TsArgs p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>(
@@ -115,6 +121,7 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
     tma_prefetch_desc(&tmX);
     tma_prefetch_desc(&tmZ);
     tma_prefetch_desc(&tmB);
+    tma_prefetch_desc(&tmP);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, TS_TMEM_COLS);
@@ -307,24 +314,38 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
       if (acc == 0) acc_phase ^= 1;
     }
     if (ok && t_end > t_first) {
-      // the split's partial sum: row h*128 + row_in_tile of part[s][g], fp32
+      // the split's partial sum: rows h*128 + 32*quarter .. of part[s][g], fp32.
+      // Once the last MMA is done the operand rings are idle: each warp stages
+      // its 32 rows there as eight 128B-swizzled 32 x 32 boxes (32 KiB per
+      // warp, 128 KiB in all across the X and Z rings) and stores them by TMA.
       const bool got = mbar_wait(gfull_bar, 0, abort_flag);
       if (!__all_sync(0xffffffffu, got)) {
         record_timeout(p.status, abort_flag);
       } else {
         tc_fence_after();
         const uint32_t g_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + 256u;
-        const long long prow = static_cast<long long>(s) * p.d + col_blk + h * 128 + row_in_tile;
-        uint4* dst = reinterpret_cast<uint4*>(p.part + prow * 256);
+        uint8_t* stg = sX + quarter * 32768;
 #pragma unroll 1
-        for (int c0 = 0; c0 < 256; c0 += 32) {
+        for (int cc = 0; cc < 8; ++cc) {
           uint32_t r[32];
-          tmem_load_32cols(g_base + c0, r);
+          tmem_load_32cols(g_base + cc * 32, r);
           tmem_load_wait();
+          uint8_t* row = stg + cc * 4096 + lane * 128;
 #pragma unroll
           for (int q = 0; q < 8; ++q)
-            dst[c0 / 4 + q] = make_uint4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+            st_shared_v4(row + ((q ^ (lane & 7)) << 4), r[4 * q], r[4 * q + 1], r[4 * q + 2],
+                         r[4 * q + 3]);
         }
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0) {
+          const int prow0 = s * p.d + col_blk + h * 128 + quarter * 32;
+#pragma unroll 1
+          for (int cc = 0; cc < 8; ++cc) tma_store_2d(&tmP, stg + cc * 4096, cc * 32, prow0);
+          bulk_commit();
+          bulk_wait_all();
+        }
+        __syncwarp();
       }
     }
   }
@@ -365,9 +386,10 @@ cudaError_t tc_transform_sum(const __nv_bfloat16* X, const __nv_bfloat16* Z,
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  CUtensorMap tmX, tmZ, tmB;
+  CUtensorMap tmX, tmZ, tmB, tmP;
   if (!make_map(&tmX, X, T, d, d, 2, 64, BM) || !make_map(&tmZ, Z, T, d, d, 2, 64, BM) ||
-      !make_map(&tmB, sb, d, 256, 256, 2, 64, 64))
+      !make_map(&tmB, sb, d, 256, 256, 2, 64, 64) ||
+      !make_map(&tmP, part, static_cast<long long>(splits) * d, 256, 256, 4, 32, 32))
     return cudaErrorInvalidValue;
   if (reinterpret_cast<uintptr_t>(out) % 16 != 0 || reinterpret_cast<uintptr_t>(part) % 16 != 0)
     return cudaErrorInvalidValue;
@@ -383,7 +405,7 @@ cudaError_t tc_transform_sum(const __nv_bfloat16* X, const __nv_bfloat16* Z,
   const int grid = 2 * (d / 256) * splits;
   prof_begin("transform_sum", stream);
   cudaError_t e = launch_pdl(transform_sum_kernel, dim3(grid), dim3(TS_THREADS), TS_SMEM, stream,
-                             tmX, tmZ, tmB, a);
+                             tmX, tmZ, tmB, tmP, a);
   prof_end("transform_sum", stream);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
