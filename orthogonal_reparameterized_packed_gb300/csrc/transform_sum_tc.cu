@@ -19,8 +19,8 @@
 // the transform tiles (the epilogue of one overlaps the next) and one
 // 256-column accumulator for the sum, 512 columns in all.
 //
-// Warp roles: warp 0 TMA producer, warp 1 TMEM owner + MMA issuer, warps 2-5
-// epilogue (transform tiles: row-per-thread 16-byte stores, as the shared
+// Warp roles: warp 0 TMA producer, warp 1 TMEM owner + transform MMA issuer,
+// warp 6 token-sum MMA issuer, warps 2-5 epilogue (transform tiles: row-per-thread 16-byte stores, as the shared
 // memory a TMA-store staging tile would take holds two more gradient chunks
 // in flight; the split's partial sum at the end: staged in the then idle
 // operand rings and stored by TMA).  Every wait is bounded; on expiry the CTA
@@ -36,7 +36,7 @@ namespace poetx {
 
 namespace {
 
-constexpr int TS_THREADS = 192;
+constexpr int TS_THREADS = 224;
 constexpr int TS_XSTAGES = 6;                  // X ring: one 128 x 64 chunk per stage
 // a tile's chunk pairs (0,1), (2,3) sit in adjacent slots (2i, 2i+1): tiles
 // start on even slots when the ring length is even
@@ -50,6 +50,8 @@ constexpr int TS_SMEM =
     1024 + TS_RES_BYTES + TS_XSTAGES * TS_X_BYTES + TS_ZSTAGES * TS_Z_BYTES + TS_BAR_BYTES;
 constexpr uint32_t TS_TMEM_COLS = 512;
 static_assert(TS_SMEM <= 227 * 1024, "shared memory per CTA");
+static_assert((2 * TS_XSTAGES + 2 * TS_ZSTAGES + 4 + 2 + 2) * 8 + 8 <= TS_BAR_BYTES,
+              "barriers exceed their shared-memory area");
 // the final partial sum is staged in the idle X and Z rings: 4 warps x 32 KiB
 static_assert(TS_XSTAGES * TS_X_BYTES + TS_ZSTAGES * TS_Z_BYTES >= 4 * 32768, "staging room");
 
@@ -84,8 +86,8 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
   uint64_t* tempty_bar = tfull_bar + 2;           // [2]
   uint64_t* bfull_bar = tempty_bar + 2;
   uint64_t* gfull_bar = bfull_bar + 1;
-  uint64_t* drain_bar = gfull_bar + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  uint64_t* drain_bar = gfull_bar + 1;   // [2]: one per MMA issuer
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain_bar + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32;
@@ -101,7 +103,7 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < TS_XSTAGES; ++i) {
       mbar_init(&full_bar[i], 1);
-      mbar_init(&empty_bar[i], 1);
+      mbar_init(&empty_bar[i], 2);  // released by both MMA issuers
     }
     for (int i = 0; i < TS_ZSTAGES; ++i) {
       mbar_init(&zfull_bar[i], 1);
@@ -113,7 +115,8 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
     }
     mbar_init(bfull_bar, 1);
     mbar_init(gfull_bar, 1);
-    mbar_init(drain_bar, 1);
+    mbar_init(&drain_bar[0], 1);
+    mbar_init(&drain_bar[1], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -197,13 +200,19 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
         }
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == 6) {
     if (lane == 0) {
-      // ------------------------------------------------------- MMA issuer
+      // ------------------------------------------------------ MMA issuers
+      // Warp 1 issues the transform tiles (into the two rotating
+      // accumulators), warp 6 the token sums (into the persistent one): two
+      // threads keep the tensor pipe fed through each other's barrier waits.
+      // An X slot is free once both have committed it.
+      const bool sums = warp == 6;
       constexpr uint32_t IDESC_T = instr_desc_bf16(BM, 128, false, true);  // X K-major, SB MN-major
       constexpr uint32_t IDESC_S = instr_desc_bf16(BM, 128, true, true);   // Z, X both MN-major
       const uint32_t g_tmem = tmem_base + 256u;
-      bool ok = mbar_wait(bfull_bar, 0, abort_flag);
+      uint64_t* my_drain = &drain_bar[sums ? 1 : 0];
+      bool ok = sums || mbar_wait(bfull_bar, 0, abort_flag);  // SB: transforms only
       if (!ok) record_timeout(p.status, abort_flag);
       tc_fence_after();
       bool any_mma = false;
@@ -211,8 +220,9 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
       uint32_t xphase = 0, zphase = 0, acc_phase = 0;
       const uint32_t res_base = smem_u32(sRes);
       for (int t = t_first; t < t_end && ok; ++t) {
-        if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1, abort_flag) ||
-            !mbar_wait(&zfull_bar[zs], zphase, abort_flag)) {
+        const bool ready = sums ? mbar_wait(&zfull_bar[zs], zphase, abort_flag)
+                                : mbar_wait(&tempty_bar[acc], acc_phase ^ 1, abort_flag);
+        if (!ready) {
           record_timeout(p.status, abort_flag);
           ok = false;
           break;
@@ -228,13 +238,16 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
           }
           tc_fence_after();
           const uint32_t x_base = smem_u32(sX + xs * TS_X_BYTES);
-          // transform: out tile += X chunk c (K = features 64c ..) x SB rows 64c ..
+          if (!sums) {
+            // transform: out tile += X chunk c (K = features 64c ..) x SB rows 64c ..
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            umma_bf16(t_tmem, smem_desc_sw128(x_base + j * 32, 16, 1024),
-                      smem_desc_sw128(res_base + c * 16384 + j * 2048, 8192, 1024), IDESC_T,
-                      (c > 0 || j > 0) ? 1u : 0u);
-          if (c & 1) {
+            for (int j = 0; j < 4; ++j)
+              umma_bf16(t_tmem, smem_desc_sw128(x_base + j * 32, 16, 1024),
+                        smem_desc_sw128(res_base + c * 16384 + j * 2048, 8192, 1024), IDESC_T,
+                        (c > 0 || j > 0) ? 1u : 0u);
+            umma_commit(&empty_bar[xs]);
+            any_mma = true;
+          } else if (c & 1) {
             // token sum over chunks c-1, c (adjacent ring slots: a tile's chunk
             // i always sits in slot i): G[m][64(c-1) ..] += sum_t Z[t][m] X[t][..]
             const uint32_t x_pair = x_base - TS_X_BYTES;
@@ -246,29 +259,32 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
                         (t > t_first || j > 0) ? 1u : 0u);
             umma_commit(&empty_bar[xs - 1]);
             umma_commit(&empty_bar[xs]);
+            any_mma = true;
           }
-          any_mma = true;
           if (++xs == TS_XSTAGES) {
             xs = 0;
             xphase ^= 1;
           }
         }
         if (!ok) break;
-        umma_commit(&tfull_bar[acc]);
-        umma_commit(&zempty_bar[zs]);
-        if (++zs == TS_ZSTAGES) {
-          zs = 0;
-          zphase ^= 1;
+        if (!sums) {
+          umma_commit(&tfull_bar[acc]);
+          acc ^= 1;
+          if (acc == 0) acc_phase ^= 1;
+        } else {
+          umma_commit(&zempty_bar[zs]);
+          if (++zs == TS_ZSTAGES) {
+            zs = 0;
+            zphase ^= 1;
+          }
         }
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1;
       }
       if (ok) {
-        umma_commit(gfull_bar);  // the split's sum is complete
+        if (sums) umma_commit(gfull_bar);  // the split's sum is complete
       } else if (any_mma) {
-        umma_commit(drain_bar);
+        umma_commit(my_drain);
         const unsigned long long t0 = global_timer_ns();
-        while (!mbar_try_wait(drain_bar, 0) && global_timer_ns() - t0 < 10000000ull) {
+        while (!mbar_try_wait(my_drain, 0) && global_timer_ns() - t0 < 10000000ull) {
         }
       }
     }
