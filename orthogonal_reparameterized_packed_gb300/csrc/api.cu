@@ -28,16 +28,22 @@ namespace poetx {
 
 __device__ int g_status_word;
 
+// Per-device caches below are filled on first use; several host threads may
+// race to fill one, which is harmless (they store the same value).
 int* device_status_ptr() {
-  static int* ptrs[64] = {};
+  static std::atomic<int*> ptrs[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return nullptr;
-  if (ptrs[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status_word) == cudaSuccess) ptrs[dev] = static_cast<int*>(p);
+  int* p = ptrs[dev].load(std::memory_order_relaxed);
+  if (p == nullptr) {
+    void* sym = nullptr;
+    if (cudaGetSymbolAddress(&sym, g_status_word) == cudaSuccess) {
+      p = static_cast<int*>(sym);
+      ptrs[dev].store(p, std::memory_order_relaxed);
+    }
   }
-  return ptrs[dev];
+  return p;
 }
 
 int read_and_clear_device_status() {
@@ -49,16 +55,18 @@ int read_and_clear_device_status() {
 }
 
 int sm_count() {
-  static int counts[64] = {};
+  static std::atomic<int> counts[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return 1;
-  if (counts[dev] == 0) {
+  int n = counts[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
     int c = 0;
     cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev);
-    counts[dev] = c > 0 ? c : 1;
+    n = c > 0 ? c : 1;
+    counts[dev].store(n, std::memory_order_relaxed);
   }
-  return counts[dev];
+  return n;
 }
 
 namespace {

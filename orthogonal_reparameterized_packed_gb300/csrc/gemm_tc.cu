@@ -38,6 +38,7 @@
 // POETX_ERR_TIMEOUT, drains what it issued, frees TMEM and returns.
 #include <algorithm>
 #include <cstdio>
+#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -772,11 +773,14 @@ template <bool A_MN, bool B_MN, int BN, bool B_RES, int EPI, bool CL2 = false>
 cudaError_t launch_tc(const TcGemm& g, cudaStream_t stream) {
   using S = TcShape<BN, B_RES, EPI>;
   auto* kernel = tc_gemm_kernel<A_MN, B_MN, BN, B_RES, EPI, CL2>;
+  // per device, once: the shared-memory attribute and (CL2) the cluster count
   static bool attr_set[64] = {false};
   static int max_clusters[64] = {0};
+  static std::mutex mu;
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::unique_lock<std::mutex> lock(mu);
   if (!attr_set[dev]) {
     cudaError_t e =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
@@ -801,6 +805,8 @@ cudaError_t launch_tc(const TcGemm& g, cudaStream_t stream) {
     }
     attr_set[dev] = true;
   }
+  const long long cmax = max_clusters[dev];
+  lock.unlock();
   CUtensorMap tmA, tmB, tmC, tmR, tmY;
   if (!make_map(&tmA, g.A.ptr, g.A.rows, g.A.cols, g.A.pitch, 2, 64, A_MN ? 64 : BM))
     return cudaErrorInvalidValue;
@@ -851,7 +857,6 @@ cudaError_t launch_tc(const TcGemm& g, cudaStream_t stream) {
     const long long units =
         static_cast<long long>(p.batches) * p.splits * p.m_pairs * p.n_tiles;
     if (units <= 0) return cudaSuccess;
-    const long long cmax = max_clusters[dev];
     int clusters = static_cast<int>(std::min<long long>(units, cmax));
     // A last round of r < cmax units leaves clusters idle; when 2r fit in one
     // round, its 2r tiles go to 2r clusters instead, each tile's K steps

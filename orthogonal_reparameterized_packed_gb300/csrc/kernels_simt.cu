@@ -3,6 +3,7 @@
 // tolerance, and for blocks narrower than one 128-wide MMA tile), plus the
 // small elementwise kernels of the path (unpack, superblock expansion,
 // split-K reduction, skew projection and pack).
+#include <mutex>
 #include <type_traits>
 
 #include "internal.h"
@@ -736,13 +737,17 @@ cudaError_t launch_permute_rows(const void* in, long long in_rows, const int* ro
   const void* fn = is_bf16 ? reinterpret_cast<const void*>(permute_rows_kernel<__nv_bfloat16>)
                            : reinterpret_cast<const void*>(permute_rows_kernel<float>);
   static bool attr_set[2][64] = {};
+  static std::mutex mu;
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[is_bf16][dev]) {
-    cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
-                         cudaSharedmemCarveoutMaxShared);
-    cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    attr_set[is_bf16][dev] = true;
+  if (dev >= 0 && dev < 64) {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!attr_set[is_bf16][dev]) {
+      cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+      attr_set[is_bf16][dev] = true;
+    }
   }
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kPermThreads, smem) !=

@@ -27,6 +27,7 @@
 // records POETX_ERR_TIMEOUT, lets its copies and MMAs in flight land and
 // returns.
 #include <algorithm>
+#include <mutex>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -394,13 +395,18 @@ cudaError_t tc_transform_sum(const __nv_bfloat16* X, const __nv_bfloat16* Z,
   if (T <= 0) return cudaSuccess;
   if (d <= 0 || d % 256 != 0 || splits != transform_sum_splits(d, T)) return cudaErrorInvalidValue;
   static bool attr_set[64] = {false};
+  static std::mutex mu;
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(transform_sum_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, TS_SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!attr_set[dev]) {
+      cudaError_t e = cudaFuncSetAttribute(transform_sum_kernel,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, TS_SMEM);
+      if (e != cudaSuccess) return e;
+      attr_set[dev] = true;
+    }
   }
   CUtensorMap tmX, tmZ, tmB, tmP;
   if (!make_map(&tmX, X, T, d, d, 2, 64, BM) || !make_map(&tmZ, Z, T, d, d, 2, 64, BM) ||
