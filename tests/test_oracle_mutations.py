@@ -1,8 +1,10 @@
 """The pins catch plausible mistakes in the oracle.  Each case plants one
 mistake in a copy of the oracle (a transposed operand, a flipped sign, a
-dropped or extra term, a wrong index formula), runs the pin tests against the
-copy in a fresh interpreter and expects them to fail; the unmodified copy
-must pass.  CPU only; the repository's oracle is never touched."""
+dropped or extra term, a wrong index formula, a wrong rounding) in the layer,
+its permuted variant, the merge, Adam and the INT8 weight, runs the pin tests
+against the copy in a fresh interpreter and expects them to fail; the
+unmodified copy must pass.  CPU only; the repository's oracle is never
+touched."""
 
 import os
 import shutil
@@ -38,6 +40,18 @@ MUTATIONS = [
      "G[g] = B[:, g * b:(g + 1) * b].T @ A[:, g * b:(g + 1) * b]"),
     ("power derivative with a wrong exponent", "G_Q += c[i] * (pw[j] @ G @ pw[i - 1 - j])",
      "G_Q += c[i] * (pw[j] @ G @ pw[i - j])"),
+    ("permuted factor conjugated the wrong way", "P = PiP.T @ BP @ PiP", "P = PiP @ BP @ PiP.T"),
+    ("permuted block gradient transposed", "dBP = a_P.T @ c_P", "dBP = c_P.T @ a_P"),
+    ("merge with R transposed", "return R @ np.asarray(W0, dtype=np.float64) @ P",
+     "return R.T @ np.asarray(W0, dtype=np.float64) @ P"),
+    ("Adam without the first moment's bias correction", "m_hat = m / (1 - beta1 ** step)",
+     "m_hat = m"),
+    ("Adam second moment of the raw gradient", "(1 - beta2) * grad * grad", "(1 - beta2) * grad"),
+    ("Adam weight decay with the wrong sign", "+ weight_decay * theta)", "- weight_decay * theta)"),
+    ("INT8 scale over 128 steps", "s = np.float32(amax / np.float32(127))",
+     "s = np.float32(amax / np.float32(128))"),
+    ("INT8 codes truncated instead of rounded", "q = np.rint(W[o] / s)", "q = np.floor(W[o] / s)"),
+    ("dequantisation divides by the scale", "return q * s[:, None]", "return q / s[:, None]"),
 ]
 
 
