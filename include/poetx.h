@@ -248,11 +248,13 @@ int poetx_set_block_epilogue_fusion(int enable);
 
 /* Scheduling of the W0 GEMMs (technical summary, section 2: the frozen-
  * weight product; the schedule is this library's).  The GEMMs run as
- * clusters of two CTAs on 128 x 256 output tiles.  When the tiles do not
- * fill the last round of clusters and at most half of the clusters would be
- * busy in it, its tiles are spread one per cluster and each cluster's two
- * CTAs sum the two halves of K, which the epilogue adds: the round takes
- * half as long.  That changes the fp32 summation order of those tiles only,
+ * clusters of two CTAs, each cluster on two 128 x 256 output tiles at a
+ * time.  When the last round keeps at most half of the clusters busy (r
+ * pairs of tiles with 2r <= clusters) and K is an even number of 64-wide
+ * steps, its 2r tiles are spread one per cluster and each cluster's two CTAs
+ * sum the two halves of K, which the epilogue adds: the round takes half as
+ * long.  GEMMs with at most half as many tile pairs as clusters run split
+ * entirely.  That changes the fp32 summation order of those tiles only,
  * so v and du agree with the unsplit schedule to rounding; with the split
  * off every tile sums K in order in one CTA and the results do not depend
  * on the GPU's SM count.  On by default.  Process-wide; returns the
