@@ -50,3 +50,39 @@ def test_single_process_max_is_identity():
     import bench
     assert bench.max_over_ranks(2.25) == 2.25
     assert bench.job_throughput(16384, 1, 1.0) == pytest.approx(16384e3)
+
+
+def _reference_lines(stdout):
+    import json
+    return [json.loads(l) for l in stdout.splitlines() if l.startswith("{")]
+
+
+def test_reference_arm_json_line():
+    # the reference arm is the float64 oracle on the host cores: one JSON line
+    # with the contract's keys, its own cpu_baseline and a host-only e2e
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1",
+                        "--warmup", "0", "--workload", "fp32_256_b32"], capture_output=True,
+                       text=True, env=env, cwd=ROOT, timeout=300)
+    assert r.returncode == 0, r.stdout + r.stderr
+    lines = _reference_lines(r.stdout)
+    assert len(lines) == 1
+    d = lines[0]
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["value"] > 0 and d["higher_is_better"] is True
+    assert d["config"]["workload"] == "fp32_256_b32"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_prints_on_rank_zero_only():
+    r = _torchrun(["bench.py", "--impl", "reference", "--gpus", "2", "--steps", "1",
+                   "--warmup", "0", "--workload", "fp32_256_b32"])
+    assert r.returncode == 0, r.stdout + r.stderr
+    lines = _reference_lines(r.stdout)
+    assert len(lines) == 1 and lines[0]["impl"] == "reference"
