@@ -26,8 +26,8 @@
 //          MMA with that block (streamed through the ring) into the same
 //          accumulator; the result is the block output.  Three ring stages
 //          leave room for the staging tile.
-//   CL2    clusters of two CTAs computing adjacent M tiles of one N tile;
-//          each loads half of the shared B tile and multicasts it to both.
+//   CL2    clusters of two CTAs computing adjacent M tiles of one N tile
+//          (each loads its own operands).
 //          When the last round of tiles would leave clusters idle, its tiles
 //          are spread one per cluster instead, the two CTAs taking the two
 //          halves of the K steps; each CTA sends the partial sums of the
@@ -261,7 +261,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], CL2 ? 2 : 1);  // CL2: both CTAs' MMAs free a stage
+      mbar_init(&empty_bar[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull_bar[a], 1);
@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (CL2) cluster_sync();  // the peer's barriers exist before any multicast reaches them
+  if (CL2) cluster_sync();  // the peer's barriers exist before the peer signals them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   pdl_wait();  // the predecessor's outputs are complete from here on
@@ -377,8 +377,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tma_load_2d(a_dst, &tmA, &full_bar[stage], a_mn, a_k);
             tma_load_2d(a_dst + 8192, &tmA, &full_bar[stage], a_mn + 64, a_k);
           }
-          if (!B_RES && CL2 && item.split) {
-            // split item: the CTAs read different K steps, each its whole B tile
+          if (!B_RES && CL2) {
+            // each CTA of the cluster loads its whole B tile itself (split
+            // items read different K steps; whole items the same tile, which
+            // L2 serves twice)
             const int b_k = g * p.b_k_per_g + ks * BK;
             uint8_t* b_dst = sB + stage * S::B_BYTES;
             if (!B_MN) {
@@ -390,21 +392,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
               for (int c = 0; c < BN / 64; ++c)
                 tma_load_2d(b_dst + c * 8192, &tmB, &full_bar[stage], b_mn + 64 * c, b_k);
-            }
-          } else if (!B_RES && CL2) {
-            // this CTA's half of the shared B tile, delivered to both CTAs
-            const int b_k = g * p.b_k_per_g + ks * BK;
-            uint8_t* b_dst = sB + stage * S::B_BYTES;
-            if (!B_MN) {
-              tma_load_2d_mc(b_dst + crank * (BN / 2) * 128, &tmB, &full_bar[stage], b_k,
-                             b_mn + static_cast<int>(crank) * (BN / 2), 0x3);
-            } else {
-#pragma unroll
-              for (int c = 0; c < BN / 128; ++c) {
-                const int cc = static_cast<int>(crank) * (BN / 128) + c;
-                tma_load_2d_mc(b_dst + cc * 8192, &tmB, &full_bar[stage], b_mn + 64 * cc, b_k,
-                               0x3);
-              }
             }
           } else if (!B_RES) {
             const int b_k = g * p.b_k_per_g + ks * BK;
@@ -545,10 +532,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             umma_bf16(d_tmem, adesc, bdesc, IDESC, (ks > ks0 || j > 0) ? 1u : 0u);
           }
           any_mma = true;
-          if (CL2)  // the stage is free once both CTAs' MMAs have read it
-            umma_commit_mc(&empty_bar[stage], 0x3);
-          else
-            umma_commit(&empty_bar[stage]);  // frees this smem stage when done
+          umma_commit(&empty_bar[stage]);  // frees this smem stage when done
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -810,7 +794,7 @@ cudaError_t launch_tc(const TcGemm& g, cudaStream_t stream) {
   CUtensorMap tmA, tmB, tmC, tmR, tmY;
   if (!make_map(&tmA, g.A.ptr, g.A.rows, g.A.cols, g.A.pitch, 2, 64, A_MN ? 64 : BM))
     return cudaErrorInvalidValue;
-  // CL2: each CTA of a cluster loads half of a K-major B tile
+  // CL2: a K-major B tile is loaded as two halves (one box of BN / 2 rows each)
   if (!make_map(&tmB, g.B.ptr, g.B.rows, g.B.cols, g.B.pitch, 2, 64,
                 B_MN ? 64 : (CL2 ? BN / 2 : BN)))
     return cudaErrorInvalidValue;

@@ -71,8 +71,8 @@ struct TcGemm {
   // Keep the B operand of a (batch, N tile) resident in shared memory while
   // the CTA walks consecutive M tiles (needs splits == 1 and BN*K*2 <= 128 KiB).
   bool b_resident = false;
-  // W0 GEMMs: run as clusters of two CTAs on adjacent M tiles that load one
-  // half of each shared B tile each (TMA multicast)
+  // W0 GEMMs: run as clusters of two CTAs on adjacent M tiles (needed by
+  // split_tail, whose partial sums move between the two CTAs)
   bool cluster2 = false;
   // cluster2: when the last round of tiles would leave clusters idle, spread
   // its tiles one per cluster, the two CTAs summing halves of K

@@ -101,18 +101,6 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* t
       : "memory");
 }
 
-// The same load delivered to every CTA of the cluster in `mask`, at the same
-// shared-memory offsets, each CTA's barrier at `bar`'s offset receiving the
-// transaction bytes.
-__device__ __forceinline__ void tma_load_2d_mc(void* smem_dst, const CUtensorMap* tm,
-                                               uint64_t* bar, int c0, int c1, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
-      "l"(tm), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(mask)
-      : "memory");
-}
-
 // ------------------------------------------------------------------ cluster
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -269,16 +257,6 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
-      : "memory");
-}
-
-// As umma_commit, arriving on the barrier at the same offset in every CTA of
-// the cluster in `mask`.
-__device__ __forceinline__ void umma_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(smem_u32(bar)),
-      "h"(mask)
       : "memory");
 }
 
