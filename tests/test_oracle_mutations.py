@@ -52,6 +52,17 @@ MUTATIONS = [
      "s = np.float32(amax / np.float32(128))"),
     ("INT8 codes truncated instead of rounded", "q = np.rint(W[o] / s)", "q = np.floor(W[o] / s)"),
     ("dequantisation divides by the scale", "return q * s[:, None]", "return q / s[:, None]"),
+    ("sampled v: W0's columns instead of its rows",
+     "return u @ np.asarray(W0, dtype=np.float64)[rows].T",
+     "return u @ np.asarray(W0, dtype=np.float64)[:, rows].T"),
+    ("sampled v: W0 not transposed", "return u @ np.asarray(W0, dtype=np.float64)[rows].T",
+     "return u @ np.asarray(W0, dtype=np.float64).T[rows]"),
+    ("sampled du: W0's rows instead of its columns",
+     "return dv @ np.asarray(W0, dtype=np.float64)[:, cols]",
+     "return dv @ np.asarray(W0, dtype=np.float64)[cols].T"),
+    ("sampled du: R applied untransposed",
+     "dv = apply_blockdiag_transposed(dy, R_blocks)\n    return dv @ np.asarray(W0",
+     "dv = apply_blockdiag(dy, R_blocks)\n    return dv @ np.asarray(W0"),
 ]
 
 

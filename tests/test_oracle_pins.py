@@ -223,6 +223,51 @@ def test_single_block_b_equals_d():
     np.testing.assert_allclose(y, want, rtol=1e-13, atol=1e-13)
 
 
+# ------------------------------------- sliced products (sampled checks)
+
+@pytest.mark.parametrize("rows", [slice(0, 24), slice(4, 8), slice(13, 22)])
+def test_forward_v_rows_equals_dense_w0_p(rows):
+    # d_out != d_in, so a slip between W0's rows and columns cannot pass
+    inp = make_layer_inputs(16, 24, 4, 3, 7, dtype="f32", sigma_theta=0.2, seed=30)
+    P = oracle.build_blocks(inp.theta_P, 4, 3)
+    W = np.asarray(inp.W0, np.float64) @ scipy.linalg.block_diag(*P)  # W0 P, dense
+    want = np.asarray(inp.x, np.float64) @ W.T
+    got = oracle.forward_v_rows(inp.x, inp.W0, P, rows)
+    assert got.shape == want[:, rows].shape
+    np.testing.assert_allclose(got, want[:, rows], rtol=0, atol=1e-13 * np.abs(want).max())
+
+
+@pytest.mark.parametrize("cols", [slice(0, 16), slice(4, 8), slice(9, 14)])
+def test_backward_du_cols_equals_dense_rt_w0(cols):
+    inp = make_layer_inputs(16, 24, 4, 3, 7, dtype="f32", sigma_theta=0.2, seed=31)
+    R = oracle.build_blocks(inp.theta_R, 4, 3)
+    # du_t = W0^T R^T dy_t, i.e. rows du = dy R W0 with dense R
+    want = np.asarray(inp.dy, np.float64) @ scipy.linalg.block_diag(*R) @ \
+        np.asarray(inp.W0, np.float64)
+    got = oracle.backward_du_cols(inp.dy, inp.W0, R, cols)
+    assert got.shape == want[:, cols].shape
+    np.testing.assert_allclose(got, want[:, cols], rtol=0, atol=1e-13 * np.abs(want).max())
+
+
+def test_sliced_products_give_the_sampled_block_gradients():
+    # the block gradients built from the sliced products equal the full
+    # backward's (FD-pinned) G_R and G_P block by block
+    inp = make_layer_inputs(8, 12, 4, 3, 6, dtype="f32", sigma_theta=0.3, seed=32)
+    P = oracle.build_blocks(inp.theta_P, 4, 3)
+    R = oracle.build_blocks(inp.theta_R, 4, 3)
+    _, _, v = oracle.forward(inp.x, inp.W0, P, R)
+    _, G_P, G_R = oracle.backward(inp.dy, inp.x, inp.W0, P, R, v)
+    for g in range(3):
+        sl = slice(4 * g, 4 * g + 4)
+        G = oracle.blockwise_outer(inp.dy[:, sl], oracle.forward_v_rows(inp.x, inp.W0, P, sl), 4)
+        np.testing.assert_allclose(G[0], G_R[g], rtol=1e-12, atol=1e-13)
+    for g in range(2):
+        sl = slice(4 * g, 4 * g + 4)
+        du = oracle.backward_du_cols(inp.dy, inp.W0, R, sl)
+        G = oracle.blockwise_outer(du, inp.x[:, sl], 4)
+        np.testing.assert_allclose(G[0], G_P[g], rtol=1e-12, atol=1e-13)
+
+
 # ------------------------------------------------- finite differences
 
 def _central_diff(f, x0, idx, h):
