@@ -35,6 +35,11 @@ from orthogonal_reparameterized_packed_gb300.inputs import (COMPOSITES, WORKLOAD
 METRIC = "POET-X layer fwd+bwd tokens/s (d=4096,b=256,bf16); % HBM / tensor-core roofline"
 UNIT = "tokens/s"
 
+# the isolated block-diagonal transform sweep: d = 4096, 8192 tokens, bf16
+SWEEP = "transform_sweep"
+SWEEP_D, SWEEP_T = 4096, 8192
+SWEEP_CASES = [(b, k) for b in (32, 64, 128, 256, 512) for k in (1, 3, 5)]
+
 
 def parse():
     ap = argparse.ArgumentParser()
@@ -43,7 +48,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="poetx", choices=["poetx", "reference"])
     ap.add_argument("--workload", default="llama3_8b_qo",
-                    choices=sorted(WORKLOADS) + sorted(COMPOSITES),
+                    choices=sorted(WORKLOADS) + sorted(COMPOSITES) + [SWEEP],
                     help="one projection, or a composite run as its projections in sequence "
                          "(llama3_8b_block: the 7 of a Llama-3-8B decoder block; "
                          "llama_1p3b_model: all 168 of the 1.3B-shaped model)")
@@ -159,26 +164,89 @@ def oracle_sample(inp, sample_tokens):
     return (t1 - t0) + (t3 - t2), (t2 - t1) / sample_tokens
 
 
+# tokens of each distinct projection shape the oracle runs per step (both
+# oracle legs use the same sample, so their figures agree)
+ORACLE_SAMPLE_TOKENS = 2048
+
+
+def oracle_step(name, inps, sample_tokens):
+    """One oracle step on the bounded sample: each distinct projection shape
+    once (block build, forward + backward on `sample_tokens` tokens, CNP
+    adjoint).  Returns the measured wall time (s) of each shape and the
+    linear extrapolation of the full step (each shape's fixed part plus its
+    per-token time times the full token count, weighted by how often the
+    step runs the shape)."""
+    counts = step_shapes(name)
+    wall, full = {}, 0.0
+    for key, inp in inps.items():
+        t0 = time.perf_counter()
+        t_fixed, t_tok = oracle_sample(inp, sample_tokens)
+        wall[key] = time.perf_counter() - t0
+        full += counts[key] * (t_fixed + t_tok * inp.tokens)
+    return wall, full
+
+
+def oracle_rates(name, inps, sample_tokens, wall, full_s, steps):
+    """(measured tokens/s, extrapolated tokens/s) over `steps` steps whose
+    per-shape wall times were summed into `wall`.  Measured: the sampled
+    tokens / the wall time they took (fixed parts included); for a
+    composite, each shape's time counts as often as the step runs it."""
+    counts = step_shapes(name)
+    weighted = sum(counts[key] * t for key, t in wall.items())
+    T = next(iter(inps.values())).tokens
+    return sample_tokens * steps / weighted, T * steps / full_s
+
+
 def cpu_baseline(name, sample_tokens, seed=0):
-    """The oracle on a bounded sample: each distinct projection shape of the
-    step once, scaled by how often the step runs it."""
-    t_fixed = t_tok = 0.0
-    T = None
-    for key, cnt in step_shapes(name).items():
-        inp = make_layer_inputs(**WORKLOADS[key], seed=seed)
-        f, tt = oracle_sample(inp, sample_tokens)
-        t_fixed += cnt * f
-        t_tok += cnt * tt
-        T = inp.tokens
-    value = T / (t_fixed + t_tok * T)
-    return {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-            "sample": (f"float64 numpy oracle: block build + CNP adjoint of both sides "
-                       f"({t_fixed:.2f} s) and forward+backward on {sample_tokens} of {T} "
-                       f"tokens ({t_tok * sample_tokens:.2f} s) per step"
-                       + ("" if name in WORKLOADS else
-                          f" (each of the {len(step_shapes(name))} distinct shapes timed once, "
-                          f"weighted by its count in the {len(projections(name))} projections)")
-                       + f"; tokens/s extrapolated linearly in tokens to the full {T}")}
+    """The oracle on a bounded sample of the step's workload (one step)."""
+    inps = {key: make_layer_inputs(**WORKLOADS[key], seed=seed) for key in step_shapes(name)}
+    wall, full = oracle_step(name, inps, sample_tokens)
+    measured, extrap = oracle_rates(name, inps, sample_tokens, wall, full, 1)
+    T = next(iter(inps.values())).tokens
+    return {"value": measured, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "sample": (f"float64 numpy oracle, one step on a bounded sample: block build + CNP "
+                       f"adjoint of both sides and forward+backward on {sample_tokens} of {T} "
+                       f"tokens" + ("" if name in WORKLOADS else
+                                    f" for each of the {len(inps)} distinct shapes, weighted by "
+                                    f"its count in the {len(projections(name))} projections")
+                       + f"; value = sampled tokens / measured {sum(wall.values()):.2f} s"),
+            "extrapolated_full_step": {"value": extrap, "unit": UNIT, "s_per_step": full,
+                                       "note": "linear in tokens to the full token count; "
+                                               "not a measured time"}}
+
+
+def run_reference_sweep(args):
+    """The oracle's isolated transform (build, z = B x, dx and packed dtheta)
+    for every (b, k) of the sweep on a bounded token sample."""
+    import oracle
+    d, T, sample = SWEEP_D, SWEEP_T, 512
+    base = make_layer_inputs(d, d, 256, 3, sample, dtype="bf16", seed=0)
+    thetas = {(b, k): (np.random.default_rng(10 * b + k).standard_normal(
+        (d // b, b * (b - 1) // 2)) * 0.02).astype(np.float32) for b, k in SWEEP_CASES}
+
+    def one_step():
+        for (b, k), th in thetas.items():
+            oracle.transform(th, base.x, base.dy, b, k)
+
+    for _ in range(args.warmup):
+        one_step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one_step()
+    wall = time.perf_counter() - t0
+    value = sample * len(SWEEP_CASES) * args.steps / wall
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * wall / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": SWEEP, "d": d, "tokens_per_gpu": T, "dtype": "bf16"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(),
+                             "kind": "oracle",
+                             "sample": f"each step: every (b, k) of the sweep on {sample} of "
+                                       f"{T} tokens; ms_per_step is the measured wall time"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
 
 
 def run_reference(args):
@@ -186,30 +254,38 @@ def run_reference(args):
     if rank != 0:
         return
     name = args.workload
-    counts = step_shapes(name)
-    inps = {key: make_layer_inputs(**WORKLOADS[key], seed=0) for key in counts}
+    if name == SWEEP:
+        run_reference_sweep(args)
+        return
+    inps = {key: make_layer_inputs(**WORKLOADS[key], seed=0) for key in step_shapes(name)}
     T = next(iter(inps.values())).tokens
-    sample = 256
+    sample = ORACLE_SAMPLE_TOKENS
     for _ in range(args.warmup):
-        for inp in inps.values():
-            oracle_sample(inp, sample)
-    t_all = 0.0
+        oracle_step(name, inps, sample)
+    wall = {key: 0.0 for key in inps}
+    full = 0.0
     for _ in range(args.steps):
-        for key, inp in inps.items():
-            t_fixed, t_tok = oracle_sample(inp, sample)
-            t_all += counts[key] * (t_fixed + t_tok * T)
-    value = args.steps * T / t_all
+        w_, f_ = oracle_step(name, inps, sample)
+        for key, t in w_.items():
+            wall[key] += t
+        full += f_
+    value, extrap = oracle_rates(name, inps, sample, wall, full, args.steps)
     cores = blas_threads()
+    sample_txt = (f"each step: block build + CNP adjoint of both sides and forward+backward "
+                  f"on {sample} of {T} tokens" +
+                  ("" if name in WORKLOADS else " per distinct projection shape, weighted by "
+                   "the shape's count") + "; ms_per_step is the measured wall time of that")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": 1e3 * t_all / args.steps, "higher_is_better": True,
+            "ms_per_step": 1e3 * sum(wall.values()) / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": config_json(name, args.gpus),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": (f"each step: block build + CNP adjoint of both sides "
-                                        f"and forward+backward on {sample} of {T} tokens per "
-                                        f"distinct projection shape, extrapolated linearly in "
-                                        f"tokens and weighted by the shape's count")},
+                             "sample": sample_txt},
+            "extrapolated_full_step": {"value": extrap, "unit": UNIT,
+                                       "ms_per_step": 1e3 * full / args.steps,
+                                       "note": "linear in tokens to the full token count; "
+                                               "not a measured time"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -462,15 +538,26 @@ def run_gpu(args):
         raise RuntimeError("device status not OK after warm-up")
 
     # (1) eager pass: every launch bracketed by CUDA events on its stream,
-    #     giving the per-kernel durations the roofline uses
+    #     giving the per-kernel durations the roofline uses.  Like the timed
+    #     region below it runs for about a second (whole K-step rounds), so
+    #     the kernels are timed in the same sustained power state.
     # (a composite step profiles a few steps: its launch count is large)
-    prof_steps = args.steps if single else min(args.steps, 3)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    est_ms = max(t0.elapsed_time(t1), 1e-3)
+    if single:
+        rounds = max(1, min(100, int(1000.0 / (est_ms * args.steps)) + 1))
+        prof_steps = args.steps * rounds
+    else:
+        prof_steps = min(args.steps, 3)
     launches0 = poetx.poetx_launch_count()
     poetx.poetx_profile_start(16 * len(projs) * prof_steps)
     barrier()
     torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for _ in range(prof_steps):
         step()
@@ -511,21 +598,34 @@ def run_gpu(args):
     run_step, graph_error = capture(step)
     graph = graphs[0] if graphs else None
 
+    # the timed region: exactly K steps between a barrier + synchronize on
+    # each side, repeated until the repeats cover at least a second (so the
+    # clock sampler sees a loaded GPU); ms_per_step is the median repeat
     clocks = ClockSampler(local)
-    barrier()
-    torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)  # let the sampler take its first reading
-    t0.record(stream)
-    for _ in range(args.steps):
-        run_step()
-    t1.record(stream)
-    torch.cuda.synchronize()
-    barrier()
+    region_ms = []
+    while len(region_ms) < 3 or (sum(region_ms) < 1000.0 and len(region_ms) < 500):
+        barrier()
+        torch.cuda.synchronize()
+        t0.record(stream)
+        for _ in range(args.steps):
+            run_step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        region_ms.append(t0.elapsed_time(t1))
     clk = clocks.stop()
-    launches = launches_per_step * args.steps
-    ms = t0.elapsed_time(t1) / args.steps
+    launches = launches_per_step * args.steps * len(region_ms)  # every repeat of the region
+    ms = statistics.median(region_ms) / args.steps
     ms_max = max_over_ranks(ms, "cuda")
+    per_step = sorted(r / args.steps for r in region_ms)
+    repeats = {"regions": len(region_ms), "steps_each": args.steps,
+               "ms_per_step_median": ms, "ms_per_step_min": per_step[0],
+               "ms_per_step_max": per_step[-1],
+               "ms_per_step_p10": per_step[len(per_step) // 10],
+               "ms_per_step_p90": per_step[(9 * len(per_step)) // 10],
+               "total_s": sum(region_ms) / 1e3}
     status = poetx.poetx_device_status()
 
     # per-kernel times over the timed region
@@ -551,9 +651,9 @@ def run_gpu(args):
     work = per_step(lambda wp: algorithmic_work(dom, wp)[0])
     achieved = work * prof_steps / (kernels[dom]["total_ms"] * 1e-3)
     # the sustained peak for a kernel inside a long step (a whole-model step of
-    # 10 ms or more, or a profiled region over a second), the burst peak
-    # otherwise; a power-cap event in a short step is reported under clocks
-    long_region = ms_eager > 10.0 or ms_eager * prof_steps > 1000.0
+    # 10 ms or more) or a profiled region of a second or more, the burst
+    # peak otherwise
+    long_region = ms_eager > 10.0 or ms_eager * prof_steps >= 900.0
     if w["dtype"] == "bf16":
         peak = peaks["bf16_tflops_sustained"] if long_region else peaks["bf16_tflops"]
         peak_note = f"{peak_src} bf16 ({'sustained' if long_region else 'burst'})"
@@ -570,7 +670,8 @@ def run_gpu(args):
                 "per_launch": (f"{formula} = {work:.4f} TFLOP" if single else
                                f"{formula} summed over the {len(projs)} projections: "
                                f"{work:.4f} TFLOP per step"),
-                "timing": "CUDA events around each launch, eager pass of the same K steps"}
+                "timing": f"CUDA events around each launch, eager pass of {prof_steps} steps "
+                          f"({ms_eager * prof_steps / 1e3:.2f} s)"}
 
     # the HBM-bound kernels: algorithmic bytes of all their launches in the
     # timed steps / their summed event time
@@ -619,9 +720,10 @@ def run_gpu(args):
     value = job_throughput(w["tokens"], world, ms_max)
 
     # end to end through the C ABI from pinned host buffers: every step's x and
-    # dy go host -> device and its dtheta device -> host inside the timed
-    # region.  Two buffer sets: step i+1's inputs upload (copy stream) while
-    # step i computes, and step i's dtheta reads back during step i+1.
+    # dy go host -> device and its results (y, dx and the packed dtheta)
+    # device -> host inside the timed region.  Two buffer sets: step i+1's
+    # inputs upload (copy stream) while step i computes, and step i's results
+    # read back (another copy stream) during step i+1.
     e2e = None
     if single and not args.no_e2e:
         hx = dev["x"].cpu().pin_memory()
@@ -634,10 +736,12 @@ def run_gpu(args):
         torch.cuda.synchronize()
         run_step2, _ = capture(step2)
         sets = [(dev, layer, run_step), (acts2, layer2, run_step2)]
-        hP = [torch.empty(layer.dtheta_P.shape, dtype=torch.float32).pin_memory()
-              for _ in range(2)]
-        hR = [torch.empty(layer.dtheta_R.shape, dtype=torch.float32).pin_memory()
-              for _ in range(2)]
+
+        def host_like(t):
+            return torch.empty(t.shape, dtype=t.dtype).pin_memory()
+
+        outs = [{"y": host_like(lay.y), "dx": host_like(lay.dx), "dtheta": host_like(lay.dtheta)}
+                for lay in (layer, layer2)]
         h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
         up = [torch.cuda.Event() for _ in range(2)]
         done = [torch.cuda.Event() for _ in range(2)]
@@ -659,15 +763,17 @@ def run_gpu(args):
                 j = i % 2
                 stream.wait_event(up[j])
                 if i >= 2:
-                    stream.wait_event(down[j])  # the set's dtheta has been read back
+                    stream.wait_event(down[j])  # the set's results have been read back
                 sets[j][2]()
                 done[j].record(stream)
                 if i + 1 < k:
                     upload((i + 1) % 2, done[(i + 1) % 2] if i >= 1 else None)
                 with torch.cuda.stream(d2h):
                     d2h.wait_event(done[j])
-                    hP[j].copy_(sets[j][1].dtheta_P, non_blocking=True)
-                    hR[j].copy_(sets[j][1].dtheta_R, non_blocking=True)
+                    lay = sets[j][1]
+                    outs[j]["y"].copy_(lay.y, non_blocking=True)
+                    outs[j]["dx"].copy_(lay.dx, non_blocking=True)
+                    outs[j]["dtheta"].copy_(lay.dtheta, non_blocking=True)
                     down[j].record(d2h)
             stream.wait_stream(d2h)
             stream.wait_stream(h2d)
@@ -678,23 +784,25 @@ def run_gpu(args):
         pipeline(2, e0)  # warm-up
         torch.cuda.synchronize()
         barrier()
-        ksteps = max(2, min(args.steps, 20))
+        # at least the driver's K steps and at least ~0.5 s of them
+        ksteps = max(args.steps, int(500.0 / max(ms, 1e-3) / 1.6) + 1)
         e0.record(stream)
         pipeline(ksteps, e0)
         e1.record(stream)
         torch.cuda.synchronize()
         ems = max_over_ranks(e0.elapsed_time(e1) / ksteps, "cuda")
+        nbytes = lambda t: t.numel() * t.element_size()  # noqa: E731
         e2e = {"value": job_throughput(w["tokens"], world, ems), "unit": UNIT,
-               "h2d_bytes_per_step": hx.numel() * hx.element_size() +
-               hdy.numel() * hdy.element_size(),
-               "d2h_bytes_per_step": (hP[0].numel() + hR[0].numel()) * 4,
+               "h2d_bytes_per_step": nbytes(hx) + nbytes(hdy),
+               "d2h_bytes_per_step": sum(nbytes(t) for t in outs[0].values()),
                "steps": ksteps, "ms_per_step": ems,
-               "overlap": "double-buffered: uploads of step i+1 and read-back of step i-1 "
-                          "run on copy streams during step i"}
+               "copies": "x, dy in; y, dx and the packed dtheta out, every step",
+               "overlap": "double-buffered: while step i computes, step i+1's inputs upload "
+                          "and step i-1's results read back on two copy streams"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(name, 2048 if single else 512, seed=rank)
+        cpu = cpu_baseline(name, ORACLE_SAMPLE_TOKENS if single else 512, seed=rank)
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -702,7 +810,8 @@ def run_gpu(args):
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": w["dtype"].replace("f32", "fp32"), "data": "synthetic",
                 "config": config_json(name, world, args),
-                "gpu_launches": launches, "launch": "cuda_graph" if graph is not None else "eager",
+                "gpu_launches": launches, "gpu_launches_per_step": launches_per_step,
+                "launch": "cuda_graph" if graph is not None else "eager",
                 "graph_error": graph_error,
                 "ms_per_step_eager": ms_eager, "roofline": roofline,
                 "step_tflops": step_flop / (ms_max * 1e-3) / 1e12,
@@ -711,6 +820,7 @@ def run_gpu(args):
                     "achieved_gbs": min_step_bytes / (ms_max * 1e-3) / 1e9,
                     "frac": min_step_bytes / (ms_max * 1e-3) / 1e9 / peaks["hbm_gbs"],
                     "note": "algorithmic floor of a fully fused layer step / step time"},
+                "timed_repeats": repeats,
                 "kernels": kernels, "merge": merge, "clocks": clk, "e2e": e2e, "cpu_baseline": cpu,
                 "device_status": status}
         print(json.dumps(line), flush=True)
@@ -718,10 +828,122 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+def sweep_bytes(b, d=SWEEP_D, T=SWEEP_T):
+    """Algorithmic HBM bytes of the isolated transform: forward reads x and
+    the blocks and writes z; backward reads dout, x and the blocks and
+    writes dx and the packed dtheta (bf16 activations and blocks, fp32
+    dtheta)."""
+    blocks = 2.0 * d * b
+    fwd = 4.0 * d * T + blocks
+    bwd = 6.0 * d * T + blocks + 4.0 * d * (b - 1) / 2
+    return fwd, bwd
+
+
+def run_sweep(args):
+    """Each (b, k) of the sweep: block build, forward z = B x and backward
+    (dx, packed dtheta) timed call by call with CUDA events; L2 is flushed
+    (a 256 MiB write) before every timed call, since x (64 MiB) fits in L2."""
+    import torch
+
+    import orthogonal_reparameterized_packed_gb300 as poetx
+
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    poetx.load_library()
+    d, T, c = SWEEP_D, SWEEP_T, poetx.BF16
+    stream = torch.cuda.current_stream()
+    base = make_layer_inputs(d, d, 256, 3, T, dtype="bf16", seed=rank)
+    x = torch.from_numpy(base.x).cuda().to(torch.bfloat16)
+    dout = torch.from_numpy(base.dy).cuda().to(torch.bfloat16)
+    z = torch.empty_like(x)
+    dx = torch.empty_like(x)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    peaks, peak_src = load_peaks()
+    hbm = peaks["hbm_gbs"]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+
+    def timed(fn, reps):
+        tot = 0.0
+        for _ in range(reps):
+            flush.zero_()
+            ev[0].record(stream)
+            fn()
+            ev[1].record(stream)
+            torch.cuda.synchronize()
+            tot += ev[0].elapsed_time(ev[1])
+        return tot / reps
+
+    cases = []
+    launches0 = poetx.poetx_launch_count()
+    clocks = ClockSampler(local)
+    clocks.start()
+    for b, k in SWEEP_CASES:
+        rng = np.random.default_rng(1000 * rank + 10 * b + k)
+        theta = torch.from_numpy((rng.standard_normal((d // b, b * (b - 1) // 2)) *
+                                  0.02).astype(np.float32)).cuda()
+        blocks = torch.empty((d // b, b, b), dtype=torch.bfloat16, device="cuda")
+        dtheta = torch.empty_like(theta)
+        ws = torch.empty((max(poetx.poetx_build_workspace_size(d, b, k, c),
+                              poetx.poetx_transform_workspace_size(d, b, k, T, c), 16),),
+                         dtype=torch.uint8, device="cuda")
+
+        def build():
+            poetx.poetx_build_blocks(theta, d, b, k, c, blocks, ws)
+
+        def fwd():
+            poetx.poetx_transform_forward(x, blocks, z, d, b, T, c, ws)
+
+        def bwd():
+            poetx.poetx_transform_backward(dout, x, theta, blocks, dx, dtheta, d, b, k, T, c, ws)
+
+        for _ in range(max(args.warmup, 3)):
+            build()
+            fwd()
+            bwd()
+        torch.cuda.synchronize()
+        reps = max(args.steps, 5)
+        ms_b, ms_f, ms_w = timed(build, reps), timed(fwd, reps), timed(bwd, reps)
+        fb, wb = sweep_bytes(b)
+        cases.append({"b": b, "k": k, "build_us": 1e3 * ms_b, "fwd_us": 1e3 * ms_f,
+                      "bwd_us": 1e3 * ms_w,
+                      "fwd_gbs": fb / (ms_f * 1e-3) / 1e9, "bwd_gbs": wb / (ms_w * 1e-3) / 1e9,
+                      "fwd_frac": fb / (ms_f * 1e-3) / 1e9 / hbm,
+                      "bwd_frac": wb / (ms_w * 1e-3) / 1e9 / hbm})
+    clk = clocks.stop()
+    status = poetx.poetx_device_status()
+    launches = poetx.poetx_launch_count() - launches0
+    t_all = sum(cs["build_us"] + cs["fwd_us"] + cs["bwd_us"] for cs in cases) * 1e-6
+    bytes_all = sum(sum(sweep_bytes(cs["b"])) for cs in cases)
+    t_tr = sum(cs["fwd_us"] + cs["bwd_us"] for cs in cases) * 1e-6
+    achieved = bytes_all / t_tr / 1e9
+    if rank == 0:
+        line = {"metric": METRIC, "value": T * len(cases) / t_all, "unit": UNIT, "n_gpus": 1,
+                "steps": args.steps, "warmup": max(args.warmup, 3),
+                "ms_per_step": 1e3 * t_all, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": SWEEP, "d": d, "tokens_per_gpu": T, "dtype": "bf16",
+                           "cases": [f"b{b}_k{k}" for b, k in SWEEP_CASES],
+                           "l2": "flushed (256 MiB write) before every timed call"},
+                "gpu_launches": launches, "launch": "eager",
+                "roofline": {"bound": "hbm", "kernel": "block transform fwd + bwd, all cases",
+                             "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                             "frac": achieved / hbm, "traffic": None,
+                             "peak_source": f"{peak_src} copy bandwidth",
+                             "per_launch": "fwd 4dT + 2db, bwd 6dT + 2db + 2d(b-1) bytes"},
+                "sweep": cases, "clocks": clk, "e2e": None, "cpu_baseline": None,
+                "device_status": status,
+                "note": "value = tokens of all cases / the summed build + fwd + bwd time; "
+                        "one step = the whole sweep once"}
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == SWEEP:
+        run_sweep(args)
     else:
         run_gpu(args)
 

@@ -3,7 +3,8 @@ them (one PoetxLayer step per projection shape).  The oracle checks sampled
 outputs it can compute one by one: y and dx rows of sampled tokens (each
 row depends on its own token only), and dtheta of sampled blocks (each
 block's gradient is a sum over all tokens of that block's features only).
-Tolerance: 2e-2 relative Frobenius (bf16 with fp32 accumulation)."""
+Tolerance: 2e-2 relative Frobenius (bf16 with fp32 accumulation) over the
+sampled rows and per sampled block, and 4e-2 on the worst single row."""
 
 import numpy as np
 import pytest
@@ -16,6 +17,7 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 TOL = 2e-2
+TOL_ROW = 4e-2  # largest single-row error: twice the Frobenius tolerance
 
 
 @pytest.fixture(scope="module")
@@ -33,17 +35,37 @@ def rel_fro(got, want):
     return float(np.linalg.norm(got - want) / max(np.linalg.norm(want), 1e-300))
 
 
+def max_row_rel(got, want):
+    """Largest relative error of one sampled row."""
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    num = np.linalg.norm(got - want, axis=1)
+    return float(np.max(num / np.maximum(np.linalg.norm(want, axis=1), 1e-300)))
+
+
+def tile_rows(T, rng, tile=128):
+    """One random token in every tile of `tile` tokens, plus the first and last."""
+    starts = np.arange(0, T, tile)
+    offs = rng.integers(0, tile, size=len(starts))
+    rows = np.minimum(starts + offs, T - 1)
+    return np.unique(np.concatenate([[0, T - 1], rows]))
+
+
 def sampled_check(layer, inp, rng):
     b, k, T = inp.b, inp.k, inp.tokens
     P = oracle.build_blocks(inp.theta_P, b, k)
     R = oracle.build_blocks(inp.theta_R, b, k)
-    # rows of sampled tokens (first, last, random)
-    rows = np.unique(np.concatenate([[0, T - 1], rng.choice(T, 46, replace=False)]))
+    # rows of sampled tokens: one at random in every 128-token tile (so every
+    # output tile of every kernel holds a checked row, the last partial round
+    # of GEMM tiles included), the first and the last
+    rows = tile_rows(T, rng)
     y_ref, _, v_ref = oracle.forward(inp.x[rows], inp.W0, P, R)
     dx_ref, _, _ = oracle.backward(inp.dy[rows], inp.x[rows], inp.W0, P, R, v_ref)
     idx = torch.from_numpy(rows).cuda()
-    errs = {"y": rel_fro(layer.y.index_select(0, idx).float().cpu().numpy(), y_ref),
-            "dx": rel_fro(layer.dx.index_select(0, idx).float().cpu().numpy(), dx_ref)}
+    y_got = layer.y.index_select(0, idx).float().cpu().numpy()
+    dx_got = layer.dx.index_select(0, idx).float().cpu().numpy()
+    errs = {"y": rel_fro(y_got, y_ref), "dx": rel_fro(dx_got, dx_ref),
+            "y max row": max_row_rel(y_got, y_ref), "dx max row": max_row_rel(dx_got, dx_ref)}
     # dtheta of sampled blocks
     nP, nR = inp.d_in // b, inp.d_out // b
     QP = oracle.unpack(inp.theta_P, b)
@@ -62,8 +84,8 @@ def sampled_check(layer, inp, rng):
         G = oracle.blockwise_outer(du_g, inp.x[:, sl], b)
         want = oracle.pack_skew_grad(oracle.cnp_adjoint(QP[g:g + 1], G, k))[0]
         errs[f"dtheta_P[{g}]"] = rel_fro(dthP[g], want)
-    bad = {n: e for n, e in errs.items() if not e <= TOL}
-    assert not bad, f"above {TOL}: {bad} (all: {errs})"
+    bad = {n: e for n, e in errs.items() if not e <= (TOL_ROW if "max row" in n else TOL)}
+    assert not bad, f"above tolerance: {bad} (all: {errs})"
 
 
 # the distinct projection shapes of the workloads, full token counts
@@ -114,15 +136,15 @@ def test_full_size_transform_sweep(px, b, k):
     torch.cuda.synchronize()
     assert px.poetx_device_status() == 0
     rng = np.random.default_rng(2)
-    rows = np.unique(np.concatenate([[0, T - 1], rng.choice(T, 30, replace=False)]))
+    rows = tile_rows(T, rng)
     B = oracle.build_blocks(inp.theta_P, b, k)
     idx = torch.from_numpy(rows).cuda()
-    errs = {
-        "z": rel_fro(out.index_select(0, idx).float().cpu().numpy(),
-                     oracle.apply_blockdiag(inp.x[rows], B)),
-        "dx": rel_fro(dx.index_select(0, idx).float().cpu().numpy(),
-                      oracle.apply_blockdiag_transposed(inp.dy[rows], B)),
-    }
+    z_got = out.index_select(0, idx).float().cpu().numpy()
+    z_ref = oracle.apply_blockdiag(inp.x[rows], B)
+    dx_got = dx.index_select(0, idx).float().cpu().numpy()
+    dx_ref = oracle.apply_blockdiag_transposed(inp.dy[rows], B)
+    errs = {"z": rel_fro(z_got, z_ref), "dx": rel_fro(dx_got, dx_ref),
+            "z max row": max_row_rel(z_got, z_ref), "dx max row": max_row_rel(dx_got, dx_ref)}
     Q = oracle.unpack(inp.theta_P, b)
     n = d // b
     dth = dtheta.cpu().numpy()
@@ -131,5 +153,5 @@ def test_full_size_transform_sweep(px, b, k):
         G = oracle.blockwise_outer(inp.dy[:, sl], inp.x[:, sl], b)
         want = oracle.pack_skew_grad(oracle.cnp_adjoint(Q[g:g + 1], G, k))[0]
         errs[f"dtheta[{g}]"] = rel_fro(dth[g], want)
-    bad = {n_: e for n_, e in errs.items() if not e <= TOL}
-    assert not bad, f"above {TOL}: {bad} (all: {errs})"
+    bad = {n_: e for n_, e in errs.items() if not e <= (TOL_ROW if "max row" in n_ else TOL)}
+    assert not bad, f"above tolerance: {bad} (all: {errs})"

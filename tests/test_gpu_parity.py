@@ -170,6 +170,23 @@ def run_layer(px, inp, recompute_v=False):
     return layer
 
 
+def max_row_rel(got, want):
+    """Largest relative error of one row (a token of y / dx, a block of
+    dtheta): a fault confined to one tile cannot average away in it."""
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    if want.shape[0] == 0:
+        return 0.0
+    num = np.linalg.norm(got - want, axis=1)
+    den = np.maximum(np.linalg.norm(want, axis=1), 1e-300)
+    return float(np.max(num / den))
+
+
+# Per-row and per-block maximum: twice the Frobenius tolerance (a row of
+# d >= 48 rounded values has almost the spread of the whole array).
+TOL_ROW = {"f32": 2e-4, "bf16": 4e-2}
+
+
 def compare_layer(layer, ref, dtype, rows=None):
     n_in = layer.d_in // layer.b
     n_out = layer.d_out // layer.b
@@ -181,6 +198,9 @@ def compare_layer(layer, ref, dtype, rows=None):
         errs[name] = rel_fro(g, ref[name])
     bad = {n: e for n, e in errs.items() if not e <= TOL[dtype]}
     assert not bad, f"errors above {TOL[dtype]}: {bad} (all: {errs})"
+    rows_err = {name: max_row_rel(g, ref[name]) for name, g in got.items()}
+    bad = {n: e for n, e in rows_err.items() if not e <= TOL_ROW[dtype]}
+    assert not bad, f"row / block errors above {TOL_ROW[dtype]}: {bad} (all: {rows_err})"
 
 
 LAYER_CASES = [
@@ -206,6 +226,25 @@ def test_layer_matches_oracle(px, d_in, d_out, b, k, T, dtype):
     sigma = 0.01 if dtype == "f32" and b == 32 else 0.02
     inp = make_layer_inputs(d_in, d_out, b, k, T, dtype=dtype, sigma_theta=sigma, seed=0)
     layer = run_layer(px, inp)
+    ref = oracle.layer(inp.theta_P, inp.theta_R, inp.W0, inp.x, inp.dy, b, k)
+    compare_layer(layer, ref, dtype)
+
+
+RECOMPUTE_CASES = [
+    (256, 256, 32, 3, 512, "f32"),
+    (512, 768, 256, 3, 333, "bf16"),
+    (256, 512, 128, 2, 130, "bf16"),
+    (512, 256, 64, 3, 257, "bf16"),
+    (1024, 512, 512, 1, 200, "bf16"),
+]
+
+
+@pytest.mark.parametrize("d_in,d_out,b,k,T,dtype", RECOMPUTE_CASES)
+def test_layer_recompute_v_matches_oracle(px, d_in, d_out, b, k, T, dtype):
+    # POET-Xmem: the backward recomputes v = W0 P x instead of reading it
+    sigma = 0.01 if dtype == "f32" and b == 32 else 0.02
+    inp = make_layer_inputs(d_in, d_out, b, k, T, dtype=dtype, sigma_theta=sigma, seed=8)
+    layer = run_layer(px, inp, recompute_v=True)
     ref = oracle.layer(inp.theta_P, inp.theta_R, inp.W0, inp.x, inp.dy, b, k)
     compare_layer(layer, ref, dtype)
 
