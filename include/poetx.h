@@ -261,6 +261,17 @@ int poetx_set_block_epilogue_fusion(int enable);
  * previous setting. */
 int poetx_set_w0_split_tail(int enable);
 
+/* The MMA form of the W0 GEMMs (technical summary, section 2: the frozen-
+ * weight product; the kernel form is this library's).  On: each cluster of
+ * two CTAs computes 256 x 256 output tiles with one tcgen05 MMA per 16-wide
+ * K slice spanning both SMs (each SM holds 128 rows of the input tile and
+ * half of the W0 tile, so it loads 32 KiB per 64-wide K step instead of
+ * 48 KiB); the split of the last round (poetx_set_w0_split_tail) does not
+ * apply.  Off: the clusters of two one-SM MMAs described above.  Both sum
+ * K in order per output element; results agree to fp32 summation order.
+ * On by default.  Process-wide; returns the previous setting. */
+int poetx_set_w0_pair_mma(int enable);
+
 /* ------------------------------------------------------------------------
  * Status and measurement
  * ------------------------------------------------------------------------ */

@@ -23,6 +23,7 @@ __all__ = [
     "poetx_merge", "poetx_adam_update", "poetx_quantize_w0", "poetx_dequantize_w0",
     "poetx_set_block_epilogue_fusion",
     "poetx_set_w0_split_tail",
+    "poetx_set_w0_pair_mma",
     "poetx_device_status", "poetx_selftest_wait_timeout", "poetx_launch_count", "poetx_profile_start", "poetx_profile_stop",
     "poetx_profile_query", "poetx_status_string", "EXPORTED_SYMBOLS",
 ]
@@ -73,6 +74,7 @@ _SIGNATURES = {
     "poetx_dequantize_w0": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_ptr]),
     "poetx_set_block_epilogue_fusion": (_c_int, [_c_int]),
     "poetx_set_w0_split_tail": (_c_int, [_c_int]),
+    "poetx_set_w0_pair_mma": (_c_int, [_c_int]),
     "poetx_device_status": (_c_int, []),
     "poetx_selftest_wait_timeout": (_c_int, [ctypes.c_uint, _c_ptr]),
     "poetx_launch_count": (ctypes.c_longlong, []),
@@ -251,6 +253,12 @@ def poetx_set_w0_split_tail(enable: bool) -> bool:
     """Turn the K split of the W0 GEMMs' last partial round of tiles on or
     off (process-wide); returns the previous setting."""
     return bool(load_library().poetx_set_w0_split_tail(1 if enable else 0))
+
+
+def poetx_set_w0_pair_mma(enable: bool) -> bool:
+    """Run the W0 GEMMs on CTA pairs (256-row MMAs across two SMs) or on
+    clusters of one-SM MMAs (process-wide); returns the previous setting."""
+    return bool(load_library().poetx_set_w0_pair_mma(1 if enable else 0))
 
 
 def poetx_device_status() -> int:

@@ -242,6 +242,10 @@ constexpr bool kW0Clusters = true;
 // with its K steps split between the two CTAs (poetx_set_w0_split_tail).
 std::atomic<int> g_w0_split_tail{1};
 
+// The W0 GEMMs run on CTA pairs (one 256-row MMA per K slice across two
+// SMs); off: clusters of two one-CTA MMAs (poetx_set_w0_pair_mma).
+std::atomic<int> g_w0_pair{1};
+
 // v = u W0^T (fwd) or du = dv W0 (dgrad), bf16.
 cudaError_t tc_w0(const bf16* A, const bf16* W0, bf16* out, int d_in, int d_out, long long T,
                   bool dgrad, cudaStream_t s) {
@@ -268,6 +272,7 @@ cudaError_t tc_w0(const bf16* A, const bf16* W0, bf16* out, int d_in, int d_out,
   g.epi.out_rows = T;
   g.cluster2 = kW0Clusters;
   g.split_tail = g_w0_split_tail.load(std::memory_order_relaxed) != 0;
+  if (g_w0_pair.load(std::memory_order_relaxed) != 0) return w0_pair_run(g, s);
   return tc_gemm_run(g, s);
 }
 
@@ -1425,6 +1430,8 @@ int poetx_set_block_epilogue_fusion(int enable) {
 int poetx_set_w0_split_tail(int enable) {
   return g_w0_split_tail.exchange(enable != 0 ? 1 : 0);
 }
+
+int poetx_set_w0_pair_mma(int enable) { return g_w0_pair.exchange(enable != 0 ? 1 : 0); }
 
 }  // extern "C"
 

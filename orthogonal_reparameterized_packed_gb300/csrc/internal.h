@@ -99,6 +99,11 @@ cudaError_t tc_transform_sum(const __nv_bfloat16* X, const __nv_bfloat16* Z,
                              const __nv_bfloat16* sb, __nv_bfloat16* out, float* part, int d,
                              long long T, int splits, cudaStream_t stream);
 
+// The W0 GEMM (bf16 out, one batch, no K split, A K-major, N a multiple of
+// 256) on CTA pairs: 256 x 256 tiles, one tcgen05.mma.cta_group::2 per K
+// slice of 16; see gemm_pair.cu.
+cudaError_t w0_pair_run(const TcGemm& g, cudaStream_t stream);
+
 // Number of K splits the engine will actually use for `want` splits.
 int tc_effective_splits(int K, int want);
 cudaError_t tc_gemm_run(const TcGemm& g, cudaStream_t stream);

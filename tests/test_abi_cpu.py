@@ -189,3 +189,7 @@ def test_process_wide_switches_return_the_previous_setting(lib):
     assert poetx.poetx_set_w0_split_tail(False) is True
     assert poetx.poetx_set_w0_split_tail(True) is False
     assert poetx.poetx_set_w0_split_tail(True) is True
+    # the W0 GEMMs on CTA pairs by default
+    assert poetx.poetx_set_w0_pair_mma(False) is True
+    assert poetx.poetx_set_w0_pair_mma(True) is False
+    assert poetx.poetx_set_w0_pair_mma(True) is True

@@ -1,6 +1,7 @@
-"""The W0 GEMMs' cluster schedule: tiles of the last partial round may be
-spread one per cluster with their K steps split between the cluster's two
-CTAs (poetx_set_w0_split_tail).  Shapes are chosen so that, on a GPU with
+"""The W0 GEMMs' forms: CTA pairs with one 256-row MMA across two SMs (the
+default, poetx_set_w0_pair_mma), or clusters of two one-SM MMAs whose last
+partial round of tiles may be spread one per cluster with the K steps split
+between the cluster's two CTAs (poetx_set_w0_split_tail).  Shapes are chosen so that, on a GPU with
 about 70-80 clusters of two, every kind of schedule occurs: all tiles split
 (few tiles), whole units plus a split last round, and no split (a last
 round more than half full).  With theta = 0 the blocks are exactly I, so
@@ -28,16 +29,23 @@ def px():
     return poetx
 
 
-def run(px, inp, split):
+# the W0 GEMM forms: (pair MMA, split last round of the cluster form)
+MODES = {"pair": (True, True), "split": (False, True), "unsplit": (False, False)}
+
+
+def run(px, inp, mode):
     from orthogonal_reparameterized_packed_gb300.layer import PoetxLayer, to_device
+    pair, split = MODES[mode]
     dev = to_device(inp)
     layer = PoetxLayer(inp.d_in, inp.d_out, inp.b, inp.k, inp.tokens, dtype=inp.dtype)
     prev = px.poetx_set_w0_split_tail(split)
+    prev_pair = px.poetx_set_w0_pair_mma(pair)
     try:
         layer.step(dev["theta_P"], dev["theta_R"], dev["W0"], dev["x"], dev["dy"])
         torch.cuda.synchronize()
     finally:
         px.poetx_set_w0_split_tail(prev)
+        px.poetx_set_w0_pair_mma(prev_pair)
     st = px.poetx_device_status()
     assert st == 0, px.poetx_status_string(st)
     return layer, dev
@@ -62,13 +70,14 @@ SHAPES = [
 ]
 
 
-@pytest.mark.parametrize("T,d_in,d_out", SHAPES)
-@pytest.mark.parametrize("split", [True, False])
-def test_zero_theta_layer_is_the_plain_linear_map(px, T, d_in, d_out, split):
+@pytest.mark.parametrize("T,d_in,d_out", SHAPES + [(1, 256, 256), (255, 256, 512),
+                                                   (257, 512, 256)])
+@pytest.mark.parametrize("mode", sorted(MODES))
+def test_zero_theta_layer_is_the_plain_linear_map(px, T, d_in, d_out, mode):
     inp = make_layer_inputs(d_in, d_out, 256, 3, T, dtype="bf16", seed=80)
     inp.theta_P[:] = 0
     inp.theta_R[:] = 0
-    layer, dev = run(px, inp, split)
+    layer, dev = run(px, inp, mode)
     ref = oracle.layer(inp.theta_P, inp.theta_R, inp.W0, inp.x, inp.dy, 256, 3)
     check_plain_linear(layer.y, ref["y"])
     check_plain_linear(layer.dx, ref["dx"])
@@ -76,10 +85,11 @@ def test_zero_theta_layer_is_the_plain_linear_map(px, T, d_in, d_out, split):
 
 @pytest.mark.parametrize("T,d_in,d_out", [(129, 512, 1024), (1280, 4096, 4096),
                                           (16384, 4096, 4096)])
-def test_split_and_unsplit_schedules_agree(px, T, d_in, d_out):
+@pytest.mark.parametrize("mode", ["split", "pair"])
+def test_schedules_agree(px, T, d_in, d_out, mode):
     inp = make_layer_inputs(d_in, d_out, 256, 3, T, dtype="bf16", seed=81)
-    a, _ = run(px, inp, True)
-    b, _ = run(px, inp, False)
+    a, _ = run(px, inp, mode)
+    b, _ = run(px, inp, "unsplit")
     # v and du (bf16 roundings of fp32 sums in two orders) differ in a few
     # elements by one bf16 step; y and dx carry that through a block product
     for name, bound in (("y", 2e-3), ("dx", 2e-3), ("dtheta_P", 1e-2), ("dtheta_R", 1e-2)):
