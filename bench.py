@@ -71,13 +71,23 @@ def parse():
     ap.add_argument("--no-split-tail", action="store_true",
                     help="W0 GEMMs: every tile sums K in one CTA (no K split of the last "
                          "partial round of tiles across a cluster's two CTAs)")
+    ap.add_argument("--profile-pass", action="store_true",
+                    help="for profilers: W warm-up steps, then K eager steps and exit (no "
+                         "timing repeats, graph, end-to-end leg or CPU baseline)")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override the workload's token count (profiling a smaller case)")
     ap.add_argument("--recompute-v", action="store_true",
                     help="backward recomputes v = W0 P x instead of reading it (saves T x d_out)")
     return ap.parse_args()
 
 
+TOKENS_OVERRIDE = None
+
+
 def workload_config(name):
     w = dict(WORKLOADS[name])
+    if TOKENS_OVERRIDE is not None:
+        w["tokens"] = TOKENS_OVERRIDE
     return w
 
 
@@ -536,6 +546,17 @@ def run_gpu(args):
     torch.cuda.synchronize()
     if poetx.poetx_device_status() != 0:
         raise RuntimeError("device status not OK after warm-up")
+    if args.profile_pass:
+        for _ in range(args.steps):
+            step()
+        torch.cuda.synchronize()
+        status = poetx.poetx_device_status()
+        if rank == 0:
+            print(json.dumps({"profile_pass": name, "steps": args.steps, "tokens": w["tokens"],
+                              "device_status": status}), flush=True)
+        if status != 0:
+            raise RuntimeError("device status not OK")
+        return
 
     # (1) eager pass: every launch bracketed by CUDA events on its stream,
     #     giving the per-kernel durations the roofline uses.  Like the timed
@@ -939,7 +960,9 @@ def run_sweep(args):
 
 
 def main():
+    global TOKENS_OVERRIDE
     args = parse()
+    TOKENS_OVERRIDE = args.tokens
     if args.impl == "reference":
         run_reference(args)
     elif args.workload == SWEEP:
