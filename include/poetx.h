@@ -103,9 +103,13 @@ poetx_status poetx_build_blocks(const float* theta, int d, int b, int k, poetx_d
  * process exits), so:
  *   - (d/b) * b * b = d * b must be <= 2^20 (e.g. d = 4096 with b = 256);
  *     larger builds return POETX_ERR_WORKSPACE before anything is enqueued;
- *   - the first call on each device looks up that array's device address
- *     (cudaGetSymbolAddress) with the device current; make that first call
- *     before any stream capture;
+ *   - each call made outside stream capture looks up that array's device
+ *     address (cudaGetSymbolAddress) with the device current, so the
+ *     address stays right after the context is re-created (for example by
+ *     cudaDeviceReset); a call made while its stream is being captured
+ *     reuses the address of the last call outside capture on that device,
+ *     so make the first call on a device, and the first after a device
+ *     reset, before any stream capture (otherwise POETX_ERR_CUDA);
  *   - calls share the array: calls that overlap on the GPU (other streams
  *     or host threads on the same device) race and must be serialised;
  *     nothing needs to be zeroed between calls.

@@ -818,8 +818,13 @@ const void* superblocks_or_blocks(const void* blocks, bf16* sb, int d, int b, bo
 //
 // Host code may not use that array's name as a device address (in host
 // code it names a host-side stand-in), so the device address is looked up
-// with cudaGetSymbolAddress once per device, with that device current, on
-// the first call made on it, and handed to the kernels.
+// with cudaGetSymbolAddress, with the device current, on every call made
+// outside stream capture (the lookup follows the module if the context was
+// destroyed and re-created, e.g. by cudaDeviceReset), and handed to the
+// kernels.  A call made while its stream is being captured uses the address
+// found by the last call outside capture on that device, so the first call
+// on a device, and the first after a device reset, must come before any
+// stream capture.
 //
 // Every call shares the one array and the array keeps whatever the last call
 // left in it.  The build needs no part of it to start at zero: every word a
@@ -842,13 +847,17 @@ static __device__ __align__(256) unsigned char g_build_scratch[kNoAllocScratchBy
 std::mutex g_scratch_mu;
 
 // Device address of g_build_scratch on the current device (nullptr on
-// failure); looked up once per device.
-void* build_scratch_address() {
-  static void* addr[64] = {};
+// failure): looked up when `stream` is not capturing, else the address the
+// last lookup on this device found.
+void* build_scratch_address(cudaStream_t stream) {
+  static std::vector<void*> addr;  // by device ordinal
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return nullptr;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return nullptr;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (addr[dev] == nullptr) {
+  if (static_cast<size_t>(dev) >= addr.size()) addr.resize(dev + 1, nullptr);
+  if (cs == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_build_scratch) != cudaSuccess) return nullptr;
     addr[dev] = p;
@@ -1248,7 +1257,7 @@ poetx_status poetx_build_blocks_noalloc(const float* theta, int d, int b, int k,
   Carver dry(nullptr);
   carve_build(dry, d / b, b, k, is_bf16);
   if (dry.off > kNoAllocScratchBytes) return POETX_ERR_WORKSPACE;
-  void* scratch = build_scratch_address();
+  void* scratch = build_scratch_address(static_cast<cudaStream_t>(stream));
   if (scratch == nullptr) return POETX_ERR_CUDA;
   Carver c(scratch);
   BuildBufs w = carve_build(c, d / b, b, k, is_bf16);

@@ -35,8 +35,11 @@ def rel_fro(a, b):
     return float(torch.linalg.norm(a - b) / torch.linalg.norm(b))
 
 
+# the last two reach the scratch limit d * b = 2^20 on the fp32 path (three
+# fp32 stacks of d * b elements: exactly 12 MiB)
 @pytest.mark.parametrize("dtype,d,b,k", [("bf16", 4096, 256, 3), ("f32", 256, 32, 3),
-                                         ("bf16", 1024, 64, 5), ("bf16", 2048, 512, 1)])
+                                         ("bf16", 1024, 64, 5), ("bf16", 2048, 512, 1),
+                                         ("f32", 4096, 256, 3), ("f32", 2048, 512, 2)])
 def test_noalloc_build_matches_workspace_build(px, dtype, d, b, k):
     code = px.BF16 if dtype == "bf16" else px.F32
     tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
