@@ -243,11 +243,14 @@ poetx_status poetx_dequantize_w0(const int8_t* W0_q, const float* scales, void* 
  * with fusion on, poetx_forward computes y = R v in the epilogue of the
  * GEMM that produces v (v is stored only into a non-NULL v_saved), and
  * poetx_backward computes dx = du P in the epilogue of the GEMM that
- * produces du, for BF16 with b <= 256.  Results agree with the unfused path
- * to bf16 rounding.  Off by default: on GB300 the fused GEMM's 64 KiB
- * staging tile leaves room for a 3-stage operand ring only, and it runs
- * slower than the plain GEMM plus the separate block transform.  Process-
- * wide; returns the previous setting. */
+ * produces du, for BF16 with b <= 256; the token sums of the P side then
+ * run on their own over x and du.  y and everything on the R side have the
+ * same bits as the unfused path; dx and dtheta_P agree to fp32 summation
+ * order.  Off by default: on GB300 the fused W0 GEMM on CTA pairs takes
+ * about 55 us longer per launch at d = 4096, T = 16384 (the block product
+ * adds 6 % of MMA work, and staging the tile twice in TMEM reads, shared
+ * memory and TMA stores slows the main loop), more than the separate block
+ * transform it replaces.  Process-wide; returns the previous setting. */
 int poetx_set_block_epilogue_fusion(int enable);
 
 /* Scheduling of the W0 GEMMs (technical summary, section 2: the frozen-

@@ -314,6 +314,7 @@ cudaError_t tc_w0_block(const bf16* A, const bf16* W0, const bf16* sb, bf16* out
   g.out_blk = out_blk;
   g.epi.row_limit = static_cast<int>(T);
   g.epi.out_rows = T;
+  if (g_w0_pair.load(std::memory_order_relaxed) != 0) return w0_pair_run(g, s);
   return tc_gemm_run(g, s);
 }
 
@@ -745,7 +746,7 @@ bool use_transform_sum(bool is_bf16, int n, int b, int k) {
 }
 
 BwdPlan carve_backward(Carver& c, int d_in, int d_out, int b, int k, long long T, bool is_bf16,
-                       bool recompute_v) {
+                       bool recompute_v, bool fused) {
   BwdPlan p;
   if (recompute_v) {
     p.sb.u = take_act(c, T, d_in, is_bf16);
@@ -760,7 +761,9 @@ BwdPlan carve_backward(Carver& c, int d_in, int d_out, int b, int k, long long T
       p.sb.rsb = c.take<bf16>(static_cast<size_t>(d_out) * 256);
     }
     const bool ts = use_transform_sum(is_bf16, (d_in + d_out) / b, b, k);
-    p.splits_in = ts ? transform_sum_splits(d_in, T) : outer_splits(d_in, S, T);
+    // with the block factor in the dgrad GEMM's epilogue, G_P's token sums
+    // run on their own (outer splits)
+    p.splits_in = ts && !fused ? transform_sum_splits(d_in, T) : outer_splits(d_in, S, T);
     p.splits_out = ts ? transform_sum_splits(d_out, T) : outer_splits(d_out, S, T);
     const long long part_in = static_cast<long long>(p.splits_in) * d_in * S;
     const long long part_out = static_cast<long long>(p.splits_out) * d_out * S;
@@ -980,8 +983,11 @@ size_t poetx_backward_workspace_size(int d_in, int d_out, int b, int k, int64_t 
       check_common(b, k, tokens, dtype) != POETX_OK)
     return 0;
   Carver c(nullptr);
-  carve_backward(c, d_in, d_out, b, k, tokens, is_bf16, recompute_v != 0);
-  return c.off;
+  // enough for either form of the backward (block factor fused or not)
+  Carver c2(nullptr);
+  carve_backward(c, d_in, d_out, b, k, tokens, is_bf16, recompute_v != 0, false);
+  carve_backward(c2, d_in, d_out, b, k, tokens, is_bf16, recompute_v != 0, true);
+  return c.off > c2.off ? c.off : c2.off;
 }
 
 poetx_status poetx_backward(const void* dy, const void* x, const void* W0, const float* theta_P,
@@ -1010,8 +1016,9 @@ poetx_status poetx_backward(const void* dy, const void* x, const void* W0, const
     if (q == nullptr || !aligned16(q)) return POETX_ERR_INVALID_ARG;
   if (!aligned16(v_saved)) return POETX_ERR_INVALID_ARG;
   const bool recompute = v_saved == nullptr;
+  const bool fused = fuse_block_epilogue(is_bf16, b);
   Carver c(workspace);
-  BwdPlan p = carve_backward(c, d_in, d_out, b, k, tokens, is_bf16, recompute);
+  BwdPlan p = carve_backward(c, d_in, d_out, b, k, tokens, is_bf16, recompute, fused);
   if (workspace == nullptr || c.off > workspace_bytes || !aligned16(workspace))
     return POETX_ERR_WORKSPACE;
   cudaError_t e;
@@ -1034,14 +1041,26 @@ poetx_status poetx_backward(const void* dy, const void* x, const void* W0, const
                          static_cast<const bf16*>(rsb), static_cast<bf16*>(p.sb.dv), p.part_out,
                          d_out, tokens, p.splits_out, s);
     if (e != cudaSuccess) return POETX_ERR_CUDA;
-    e = tc_w0(static_cast<const bf16*>(p.sb.dv), static_cast<const bf16*>(W0),
-              static_cast<bf16*>(p.sb.du), d_in, d_out, tokens, true, s);
-    if (e != cudaSuccess) return POETX_ERR_CUDA;
-    // dx = du P with the G_P^T partials (sum_t x_t du_t^T) in one pass over du
-    e = tc_transform_sum(static_cast<const bf16*>(p.sb.du), static_cast<const bf16*>(x),
-                         static_cast<const bf16*>(psb), static_cast<bf16*>(dx), p.sb.part, d_in,
-                         tokens, p.splits_in, s);
-    if (e != cudaSuccess) return POETX_ERR_CUDA;
+    if (fused) {
+      // du = dv W0 and dx = du P in one GEMM; then the G_P^T partials
+      // (sum_t x_t du_t^T) from du and x
+      e = tc_w0_block(static_cast<const bf16*>(p.sb.dv), static_cast<const bf16*>(W0),
+                      static_cast<const bf16*>(psb), static_cast<bf16*>(p.sb.du),
+                      static_cast<bf16*>(dx), d_in, d_out, tokens, true, s);
+      if (e != cudaSuccess) return POETX_ERR_CUDA;
+      e = tc_outer(static_cast<const bf16*>(x), static_cast<const bf16*>(p.sb.du), p.sb.part,
+                   d_in, S, tokens, p.splits_in, s);
+      if (e != cudaSuccess) return POETX_ERR_CUDA;
+    } else {
+      e = tc_w0(static_cast<const bf16*>(p.sb.dv), static_cast<const bf16*>(W0),
+                static_cast<bf16*>(p.sb.du), d_in, d_out, tokens, true, s);
+      if (e != cudaSuccess) return POETX_ERR_CUDA;
+      // dx = du P with the G_P^T partials (sum_t x_t du_t^T) in one pass over du
+      e = tc_transform_sum(static_cast<const bf16*>(p.sb.du), static_cast<const bf16*>(x),
+                           static_cast<const bf16*>(psb), static_cast<bf16*>(dx), p.sb.part,
+                           d_in, tokens, p.splits_in, s);
+      if (e != cudaSuccess) return POETX_ERR_CUDA;
+    }
     return to_status(chain_adjoint_from_parts(theta_P, d_in / b, p.sb.part, p.splits_in,
                                               theta_R, d_out / b, p.part_out, p.splits_out, b, k,
                                               p.cnp, dtheta_P, dtheta_R, s));
@@ -1062,7 +1081,6 @@ poetx_status poetx_backward(const void* dy, const void* x, const void* W0, const
                        p.cnp.g32[0] + off_R, p.cnp.g16[0] ? p.cnp.g16[0] + off_R : nullptr, s);
   if (e != cudaSuccess) return POETX_ERR_CUDA;
   // du = dv W0, and dx = du P (in the same GEMM's epilogue when it fuses)
-  const bool fused = fuse_block_epilogue(is_bf16, b);
   if (fused)
     e = tc_w0_block(static_cast<const bf16*>(p.sb.dv), static_cast<const bf16*>(W0),
                     static_cast<const bf16*>(psb), static_cast<bf16*>(p.sb.du),
