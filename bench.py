@@ -387,8 +387,9 @@ def load_peaks():
 # the files each kernel is compiled from: its DRAM counters stay valid while
 # these are unchanged
 GEMM_SOURCES = ("gemm_tc.cu", "tc_common.cuh", "ptx.cuh", "internal.h")
+PAIR_SOURCES = ("gemm_pair.cu", "tc_common.cuh", "ptx.cuh", "internal.h")
 KERNEL_SOURCES = {
-    "gemm_w0": GEMM_SOURCES, "gemm_w0_dgrad": GEMM_SOURCES, "transform": GEMM_SOURCES,
+    "gemm_w0": PAIR_SOURCES, "gemm_w0_dgrad": PAIR_SOURCES, "transform": GEMM_SOURCES,
     "transform_t": GEMM_SOURCES, "outer": GEMM_SOURCES,
     "transform_sum": ("transform_sum_tc.cu", "tc_common.cuh", "ptx.cuh", "internal.h"),
 }
