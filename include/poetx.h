@@ -87,6 +87,9 @@ size_t poetx_packed_size(int d, int b);
  * Blocks are independent, so both factors of a layer are one call when
  * theta_P and theta_R lie back to back (and the blocks likewise):
  * d = d_in + d_out builds P's blocks then R's, bitwise as two calls would.
+ * BF16 with k = 3 and b <= 256 runs on CTA pairs with every operand in
+ * shared memory and needs no workspace (its size is 0 and the workspace
+ * may be NULL).
  * ------------------------------------------------------------------------ */
 size_t poetx_build_workspace_size(int d, int b, int k, poetx_dtype dtype);
 poetx_status poetx_build_blocks(const float* theta, int d, int b, int k, poetx_dtype dtype,

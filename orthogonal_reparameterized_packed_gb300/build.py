@@ -18,8 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpoetx.so")
-SOURCES = ["api.cu", "gemm_tc.cu", "gemm_pair.cu", "chain_tc.cu", "transform_sum_tc.cu",
-           "kernels_simt.cu", "selftest.cu"]
+SOURCES = ["api.cu", "gemm_tc.cu", "gemm_pair.cu", "chain_tc.cu", "cnp_pair.cu",
+           "transform_sum_tc.cu", "kernels_simt.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

@@ -488,8 +488,15 @@ struct BuildBufs {
 // Buffers of one block build: the one-launch chain needs bf16 Q (hi and lo
 // parts), 2I and two bf16 E stacks; the per-product path fp32 Q plus bf16 (tensor
 // cores) or fp32 (FFMA) E stacks.
+// The k = 3 build of bf16 blocks with b <= 256 runs on CTA pairs with its
+// operands in shared memory (cnp_pair.cu): no workspace.
+bool use_pair_build(bool is_bf16, int n, int b, int k) {
+  return is_bf16 && cnp_pair_fits(b, k) && (static_cast<long long>(n) * b) % 256 == 0;
+}
+
 BuildBufs carve_build(Carver& c, int n, int b, int k, bool is_bf16) {
   BuildBufs w;
+  if (use_pair_build(is_bf16, n, b, k)) return w;
   const size_t nbb = static_cast<size_t>(n) * b * b;
   if (use_chain(is_bf16, n, b, k)) {
     w.q16 = c.take<bf16>(nbb);
@@ -515,6 +522,8 @@ BuildBufs carve_build(Carver& c, int n, int b, int k, bool is_bf16) {
 cudaError_t run_build(const float* theta, int n, int b, int k, bool is_bf16, void* blocks,
                       const BuildBufs& w, cudaStream_t s) {
   const bool tc = tc_small(is_bf16, b);
+  if (use_pair_build(is_bf16, n, b, k))
+    return cnp_build_pair(theta, n, b, static_cast<bf16*>(blocks), s);
   if (use_chain(is_bf16, n, b, k)) {  // the whole recursion in one cooperative launch
     ChainBuildArgs a;
     a.n = n;
@@ -913,7 +922,7 @@ poetx_status poetx_build_blocks(const float* theta, int d, int b, int k, poetx_d
     return POETX_ERR_INVALID_ARG;
   Carver c(workspace);
   BuildBufs w = carve_build(c, d / b, b, k, is_bf16);
-  if (workspace == nullptr || c.off > workspace_bytes || !aligned16(workspace))
+  if (c.off > 0 && (workspace == nullptr || c.off > workspace_bytes || !aligned16(workspace)))
     return POETX_ERR_WORKSPACE;
   return to_status(
       run_build(theta, d / b, b, k, is_bf16, blocks, w, static_cast<cudaStream_t>(stream)));

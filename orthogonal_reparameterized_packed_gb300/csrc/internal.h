@@ -172,6 +172,15 @@ struct ChainAdjointArgs {
 };
 cudaError_t chain_adjoint(const ChainAdjointArgs& a, cudaStream_t stream);
 
+// ------------------------------------------- b x b chains on CTA pairs
+// k = 3 and b in {32, 64, 128, 256} (256 x 256 superblocks), bf16 blocks:
+// one cluster of two CTAs per superblock with every operand in shared
+// memory (cnp_pair.cu).  n * b must be a multiple of 256.
+bool cnp_pair_fits(int b, int k);
+// blocks [n][b][b] = (I + Q)(I + Q + Q^2 + Q^3) from theta [n][b(b-1)/2].
+cudaError_t cnp_build_pair(const float* theta, int n, int b, __nv_bfloat16* blocks,
+                           cudaStream_t stream);
+
 // ------------------------------------------------------------ elementwise
 // Packed parameters of two sides (theta_a: n_a blocks, theta_b: n_b blocks;
 // theta_b may be null when n_b = 0) -> Q [n_a + n_b][b][b], fp32 and/or bf16.

@@ -118,7 +118,9 @@ def test_unpack_is_bit_exact(px, dtype, d, b):
     ("bf16", 512, 32, 5), ("bf16", 512, 64, 3), ("bf16", 512, 128, 1), ("bf16", 512, 128, 3),
     ("bf16", 1024, 256, 3), ("bf16", 1024, 256, 5), ("bf16", 1024, 512, 3),
     ("bf16", 1024, 512, 1), ("bf16", 512, 256, 10), ("bf16", 512, 128, 0),
-    ("bf16", 512, 256, 16), ("f32", 64, 8, 16), ("bf16", 768, 256, 8)])  # k = 16: the maximum
+    ("bf16", 512, 256, 16), ("f32", 64, 8, 16), ("bf16", 768, 256, 8),  # k = 16: the maximum
+    # k = 3, b <= 256: the CTA-pair build (256 x 256 superblocks)
+    ("bf16", 256, 32, 3), ("bf16", 768, 64, 3), ("bf16", 2048, 128, 3), ("bf16", 4096, 256, 3)])
 def test_build_blocks_matches_oracle(px, dtype, d, b, k):
     rng = np.random.default_rng(21)
     theta = (rng.standard_normal((d // b, b * (b - 1) // 2)) * 0.02).astype(np.float32)
