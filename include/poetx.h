@@ -81,7 +81,8 @@ size_t poetx_packed_size(int d, int b);
  *   = I + 2Q + ... + 2Q^k + Q^{k+1}, the Neumann-truncated Cayley transform
  * (technical summary, section 2, CNP bullet: the powers Q^2..Q^4 of k = 3
  * are built in one fused step).  Arithmetic in fp32 (F32) or bf16 tensor
- * cores with fp32 accumulation (BF16, b >= 128); rounded once at the store.
+ * cores with fp32 accumulation (BF16: b >= 128, and k = 3 with b = 32..256);
+ * rounded once at the store.
  *   theta  [d/b][b(b-1)/2] float32 (read only)
  *   blocks [d/b][b][b] dtype (written)
  * Blocks are independent, so both factors of a layer are one call when

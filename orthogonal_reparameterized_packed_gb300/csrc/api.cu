@@ -579,10 +579,21 @@ struct CnpBufs {
   unsigned int* counter = nullptr;
   bf16* two_i = nullptr;  // chain: constant 2I
   bf16* x16 = nullptr;    // chain, k = 3: 2Q
+  // the adjoint on CTA pairs (k = 3, b <= 256): H (bf16) per 256 x 256
+  // superblock
+  bool pair = false;
+  bf16* hg = nullptr;
 };
 
-CnpBufs carve_cnp(Carver& c, int n, int b, int k, bool tc) {
+CnpBufs carve_cnp(Carver& c, int n, int b, int k, bool is_bf16) {
   CnpBufs w;
+  if (use_pair_build(is_bf16, n, b, k)) {
+    const size_t sq = static_cast<size_t>(n) * b * 256;  // superblocks x 256 x 256
+    w.pair = true;
+    w.hg = c.take<bf16>(sq);
+    return w;
+  }
+  const bool tc = tc_small(is_bf16, b);
   const size_t nbb = static_cast<size_t>(n) * b * b;
   w.q32 = c.take<float>(nbb);
   if (tc) w.q16 = c.take<bf16>(nbb);
@@ -614,6 +625,22 @@ cudaError_t chain_adjoint_from_parts(const float* theta_a, int n_a, const float*
                                      const float* part_b, int splits_b, int b, int k,
                                      const CnpBufs& w, float* dtheta_a, float* dtheta_b,
                                      cudaStream_t s) {
+  if (w.pair) {  // one launch on CTA pairs, superblocks of both sides
+    CnpAdjointPairArgs x;
+    x.n_a = n_a;
+    x.n_b = n_b;
+    x.b = b;
+    x.theta_a = theta_a;
+    x.theta_b = theta_b;
+    x.part_a = part_a;
+    x.part_b = part_b;
+    x.splits_a = splits_a;
+    x.splits_b = splits_b;
+    x.hg = w.hg;
+    x.dtheta_a = dtheta_a;
+    x.dtheta_b = dtheta_b;
+    return cnp_adjoint_pair(x, s);
+  }
   ChainAdjointArgs a;
   a.n_a = n_a;
   a.n_b = n_b;
@@ -751,7 +778,7 @@ struct BwdPlan {
 // The backward's transposed transforms and token sums run fused (one pass over
 // dy and one over du) on the chain path with 256 x 256 superblocks.
 bool use_transform_sum(bool is_bf16, int n, int b, int k) {
-  return use_chain(is_bf16, n, b, k) && b <= 256;
+  return (use_chain(is_bf16, n, b, k) && b <= 256) || use_pair_build(is_bf16, n, b, k);
 }
 
 BwdPlan carve_backward(Carver& c, int d_in, int d_out, int b, int k, long long T, bool is_bf16,
@@ -776,14 +803,15 @@ BwdPlan carve_backward(Carver& c, int d_in, int d_out, int b, int k, long long T
     p.splits_out = ts ? transform_sum_splits(d_out, T) : outer_splits(d_out, S, T);
     const long long part_in = static_cast<long long>(p.splits_in) * d_in * S;
     const long long part_out = static_cast<long long>(p.splits_out) * d_out * S;
-    if (use_chain(is_bf16, (d_in + d_out) / b, b, k)) {
+    if (use_chain(is_bf16, (d_in + d_out) / b, b, k) ||
+        use_pair_build(is_bf16, (d_in + d_out) / b, b, k)) {  // both live until the adjoint
       p.sb.part = c.take<float>(static_cast<size_t>(part_in));
       p.part_out = c.take<float>(static_cast<size_t>(part_out));
     } else {
       p.sb.part = c.take<float>(static_cast<size_t>(part_in > part_out ? part_in : part_out));
     }
   }
-  p.cnp = carve_cnp(c, (d_in + d_out) / b, b, k, tc_small(is_bf16, b));
+  p.cnp = carve_cnp(c, (d_in + d_out) / b, b, k, is_bf16);
   return p;
 }
 
@@ -1139,7 +1167,7 @@ size_t poetx_transform_workspace_size(int d, int b, int k, int64_t tokens, poetx
                                                                : outer_splits(d, S, tokens);
     c.take<float>(static_cast<size_t>(splits) * d * S);
   }
-  carve_cnp(c, d / b, b, k, tc_small(is_bf16, b));
+  carve_cnp(c, d / b, b, k, is_bf16);
   return c.off;
 }
 
@@ -1193,7 +1221,7 @@ poetx_status poetx_transform_backward(const void* dout, const void* x, const flo
   const int splits =
       !is_bf16 ? 1 : (ts ? transform_sum_splits(d, tokens) : outer_splits(d, S, tokens));
   float* part = is_bf16 ? c.take<float>(static_cast<size_t>(splits) * d * S) : nullptr;
-  CnpBufs cnp = carve_cnp(c, d / b, b, k, tc_small(is_bf16, b));
+  CnpBufs cnp = carve_cnp(c, d / b, b, k, is_bf16);
   if (workspace == nullptr || c.off > workspace_bytes || !aligned16(workspace))
     return POETX_ERR_WORKSPACE;
   cudaError_t e;

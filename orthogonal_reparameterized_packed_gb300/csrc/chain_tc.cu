@@ -100,9 +100,6 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
   return v;
 }
 
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
 
 // Wait until every CTA has finished phase `phase - 1`.
 __device__ bool grid_wait(const ChainParams& P, int phase, volatile int* abort) {

@@ -181,6 +181,23 @@ bool cnp_pair_fits(int b, int k);
 cudaError_t cnp_build_pair(const float* theta, int n, int b, __nv_bfloat16* blocks,
                            cudaStream_t stream);
 
+// Packed gradients of both sides from the split-K partials of the
+// TRANSPOSED block gradients G^T over 256 x 256 superblocks (blocks
+// [0, n_a) of side a, then n_b of side b), k = 3.  Scratch: hg
+// [(n_a + n_b) * b / 256 * 256][256] bf16.
+struct CnpAdjointPairArgs {
+  int n_a = 0, n_b = 0, b = 0;
+  const float* theta_a = nullptr;
+  const float* theta_b = nullptr;
+  const float* part_a = nullptr;
+  const float* part_b = nullptr;
+  int splits_a = 1, splits_b = 1;
+  __nv_bfloat16* hg = nullptr;
+  float* dtheta_a = nullptr;
+  float* dtheta_b = nullptr;
+};
+cudaError_t cnp_adjoint_pair(const CnpAdjointPairArgs& a, cudaStream_t stream);
+
 // ------------------------------------------------------------ elementwise
 // Packed parameters of two sides (theta_a: n_a blocks, theta_b: n_b blocks;
 // theta_b may be null when n_b = 0) -> Q [n_a + n_b][b][b], fp32 and/or bf16.

@@ -113,6 +113,12 @@ __device__ __forceinline__ void bulk_load_1d(void* smem_dst, const void* src, ui
       : "memory");
 }
 
+// Order this thread's generic-proxy writes to global memory before later
+// async-proxy (TMA) reads of it.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // Order this thread's generic-proxy writes to shared memory of any CTA of
 // the cluster before later async-proxy (tensor core, TMA) accesses.
 __device__ __forceinline__ void fence_proxy_async_all() {
@@ -163,6 +169,18 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_
 // 2-byte store to a shared::cluster address (this CTA's or a peer's).
 __device__ __forceinline__ void st_cluster_b16(uint32_t addr, uint16_t v) {
   asm volatile("st.shared::cluster.b16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
+// 4-byte load from this CTA's shared memory (a 32-bit shared address).
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+
+// 4-byte store to a shared::cluster address (this CTA's or a peer's).
+__device__ __forceinline__ void st_cluster_b32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 // 4-byte load from a shared::cluster address (this CTA's or a peer's).
