@@ -191,7 +191,7 @@ poetx_status poetx_transform_backward(const void* dout, const void* x, const flo
  *   permutation.
  *   Entries outside 0..d-1 are not followed: the output gets 0 and
  *   POETX_ERR_INVALID_ARG is recorded in the status word.  Rows must be a
- *   multiple of 16 bytes and d <= 25600 (INVALID_ARG otherwise).
+ *   multiple of 16 bytes and d <= 28672 (INVALID_ARG otherwise).
  * ------------------------------------------------------------------------ */
 /* out[r][i] = in[r][perm[i]] for rows x d activations (in != out). */
 poetx_status poetx_permute_features(const void* in, const int32_t* perm, void* out, int64_t rows,

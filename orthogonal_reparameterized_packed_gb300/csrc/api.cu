@@ -1321,8 +1321,8 @@ poetx_status poetx_build_blocks_noalloc(const float* theta, int d, int b, int k,
 }
 
 // The index-map kernel keeps one 8-byte entry per feature (4 bf16 or 2 fp32
-// rows interleaved) in 200 KiB of shared memory.
-constexpr int kMaxPermuteFeatures = 25600;
+// rows interleaved) in at most 224 KiB of shared memory.
+constexpr int kMaxPermuteFeatures = 28672;
 
 poetx_status poetx_permute_features(const void* in, const int32_t* perm, void* out, int64_t rows,
                                     int d, poetx_dtype dtype, poetx_stream stream) {

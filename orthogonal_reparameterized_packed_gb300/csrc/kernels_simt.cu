@@ -384,20 +384,30 @@ __global__ void __launch_bounds__(256) pack_tiles_kernel(const float* __restrict
 }
 
 // out[r][i] = in[row_map ? row_map[r] : r][col_map[i]] for r < rows, i < d.
-// One CTA per group of R rows at a time (R = 8 bytes / element: 4 bf16 or 2
-// fp32 rows): the CTA reads its R source rows with 16-byte coalesced loads
-// and writes them into shared memory interleaved, one 8-byte entry per column
-// holding that column of all R rows; each thread then gathers 8-byte entries
-// at the mapped columns (column map read as 16-byte vectors), so one random
-// shared-memory read serves R outputs, and writes each row's 16 bytes of
-// consecutive outputs with one 16-byte store.  The d x 8-byte table is small
-// enough for several CTAs per SM, whose groups overlap one another's loads.
+// A CTA takes groups of R rows (R = 8 bytes / element: 4 bf16 or 2 fp32
+// rows) in turn.  Its producer warps read a group's R source rows with
+// 16-byte coalesced loads (128 bytes per thread in flight)
+// and write them into a shared-memory table interleaved, one 8-byte entry
+// per column holding that column of all R rows; its consumer warps gather
+// 8-byte entries at the mapped columns, so one random shared-memory read
+// serves R outputs, and write each row's 16 bytes of consecutive outputs
+// with one 16-byte store.  With two tables (NBUF = 2, when 16 d bytes fit)
+// the producers fill one while the consumers drain the other, so the loads
+// of the next group run during this group's gather and stores; named
+// barriers hand the tables over (producers arrive, consumers wait, and back).
+// Table order: the entry of column c sits at (c % V) * (d / V) + c / V (V
+// columns per 16-byte vector), so a warp's stores of entries are consecutive
+// 8-byte words; bf16 entries and output words are assembled by byte
+// permutes.  A consumer serves the same vectors in every group and keeps
+// the table positions of its first KR vectors in registers.
 // Map entries outside [0, d) (or [0, in_rows)) are not followed: the output
 // gets 0 and the status word POETX_ERR_INVALID_ARG.
-constexpr int kPermThreads = 128;  // small CTAs: six fit an SM by registers and shared memory
+constexpr int kPermRoleThreads = 128;  // producers, and as many consumers
+constexpr int kPermThreads = 2 * kPermRoleThreads;
+constexpr size_t kPermSmemMax = 224 * 1024;
 
-template <typename T>
-__global__ void __launch_bounds__(kPermThreads)
+template <typename T, int NBUF>
+__global__ void __launch_bounds__(kPermThreads, 3)
     permute_rows_kernel(const T* __restrict__ in, long long in_rows,
                         const int* __restrict__ row_map, const int* __restrict__ col_map,
                         T* __restrict__ out, long long rows, int d, int* status) {
@@ -406,14 +416,19 @@ __global__ void __launch_bounds__(kPermThreads)
   extern __shared__ __align__(16) unsigned char row_smem[];
   constexpr int V = 16 / sizeof(T);  // elements per 16-byte vector
   constexpr int R = 8 / sizeof(T);   // rows per group: one 8-byte entry per column
-  const int lane = threadIdx.x % 32;
-  uint2* ent = reinterpret_cast<uint2*>(row_smem);
+  constexpr int U = 8 / R;           // vectors of each row in flight per producer thread
+  constexpr int KR = 4;              // vectors whose table positions a consumer keeps
   const int nv = d / V;
   const long long groups = (rows + R - 1) / R;
-  for (long long grp = blockIdx.x; grp < groups; grp += gridDim.x) {
-    const long long r0 = grp * R;
-    long long src[R];
-    bool any_bad_row = false;
+  const bool producer = threadIdx.x < kPermRoleThreads;
+  const int tid = threadIdx.x % kPermRoleThreads;
+  // this CTA's groups: blockIdx.x + n * gridDim.x, n < count
+  const long long count =
+      blockIdx.x < groups ? (groups - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+
+  // the source rows of a group (-1: none, the output row is zero)
+  auto sources = [&](long long r0, long long (&src)[R]) {
+    bool bad = false;
 #pragma unroll
     for (int q = 0; q < R; ++q) {
       const long long r = r0 + q;
@@ -423,93 +438,166 @@ __global__ void __launch_bounds__(kPermThreads)
         if (row_map != nullptr) {
           const int m = row_map[r];
           src[q] = (m >= 0 && m < in_rows) ? m : -1;
-          any_bad_row |= src[q] < 0;
+          bad |= src[q] < 0;
         }
       }
     }
-    if (any_bad_row && threadIdx.x == 0) atomicCAS(status, 0, 1);
-    // interleave: entry j holds column j of the R rows (missing rows: 0);
-    // bf16: (r0 | r1 << 16, r2 | r3 << 16), fp32: (r0, r1)
-    for (int v = threadIdx.x; v < nv; v += kPermThreads) {
-      uint32_t w[R][4];
-#pragma unroll
-      for (int q = 0; q < R; ++q) {
-        uint4 u = make_uint4(0u, 0u, 0u, 0u);
-        if (src[q] >= 0) u = reinterpret_cast<const uint4*>(in + src[q] * d)[v];
-        w[q][0] = u.x;
-        w[q][1] = u.y;
-        w[q][2] = u.z;
-        w[q][3] = u.w;
-      }
-      // word i of row q, i chosen at run time, by selects (no local memory)
-      auto pick = [&](int q, int i) {
-        uint32_t r = w[q][0];
-        r = i == 1 ? w[q][1] : r;
-        r = i == 2 ? w[q][2] : r;
-        r = i == 3 ? w[q][3] : r;
-        return r;
-      };
-#pragma unroll
-      for (int k = 0; k < V; ++k) {
-        const int e = (k + lane) & (V - 1);  // rotated order spreads the banks
-        uint2 entry;
-        if constexpr (sizeof(T) == 2) {
-          const int sh = 16 * (e & 1);
-          entry.x = ((pick(0, e >> 1) >> sh) & 0xffffu) | (((pick(1, e >> 1) >> sh) & 0xffffu) << 16);
-          entry.y = ((pick(2, e >> 1) >> sh) & 0xffffu) | (((pick(3, e >> 1) >> sh) & 0xffffu) << 16);
-        } else {
-          entry.x = pick(0, e);
-          entry.y = pick(1, e);
-        }
-        ent[v * V + e] = entry;
-      }
+    return bad;
+  };
+  // named barriers 1 + b: table b is full; 1 + NBUF + b: table b is free
+  // (immediate ids: a register id would reserve all sixteen barriers)
+  auto bar_sync = [](int id) {
+    switch (id) {
+      case 1: asm volatile("bar.sync 1, %0;" ::"n"(kPermThreads) : "memory"); break;
+      case 2: asm volatile("bar.sync 2, %0;" ::"n"(kPermThreads) : "memory"); break;
+      case 3: asm volatile("bar.sync 3, %0;" ::"n"(kPermThreads) : "memory"); break;
+      default: asm volatile("bar.sync 4, %0;" ::"n"(kPermThreads) : "memory"); break;
     }
-    __syncthreads();
-    const int4* c4 = reinterpret_cast<const int4*>(col_map);
-    for (int v = threadIdx.x; v < nv; v += kPermThreads) {
-      int cols[V];
+  };
+  auto bar_arrive = [](int id) {
+    switch (id) {
+      case 1: asm volatile("bar.arrive 1, %0;" ::"n"(kPermThreads) : "memory"); break;
+      case 2: asm volatile("bar.arrive 2, %0;" ::"n"(kPermThreads) : "memory"); break;
+      case 3: asm volatile("bar.arrive 3, %0;" ::"n"(kPermThreads) : "memory"); break;
+      default: asm volatile("bar.arrive 4, %0;" ::"n"(kPermThreads) : "memory"); break;
+    }
+  };
+
+  if (producer) {
+    for (long long n = 0; n < count; ++n) {
+      const int buf = static_cast<int>(n % NBUF);
+      uint2* ent = reinterpret_cast<uint2*>(row_smem) + static_cast<size_t>(buf) * d;
+      const long long r0 = (blockIdx.x + n * gridDim.x) * R;
+      long long src[R];
+      if (sources(r0, src) && tid == 0) atomicCAS(status, 0, 1);
+      if (n >= NBUF) bar_sync(1 + NBUF + buf);  // the consumers are done with this table
+      // interleave: the entry of column c holds column c of the R rows
+      // (missing rows: 0); bf16: (r0 | r1 << 16, r2 | r3 << 16), fp32: (r0, r1)
+      for (int v0 = tid; v0 < nv; v0 += U * kPermRoleThreads) {
+        uint4 w[U][R];
 #pragma unroll
-      for (int q = 0; q < V / 4; ++q) {
-        const int4 c = c4[v * (V / 4) + q];
-        cols[4 * q + 0] = c.x;
-        cols[4 * q + 1] = c.y;
-        cols[4 * q + 2] = c.z;
-        cols[4 * q + 3] = c.w;
+        for (int k = 0; k < U; ++k) {
+          const int v = v0 + k * kPermRoleThreads;
+#pragma unroll
+          for (int q = 0; q < R; ++q) {
+            w[k][q] = make_uint4(0u, 0u, 0u, 0u);
+            if (v < nv && src[q] >= 0) w[k][q] = reinterpret_cast<const uint4*>(in + src[q] * d)[v];
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < U; ++k) {
+          const int v = v0 + k * kPermRoleThreads;
+          if (v >= nv) break;
+          uint32_t wd[R][4];
+#pragma unroll
+          for (int q = 0; q < R; ++q) {
+            wd[q][0] = w[k][q].x;
+            wd[q][1] = w[k][q].y;
+            wd[q][2] = w[k][q].z;
+            wd[q][3] = w[k][q].w;
+          }
+#pragma unroll
+          for (int e = 0; e < V; ++e) {
+            uint2 entry;
+            if constexpr (sizeof(T) == 2) {  // column 8v + e: halves e % 2 of word e / 2
+              const uint32_t sel = (e & 1) ? 0x7632u : 0x5410u;
+              entry.x = __byte_perm(wd[0][e >> 1], wd[1][e >> 1], sel);
+              entry.y = __byte_perm(wd[2][e >> 1], wd[3][e >> 1], sel);
+            } else {
+              entry.x = wd[0][e];
+              entry.y = wd[1][e];
+            }
+            ent[e * nv + v] = entry;
+          }
+        }
       }
-      uint32_t o[R][4];
-#pragma unroll
-      for (int q = 0; q < R; ++q)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) o[q][i] = 0u;
+      bar_arrive(1 + buf);  // table full
+    }
+  } else {
+    // table positions of the map entries of output vector v, two 16-bit
+    // positions per word (0xffff: the entry is out of range, the output 0);
+    // returns whether any entry was out of range
+    auto table_positions = [&](int v, uint32_t (&pos)[V / 2]) {
+      const int4* c4 = reinterpret_cast<const int4*>(col_map) + v * (V / 4);
       bool bad = false;
 #pragma unroll
-      for (int e = 0; e < V; ++e) {
-        const bool in_range = cols[e] >= 0 && cols[e] < d;
-        bad |= !in_range;
-        uint2 u = make_uint2(0u, 0u);
-        if (in_range) u = ent[cols[e]];
-        if constexpr (sizeof(T) == 2) {
-          const int sh = 16 * (e & 1);
-          o[0][e >> 1] |= (u.x & 0xffffu) << sh;
-          o[1][e >> 1] |= (u.x >> 16) << sh;
-          o[2][e >> 1] |= (u.y & 0xffffu) << sh;
-          o[3][e >> 1] |= (u.y >> 16) << sh;
-        } else {
-          o[0][e] = u.x;
-          o[1][e] = u.y;
-        }
-      }
-      if (bad) atomicCAS(status, 0, 1);
+      for (int i = 0; i < V / 2; ++i) pos[i] = 0u;
 #pragma unroll
-      for (int q = 0; q < R; ++q) {
-        if (r0 + q < rows) {
-          uint4 val = make_uint4(o[q][0], o[q][1], o[q][2], o[q][3]);
-          if (src[q] < 0) val = make_uint4(0u, 0u, 0u, 0u);
-          reinterpret_cast<uint4*>(out + (r0 + q) * d)[v] = val;
+      for (int qv = 0; qv < V / 4; ++qv) {
+        const int4 c = c4[qv];
+        const int cs[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int e = 4 * qv + t;
+          const bool ok = cs[t] >= 0 && cs[t] < d;
+          bad |= !ok;
+          const uint32_t at =
+              ok ? static_cast<uint32_t>((cs[t] & (V - 1)) * nv + cs[t] / V) : 0xffffu;
+          pos[e >> 1] |= at << (16 * (e & 1));
         }
       }
+      return bad;
+    };
+    uint32_t pos_r[KR][V / 2];
+    bool bad_cols = false;
+#pragma unroll
+    for (int k = 0; k < KR; ++k) {
+      const int v = tid + k * kPermRoleThreads;
+#pragma unroll
+      for (int i = 0; i < V / 2; ++i) pos_r[k][i] = 0xffffffffu;
+      if (v < nv) bad_cols |= table_positions(v, pos_r[k]);
     }
-    __syncthreads();  // the entries are free for the next group
+    if (bad_cols && count > 0) atomicCAS(status, 0, 1);
+    for (long long n = 0; n < count; ++n) {
+      const int buf = static_cast<int>(n % NBUF);
+      const uint2* ent = reinterpret_cast<const uint2*>(row_smem) + static_cast<size_t>(buf) * d;
+      const long long r0 = (blockIdx.x + n * gridDim.x) * R;
+      long long src[R];
+      sources(r0, src);
+      bar_sync(1 + buf);  // the producers have filled this table
+      // out[r0 + q][V v .. V v + V - 1] from the entries at the table
+      // positions of those columns' map entries
+      auto gather_store = [&](int v, const uint32_t (&pos)[V / 2]) {
+        uint2 u[V];
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+          const uint32_t at = (pos[e >> 1] >> (16 * (e & 1))) & 0xffffu;
+          u[e] = at != 0xffffu ? ent[at] : make_uint2(0u, 0u);
+        }
+        uint32_t o[R][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if constexpr (sizeof(T) == 2) {  // output word i: columns 2i, 2i + 1 of each row
+            o[0][i] = __byte_perm(u[2 * i].x, u[2 * i + 1].x, 0x5410u);
+            o[1][i] = __byte_perm(u[2 * i].x, u[2 * i + 1].x, 0x7632u);
+            o[2][i] = __byte_perm(u[2 * i].y, u[2 * i + 1].y, 0x5410u);
+            o[3][i] = __byte_perm(u[2 * i].y, u[2 * i + 1].y, 0x7632u);
+          } else {
+            o[0][i] = u[i].x;
+            o[1][i] = u[i].y;
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < R; ++q) {
+          if (r0 + q < rows) {
+            uint4 val = make_uint4(o[q][0], o[q][1], o[q][2], o[q][3]);
+            if (src[q] < 0) val = make_uint4(0u, 0u, 0u, 0u);
+            reinterpret_cast<uint4*>(out + (r0 + q) * d)[v] = val;
+          }
+        }
+      };
+#pragma unroll
+      for (int k = 0; k < KR; ++k) {
+        const int v = tid + k * kPermRoleThreads;
+        if (v < nv) gather_store(v, pos_r[k]);
+      }
+      for (int v = tid + KR * kPermRoleThreads; v < nv; v += kPermRoleThreads) {
+        uint32_t pos[V / 2];
+        if (table_positions(v, pos)) atomicCAS(status, 0, 1);
+        gather_store(v, pos);
+      }
+      if (n + NBUF < count) bar_arrive(1 + NBUF + buf);  // table free for group n + NBUF
+    }
   }
 }
 
@@ -725,30 +813,30 @@ cudaError_t launch_pack_tiles(const float* D, float sign, int n_a, int n_b, int 
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-cudaError_t launch_permute_rows(const void* in, long long in_rows, const int* row_map,
+namespace {
+template <typename T, int NBUF>
+cudaError_t permute_rows_launch(const void* in, long long in_rows, const int* row_map,
                                 const int* col_map, void* out, long long rows, int d,
-                                bool is_bf16, cudaStream_t s) {
-  if (rows <= 0 || d <= 0) return cudaSuccess;
-  const size_t smem = static_cast<size_t>(d) * 8;  // one 8-byte entry per column
-  if (smem > 200 * 1024) return cudaErrorInvalidValue;
-  const int R = is_bf16 ? 4 : 2;
+                                cudaStream_t s) {
+  constexpr int R = 8 / sizeof(T);
+  const size_t smem = static_cast<size_t>(NBUF) * d * 8;  // one 8-byte entry per column
   const long long groups = (rows + R - 1) / R;
-  // as many CTAs as fit at once (each holds R rows in flight)
-  const void* fn = is_bf16 ? reinterpret_cast<const void*>(permute_rows_kernel<__nv_bfloat16>)
-                           : reinterpret_cast<const void*>(permute_rows_kernel<float>);
-  static bool attr_set[2][64] = {};
+  const void* fn = reinterpret_cast<const void*>(permute_rows_kernel<T, NBUF>);
+  static bool attr_set[64] = {};
   static std::mutex mu;
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 0 && dev < 64) {
     std::lock_guard<std::mutex> lock(mu);
-    if (!attr_set[is_bf16][dev]) {
+    if (!attr_set[dev]) {
       cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared);
-      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-      attr_set[is_bf16][dev] = true;
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kPermSmemMax));
+      attr_set[dev] = true;
     }
   }
+  // as many CTAs as fit at once
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kPermThreads, smem) !=
           cudaSuccess ||
@@ -756,18 +844,27 @@ cudaError_t launch_permute_rows(const void* in, long long in_rows, const int* ro
     per_sm = 1;
   const long long cap = static_cast<long long>(sm_count()) * per_sm;
   const dim3 grid(static_cast<unsigned>(groups < cap ? groups : cap));
-  const int warps = kPermThreads / 32;
+  return launch_pdl(permute_rows_kernel<T, NBUF>, grid, dim3(kPermThreads), smem, s,
+                    static_cast<const T*>(in), in_rows, row_map, col_map, static_cast<T*>(out),
+                    rows, d, device_status_ptr());
+}
+}  // namespace
+
+cudaError_t launch_permute_rows(const void* in, long long in_rows, const int* row_map,
+                                const int* col_map, void* out, long long rows, int d,
+                                bool is_bf16, cudaStream_t s) {
+  if (rows <= 0 || d <= 0) return cudaSuccess;
+  const size_t table = static_cast<size_t>(d) * 8;
+  if (table > kPermSmemMax) return cudaErrorInvalidValue;
+  const bool two = 2 * table <= kPermSmemMax;  // two tables: loads overlap the gather
   cudaError_t e;
   prof_begin("permute", s);
-  if (is_bf16) {
-    e = launch_pdl(permute_rows_kernel<__nv_bfloat16>, grid, dim3(warps * 32), smem, s,
-                   static_cast<const __nv_bfloat16*>(in), in_rows, row_map, col_map,
-                   static_cast<__nv_bfloat16*>(out), rows, d, device_status_ptr());
-  } else {
-    e = launch_pdl(permute_rows_kernel<float>, grid, dim3(warps * 32), smem, s,
-                   static_cast<const float*>(in), in_rows, row_map, col_map,
-                   static_cast<float*>(out), rows, d, device_status_ptr());
-  }
+  if (is_bf16)
+    e = two ? permute_rows_launch<__nv_bfloat16, 2>(in, in_rows, row_map, col_map, out, rows, d, s)
+            : permute_rows_launch<__nv_bfloat16, 1>(in, in_rows, row_map, col_map, out, rows, d, s);
+  else
+    e = two ? permute_rows_launch<float, 2>(in, in_rows, row_map, col_map, out, rows, d, s)
+            : permute_rows_launch<float, 1>(in, in_rows, row_map, col_map, out, rows, d, s);
   prof_end("permute", s);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -175,14 +175,14 @@ def test_index_map_calls_reject_invalid_arguments(lib):
     L = _raw()
     B, F = poetx.BF16, poetx.F32
     # d beyond the shared-memory entry table, d * element size not a multiple of 16
-    assert L.poetx_permute_features(FAKE, FAKE, FAKE + 4096, 8, 25600 + 8, B, None) == 1
+    assert L.poetx_permute_features(FAKE, FAKE, FAKE + 4096, 8, 28672 + 8, B, None) == 1
     assert L.poetx_permute_features(FAKE, FAKE, FAKE + 4096, 8, 12, B, None) == 1
     # the column map is read as 16-byte vectors
     assert L.poetx_permute_features(FAKE, FAKE + 4, FAKE + 4096, 8, 64, B, None) == 1
     assert L.poetx_permute_features(FAKE, FAKE, FAKE, 8, 64, B, None) == 1  # in == out
     assert L.poetx_permute_features(None, None, None, 0, 64, F, None) == 0  # no rows
     assert L.poetx_fold_permutations(FAKE, FAKE, FAKE + 4, FAKE + 4096, 64, 64, B, None) == 1
-    assert L.poetx_fold_permutations(FAKE, FAKE, FAKE, FAKE + 4096, 25608, 64, B, None) == 1
+    assert L.poetx_fold_permutations(FAKE, FAKE, FAKE, FAKE + 4096, 28680, 64, B, None) == 1
 
 
 def test_process_wide_switches_return_the_previous_setting(lib):

@@ -55,6 +55,33 @@ def test_index_maps_are_exact(px, dtype):
     assert torch.equal(Wf, want)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("d,T", [(8, 5), (14336, 11), (14344, 6), (28672, 9)],
+                         ids=["tiny", "staged-max", "unstaged", "max"])
+def test_index_maps_at_both_table_forms(px, d, T, dtype):
+    """Rows whose table and staged copy fit shared memory (d <= 14336) are
+    copied in by bulk copies; wider rows are read straight into the table."""
+    if dtype == "f32" and d % 4:
+        pytest.skip("rows must be a multiple of 16 bytes")
+    rng = np.random.default_rng(d + T)
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    code = px.BF16 if dtype == "bf16" else px.F32
+    x = torch.randn((T, d), device="cuda").to(tdt)
+    perm = torch.from_numpy(rng.permutation(d).astype(np.int32)).cuda()
+    out = torch.empty_like(x)
+    px.poetx_permute_features(x, perm, out, T, d, code)
+    # the fold: rows through a map too, fewer rows than a CTA's group at the end
+    rows = 7
+    W = torch.randn((rows, d), device="cuda").to(tdt)
+    po = torch.from_numpy(rng.permutation(rows).astype(np.int32)).cuda()
+    Wf = torch.empty_like(W)
+    px.poetx_fold_permutations(W, po, perm, Wf, d, rows, code)
+    torch.cuda.synchronize()
+    assert px.poetx_device_status() == 0
+    assert torch.equal(out, x[:, perm.long()])
+    assert torch.equal(Wf, W[po.long()][:, perm.long()])
+
+
 def test_out_of_range_map_entries_are_not_followed(px):
     x = torch.randn((4, 256), device="cuda").to(torch.bfloat16)
     perm = np.arange(256, dtype=np.int32)
