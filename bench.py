@@ -78,6 +78,9 @@ def parse():
                     help="override the workload's token count (profiling a smaller case)")
     ap.add_argument("--recompute-v", action="store_true",
                     help="backward recomputes v = W0 P x instead of reading it (saves T x d_out)")
+    ap.add_argument("--sweep-case", default=None, metavar="B,K",
+                    help="transform sweep: run only the case (b, k), e.g. 32,3 (profiling one "
+                         "path of the sweep)")
     return ap.parse_args()
 
 
@@ -896,11 +899,17 @@ def run_sweep(args):
             tot += ev[0].elapsed_time(ev[1])
         return tot / reps
 
+    sweep_cases = SWEEP_CASES
+    if args.sweep_case:
+        b_k = tuple(int(t) for t in args.sweep_case.split(","))
+        if b_k not in SWEEP_CASES:
+            raise SystemExit(f"--sweep-case {args.sweep_case}: not a case of the sweep")
+        sweep_cases = [b_k]
     cases = []
     launches0 = poetx.poetx_launch_count()
     clocks = ClockSampler(local)
     clocks.start()
-    for b, k in SWEEP_CASES:
+    for b, k in sweep_cases:
         rng = np.random.default_rng(1000 * rank + 10 * b + k)
         theta = torch.from_numpy((rng.standard_normal((d // b, b * (b - 1) // 2)) *
                                   0.02).astype(np.float32)).cuda()
@@ -945,7 +954,7 @@ def run_sweep(args):
                 "ms_per_step": 1e3 * t_all, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": {"workload": SWEEP, "d": d, "tokens_per_gpu": T, "dtype": "bf16",
-                           "cases": [f"b{b}_k{k}" for b, k in SWEEP_CASES],
+                           "cases": [f"b{b}_k{k}" for b, k in sweep_cases],
                            "l2": "flushed (256 MiB write) before every timed call"},
                 "gpu_launches": launches, "launch": "eager",
                 "roofline": {"bound": "hbm", "kernel": "block transform fwd + bwd, all cases",

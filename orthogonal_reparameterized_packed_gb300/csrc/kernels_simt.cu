@@ -133,20 +133,27 @@ __global__ void identity_plus_kernel(const float* __restrict__ q, int b, int tot
   }
 }
 
+// One 16-byte vector (8 columns) per thread: b is a multiple of 8, so the
+// vector lies in one block column and is either a copy of 8 block entries
+// (16-byte aligned: b * b and b are multiples of 8) or zero.  total8 counts
+// vectors.
 __global__ void expand_superblocks_kernel(const __nv_bfloat16* __restrict__ blocks, int n, int b,
-                                          int S, int total, __nv_bfloat16* __restrict__ out) {
+                                          int S, int total8, __nv_bfloat16* __restrict__ out) {
   pdl_wait();
   pdl_trigger();
   const int per = S / b;
-  for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+  const int vrow = S / 8;  // vectors per superblock row
+  for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < total8;
        idx += gridDim.x * blockDim.x) {
-    const int c = idx % S;
-    const int r = (idx / S) % S;
-    const int sb = idx / (S * S);
-    __nv_bfloat16 v = __float2bfloat16_rn(0.f);
+    const int c = 8 * (idx % vrow);
+    const int r = (idx / vrow) % S;
+    const int sb = idx / (vrow * S);
     const int gblk = sb * per + r / b;
-    if (r / b == c / b && gblk < n) v = blocks[(gblk * b + (r % b)) * b + (c % b)];
-    out[idx] = v;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (r / b == c / b && gblk < n)
+      v = *reinterpret_cast<const uint4*>(blocks + (static_cast<long long>(gblk) * b + (r % b)) * b +
+                                          (c % b));
+    reinterpret_cast<uint4*>(out)[idx] = v;
   }
 }
 
@@ -773,8 +780,11 @@ cudaError_t launch_expand_superblocks(const __nv_bfloat16* blocks, int n, int b,
                                       __nv_bfloat16* out, cudaStream_t s) {
   const int per = S / b;
   const int nsb = (n + per - 1) / per;
-  const int total = nsb * S * S;
-  POETX_EW_LAUNCH("expand_superblocks", total, expand_superblocks_kernel, blocks, n, b, S, total,
+  const int total8 = nsb * S * S / 8;  // 16-byte vectors
+  if (b % 8 != 0 || S % b != 0 || reinterpret_cast<uintptr_t>(blocks) % 16 != 0 ||
+      reinterpret_cast<uintptr_t>(out) % 16 != 0)
+    return cudaErrorInvalidValue;
+  POETX_EW_LAUNCH("expand_superblocks", total8, expand_superblocks_kernel, blocks, n, b, S, total8,
                   out);
 }
 
