@@ -81,16 +81,17 @@ size_t poetx_packed_size(int d, int b);
  *   = I + 2Q + ... + 2Q^k + Q^{k+1}, the Neumann-truncated Cayley transform
  * (technical summary, section 2, CNP bullet: the powers Q^2..Q^4 of k = 3
  * are built in one fused step).  Arithmetic in fp32 (F32) or bf16 tensor
- * cores with fp32 accumulation (BF16: b >= 128, and k = 3 with b = 32..256);
+ * cores with fp32 accumulation (BF16: b >= 128, and 1 <= k <= 16 with
+ * b = 32..256);
  * rounded once at the store.
  *   theta  [d/b][b(b-1)/2] float32 (read only)
  *   blocks [d/b][b][b] dtype (written)
  * Blocks are independent, so both factors of a layer are one call when
  * theta_P and theta_R lie back to back (and the blocks likewise):
  * d = d_in + d_out builds P's blocks then R's, bitwise as two calls would.
- * BF16 with k = 3 and b <= 256 runs on CTA pairs with every operand in
- * shared memory and needs no workspace (its size is 0 and the workspace
- * may be NULL).
+ * BF16 with 1 <= k <= 16 and b <= 256 runs on CTA pairs with every
+ * operand in shared memory and needs no workspace (its size is 0 and the
+ * workspace may be NULL).
  * ------------------------------------------------------------------------ */
 size_t poetx_build_workspace_size(int d, int b, int k, poetx_dtype dtype);
 poetx_status poetx_build_blocks(const float* theta, int d, int b, int k, poetx_dtype dtype,

@@ -488,8 +488,8 @@ struct BuildBufs {
 // Buffers of one block build: the one-launch chain needs bf16 Q (hi and lo
 // parts), 2I and two bf16 E stacks; the per-product path fp32 Q plus bf16 (tensor
 // cores) or fp32 (FFMA) E stacks.
-// The k = 3 build of bf16 blocks with b <= 256 runs on CTA pairs with its
-// operands in shared memory (cnp_pair.cu): no workspace.
+// The build of bf16 blocks with b <= 256 and 1 <= k <= 16 runs on CTA pairs
+// with its operands in shared memory (cnp_pair.cu): no workspace.
 bool use_pair_build(bool is_bf16, int n, int b, int k) {
   return is_bf16 && cnp_pair_fits(b, k) && (static_cast<long long>(n) * b) % 256 == 0;
 }
@@ -523,7 +523,7 @@ cudaError_t run_build(const float* theta, int n, int b, int k, bool is_bf16, voi
                       const BuildBufs& w, cudaStream_t s) {
   const bool tc = tc_small(is_bf16, b);
   if (use_pair_build(is_bf16, n, b, k))
-    return cnp_build_pair(theta, n, b, static_cast<bf16*>(blocks), s);
+    return cnp_build_pair(theta, n, b, k, static_cast<bf16*>(blocks), s);
   if (use_chain(is_bf16, n, b, k)) {  // the whole recursion in one cooperative launch
     ChainBuildArgs a;
     a.n = n;
@@ -579,8 +579,8 @@ struct CnpBufs {
   unsigned int* counter = nullptr;
   bf16* two_i = nullptr;  // chain: constant 2I
   bf16* x16 = nullptr;    // chain, k = 3: 2Q
-  // the adjoint on CTA pairs (k = 3, b <= 256): H (bf16) per 256 x 256
-  // superblock
+  // the adjoint on CTA pairs (1 <= k <= 16, b <= 256): H (bf16) per
+  // 256 x 256 superblock
   bool pair = false;
   bf16* hg = nullptr;
 };
@@ -630,6 +630,7 @@ cudaError_t chain_adjoint_from_parts(const float* theta_a, int n_a, const float*
     x.n_a = n_a;
     x.n_b = n_b;
     x.b = b;
+    x.k = k;
     x.theta_a = theta_a;
     x.theta_b = theta_b;
     x.part_a = part_a;

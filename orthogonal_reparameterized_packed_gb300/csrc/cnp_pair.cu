@@ -1,6 +1,8 @@
-// The Cayley-Neumann block build for k = 3 on CTA pairs, every operand in
-// shared memory: the pages' fused CNP kernel that loads Q (and Q^2) into
-// shared memory once, laid out for two SMs.
+// The Cayley-Neumann block build and its adjoint on CTA pairs, every operand
+// in shared memory: the pages' fused CNP kernel that loads Q (and Q^2) into
+// shared memory once, laid out for two SMs.  k = 3 has kernels of its own
+// (two and three dependent phases); any other k >= 1 runs a Horner
+// recursion of k phases (further below).
 //
 // One cluster of two CTAs per 256 x 256 superblock (one block of b = 256, or
 // 256 / b blocks of b = 32, 64, 128 on its diagonal: products of block-
@@ -431,6 +433,109 @@ __device__ __forceinline__ uint32_t mn_off(int k, int n) {
                                ((((n & 63) >> 3) ^ (k & 7)) << 4) + ((n & 7) << 1));
 }
 
+// All threads of a CTA: H's rows of this CTA (superblock sb, side-local
+// superblock lsb), summed over the K splits of the partials, to the bf16
+// scratch hg [superblocks][256][256] (zero outside the diagonal blocks).  A
+// warp takes one row (1 KiB per split); a thread keeps four splits' loads in
+// flight.
+__device__ void sum_partials_to_h(const float* part, int splits, int nsb_side, int lsb, int sb,
+                                  int rank, int lb, __nv_bfloat16* hg) {
+  const long long split_stride = static_cast<long long>(nsb_side) * 65536;
+  const float* pt = part + static_cast<long long>(lsb) * 65536;
+  const long long grow0 = static_cast<long long>(sb) * 256;
+  for (int t = threadIdx.x; t < 128 * 32; t += blockDim.x) {
+    const int pp = 128 * rank + (t >> 5);
+    const int c8 = 8 * (t & 31);
+    float h[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) h[e] = 0.f;
+    if ((c8 >> lb) == (pp >> lb)) {
+      const float* ps = pt + pp * 256 + c8;
+      int sp = 0;
+      for (; sp + 4 <= splits; sp += 4) {
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          v[2 * u] = *reinterpret_cast<const float4*>(ps + (sp + u) * split_stride);
+          v[2 * u + 1] = *reinterpret_cast<const float4*>(ps + (sp + u) * split_stride + 4);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          h[0] += v[2 * u].x; h[1] += v[2 * u].y; h[2] += v[2 * u].z; h[3] += v[2 * u].w;
+          h[4] += v[2 * u + 1].x; h[5] += v[2 * u + 1].y; h[6] += v[2 * u + 1].z;
+          h[7] += v[2 * u + 1].w;
+        }
+      }
+      for (; sp < splits; ++sp) {
+        const float4 v0 = *reinterpret_cast<const float4*>(ps + sp * split_stride);
+        const float4 v1 = *reinterpret_cast<const float4*>(ps + sp * split_stride + 4);
+        h[0] += v0.x; h[1] += v0.y; h[2] += v0.z; h[3] += v0.w;
+        h[4] += v1.x; h[5] += v1.y; h[6] += v1.z; h[7] += v1.w;
+      }
+    }
+    uint32_t hw[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __nv_bfloat162 hh = __floats2bfloat162_rn(h[2 * e], h[2 * e + 1]);
+      hw[e] = *reinterpret_cast<const uint32_t*>(&hh);
+    }
+    *reinterpret_cast<uint4*>(hg + (grow0 + pp) * 256 + c8) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+  }
+}
+
+// One thread, 32 consecutive columns c0.. of its row of G_Q (fp32 bits):
+// into its own staged row, or (rank 1 of a 256-block, columns < 128) into
+// rank 0's transposed quadrant at [c][row] (cross: that quadrant's shared::
+// cluster address plus 4 * row).
+__device__ __forceinline__ void stage_gq32(const uint32_t (&r)[32], int c0, bool to_peer,
+                                           float* own_row, uint32_t cross) {
+  if (to_peer) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) st_cluster_b32(cross + 4u * static_cast<uint32_t>((c0 + e) * 128), r[e]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) own_row[c0 + e] = __uint_as_float(r[e]);
+  }
+}
+
+// All threads of a CTA, after both CTAs staged G_Q: dtheta = G_Q - G_Q^T
+// over the upper triangles of the blocks whose rows this CTA holds, from
+// shared memory only.  b <= 128: whole blocks; b = 256: rank 0 takes the
+// triangle's rows 0..127 (the quadrant of rows 128.. it reads transposed
+// from gq_cross), rank 1 rows 128..254.
+__device__ void pack_dtheta(int b, int lb, int P, int rank, int lsb, int nb, float* dtheta,
+                            const float* gq_own, const float* gq_cross) {
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t own_s = smem_u32(gq_own), cross_s = smem_u32(gq_cross);
+  const int bpc = b <= 128 ? 128 / b : 1;               // blocks per CTA
+  const int rows_per = b <= 128 ? b - 1 : 128 - rank;  // triangle rows per block here
+  for (int r = warp; r < bpc * rows_per; r += blockDim.x / 32) {
+    const int blo = r / rows_per, rr = r - blo * rows_per;
+    const int il = b <= 128 ? blo * b + rr : rr;  // local row
+    const int i = 128 * rank + il;                // superblock row
+    const int ib = i & (b - 1);                   // row in its block
+    const int cb0 = i - ib;                       // the block's first column
+    const int bl = cb0 >> lb;
+    float* dst = dtheta + (static_cast<long long>(lsb) * nb + bl) * P + tri_start_of(ib, b) - ib - 1;
+    const uint32_t rowi = own_s + 4u * static_cast<uint32_t>(il * kGqPitch + cb0);
+    for (int j0 = ib + 1 + lane; j0 < b; j0 += 128) {
+      float d4[4];  // four columns' loads before the stores
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int jb = min(j0 + 32 * u, b - 1);
+        const int j = cb0 + jb;  // superblock column = row of the transposed entry
+        const uint32_t at_ji = j - 128 * rank < 128
+                                   ? own_s + 4u * static_cast<uint32_t>((j - 128 * rank) * kGqPitch + i)
+                                   : cross_s + 4u * static_cast<uint32_t>(i * 128 + (j - 128));
+        d4[u] = ld_shared_f32(rowi + 4u * static_cast<uint32_t>(jb)) - ld_shared_f32(at_ji);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (j0 + 32 * u < b) dst[j0 + 32 * u] = d4[u];
+    }
+  }
+}
+
 struct CnpAdjArgs {
   const float* theta_a;
   const float* theta_b;
@@ -593,53 +698,8 @@ __global__ void __launch_bounds__(kCnpThreads, 1)
   // ------------------------------------------------------ the token sums H
   pdl_wait();  // the partials are complete from here on
   pdl_trigger();
-  {
-    // H's rows of this CTA, summed over the splits, to the bf16 scratch
-    // (zero outside the diagonal blocks).  A warp takes one row (1 KiB per
-    // split); a thread keeps four splits' loads in flight.
-    const long long split_stride = static_cast<long long>(nsb_side) * 65536;
-    const float* pt = part + static_cast<long long>(lsb) * 65536;
-    const long long grow0 = static_cast<long long>(sb) * 256;
-    for (int t = threadIdx.x; t < 128 * 32; t += kCnpThreads) {
-      const int pp = 128 * rank + (t >> 5);
-      const int c8 = 8 * (t & 31);
-      float h[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) h[e] = 0.f;
-      if ((c8 >> lb) == (pp >> lb)) {
-        const float* ps = pt + pp * 256 + c8;
-        int sp = 0;
-        for (; sp + 4 <= splits; sp += 4) {
-          float4 v[8];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            v[2 * u] = *reinterpret_cast<const float4*>(ps + (sp + u) * split_stride);
-            v[2 * u + 1] = *reinterpret_cast<const float4*>(ps + (sp + u) * split_stride + 4);
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            h[0] += v[2 * u].x; h[1] += v[2 * u].y; h[2] += v[2 * u].z; h[3] += v[2 * u].w;
-            h[4] += v[2 * u + 1].x; h[5] += v[2 * u + 1].y; h[6] += v[2 * u + 1].z;
-            h[7] += v[2 * u + 1].w;
-          }
-        }
-        for (; sp < splits; ++sp) {
-          const float4 v0 = *reinterpret_cast<const float4*>(ps + sp * split_stride);
-          const float4 v1 = *reinterpret_cast<const float4*>(ps + sp * split_stride + 4);
-          h[0] += v0.x; h[1] += v0.y; h[2] += v0.z; h[3] += v0.w;
-          h[4] += v1.x; h[5] += v1.y; h[6] += v1.z; h[7] += v1.w;
-        }
-      }
-      uint32_t hw[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const __nv_bfloat162 hh = __floats2bfloat162_rn(h[2 * e], h[2 * e + 1]);
-        hw[e] = *reinterpret_cast<const uint32_t*>(&hh);
-      }
-      *reinterpret_cast<uint4*>(a.hg + (grow0 + pp) * 256 + c8) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-    }
-    fence_proxy_async_global();  // these stores -> the TMA loads of the chunks
-  }
+  sum_partials_to_h(part, splits, nsb_side, lsb, sb, rank, lb, a.hg);
+  fence_proxy_async_global();  // these stores -> the TMA loads of the chunks
   __syncthreads();
   cluster_sync();  // H scratch written by both CTAs
 
@@ -810,14 +870,7 @@ __global__ void __launch_bounds__(kCnpThreads, 1)
           uint32_t r[32];
           tmem_load_32cols(t_row + 256 + c0, r);
           tmem_load_wait();
-          if (to_peer) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              st_cluster_b32(cross + 4u * static_cast<uint32_t>((c0 + e) * 128), r[e]);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) own[c0 + e] = __uint_as_float(r[e]);
-          }
+          stage_gq32(r, c0, to_peer, own, cross);
         }
       } else {
         record_timeout(a.status, abort_flag);
@@ -831,41 +884,418 @@ __global__ void __launch_bounds__(kCnpThreads, 1)
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // G_Q staged in both CTAs
-  {
-    // dtheta = G_Q - G_Q^T over the upper triangles of the blocks whose rows
-    // this CTA holds, from shared memory only.  b <= 128: whole blocks;
-    // b = 256: rank 0 takes the triangle's rows 0..127 (the quadrant of rows
-    // 128.. it reads transposed from gq_cross), rank 1 rows 128..254.
-    const int P = qs.P;
-    const uint32_t own_s = smem_u32(gq_own), cross_s = smem_u32(gq_cross);
-    const int bpc = b <= 128 ? 128 / b : 1;                  // blocks per CTA
-    const int rows_per = b <= 128 ? b - 1 : 128 - rank;     // triangle rows per block here
-    for (int r = warp; r < bpc * rows_per; r += kCnpThreads / 32) {
-      const int blo = r / rows_per, rr = r - blo * rows_per;
-      const int il = b <= 128 ? blo * b + rr : rr;  // local row
-      const int i = 128 * rank + il;                // superblock row
-      const int ib = i & (b - 1);                   // row in its block
-      const int cb0 = i - ib;                       // the block's first column
-      const int bl = cb0 >> lb;
-      float* dst = dtheta + (static_cast<long long>(lsb) * a.nb + bl) * P + tri_start_of(ib, b) - ib - 1;
-      const uint32_t rowi = own_s + 4u * static_cast<uint32_t>(il * kGqPitch + cb0);
-      for (int j0 = ib + 1 + lane; j0 < b; j0 += 128) {
-        float d4[4];  // four columns' loads before the stores
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int jb = min(j0 + 32 * u, b - 1);
-          const int j = cb0 + jb;  // superblock column = row of the transposed entry
-          const uint32_t at_ji = j - 128 * rank < 128
-                                     ? own_s + 4u * static_cast<uint32_t>((j - 128 * rank) * kGqPitch + i)
-                                     : cross_s + 4u * static_cast<uint32_t>(i * 128 + (j - 128));
-          d4[u] = ld_shared_f32(rowi + 4u * static_cast<uint32_t>(jb)) - ld_shared_f32(at_ji);
+  pack_dtheta(b, lb, qs.P, rank, lsb, a.nb, dtheta, gq_own, gq_cross);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no CTA leaves while its peer may still signal or read it
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, 512);
+  }
+}
+
+// ------------------------------------------------- the build for any k >= 1
+// E_{k+1} = Q,  E_i = 2Q + E_{i+1} Q  (i = k .. 1),  R = I + E_1, i.e.
+// R = I + 2Q + ... + 2Q^k + Q^{k+1}.  With MMA(A, B) = A B^T and Q^T = -Q,
+// E_{i+1} Q = -MMA(E_{i+1}, Q): both operands are a CTA's own rows, so the
+// k phases exchange nothing:
+//   phase i   acc = MMA(E, Q_hi)            (E = Q_hi in the first phase)
+//   epilogue  E = 2Q - acc -> bf16 tile      (2Q from the hi and lo parts)
+//   last      block rows = I + 2Q - acc -> bf16
+// Same shared-memory layout as the k = 3 build (Q hi, Q lo, staging then E).
+__global__ void __launch_bounds__(kCnpThreads, 1) cnp_build_pair_k_kernel(const CnpBuildArgs a,
+                                                                          int k) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* tA = base;                 // Q hi
+  uint8_t* tC = base + kOpBytes;      // Q lo
+  uint8_t* tB = base + 2 * kOpBytes;  // staged theta, then E
+  uint64_t* ready1 = reinterpret_cast<uint64_t*>(base + 2 * kOpBytes + kStageBytes);
+  uint64_t* pdone = ready1 + 1;   // each CTA: a phase's MMAs are done (parity: phase % 2)
+  uint64_t* readyE = pdone + 1;   // leader: E written (eight warps of each CTA)
+  uint64_t* drain = readyE + 1;
+  uint64_t* staged = drain + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(staged + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const bool leader = rank == 0;
+  const int sb = static_cast<int>(cluster_id_x());
+  const int b = a.b;
+
+  if (threadIdx.x == 0) {
+    mbar_init(ready1, 2);
+    mbar_init(pdone, 1);
+    mbar_init(readyE, 16);
+    mbar_init(drain, 1);
+    mbar_init(staged, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, 256);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();
+  pdl_trigger();
+
+  const QStage qs = qstage_geom(b, a.nb, rank);
+  if (threadIdx.x == 0)
+    qstage_issue(qs, a.theta + static_cast<long long>(sb) * a.nb * qs.P, tB, staged);
+  q_gather(qs, rank, tB, staged, tA, tC, abort_flag, a.status);
+  fence_proxy_async_all();
+  cluster_sync();  // both CTAs' Q tiles are complete; the staging is free
+  if (threadIdx.x == 0) mbar_arrive_remote(map_peer(smem_u32(ready1), 0));
+
+  constexpr uint32_t IDESC = instr_desc_bf16(2 * BM, 256, false, false);
+  if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ----------------------------------------------------------- MMA issuer
+      const uint32_t pd_own = smem_u32(pdone), pd_peer = map_peer(pd_own, 1);
+      bool ok = mbar_wait_cluster(ready1, 0, abort_flag), any = false;
+      for (int ph = 0; ph < k && ok; ++ph) {
+        if (ph > 0 && !mbar_wait_cluster(readyE, static_cast<uint32_t>(ph - 1) & 1u, abort_flag)) {
+          ok = false;
+          break;
         }
+        tc_fence_after();
+        mma_tiles(tmem_base, ph == 0 ? tA : tB, tA, IDESC);  // acc = E Q^T
+        any = true;
+        umma_commit_pair(pd_own);
+        umma_commit_pair(pd_peer);
+      }
+      if (!ok) record_timeout(a.status, abort_flag);
+      if (!ok && any) {  // the MMAs in flight finish before TMEM is released
+        umma_commit_pair(smem_u32(drain));
+        const unsigned long long t0 = global_timer_ns();
+        while (!mbar_try_wait(drain, 0) && global_timer_ns() - t0 < 10000000ull) {
+        }
+      }
+    }
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ epilogues
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int row = quarter * 32 + lane;
+    const int i = 128 * rank + row;
+    const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+    for (int ph = 0; ph < k; ++ph) {
+      const bool ok = mbar_wait_cluster(pdone, static_cast<uint32_t>(ph) & 1u, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) {
+        record_timeout(a.status, abort_flag);
+        break;
+      }
+      tc_fence_after();
+      if (ph + 1 < k) {
+        // E = 2Q - acc over this half's 128 columns, bf16 into the E tile
+#pragma unroll 1
+        for (int c0 = 128 * half; c0 < 128 * half + 128; c0 += 32) {
+          uint32_t r[32];
+          tmem_load_32cols(t_row + c0, r);
+          tmem_load_wait();
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (j0 + 32 * u < b) dst[j0 + 32 * u] = d4[u];
+          for (int g = 0; g < 4; ++g) {
+            const uint32_t off = op_off(row, c0 + 8 * g);
+            const uint4 hv = *reinterpret_cast<const uint4*>(tA + off);
+            const uint4 lv = *reinterpret_cast<const uint4*>(tC + off);
+            const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
+            const uint32_t lw[4] = {lv.x, lv.y, lv.z, lv.w};
+            uint32_t e_out[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float qa = bf_lo(hw[e]) + bf_lo(lw[e]), qb = bf_hi(hw[e]) + bf_hi(lw[e]);
+              const __nv_bfloat162 v = __floats2bfloat162_rn(
+                  2.f * qa - __uint_as_float(r[8 * g + 2 * e]),
+                  2.f * qb - __uint_as_float(r[8 * g + 2 * e + 1]));
+              e_out[e] = *reinterpret_cast<const uint32_t*>(&v);
+            }
+            st_shared_v4(tB + off, e_out[0], e_out[1], e_out[2], e_out[3]);
+          }
+        }
+        fence_proxy_async_shared();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(map_peer(smem_u32(readyE), 0));
+      } else {
+        // the block rows: I + 2Q - acc on the diagonal b-block of row i
+        const int bl = i / b, ib = i - bl * b;
+        uint4* out = reinterpret_cast<uint4*>(
+            a.blocks + ((static_cast<long long>(sb) * a.nb + bl) * b + ib) * b);
+        const int cw = b >= 64 ? b / 2 : (half == 0 ? b : 0);
+        const int cb = bl * b + (b >= 64 ? half * (b / 2) : 0);
+#pragma unroll 1
+        for (int c0 = cb; c0 < cb + cw; c0 += 32) {
+          uint32_t r[32];
+          tmem_load_32cols(t_row + c0, r);
+          tmem_load_wait();
+          uint32_t w[16];
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const uint32_t off = op_off(row, c0 + 8 * g);
+            const uint4 hv = *reinterpret_cast<const uint4*>(tA + off);
+            const uint4 lv = *reinterpret_cast<const uint4*>(tC + off);
+            const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w};
+            const uint32_t lw[4] = {lv.x, lv.y, lv.z, lv.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int ca = c0 + 8 * g + 2 * e;
+              const float qa = bf_lo(hw[e]) + bf_lo(lw[e]), qb = bf_hi(hw[e]) + bf_hi(lw[e]);
+              const __nv_bfloat162 v = __floats2bfloat162_rn(
+                  (i == ca ? 1.f : 0.f) + 2.f * qa - __uint_as_float(r[8 * g + 2 * e]),
+                  (i == ca + 1 ? 1.f : 0.f) + 2.f * qb - __uint_as_float(r[8 * g + 2 * e + 1]));
+              w[4 * g + e] = *reinterpret_cast<const uint32_t*>(&v);
+            }
+          }
+          uint4* dst = out + (c0 - bl * b) / 8;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) dst[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+        }
       }
     }
   }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no CTA leaves while its peer may still signal or read it
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, 256);
+  }
+}
+
+// ----------------------------------------------- the adjoint for any k >= 1
+// With H = G^T (the token sums) and D = (dL/dQ)^T, the reverse sweep of the
+// build (Gbar_1 = G, dQ += 2 Gbar_i + E_{i+1}^T Gbar_i, Gbar_{i+1} = Gbar_i Q^T,
+// dQ += Gbar_{k+1}) regrouped by Horner's rule on both sides of H:
+//   P = H, Y = H;  for m = 0 .. k-1:  P <- 2H + P Q,  Y <- P + Q Y;   D = Y
+// (P_m = H a_m(Q) with a_m(x) = 2 + 2x + .. + 2x^m + x^{m+1} = 2I + E_{k-m}
+// transposed; Y accumulates Q^p H a_{k-1-p}(Q) + Q^k H).  Both recursions
+// run forward, so no E_i is stored.  dtheta(i, j) = dQ[i][j] - dQ[j][i] =
+// D[j][i] - D[i][j]: -D is staged and packed like G_Q of the k = 3 adjoint.
+//   prologue  Q hi from theta (before the wait for the partials); H's rows
+//             summed to bf16 scratch; P's tile (H's own rows, K-major) and
+//             Y's tile (H read MN-major: rows k, this CTA's columns) by TMA
+//   phase m   accP = MMA(P, Q_hi) = -P Q,  accY = MMA_mn(Q_hi, Y) = Q Y
+//   epilogue  P = 2H - accP -> bf16 (own rows), Y = P + accY -> bf16 MN tile
+//             (the half of each row in the peer's columns through
+//             distributed shared memory); in the last phase -Y -> fp32 rows
+//             in shared memory, then the pack
+// Shared memory as the k = 3 adjoint (Q, then P and Y in the Q2 and X
+// places; the staged G_Q rows over all of it).
+__global__ void __launch_bounds__(kCnpThreads, 1)
+    cnp_adjoint_pair_k_kernel(const __grid_constant__ CUtensorMap tmH,
+                              const __grid_constant__ CUtensorMap tmHmn, const CnpAdjArgs a, int k) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* tQ = base;                 // Q hi
+  uint8_t* tP = base + kOpBytes;      // theta staging; then P (own rows, K-major)
+  uint8_t* tY = base + 2 * kOpBytes;  // (staging); then Y (MN-major, this CTA's columns)
+  float* gq_own = reinterpret_cast<float*>(base);
+  float* gq_cross = reinterpret_cast<float*>(base + kGqOwnBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(base + 3 * kOpBytes + 2 * kAdjSlot);
+  uint64_t* readyH = bars + 0;   // leader: P and Y tiles of H loaded (one arrival per CTA)
+  uint64_t* pdone = bars + 1;    // each CTA; parity: phase % 2
+  uint64_t* readyE = bars + 2;   // leader: P and Y written (eight warps per CTA)
+  uint64_t* hload = bars + 3;    // each CTA: its TMA loads of H landed
+  uint64_t* drain = bars + 4;
+  uint64_t* staged = bars + 5;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 6);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const bool leader = rank == 0;
+  const int sb = static_cast<int>(cluster_id_x());
+  const bool side_b = sb >= a.nsb_a;
+  const int lsb = side_b ? sb - a.nsb_a : sb;
+  const int nsb_side = side_b ? a.nsb_b : a.nsb_a;
+  const float* theta = side_b ? a.theta_b : a.theta_a;
+  const float* part = side_b ? a.part_b : a.part_a;
+  const int splits = side_b ? a.splits_b : a.splits_a;
+  float* dtheta = side_b ? a.dtheta_b : a.dtheta_a;
+  const int b = a.b;
+  const int lb = __ffs(b) - 1;
+
+  if (threadIdx.x == 0) {
+    mbar_init(readyH, 2);
+    mbar_init(pdone, 1);
+    mbar_init(readyE, 16);
+    mbar_init(hload, 1);
+    mbar_init(drain, 1);
+    mbar_init(staged, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmH);
+    tma_prefetch_desc(&tmHmn);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, 512);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  // Q from theta alone: may overlap the end of the previous kernel (theta is
+  // no recent kernel's output: every kernel here waits before it triggers)
+  const QStage qs = qstage_geom(b, a.nb, rank);
+  if (threadIdx.x == 0)
+    qstage_issue(qs, theta + static_cast<long long>(lsb) * a.nb * qs.P, tP, staged);
+  q_gather(qs, rank, tP, staged, tQ, nullptr, abort_flag, a.status);
+
+  pdl_wait();  // the partials are complete from here on
+  pdl_trigger();
+  sum_partials_to_h(part, splits, nsb_side, lsb, sb, rank, lb, a.hg);
+  fence_proxy_async_global();  // these stores -> the TMA loads of H
+  fence_proxy_async_all();     // the Q tile and the staging reads -> the async proxy
+  __syncthreads();
+  cluster_sync();  // H and both CTAs' Q tiles complete
+  if (threadIdx.x == 0) {
+    // P = H's own rows (four 128 x 64 K-major chunks), Y = H MN-major: rows
+    // k of the superblock, this CTA's 128 columns (two 64-column boxes per
+    // 64-row K step)
+    mbar_arrive_expect_tx(hload, 2 * kOpBytes);
+    const int hrow = sb * 256 + 128 * rank;
+    for (int kc = 0; kc < 4; ++kc) {
+      tma_load_2d(tP + kc * (BM * 128), &tmH, hload, kc * BK, hrow);
+      tma_load_2d(tY + kc * 16384, &tmHmn, hload, 128 * rank, sb * 256 + kc * BK);
+      tma_load_2d(tY + kc * 16384 + 8192, &tmHmn, hload, 128 * rank + 64, sb * 256 + kc * BK);
+    }
+    if (mbar_wait(hload, 0, abort_flag))
+      mbar_arrive_remote(map_peer(smem_u32(readyH), 0));
+    else
+      record_timeout(a.status, abort_flag);
+  }
+
+  constexpr uint32_t IDESC = instr_desc_bf16(2 * BM, 256, false, false);
+  constexpr uint32_t IDESC_MN = instr_desc_bf16(2 * BM, 256, false, true);
+  if (warp == 1) {
+    if (lane == 0 && leader) {
+      // ----------------------------------------------------------- MMA issuer
+      const uint32_t pd_own = smem_u32(pdone), pd_peer = map_peer(pd_own, 1);
+      bool ok = mbar_wait_cluster(readyH, 0, abort_flag), any = false;
+      const uint32_t q0 = smem_u32(tQ), y0 = smem_u32(tY);
+      for (int m = 0; m < k && ok; ++m) {
+        if (m > 0 && !mbar_wait_cluster(readyE, static_cast<uint32_t>(m - 1) & 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        mma_tiles(tmem_base, tP, tQ, IDESC);  // accP = P Q^T = -P Q
+#pragma unroll
+        for (int kc = 0; kc < 4; ++kc)
+#pragma unroll
+          for (int j = 0; j < BK / 16; ++j)  // accY = Q Y
+            umma_bf16_pair(tmem_base + 256,
+                           smem_desc_sw128(q0 + kc * (BM * 128) + j * 32, 16, 1024),
+                           smem_desc_sw128(y0 + kc * 16384 + j * 2048, 8192, 1024), IDESC_MN,
+                           (kc > 0 || j > 0) ? 1u : 0u);
+        any = true;
+        umma_commit_pair(pd_own);
+        umma_commit_pair(pd_peer);
+      }
+      if (!ok) record_timeout(a.status, abort_flag);
+      if (!ok && any) {
+        umma_commit_pair(smem_u32(drain));
+        const unsigned long long t0 = global_timer_ns();
+        while (!mbar_try_wait(drain, 0) && global_timer_ns() - t0 < 10000000ull) {
+        }
+      }
+    }
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ epilogues
+    const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int row = quarter * 32 + lane;
+    const int p = 128 * rank + row;
+    const uint32_t t_row = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t mnY[2] = {map_peer(smem_u32(tY), 0), map_peer(smem_u32(tY), 1)};
+    const uint4* hrow = reinterpret_cast<const uint4*>(a.hg + (static_cast<long long>(sb) * 256 + p) * 256);
+    for (int m = 0; m < k; ++m) {
+      const bool last = m + 1 == k;
+      const bool ok = mbar_wait_cluster(pdone, static_cast<uint32_t>(m) & 1u, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) {
+        record_timeout(a.status, abort_flag);
+        break;
+      }
+      tc_fence_after();
+      const bool to_peer = last && b == 256 && rank == 1 && half == 0;
+      const uint32_t cross = map_peer(smem_u32(gq_cross), 0) + 4u * static_cast<uint32_t>(row);
+      float* own = gq_own + row * kGqPitch;
+#pragma unroll 1
+      for (int c0 = 128 * half; c0 < 128 * half + 128; c0 += 32) {
+        uint4 hv[4];  // H[p][c0 .. c0 + 31] (bf16)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) hv[q] = hrow[c0 / 8 + q];
+        uint32_t rp[32], ry[32];
+        tmem_load_32cols(t_row + c0, rp);
+        tmem_load_32cols(t_row + 256 + c0, ry);
+        tmem_load_wait();
+        const uint32_t hw[16] = {hv[0].x, hv[0].y, hv[0].z, hv[0].w, hv[1].x, hv[1].y,
+                                 hv[1].z, hv[1].w, hv[2].x, hv[2].y, hv[2].z, hv[2].w,
+                                 hv[3].x, hv[3].y, hv[3].z, hv[3].w};
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float h = (e & 1) ? bf_hi(hw[e >> 1]) : bf_lo(hw[e >> 1]);
+          const float pn = 2.f * h - __uint_as_float(rp[e]);
+          rp[e] = __float_as_uint(pn);
+          ry[e] = __float_as_uint(pn + __uint_as_float(ry[e]));
+        }
+        if (!last) {
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            uint32_t pw[4], yw[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int ia = 8 * g + 2 * e;
+              const __nv_bfloat162 pz =
+                  __floats2bfloat162_rn(__uint_as_float(rp[ia]), __uint_as_float(rp[ia + 1]));
+              const __nv_bfloat162 yz =
+                  __floats2bfloat162_rn(__uint_as_float(ry[ia]), __uint_as_float(ry[ia + 1]));
+              pw[e] = *reinterpret_cast<const uint32_t*>(&pz);
+              yw[e] = *reinterpret_cast<const uint32_t*>(&yz);
+            }
+            const int c = c0 + 8 * g;
+            st_shared_v4(tP + op_off(row, c), pw[0], pw[1], pw[2], pw[3]);
+            // Y[p][c..c+7] is row k = p, columns c of the MN tile of the CTA
+            // that owns columns c (this one or the peer)
+            st_cluster_v4(mnY[c >> 7] + mn_off(p, c & 127), yw[0], yw[1], yw[2], yw[3]);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) ry[e] = __float_as_uint(-__uint_as_float(ry[e]));
+          stage_gq32(ry, c0, to_peer, own, cross);
+        }
+      }
+      if (!last) {
+        fence_proxy_async_all();  // P, Y (here and in the peer) -> the next MMAs
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote(map_peer(smem_u32(readyE), 0));
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // -D staged in both CTAs
+  pack_dtheta(b, lb, qs.P, rank, lsb, a.nb, dtheta, gq_own, gq_cross);
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // no CTA leaves while its peer may still signal or read it
@@ -878,11 +1308,13 @@ __global__ void __launch_bounds__(kCnpThreads, 1)
 
 }  // namespace
 
-bool cnp_pair_fits(int b, int k) { return k == 3 && b >= 32 && b <= 256 && 256 % b == 0; }
+bool cnp_pair_fits(int b, int k) {
+  return k >= 1 && k <= 16 && b >= 32 && b <= 256 && 256 % b == 0;
+}
 
-cudaError_t cnp_build_pair(const float* theta, int n, int b, __nv_bfloat16* blocks,
+cudaError_t cnp_build_pair(const float* theta, int n, int b, int k, __nv_bfloat16* blocks,
                            cudaStream_t stream) {
-  if (!cnp_pair_fits(b, 3) || n <= 0 || (static_cast<long long>(n) * b) % 256 != 0)
+  if (!cnp_pair_fits(b, k) || n <= 0 || (static_cast<long long>(n) * b) % 256 != 0)
     return cudaErrorInvalidValue;
   static bool attr_set[64] = {false};
   static std::mutex mu;
@@ -894,6 +1326,9 @@ cudaError_t cnp_build_pair(const float* theta, int n, int b, __nv_bfloat16* bloc
     if (!attr_set[dev]) {
       cudaError_t e = cudaFuncSetAttribute(cnp_build_pair_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, kBuildSmem);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(cnp_build_pair_k_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kBuildSmem);
       if (e != cudaSuccess) return e;
       attr_set[dev] = true;
     }
@@ -920,7 +1355,8 @@ cudaError_t cnp_build_pair(const float* theta, int n, int b, __nv_bfloat16* bloc
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   prof_begin("cnp_build", stream);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, cnp_build_pair_kernel, a);
+  cudaError_t e = k == 3 ? cudaLaunchKernelEx(&cfg, cnp_build_pair_kernel, a)
+                         : cudaLaunchKernelEx(&cfg, cnp_build_pair_k_kernel, a, k);
   prof_end("cnp_build", stream);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -928,7 +1364,7 @@ cudaError_t cnp_build_pair(const float* theta, int n, int b, __nv_bfloat16* bloc
 
 cudaError_t cnp_adjoint_pair(const CnpAdjointPairArgs& x, cudaStream_t stream) {
   const int b = x.b;
-  if (!cnp_pair_fits(b, 3) || x.n_a + x.n_b <= 0 ||
+  if (!cnp_pair_fits(b, x.k) || x.n_a + x.n_b <= 0 ||
       (static_cast<long long>(x.n_a) * b) % 256 != 0 || (static_cast<long long>(x.n_b) * b) % 256 != 0)
     return cudaErrorInvalidValue;
   static bool attr_set[64] = {false};
@@ -941,6 +1377,9 @@ cudaError_t cnp_adjoint_pair(const CnpAdjointPairArgs& x, cudaStream_t stream) {
     if (!attr_set[dev]) {
       cudaError_t e = cudaFuncSetAttribute(cnp_adjoint_pair_kernel,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, kAdjSmem);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(cnp_adjoint_pair_k_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kAdjSmem);
       if (e != cudaSuccess) return e;
       attr_set[dev] = true;
     }
@@ -981,7 +1420,8 @@ cudaError_t cnp_adjoint_pair(const CnpAdjointPairArgs& x, cudaStream_t stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   prof_begin("cnp_adjoint", stream);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, cnp_adjoint_pair_kernel, tmH, tmHmn, a);
+  cudaError_t e = x.k == 3 ? cudaLaunchKernelEx(&cfg, cnp_adjoint_pair_kernel, tmH, tmHmn, a)
+                            : cudaLaunchKernelEx(&cfg, cnp_adjoint_pair_k_kernel, tmH, tmHmn, a, x.k);
   prof_end("cnp_adjoint", stream);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

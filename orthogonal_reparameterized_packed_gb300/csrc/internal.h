@@ -173,20 +173,20 @@ struct ChainAdjointArgs {
 cudaError_t chain_adjoint(const ChainAdjointArgs& a, cudaStream_t stream);
 
 // ------------------------------------------- b x b chains on CTA pairs
-// k = 3 and b in {32, 64, 128, 256} (256 x 256 superblocks), bf16 blocks:
-// one cluster of two CTAs per superblock with every operand in shared
-// memory (cnp_pair.cu).  n * b must be a multiple of 256.
+// 1 <= k <= 16 and b in {32, 64, 128, 256} (256 x 256 superblocks), bf16
+// blocks: one cluster of two CTAs per superblock with every operand in
+// shared memory (cnp_pair.cu).  n * b must be a multiple of 256.
 bool cnp_pair_fits(int b, int k);
-// blocks [n][b][b] = (I + Q)(I + Q + Q^2 + Q^3) from theta [n][b(b-1)/2].
-cudaError_t cnp_build_pair(const float* theta, int n, int b, __nv_bfloat16* blocks,
+// blocks [n][b][b] = (I + Q)(I + Q + ... + Q^k) from theta [n][b(b-1)/2].
+cudaError_t cnp_build_pair(const float* theta, int n, int b, int k, __nv_bfloat16* blocks,
                            cudaStream_t stream);
 
 // Packed gradients of both sides from the split-K partials of the
 // TRANSPOSED block gradients G^T over 256 x 256 superblocks (blocks
-// [0, n_a) of side a, then n_b of side b), k = 3.  Scratch: hg
+// [0, n_a) of side a, then n_b of side b).  Scratch: hg
 // [(n_a + n_b) * b / 256 * 256][256] bf16.
 struct CnpAdjointPairArgs {
-  int n_a = 0, n_b = 0, b = 0;
+  int n_a = 0, n_b = 0, b = 0, k = 3;
   const float* theta_a = nullptr;
   const float* theta_b = nullptr;
   const float* part_a = nullptr;

@@ -61,9 +61,13 @@ def test_packed_size_rejects_bad_dims(lib):
 
 def test_workspace_sizes_are_positive_and_monotone(lib):
     F32, BF16 = poetx.F32, poetx.BF16
-    # the k = 3 bf16 build on CTA pairs keeps its operands in shared memory
+    # the bf16 builds on CTA pairs (b <= 256, 1 <= k <= 16) keep their
+    # operands in shared memory; the chain (b = 512) and k = 0 need scratch
     assert poetx.poetx_build_workspace_size(4096, 256, 3, BF16) == 0
-    assert poetx.poetx_build_workspace_size(4096, 256, 5, BF16) > 0
+    assert poetx.poetx_build_workspace_size(4096, 256, 5, BF16) == 0
+    assert poetx.poetx_build_workspace_size(4096, 64, 16, BF16) == 0
+    assert poetx.poetx_build_workspace_size(4096, 512, 3, BF16) > 0
+    assert poetx.poetx_build_workspace_size(4096, 256, 0, BF16) > 0
     assert poetx.poetx_build_workspace_size(256, 32, 3, F32) > 0
     a = poetx.poetx_forward_workspace_size(4096, 4096, 256, 1024, BF16)
     b = poetx.poetx_forward_workspace_size(4096, 4096, 256, 2048, BF16)

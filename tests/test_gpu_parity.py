@@ -119,8 +119,10 @@ def test_unpack_is_bit_exact(px, dtype, d, b):
     ("bf16", 1024, 256, 3), ("bf16", 1024, 256, 5), ("bf16", 1024, 512, 3),
     ("bf16", 1024, 512, 1), ("bf16", 512, 256, 10), ("bf16", 512, 128, 0),
     ("bf16", 512, 256, 16), ("f32", 64, 8, 16), ("bf16", 768, 256, 8),  # k = 16: the maximum
-    # k = 3, b <= 256: the CTA-pair build (256 x 256 superblocks)
-    ("bf16", 256, 32, 3), ("bf16", 768, 64, 3), ("bf16", 2048, 128, 3), ("bf16", 4096, 256, 3)])
+    # b <= 256: the CTA-pair builds (256 x 256 superblocks; k = 3 and any other k)
+    ("bf16", 256, 32, 3), ("bf16", 768, 64, 3), ("bf16", 2048, 128, 3), ("bf16", 4096, 256, 3),
+    ("bf16", 512, 64, 1), ("bf16", 256, 32, 2), ("bf16", 1024, 64, 5), ("bf16", 768, 128, 4),
+    ("bf16", 4096, 256, 6)])
 def test_build_blocks_matches_oracle(px, dtype, d, b, k):
     rng = np.random.default_rng(21)
     theta = (rng.standard_normal((d // b, b * (b - 1) // 2)) * 0.02).astype(np.float32)
@@ -220,6 +222,11 @@ LAYER_CASES = [
     (512, 256, 256, 16, 40, "bf16"),     # the largest k
     (64, 32, 8, 16, 20, "f32"),
     (512, 256, 256, 0, 70, "bf16"),
+    # the CTA-pair adjoint for k != 3 (Horner form), every block size
+    (512, 256, 32, 5, 100, "bf16"),
+    (256, 512, 64, 1, 70, "bf16"),
+    (768, 512, 128, 4, 150, "bf16"),
+    (512, 512, 256, 2, 96, "bf16"),
 ]
 
 
