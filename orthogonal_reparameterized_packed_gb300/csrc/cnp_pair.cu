@@ -9,8 +9,9 @@
 // diagonal matrices stay block diagonal).  CTA rank r owns rows 128 r ..
 // 128 r + 127 of every matrix; a pair MMA (M = 256 over both CTAs, N = 256,
 // D = A B^T) reads A from each CTA's own rows and B from each CTA's own
-// rows of the second operand, so with Q^T = -Q and (Q^2)^T = Q^2 no matrix
-// ever has to be transposed or exchanged:
+// rows of the second operand, so with Q^T = -Q and (Q^2)^T = Q^2 the builds
+// never transpose or exchange a matrix (the adjoints exchange one MN-major
+// tile per phase through distributed shared memory).  The k = 3 build:
 //
 //   R = I + 2Q + 2Q^2 + 2Q^3 + Q^4 = I + 2Q + 2 Q2 + Q2 W^T,
 //   Q2 = Q Q = -(Q Q^T),  W = Q2 - 2Q  (W^T = Q2 + 2Q)
