@@ -536,6 +536,29 @@ def run_gpu(args):
         insts[key] = {"w": wk, "dev": dev_k, "layer": lay_k, "step": fn_k}
     dev, layer = insts[keys[0]]["dev"], insts[keys[0]]["layer"]
     order = [insts[key]["step"] for _, key in projs]
+    if len(projs) > 1 and not (args.permute or args.w0_int8 or args.train_step):
+        # a model step: every projection's factors built by one call at the
+        # start (its own packed parameters, copied from its shape's seeded
+        # inputs), then each projection's forward and backward on its blocks
+        from orthogonal_reparameterized_packed_gb300.layer import BlockStack
+        stack = BlockStack([(insts[key]["w"]["d_in"], insts[key]["w"]["d_out"])
+                            for _, key in projs], w["b"], w["k"], dtype=w["dtype"])
+        for i, (_, key) in enumerate(projs):
+            tp, tr = stack.theta_views(i)
+            tp.copy_(insts[key]["dev"]["theta_P"])
+            tr.copy_(insts[key]["dev"]["theta_R"])
+
+        def proj_fn(i, key):
+            lay_i, dev_i = insts[key]["layer"], insts[key]["dev"]
+            tp, tr = stack.theta_views(i)
+            P, R = stack.block_views(i)
+
+            def fn():
+                lay_i.forward(dev_i["x"], dev_i["W0"], P_blocks=P, R_blocks=R)
+                lay_i.backward(dev_i["dy"], dev_i["x"], dev_i["W0"], tp, tr, P_blocks=P,
+                               R_blocks=R)
+            return fn
+        order = [stack.build] + [proj_fn(i, key) for i, (_, key) in enumerate(projs)]
 
     def step():
         for fn in order:

@@ -82,15 +82,21 @@ class PoetxLayer:
         poetx_build_blocks(theta_R, self.d_out, self.b, self.k, self.code, self.R_blocks,
                            self.workspace, stream)
 
-    def forward(self, x, W0, stream=None):
-        poetx_forward(x, W0, self.P_blocks, self.R_blocks, self.y, self.v, self.d_in,
-                      self.d_out, self.b, self.tokens, self.code, self.workspace, stream)
+    def forward(self, x, W0, stream=None, P_blocks=None, R_blocks=None):
+        """P_blocks, R_blocks: blocks built elsewhere (e.g. by a BlockStack)
+        instead of this layer's own."""
+        P = self.P_blocks if P_blocks is None else P_blocks
+        R = self.R_blocks if R_blocks is None else R_blocks
+        poetx_forward(x, W0, P, R, self.y, self.v, self.d_in, self.d_out, self.b, self.tokens,
+                      self.code, self.workspace, stream)
         return self.y
 
-    def backward(self, dy, x, W0, theta_P, theta_R, stream=None):
-        poetx_backward(dy, x, W0, theta_P, theta_R, self.P_blocks, self.R_blocks, self.v,
-                       self.dx, self.dtheta_P, self.dtheta_R, self.d_in, self.d_out, self.b,
-                       self.k, self.tokens, self.code, self.workspace, stream)
+    def backward(self, dy, x, W0, theta_P, theta_R, stream=None, P_blocks=None, R_blocks=None):
+        P = self.P_blocks if P_blocks is None else P_blocks
+        R = self.R_blocks if R_blocks is None else R_blocks
+        poetx_backward(dy, x, W0, theta_P, theta_R, P, R, self.v, self.dx, self.dtheta_P,
+                       self.dtheta_R, self.d_in, self.d_out, self.b, self.k, self.tokens,
+                       self.code, self.workspace, stream)
         return self.dx, self.dtheta_P, self.dtheta_R
 
     def step(self, theta_P, theta_R, W0, x, dy, stream=None):
@@ -190,6 +196,48 @@ def to_device(inp, device="cuda"):
     return dict(theta=theta, theta_P=theta[:nP].view(inp.theta_P.shape),
                 theta_R=theta[nP:].view(inp.theta_R.shape),
                 W0=act(inp.W0), x=act(inp.x), dy=act(inp.dy))
+
+
+class BlockStack:
+    """The packed parameters and blocks of many projections (same b, k and
+    dtype) in two allocations, so that one poetx_build_blocks call builds
+    every factor of a model at the start of a step (blocks are independent).
+    `shapes` lists (d_in, d_out) per projection; theta(i) and blocks(i) give
+    projection i's (theta_P, theta_R) and (P_blocks, R_blocks) views."""
+
+    def __init__(self, shapes, b, k, dtype="bf16", device="cuda"):
+        self.b, self.k, self.code = b, k, dtype_code(dtype)
+        dev = torch.device(device)
+        self.shapes = list(shapes)
+        self.d = sum(di + do for di, do in self.shapes)
+        self._theta_off, self._block_off = [], []
+        t = n = 0
+        for di, do in self.shapes:
+            self._theta_off.append(t)
+            self._block_off.append(n)
+            t += poetx_packed_size(di, b) + poetx_packed_size(do, b)
+            n += (di + do) // b
+        self.theta = torch.zeros((t,), dtype=torch.float32, device=dev)
+        self.blocks = torch.empty((n, b, b), dtype=_TORCH_DTYPE[self.code], device=dev)
+        ws = poetx_build_workspace_size(self.d, b, k, self.code)
+        self.workspace = torch.empty((max(ws, 16),), dtype=torch.uint8, device=dev)
+
+    def theta_views(self, i):
+        di, do = self.shapes[i]
+        mP, mR = poetx_packed_size(di, self.b), poetx_packed_size(do, self.b)
+        o = self._theta_off[i]
+        return (self.theta[o:o + mP].view(di // self.b, -1),
+                self.theta[o + mP:o + mP + mR].view(do // self.b, -1))
+
+    def block_views(self, i):
+        di, do = self.shapes[i]
+        o = self._block_off[i]
+        return self.blocks[o:o + di // self.b], self.blocks[o + di // self.b:o + (di + do) // self.b]
+
+    def build(self, stream=None):
+        """Every factor of every projection, one call."""
+        poetx_build_blocks(self.theta, self.d, self.b, self.k, self.code, self.blocks,
+                           self.workspace, stream)
 
 
 class PoetxPermutedLayer:

@@ -313,3 +313,21 @@ def test_one_call_build_equals_two_calls(px, dtype, b):
     two.build(tP, tR)
     check_status(px)
     assert torch.equal(one.blocks, two.blocks)
+
+
+@pytest.mark.parametrize("b,k", [(256, 3), (64, 5), (512, 3)])
+def test_block_stack_builds_every_projection_in_one_call(px, b, k):
+    # a model's factors built by one call equal each projection built alone
+    from orthogonal_reparameterized_packed_gb300.layer import BlockStack, PoetxLayer
+    shapes = [(512, 1024), (1024, 512), (512, 512)]
+    stack = BlockStack(shapes, b, k, dtype="bf16")
+    rng = np.random.default_rng(70 + b + k)
+    stack.theta.copy_(torch.from_numpy(
+        (rng.standard_normal(stack.theta.numel()) * 0.02).astype(np.float32)))
+    stack.build()
+    for i, (di, do) in enumerate(shapes):
+        lay = PoetxLayer(di, do, b, k, 8, dtype="bf16")
+        lay.build(*stack.theta_views(i))
+        check_status(px)
+        P, R = stack.block_views(i)
+        assert torch.equal(P, lay.P_blocks) and torch.equal(R, lay.R_blocks), i
