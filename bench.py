@@ -680,7 +680,7 @@ def run_gpu(args):
     tags = ["build", "unpack", "identity_plus", "expand_superblocks", "transform",
             "transform_t", "gemm_w0", "gemm_w0_dgrad", "gemm_w0_r", "gemm_w0_dgrad_p", "outer", "reduce_extract", "cnp_bwd",
             "pack_skew", "f32_to_bf16", "chain", "prep_tiles", "pack_tiles", "permute", "adam",
-            "transform_sum", "cnp_build", "cnp_adjoint",
+            "transform_sum", "cnp_build", "cnp_sums", "cnp_adjoint",
             "dequantize", "quantize"]
     kernels = {}
     for t in tags:

@@ -397,8 +397,9 @@ __global__ void __launch_bounds__(kCnpThreads, 1) cnp_build_pair_kernel(const Cn
 //   phase 1   Q (bf16) from theta as in the build; acc0 = MMA(Q, Q) = -Q2;
 //             epilogue: Q2, X = 2Q + Q2 (bf16 tiles; X^T = Q2 - 2Q).  This
 //             needs theta only and runs before the wait for the partials.
-//   sums      H's rows of this CTA, summed over the K splits, to bf16
-//             scratch in global memory
+//   sums      H, summed over the K splits into bf16 scratch, by a kernel
+//             of its own on all SMs (cnp_sum_partials_kernel) before this
+//             one passes its wait
 //   phase 2   acc1 = MMA(Q2, H) = Q2 G, acc0 = MMA(G, X) = G (Q2 - 2Q);
 //             H's row chunks (B) and G's (A, read MN-major from H's columns:
 //             G = H^T is never formed) stream through a two-slot ring of
@@ -432,56 +433,6 @@ static_assert(2 * kOpBytes >= (32640 - 8128) * 4, "theta staging in the Q2 and X
 __device__ __forceinline__ uint32_t mn_off(int k, int n) {
   return static_cast<uint32_t>((k >> 6) * 16384 + (n >> 6) * 8192 + (k & 63) * 128 +
                                ((((n & 63) >> 3) ^ (k & 7)) << 4) + ((n & 7) << 1));
-}
-
-// All threads of a CTA: H's rows of this CTA (superblock sb, side-local
-// superblock lsb), summed over the K splits of the partials, to the bf16
-// scratch hg [superblocks][256][256] (zero outside the diagonal blocks).  A
-// warp takes one row (1 KiB per split); a thread keeps four splits' loads in
-// flight.
-__device__ void sum_partials_to_h(const float* part, int splits, int nsb_side, int lsb, int sb,
-                                  int rank, int lb, __nv_bfloat16* hg) {
-  const long long split_stride = static_cast<long long>(nsb_side) * 65536;
-  const float* pt = part + static_cast<long long>(lsb) * 65536;
-  const long long grow0 = static_cast<long long>(sb) * 256;
-  for (int t = threadIdx.x; t < 128 * 32; t += blockDim.x) {
-    const int pp = 128 * rank + (t >> 5);
-    const int c8 = 8 * (t & 31);
-    float h[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) h[e] = 0.f;
-    if ((c8 >> lb) == (pp >> lb)) {
-      const float* ps = pt + pp * 256 + c8;
-      int sp = 0;
-      for (; sp + 4 <= splits; sp += 4) {
-        float4 v[8];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          v[2 * u] = *reinterpret_cast<const float4*>(ps + (sp + u) * split_stride);
-          v[2 * u + 1] = *reinterpret_cast<const float4*>(ps + (sp + u) * split_stride + 4);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          h[0] += v[2 * u].x; h[1] += v[2 * u].y; h[2] += v[2 * u].z; h[3] += v[2 * u].w;
-          h[4] += v[2 * u + 1].x; h[5] += v[2 * u + 1].y; h[6] += v[2 * u + 1].z;
-          h[7] += v[2 * u + 1].w;
-        }
-      }
-      for (; sp < splits; ++sp) {
-        const float4 v0 = *reinterpret_cast<const float4*>(ps + sp * split_stride);
-        const float4 v1 = *reinterpret_cast<const float4*>(ps + sp * split_stride + 4);
-        h[0] += v0.x; h[1] += v0.y; h[2] += v0.z; h[3] += v0.w;
-        h[4] += v1.x; h[5] += v1.y; h[6] += v1.z; h[7] += v1.w;
-      }
-    }
-    uint32_t hw[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const __nv_bfloat162 hh = __floats2bfloat162_rn(h[2 * e], h[2 * e + 1]);
-      hw[e] = *reinterpret_cast<const uint32_t*>(&hh);
-    }
-    *reinterpret_cast<uint4*>(hg + (grow0 + pp) * 256 + c8) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-  }
 }
 
 // One thread, 32 consecutive columns c0.. of its row of G_Q (fp32 bits):
@@ -537,6 +488,9 @@ __device__ void pack_dtheta(int b, int lb, int P, int rank, int lsb, int nb, flo
   }
 }
 
+struct CnpAdjArgs;
+__global__ void cnp_sum_partials_kernel(const CnpAdjArgs a);
+
 struct CnpAdjArgs {
   const float* theta_a;
   const float* theta_b;
@@ -549,6 +503,66 @@ struct CnpAdjArgs {
   float* dtheta_b;
   int* status;
 };
+
+// The token sums H of every superblock of both sides: the split-K
+// partials [splits][superblocks][256][256] (fp32) summed, rounded to bf16
+// into hg (zero outside the diagonal b-blocks).  One 8-column group of a
+// row per thread, four splits' loads in flight; all SMs, ahead of the
+// adjoint.  It lets the adjoint launch before it waits itself: the adjoint
+// reads only theta before its own wait (no kernel that may still run writes
+// theta: the kernels before this one's predecessor are complete once that
+// predecessor has been launched), and after its wait this kernel is done.
+__global__ void __launch_bounds__(256) cnp_sum_partials_kernel(const CnpAdjArgs a) {
+  pdl_trigger();
+  pdl_wait();  // the partials are complete from here on
+  const int lb = __ffs(a.b) - 1;
+  const long long items = static_cast<long long>(a.nsb_a + a.nsb_b) * 256 * 32;
+  for (long long it = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; it < items;
+       it += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int sb = static_cast<int>(it >> 13);  // 8192 groups per superblock
+    const int p = static_cast<int>(it >> 5) & 255;
+    const int c8 = 8 * static_cast<int>(it & 31);
+    const bool side_b = sb >= a.nsb_a;
+    const int lsb = side_b ? sb - a.nsb_a : sb;
+    const long long split_stride = static_cast<long long>(side_b ? a.nsb_b : a.nsb_a) * 65536;
+    const int splits = side_b ? a.splits_b : a.splits_a;
+    const float* ps = (side_b ? a.part_b : a.part_a) + static_cast<long long>(lsb) * 65536 + p * 256 + c8;
+    float h[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) h[e] = 0.f;
+    if ((c8 >> lb) == (p >> lb)) {
+      int sp = 0;
+      for (; sp + 4 <= splits; sp += 4) {
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          v[2 * u] = *reinterpret_cast<const float4*>(ps + (sp + u) * split_stride);
+          v[2 * u + 1] = *reinterpret_cast<const float4*>(ps + (sp + u) * split_stride + 4);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          h[0] += v[2 * u].x; h[1] += v[2 * u].y; h[2] += v[2 * u].z; h[3] += v[2 * u].w;
+          h[4] += v[2 * u + 1].x; h[5] += v[2 * u + 1].y; h[6] += v[2 * u + 1].z;
+          h[7] += v[2 * u + 1].w;
+        }
+      }
+      for (; sp < splits; ++sp) {
+        const float4 v0 = *reinterpret_cast<const float4*>(ps + sp * split_stride);
+        const float4 v1 = *reinterpret_cast<const float4*>(ps + sp * split_stride + 4);
+        h[0] += v0.x; h[1] += v0.y; h[2] += v0.z; h[3] += v0.w;
+        h[4] += v1.x; h[5] += v1.y; h[6] += v1.z; h[7] += v1.w;
+      }
+    }
+    uint32_t hw[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const __nv_bfloat162 hh = __floats2bfloat162_rn(h[2 * e], h[2 * e + 1]);
+      hw[e] = *reinterpret_cast<const uint32_t*>(&hh);
+    }
+    *reinterpret_cast<uint4*>(a.hg + (static_cast<long long>(sb) * 256 + p) * 256 + c8) =
+        make_uint4(hw[0], hw[1], hw[2], hw[3]);
+  }
+}
 
 __global__ void __launch_bounds__(kCnpThreads, 1)
     cnp_adjoint_pair_kernel(const __grid_constant__ CUtensorMap tmH,
@@ -586,10 +600,7 @@ __global__ void __launch_bounds__(kCnpThreads, 1)
   const int sb = static_cast<int>(cluster_id_x());  // superblock over both sides
   const bool side_b = sb >= a.nsb_a;
   const int lsb = side_b ? sb - a.nsb_a : sb;
-  const int nsb_side = side_b ? a.nsb_b : a.nsb_a;
   const float* theta = side_b ? a.theta_b : a.theta_a;
-  const float* part = side_b ? a.part_b : a.part_a;
-  const int splits = side_b ? a.splits_b : a.splits_a;
   float* dtheta = side_b ? a.dtheta_b : a.dtheta_a;
   const int b = a.b;
   const int lb = __ffs(b) - 1;
@@ -696,13 +707,11 @@ __global__ void __launch_bounds__(kCnpThreads, 1)
     }
   }
 
-  // ------------------------------------------------------ the token sums H
-  pdl_wait();  // the partials are complete from here on
+  // ---------------------------------------------- the token sums H (ready)
+  pdl_wait();  // the sums kernel is complete: H is in the scratch
   pdl_trigger();
-  sum_partials_to_h(part, splits, nsb_side, lsb, sb, rank, lb, a.hg);
-  fence_proxy_async_global();  // these stores -> the TMA loads of the chunks
   __syncthreads();
-  cluster_sync();  // H scratch written by both CTAs
+  cluster_sync();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -1083,9 +1092,10 @@ __global__ void __launch_bounds__(kCnpThreads, 1) cnp_build_pair_k_kernel(const 
 // transposed; Y accumulates Q^p H a_{k-1-p}(Q) + Q^k H).  Both recursions
 // run forward, so no E_i is stored.  dtheta(i, j) = dQ[i][j] - dQ[j][i] =
 // D[j][i] - D[i][j]: -D is staged and packed like G_Q of the k = 3 adjoint.
-//   prologue  Q hi from theta (before the wait for the partials); H's rows
-//             summed to bf16 scratch; P's tile (H's own rows, K-major) and
-//             Y's tile (H read MN-major: rows k, this CTA's columns) by TMA
+//   prologue  Q hi from theta (before the wait for the token sums, which
+//             the sums kernel leaves in bf16 scratch); P's tile (H's own
+//             rows, K-major) and Y's tile (H read MN-major: rows k, this
+//             CTA's columns) by TMA
 //   phase m   accP = MMA(P, Q_hi) = -P Q,  accY = MMA_mn(Q_hi, Y) = Q Y
 //   epilogue  P = 2H - accP -> bf16 (own rows), Y = P + accY -> bf16 MN tile
 //             (the half of each row in the peer's columns through
@@ -1121,10 +1131,7 @@ __global__ void __launch_bounds__(kCnpThreads, 1)
   const int sb = static_cast<int>(cluster_id_x());
   const bool side_b = sb >= a.nsb_a;
   const int lsb = side_b ? sb - a.nsb_a : sb;
-  const int nsb_side = side_b ? a.nsb_b : a.nsb_a;
   const float* theta = side_b ? a.theta_b : a.theta_a;
-  const float* part = side_b ? a.part_b : a.part_a;
-  const int splits = side_b ? a.splits_b : a.splits_a;
   float* dtheta = side_b ? a.dtheta_b : a.dtheta_a;
   const int b = a.b;
   const int lb = __ffs(b) - 1;
@@ -1160,11 +1167,9 @@ __global__ void __launch_bounds__(kCnpThreads, 1)
     qstage_issue(qs, theta + static_cast<long long>(lsb) * a.nb * qs.P, tP, staged);
   q_gather(qs, rank, tP, staged, tQ, nullptr, abort_flag, a.status);
 
-  pdl_wait();  // the partials are complete from here on
+  pdl_wait();  // the sums kernel is complete: H is in the scratch
   pdl_trigger();
-  sum_partials_to_h(part, splits, nsb_side, lsb, sb, rank, lb, a.hg);
-  fence_proxy_async_global();  // these stores -> the TMA loads of H
-  fence_proxy_async_all();     // the Q tile and the staging reads -> the async proxy
+  fence_proxy_async_all();  // the Q tile and the staging reads -> the async proxy
   __syncthreads();
   cluster_sync();  // H and both CTAs' Q tiles complete
   if (threadIdx.x == 0) {
@@ -1420,8 +1425,18 @@ cudaError_t cnp_adjoint_pair(const CnpAdjointPairArgs& x, cudaStream_t stream) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
+  // the token sums first, on all SMs
+  const long long sum_items = static_cast<long long>(nsb) * 256 * 32;
+  const long long sum_cap = static_cast<long long>(sm_count()) * 8;
+  const long long sum_blocks = (sum_items + 255) / 256;
+  prof_begin("cnp_sums", stream);
+  cudaError_t e = launch_pdl(cnp_sum_partials_kernel,
+                             dim3(static_cast<unsigned>(sum_blocks < sum_cap ? sum_blocks : sum_cap)),
+                             dim3(256), 0, stream, a);
+  prof_end("cnp_sums", stream);
+  if (e != cudaSuccess) return e;
   prof_begin("cnp_adjoint", stream);
-  cudaError_t e = x.k == 3 ? cudaLaunchKernelEx(&cfg, cnp_adjoint_pair_kernel, tmH, tmHmn, a)
+  e = x.k == 3 ? cudaLaunchKernelEx(&cfg, cnp_adjoint_pair_kernel, tmH, tmHmn, a)
                             : cudaLaunchKernelEx(&cfg, cnp_adjoint_pair_k_kernel, tmH, tmHmn, a, x.k);
   prof_end("cnp_adjoint", stream);
   return e != cudaSuccess ? e : cudaGetLastError();
