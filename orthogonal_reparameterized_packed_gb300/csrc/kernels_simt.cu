@@ -615,15 +615,34 @@ __global__ void adam_kernel(float* __restrict__ theta, const float* __restrict__
                             float beta1, float beta2, float eps, float wd, float bc1, float bc2) {
   pdl_wait();
   pdl_trigger();
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const float g = grad[i];
-    const float mi = beta1 * m[i] + (1.f - beta1) * g;
-    const float vi = beta2 * v[i] + (1.f - beta2) * g * g;
+  auto step1 = [&](float th, float g, float& mi, float& vi) {
+    mi = beta1 * mi + (1.f - beta1) * g;
+    vi = beta2 * vi + (1.f - beta2) * g * g;
+    return th - lr * ((mi / bc1) / (sqrtf(vi / bc2) + eps) + wd * th);
+  };
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  const long long first = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  // 16-byte vectors where all four arrays allow them, the same arithmetic per element
+  const bool vec = ((reinterpret_cast<uintptr_t>(theta) | reinterpret_cast<uintptr_t>(grad) |
+                     reinterpret_cast<uintptr_t>(m) | reinterpret_cast<uintptr_t>(v)) & 15u) == 0;
+  const long long n4 = vec ? n / 4 : 0;
+  for (long long i = first; i < n4; i += stride) {
+    const float4 g = reinterpret_cast<const float4*>(grad)[i];
+    float4 mi = reinterpret_cast<float4*>(m)[i], vi = reinterpret_cast<float4*>(v)[i];
+    float4 th = reinterpret_cast<float4*>(theta)[i];
+    th.x = step1(th.x, g.x, mi.x, vi.x);
+    th.y = step1(th.y, g.y, mi.y, vi.y);
+    th.z = step1(th.z, g.z, mi.z, vi.z);
+    th.w = step1(th.w, g.w, mi.w, vi.w);
+    reinterpret_cast<float4*>(m)[i] = mi;
+    reinterpret_cast<float4*>(v)[i] = vi;
+    reinterpret_cast<float4*>(theta)[i] = th;
+  }
+  for (long long i = 4 * n4 + first; i < n; i += stride) {
+    float mi = m[i], vi = v[i];
+    theta[i] = step1(theta[i], grad[i], mi, vi);
     m[i] = mi;
     v[i] = vi;
-    const float th = theta[i];
-    theta[i] = th - lr * ((mi / bc1) / (sqrtf(vi / bc2) + eps) + wd * th);
   }
 }
 
@@ -882,7 +901,8 @@ cudaError_t launch_permute_rows(const void* in, long long in_rows, const int* ro
 cudaError_t launch_adam(float* theta, const float* grad, float* m, float* v, long long n,
                         float lr, float beta1, float beta2, float eps, float wd, float bc1,
                         float bc2, cudaStream_t s) {
-  POETX_EW_LAUNCH("adam", n, adam_kernel, theta, grad, m, v, n, lr, beta1, beta2, eps, wd, bc1,
+  // one thread per 16-byte vector (a grid-stride loop covers the rest)
+  POETX_EW_LAUNCH("adam", (n + 3) / 4, adam_kernel, theta, grad, m, v, n, lr, beta1, beta2, eps, wd, bc1,
                   bc2);
 }
 
