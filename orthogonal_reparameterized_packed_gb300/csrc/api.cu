@@ -201,8 +201,12 @@ cudaError_t tc_transform(const bf16* in, const bf16* sb, bf16* out, int d, int S
   g.N = S;
   g.K = S;
   g.batches = d / S;
-  g.BN = S == 256 ? 256 : 128;  // the resident B tile (BN x S bf16) must fit 128 KiB
-  g.b_resident = true;
+  // S = 256: the block (256 x 256 bf16, 128 KiB) stays resident while a CTA
+  // walks token tiles; S = 512: 256-wide tiles with the block's rows streamed
+  // (a resident 512 x 128 slice gives N = 128 tiles whose K steps hold too
+  // little MMA work to cover the loads)
+  g.BN = 256;
+  g.b_resident = S == 256;
   g.A = op(in, T, d, d, false, 0, S);
   g.B = transposed ? op(sb, d, S, S, true, 0, S) : op(sb, d, S, S, false, S, 0);
   g.epi.out_bf16 = out;
