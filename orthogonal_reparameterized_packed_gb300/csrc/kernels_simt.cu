@@ -729,10 +729,12 @@ __global__ void dequantize_kernel(const int8_t* __restrict__ q, const float* __r
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   if (vec) {
     const long long chunks = total / 16;
+    const unsigned per_row = static_cast<unsigned>(d_in / 16);  // d_in % 16 == 0: one row per chunk
     for (long long c = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; c < chunks;
          c += stride) {
       const long long e0 = c * 16;
-      const float s = scales[e0 / d_in];  // d_in % 16 == 0: one row per chunk
+      const long long row = chunks < (1ll << 32) ? static_cast<unsigned>(c) / per_row : c / per_row;
+      const float s = scales[row];
       const int4 raw = reinterpret_cast<const int4*>(q)[c];
       const int words[4] = {raw.x, raw.y, raw.z, raw.w};
       float v[16];
@@ -929,7 +931,8 @@ cudaError_t launch_dequantize(const int8_t* q, const float* scales, void* W, boo
                       : 0;
   const long long items = vec ? total / 16 : total;
   long long blocks = (items + 255) / 256;
-  const long long cap = static_cast<long long>(sm_count()) * 8;
+  // enough threads for one 16-code chunk each at 4096 x 4096 (all loads in flight at once)
+  const long long cap = static_cast<long long>(sm_count()) * 32;
   if (blocks > cap) blocks = cap;
   prof_begin("dequantize", s);
   cudaError_t e =
