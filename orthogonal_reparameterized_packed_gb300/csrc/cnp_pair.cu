@@ -1427,7 +1427,9 @@ cudaError_t cnp_adjoint_pair(const CnpAdjointPairArgs& x, cudaStream_t stream) {
   cfg.numAttrs = 2;
   // the token sums first, on all SMs
   const long long sum_items = static_cast<long long>(nsb) * 256 * 32;
-  const long long sum_cap = static_cast<long long>(sm_count()) * 8;
+  // two CTAs per SM: the adjoint's CTAs (which it lets launch at once) still
+  // fit beside them by registers and start their theta-only phase
+  const long long sum_cap = static_cast<long long>(sm_count()) * 2;
   const long long sum_blocks = (sum_items + 255) / 256;
   prof_begin("cnp_sums", stream);
   cudaError_t e = launch_pdl(cnp_sum_partials_kernel,
