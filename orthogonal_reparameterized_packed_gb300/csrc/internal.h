@@ -114,6 +114,7 @@ cudaError_t tc_gemm_run(const TcGemm& g, cudaStream_t stream);
 // Inputs are float or bf16 (both operands the same type).
 struct SimtGemm {
   int M = 0, N = 0, K = 0, batches = 1;
+  int splits = 1;  // set by simt_gemm_run: K slices per output tile (a cluster)
   bool bf16_inputs = false;
   const void* A = nullptr;
   long long a_g = 0, a_m = 0, a_k = 0;

@@ -26,31 +26,41 @@ __device__ __forceinline__ float load_f<__nv_bfloat16>(const __nv_bfloat16* p, l
   return __bfloat162float(p[i]);
 }
 
-// C(g) = A(g) * B(g), 64x64 output tile per CTA, 4x4 per thread.
+// C(g) = A(g) * B(g), 64x64 output tile per CTA, 4x4 per thread.  With
+// p.splits > 1 the K range is cut into that many slices, one per CTA of a
+// cluster along x (the tile's N index is blockIdx.x / splits); the slices'
+// partial tiles meet in rank 0's shared memory in rank order (a fixed
+// summation order: results do not depend on timing), and rank 0 applies the
+// epilogue.  No global scratch, no atomics.
 template <typename T>
 __global__ void __launch_bounds__(SIMT_THREADS) simt_gemm_kernel(const SimtGemm p) {
   pdl_wait();
   pdl_trigger();
   __shared__ float As[TK][TM + 4];
   __shared__ float Bs[TK][TN + 4];
+  __shared__ float Ps[TM][TN + 1];  // this slice's partial tile (splits > 1)
   const int g = blockIdx.z;
   const int m0 = blockIdx.y * TM;
-  const int n0 = blockIdx.x * TN;
+  const int split = p.splits > 1 ? static_cast<int>(blockIdx.x) % p.splits : 0;
+  const int n0 = (p.splits > 1 ? static_cast<int>(blockIdx.x) / p.splits : blockIdx.x) * TN;
+  const int kslice = p.splits > 1 ? ((p.K + p.splits * TK - 1) / (p.splits * TK)) * TK : p.K;
+  const int k_begin = split * kslice;
+  const int k_end = min(p.K, k_begin + kslice);
   const T* A = static_cast<const T*>(p.A) + static_cast<long long>(g) * p.a_g;
   const T* B = static_cast<const T*>(p.B) + static_cast<long long>(g) * p.b_g;
   const int tx = threadIdx.x % 16;  // n direction
   const int ty = threadIdx.x / 16;  // m direction
   float acc[4][4] = {};
-  for (int k0 = 0; k0 < p.K; k0 += TK) {
+  for (int k0 = k_begin; k0 < k_end; k0 += TK) {
     for (int e = threadIdx.x; e < TM * TK; e += SIMT_THREADS) {
       const int mm = e / TK, kk = e % TK;
       const int m = m0 + mm, k = k0 + kk;
-      As[kk][mm] = (m < p.M && k < p.K) ? load_f(A, m * p.a_m + k * p.a_k) : 0.f;
+      As[kk][mm] = (m < p.M && k < k_end) ? load_f(A, m * p.a_m + k * p.a_k) : 0.f;
     }
     for (int e = threadIdx.x; e < TN * TK; e += SIMT_THREADS) {
       const int nn = e % TN, kk = e / TN;
       const int n = n0 + nn, k = k0 + kk;
-      Bs[kk][nn] = (n < p.N && k < p.K) ? load_f(B, k * p.b_k + n * p.b_n) : 0.f;
+      Bs[kk][nn] = (n < p.N && k < k_end) ? load_f(B, k * p.b_k + n * p.b_n) : 0.f;
     }
     __syncthreads();
 #pragma unroll
@@ -66,6 +76,26 @@ __global__ void __launch_bounds__(SIMT_THREADS) simt_gemm_kernel(const SimtGemm 
         for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
     }
     __syncthreads();
+  }
+  if (p.splits > 1) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) Ps[ty * 4 + i][tx * 4 + j] = acc[i][j];
+    cluster_sync();  // every slice's partial tile is in its CTA's shared memory
+    if (split == 0) {
+      for (int r = 1; r < p.splits; ++r) {
+        const uint32_t peer = map_peer(smem_u32(&Ps[0][0]), static_cast<uint32_t>(r));
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            acc[i][j] += ld_cluster_f32(
+                peer + 4u * static_cast<uint32_t>((ty * 4 + i) * (TN + 1) + tx * 4 + j));
+      }
+    }
+    cluster_sync();  // no CTA leaves while rank 0 still reads its tile
+    if (split != 0) return;
   }
   const EpiArgs& e = p.epi;
 #pragma unroll
@@ -762,16 +792,37 @@ int ew_grid(long long total) {
 
 }  // namespace
 
-cudaError_t simt_gemm_run(const SimtGemm& g, cudaStream_t stream) {
+cudaError_t simt_gemm_run(const SimtGemm& g_in, cudaStream_t stream) {
+  SimtGemm g = g_in;
   if (g.M <= 0 || g.N <= 0 || g.batches <= 0) return cudaSuccess;
   if (g.batches > 65535) return cudaErrorInvalidValue;
-  dim3 grid((g.N + TN - 1) / TN, (g.M + TM - 1) / TM, g.batches);
-  if (grid.y > 65535) return cudaErrorInvalidValue;
+  const int tiles_n = (g.N + TN - 1) / TN, tiles_m = (g.M + TM - 1) / TM;
+  if (tiles_m > 65535) return cudaErrorInvalidValue;
+  // Small grids with long K: split K over a cluster of up to 8 CTAs per tile
+  // (slices of at least four TK steps) until about two CTAs per SM work.
+  const long long tiles = static_cast<long long>(tiles_n) * tiles_m * g.batches;
+  int splits = 1;
+  const long long want = 2LL * sm_count();
+  while (splits < 8 && tiles * splits * 2 <= want && g.K >= 2 * splits * 4 * TK) splits *= 2;
+  g.splits = splits;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(tiles_n * splits), static_cast<unsigned>(tiles_m),
+                     static_cast<unsigned>(g.batches));
+  cfg.blockDim = dim3(SIMT_THREADS);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(splits);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = splits > 1 ? 2 : 1;
   prof_begin(g.tag, stream);
-  cudaError_t e =
-      g.bf16_inputs
-          ? launch_pdl(simt_gemm_kernel<__nv_bfloat16>, grid, dim3(SIMT_THREADS), 0, stream, g)
-          : launch_pdl(simt_gemm_kernel<float>, grid, dim3(SIMT_THREADS), 0, stream, g);
+  cudaError_t e = g.bf16_inputs ? cudaLaunchKernelEx(&cfg, simt_gemm_kernel<__nv_bfloat16>, g)
+                                : cudaLaunchKernelEx(&cfg, simt_gemm_kernel<float>, g);
   prof_end(g.tag, stream);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
