@@ -543,9 +543,11 @@ cudaError_t run_build(const float* theta, int n, int b, int k, bool is_bf16, voi
     a.blocks = static_cast<bf16*>(blocks);
     return chain_build(a, s);
   }
-  CK(launch_unpack(theta, n, nullptr, 0, b, w.q32, tc ? w.q16 : nullptr, s));
   float* out32 = is_bf16 ? nullptr : static_cast<float*>(blocks);
   bf16* out16 = is_bf16 ? static_cast<bf16*>(blocks) : nullptr;
+  if (!tc && small_chain_fits(b))  // the whole recursion per block in one CTA
+    return launch_small_build(theta, n, b, k, out32, out16, s);
+  CK(launch_unpack(theta, n, nullptr, 0, b, w.q32, tc ? w.q16 : nullptr, s));
   if (k == 0) return launch_identity_plus(w.q32, n, b, out32, out16, s);
   int cur = -1;  // -1: E_{k+1} = Q itself
   for (int i = k; i >= 1; --i) {
@@ -684,6 +686,9 @@ cudaError_t run_cnp_backward(const float* theta_a, int n_a, const float* theta_b
                              float* dtheta_b, cudaStream_t s) {
   const bool tc = tc_small(is_bf16, b);
   const int n = n_a + n_b;
+  if (!tc && small_chain_fits(b))  // the whole adjoint per block in one CTA
+    return launch_small_adjoint(theta_a, n_a, theta_b, n_b, b, k, w.g32[0], dtheta_a, dtheta_b,
+                                s);
   if (k == 0) return launch_pack_skew(w.g32[0], nullptr, n_a, n_b, b, dtheta_a, dtheta_b, s);
   CK(launch_unpack(theta_a, n_a, theta_b, n_b, b, w.q32, tc ? w.q16 : nullptr, s));
   // E_i for i = k .. 2 (E_{k+1} = Q)

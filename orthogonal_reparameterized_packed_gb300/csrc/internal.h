@@ -217,6 +217,15 @@ cudaError_t launch_reduce_extract(const float* part, int splits, int n, int b, i
                                   float* out_f32, __nv_bfloat16* out_bf16, cudaStream_t s);
 // dtheta[g][idx(i,j)] = M[g][i][j] - M[g][j][i] with M = A (+ B if B != null),
 // for n_a + n_b blocks: the first n_a go to dtheta_a, the rest to dtheta_b.
+// Blocks of b <= 64 with every matrix of one block in one CTA's shared
+// memory (fp32 arithmetic): the whole build, or the whole adjoint of both
+// sides (G = dL/dR per block, [n_a + n_b][b][b] fp32), in one launch.
+bool small_chain_fits(int b);
+cudaError_t launch_small_build(const float* theta, int n, int b, int k, float* out32,
+                               __nv_bfloat16* out16, cudaStream_t s);
+cudaError_t launch_small_adjoint(const float* theta_a, int n_a, const float* theta_b, int n_b,
+                                 int b, int k, const float* G, float* dtheta_a, float* dtheta_b,
+                                 cudaStream_t s);
 cudaError_t launch_pack_skew(const float* A, const float* B, int n_a, int n_b, int b,
                              float* dtheta_a, float* dtheta_b, cudaStream_t s);
 // Tiled elementwise steps of the b x b chains (b a multiple of 32), blocks

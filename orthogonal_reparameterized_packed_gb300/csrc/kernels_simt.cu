@@ -123,6 +123,113 @@ __device__ __forceinline__ int packed_pos(int i, int j, int b) {
   return i * b - (i * (i + 1)) / 2 + (j - i - 1);
 }
 
+// Blocks of b <= 64 (fp32 arithmetic), one CTA per block and every matrix in
+// shared memory, so the whole recursion is one launch instead of one per
+// product.  Each product entry is a plain fmaf sum over t = 0 .. b-1.
+//   build:   E = Q;  k times E <- 2Q + Q E;  R = I + E
+//   adjoint: H = G^T (G = dL/dR);  P = Y = H;  k times P <- 2H + P Q,
+//            Y <- P + Q Y;  D = Y = (dL/dQ)^T;  dtheta(i, j) = D[j][i] - D[i][j]
+// (the reverse sweep of the build regrouped by Horner's rule on both sides
+// of H: both recursions run forward and no power of Q is kept).
+constexpr int kSmallMaxB = 64;
+
+__device__ __forceinline__ void small_load_q(const float* th, int b, float* Q) {
+  for (int e = threadIdx.x; e < b * b; e += blockDim.x) {
+    const int i = e / b, j = e - (e / b) * b;
+    Q[e] = i < j ? th[packed_pos(i, j, b)] : (i > j ? -th[packed_pos(j, i, b)] : 0.f);
+  }
+}
+
+// out = add + scale_add * X + L R  (b x b, row-major; X and add may alias nothing written here)
+__device__ __forceinline__ void small_mm(int b, const float* L, const float* R, const float* X,
+                                              float xs, const float* Y, float* out) {
+  for (int e = threadIdx.x; e < b * b; e += blockDim.x) {
+    const int i = e / b, j = e - (e / b) * b;
+    float acc = 0.f;
+    for (int t = 0; t < b; ++t) acc = fmaf(L[i * b + t], R[t * b + j], acc);
+    float v = acc;
+    if (X != nullptr) v = xs * X[e] + v;
+    if (Y != nullptr) v = Y[e] + v;
+    out[e] = v;
+  }
+}
+
+__global__ void __launch_bounds__(256) small_build_kernel(const float* __restrict__ theta, int b,
+                                                          int k, float* __restrict__ out32,
+                                                          __nv_bfloat16* __restrict__ out16) {
+  pdl_wait();
+  pdl_trigger();
+  extern __shared__ float small_smem[];
+  const int bb = b * b;
+  float* Q = small_smem;
+  float* E = Q + bb;
+  float* F = E + bb;
+  const long long g = blockIdx.x;
+  small_load_q(theta + g * (static_cast<long long>(b) * (b - 1) / 2), b, Q);
+  __syncthreads();
+  for (int e = threadIdx.x; e < bb; e += blockDim.x) E[e] = Q[e];
+  __syncthreads();
+  for (int it = 0; it < k; ++it) {
+    small_mm(b, Q, E, Q, 2.f, nullptr, F);  // F = 2Q + Q E
+    __syncthreads();
+    float* t = E;
+    E = F;
+    F = t;
+  }
+  for (int e = threadIdx.x; e < bb; e += blockDim.x) {
+    const int i = e / b, j = e - (e / b) * b;
+    const float v = E[e] + (i == j ? 1.f : 0.f);
+    if (out32 != nullptr) out32[g * bb + e] = v;
+    if (out16 != nullptr) out16[g * bb + e] = __float2bfloat16_rn(v);
+  }
+}
+
+__global__ void __launch_bounds__(256) small_adjoint_kernel(
+    const float* __restrict__ theta_a, int n_a, const float* __restrict__ theta_b, int b, int k,
+    const float* __restrict__ G, float* __restrict__ dtheta_a, float* __restrict__ dtheta_b) {
+  pdl_wait();
+  pdl_trigger();
+  extern __shared__ float small_smem[];
+  const int bb = b * b;
+  const long long m = static_cast<long long>(b) * (b - 1) / 2;
+  float* Q = small_smem;
+  float* H = Q + bb;
+  float* P = H + bb;
+  float* Y = P + bb;
+  float* P2 = Y + bb;
+  float* Y2 = P2 + bb;
+  const int g = blockIdx.x;
+  const bool side_b = g >= n_a;
+  const long long lg = side_b ? g - n_a : g;
+  small_load_q((side_b ? theta_b : theta_a) + lg * m, b, Q);
+  const float* Gg = G + static_cast<long long>(g) * bb;
+  for (int e = threadIdx.x; e < bb; e += blockDim.x) {
+    const int i = e / b, j = e - (e / b) * b;
+    const float h = Gg[j * b + i];
+    H[e] = h;
+    P[e] = h;
+    Y[e] = h;
+  }
+  __syncthreads();
+  for (int it = 0; it < k; ++it) {
+    small_mm(b, P, Q, H, 2.f, nullptr, P2);  // P2 = 2H + P Q
+    __syncthreads();
+    small_mm(b, Q, Y, nullptr, 0.f, P2, Y2);  // Y2 = P2 + Q Y
+    __syncthreads();
+    float* t = P;
+    P = P2;
+    P2 = t;
+    t = Y;
+    Y = Y2;
+    Y2 = t;
+  }
+  float* out = (side_b ? dtheta_b : dtheta_a) + lg * m;
+  for (int e = threadIdx.x; e < bb; e += blockDim.x) {
+    const int i = e / b, j = e - (e / b) * b;
+    if (i < j) out[packed_pos(i, j, b)] = Y[j * b + i] - Y[i * b + j];
+  }
+}
+
 // Index arithmetic below is 32-bit: the host guarantees n * b * b < 2^31.
 // Blocks [0, n_a) come from theta_a, blocks [n_a, n_a + n_b) from theta_b.
 __global__ void unpack_kernel(const float* __restrict__ theta_a, int n_a,
@@ -865,6 +972,46 @@ cudaError_t launch_reduce_extract(const float* part, int splits, int n, int b, i
   const int total = n * b * b;
   POETX_EW_LAUNCH("reduce_extract", total, reduce_extract_kernel, part, splits, n, b, S, total,
                   o32, o16);
+}
+
+bool small_chain_fits(int b) { return b >= 1 && b <= kSmallMaxB; }
+
+cudaError_t launch_small_build(const float* theta, int n, int b, int k, float* out32,
+                               __nv_bfloat16* out16, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  if (!small_chain_fits(b)) return cudaErrorInvalidValue;
+  const size_t smem = 3ull * b * b * sizeof(float);  // at most 48 KiB
+  prof_begin("build", s);
+  cudaError_t e = launch_pdl(small_build_kernel, dim3(static_cast<unsigned>(n)), dim3(256), smem, s,
+                             theta, b, k, out32, out16);
+  prof_end("build", s);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+cudaError_t launch_small_adjoint(const float* theta_a, int n_a, const float* theta_b, int n_b,
+                                 int b, int k, const float* G, float* dtheta_a, float* dtheta_b,
+                                 cudaStream_t s) {
+  if (n_a + n_b <= 0) return cudaSuccess;
+  if (!small_chain_fits(b)) return cudaErrorInvalidValue;
+  const size_t smem = 6ull * b * b * sizeof(float);  // at most 96 KiB
+  static bool attr_set[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64) {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!attr_set[dev]) {
+      cudaFuncSetAttribute(small_adjoint_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           6 * kSmallMaxB * kSmallMaxB * static_cast<int>(sizeof(float)));
+      attr_set[dev] = true;
+    }
+  }
+  prof_begin("cnp_bwd", s);
+  cudaError_t e = launch_pdl(small_adjoint_kernel, dim3(static_cast<unsigned>(n_a + n_b)),
+                             dim3(256), smem, s, theta_a, n_a, theta_b, b, k, G, dtheta_a,
+                             dtheta_b);
+  prof_end("cnp_bwd", s);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_pack_skew(const float* A, const float* B, int n_a, int n_b, int b,
