@@ -86,12 +86,17 @@ __global__ void __launch_bounds__(SIMT_THREADS) simt_gemm_kernel(const SimtGemm 
     if (split == 0) {
       for (int r = 1; r < p.splits; ++r) {
         const uint32_t peer = map_peer(smem_u32(&Ps[0][0]), static_cast<uint32_t>(r));
+        float v[4][4];  // a peer's 16 values in flight at once, then added in order
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            acc[i][j] += ld_cluster_f32(
+            v[i][j] = ld_cluster_f32(
                 peer + 4u * static_cast<uint32_t>((ty * 4 + i) * (TN + 1) + tx * 4 + j));
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[i][j] += v[i][j];
       }
     }
     cluster_sync();  // no CTA leaves while rank 0 still reads its tile
