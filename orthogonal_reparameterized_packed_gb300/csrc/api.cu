@@ -624,7 +624,8 @@ CnpBufs carve_cnp(Carver& c, int n, int b, int k, bool is_bf16) {
 
 
 
-// The adjoint chain for blocks [0, n_a) (side a) and [n_a, n_a + n_b) (side b)
+// The adjoint (on CTA pairs, else the one-launch chain) for blocks [0, n_a)
+// (side a) and [n_a, n_a + n_b) (side b)
 // from the split-K partials of the transposed block gradients.
 cudaError_t chain_adjoint_from_parts(const float* theta_a, int n_a, const float* part_a,
                                      int splits_a, const float* theta_b, int n_b,
@@ -786,7 +787,8 @@ struct BwdPlan {
 };
 
 // The backward's transposed transforms and token sums run fused (one pass over
-// dy and one over du) on the chain path with 256 x 256 superblocks.
+// dy and one over du) wherever the adjoint reads split-K partials of 256 x 256
+// superblocks: the CTA-pair kernels and the one-launch chain up to b = 256.
 bool use_transform_sum(bool is_bf16, int n, int b, int k) {
   return (use_chain(is_bf16, n, b, k) && b <= 256) || use_pair_build(is_bf16, n, b, k);
 }
