@@ -254,7 +254,7 @@ cudaError_t launch_pack_tiles(const float* D, float sign, int n_a, int n_b, int 
                               float* dtheta_a, float* dtheta_b, cudaStream_t s);
 // out[r][i] = in[row_map ? row_map[r] : r][col_map[i]]; in has in_rows rows
 // of d elements, out has rows rows; d * elem_size multiple of 16 and
-// d * 8 bytes at most 200 KiB.  Out-of-range map entries give 0 and POETX_ERR_INVALID_ARG in the
+// d * 8 bytes at most 224 KiB.  Out-of-range map entries give 0 and POETX_ERR_INVALID_ARG in the
 // status word.
 cudaError_t launch_permute_rows(const void* in, long long in_rows, const int* row_map,
                                 const int* col_map, void* out, long long rows, int d,

@@ -534,26 +534,132 @@ __global__ void __launch_bounds__(256) pack_tiles_kernel(const float* __restrict
 
 // out[r][i] = in[row_map ? row_map[r] : r][col_map[i]] for r < rows, i < d.
 // A CTA takes groups of R rows (R = 8 bytes / element: 4 bf16 or 2 fp32
-// rows) in turn.  Its producer warps read a group's R source rows with
-// 16-byte coalesced loads (128 bytes per thread in flight)
-// and write them into a shared-memory table interleaved, one 8-byte entry
-// per column holding that column of all R rows; its consumer warps gather
-// 8-byte entries at the mapped columns, so one random shared-memory read
-// serves R outputs, and write each row's 16 bytes of consecutive outputs
-// with one 16-byte store.  With two tables (NBUF = 2, when 16 d bytes fit)
-// the producers fill one while the consumers drain the other, so the loads
-// of the next group run during this group's gather and stores; named
-// barriers hand the tables over (producers arrive, consumers wait, and back).
-// Table order: the entry of column c sits at (c % V) * (d / V) + c / V (V
-// columns per 16-byte vector), so a warp's stores of entries are consecutive
-// 8-byte words; bf16 entries and output words are assembled by byte
-// permutes.  A consumer serves the same vectors in every group and keeps
-// the table positions of its first KR vectors in registers.
-// Map entries outside [0, d) (or [0, in_rows)) are not followed: the output
-// gets 0 and the status word POETX_ERR_INVALID_ARG.
+// rows) in turn and writes them into a shared-memory table interleaved, one
+// 8-byte entry per column holding that column of all R rows; the gather
+// then reads 8-byte entries at the mapped columns, so one random
+// shared-memory read serves R outputs, and assembles each row's 16 bytes of
+// consecutive outputs.  Table order: the entry of column c sits at
+// (c % V) * (d / V) + c / V (V columns per 16-byte vector), so a warp's
+// stores of entries are consecutive 8-byte words; bf16 entries and output
+// words are assembled by byte permutes.  A thread serves the same output
+// vectors in every group and keeps the table positions of its first few
+// vectors in registers.  Map entries outside [0, d) (or [0, in_rows)) are
+// not followed: the output gets 0 and the status word POETX_ERR_INVALID_ARG.
+//
+// Two kernels move the rows:
+//  - permute_bulk_kernel (rows of up to 9556 features, where two staged
+//    groups and the table fit in shared memory): 1-D bulk copies bring a
+//    group's source rows into one of two stages two groups ahead, all
+//    threads interleave the stage into the table and gather the permuted
+//    rows back into the same stage, and one bulk store writes them out.  No
+//    thread waits on a global load, so the bytes in flight are not bounded
+//    by registers.
+//  - permute_rows_kernel (wider rows): producer warps read the source rows
+//    with 16-byte loads straight into the table, consumer warps gather and
+//    store with 16-byte stores; with two tables (NBUF = 2, when 16 d bytes
+//    fit) the producers fill one while the consumers drain the other, and
+//    named barriers hand the tables over.
 constexpr int kPermRoleThreads = 128;  // producers, and as many consumers
 constexpr int kPermThreads = 2 * kPermRoleThreads;
+constexpr int kPermBulkThreads = 256;
 constexpr size_t kPermSmemMax = 224 * 1024;
+
+// The source rows of the group of R rows starting at r0 (-1: none, the
+// output row is 0); returns whether a row-map entry was out of range.
+template <int R>
+__device__ __forceinline__ bool perm_group_sources(long long r0, long long rows,
+                                                   const int* __restrict__ row_map,
+                                                   long long in_rows, long long (&src)[R]) {
+  bool bad = false;
+#pragma unroll
+  for (int q = 0; q < R; ++q) {
+    const long long r = r0 + q;
+    src[q] = -1;
+    if (r < rows) {
+      src[q] = r;
+      if (row_map != nullptr) {
+        const int m = row_map[r];
+        src[q] = (m >= 0 && m < in_rows) ? m : -1;
+        bad |= src[q] < 0;
+      }
+    }
+  }
+  return bad;
+}
+
+// Table entries of 16-byte source vector v of the R rows (wd[q] = row q's
+// four words): column V v + e goes to position e * nv + v.
+template <typename T>
+__device__ __forceinline__ void perm_store_entries(uint2* ent, int nv, int v,
+                                                   const uint32_t (&wd)[8 / sizeof(T)][4]) {
+  constexpr int V = 16 / sizeof(T);
+#pragma unroll
+  for (int e = 0; e < V; ++e) {
+    uint2 entry;
+    if constexpr (sizeof(T) == 2) {  // column 8v + e: halves e % 2 of word e / 2
+      const uint32_t sel = (e & 1) ? 0x7632u : 0x5410u;
+      entry.x = __byte_perm(wd[0][e >> 1], wd[1][e >> 1], sel);
+      entry.y = __byte_perm(wd[2][e >> 1], wd[3][e >> 1], sel);
+    } else {
+      entry.x = wd[0][e];
+      entry.y = wd[1][e];
+    }
+    ent[e * nv + v] = entry;
+  }
+}
+
+// Table positions of the map entries of output vector v, two 16-bit
+// positions per word (0xffff: the entry is out of range, the output 0);
+// returns whether any entry was out of range.
+template <typename T>
+__device__ __forceinline__ bool perm_table_positions(const int* __restrict__ col_map, int v, int d,
+                                                     int nv, uint32_t (&pos)[8 / sizeof(T)]) {
+  constexpr int V = 16 / sizeof(T);
+  const int4* c4 = reinterpret_cast<const int4*>(col_map) + v * (V / 4);
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < V / 2; ++i) pos[i] = 0u;
+#pragma unroll
+  for (int qv = 0; qv < V / 4; ++qv) {
+    const int4 c = c4[qv];
+    const int cs[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int e = 4 * qv + t;
+      const bool ok = cs[t] >= 0 && cs[t] < d;
+      bad |= !ok;
+      const uint32_t at = ok ? static_cast<uint32_t>((cs[t] & (V - 1)) * nv + cs[t] / V) : 0xffffu;
+      pos[e >> 1] |= at << (16 * (e & 1));
+    }
+  }
+  return bad;
+}
+
+// Output vector of the R rows from the entries at the table positions pos:
+// o[q] = row q's four words.
+template <typename T>
+__device__ __forceinline__ void perm_gather(const uint2* ent, const uint32_t (&pos)[8 / sizeof(T)],
+                                            uint32_t (&o)[8 / sizeof(T)][4]) {
+  constexpr int V = 16 / sizeof(T);
+  uint2 u[V];
+#pragma unroll
+  for (int e = 0; e < V; ++e) {
+    const uint32_t at = (pos[e >> 1] >> (16 * (e & 1))) & 0xffffu;
+    u[e] = at != 0xffffu ? ent[at] : make_uint2(0u, 0u);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if constexpr (sizeof(T) == 2) {  // output word i: columns 2i, 2i + 1 of each row
+      o[0][i] = __byte_perm(u[2 * i].x, u[2 * i + 1].x, 0x5410u);
+      o[1][i] = __byte_perm(u[2 * i].x, u[2 * i + 1].x, 0x7632u);
+      o[2][i] = __byte_perm(u[2 * i].y, u[2 * i + 1].y, 0x5410u);
+      o[3][i] = __byte_perm(u[2 * i].y, u[2 * i + 1].y, 0x7632u);
+    } else {
+      o[0][i] = u[i].x;
+      o[1][i] = u[i].y;
+    }
+  }
+}
 
 template <typename T, int NBUF>
 __global__ void __launch_bounds__(kPermThreads, 3)
@@ -575,24 +681,6 @@ __global__ void __launch_bounds__(kPermThreads, 3)
   const long long count =
       blockIdx.x < groups ? (groups - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
 
-  // the source rows of a group (-1: none, the output row is zero)
-  auto sources = [&](long long r0, long long (&src)[R]) {
-    bool bad = false;
-#pragma unroll
-    for (int q = 0; q < R; ++q) {
-      const long long r = r0 + q;
-      src[q] = -1;
-      if (r < rows) {
-        src[q] = r;
-        if (row_map != nullptr) {
-          const int m = row_map[r];
-          src[q] = (m >= 0 && m < in_rows) ? m : -1;
-          bad |= src[q] < 0;
-        }
-      }
-    }
-    return bad;
-  };
   // named barriers 1 + b: table b is full; 1 + NBUF + b: table b is free
   // (immediate ids: a register id would reserve all sixteen barriers)
   auto bar_sync = [](int id) {
@@ -618,10 +706,10 @@ __global__ void __launch_bounds__(kPermThreads, 3)
       uint2* ent = reinterpret_cast<uint2*>(row_smem) + static_cast<size_t>(buf) * d;
       const long long r0 = (blockIdx.x + n * gridDim.x) * R;
       long long src[R];
-      if (sources(r0, src) && tid == 0) atomicCAS(status, 0, 1);
+      if (perm_group_sources<R>(r0, rows, row_map, in_rows, src) && tid == 0)
+        atomicCAS(status, 0, 1);
       if (n >= NBUF) bar_sync(1 + NBUF + buf);  // the consumers are done with this table
-      // interleave: the entry of column c holds column c of the R rows
-      // (missing rows: 0); bf16: (r0 | r1 << 16, r2 | r3 << 16), fp32: (r0, r1)
+      // interleave (missing rows: 0), U vectors of each row in flight
       for (int v0 = tid; v0 < nv; v0 += U * kPermRoleThreads) {
         uint4 w[U][R];
 #pragma unroll
@@ -645,48 +733,12 @@ __global__ void __launch_bounds__(kPermThreads, 3)
             wd[q][2] = w[k][q].z;
             wd[q][3] = w[k][q].w;
           }
-#pragma unroll
-          for (int e = 0; e < V; ++e) {
-            uint2 entry;
-            if constexpr (sizeof(T) == 2) {  // column 8v + e: halves e % 2 of word e / 2
-              const uint32_t sel = (e & 1) ? 0x7632u : 0x5410u;
-              entry.x = __byte_perm(wd[0][e >> 1], wd[1][e >> 1], sel);
-              entry.y = __byte_perm(wd[2][e >> 1], wd[3][e >> 1], sel);
-            } else {
-              entry.x = wd[0][e];
-              entry.y = wd[1][e];
-            }
-            ent[e * nv + v] = entry;
-          }
+          perm_store_entries<T>(ent, nv, v, wd);
         }
       }
       bar_arrive(1 + buf);  // table full
     }
   } else {
-    // table positions of the map entries of output vector v, two 16-bit
-    // positions per word (0xffff: the entry is out of range, the output 0);
-    // returns whether any entry was out of range
-    auto table_positions = [&](int v, uint32_t (&pos)[V / 2]) {
-      const int4* c4 = reinterpret_cast<const int4*>(col_map) + v * (V / 4);
-      bool bad = false;
-#pragma unroll
-      for (int i = 0; i < V / 2; ++i) pos[i] = 0u;
-#pragma unroll
-      for (int qv = 0; qv < V / 4; ++qv) {
-        const int4 c = c4[qv];
-        const int cs[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const int e = 4 * qv + t;
-          const bool ok = cs[t] >= 0 && cs[t] < d;
-          bad |= !ok;
-          const uint32_t at =
-              ok ? static_cast<uint32_t>((cs[t] & (V - 1)) * nv + cs[t] / V) : 0xffffu;
-          pos[e >> 1] |= at << (16 * (e & 1));
-        }
-      }
-      return bad;
-    };
     uint32_t pos_r[KR][V / 2];
     bool bad_cols = false;
 #pragma unroll
@@ -694,7 +746,7 @@ __global__ void __launch_bounds__(kPermThreads, 3)
       const int v = tid + k * kPermRoleThreads;
 #pragma unroll
       for (int i = 0; i < V / 2; ++i) pos_r[k][i] = 0xffffffffu;
-      if (v < nv) bad_cols |= table_positions(v, pos_r[k]);
+      if (v < nv) bad_cols |= perm_table_positions<T>(col_map, v, d, nv, pos_r[k]);
     }
     if (bad_cols && count > 0) atomicCAS(status, 0, 1);
     for (long long n = 0; n < count; ++n) {
@@ -702,30 +754,11 @@ __global__ void __launch_bounds__(kPermThreads, 3)
       const uint2* ent = reinterpret_cast<const uint2*>(row_smem) + static_cast<size_t>(buf) * d;
       const long long r0 = (blockIdx.x + n * gridDim.x) * R;
       long long src[R];
-      sources(r0, src);
+      perm_group_sources<R>(r0, rows, row_map, in_rows, src);
       bar_sync(1 + buf);  // the producers have filled this table
-      // out[r0 + q][V v .. V v + V - 1] from the entries at the table
-      // positions of those columns' map entries
       auto gather_store = [&](int v, const uint32_t (&pos)[V / 2]) {
-        uint2 u[V];
-#pragma unroll
-        for (int e = 0; e < V; ++e) {
-          const uint32_t at = (pos[e >> 1] >> (16 * (e & 1))) & 0xffffu;
-          u[e] = at != 0xffffu ? ent[at] : make_uint2(0u, 0u);
-        }
         uint32_t o[R][4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          if constexpr (sizeof(T) == 2) {  // output word i: columns 2i, 2i + 1 of each row
-            o[0][i] = __byte_perm(u[2 * i].x, u[2 * i + 1].x, 0x5410u);
-            o[1][i] = __byte_perm(u[2 * i].x, u[2 * i + 1].x, 0x7632u);
-            o[2][i] = __byte_perm(u[2 * i].y, u[2 * i + 1].y, 0x5410u);
-            o[3][i] = __byte_perm(u[2 * i].y, u[2 * i + 1].y, 0x7632u);
-          } else {
-            o[0][i] = u[i].x;
-            o[1][i] = u[i].y;
-          }
-        }
+        perm_gather<T>(ent, pos, o);
 #pragma unroll
         for (int q = 0; q < R; ++q) {
           if (r0 + q < rows) {
@@ -742,11 +775,156 @@ __global__ void __launch_bounds__(kPermThreads, 3)
       }
       for (int v = tid + KR * kPermRoleThreads; v < nv; v += kPermRoleThreads) {
         uint32_t pos[V / 2];
-        if (table_positions(v, pos)) atomicCAS(status, 0, 1);
+        if (perm_table_positions<T>(col_map, v, d, nv, pos)) atomicCAS(status, 0, 1);
         gather_store(v, pos);
       }
       if (n + NBUF < count) bar_arrive(1 + NBUF + buf);  // table free for group n + NBUF
     }
+  }
+}
+
+// Shared memory of permute_bulk_kernel: two stages and the table (8 d bytes
+// each), two mbarriers and the abort flag.
+__host__ __device__ constexpr size_t perm_bulk_smem(int d) {
+  return 3 * static_cast<size_t>(d) * 8 + 32;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kPermBulkThreads, 2)
+    permute_bulk_kernel(const T* __restrict__ in, long long in_rows,
+                        const int* __restrict__ row_map, const int* __restrict__ col_map,
+                        T* __restrict__ out, long long rows, int d, int* status) {
+  pdl_wait();
+  pdl_trigger();
+  extern __shared__ __align__(16) unsigned char bulk_smem[];
+  constexpr int V = 16 / sizeof(T);
+  constexpr int R = 8 / sizeof(T);
+  constexpr int KR = 2;  // vectors whose table positions a thread keeps in registers
+  const int nv = d / V;
+  const int tid = threadIdx.x;
+  const uint32_t row_bytes = static_cast<uint32_t>(d) * static_cast<uint32_t>(sizeof(T));
+  const size_t tile = static_cast<size_t>(R) * row_bytes;  // one group: 8 d bytes
+  uint2* ent = reinterpret_cast<uint2*>(bulk_smem + 2 * tile);
+  uint64_t* full = reinterpret_cast<uint64_t*>(bulk_smem + 3 * tile);  // one per stage
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(full + 2);
+  const long long groups = (rows + R - 1) / R;
+  const long long count =
+      blockIdx.x < groups ? (groups - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  // group n of this CTA: rows first_row(n) ..; stage n % 2, whose barrier
+  // completes its (n / 2)-th phase when the group's rows have landed
+  auto first_row = [&](long long n) { return (blockIdx.x + n * gridDim.x) * R; };
+  auto stage = [&](long long n) { return bulk_smem + static_cast<size_t>(n & 1) * tile; };
+  auto issue = [&](long long n) {  // thread 0: copy group n's source rows into its stage
+    long long src[R];
+    perm_group_sources<R>(first_row(n), rows, row_map, in_rows, src);
+    uint32_t bytes = 0;
+#pragma unroll
+    for (int q = 0; q < R; ++q) bytes += src[q] >= 0 ? row_bytes : 0u;
+    uint64_t* bar = &full[n & 1];
+    mbar_arrive_expect_tx(bar, bytes);
+#pragma unroll
+    for (int q = 0; q < R; ++q)
+      if (src[q] >= 0) bulk_load_1d(stage(n) + q * row_bytes, in + src[q] * d, row_bytes, bar);
+  };
+
+  if (tid == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  long long issued = 0;  // thread 0: groups whose copies are issued
+  if (tid == 0)
+    for (; issued < 2 && issued < count; ++issued) issue(issued);
+
+  uint32_t pos_r[KR][V / 2];
+  bool bad_cols = false;
+#pragma unroll
+  for (int k = 0; k < KR; ++k) {
+    const int v = tid + k * kPermBulkThreads;
+#pragma unroll
+    for (int i = 0; i < V / 2; ++i) pos_r[k][i] = 0xffffffffu;
+    if (v < nv) bad_cols |= perm_table_positions<T>(col_map, v, d, nv, pos_r[k]);
+  }
+  if (bad_cols && count > 0) atomicCAS(status, 0, 1);
+
+  long long n = 0;
+  bool ok = true;
+  for (; n < count; ++n) {
+    unsigned char* st = stage(n);
+    const long long r0 = first_row(n);
+    long long src[R];
+    if (perm_group_sources<R>(r0, rows, row_map, in_rows, src) && tid == 0)
+      atomicCAS(status, 0, 1);
+    const bool got = mbar_wait(&full[n & 1], static_cast<uint32_t>((n >> 1) & 1), abort_flag);
+    if (!got) *abort_flag = 1;
+    if (!__syncthreads_and(got)) {
+      ok = false;
+      break;
+    }
+    // interleave the staged rows into the table (rows without a source: 0)
+    for (int v = tid; v < nv; v += kPermBulkThreads) {
+      uint32_t wd[R][4];
+#pragma unroll
+      for (int q = 0; q < R; ++q) {
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (src[q] >= 0) w = *reinterpret_cast<const uint4*>(st + q * row_bytes + v * 16);
+        wd[q][0] = w.x;
+        wd[q][1] = w.y;
+        wd[q][2] = w.z;
+        wd[q][3] = w.w;
+      }
+      perm_store_entries<T>(ent, nv, v, wd);
+    }
+    __syncthreads();
+    // gather the permuted rows back into the stage (row q at q * row_bytes)
+    auto gather = [&](int v, const uint32_t (&pos)[V / 2]) {
+      uint32_t o[R][4];
+      perm_gather<T>(ent, pos, o);
+#pragma unroll
+      for (int q = 0; q < R; ++q)
+        if (r0 + q < rows)
+          *reinterpret_cast<uint4*>(st + q * row_bytes + v * 16) =
+              make_uint4(o[q][0], o[q][1], o[q][2], o[q][3]);
+    };
+#pragma unroll
+    for (int k = 0; k < KR; ++k) {
+      const int v = tid + k * kPermBulkThreads;
+      if (v < nv) gather(v, pos_r[k]);
+    }
+    for (int v = tid + KR * kPermBulkThreads; v < nv; v += kPermBulkThreads) {
+      uint32_t pos[V / 2];
+      if (perm_table_positions<T>(col_map, v, d, nv, pos)) atomicCAS(status, 0, 1);
+      gather(v, pos);
+    }
+    fence_proxy_async_shared();
+    __syncthreads();
+    if (tid == 0) {
+      // the group's rows are consecutive in out: one store
+      const long long left = rows - r0;
+      const uint32_t nrows = left < R ? static_cast<uint32_t>(left) : static_cast<uint32_t>(R);
+      bulk_store_1d(out + r0 * d, st, nrows * row_bytes);
+      bulk_commit();
+      if (issued < count) {  // group n + 2 goes to this stage
+        bulk_wait_read_all();
+        issue(issued);
+        ++issued;
+      }
+    }
+  }
+  if (tid == 0) {
+    if (!ok) {
+      atomicCAS(status, 0, 5);  // POETX_ERR_TIMEOUT
+      // let the copies still in flight land before the CTA exits
+      for (long long m = n; m < issued; ++m) {
+        const unsigned long long t0 = global_timer_ns();
+        while (!mbar_try_wait(&full[m & 1], static_cast<uint32_t>((m >> 1) & 1)) &&
+               global_timer_ns() - t0 < 10000000ull) {
+        }
+      }
+    }
+    bulk_wait_all();
   }
 }
 
@@ -1048,14 +1226,16 @@ cudaError_t launch_pack_tiles(const float* D, float sign, int n_a, int n_b, int 
 }
 
 namespace {
-template <typename T, int NBUF>
-cudaError_t permute_rows_launch(const void* in, long long in_rows, const int* row_map,
-                                const int* col_map, void* out, long long rows, int d,
-                                cudaStream_t s) {
+// One launch of an index-map kernel with as many CTAs as fit at once (the
+// maximum shared-memory carveout, set once per device and kernel: one
+// instance of this function per kernel).
+template <typename T, auto kernel>
+cudaError_t permute_launch(int threads, size_t smem, const void* in, long long in_rows,
+                           const int* row_map, const int* col_map, void* out, long long rows,
+                           int d, cudaStream_t s) {
   constexpr int R = 8 / sizeof(T);
-  const size_t smem = static_cast<size_t>(NBUF) * d * 8;  // one 8-byte entry per column
   const long long groups = (rows + R - 1) / R;
-  const void* fn = reinterpret_cast<const void*>(permute_rows_kernel<T, NBUF>);
+  const void* fn = reinterpret_cast<const void*>(kernel);
   static bool attr_set[64] = {};
   static std::mutex mu;
   int dev = 0;
@@ -1070,17 +1250,29 @@ cudaError_t permute_rows_launch(const void* in, long long in_rows, const int* ro
       attr_set[dev] = true;
     }
   }
-  // as many CTAs as fit at once
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kPermThreads, smem) !=
-          cudaSuccess ||
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem) != cudaSuccess ||
       per_sm < 1)
     per_sm = 1;
   const long long cap = static_cast<long long>(sm_count()) * per_sm;
   const dim3 grid(static_cast<unsigned>(groups < cap ? groups : cap));
-  return launch_pdl(permute_rows_kernel<T, NBUF>, grid, dim3(kPermThreads), smem, s,
-                    static_cast<const T*>(in), in_rows, row_map, col_map, static_cast<T*>(out),
-                    rows, d, device_status_ptr());
+  return launch_pdl(kernel, grid, dim3(threads), smem, s, static_cast<const T*>(in), in_rows,
+                    row_map, col_map, static_cast<T*>(out), rows, d, device_status_ptr());
+}
+
+template <typename T>
+cudaError_t permute_dispatch(const void* in, long long in_rows, const int* row_map,
+                             const int* col_map, void* out, long long rows, int d,
+                             cudaStream_t s) {
+  const size_t table = static_cast<size_t>(d) * 8;  // one 8-byte entry per column
+  if (perm_bulk_smem(d) <= kPermSmemMax)
+    return permute_launch<T, permute_bulk_kernel<T>>(kPermBulkThreads, perm_bulk_smem(d), in,
+                                                      in_rows, row_map, col_map, out, rows, d, s);
+  if (2 * table <= kPermSmemMax)  // two tables: loads overlap the gather
+    return permute_launch<T, permute_rows_kernel<T, 2>>(kPermThreads, 2 * table, in, in_rows,
+                                                         row_map, col_map, out, rows, d, s);
+  return permute_launch<T, permute_rows_kernel<T, 1>>(kPermThreads, table, in, in_rows, row_map,
+                                                       col_map, out, rows, d, s);
 }
 }  // namespace
 
@@ -1088,17 +1280,11 @@ cudaError_t launch_permute_rows(const void* in, long long in_rows, const int* ro
                                 const int* col_map, void* out, long long rows, int d,
                                 bool is_bf16, cudaStream_t s) {
   if (rows <= 0 || d <= 0) return cudaSuccess;
-  const size_t table = static_cast<size_t>(d) * 8;
-  if (table > kPermSmemMax) return cudaErrorInvalidValue;
-  const bool two = 2 * table <= kPermSmemMax;  // two tables: loads overlap the gather
-  cudaError_t e;
+  if (static_cast<size_t>(d) * 8 > kPermSmemMax) return cudaErrorInvalidValue;
   prof_begin("permute", s);
-  if (is_bf16)
-    e = two ? permute_rows_launch<__nv_bfloat16, 2>(in, in_rows, row_map, col_map, out, rows, d, s)
-            : permute_rows_launch<__nv_bfloat16, 1>(in, in_rows, row_map, col_map, out, rows, d, s);
-  else
-    e = two ? permute_rows_launch<float, 2>(in, in_rows, row_map, col_map, out, rows, d, s)
-            : permute_rows_launch<float, 1>(in, in_rows, row_map, col_map, out, rows, d, s);
+  const cudaError_t e =
+      is_bf16 ? permute_dispatch<__nv_bfloat16>(in, in_rows, row_map, col_map, out, rows, d, s)
+              : permute_dispatch<float>(in, in_rows, row_map, col_map, out, rows, d, s);
   prof_end("permute", s);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -56,11 +56,14 @@ def test_index_maps_are_exact(px, dtype):
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
-@pytest.mark.parametrize("d,T", [(8, 5), (14336, 11), (14344, 6), (28672, 9)],
-                         ids=["tiny", "staged-max", "unstaged", "max"])
-def test_index_maps_at_both_table_forms(px, d, T, dtype):
-    """Rows whose table and staged copy fit shared memory (d <= 14336) are
-    copied in by bulk copies; wider rows are read straight into the table."""
+@pytest.mark.parametrize("d,T", [(8, 5), (9552, 13), (9560, 7), (14336, 11), (14344, 6),
+                                 (28672, 9)],
+                         ids=["tiny", "bulk-max", "two-tables", "two-tables-max", "one-table",
+                              "max"])
+def test_index_maps_at_every_kernel_form(px, d, T, dtype):
+    """Rows whose two staged groups and table fit shared memory (d <= 9556)
+    move by bulk copies; wider rows are read straight into one or two
+    tables by producer warps."""
     if dtype == "f32" and d % 4:
         pytest.skip("rows must be a multiple of 16 bytes")
     rng = np.random.default_rng(d + T)
@@ -80,6 +83,21 @@ def test_index_maps_at_both_table_forms(px, d, T, dtype):
     assert px.poetx_device_status() == 0
     assert torch.equal(out, x[:, perm.long()])
     assert torch.equal(Wf, W[po.long()][:, perm.long()])
+
+
+@pytest.mark.parametrize("d", [256, 14336], ids=["bulk", "two-tables"])
+def test_out_of_range_row_map_entries_give_zero_rows(px, d):
+    rows = 6
+    W = torch.randn((rows, d), device="cuda").to(torch.bfloat16)
+    po = np.array([3, -1, 0, 6, 5, 1], dtype=np.int32)  # -1 and 6: out of range
+    perm = torch.arange(d, dtype=torch.int32, device="cuda").flip(0).contiguous()
+    Wf = torch.full_like(W, 7.0)
+    px.poetx_fold_permutations(W, torch.from_numpy(po).cuda(), perm, Wf, d, rows, px.BF16)
+    torch.cuda.synchronize()
+    assert px.poetx_device_status() == 1  # POETX_ERR_INVALID_ARG recorded
+    for i, r in enumerate(po):
+        want = W[r].flip(0) if 0 <= r < rows else torch.zeros_like(W[0])
+        assert torch.equal(Wf[i], want), i
 
 
 def test_out_of_range_map_entries_are_not_followed(px):
