@@ -549,11 +549,11 @@ __global__ void __launch_bounds__(256) pack_tiles_kernel(const float* __restrict
 // Two kernels move the rows:
 //  - permute_bulk_kernel (rows of up to 9556 features, where two staged
 //    groups and the table fit in shared memory): 1-D bulk copies bring a
-//    group's source rows into one of two stages two groups ahead, all
-//    threads interleave the stage into the table and gather the permuted
-//    rows back into the same stage, and one bulk store writes them out.  No
-//    thread waits on a global load, so the bytes in flight are not bounded
-//    by registers.
+//    group's source rows into one of two stages, all threads interleave the
+//    stage into the table (after which the stage takes the copies of the
+//    group two ahead), then gather and write the permuted rows with 16-byte
+//    stores.  No thread waits on a global load, so the bytes in flight are
+//    not bounded by registers.
 //  - permute_rows_kernel (wider rows): producer warps read the source rows
 //    with 16-byte loads straight into the table, consumer warps gather and
 //    store with 16-byte stores; with two tables (NBUF = 2, when 16 d bytes
@@ -561,7 +561,7 @@ __global__ void __launch_bounds__(256) pack_tiles_kernel(const float* __restrict
 //    named barriers hand the tables over.
 constexpr int kPermRoleThreads = 128;  // producers, and as many consumers
 constexpr int kPermThreads = 2 * kPermRoleThreads;
-constexpr int kPermBulkThreads = 256;
+constexpr int kPermBulkThreads = 512;
 constexpr size_t kPermSmemMax = 224 * 1024;
 
 // The source rows of the group of R rows starting at r0 (-1: none, the
@@ -799,7 +799,7 @@ __global__ void __launch_bounds__(kPermBulkThreads, 2)
   extern __shared__ __align__(16) unsigned char bulk_smem[];
   constexpr int V = 16 / sizeof(T);
   constexpr int R = 8 / sizeof(T);
-  constexpr int KR = 2;  // vectors whose table positions a thread keeps in registers
+  constexpr int KR = 1;  // vectors whose table positions a thread keeps in registers
   const int nv = d / V;
   const int tid = threadIdx.x;
   const uint32_t row_bytes = static_cast<uint32_t>(d) * static_cast<uint32_t>(sizeof(T));
@@ -877,15 +877,20 @@ __global__ void __launch_bounds__(kPermBulkThreads, 2)
       }
       perm_store_entries<T>(ent, nv, v, wd);
     }
+    // the stage has been read: the copies of group n + 2 go to it
+    fence_proxy_async_shared();
     __syncthreads();
-    // gather the permuted rows back into the stage (row q at q * row_bytes)
+    if (tid == 0 && issued < count) {
+      issue(issued);
+      ++issued;
+    }
     auto gather = [&](int v, const uint32_t (&pos)[V / 2]) {
       uint32_t o[R][4];
       perm_gather<T>(ent, pos, o);
 #pragma unroll
       for (int q = 0; q < R; ++q)
         if (r0 + q < rows)
-          *reinterpret_cast<uint4*>(st + q * row_bytes + v * 16) =
+          reinterpret_cast<uint4*>(out + (r0 + q) * d)[v] =
               make_uint4(o[q][0], o[q][1], o[q][2], o[q][3]);
     };
 #pragma unroll
@@ -898,20 +903,7 @@ __global__ void __launch_bounds__(kPermBulkThreads, 2)
       if (perm_table_positions<T>(col_map, v, d, nv, pos)) atomicCAS(status, 0, 1);
       gather(v, pos);
     }
-    fence_proxy_async_shared();
-    __syncthreads();
-    if (tid == 0) {
-      // the group's rows are consecutive in out: one store
-      const long long left = rows - r0;
-      const uint32_t nrows = left < R ? static_cast<uint32_t>(left) : static_cast<uint32_t>(R);
-      bulk_store_1d(out + r0 * d, st, nrows * row_bytes);
-      bulk_commit();
-      if (issued < count) {  // group n + 2 goes to this stage
-        bulk_wait_read_all();
-        issue(issued);
-        ++issued;
-      }
-    }
+    __syncthreads();  // the table is free
   }
   if (tid == 0) {
     if (!ok) {
@@ -924,7 +916,6 @@ __global__ void __launch_bounds__(kPermBulkThreads, 2)
         }
       }
     }
-    bulk_wait_all();
   }
 }
 

@@ -113,15 +113,6 @@ __device__ __forceinline__ void bulk_load_1d(void* smem_dst, const void* src, ui
       : "memory");
 }
 
-// 1-D bulk copy of `bytes` (a multiple of 16; both addresses 16-byte
-// aligned) from this CTA's shared memory to global memory; completion is
-// tracked by bulk groups (bulk_commit / bulk_wait_*).
-__device__ __forceinline__ void bulk_store_1d(void* dst, const void* smem_src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
-               "r"(smem_u32(smem_src)), "r"(bytes)
-               : "memory");
-}
-
 // Order this thread's generic-proxy writes to global memory before later
 // async-proxy (TMA) reads of it.
 __device__ __forceinline__ void fence_proxy_async_global() {
