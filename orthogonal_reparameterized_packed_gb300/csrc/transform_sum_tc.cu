@@ -378,15 +378,33 @@ __global__ void __launch_bounds__(TS_THREADS, 1)
 
 }  // namespace
 
+// Token splits: one CTA per (block, half, split) and one CTA per SM, so the
+// launch runs in ceil(CTAs / SMs) waves of `per` token tiles each.  The
+// split count minimises waves x (per + 3), the 3 standing for a CTA's fixed
+// cost in tile times (the pipeline fill, the resident block half in, the
+// partial sum out); more splits are taken only for a gain of over 5 %
+// (they add partial sums to add up).  One wave where one fits (d = 4096,
+// 16384 tokens: 4 splits, 128 CTAs); wide sides take several (d = 14336:
+// 4 splits in 3 waves instead of 112 CTAs over the whole run).
 int transform_sum_splits(int d, long long T) {
   const int m_tiles = static_cast<int>((T + BM - 1) / BM);
   const int units = 2 * (d / 256);
-  int splits = sm_count() / (units > 0 ? units : 1);
-  if (splits < 1) splits = 1;
-  if (splits > m_tiles) splits = m_tiles;
-  if (splits < 1) splits = 1;
-  const int per = (m_tiles + splits - 1) / splits;
-  return (m_tiles + per - 1) / per;  // no empty split
+  if (m_tiles <= 1 || units <= 0) return 1;
+  const long long sms = sm_count();
+  int best = 1;
+  long long best_cost = -1;
+  const int max_splits = static_cast<int>(std::min<long long>(m_tiles, 2 * sms));
+  for (int s = 1; s <= max_splits; ++s) {
+    const int per = (m_tiles + s - 1) / s;
+    if ((m_tiles + per - 1) / per != s) continue;  // no empty split
+    const long long waves = (static_cast<long long>(units) * s + sms - 1) / sms;
+    const long long cost = waves * (per + 3);
+    if (best_cost < 0 || cost * 20 < best_cost * 19) {
+      best = s;
+      best_cost = cost;
+    }
+  }
+  return best;
 }
 
 cudaError_t tc_transform_sum(const __nv_bfloat16* X, const __nv_bfloat16* Z,
