@@ -137,6 +137,7 @@ def test_build_blocks_matches_oracle(px, dtype, d, b, k):
 TRANSFORM_CASES = [
     ("bf16", 1024, 32, 5, 300), ("bf16", 1024, 64, 3, 300), ("bf16", 1024, 128, 1, 300),
     ("bf16", 1024, 256, 3, 300), ("bf16", 1024, 512, 3, 300), ("bf16", 512, 256, 0, 129),
+    ("bf16", 1536, 512, 1, 37), ("bf16", 2048, 512, 5, 513),  # 512-blocks on CTA pairs
     ("f32", 256, 32, 3, 300), ("f32", 96, 3, 2, 50),
 ]
 
