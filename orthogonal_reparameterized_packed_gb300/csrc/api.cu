@@ -840,6 +840,9 @@ cudaError_t block_gradient(const void* dout, const void* in, int d, int b, long 
     return launch_reduce_extract(part, splits, n, b, S, g32, tc_small(true, b) ? g16 : nullptr,
                                  s);
   }
+  if (small_chain_fits(b))  // small blocks: one cluster per block
+    return launch_small_outer(static_cast<const float*>(dout), static_cast<const float*>(in), g32,
+                              d, b, T, s);
   return simt_outer(static_cast<const float*>(dout), static_cast<const float*>(in), g32, d, b, T,
                     s);
 }

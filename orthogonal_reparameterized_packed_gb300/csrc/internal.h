@@ -221,6 +221,10 @@ cudaError_t launch_reduce_extract(const float* part, int splits, int n, int b, i
 // memory (fp32 arithmetic): the whole build, or the whole adjoint of both
 // sides (G = dL/dR per block, [n_a + n_b][b][b] fp32), in one launch.
 bool small_chain_fits(int b);
+// G[g] = sum_t A[t][g-block]^T B[t][g-block] for fp32 blocks of b <= 64
+// (small_chain_fits), [d/b][b][b].
+cudaError_t launch_small_outer(const float* A, const float* B, float* G, int d, int b, long long T,
+                               cudaStream_t s);
 cudaError_t launch_small_build(const float* theta, int n, int b, int k, float* out32,
                                __nv_bfloat16* out16, cudaStream_t s);
 cudaError_t launch_small_adjoint(const float* theta_a, int n_a, const float* theta_b, int n_b,

@@ -235,6 +235,93 @@ __global__ void __launch_bounds__(256) small_adjoint_kernel(
   }
 }
 
+// Token sums of fp32 blocks of b <= 64: G[g][m][n] = sum_t A[t][g b + m] B[t][g b + n]
+// for the d / b blocks g (one side's block gradients).  One cluster of
+// `splits` CTAs per block, each CTA a contiguous token range staged 64
+// tokens at a time in shared memory (a token's b-wide pieces of A and B are
+// consecutive words); the CTAs' partial b x b sums meet in rank 0's shared
+// memory and are added in rank order (a fixed summation order, no scratch,
+// no atomics).
+constexpr int kOuterTC = 64;                                    // tokens per staged chunk
+constexpr int kOuterPer = kSmallMaxB * kSmallMaxB / 256;        // outputs per thread
+
+__global__ void __launch_bounds__(256) small_outer_kernel(const float* __restrict__ A,
+                                                          const float* __restrict__ B,
+                                                          float* __restrict__ G, int d, int b,
+                                                          long long T, int splits) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ float As[kOuterTC][kSmallMaxB];
+  __shared__ float Bs[kOuterTC][kSmallMaxB];
+  __shared__ float Ps[kSmallMaxB * kSmallMaxB];  // this CTA's partial sums (splits > 1)
+  const int g = blockIdx.y;
+  const int split = blockIdx.x;  // the rank in the block's cluster
+  const long long per = (T + splits - 1) / splits;
+  const long long t0 = split * per;
+  const long long t1 = t0 + per < T ? t0 + per : T;
+  const int bb = b * b;
+  const long long col0 = static_cast<long long>(g) * b;
+  float acc[kOuterPer];
+#pragma unroll
+  for (int i = 0; i < kOuterPer; ++i) acc[i] = 0.f;
+  for (long long c = t0; c < t1; c += kOuterTC) {
+    const long long left = t1 - c;
+    const int nt = left < kOuterTC ? static_cast<int>(left) : kOuterTC;
+    for (int e = threadIdx.x; e < kOuterTC * b; e += blockDim.x) {
+      const int tt = e / b, j = e - tt * b;
+      float av = 0.f, bv = 0.f;  // tokens past the range: zeros, which add nothing
+      if (tt < nt) {
+        const long long off = (c + tt) * d + col0 + j;
+        av = A[off];
+        bv = B[off];
+      }
+      As[tt][j] = av;
+      Bs[tt][j] = bv;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kOuterPer; ++i) {
+      const int o = threadIdx.x + i * 256;
+      if (o < bb) {
+        const int m = o / b, n = o - m * b;
+        float s = acc[i];
+#pragma unroll 8
+        for (int tt = 0; tt < kOuterTC; ++tt) s = fmaf(As[tt][m], Bs[tt][n], s);
+        acc[i] = s;
+      }
+    }
+    __syncthreads();
+  }
+  if (splits > 1) {
+#pragma unroll
+    for (int i = 0; i < kOuterPer; ++i) {
+      const int o = threadIdx.x + i * 256;
+      if (o < bb) Ps[o] = acc[i];
+    }
+    cluster_sync();  // every CTA's partial sums are in its shared memory
+    if (split == 0) {
+      for (int r = 1; r < splits; ++r) {
+        const uint32_t peer = map_peer(smem_u32(Ps), static_cast<uint32_t>(r));
+        float v[kOuterPer];  // a peer's values in flight at once, then added in order
+#pragma unroll
+        for (int i = 0; i < kOuterPer; ++i) {
+          const int o = threadIdx.x + i * 256;
+          v[i] = o < bb ? ld_cluster_f32(peer + 4u * static_cast<uint32_t>(o)) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < kOuterPer; ++i) acc[i] += v[i];
+      }
+    }
+    cluster_sync();  // no CTA leaves while rank 0 still reads its partial sums
+    if (split != 0) return;
+  }
+#pragma unroll
+  for (int i = 0; i < kOuterPer; ++i) {
+    const int o = threadIdx.x + i * 256;
+    if (o < bb) G[static_cast<long long>(g) * bb + o] = acc[i];
+  }
+}
+
 // Index arithmetic below is 32-bit: the host guarantees n * b * b < 2^31.
 // Blocks [0, n_a) come from theta_a, blocks [n_a, n_a + n_b) from theta_b.
 __global__ void unpack_kernel(const float* __restrict__ theta_a, int n_a,
@@ -1149,6 +1236,37 @@ cudaError_t launch_reduce_extract(const float* part, int splits, int n, int b, i
 }
 
 bool small_chain_fits(int b) { return b >= 1 && b <= kSmallMaxB; }
+
+cudaError_t launch_small_outer(const float* A, const float* B, float* G, int d, int b, long long T,
+                               cudaStream_t s) {
+  const int n = d / b;
+  if (n <= 0) return cudaSuccess;
+  if (!small_chain_fits(b) || n > 65535) return cudaErrorInvalidValue;
+  // a cluster of up to 8 CTAs per block, a chunk of tokens at least each,
+  // until about two CTAs per SM work
+  int splits = 1;
+  while (splits < 8 && static_cast<long long>(n) * splits * 2 <= 2LL * sm_count() &&
+         T >= static_cast<long long>(splits) * 2 * kOuterTC)
+    splits *= 2;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(splits), static_cast<unsigned>(n), 1);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(splits);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = splits > 1 ? 2 : 1;
+  prof_begin("outer", s);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, small_outer_kernel, A, B, G, d, b, T, splits);
+  prof_end("outer", s);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
 
 cudaError_t launch_small_build(const float* theta, int n, int b, int k, float* out32,
                                __nv_bfloat16* out16, cudaStream_t s) {

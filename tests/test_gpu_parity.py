@@ -222,6 +222,7 @@ LAYER_CASES = [
     (256, 512, 128, 9, 64, "bf16"),      # k above the one-launch chain limit
     (512, 256, 256, 16, 40, "bf16"),     # the largest k
     (64, 32, 8, 16, 20, "f32"),
+    (256, 256, 64, 3, 300, "f32"),      # fp32 token sums split over 4 CTAs, ragged ranges
     (512, 256, 256, 0, 70, "bf16"),
     # the CTA-pair adjoint for k != 3 (Horner form), every block size
     (512, 256, 32, 5, 100, "bf16"),
