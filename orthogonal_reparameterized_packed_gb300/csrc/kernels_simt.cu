@@ -13,7 +13,7 @@ namespace poetx {
 
 namespace {
 
-constexpr int TM = 64, TN = 64, TK = 16, SIMT_THREADS = 256;
+constexpr int TM = 64, TN = 64, TK = 32, SIMT_THREADS = 256;
 
 template <typename T>
 __device__ __forceinline__ float load_f(const T* p, long long i);
@@ -26,7 +26,9 @@ __device__ __forceinline__ float load_f<__nv_bfloat16>(const __nv_bfloat16* p, l
   return __bfloat162float(p[i]);
 }
 
-// C(g) = A(g) * B(g), 64x64 output tile per CTA, 4x4 per thread.  With
+// C(g) = A(g) * B(g), 64x64 output tile per CTA, 4x4 per thread, K in steps
+// of 32 staged in shared memory; each thread loads its share of the next
+// step's operands into registers while the current step's FMAs run.  With
 // p.splits > 1 the K range is cut into that many slices, one per CTA of a
 // cluster along x (the tile's N index is blockIdx.x / splits); the slices'
 // partial tiles meet in rank 0's shared memory in rank order (a fixed
@@ -51,18 +53,38 @@ __global__ void __launch_bounds__(SIMT_THREADS) simt_gemm_kernel(const SimtGemm 
   const int tx = threadIdx.x % 16;  // n direction
   const int ty = threadIdx.x / 16;  // m direction
   float acc[4][4] = {};
-  for (int k0 = k_begin; k0 < k_end; k0 += TK) {
-    for (int e = threadIdx.x; e < TM * TK; e += SIMT_THREADS) {
+  constexpr int PA = TM * TK / SIMT_THREADS, PB = TN * TK / SIMT_THREADS;
+  float ra[PA], rb[PB];  // the next K step's operands, loaded during this step's FMAs
+  auto fetch = [&](int k0) {
+#pragma unroll
+    for (int q = 0; q < PA; ++q) {
+      const int e = threadIdx.x + q * SIMT_THREADS;
       const int mm = e / TK, kk = e % TK;
       const int m = m0 + mm, k = k0 + kk;
-      As[kk][mm] = (m < p.M && k < k_end) ? load_f(A, m * p.a_m + k * p.a_k) : 0.f;
+      ra[q] = (m < p.M && k < k_end) ? load_f(A, m * p.a_m + k * p.a_k) : 0.f;
     }
-    for (int e = threadIdx.x; e < TN * TK; e += SIMT_THREADS) {
+#pragma unroll
+    for (int q = 0; q < PB; ++q) {
+      const int e = threadIdx.x + q * SIMT_THREADS;
       const int nn = e % TN, kk = e / TN;
       const int n = n0 + nn, k = k0 + kk;
-      Bs[kk][nn] = (n < p.N && k < k_end) ? load_f(B, k * p.b_k + n * p.b_n) : 0.f;
+      rb[q] = (n < p.N && k < k_end) ? load_f(B, k * p.b_k + n * p.b_n) : 0.f;
+    }
+  };
+  if (k_begin < k_end) fetch(k_begin);
+  for (int k0 = k_begin; k0 < k_end; k0 += TK) {
+#pragma unroll
+    for (int q = 0; q < PA; ++q) {
+      const int e = threadIdx.x + q * SIMT_THREADS;
+      As[e % TK][e / TK] = ra[q];
+    }
+#pragma unroll
+    for (int q = 0; q < PB; ++q) {
+      const int e = threadIdx.x + q * SIMT_THREADS;
+      Bs[e / TN][e % TN] = rb[q];
     }
     __syncthreads();
+    if (k0 + TK < k_end) fetch(k0 + TK);
 #pragma unroll
     for (int kk = 0; kk < TK; ++kk) {
       float a[4], b[4];
@@ -1167,11 +1189,11 @@ cudaError_t simt_gemm_run(const SimtGemm& g_in, cudaStream_t stream) {
   const int tiles_n = (g.N + TN - 1) / TN, tiles_m = (g.M + TM - 1) / TM;
   if (tiles_m > 65535) return cudaErrorInvalidValue;
   // Small grids with long K: split K over a cluster of up to 8 CTAs per tile
-  // (slices of at least four TK steps) until about two CTAs per SM work.
+  // (slices of at least 64 K elements) until about two CTAs per SM work.
   const long long tiles = static_cast<long long>(tiles_n) * tiles_m * g.batches;
   int splits = 1;
   const long long want = 2LL * sm_count();
-  while (splits < 8 && tiles * splits * 2 <= want && g.K >= 2 * splits * 4 * TK) splits *= 2;
+  while (splits < 8 && tiles * splits * 2 <= want && g.K >= 2 * splits * 4 * 16) splits *= 2;
   g.splits = splits;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(tiles_n * splits), static_cast<unsigned>(tiles_m),
