@@ -167,10 +167,46 @@ __device__ __forceinline__ void small_load_q(const float* th, int b, float* Q) {
   }
 }
 
-// out = add + scale_add * X + L R  (b x b, row-major; X and add may alias nothing written here)
+// out = xs X + Y + L R  (b x b, row-major; X, Y may be null; none of them
+// aliases out).  When blockDim.x is a multiple of b and the b x b outputs
+// are PER times blockDim.x, a thread's outputs (e, e + blockDim.x, ..) share
+// one column j: R[t][j] is loaded once per t for all PER of them.  Every
+// output is the same fmaf sum over t = 0 .. b-1 either way.
+template <int PER>
+__device__ __forceinline__ void small_mm_cols(int b, const float* L, const float* R,
+                                              const float* X, float xs, const float* Y,
+                                              float* out) {
+  const int j = threadIdx.x % b, i0 = threadIdx.x / b, di = blockDim.x / b;
+  float acc[PER];
+#pragma unroll
+  for (int r = 0; r < PER; ++r) acc[r] = 0.f;
+  for (int t = 0; t < b; ++t) {
+    const float rv = R[t * b + j];
+#pragma unroll
+    for (int r = 0; r < PER; ++r) acc[r] = fmaf(L[(i0 + r * di) * b + t], rv, acc[r]);
+  }
+#pragma unroll
+  for (int r = 0; r < PER; ++r) {
+    const int e = (i0 + r * di) * b + j;
+    float v = acc[r];
+    if (X != nullptr) v = xs * X[e] + v;
+    if (Y != nullptr) v = Y[e] + v;
+    out[e] = v;
+  }
+}
+
 __device__ __forceinline__ void small_mm(int b, const float* L, const float* R, const float* X,
-                                              float xs, const float* Y, float* out) {
-  for (int e = threadIdx.x; e < b * b; e += blockDim.x) {
+                                         float xs, const float* Y, float* out) {
+  const int bb = b * b, nt = blockDim.x;
+  if (nt % b == 0 && bb % nt == 0) {
+    switch (bb / nt) {
+      case 1: return small_mm_cols<1>(b, L, R, X, xs, Y, out);
+      case 4: return small_mm_cols<4>(b, L, R, X, xs, Y, out);
+      case 16: return small_mm_cols<16>(b, L, R, X, xs, Y, out);
+      default: break;
+    }
+  }
+  for (int e = threadIdx.x; e < bb; e += nt) {
     const int i = e / b, j = e - (e / b) * b;
     float acc = 0.f;
     for (int t = 0; t < b; ++t) acc = fmaf(L[i * b + t], R[t * b + j], acc);
@@ -301,15 +337,34 @@ __global__ void __launch_bounds__(256) small_outer_kernel(const float* __restric
       Bs[tt][j] = bv;
     }
     __syncthreads();
+    // a thread's outputs share column n when 256 % b == 0: Bs[tt][n] loaded
+    // once per token for all of them
+    auto cols = [&](auto per_c) {
+      constexpr int PER = decltype(per_c)::value;
+      const int n = threadIdx.x % b, m0 = threadIdx.x / b, dm = 256 / b;
+      for (int tt = 0; tt < kOuterTC; ++tt) {
+        const float bv = Bs[tt][n];
 #pragma unroll
-    for (int i = 0; i < kOuterPer; ++i) {
-      const int o = threadIdx.x + i * 256;
-      if (o < bb) {
-        const int m = o / b, n = o - m * b;
-        float s = acc[i];
+        for (int i = 0; i < PER; ++i) acc[i] = fmaf(As[tt][m0 + i * dm], bv, acc[i]);
+      }
+    };
+    if (bb == 4096) {
+      cols(std::integral_constant<int, 16>{});
+    } else if (bb == 1024) {
+      cols(std::integral_constant<int, 4>{});
+    } else if (bb == 256) {
+      cols(std::integral_constant<int, 1>{});
+    } else {
+#pragma unroll
+      for (int i = 0; i < kOuterPer; ++i) {
+        const int o = threadIdx.x + i * 256;
+        if (o < bb) {
+          const int m = o / b, n = o - m * b;
+          float s = acc[i];
 #pragma unroll 8
-        for (int tt = 0; tt < kOuterTC; ++tt) s = fmaf(As[tt][m], Bs[tt][n], s);
-        acc[i] = s;
+          for (int tt = 0; tt < kOuterTC; ++tt) s = fmaf(As[tt][m], Bs[tt][n], s);
+          acc[i] = s;
+        }
       }
     }
     __syncthreads();
