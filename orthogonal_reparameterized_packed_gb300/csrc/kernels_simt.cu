@@ -30,10 +30,11 @@ __device__ __forceinline__ float load_f<__nv_bfloat16>(const __nv_bfloat16* p, l
 // of 32 staged in shared memory; each thread loads its share of the next
 // step's operands into registers while the current step's FMAs run.  With
 // p.splits > 1 the K range is cut into that many slices, one per CTA of a
-// cluster along x (the tile's N index is blockIdx.x / splits); the slices'
-// partial tiles meet in rank 0's shared memory in rank order (a fixed
-// summation order: results do not depend on timing), and rank 0 applies the
-// epilogue.  No global scratch, no atomics.
+// cluster along x (the tile's N index is blockIdx.x / splits); each rank
+// finalises a share of the tile's 4 x 4 outputs, reading the other slices'
+// partial values from their shared memory and adding them in rank order (a
+// fixed summation order: results do not depend on timing or on which rank
+// adds), and applies the epilogue to them.  No global scratch, no atomics.
 template <typename T>
 __global__ void __launch_bounds__(SIMT_THREADS) simt_gemm_kernel(const SimtGemm p) {
   pdl_wait();
@@ -99,14 +100,28 @@ __global__ void __launch_bounds__(SIMT_THREADS) simt_gemm_kernel(const SimtGemm 
     }
     __syncthreads();
   }
+  bool mine = true;  // this thread finalises its 4 x 4 outputs
   if (p.splits > 1) {
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) Ps[ty * 4 + i][tx * 4 + j] = acc[i][j];
     cluster_sync();  // every slice's partial tile is in its CTA's shared memory
-    if (split == 0) {
-      for (int r = 1; r < p.splits; ++r) {
+    // rank s finalises the rows of 4 x 4 outputs with ty % splits == s: the
+    // sum starts from rank 0's partial values and adds ranks 1, 2, .. in
+    // order, whichever rank does it
+    mine = ty % p.splits == split;
+    if (mine) {
+      for (int r = 0; r < p.splits; ++r) {
+        if (r == split) {
+          if (r > 0) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+              for (int j = 0; j < 4; ++j) acc[i][j] = Ps[ty * 4 + i][tx * 4 + j] + acc[i][j];
+          }
+          continue;
+        }
         const uint32_t peer = map_peer(smem_u32(&Ps[0][0]), static_cast<uint32_t>(r));
         float v[4][4];  // a peer's 16 values in flight at once, then added in order
 #pragma unroll
@@ -115,14 +130,21 @@ __global__ void __launch_bounds__(SIMT_THREADS) simt_gemm_kernel(const SimtGemm 
           for (int j = 0; j < 4; ++j)
             v[i][j] = ld_cluster_f32(
                 peer + 4u * static_cast<uint32_t>((ty * 4 + i) * (TN + 1) + tx * 4 + j));
+        if (r == 0) {
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+          for (int i = 0; i < 4; ++i)
 #pragma unroll
-          for (int j = 0; j < 4; ++j) acc[i][j] += v[i][j];
+            for (int j = 0; j < 4; ++j) acc[i][j] = v[i][j];  // the sum starts from rank 0's
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[i][j] += v[i][j];
+        }
       }
     }
-    cluster_sync();  // no CTA leaves while rank 0 still reads its tile
-    if (split != 0) return;
+    cluster_sync();  // no CTA leaves while a peer still reads its tile
+    if (!mine) return;
   }
   const EpiArgs& e = p.epi;
 #pragma unroll
@@ -1244,11 +1266,11 @@ cudaError_t simt_gemm_run(const SimtGemm& g_in, cudaStream_t stream) {
   const int tiles_n = (g.N + TN - 1) / TN, tiles_m = (g.M + TM - 1) / TM;
   if (tiles_m > 65535) return cudaErrorInvalidValue;
   // Small grids with long K: split K over a cluster of up to 8 CTAs per tile
-  // (slices of at least 64 K elements) until about two CTAs per SM work.
+  // (slices of at least one K step) until about two CTAs per SM work.
   const long long tiles = static_cast<long long>(tiles_n) * tiles_m * g.batches;
   int splits = 1;
   const long long want = 2LL * sm_count();
-  while (splits < 8 && tiles * splits * 2 <= want && g.K >= 2 * splits * 4 * 16) splits *= 2;
+  while (splits < 8 && tiles * splits * 2 <= want && g.K >= 2 * splits * 32) splits *= 2;
   g.splits = splits;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(tiles_n * splits), static_cast<unsigned>(tiles_m),
