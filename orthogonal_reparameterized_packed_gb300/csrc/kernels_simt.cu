@@ -31,10 +31,10 @@ __device__ __forceinline__ float load_f<__nv_bfloat16>(const __nv_bfloat16* p, l
 // step's operands into registers while the current step's FMAs run.  With
 // p.splits > 1 the K range is cut into that many slices, one per CTA of a
 // cluster along x (the tile's N index is blockIdx.x / splits); each rank
-// finalises a share of the tile's 4 x 4 outputs, reading the other slices'
-// partial values from their shared memory and adding them in rank order (a
-// fixed summation order: results do not depend on timing or on which rank
-// adds), and applies the epilogue to them.  No global scratch, no atomics.
+// finalises a contiguous share of the tile's entries, loading all slices'
+// partial values of an entry at once and adding them in rank order (a fixed
+// summation order: results do not depend on timing or on which rank adds),
+// and applies the epilogue to them.  No global scratch, no atomics.
 template <typename T>
 __global__ void __launch_bounds__(SIMT_THREADS) simt_gemm_kernel(const SimtGemm p) {
   pdl_wait();
@@ -100,71 +100,54 @@ __global__ void __launch_bounds__(SIMT_THREADS) simt_gemm_kernel(const SimtGemm 
     }
     __syncthreads();
   }
-  bool mine = true;  // this thread finalises its 4 x 4 outputs
+  const EpiArgs& e = p.epi;
+  auto store = [&](int mm, int nn, float acc_v) {  // the epilogue of tile entry (mm, nn)
+    const int m = m0 + mm, n = n0 + nn;
+    if (m >= p.M || m >= e.row_limit || n >= p.N) return;
+    const long long off =
+        (static_cast<long long>(g) * e.row_g + m) * e.ld + static_cast<long long>(g) * e.col_g + n;
+    float v = e.alpha * acc_v;
+    if (e.X != nullptr) v += e.beta * e.X[off];
+    if (e.Y != nullptr) v += e.gamma * e.Y[off];
+    if (m == n) v += e.delta;
+    if (e.out_f32 != nullptr) e.out_f32[off] = v;
+    if (e.out_bf16 != nullptr) e.out_bf16[off] = __float2bfloat16_rn(v);
+  };
   if (p.splits > 1) {
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
       for (int j = 0; j < 4; ++j) Ps[ty * 4 + i][tx * 4 + j] = acc[i][j];
     cluster_sync();  // every slice's partial tile is in its CTA's shared memory
-    // rank s finalises the rows of 4 x 4 outputs with ty % splits == s: the
-    // sum starts from rank 0's partial values and adds ranks 1, 2, .. in
-    // order, whichever rank does it
-    mine = ty % p.splits == split;
-    if (mine) {
-      for (int r = 0; r < p.splits; ++r) {
-        if (r == split) {
-          if (r > 0) {
+    // rank s finalises tile entries [s chunk, (s + 1) chunk): all slices'
+    // values of an entry are loaded at once, then added from rank 0 upwards
+    // in order (the same sum whichever rank does it)
+    const int chunk = TM * TN / p.splits;
+    for (int idx = split * chunk + threadIdx.x; idx < (split + 1) * chunk; idx += SIMT_THREADS) {
+      const int mm = idx / TN, nn = idx % TN;
+      const uint32_t at = 4u * static_cast<uint32_t>(mm * (TN + 1) + nn);
+      float v[8];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-              for (int j = 0; j < 4; ++j) acc[i][j] = Ps[ty * 4 + i][tx * 4 + j] + acc[i][j];
-          }
-          continue;
-        }
-        const uint32_t peer = map_peer(smem_u32(&Ps[0][0]), static_cast<uint32_t>(r));
-        float v[4][4];  // a peer's 16 values in flight at once, then added in order
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            v[i][j] = ld_cluster_f32(
-                peer + 4u * static_cast<uint32_t>((ty * 4 + i) * (TN + 1) + tx * 4 + j));
-        if (r == 0) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) acc[i][j] = v[i][j];  // the sum starts from rank 0's
-        } else {
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) acc[i][j] += v[i][j];
-        }
+      for (int r = 0; r < 8; ++r) {
+        v[r] = 0.f;
+        if (r < p.splits)
+          v[r] = r == split ? Ps[mm][nn]
+                            : ld_cluster_f32(map_peer(smem_u32(&Ps[0][0]),
+                                                      static_cast<uint32_t>(r)) + at);
       }
+      float s = v[0];
+#pragma unroll
+      for (int r = 1; r < 8; ++r)
+        if (r < p.splits) s += v[r];
+      store(mm, nn, s);
     }
     cluster_sync();  // no CTA leaves while a peer still reads its tile
-    if (!mine) return;
+    return;
   }
-  const EpiArgs& e = p.epi;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int m = m0 + ty * 4 + i;
-    if (m >= p.M || m >= e.row_limit) continue;
+  for (int i = 0; i < 4; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int n = n0 + tx * 4 + j;
-      if (n >= p.N) continue;
-      const long long off =
-          (static_cast<long long>(g) * e.row_g + m) * e.ld + static_cast<long long>(g) * e.col_g + n;
-      float v = e.alpha * acc[i][j];
-      if (e.X != nullptr) v += e.beta * e.X[off];
-      if (e.Y != nullptr) v += e.gamma * e.Y[off];
-      if (m == n) v += e.delta;
-      if (e.out_f32 != nullptr) e.out_f32[off] = v;
-      if (e.out_bf16 != nullptr) e.out_bf16[off] = __float2bfloat16_rn(v);
-    }
-  }
+    for (int j = 0; j < 4; ++j) store(ty * 4 + i, tx * 4 + j, acc[i][j]);
 }
 
 // Position of Q[i][j] (i < j) in the row-by-row packed strict upper triangle.
@@ -319,9 +302,9 @@ __global__ void __launch_bounds__(256) small_adjoint_kernel(
 // for the d / b blocks g (one side's block gradients).  One cluster of
 // `splits` CTAs per block, each CTA a contiguous token range staged 64
 // tokens at a time in shared memory (a token's b-wide pieces of A and B are
-// consecutive words); the CTAs' partial b x b sums meet in rank 0's shared
-// memory and are added in rank order (a fixed summation order, no scratch,
-// no atomics).
+// consecutive words); each rank then finalises a share of the b x b sums,
+// adding the CTAs' partial values in rank order (a fixed summation order,
+// no scratch, no atomics).
 constexpr int kOuterTC = 64;                                    // tokens per staged chunk
 constexpr int kOuterPer = kSmallMaxB * kSmallMaxB / 256;        // outputs per thread
 
@@ -398,21 +381,28 @@ __global__ void __launch_bounds__(256) small_outer_kernel(const float* __restric
       if (o < bb) Ps[o] = acc[i];
     }
     cluster_sync();  // every CTA's partial sums are in its shared memory
-    if (split == 0) {
-      for (int r = 1; r < splits; ++r) {
-        const uint32_t peer = map_peer(smem_u32(Ps), static_cast<uint32_t>(r));
-        float v[kOuterPer];  // a peer's values in flight at once, then added in order
+    // rank s finalises outputs [s chunk, (s + 1) chunk): all ranks' values of
+    // an output are loaded at once, then added from rank 0 upwards in order
+    const int chunk = (bb + splits - 1) / splits;
+    const int o_end = min(bb, (split + 1) * chunk);
+    for (int o = split * chunk + threadIdx.x; o < o_end; o += blockDim.x) {
+      float v[8];
 #pragma unroll
-        for (int i = 0; i < kOuterPer; ++i) {
-          const int o = threadIdx.x + i * 256;
-          v[i] = o < bb ? ld_cluster_f32(peer + 4u * static_cast<uint32_t>(o)) : 0.f;
-        }
-#pragma unroll
-        for (int i = 0; i < kOuterPer; ++i) acc[i] += v[i];
+      for (int r = 0; r < 8; ++r) {
+        v[r] = 0.f;
+        if (r < splits)
+          v[r] = r == split ? Ps[o]
+                            : ld_cluster_f32(map_peer(smem_u32(Ps), static_cast<uint32_t>(r)) +
+                                             4u * static_cast<uint32_t>(o));
       }
+      float s = v[0];
+#pragma unroll
+      for (int r = 1; r < 8; ++r)
+        if (r < splits) s += v[r];
+      G[static_cast<long long>(g) * bb + o] = s;
     }
-    cluster_sync();  // no CTA leaves while rank 0 still reads its partial sums
-    if (split != 0) return;
+    cluster_sync();  // no CTA leaves while a peer still reads its partial sums
+    return;
   }
 #pragma unroll
   for (int i = 0; i < kOuterPer; ++i) {
