@@ -165,8 +165,33 @@ __device__ __forceinline__ int packed_pos(int i, int j, int b) {
 // of H: both recursions run forward and no power of Q is kept).
 constexpr int kSmallMaxB = 64;
 
+// Q from the packed strict upper triangle th.  With b x b = PER x blockDim.x
+// (PER = 1, 4, 16), a thread's PER entries are loaded before any of them is
+// stored; otherwise one entry at a time.
+template <int PER>
+__device__ __forceinline__ void small_load_q_per(const float* th, int b, float* Q) {
+  float v[PER];
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int e = threadIdx.x + u * blockDim.x;
+    const int i = e / b, j = e - (e / b) * b;
+    v[u] = i < j ? th[packed_pos(i, j, b)] : (i > j ? -th[packed_pos(j, i, b)] : 0.f);
+  }
+#pragma unroll
+  for (int u = 0; u < PER; ++u) Q[threadIdx.x + u * blockDim.x] = v[u];
+}
+
 __device__ __forceinline__ void small_load_q(const float* th, int b, float* Q) {
-  for (int e = threadIdx.x; e < b * b; e += blockDim.x) {
+  const int bb = b * b;
+  if (bb % blockDim.x == 0) {
+    switch (bb / blockDim.x) {
+      case 1: return small_load_q_per<1>(th, b, Q);
+      case 4: return small_load_q_per<4>(th, b, Q);
+      case 16: return small_load_q_per<16>(th, b, Q);
+      default: break;
+    }
+  }
+  for (int e = threadIdx.x; e < bb; e += blockDim.x) {
     const int i = e / b, j = e - (e / b) * b;
     Q[e] = i < j ? th[packed_pos(i, j, b)] : (i > j ? -th[packed_pos(j, i, b)] : 0.f);
   }
@@ -271,12 +296,37 @@ __global__ void __launch_bounds__(256) small_adjoint_kernel(
   const long long lg = side_b ? g - n_a : g;
   small_load_q((side_b ? theta_b : theta_a) + lg * m, b, Q);
   const float* Gg = G + static_cast<long long>(g) * bb;
-  for (int e = threadIdx.x; e < bb; e += blockDim.x) {
-    const int i = e / b, j = e - (e / b) * b;
-    const float h = Gg[j * b + i];
-    H[e] = h;
-    P[e] = h;
-    Y[e] = h;
+  // H = G^T (and the first P and Y); a thread's PER entries loaded before
+  // any is stored when b x b = PER x blockDim.x
+  auto load_h = [&](auto per_c) {
+    constexpr int PER = decltype(per_c)::value;
+    float v[PER];
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int e = threadIdx.x + u * blockDim.x;
+      const int i = e / b, j = e - (e / b) * b;
+      v[u] = Gg[j * b + i];
+    }
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+      const int e = threadIdx.x + u * blockDim.x;
+      H[e] = v[u];
+      P[e] = v[u];
+      Y[e] = v[u];
+    }
+  };
+  if (bb == 4 * static_cast<int>(blockDim.x)) {
+    load_h(std::integral_constant<int, 4>{});
+  } else if (bb == 16 * static_cast<int>(blockDim.x)) {
+    load_h(std::integral_constant<int, 16>{});
+  } else {
+    for (int e = threadIdx.x; e < bb; e += blockDim.x) {
+      const int i = e / b, j = e - (e / b) * b;
+      const float h = Gg[j * b + i];
+      H[e] = h;
+      P[e] = h;
+      Y[e] = h;
+    }
   }
   __syncthreads();
   for (int it = 0; it < k; ++it) {
@@ -330,16 +380,52 @@ __global__ void __launch_bounds__(256) small_outer_kernel(const float* __restric
   for (long long c = t0; c < t1; c += kOuterTC) {
     const long long left = t1 - c;
     const int nt = left < kOuterTC ? static_cast<int>(left) : kOuterTC;
-    for (int e = threadIdx.x; e < kOuterTC * b; e += blockDim.x) {
-      const int tt = e / b, j = e - tt * b;
-      float av = 0.f, bv = 0.f;  // tokens past the range: zeros, which add nothing
-      if (tt < nt) {
-        const long long off = (c + tt) * d + col0 + j;
-        av = A[off];
-        bv = B[off];
+    if ((b & 3) == 0) {
+      // 16-byte pieces (b, d and the block offset are multiples of 4 floats;
+      // the activations are 16-byte aligned): every load of the thread is
+      // issued before any of them is stored (at most 4 pieces per operand)
+      const int q4 = b >> 2, total = kOuterTC * q4;
+      float4 av[4], bv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = threadIdx.x + u * 256;
+        av[u] = bv[u] = make_float4(0.f, 0.f, 0.f, 0.f);  // tokens past the range: zeros
+        if (e < total) {
+          const int tt = e / q4, j4 = e - tt * q4;
+          if (tt < nt) {
+            const long long off = (c + tt) * d + col0 + 4 * j4;
+            av[u] = *reinterpret_cast<const float4*>(A + off);
+            bv[u] = *reinterpret_cast<const float4*>(B + off);
+          }
+        }
       }
-      As[tt][j] = av;
-      Bs[tt][j] = bv;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = threadIdx.x + u * 256;
+        if (e < total) {
+          const int tt = e / q4, j = 4 * (e - tt * q4);
+          As[tt][j] = av[u].x;
+          As[tt][j + 1] = av[u].y;
+          As[tt][j + 2] = av[u].z;
+          As[tt][j + 3] = av[u].w;
+          Bs[tt][j] = bv[u].x;
+          Bs[tt][j + 1] = bv[u].y;
+          Bs[tt][j + 2] = bv[u].z;
+          Bs[tt][j + 3] = bv[u].w;
+        }
+      }
+    } else {
+      for (int e = threadIdx.x; e < kOuterTC * b; e += blockDim.x) {
+        const int tt = e / b, j = e - tt * b;
+        float av = 0.f, bv = 0.f;  // tokens past the range: zeros, which add nothing
+        if (tt < nt) {
+          const long long off = (c + tt) * d + col0 + j;
+          av = A[off];
+          bv = B[off];
+        }
+        As[tt][j] = av;
+        Bs[tt][j] = bv;
+      }
     }
     __syncthreads();
     // a thread's outputs share column n when 256 % b == 0: Bs[tt][n] loaded
