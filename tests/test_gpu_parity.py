@@ -139,6 +139,7 @@ TRANSFORM_CASES = [
     ("bf16", 1024, 256, 3, 300), ("bf16", 1024, 512, 3, 300), ("bf16", 512, 256, 0, 129),
     ("bf16", 1536, 512, 1, 37), ("bf16", 2048, 512, 5, 513),  # 512-blocks on CTA pairs
     ("f32", 256, 32, 3, 300), ("f32", 96, 3, 2, 50),
+    ("f32", 256, 32, 3, 37),  # fp32 token sums over one partial 64-token chunk
 ]
 
 

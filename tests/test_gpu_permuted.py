@@ -85,6 +85,23 @@ def test_index_maps_at_every_kernel_form(px, d, T, dtype):
     assert torch.equal(Wf, W[po.long()][:, perm.long()])
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("T", [1, 2, 3, 6])
+def test_index_maps_over_fewer_rows_than_a_group(px, T, dtype):
+    """A group is four bf16 (two fp32) rows; shorter and ragged row counts."""
+    rng = np.random.default_rng(T)
+    d = 4096
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    code = px.BF16 if dtype == "bf16" else px.F32
+    x = torch.randn((T, d), device="cuda").to(tdt)
+    perm = torch.from_numpy(rng.permutation(d).astype(np.int32)).cuda()
+    out = torch.full_like(x, 7.0)
+    px.poetx_permute_features(x, perm, out, T, d, code)
+    torch.cuda.synchronize()
+    assert px.poetx_device_status() == 0
+    assert torch.equal(out, x[:, perm.long()])
+
+
 @pytest.mark.parametrize("d", [256, 14336], ids=["bulk", "two-tables"])
 def test_out_of_range_row_map_entries_give_zero_rows(px, d):
     rows = 6
