@@ -431,6 +431,9 @@ def algorithmic_work(tag, w):
         return 2.0 * T * do * (di + b) / 1e12, "TFLOP", "tensor", "2*T*d_out*(d_in+b)"
     if tag == "gemm_w0_dgrad_p":  # du = dv W0 with dx = du P in the epilogue
         return 2.0 * T * di * (do + b) / 1e12, "TFLOP", "tensor", "2*T*d_in*(d_out+b)"
+    if tag in ("gemm_w0_fused", "gemm_w0_dgrad_fused"):  # both block factors and W0, one launch
+        return (2.0 * T * (di * b + di * do + do * b) / 1e12, "TFLOP", "tensor",
+                "2*T*(d_in*b+d_in*d_out+d_out*b)")
     return None
 
 
@@ -678,7 +681,8 @@ def run_gpu(args):
 
     # per-kernel times over the timed region
     tags = ["build", "unpack", "identity_plus", "expand_superblocks", "transform",
-            "transform_t", "gemm_w0", "gemm_w0_dgrad", "gemm_w0_r", "gemm_w0_dgrad_p", "outer", "reduce_extract", "cnp_bwd",
+            "transform_t", "gemm_w0", "gemm_w0_dgrad", "gemm_w0_r", "gemm_w0_dgrad_p",
+            "gemm_w0_fused", "gemm_w0_dgrad_fused", "outer", "reduce_extract", "cnp_bwd",
             "pack_skew", "f32_to_bf16", "chain", "prep_tiles", "pack_tiles", "permute", "adam",
             "transform_sum", "cnp_build", "cnp_sums", "cnp_adjoint",
             "dequantize", "quantize"]

@@ -1016,6 +1016,13 @@ poetx_status poetx_forward(const void* x, const void* W0, const void* P_blocks,
                                  static_cast<const bf16*>(rsb), static_cast<bf16*>(v_saved),
                                  static_cast<bf16*>(y), d_in, d_out, tokens, false, s));
   }
+  if (!is_bf16 && simt_fused_fits(b))  // u = P x on the fly, v = W0 u, y = R v: one launch
+    return to_status(simt_fused_run(static_cast<const float*>(x), static_cast<const float*>(psb),
+                                    false, static_cast<const float*>(W0), 1, d_in,
+                                    static_cast<const float*>(rsb), false,
+                                    static_cast<float*>(v_saved), static_cast<float*>(y),
+                                    static_cast<int>(tokens), d_out, d_in, b, "gemm_w0_fused",
+                                    s));
   void* v = v_saved != nullptr ? v_saved : p.sb.v;
   e = run_forward_uv(x, W0, psb, p.sb.u, v, d_in, d_out, b, tokens, is_bf16, s);
   if (e != cudaSuccess) return POETX_ERR_CUDA;
@@ -1079,8 +1086,15 @@ poetx_status poetx_backward(const void* dy, const void* x, const void* W0, const
   const void* rsb = superblocks_or_blocks(R_blocks, p.sb.rsb, d_out, b, is_bf16, s, &e);
   if (e != cudaSuccess) return POETX_ERR_CUDA;
   const void* v = v_saved;
+  const bool fused32 = !is_bf16 && simt_fused_fits(b);  // fp32: the factors fused into W0's GEMMs
   if (recompute) {
-    e = run_forward_uv(x, W0, psb, p.sb.u, p.sb.v, d_in, d_out, b, tokens, is_bf16, s);
+    if (fused32)  // v = W0 (P x), u formed on the fly
+      e = simt_fused_run(static_cast<const float*>(x), static_cast<const float*>(psb), false,
+                         static_cast<const float*>(W0), 1, d_in, nullptr, false,
+                         static_cast<float*>(p.sb.v), nullptr, static_cast<int>(tokens), d_out,
+                         d_in, b, "gemm_w0_fused", s);
+    else
+      e = run_forward_uv(x, W0, psb, p.sb.u, p.sb.v, d_in, d_out, b, tokens, is_bf16, s);
     if (e != cudaSuccess) return POETX_ERR_CUDA;
     v = p.sb.v;
   }
@@ -1116,6 +1130,23 @@ poetx_status poetx_backward(const void* dy, const void* x, const void* W0, const
     return to_status(chain_adjoint_from_parts(theta_P, d_in / b, p.sb.part, p.splits_in,
                                               theta_R, d_out / b, p.part_out, p.splits_out, b, k,
                                               p.cnp, dtheta_P, dtheta_R, s));
+  }
+  if (fused32) {
+    // dv = dy R on the fly, du = dv W0 (kept for G_P) and dx = du P in one
+    // launch; then G_R = sum_t dy_t v_t^T and G_P = sum_t du_t x_t^T
+    e = simt_fused_run(static_cast<const float*>(dy), static_cast<const float*>(rsb), true,
+                       static_cast<const float*>(W0), d_in, 1, static_cast<const float*>(psb), true,
+                       static_cast<float*>(p.sb.du), static_cast<float*>(dx),
+                       static_cast<int>(tokens), d_in, d_out, b, "gemm_w0_dgrad_fused", s);
+    if (e != cudaSuccess) return POETX_ERR_CUDA;
+    e = block_gradient(dy, v, d_out, b, tokens, is_bf16, p.sb.part, p.splits_out,
+                       p.cnp.g32[0] + off_R, p.cnp.g16[0] ? p.cnp.g16[0] + off_R : nullptr, s);
+    if (e != cudaSuccess) return POETX_ERR_CUDA;
+    e = block_gradient(p.sb.du, x, d_in, b, tokens, is_bf16, p.sb.part, p.splits_in,
+                       p.cnp.g32[0], p.cnp.g16[0], s);
+    if (e != cudaSuccess) return POETX_ERR_CUDA;
+    return to_status(run_cnp_backward(theta_P, d_in / b, theta_R, d_out / b, b, k, is_bf16,
+                                      p.cnp, dtheta_P, dtheta_R, s));
   }
   // R side: dv = dy R, G_R = sum_t dy_t v_t^T
   if (is_bf16)

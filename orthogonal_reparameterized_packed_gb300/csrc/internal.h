@@ -124,6 +124,17 @@ struct SimtGemm {
   const char* tag = "simt_gemm";
 };
 cudaError_t simt_gemm_run(const SimtGemm& g, cudaStream_t stream);
+// The fp32 W0 product with block-diagonal factors on both sides in one
+// launch (simt_fused_fits(b): b divides 32, or b = 64):
+//   C = A W^T-style product with A[t][k] = sum_j X[t][g b + j] L_g(k % b, j),
+//   out[t][n] = sum_j C[t][g b + j] R_g(n % b, j); L_g(kl, j) = L_g[kl][j]
+//   (or L_g[j][kl] when l_trans), likewise R; B(k, n) = W[k w_k + n w_n].
+// C (if not null) is stored; R null: no right factor (out unused).
+bool simt_fused_fits(int b);
+cudaError_t simt_fused_run(const float* X, const float* L, bool l_trans, const float* W,
+                           long long w_k, long long w_n, const float* R, bool r_trans, float* C,
+                           float* out, int M, int N, int K, int b, const char* tag,
+                           cudaStream_t stream);
 
 // ------------------------------------------------------------ b x b chains
 // One cooperative launch per chain of b x b products (tensor cores, b a

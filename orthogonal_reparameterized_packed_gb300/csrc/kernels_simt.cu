@@ -14,6 +14,7 @@ namespace poetx {
 namespace {
 
 constexpr int TM = 64, TN = 64, TK = 32, SIMT_THREADS = 256;
+constexpr int kFusedXW = 64;  // the fused kernel's widest block
 
 template <typename T>
 __device__ __forceinline__ float load_f(const T* p, long long i);
@@ -148,6 +149,216 @@ __global__ void __launch_bounds__(SIMT_THREADS) simt_gemm_kernel(const SimtGemm 
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) store(ty * 4 + i, tx * 4 + j, acc[i][j]);
+}
+
+// The fp32 W0 product with the block-diagonal factors on both sides in one
+// launch (blocks of b dividing 32, or b = 64, so that blocks tile the 32-wide
+// K steps and the 64-column output tiles):
+//   forward:  u = x P^T (per K step, as the A operand), C = v = u W0^T,
+//             out = y = v R^T
+//   backward: dv = dy R (A operand), C = du = dv W0, out = dx = du P
+// Per K step the activation's rows (x or dy, the columns the step's blocks
+// cover) and the left blocks' rows for the step's 32 columns are staged in
+// shared memory and form the step's A tile there (a sum over the b columns
+// of a block, in order), which then feeds the 64 x 64 tile product as in
+// simt_gemm_kernel, K split over a cluster the same way.  After the split
+// sums each finalising rank holds whole rows of C: it stores them if asked,
+// and applies the right factor to them (the 64-column tile holds whole
+// blocks).
+struct SimtFusedArgs {
+  int M, N, K, b, splits;
+  const float* X;           // [M][K]: x or dy
+  const float* L;           // left blocks [K/b][b][b]
+  int l_trans;              // A[t][k] = sum_j X[t][g b + j] L_g[kl][j] (0) or L_g[j][kl] (1)
+  const float* W;           // W0 as B(k, n) = W[k w_k + n w_n]
+  long long w_k, w_n;
+  const float* R;           // right blocks [N/b][b][b] (null: C only)
+  int r_trans;              // out[t][n] = sum_j C[t][g b + j] R_g[nl][j] (0) or R_g[j][nl] (1)
+  float* C;                 // [M][N] (null: not stored)
+  float* out;               // [M][N]
+};
+
+constexpr int kFusedSmemFloats = TK * (TM + 4) + TK * (TN + 4) + 2 * TM * (TN + 1) +
+                                 TM * (kFusedXW + 1) + TK * (kFusedXW + 1) + TN * (kFusedXW + 1);
+
+// B: the block size (a template parameter, so that every staging loop has a
+// fixed trip count and a thread's global loads of a step are all in flight
+// before it stores any of them).
+template <int B>
+__global__ void __launch_bounds__(SIMT_THREADS) simt_fused_kernel(const SimtFusedArgs p) {
+  pdl_wait();
+  pdl_trigger();
+  extern __shared__ float fsm[];
+  float (*As)[TM + 4] = reinterpret_cast<float (*)[TM + 4]>(fsm);
+  float (*Bs)[TN + 4] = reinterpret_cast<float (*)[TN + 4]>(fsm + TK * (TM + 4));
+  float (*Ps)[TN + 1] = reinterpret_cast<float (*)[TN + 1]>(fsm + TK * (TM + 4) + TK * (TN + 4));
+  float (*Cs)[TN + 1] = Ps + TM;  // the finalised rows of C
+  float (*Xs)[kFusedXW + 1] = reinterpret_cast<float (*)[kFusedXW + 1]>(Cs + TM);
+  float (*Ls)[kFusedXW + 1] = Xs + TM;
+  float (*Rs)[kFusedXW + 1] = Ls + TK;
+  constexpr int XW = B >= TK ? B : TK;           // activation columns a K step reads
+  constexpr int NX = TM * XW / SIMT_THREADS;     // per thread: activation values
+  constexpr int NL = (TK * B + SIMT_THREADS - 1) / SIMT_THREADS;  // left block values
+  constexpr int NW = TN * TK / SIMT_THREADS;     // W0 values
+  constexpr int NR = (TN * B + SIMT_THREADS - 1) / SIMT_THREADS;  // right block values
+  const int m0 = blockIdx.y * TM;
+  const int split = p.splits > 1 ? static_cast<int>(blockIdx.x) % p.splits : 0;
+  const int n0 = (p.splits > 1 ? static_cast<int>(blockIdx.x) / p.splits : blockIdx.x) * TN;
+  const int kslice = ((p.K + p.splits * TK - 1) / (p.splits * TK)) * TK;
+  const int k_begin = split * kslice;
+  const int k_end = min(p.K, k_begin + kslice);
+  const int tx = threadIdx.x % 16;  // n direction
+  const int ty = threadIdx.x / 16;  // m direction
+
+  // the right factor's rows for the tile's columns: loaded first, stored
+  // after the first step's loads are in flight
+  float rr[NR];
+  if (p.R != nullptr) {
+#pragma unroll
+    for (int q = 0; q < NR; ++q) {
+      const int e = threadIdx.x + q * SIMT_THREADS;
+      const int nn = e / B, j = e - nn * B;
+      const int n = n0 + nn;
+      rr[q] = 0.f;
+      if (e < TN * B && n < p.N) {
+        const int blk = n / B, nl = n - blk * B;
+        const float* Rb = p.R + static_cast<long long>(blk) * B * B;
+        rr[q] = p.r_trans ? Rb[j * B + nl] : Rb[nl * B + j];
+      }
+    }
+  }
+  float acc[4][4] = {};
+  bool r_stored = false;
+  for (int k0 = k_begin; k0 < k_end; k0 += TK) {
+    const int xb = B >= TK ? (k0 / B) * B : k0;  // the first activation column
+    float rx[NX], rl[NL], rw[NW];
+#pragma unroll
+    for (int q = 0; q < NX; ++q) {
+      const int e = threadIdx.x + q * SIMT_THREADS;
+      const int mm = e / XW, c = e - mm * XW;
+      const int m = m0 + mm, col = xb + c;
+      rx[q] = (m < p.M && col < p.K) ? p.X[static_cast<long long>(m) * p.K + col] : 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < NL; ++q) {
+      const int e = threadIdx.x + q * SIMT_THREADS;
+      const int kk = e / B, j = e - kk * B;
+      const int k = k0 + kk;
+      rl[q] = 0.f;
+      if (e < TK * B && k < k_end) {
+        const int blk = k / B, kl = k - blk * B;
+        const float* Lb = p.L + static_cast<long long>(blk) * B * B;
+        rl[q] = p.l_trans ? Lb[j * B + kl] : Lb[kl * B + j];
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < NW; ++q) {
+      const int e = threadIdx.x + q * SIMT_THREADS;
+      const int nn = e % TN, kk = e / TN;
+      const int n = n0 + nn, k = k0 + kk;
+      rw[q] = (n < p.N && k < k_end) ? p.W[k * p.w_k + n * p.w_n] : 0.f;
+    }
+    if (p.R != nullptr && !r_stored) {
+#pragma unroll
+      for (int q = 0; q < NR; ++q) {
+        const int e = threadIdx.x + q * SIMT_THREADS;
+        if (e < TN * B) Rs[e / B][e % B] = rr[q];
+      }
+      r_stored = true;
+    }
+#pragma unroll
+    for (int q = 0; q < NX; ++q) {
+      const int e = threadIdx.x + q * SIMT_THREADS;
+      Xs[e / XW][e % XW] = rx[q];
+    }
+#pragma unroll
+    for (int q = 0; q < NL; ++q) {
+      const int e = threadIdx.x + q * SIMT_THREADS;
+      if (e < TK * B) Ls[e / B][e % B] = rl[q];
+    }
+#pragma unroll
+    for (int q = 0; q < NW; ++q) {
+      const int e = threadIdx.x + q * SIMT_THREADS;
+      Bs[e / TN][e % TN] = rw[q];
+    }
+    __syncthreads();
+    // the step's A tile: A[kk][m] = sum_j Xs[m][its block's column j] Ls[kk][j]
+#pragma unroll
+    for (int q = 0; q < TK * TM / SIMT_THREADS; ++q) {
+      const int e = threadIdx.x + q * SIMT_THREADS;
+      const int kk = e / TM, mm = e - kk * TM;
+      const int xo = B >= TK ? 0 : (kk / B) * B;
+      float s = 0.f;
+#pragma unroll
+      for (int j = 0; j < B; ++j) s = fmaf(Xs[mm][xo + j], Ls[kk][j], s);
+      As[kk][mm] = s;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < TK; ++kk) {
+      float a[4], bv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) bv[j] = Bs[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], bv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+  if (p.R != nullptr && !r_stored) {  // an empty K range
+#pragma unroll
+    for (int q = 0; q < NR; ++q) {
+      const int e = threadIdx.x + q * SIMT_THREADS;
+      if (e < TN * B) Rs[e / B][e % B] = rr[q];
+    }
+  }
+  // the split sums: rank s finalises rows [s rows, (s + 1) rows) of C, all
+  // slices' values of an entry loaded at once and added in rank order
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) Ps[ty * 4 + i][tx * 4 + j] = acc[i][j];
+  if (p.splits > 1)
+    cluster_sync();
+  else
+    __syncthreads();
+  const int rows = TM / p.splits, r0 = split * rows;
+  for (int idx = threadIdx.x; idx < rows * TN; idx += SIMT_THREADS) {
+    const int mm = r0 + idx / TN, nn = idx % TN;
+    const uint32_t at = 4u * static_cast<uint32_t>(mm * (TN + 1) + nn);
+    float v[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      v[r] = 0.f;
+      if (r < p.splits)
+        v[r] = r == split ? Ps[mm][nn]
+                          : ld_cluster_f32(map_peer(smem_u32(&Ps[0][0]), static_cast<uint32_t>(r)) +
+                                           at);
+    }
+    float s = v[0];
+#pragma unroll
+    for (int r = 1; r < 8; ++r)
+      if (r < p.splits) s += v[r];
+    Cs[mm][nn] = s;
+    const int m = m0 + mm, n = n0 + nn;
+    if (p.C != nullptr && m < p.M && n < p.N) p.C[static_cast<long long>(m) * p.N + n] = s;
+  }
+  if (p.splits > 1) cluster_sync();  // no CTA leaves or reuses Ps while a peer reads it
+  if (p.R == nullptr) return;
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < rows * TN; idx += SIMT_THREADS) {
+    const int mm = r0 + idx / TN, nn = idx % TN;
+    const int m = m0 + mm, n = n0 + nn;
+    if (m >= p.M || n >= p.N) continue;
+    const int co = (nn / B) * B;  // the block's first column in the tile
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < B; ++j) s = fmaf(Cs[mm][co + j], Rs[nn][j], s);
+    p.out[static_cast<long long>(m) * p.N + n] = s;
+  }
 }
 
 // Position of Q[i][j] (i < j) in the row-by-row packed strict upper triangle.
@@ -1367,6 +1578,91 @@ cudaError_t simt_gemm_run(const SimtGemm& g_in, cudaStream_t stream) {
   cudaError_t e = g.bf16_inputs ? cudaLaunchKernelEx(&cfg, simt_gemm_kernel<__nv_bfloat16>, g)
                                 : cudaLaunchKernelEx(&cfg, simt_gemm_kernel<float>, g);
   prof_end(g.tag, stream);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+bool simt_fused_fits(int b) { return b >= 1 && b <= kFusedXW && (TK % b == 0 || b % TK == 0); }
+
+cudaError_t simt_fused_run(const float* X, const float* L, bool l_trans, const float* W,
+                           long long w_k, long long w_n, const float* R, bool r_trans, float* C,
+                           float* out, int M, int N, int K, int b, const char* tag,
+                           cudaStream_t stream) {
+  if (M <= 0 || N <= 0 || K <= 0) return cudaSuccess;
+  if (!simt_fused_fits(b) || N % b != 0 || K % b != 0 || (R != nullptr && out == nullptr))
+    return cudaErrorInvalidValue;
+  const int smem = kFusedSmemFloats * static_cast<int>(sizeof(float));
+  void (*kernel)(const SimtFusedArgs) = nullptr;
+  switch (b) {
+    case 1: kernel = simt_fused_kernel<1>; break;
+    case 2: kernel = simt_fused_kernel<2>; break;
+    case 4: kernel = simt_fused_kernel<4>; break;
+    case 8: kernel = simt_fused_kernel<8>; break;
+    case 16: kernel = simt_fused_kernel<16>; break;
+    case 32: kernel = simt_fused_kernel<32>; break;
+    default: kernel = simt_fused_kernel<64>; break;
+  }
+  static bool attr_set[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64) {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!attr_set[dev]) {  // every instance, once per device
+      const void* all[] = {
+          reinterpret_cast<const void*>(simt_fused_kernel<1>),
+          reinterpret_cast<const void*>(simt_fused_kernel<2>),
+          reinterpret_cast<const void*>(simt_fused_kernel<4>),
+          reinterpret_cast<const void*>(simt_fused_kernel<8>),
+          reinterpret_cast<const void*>(simt_fused_kernel<16>),
+          reinterpret_cast<const void*>(simt_fused_kernel<32>),
+          reinterpret_cast<const void*>(simt_fused_kernel<64>)};
+      for (const void* f : all) {
+        cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+      }
+      attr_set[dev] = true;
+    }
+  }
+  SimtFusedArgs a;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.b = b;
+  a.X = X;
+  a.L = L;
+  a.l_trans = l_trans ? 1 : 0;
+  a.W = W;
+  a.w_k = w_k;
+  a.w_n = w_n;
+  a.R = R;
+  a.r_trans = r_trans ? 1 : 0;
+  a.C = C;
+  a.out = out;
+  const int tiles_n = (N + TN - 1) / TN, tiles_m = (M + TM - 1) / TM;
+  if (tiles_m > 65535) return cudaErrorInvalidValue;
+  // K split over a cluster of up to 8 CTAs per tile, as in simt_gemm_run
+  const long long tiles = static_cast<long long>(tiles_n) * tiles_m;
+  int splits = 1;
+  while (splits < 8 && tiles * splits * 2 <= 2LL * sm_count() && K >= 2 * splits * 32)
+    splits *= 2;
+  a.splits = splits;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(tiles_n * splits), static_cast<unsigned>(tiles_m), 1);
+  cfg.blockDim = dim3(SIMT_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = static_cast<unsigned>(splits);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = splits > 1 ? 2 : 1;
+  prof_begin(tag, stream);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, a);
+  prof_end(tag, stream);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
