@@ -1133,17 +1133,17 @@ poetx_status poetx_backward(const void* dy, const void* x, const void* W0, const
   }
   if (fused32) {
     // dv = dy R on the fly, du = dv W0 (kept for G_P) and dx = du P in one
-    // launch; then G_R = sum_t dy_t v_t^T and G_P = sum_t du_t x_t^T
+    // launch; then G_P = sum_t du_t x_t^T and G_R = sum_t dy_t v_t^T
     e = simt_fused_run(static_cast<const float*>(dy), static_cast<const float*>(rsb), true,
                        static_cast<const float*>(W0), d_in, 1, static_cast<const float*>(psb), true,
                        static_cast<float*>(p.sb.du), static_cast<float*>(dx),
                        static_cast<int>(tokens), d_in, d_out, b, "gemm_w0_dgrad_fused", s);
     if (e != cudaSuccess) return POETX_ERR_CUDA;
-    e = block_gradient(dy, v, d_out, b, tokens, is_bf16, p.sb.part, p.splits_out,
-                       p.cnp.g32[0] + off_R, p.cnp.g16[0] ? p.cnp.g16[0] + off_R : nullptr, s);
-    if (e != cudaSuccess) return POETX_ERR_CUDA;
-    e = block_gradient(p.sb.du, x, d_in, b, tokens, is_bf16, p.sb.part, p.splits_in,
-                       p.cnp.g32[0], p.cnp.g16[0], s);
+    // G_P (P blocks first) and G_R in one launch
+    e = launch_small_outer2(static_cast<const float*>(p.sb.du), static_cast<const float*>(x),
+                            p.cnp.g32[0], d_in, static_cast<const float*>(dy),
+                            static_cast<const float*>(v), p.cnp.g32[0] + off_R, d_out, b, tokens,
+                            s);
     if (e != cudaSuccess) return POETX_ERR_CUDA;
     return to_status(run_cnp_backward(theta_P, d_in / b, theta_R, d_out / b, b, k, is_bf16,
                                       p.cnp, dtheta_P, dtheta_R, s));

@@ -236,6 +236,11 @@ bool small_chain_fits(int b);
 // (small_chain_fits), [d/b][b][b].
 cudaError_t launch_small_outer(const float* A, const float* B, float* G, int d, int b, long long T,
                                cudaStream_t s);
+// Both sides in one launch: G0 from (A0, B0) over d0 features, G1 from
+// (A1, B1) over d1.
+cudaError_t launch_small_outer2(const float* A0, const float* B0, float* G0, int d0,
+                                const float* A1, const float* B1, float* G1, int d1, int b,
+                                long long T, cudaStream_t s);
 cudaError_t launch_small_build(const float* theta, int n, int b, int k, float* out32,
                                __nv_bfloat16* out16, cudaStream_t s);
 cudaError_t launch_small_adjoint(const float* theta_a, int n_a, const float* theta_b, int n_b,

@@ -569,16 +569,29 @@ __global__ void __launch_bounds__(256) small_adjoint_kernel(
 constexpr int kOuterTC = 64;                                    // tokens per staged chunk
 constexpr int kOuterPer = kSmallMaxB * kSmallMaxB / 256;        // outputs per thread
 
-__global__ void __launch_bounds__(256) small_outer_kernel(const float* __restrict__ A,
-                                                          const float* __restrict__ B,
-                                                          float* __restrict__ G, int d, int b,
+// One launch may cover two sides (the P and R blocks of a layer): blocks
+// g < n_a belong to side 0, the rest to side 1.
+struct OuterSides {
+  const float* A[2];
+  const float* B[2];
+  float* G[2];
+  int d[2];
+  int n_a;
+};
+
+__global__ void __launch_bounds__(256) small_outer_kernel(const OuterSides sides, int b,
                                                           long long T, int splits) {
   pdl_wait();
   pdl_trigger();
   __shared__ float As[kOuterTC][kSmallMaxB];
   __shared__ float Bs[kOuterTC][kSmallMaxB];
   __shared__ float Ps[kSmallMaxB * kSmallMaxB];  // this CTA's partial sums (splits > 1)
-  const int g = blockIdx.y;
+  const int side = static_cast<int>(blockIdx.y) >= sides.n_a ? 1 : 0;
+  const int g = static_cast<int>(blockIdx.y) - (side ? sides.n_a : 0);
+  const float* __restrict__ A = sides.A[side];
+  const float* __restrict__ B = sides.B[side];
+  float* __restrict__ G = sides.G[side];
+  const int d = sides.d[side];
   const int split = blockIdx.x;  // the rank in the block's cluster
   const long long per = (T + splits - 1) / splits;
   const long long t0 = split * per;
@@ -1708,9 +1721,9 @@ cudaError_t launch_reduce_extract(const float* part, int splits, int n, int b, i
 
 bool small_chain_fits(int b) { return b >= 1 && b <= kSmallMaxB; }
 
-cudaError_t launch_small_outer(const float* A, const float* B, float* G, int d, int b, long long T,
+namespace {
+cudaError_t small_outer_launch(const OuterSides& sides, int n, int b, long long T,
                                cudaStream_t s) {
-  const int n = d / b;
   if (n <= 0) return cudaSuccess;
   if (!small_chain_fits(b) || n > 65535) return cudaErrorInvalidValue;
   // a cluster of up to 8 CTAs per block, a chunk of tokens at least each,
@@ -1734,9 +1747,26 @@ cudaError_t launch_small_outer(const float* A, const float* B, float* G, int d, 
   cfg.attrs = attr;
   cfg.numAttrs = splits > 1 ? 2 : 1;
   prof_begin("outer", s);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, small_outer_kernel, A, B, G, d, b, T, splits);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, small_outer_kernel, sides, b, T, splits);
   prof_end("outer", s);
   return e != cudaSuccess ? e : cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_small_outer(const float* A, const float* B, float* G, int d, int b, long long T,
+                               cudaStream_t s) {
+  OuterSides sides = {{A, A}, {B, B}, {G, G}, {d, d}, 0};
+  const int n = b > 0 ? d / b : 0;
+  sides.n_a = n;
+  return small_outer_launch(sides, n, b, T, s);
+}
+
+cudaError_t launch_small_outer2(const float* A0, const float* B0, float* G0, int d0,
+                                const float* A1, const float* B1, float* G1, int d1, int b,
+                                long long T, cudaStream_t s) {
+  if (b <= 0) return cudaErrorInvalidValue;
+  OuterSides sides = {{A0, A1}, {B0, B1}, {G0, G1}, {d0, d1}, d0 / b};
+  return small_outer_launch(sides, d0 / b + d1 / b, b, T, s);
 }
 
 cudaError_t launch_small_build(const float* theta, int n, int b, int k, float* out32,

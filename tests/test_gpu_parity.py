@@ -224,6 +224,7 @@ LAYER_CASES = [
     (512, 256, 256, 16, 40, "bf16"),     # the largest k
     (64, 32, 8, 16, 20, "f32"),
     (256, 256, 64, 3, 300, "f32"),      # fp32 token sums split over 4 CTAs, ragged ranges
+    (96, 192, 32, 3, 200, "f32"),       # one token-sum launch over 3 P blocks and 6 R blocks
     (512, 256, 256, 0, 70, "bf16"),
     # the CTA-pair adjoint for k != 3 (Horner form), every block size
     (512, 256, 32, 5, 100, "bf16"),
