@@ -225,6 +225,12 @@ LAYER_CASES = [
     (64, 32, 8, 16, 20, "f32"),
     (256, 256, 64, 3, 300, "f32"),      # fp32 token sums split over 4 CTAs, ragged ranges
     (96, 192, 32, 3, 200, "f32"),       # one token-sum launch over 3 P blocks and 6 R blocks
+    # the fused fp32 W0 GEMM's other block sizes: ragged K step (48 = 1.5 steps),
+    # ragged N tile, ragged token tile; a K slice boundary inside a 64-block
+    (48, 80, 16, 3, 70, "f32"),
+    (32, 64, 4, 2, 45, "f32"),
+    (16, 8, 2, 1, 33, "f32"),
+    (192, 64, 64, 2, 100, "f32"),
     (512, 256, 256, 0, 70, "bf16"),
     # the CTA-pair adjoint for k != 3 (Horner form), every block size
     (512, 256, 32, 5, 100, "bf16"),
@@ -245,6 +251,7 @@ def test_layer_matches_oracle(px, d_in, d_out, b, k, T, dtype):
 
 RECOMPUTE_CASES = [
     (256, 256, 32, 3, 512, "f32"),
+    (48, 80, 16, 3, 70, "f32"),
     (512, 768, 256, 3, 333, "bf16"),
     (256, 512, 128, 2, 130, "bf16"),
     (512, 256, 64, 3, 257, "bf16"),
