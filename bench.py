@@ -894,7 +894,8 @@ def sweep_bytes(b, d=SWEEP_D, T=SWEEP_T):
 def run_sweep(args):
     """Each (b, k) of the sweep: block build, forward z = B x and backward
     (dx, packed dtheta) timed call by call with CUDA events; L2 is flushed
-    (a 256 MiB write) before every timed call, since x (64 MiB) fits in L2."""
+    (a 256 MiB write, then a 256 MiB read) before every timed call, since x
+    (64 MiB) fits in L2."""
     import torch
 
     import orthogonal_reparameterized_packed_gb300 as poetx
@@ -911,6 +912,10 @@ def run_sweep(args):
     z = torch.empty_like(x)
     dx = torch.empty_like(x)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    # read after the write: its lines displace the flush's dirty ones, so the
+    # timed call starts with an L2 that holds none of its data and owes no
+    # write-backs of someone else's
+    flush_read = torch.ones(64 << 20, dtype=torch.int32, device="cuda")
     peaks, peak_src = load_peaks()
     hbm = peaks["hbm_gbs"]
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
@@ -919,6 +924,7 @@ def run_sweep(args):
         tot = 0.0
         for _ in range(reps):
             flush.zero_()
+            flush_read.sum()
             ev[0].record(stream)
             fn()
             ev[1].record(stream)
@@ -933,6 +939,9 @@ def run_sweep(args):
             raise SystemExit(f"--sweep-case {args.sweep_case}: not a case of the sweep")
         sweep_cases = [b_k]
     cases = []
+    flush.zero_()  # the flush's own kernels warmed up before the first timed call
+    flush_read.sum()
+    torch.cuda.synchronize()
     launches0 = poetx.poetx_launch_count()
     clocks = ClockSampler(local)
     clocks.start()
@@ -982,7 +991,8 @@ def run_sweep(args):
                 "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": {"workload": SWEEP, "d": d, "tokens_per_gpu": T, "dtype": "bf16",
                            "cases": [f"b{b}_k{k}" for b, k in sweep_cases],
-                           "l2": "flushed (256 MiB write) before every timed call"},
+                           "l2": "flushed before every timed call: a 256 MiB write, then a "
+                                 "256 MiB read that leaves no dirty line in L2"},
                 "gpu_launches": launches, "launch": "eager",
                 "roofline": {"bound": "hbm", "kernel": "block transform fwd + bwd, all cases",
                              "achieved": achieved, "peak": hbm, "unit": "GB/s",
