@@ -86,3 +86,24 @@ def test_reference_arm_prints_on_rank_zero_only():
     assert r.returncode == 0, r.stdout + r.stderr
     lines = _reference_lines(r.stdout)
     assert len(lines) == 1 and lines[0]["impl"] == "reference"
+
+
+def test_l2_rule_per_workload():
+    # a single projection whose x, dy and W0 are under twice the L2 is timed
+    # step by step after a flush; the larger ones run back to back, and the
+    # config says which, with the input size
+    sys.path.insert(0, ROOT)
+    import bench
+    from orthogonal_reparameterized_packed_gb300.inputs import WORKLOADS
+    w = WORKLOADS["llama3_8b_qo"]
+    assert bench.input_bytes(w) == 2 * (16384 * 8192 + 4096 * 4096)
+    assert bench.input_bytes(WORKLOADS["fp32_256_b32"]) == 4 * (512 * 512 + 256 * 256)
+    assert not bench.flush_between_steps("llama3_8b_qo")
+    assert bench.flush_between_steps("fp32_256_b32")
+    assert bench.flush_between_steps("bf16_2048x5632")
+    assert not bench.flush_between_steps("llama3_8b_block")  # composites: not single projections
+    for name in WORKLOADS:
+        l2 = bench.config_json(name, 1)["l2"]
+        assert l2.startswith("flushed" if bench.flush_between_steps(name) else "inputs larger"), l2
+        big = bench.input_bytes(WORKLOADS[name]) >= 2 * bench.L2_BYTES
+        assert big != bench.flush_between_steps(name)
